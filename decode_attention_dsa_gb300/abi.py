@@ -1,0 +1,180 @@
+"""ctypes binding of ``libdsa_decode.so``: the C ABI of ``include/dsa_decode.h``
+under the same names. Argument marshalling only: every step runs in the CUDA
+kernels of the library. Pointers may be given as torch tensors (their
+``data_ptr()``), plain integers, or None (NULL). Streams may be a
+``torch.cuda.Stream``, an integer handle, or None (the current torch stream).
+
+A non-zero status raises ``DsaError``. Loading fails loudly if the library is
+missing: there is no fallback path.
+"""
+from __future__ import annotations
+
+import ctypes
+import os
+
+PKG = os.path.dirname(os.path.abspath(__file__))
+LIB_PATH = os.path.join(PKG, "libdsa_decode.so")
+
+DSA_OK = 0
+DSA_ERR_ARG, DSA_ERR_SHAPE, DSA_ERR_WS, DSA_ERR_CUDA, DSA_ERR_DEVICE_CHECK = -1, -2, -3, -4, -6
+DEVERR_BOUNDS, DEVERR_CAPACITY, DEVERR_QRANGE = 0x1, 0x2, 0x4
+ROW_BYTES, LAT_DIM, ROPE_DIM, IDX_HEADS, IDX_DIM, RING_ROWS = 656, 512, 64, 8, 64, 64
+MAX_K, MAX_ROWS = 4096, 8
+CLS_HOT, CLS_RING, CLS_RAM, CLS_PAD = 0, 1, 2, 3
+WARM_EMPTY, WARM_LAST_S = 0, 1
+ST_LEN, ST_RAM, ST_HAND, ST_EPOCH, ST_WRITEBACKS, ST_WORDS = 0, 1, 2, 3, 4, 8
+
+
+class DsaError(RuntimeError):
+    def __init__(self, fn: str, status: int):
+        super().__init__(f"{fn} failed: {status} ({status_string(status)})")
+        self.status = status
+
+
+class DsaUnit(ctypes.Structure):
+    """Mirror of ``struct dsa_unit``."""
+    _fields_ = [
+        ("keys", ctypes.c_void_p), ("slots", ctypes.c_void_p), ("slot_pos", ctypes.c_void_p),
+        ("pos_slot", ctypes.c_void_p), ("fill_round", ctypes.c_void_p),
+        ("pin_epoch", ctypes.c_void_p), ("ring", ctypes.c_void_p), ("mirror", ctypes.c_void_p),
+        ("state", ctypes.c_void_p), ("slots_n", ctypes.c_int32), ("reserved0", ctypes.c_int32),
+        ("lmax", ctypes.c_int64),
+    ]
+
+
+assert ctypes.sizeof(DsaUnit) == 88
+
+_VP, _I32, _I64, _SZ, _F = ctypes.c_void_p, ctypes.c_int32, ctypes.c_int64, ctypes.c_size_t, ctypes.c_float
+
+# name -> (restype, argtypes), in the order of the header
+SIGNATURES = {
+    "dsa_abi_version": (ctypes.c_int, []),
+    "dsa_status_string": (ctypes.c_char_p, [ctypes.c_int]),
+    "dsa_check": (ctypes.c_int, [_I32]),
+    "dsa_host_alloc": (ctypes.c_int, [ctypes.POINTER(_VP), ctypes.POINTER(_VP), _SZ]),
+    "dsa_host_free": (ctypes.c_int, [_VP]),
+    "hc_init": (ctypes.c_int, [_VP, _I32, _I32, _VP, _I32, _I64, _VP, _VP]),
+    "dsa_score_topk_workspace": (_SZ, [_I32, _I32, _I64]),
+    "dsa_score_topk": (ctypes.c_int, [_VP, _I32, _I32, _I32, _VP, _VP, _VP, _I64, _VP, _SZ, _VP, _VP]),
+    "hot_gather_workspace": (_SZ, [_I32, _I32, _I32]),
+    "hot_gather": (ctypes.c_int, [_VP, _I32, _I32, _I32, _I32, _VP, _VP, _VP, _VP, _VP, _SZ, _VP, _VP]),
+    "mla_decode_attn_workspace": (_SZ, [_I32, _I32, _I32, _I32]),
+    "mla_decode_attn": (ctypes.c_int, [_I32, _I32, _I32, _I32, _VP, _VP, _VP, _VP, _F, _VP, _VP, _VP,
+                                       _SZ, _VP, _VP]),
+    "kv_append_writeback": (ctypes.c_int, [_VP, _I32, _I32, _VP, _VP, _VP, _VP]),
+    "kv_flush": (ctypes.c_int, [_VP, _I32, _VP, _VP]),
+}
+
+_lib = None
+
+
+def load(path: str = LIB_PATH) -> ctypes.CDLL:
+    """Load the library (once). Raises if it is missing or incomplete."""
+    global _lib
+    if _lib is not None:
+        return _lib
+    if not os.path.exists(path):
+        raise RuntimeError(f"{path} is missing: build it with __graft_entry__.build() "
+                           "or python -m decode_attention_dsa_gb300.build")
+    lib = ctypes.CDLL(path)
+    for name, (res, args) in SIGNATURES.items():
+        fn = getattr(lib, name)          # AttributeError if a symbol is missing
+        fn.restype = res
+        fn.argtypes = args
+    _lib = lib
+    return lib
+
+
+def _p(x):
+    if x is None:
+        return None
+    if hasattr(x, "data_ptr"):
+        return x.data_ptr()
+    return int(x)
+
+
+def _s(stream):
+    if stream is None:
+        import torch
+        return torch.cuda.current_stream().cuda_stream
+    if hasattr(stream, "cuda_stream"):
+        return stream.cuda_stream
+    return int(stream)
+
+
+def _ok(fn, st):
+    if st != DSA_OK:
+        raise DsaError(fn, st)
+    return st
+
+
+def dsa_abi_version() -> int:
+    return load().dsa_abi_version()
+
+
+def status_string(status: int) -> str:
+    return load().dsa_status_string(status).decode()
+
+
+dsa_status_string = status_string
+
+
+def dsa_check(dev_err_value: int) -> int:
+    return load().dsa_check(int(dev_err_value))
+
+
+def dsa_host_alloc(nbytes: int) -> tuple[int, int]:
+    """Pinned, mapped host memory: returns (host address, device alias)."""
+    h, d = _VP(), _VP()
+    _ok("dsa_host_alloc", load().dsa_host_alloc(ctypes.byref(h), ctypes.byref(d), nbytes))
+    return h.value, d.value
+
+
+def dsa_host_free(host_ptr: int) -> None:
+    _ok("dsa_host_free", load().dsa_host_free(host_ptr))
+
+
+def hc_init(units, U, warm, l0, max_slots, max_lmax, dev_err, stream=None):
+    return _ok("hc_init", load().hc_init(_p(units), U, warm, _p(l0), max_slots, max_lmax,
+                                         _p(dev_err), _s(stream)))
+
+
+def dsa_score_topk_workspace(U, R, max_len) -> int:
+    return load().dsa_score_topk_workspace(U, R, max_len)
+
+
+def dsa_score_topk(units, U, R, K, q, w, topk_idx, max_len, ws, ws_bytes, dev_err, stream=None):
+    return _ok("dsa_score_topk", load().dsa_score_topk(
+        _p(units), U, R, K, _p(q), _p(w), _p(topk_idx), max_len, _p(ws), ws_bytes, _p(dev_err),
+        _s(stream)))
+
+
+def hot_gather_workspace(U, R, K) -> int:
+    return load().hot_gather_workspace(U, R, K)
+
+
+def hot_gather(units, U, R, K, round_, topk_idx, cls, rows, counters, ws, ws_bytes, dev_err,
+               stream=None):
+    return _ok("hot_gather", load().hot_gather(
+        _p(units), U, R, K, round_, _p(topk_idx), _p(cls), _p(rows), _p(counters), _p(ws), ws_bytes,
+        _p(dev_err), _s(stream)))
+
+
+def mla_decode_attn_workspace(U, R, H, K) -> int:
+    return load().mla_decode_attn_workspace(U, R, H, K)
+
+
+def mla_decode_attn(U, R, H, K, q_lat, q_rope, rows, topk_idx, scale, out, lse, ws, ws_bytes,
+                    dev_err, stream=None):
+    return _ok("mla_decode_attn", load().mla_decode_attn(
+        U, R, H, K, _p(q_lat), _p(q_rope), _p(rows), _p(topk_idx), float(scale), _p(out), _p(lse),
+        _p(ws), ws_bytes, _p(dev_err), _s(stream)))
+
+
+def kv_append_writeback(units, U, A, new_rows, new_keys, dev_err, stream=None):
+    return _ok("kv_append_writeback", load().kv_append_writeback(
+        _p(units), U, A, _p(new_rows), _p(new_keys), _p(dev_err), _s(stream)))
+
+
+def kv_flush(units, U, dev_err, stream=None):
+    return _ok("kv_flush", load().kv_flush(_p(units), U, _p(dev_err), _s(stream)))

@@ -1,0 +1,213 @@
+// Housekeeping entry points, cache initialisation (hc_init) and A6: append
+// with batched write-back (kv_append_writeback, kv_flush).
+//
+// [P3] "From 1M total to 15+ x 1M: GLM-5.3 KV-cache offload":
+//  * section "第二次决策" (second decision): per-row, per-layer host-mirror
+//    updates meant 156 stream operations per token (468 when split further);
+//    batching write-back per 64 rows cut the operation count.
+//  * section "第三次决策" (third decision) diagram: new KV -> GPU recent ring ->
+//    batched write-back -> RAM history.
+//  * section "第四次决策" (fourth decision): small logs are copied and packed
+//    by compute kernels to cut DMA queue operations.
+//  * section "容量优化必须通过会话生命周期" (session lifecycle): before export
+//    or restore, flush the log and check RAM rows == logical rows.
+// Here the write-back is a plain kernel store of 64 ring rows (41,984 B) into
+// the mapped mirror: no DMA operation, no host involvement.
+#include <algorithm>
+#include <cstring>
+
+#include "common.cuh"
+
+namespace {
+
+constexpr int APP_THREADS = 256;
+constexpr int INIT_THREADS = 256;
+
+// Store ring rows of positions [from, to) to the mirror (block-wide).
+__device__ void write_back(const dsa_unit& un, int64_t from, int64_t to) {
+  const int64_t n16 = (to - from) * (DSA_ROW_BYTES / 16);
+  for (int64_t i = threadIdx.x; i < n16; i += blockDim.x) {
+    const int64_t r = i / (DSA_ROW_BYTES / 16);
+    const int c = (int)(i % (DSA_ROW_BYTES / 16));
+    const int64_t p = from + r;
+    const uint4* src = reinterpret_cast<const uint4*>(un.ring + (p & (DSA_RING_ROWS - 1)) * DSA_ROW_BYTES);
+    uint4* dst = reinterpret_cast<uint4*>(un.mirror + p * DSA_ROW_BYTES);
+    dst[c] = src[c];
+  }
+}
+
+__global__ void __launch_bounds__(APP_THREADS)
+k_append(const dsa_unit* __restrict__ units, int A, const uint8_t* __restrict__ new_rows,
+         const uint16_t* __restrict__ new_keys, int32_t* dev_err) {
+  const int u = blockIdx.x;
+  const dsa_unit& un = units[u];
+  __shared__ int64_t s_len, s_ram;
+  if (threadIdx.x == 0) {
+    s_len = un.state[DSA_ST_LEN];
+    s_ram = un.state[DSA_ST_RAM];
+  }
+  __syncthreads();
+  int64_t len = s_len, ram = s_ram;
+  int64_t wb = 0;
+  for (int a = 0; a < A; ++a) {
+    const int64_t p = len;
+    if (p >= un.lmax || p - ram >= DSA_RING_ROWS) {
+      if (threadIdx.x == 0) dsa_flag(dev_err, DSA_DEVERR_CAPACITY);
+      break;
+    }
+    const uint4* src = reinterpret_cast<const uint4*>(new_rows + ((size_t)u * A + a) * DSA_ROW_BYTES);
+    uint4* dst = reinterpret_cast<uint4*>(un.ring + (p & (DSA_RING_ROWS - 1)) * DSA_ROW_BYTES);
+    for (int c = threadIdx.x; c < DSA_ROW_BYTES / 16; c += APP_THREADS) dst[c] = src[c];
+    const uint4* ks = reinterpret_cast<const uint4*>(new_keys + ((size_t)u * A + a) * DSA_IDX_DIM);
+    uint4* kd = reinterpret_cast<uint4*>(un.keys + p * DSA_IDX_DIM);
+    if (threadIdx.x < 8) kd[threadIdx.x] = ks[threadIdx.x];
+    len = p + 1;
+    if (len - ram == DSA_RING_ROWS) {
+      __syncthreads();              // the ring row just written is part of the batch
+      write_back(un, ram, len);
+      __syncthreads();              // the batch is read before its ring rows are reused
+      ram = len;
+      ++wb;
+    }
+  }
+  if (threadIdx.x == 0) {
+    un.state[DSA_ST_LEN] = len;
+    un.state[DSA_ST_RAM] = ram;
+    un.state[DSA_ST_WRITEBACKS] += wb;
+  }
+}
+
+__global__ void __launch_bounds__(APP_THREADS) k_flush(const dsa_unit* __restrict__ units) {
+  const int u = blockIdx.x;
+  const dsa_unit& un = units[u];
+  const int64_t len = un.state[DSA_ST_LEN];
+  const int64_t ram = un.state[DSA_ST_RAM];
+  if (len <= ram) return;
+  write_back(un, ram, len);
+  __syncthreads();
+  if (threadIdx.x == 0) {
+    un.state[DSA_ST_RAM] = len;
+    un.state[DSA_ST_WRITEBACKS] += 1;
+  }
+}
+
+// pos_slot for every position, and the slot arrays, in one pass over
+// max(lmax, S) indices per unit.
+__global__ void __launch_bounds__(INIT_THREADS)
+k_init_map(const dsa_unit* __restrict__ units, int warm, const int64_t* __restrict__ l0v,
+           int32_t* dev_err) {
+  const int u = blockIdx.y;
+  const dsa_unit& un = units[u];
+  const int64_t i = (int64_t)blockIdx.x * INIT_THREADS + threadIdx.x;
+  const int64_t l0 = l0v[u];
+  const int S = un.slots_n;
+  if (l0 < 0 || l0 > un.lmax || S < 1) {
+    if (i == 0) dsa_flag(dev_err, DSA_DEVERR_BOUNDS);
+    return;
+  }
+  const int64_t n = warm == DSA_WARM_LAST_S ? min((int64_t)S, l0) : 0;
+  const int64_t first = l0 - n;
+  if (i < un.lmax) un.pos_slot[i] = (i >= first && i < l0) ? (int32_t)(i - first) : -1;
+  if (i < S) {
+    un.slot_pos[i] = i < n ? (int32_t)(first + i) : -1;
+    un.fill_round[i] = -1;
+    un.pin_epoch[i] = -1;
+  }
+  if (i < DSA_ST_WORDS) {
+    int64_t v = 0;
+    if (i == DSA_ST_LEN || i == DSA_ST_RAM) v = l0;
+    un.state[i] = v;
+  }
+}
+
+// Warm slot bytes: slot i <- mirror[l0 - n + i] (one warp per row).
+__global__ void __launch_bounds__(INIT_THREADS)
+k_init_slots(const dsa_unit* __restrict__ units, int warm, const int64_t* __restrict__ l0v) {
+  const int u = blockIdx.y;
+  const dsa_unit& un = units[u];
+  const int64_t i = (int64_t)blockIdx.x * (INIT_THREADS / 32) + (threadIdx.x >> 5);
+  const int64_t l0 = l0v[u];
+  const int S = un.slots_n;
+  if (warm != DSA_WARM_LAST_S || l0 < 0 || l0 > un.lmax || S < 1) return;
+  const int64_t n = min((int64_t)S, l0);
+  if (i >= n) return;
+  warp_copy_row(un.slots + i * DSA_ROW_BYTES, un.mirror + (l0 - n + i) * DSA_ROW_BYTES,
+                threadIdx.x & 31);
+}
+
+}  // namespace
+
+extern "C" int dsa_abi_version(void) { return 1; }
+
+extern "C" const char* dsa_status_string(int status) {
+  switch (status) {
+    case DSA_OK: return "ok";
+    case DSA_ERR_ARG: return "invalid argument";
+    case DSA_ERR_SHAPE: return "unsupported shape";
+    case DSA_ERR_WS: return "workspace missing or too small";
+    case DSA_ERR_CUDA: return "CUDA runtime or launch error";
+    case DSA_ERR_DEVICE_CHECK: return "device-side check failed (see the dev_err bits)";
+    default: return "unknown status";
+  }
+}
+
+extern "C" int dsa_check(int32_t dev_err_value) {
+  return dev_err_value == 0 ? DSA_OK : DSA_ERR_DEVICE_CHECK;
+}
+
+extern "C" int dsa_host_alloc(void** host_ptr, void** dev_ptr, size_t bytes) {
+  if (!host_ptr || !dev_ptr || bytes == 0) return DSA_ERR_ARG;
+  *host_ptr = nullptr;
+  *dev_ptr = nullptr;
+  void* h = nullptr;
+  if (cudaHostAlloc(&h, bytes, cudaHostAllocMapped | cudaHostAllocPortable) != cudaSuccess)
+    return DSA_ERR_CUDA;
+  void* d = nullptr;
+  if (cudaHostGetDevicePointer(&d, h, 0) != cudaSuccess) {
+    cudaFreeHost(h);
+    return DSA_ERR_CUDA;
+  }
+  *host_ptr = h;
+  *dev_ptr = d;
+  return DSA_OK;
+}
+
+extern "C" int dsa_host_free(void* host_ptr) {
+  if (!host_ptr) return DSA_ERR_ARG;
+  return cudaFreeHost(host_ptr) == cudaSuccess ? DSA_OK : DSA_ERR_CUDA;
+}
+
+extern "C" int hc_init(const dsa_unit* units, int32_t U, int32_t warm, const int64_t* l0,
+                       int32_t max_slots, int64_t max_lmax, int32_t* dev_err, void* stream) {
+  if (!units || !l0 || U < 1 || U > 65535 || max_slots < 1 || max_lmax < 0) return DSA_ERR_ARG;
+  if (warm != DSA_WARM_EMPTY && warm != DSA_WARM_LAST_S) return DSA_ERR_ARG;
+  cudaStream_t st = static_cast<cudaStream_t>(stream);
+  const int64_t n = std::max<int64_t>(std::max<int64_t>(max_lmax, max_slots), DSA_ST_WORDS);
+  const int64_t gx = (n + INIT_THREADS - 1) / INIT_THREADS;
+  if (gx > 0x7fffffff) return DSA_ERR_ARG;
+  k_init_map<<<dim3((unsigned)gx, U), INIT_THREADS, 0, st>>>(units, warm, l0, dev_err);
+  if (dsa_launch_status() != DSA_OK) return DSA_ERR_CUDA;
+  if (warm == DSA_WARM_LAST_S) {
+    const int64_t gs = ((int64_t)max_slots + INIT_THREADS / 32 - 1) / (INIT_THREADS / 32);
+    k_init_slots<<<dim3((unsigned)gs, U), INIT_THREADS, 0, st>>>(units, warm, l0);
+    if (dsa_launch_status() != DSA_OK) return DSA_ERR_CUDA;
+  }
+  return DSA_OK;
+}
+
+extern "C" int kv_append_writeback(const dsa_unit* units, int32_t U, int32_t A,
+                                   const uint8_t* new_rows, const uint16_t* new_keys,
+                                   int32_t* dev_err, void* stream) {
+  if (!units || !new_rows || !new_keys || U < 1 || U > 65535 || A < 1 || A > DSA_RING_ROWS)
+    return DSA_ERR_ARG;
+  k_append<<<U, APP_THREADS, 0, static_cast<cudaStream_t>(stream)>>>(units, A, new_rows, new_keys,
+                                                                     dev_err);
+  return dsa_launch_status();
+}
+
+extern "C" int kv_flush(const dsa_unit* units, int32_t U, int32_t* dev_err, void* stream) {
+  (void)dev_err;
+  if (!units || U < 1 || U > 65535) return DSA_ERR_ARG;
+  k_flush<<<U, APP_THREADS, 0, static_cast<cudaStream_t>(stream)>>>(units);
+  return dsa_launch_status();
+}

@@ -1,0 +1,325 @@
+// A3: GPU-managed hot-cache gather.
+//
+// [P3] "From 1M total to 15+ x 1M: GLM-5.3 KV-cache offload", section
+// "第三次决策：让 GPU 直接管理热缓存" (third decision: the GPU manages the hot
+// cache): the selection stays on the GPU, the GPU looks up the hot slots, hits
+// read VRAM and misses read the registered RAM mirror, forming the compact set
+// attention uses. Section "GPU 管缓存也会犯错：跨 block 可见性与置换长扫描"
+// (cross-block visibility and long replacement sweeps): slots filled in a
+// round are hit sources only from the next round and duplicate misses read
+// RAM (an early version let one block read a slot another block was still
+// filling); slots in use are pinned; rows not yet written back are served by
+// the recent ring; replacement is a ring that skips pinned slots (the
+// reference-bit clock's long sweeps cost ~1 ms per gather).
+//
+// Three launches per call, each over all units:
+//  1. k_classify  one thread per selected entry: classify with the state as
+//                 it is at call start and pin HOT slots (pin_epoch = call id).
+//                 Nothing is filled yet, so no entry can see a slot filled in
+//                 this call: the visibility rule holds by construction.
+//  2. k_assign    one 1024-thread CTA per unit: counts, the ascending list of
+//                 distinct unmapped misses (first occurrence across rows found
+//                 by binary search in the lower rows, rank by per-row prefix
+//                 counts), the eligible slots in cyclic order from the hand
+//                 (block scans over 1024-slot windows), and the map update.
+//                 The parallel assignment reproduces the sequential rule
+//                 "i-th miss takes the i-th eligible slot" exactly.
+//  3. k_copy      one warp per 656-byte row: fills read the mirror row once
+//                 (zero-copy over the host link) and write both the victim
+//                 slot and the owner entry's compact row; every other entry
+//                 copies from its source (slot / ring / mirror).
+#include "common.cuh"
+
+namespace {
+
+constexpr int CLS_THREADS = 256;
+constexpr int ASSIGN_THREADS = 1024;
+constexpr int COPY_THREADS = 256;
+constexpr int COPY_WARPS = COPY_THREADS / 32;
+
+struct GatherWs {
+  int32_t* fill_pos;    // [U][RK] position of the i-th inserted miss (ascending)
+  int32_t* fill_slot;   // [U][RK] its slot
+  int32_t* fill_entry;  // [U][RK] entry (r*K + j) whose compact row it also writes
+  int32_t* opc;         // [U][RK] per-row exclusive prefix count of owner entries
+  int32_t* nfill;       // [U]
+  uint8_t* served;      // [U][RK] 1 if the entry's row is written by a fill
+};
+
+inline GatherWs gather_ws(void* ws, int32_t U, int32_t R, int32_t K) {
+  const size_t rk = (size_t)R * K;
+  const size_t a = dsa_align((size_t)U * rk * 4, 256);
+  char* b = static_cast<char*>(ws);
+  GatherWs g;
+  g.fill_pos = reinterpret_cast<int32_t*>(b);
+  g.fill_slot = reinterpret_cast<int32_t*>(b + a);
+  g.fill_entry = reinterpret_cast<int32_t*>(b + 2 * a);
+  g.opc = reinterpret_cast<int32_t*>(b + 3 * a);
+  g.nfill = reinterpret_cast<int32_t*>(b + 4 * a);
+  g.served = reinterpret_cast<uint8_t*>(b + 4 * a + dsa_align((size_t)U * 4, 256));
+  return g;
+}
+
+__global__ void __launch_bounds__(CLS_THREADS)
+k_classify(const dsa_unit* __restrict__ units, int R, int K, int round,
+           const int32_t* __restrict__ topk, uint8_t* __restrict__ cls, int32_t* dev_err) {
+  const int u = blockIdx.y;
+  const int e = blockIdx.x * CLS_THREADS + threadIdx.x;
+  if (e >= R * K) return;
+  const dsa_unit& un = units[u];
+  const int64_t len = un.state[DSA_ST_LEN];
+  const int64_t ram = un.state[DSA_ST_RAM];
+  const int32_t epoch = (int32_t)(un.state[DSA_ST_EPOCH] + 1);
+  const int32_t p = topk[(size_t)u * R * K + e];
+  uint8_t c = DSA_CLS_PAD;
+  if (p >= 0) {
+    if (p >= len) {
+      dsa_flag(dev_err, DSA_DEVERR_BOUNDS);
+    } else if (p >= ram) {
+      c = DSA_CLS_RING;
+    } else {
+      const int32_t s = un.pos_slot[p];
+      if (s >= 0 && s < un.slots_n && un.fill_round[s] < round) {
+        c = DSA_CLS_HOT;
+        un.pin_epoch[s] = epoch;
+      } else {
+        c = DSA_CLS_RAM;
+      }
+    }
+  }
+  cls[(size_t)u * R * K + e] = c;
+}
+
+// lower_bound of p in an ascending row whose tail is -1 padding (-1 = +inf).
+__device__ __forceinline__ int row_lower_bound(const int32_t* row, int K, int32_t p) {
+  int lo = 0, hi = K;
+  while (lo < hi) {
+    const int mid = (lo + hi) >> 1;
+    const int32_t v = row[mid];
+    if (v >= 0 && v < p) lo = mid + 1;
+    else hi = mid;
+  }
+  return lo;
+}
+
+__global__ void __launch_bounds__(ASSIGN_THREADS)
+k_assign(const dsa_unit* __restrict__ units, int R, int K, int round,
+         const int32_t* __restrict__ topk_all, const uint8_t* __restrict__ cls_all,
+         int32_t* __restrict__ counters, GatherWs g, int32_t* dev_err) {
+  __shared__ int s_tmp[32];
+  __shared__ int s_cnt[4];
+  const int u = blockIdx.x;
+  const dsa_unit& un = units[u];
+  const int RK = R * K;
+  const int32_t* topk = topk_all + (size_t)u * RK;
+  const uint8_t* cls = cls_all + (size_t)u * RK;
+  int32_t* fill_pos = g.fill_pos + (size_t)u * RK;
+  int32_t* fill_slot = g.fill_slot + (size_t)u * RK;
+  int32_t* fill_entry = g.fill_entry + (size_t)u * RK;
+  int32_t* opc = g.opc + (size_t)u * RK;
+  uint8_t* served = g.served + (size_t)u * RK;
+  const int S = un.slots_n;
+  const int32_t epoch = (int32_t)(un.state[DSA_ST_EPOCH] + 1);
+
+  if (threadIdx.x < 4) s_cnt[threadIdx.x] = 0;
+  __syncthreads();
+
+  // 1. counts, owner flags (first occurrence of an unmapped RAM position) and
+  //    the per-row exclusive prefix count of owners.
+  int hot = 0, ring = 0, rm = 0;
+  for (int r = 0; r < R; ++r) {
+    const int32_t* row = topk + (size_t)r * K;
+    const int per = (K + ASSIGN_THREADS - 1) / ASSIGN_THREADS;   // contiguous run per thread
+    const int j0 = threadIdx.x * per;
+    const int j1 = min(j0 + per, K);
+    int own = 0;
+    for (int j = j0; j < j1; ++j) {
+      const uint8_t c = cls[(size_t)r * K + j];
+      hot += c == DSA_CLS_HOT;
+      ring += c == DSA_CLS_RING;
+      rm += c == DSA_CLS_RAM;
+      bool owner = false;
+      if (c == DSA_CLS_RAM) {
+        const int32_t p = row[j];
+        if (un.pos_slot[p] < 0) {
+          owner = true;
+          for (int r2 = 0; r2 < r && owner; ++r2) {
+            const int32_t* o = topk + (size_t)r2 * K;
+            const int lb = row_lower_bound(o, K, p);
+            if (lb < K && o[lb] == p) owner = false;
+          }
+        }
+      }
+      served[(size_t)r * K + j] = owner ? 1 : 0;   // provisional: 1 = owner
+      own += owner;
+    }
+    int tot;
+    const int inc = block_inclusive_scan<ASSIGN_THREADS>(own, s_tmp, &tot);
+    int run = inc - own;
+    for (int j = j0; j < j1; ++j) {
+      opc[(size_t)r * K + j] = run;
+      run += served[(size_t)r * K + j];
+    }
+    __syncthreads();
+  }
+  {
+    int t;
+    block_inclusive_scan<ASSIGN_THREADS>(hot, s_tmp, &t);
+    if (threadIdx.x == 0) s_cnt[0] = t;
+    block_inclusive_scan<ASSIGN_THREADS>(ring, s_tmp, &t);
+    if (threadIdx.x == 0) s_cnt[1] = t;
+    block_inclusive_scan<ASSIGN_THREADS>(rm, s_tmp, &t);
+    if (threadIdx.x == 0) s_cnt[2] = t;
+  }
+  __syncthreads();
+
+  // 2. rank of each owner among all owners (ascending position)
+  int nM_local = 0;
+  for (int e = threadIdx.x; e < RK; e += ASSIGN_THREADS) {
+    if (!served[e]) continue;
+    const int r = e / K, j = e % K;
+    const int32_t p = topk[e];
+    int rank = opc[e];
+    for (int r2 = 0; r2 < R; ++r2) {
+      if (r2 == r) continue;
+      const int32_t* o = topk + (size_t)r2 * K;
+      const int lb = row_lower_bound(o, K, p);
+      rank += lb < K ? opc[(size_t)r2 * K + lb] : (opc[(size_t)r2 * K + K - 1] + served[(size_t)r2 * K + K - 1]);
+    }
+    (void)j;
+    if (rank < RK) {
+      fill_pos[rank] = p;
+      fill_entry[rank] = e;
+    } else {
+      dsa_flag(dev_err, DSA_DEVERR_BOUNDS);
+    }
+    ++nM_local;
+  }
+  int nM;
+  block_inclusive_scan<ASSIGN_THREADS>(nM_local, s_tmp, &nM);
+
+  // 3. eligible slots in cyclic order from the hand
+  const int hand0 = (int)un.state[DSA_ST_HAND];
+  int found = 0;
+  for (int base = 0; base < S && found < nM; base += ASSIGN_THREADS) {
+    const int t = base + threadIdx.x;
+    int s = -1;
+    int elig = 0;
+    if (t < S) {
+      s = hand0 + t;
+      if (s >= S) s -= S;
+      elig = (un.pin_epoch[s] != epoch) && (un.fill_round[s] < round);
+    }
+    int tot;
+    const int inc = block_inclusive_scan<ASSIGN_THREADS>(elig, s_tmp, &tot);
+    const int rank = found + inc - elig;
+    if (elig && rank < nM) fill_slot[rank] = s;
+    found += tot;
+  }
+  const int n = min(found, nM);
+  __syncthreads();
+
+  // 4. map update (distinct slots, distinct new positions, and old positions
+  //    that are neither new positions nor pinned: safe in parallel)
+  for (int i = threadIdx.x; i < n; i += ASSIGN_THREADS) {
+    const int s = fill_slot[i];
+    const int32_t p = fill_pos[i];
+    const int32_t old = un.slot_pos[s];
+    if (old >= 0 && old < un.lmax) un.pos_slot[old] = -1;
+    un.slot_pos[s] = p;
+    un.pos_slot[p] = s;
+    un.fill_round[s] = round;
+  }
+  // served[e] = 1 only for owners that received a slot
+  for (int i = threadIdx.x; i < nM; i += ASSIGN_THREADS) {
+    if (i >= n) served[fill_entry[i]] = 0;
+  }
+  if (threadIdx.x == 0) {
+    if (n > 0) {
+      int h = fill_slot[n - 1] + 1;
+      un.state[DSA_ST_HAND] = h >= S ? 0 : h;
+    }
+    un.state[DSA_ST_EPOCH] = epoch;
+    g.nfill[u] = n;
+    int32_t* cu = counters + (size_t)u * 4;
+    cu[0] = s_cnt[0];
+    cu[1] = s_cnt[1];
+    cu[2] = s_cnt[2];
+    cu[3] = n;
+  }
+}
+
+__global__ void __launch_bounds__(COPY_THREADS)
+k_copy(const dsa_unit* __restrict__ units, int R, int K, const int32_t* __restrict__ topk_all,
+       const uint8_t* __restrict__ cls_all, uint8_t* __restrict__ rows_all, GatherWs g) {
+  const int u = blockIdx.y;
+  const int lane = threadIdx.x & 31;
+  const int item = blockIdx.x * COPY_WARPS + (threadIdx.x >> 5);
+  const int RK = R * K;
+  const dsa_unit& un = units[u];
+  uint8_t* rows = rows_all + (size_t)u * RK * DSA_ROW_BYTES;
+  if (item < RK) {
+    const int e = item;
+    if (g.served[(size_t)u * RK + e]) return;   // written by its fill below
+    const uint8_t c = cls_all[(size_t)u * RK + e];
+    const int32_t p = topk_all[(size_t)u * RK + e];
+    uint8_t* dst = rows + (size_t)e * DSA_ROW_BYTES;
+    if (c == DSA_CLS_HOT) {
+      warp_copy_row(dst, un.slots + (size_t)un.pos_slot[p] * DSA_ROW_BYTES, lane);
+    } else if (c == DSA_CLS_RING) {
+      warp_copy_row(dst, un.ring + (size_t)(p & (DSA_RING_ROWS - 1)) * DSA_ROW_BYTES, lane);
+    } else if (c == DSA_CLS_RAM) {
+      warp_copy_row(dst, un.mirror + (size_t)p * DSA_ROW_BYTES, lane);
+    } else {
+      warp_zero_row(dst, lane);
+    }
+  } else {
+    const int f = item - RK;
+    if (f >= g.nfill[u]) return;
+    const size_t o = (size_t)u * RK + f;
+    const int32_t p = g.fill_pos[o];
+    const int32_t s = g.fill_slot[o];
+    const int32_t e = g.fill_entry[o];
+    const uint4* src = reinterpret_cast<const uint4*>(un.mirror + (size_t)p * DSA_ROW_BYTES);
+    uint4* d1 = reinterpret_cast<uint4*>(un.slots + (size_t)s * DSA_ROW_BYTES);
+    uint4* d2 = reinterpret_cast<uint4*>(rows + (size_t)e * DSA_ROW_BYTES);
+    const uint4 a = ldg_nc_v4(src + lane);
+    uint4 b;
+    if (lane < 9) b = ldg_nc_v4(src + 32 + lane);
+    d1[lane] = a;
+    d2[lane] = a;
+    if (lane < 9) {
+      d1[32 + lane] = b;
+      d2[32 + lane] = b;
+    }
+  }
+}
+
+}  // namespace
+
+extern "C" size_t hot_gather_workspace(int32_t U, int32_t R, int32_t K) {
+  if (U < 1 || R < 1 || K < 1) return 0;
+  const size_t rk = (size_t)R * K;
+  return 4 * dsa_align((size_t)U * rk * 4, 256) + dsa_align((size_t)U * 4, 256) +
+         dsa_align((size_t)U * rk, 256);
+}
+
+extern "C" int hot_gather(const dsa_unit* units, int32_t U, int32_t R, int32_t K, int32_t round,
+                          const int32_t* topk_idx, uint8_t* cls, uint8_t* rows, int32_t* counters,
+                          void* ws, size_t ws_bytes, int32_t* dev_err, void* stream) {
+  if (!units || !topk_idx || !cls || !rows || !counters) return DSA_ERR_ARG;
+  if (U < 1 || U > 65535 || R < 1 || R > DSA_MAX_ROWS) return DSA_ERR_ARG;
+  if (K < 1 || K > DSA_MAX_K) return DSA_ERR_SHAPE;
+  if (!ws || ws_bytes < hot_gather_workspace(U, R, K)) return DSA_ERR_WS;
+  cudaStream_t st = static_cast<cudaStream_t>(stream);
+  GatherWs g = gather_ws(ws, U, R, K);
+  const int RK = R * K;
+  k_classify<<<dim3((RK + CLS_THREADS - 1) / CLS_THREADS, U), CLS_THREADS, 0, st>>>(
+      units, R, K, round, topk_idx, cls, dev_err);
+  if (dsa_launch_status() != DSA_OK) return DSA_ERR_CUDA;
+  k_assign<<<U, ASSIGN_THREADS, 0, st>>>(units, R, K, round, topk_idx, cls, counters, g, dev_err);
+  if (dsa_launch_status() != DSA_OK) return DSA_ERR_CUDA;
+  k_copy<<<dim3((2 * RK + COPY_WARPS - 1) / COPY_WARPS, U), COPY_THREADS, 0, st>>>(
+      units, R, K, topk_idx, cls, rows, g);
+  return dsa_launch_status();
+}

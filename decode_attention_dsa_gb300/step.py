@@ -1,0 +1,64 @@
+"""One decode step over a UnitSet: the four C-ABI calls in order, with
+persistent workspaces and outputs (marshalling only)."""
+from __future__ import annotations
+
+import torch
+
+from . import abi
+from .units import UnitSet
+
+
+class DecodePath:
+    """Workspaces and outputs for steps of ``R`` query rows, Top-``K``, ``H``
+    heads and ``A`` appended rows per unit per step."""
+
+    def __init__(self, units: UnitSet, R: int, K: int, H: int, A: int, scale: float,
+                 max_len: int | None = None):
+        self.u = units
+        U = units.U
+        self.R, self.K, self.H, self.A, self.scale = R, K, H, A, float(scale)
+        self.max_len = units.lmax if max_len is None else max_len
+        dev = units.device
+        self.ws_topk_bytes = abi.dsa_score_topk_workspace(U, R, self.max_len)
+        self.ws_topk = torch.zeros(self.ws_topk_bytes, dtype=torch.uint8, device=dev)
+        self.ws_gather_bytes = abi.hot_gather_workspace(U, R, K)
+        self.ws_gather = torch.zeros(self.ws_gather_bytes, dtype=torch.uint8, device=dev)
+        self.ws_attn_bytes = abi.mla_decode_attn_workspace(U, R, H, K)
+        self.ws_attn = torch.zeros(self.ws_attn_bytes, dtype=torch.uint8, device=dev)
+        self.topk = torch.empty((U, R, K), dtype=torch.int32, device=dev)
+        self.cls = torch.empty((U, R, K), dtype=torch.uint8, device=dev)
+        self.rows = torch.empty((U, R, K, abi.ROW_BYTES), dtype=torch.uint8, device=dev)
+        self.counters = torch.zeros((U, 4), dtype=torch.int32, device=dev)
+        self.out = torch.empty((U, R, H, abi.LAT_DIM), dtype=torch.float32, device=dev)
+        self.lse = torch.empty((U, R, H), dtype=torch.float32, device=dev)
+
+    def score_topk(self, q_idx, w, stream=None):
+        u = self.u
+        abi.dsa_score_topk(u.units, u.U, self.R, self.K, q_idx, w, self.topk, self.max_len,
+                           self.ws_topk, self.ws_topk_bytes, u.dev_err, stream)
+
+    def gather(self, rnd: int, stream=None):
+        u = self.u
+        abi.hot_gather(u.units, u.U, self.R, self.K, rnd, self.topk, self.cls, self.rows,
+                       self.counters, self.ws_gather, self.ws_gather_bytes, u.dev_err, stream)
+
+    def attend(self, q_lat, q_rope, stream=None):
+        u = self.u
+        abi.mla_decode_attn(u.U, self.R, self.H, self.K, q_lat, q_rope, self.rows, self.topk,
+                            self.scale, self.out, self.lse, self.ws_attn, self.ws_attn_bytes,
+                            u.dev_err, stream)
+
+    def append(self, new_rows, new_keys, stream=None):
+        u = self.u
+        abi.kv_append_writeback(u.units, u.U, self.A, new_rows, new_keys, u.dev_err, stream)
+
+    def step(self, rnd, q_idx, w, q_lat, q_rope, new_rows, new_keys, stream=None):
+        self.score_topk(q_idx, w, stream)
+        self.gather(rnd, stream)
+        self.attend(q_lat, q_rope, stream)
+        self.append(new_rows, new_keys, stream)
+
+    def launches_per_step(self) -> int:
+        """Kernel launches one step enqueues (score, select, classify, assign,
+        copy, attention partial, attention combine, append)."""
+        return 8

@@ -1,0 +1,104 @@
+"""Device buffers of a set of units and the device array of ``dsa_unit``.
+
+Host plumbing only (allocation, pointer marshalling, host views of the pinned
+mirror). Every array is carved so that the per-unit pieces keep the 16-byte
+alignment the kernels require.
+"""
+from __future__ import annotations
+
+import ctypes
+
+import numpy as np
+import torch
+
+from . import abi
+
+
+class UnitSet:
+    """U units with S hot slots and capacity ``lmax`` positions each.
+
+    ``mirror='host'`` puts the RAM mirror in pinned, mapped host memory
+    (offloaded, the pages' design); ``mirror='device'`` puts it in HBM (the
+    fully resident run of the same kernels).
+    """
+
+    def __init__(self, U: int, S: int, lmax: int, mirror: str = "host", device="cuda"):
+        abi.load()
+        self.U, self.S, self.lmax, self.mirror_kind = U, S, lmax, mirror
+        dev = torch.device(device)
+        self.device = dev
+        self.keys = torch.zeros((U, lmax, abi.IDX_DIM), dtype=torch.int16, device=dev)
+        self.slots = torch.zeros((U, S, abi.ROW_BYTES), dtype=torch.uint8, device=dev)
+        self.slot_pos = torch.full((U, S), -1, dtype=torch.int32, device=dev)
+        self.pos_slot = torch.full((U, lmax), -1, dtype=torch.int32, device=dev)
+        self.fill_round = torch.full((U, S), -1, dtype=torch.int32, device=dev)
+        self.pin_epoch = torch.full((U, S), -1, dtype=torch.int32, device=dev)
+        self.ring = torch.zeros((U, abi.RING_ROWS, abi.ROW_BYTES), dtype=torch.uint8, device=dev)
+        self.state = torch.zeros((U, abi.ST_WORDS), dtype=torch.int64, device=dev)
+        nbytes = U * lmax * abi.ROW_BYTES
+        self._host_ptr = None
+        if mirror == "host":
+            h, d = abi.dsa_host_alloc(max(nbytes, 16))
+            self._host_ptr = h
+            self._mirror_dev = d
+            buf = (ctypes.c_uint8 * max(nbytes, 16)).from_address(h)
+            self.mirror_host = np.ctypeslib.as_array(buf)[:nbytes].reshape(U, lmax, abi.ROW_BYTES)
+            self.mirror_dev_tensor = None
+        elif mirror == "device":
+            self.mirror_dev_tensor = torch.zeros((U, lmax, abi.ROW_BYTES), dtype=torch.uint8, device=dev)
+            self._mirror_dev = self.mirror_dev_tensor.data_ptr()
+            self.mirror_host = None
+        else:
+            raise ValueError(mirror)
+        arr = (abi.DsaUnit * U)()
+        for u in range(U):
+            arr[u] = abi.DsaUnit(
+                self.keys[u].data_ptr(), self.slots[u].data_ptr(), self.slot_pos[u].data_ptr(),
+                self.pos_slot[u].data_ptr(), self.fill_round[u].data_ptr(),
+                self.pin_epoch[u].data_ptr(), self.ring[u].data_ptr(),
+                self._mirror_dev + u * lmax * abi.ROW_BYTES, self.state[u].data_ptr(), S, 0, lmax)
+        raw = np.frombuffer(bytes(arr), dtype=np.uint8).copy()
+        self.units = torch.from_numpy(raw).to(dev)
+        self.dev_err = torch.zeros(1, dtype=torch.int32, device=dev)
+
+    # -------------------------------------------------------------- mirror
+    def mirror_unit(self, u: int):
+        """Host-visible view (numpy, host mirror) or tensor (device mirror) of unit u."""
+        return self.mirror_host[u] if self.mirror_host is not None else self.mirror_dev_tensor[u]
+
+    def set_mirror_rows(self, u: int, start: int, rows: np.ndarray) -> None:
+        n = rows.shape[0]
+        if self.mirror_host is not None:
+            self.mirror_host[u, start:start + n] = rows
+        else:
+            self.mirror_dev_tensor[u, start:start + n] = torch.from_numpy(rows).to(self.device)
+
+    def get_mirror_rows(self, u: int, start: int, n: int) -> np.ndarray:
+        if self.mirror_host is not None:
+            return np.array(self.mirror_host[u, start:start + n])
+        return self.mirror_dev_tensor[u, start:start + n].cpu().numpy()
+
+    def set_keys(self, u: int, start: int, keys_bits: np.ndarray) -> None:
+        t = torch.from_numpy(np.ascontiguousarray(keys_bits, dtype=np.uint16).view(np.int16))
+        self.keys[u, start:start + keys_bits.shape[0]] = t.to(self.device)
+
+    def init(self, l0, warm: int, stream=None) -> None:
+        l0t = torch.as_tensor(np.asarray(l0, dtype=np.int64).reshape(self.U), device=self.device)
+        self._l0 = l0t
+        abi.hc_init(self.units, self.U, warm, l0t, self.S, self.lmax, self.dev_err, stream)
+
+    def check(self) -> int:
+        return int(self.dev_err.item())
+
+    def close(self) -> None:
+        if self._host_ptr is not None:
+            torch.cuda.synchronize(self.device)
+            self.mirror_host = None
+            abi.dsa_host_free(self._host_ptr)
+            self._host_ptr = None
+
+    def __del__(self):
+        try:
+            self.close()
+        except Exception:
+            pass

@@ -1,0 +1,296 @@
+/*
+ * dsa_decode.h -- C ABI of the GB300 sparse-attention decode path.
+ *
+ * One decode step of one unit (a (session, layer) pair) runs five steps:
+ * DSA indexer scoring + Top-K, hot-cache gather, Q8G64 dequantisation,
+ * absorbed-MLA attention over the selected rows, and append with batched
+ * write-back. Every call below is batched over U units in one launch
+ * sequence, enqueues asynchronously on the caller's CUDA stream, and returns
+ * after host-side argument checks.
+ *
+ * Sources (page titles; section headings in the original and in English):
+ *   [P3]  "从总共 1M 到 15+ 路 × 1M：GLM-5.3 KV Cache 换出的容量突破"
+ *         (From 1M total to 15+ x 1M: GLM-5.3 KV-cache offload)
+ *   [ALG] "算法层：从注意力、KV Cache 到 FFN 与 MoE"
+ *         (Algorithm layer: from attention and KV cache to FFN and MoE)
+ *   [QNT] "量化不是压缩包：从模型分层到 4-bit 推理的工程真相"
+ *         (Quantization is not a zip file)
+ *
+ * Conventions
+ *   - The caller owns all memory. "device" pointers are CUDA device memory
+ *     (or a device-accessible alias of pinned host memory where stated).
+ *     No call allocates memory; scratch is a caller-provided workspace whose
+ *     size the matching *_workspace() query returns.
+ *   - `stream` is a cudaStream_t passed as void* (NULL = legacy stream).
+ *   - Return value: DSA_OK (0) or a negative DSA_ERR_* code. A host-side
+ *     error enqueues nothing. DSA_ERR_CUDA means a launch failed.
+ *   - Errors found on the device (an index out of bounds, an append beyond
+ *     capacity, a query value outside the attention kernel's range) are OR-ed
+ *     into the caller's device word `dev_err` as DSA_DEVERR_* bits; the kernel
+ *     skips the offending access and carries on. Read the word back after the
+ *     stream completes and pass it to dsa_check().
+ *   - bf16 and fp16 values are passed as their 16-bit patterns.
+ */
+#ifndef DSA_DECODE_H
+#define DSA_DECODE_H
+
+#include <stddef.h>
+#include <stdint.h>
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+/* ---------------------------------------------------------------- constants */
+
+#define DSA_OK 0
+#define DSA_ERR_ARG (-1)          /* null pointer or out-of-range argument        */
+#define DSA_ERR_SHAPE (-2)        /* unsupported shape (e.g. K > 4096, bad H)     */
+#define DSA_ERR_WS (-3)           /* workspace missing or too small               */
+#define DSA_ERR_CUDA (-4)         /* a CUDA runtime call or launch failed         */
+#define DSA_ERR_DEVICE_CHECK (-6) /* dsa_check(): the device word is non-zero     */
+
+#define DSA_DEVERR_BOUNDS 0x1     /* a position/slot index was out of range       */
+#define DSA_DEVERR_CAPACITY 0x2   /* append beyond the unit's lmax                */
+#define DSA_DEVERR_QRANGE 0x4     /* attention query outside the fp16 range       */
+
+#define DSA_ROW_BYTES 656         /* Q8G64 MLA row: 512 int8 + 8 fp16 + 64 bf16   */
+#define DSA_LAT_DIM 512
+#define DSA_ROPE_DIM 64
+#define DSA_IDX_HEADS 8
+#define DSA_IDX_DIM 64
+#define DSA_RING_ROWS 64
+#define DSA_MAX_K 4096
+#define DSA_MAX_ROWS 8            /* query rows per unit per step (MTP verify)   */
+
+#define DSA_CLS_HOT 0             /* read from an HBM hot slot                    */
+#define DSA_CLS_RING 1            /* read from the GPU recent ring                */
+#define DSA_CLS_RAM 2             /* read from the host RAM mirror                */
+#define DSA_CLS_PAD 3             /* no position (-1 in topk_idx)                 */
+
+#define DSA_WARM_EMPTY 0
+#define DSA_WARM_LAST_S 1
+
+/* state[] word indices of a unit (int64 each) */
+#define DSA_ST_LEN 0              /* logical rows (history length)               */
+#define DSA_ST_RAM 1              /* positions < this are in the RAM mirror       */
+#define DSA_ST_HAND 2             /* ring-replacement hand                        */
+#define DSA_ST_EPOCH 3            /* gather-call counter (pins are per call)      */
+#define DSA_ST_WRITEBACKS 4       /* number of write-back batches issued          */
+#define DSA_ST_WORDS 8
+
+/*
+ * One unit's cache state. An array of these lives in DEVICE memory and is
+ * passed to the calls as `units`. All pointers are device-accessible; the
+ * struct itself is written only by the caller (the kernels update the arrays
+ * it points to).
+ *
+ *   keys       bf16 [lmax][64]   indexer keys; position p at keys + 64*p.
+ *   slots      u8   [S][656]     hot-cache rows (HBM).
+ *   slot_pos   i32  [S]          position held by each slot, -1 = empty.
+ *   pos_slot   i32  [lmax]       slot holding each position, -1 = none.
+ *   fill_round i32  [S]          round of the slot's last fill (-1 = warm).
+ *   pin_epoch  i32  [S]          internal: gather call that last pinned it.
+ *   ring       u8   [64][656]    recent ring; position p at row p % 64.
+ *   mirror     u8   [lmax][656]  RAM mirror: device alias of pinned host
+ *                                memory from dsa_host_alloc() (offloaded), or
+ *                                HBM (the fully resident variant).
+ *   state      i64  [8]          DSA_ST_* words.
+ *   slots_n    S (>= 1).
+ *   lmax       capacity in positions (history + all appends).
+ * 16-byte alignment is required for keys, slots, ring and mirror.
+ */
+typedef struct dsa_unit {
+  uint16_t* keys;
+  uint8_t* slots;
+  int32_t* slot_pos;
+  int32_t* pos_slot;
+  int32_t* fill_round;
+  int32_t* pin_epoch;
+  uint8_t* ring;
+  uint8_t* mirror;
+  int64_t* state;
+  int32_t slots_n;
+  int32_t reserved0;
+  int64_t lmax;
+} dsa_unit;
+
+/* ------------------------------------------------------------ housekeeping */
+
+/* ABI version of this header (returns 1). */
+int dsa_abi_version(void);
+
+/* Static text for a DSA_* status code. */
+const char* dsa_status_string(int status);
+
+/* Map a device error word read back from `dev_err` to a status:
+ * DSA_OK if it is 0, else DSA_ERR_DEVICE_CHECK. */
+int dsa_check(int32_t dev_err_value);
+
+/*
+ * Pinned, mapped host memory for a unit's RAM mirror ([P3] section
+ * "第三次决策：让 GPU 直接管理热缓存" (third decision: the GPU manages the hot
+ * cache): a miss reads the *registered* RAM mirror directly; section
+ * "GPU 管缓存也会犯错": registration is done ahead of time so no first-use
+ * registration stall lands on the decode path).
+ *   host_ptr  out: host address (page-locked, mapped, portable).
+ *   dev_ptr   out: the device-accessible alias to put in dsa_unit.mirror.
+ * Returns DSA_ERR_CUDA if the allocation fails. Free with dsa_host_free().
+ * This is setup, not part of a decode step.
+ */
+int dsa_host_alloc(void** host_ptr, void** dev_ptr, size_t bytes);
+int dsa_host_free(void* host_ptr);
+
+/*
+ * Initialise U units' cache state for histories of l0[u] rows that are
+ * already in the mirror (positions [0, l0) are RAM-resident, the ring is
+ * empty, hand = 0).
+ *   units    device dsa_unit[U].
+ *   l0       device int64 [U]; 0 <= l0[u] <= lmax.
+ *   warm     DSA_WARM_EMPTY: every slot empty. DSA_WARM_LAST_S: slot i holds
+ *            position l0 - n + i for n = min(S, l0), fill_round -1, and its
+ *            bytes are copied from the mirror.
+ *   max_slots, max_lmax  host bounds: max over units of S and of lmax
+ *            (they size the grid).
+ * Also clears pin_epoch and the DSA_ST_* words. A unit whose l0 is outside
+ * [0, lmax] or whose S < 1 is left untouched and sets DSA_DEVERR_BOUNDS.
+ */
+int hc_init(const dsa_unit* units, int32_t U, int32_t warm, const int64_t* l0,
+            int32_t max_slots, int64_t max_lmax, int32_t* dev_err, void* stream);
+
+/* --------------------------------------------- A1 + A2: DSA score and Top-K */
+
+/*
+ * [P3] section "起点：把容量和当前计算的工作集分开" (starting point): the DSA
+ * indexer selects the Top-2048 history positions that MLA attention then
+ * consumes; section "第一次决策" (first decision): this stays the exact GPU
+ * path with a BF16 query.
+ *
+ * For each unit u and query row r, over the positions s in [0, L) with
+ * L = state[DSA_ST_LEN] at the start of the call:
+ *     I[r][s] = sum_h w[r][h] * max(0, sum_d q[r][h][d] * keys[s][d])
+ * (8 indexer heads, d = 64, float32 accumulation), and keeps the K largest
+ * scores, equal scores going to the lower position. Output: the K selected
+ * positions in ascending order, padded with -1 when L < K.
+ *
+ *   units     device dsa_unit[U] (keys and state[DSA_ST_LEN] are read).
+ *   q         device bf16 [U][R][8][64].
+ *   w         device float [U][R][8].
+ *   topk_idx  device int32 [U][R][K] (written).
+ *   max_len   host bound: max over units of L (sizes the grid).
+ *   ws        device workspace of dsa_score_topk_workspace(U, R, max_len)
+ *             bytes. It must be zero-filled once before its first use; every
+ *             call leaves it ready for the next.
+ * Shapes: 1 <= U, 1 <= R <= 8, 1 <= K <= 4096.
+ */
+size_t dsa_score_topk_workspace(int32_t U, int32_t R, int64_t max_len);
+int dsa_score_topk(const dsa_unit* units, int32_t U, int32_t R, int32_t K,
+                   const uint16_t* q, const float* w, int32_t* topk_idx,
+                   int64_t max_len, void* ws, size_t ws_bytes,
+                   int32_t* dev_err, void* stream);
+
+/* -------------------------------------------------------- A3: hot gather */
+
+/*
+ * [P3] section "第三次决策：让 GPU 直接管理热缓存" (third decision): the GPU
+ * looks up the hot slot of every selected position; a hit reads VRAM, a miss
+ * reads the registered RAM mirror, forming the compact selected set.
+ * [P3] section "GPU 管缓存也会犯错：跨 block 可见性与置换长扫描" (cross-block
+ * visibility and long replacement sweeps): slots filled in round r are hits
+ * only from round r + 1; duplicate misses of a round read RAM; slots in use
+ * this round are pinned; rows not yet written back are served by the recent
+ * ring; replacement is a ring that skips pinned slots.
+ *
+ * Per unit, with the state as it is when the call starts:
+ *   RING if p >= state[DSA_ST_RAM]; else HOT if pos_slot[p] = s >= 0 and
+ *   fill_round[s] < round; else RAM. HOT slots are pinned for this call.
+ *   The distinct RAM positions that hold no slot, in ascending order, take
+ *   the eligible slots (not pinned, fill_round < round) in cyclic order from
+ *   the hand: the old position loses its mapping, the slot gets the new
+ *   position, fill_round = round and the mirror row's bytes; then
+ *   hand = last slot + 1 (mod S). Misses beyond the eligible slots are served
+ *   from RAM and not inserted.
+ *
+ *   topk_idx  device int32 [U][R][K] (ascending per row, -1 padded).
+ *   cls       device u8 [U][R][K]: DSA_CLS_* per entry (written).
+ *   rows      device u8 [U][R][K][656]: the compact selected rows, bytes
+ *             exactly as read from their source (PAD entries are zeroed).
+ *   counters  device int32 [U][4]: HOT, RING, RAM entries, slots filled.
+ *   ws        device workspace of hot_gather_workspace(U, R, K) bytes.
+ * Shapes: 1 <= U, 1 <= R <= 8, 1 <= K <= 4096. `round` should not decrease
+ * from call to call on a unit (a repeated round is allowed).
+ */
+size_t hot_gather_workspace(int32_t U, int32_t R, int32_t K);
+int hot_gather(const dsa_unit* units, int32_t U, int32_t R, int32_t K,
+               int32_t round, const int32_t* topk_idx, uint8_t* cls,
+               uint8_t* rows, int32_t* counters, void* ws, size_t ws_bytes,
+               int32_t* dev_err, void* stream);
+
+/* ---------------------------------- A4 + A5: dequant and MLA decode attention */
+
+/*
+ * [ALG] section "2. Attention": softmax(Q K^T / sqrt(d_k)) V; section
+ * "3. KV Cache": MLA keeps the normalised latent and the RoPE part, INT8 per
+ * group for the latent. [QNT] section "三、基本思路": w_hat = scale * q with
+ * one scale per group (G64: 64 latent values). [P3] section "起点": a row is
+ * 512 B latent + 16 B scales + 128 B RoPE = 656 B.
+ *
+ * Absorbed MLA over the compact rows, for each unit u, query row r, head h:
+ *   c_j[d]  = int8_j[d] * fp16scale_j[d / 64]           (d < 512)
+ *   logit_j = scale * (q_lat[h] . c_j + q_rope[h] . rope_j)
+ *   out[h]  = sum_j softmax_j(logit) * c_j,   lse[h] = log sum_j exp(logit_j)
+ * over the entries j with topk_idx >= 0; with none, out = 0 and lse = -inf.
+ *
+ *   q_lat   device bf16 [U][R][H][512];  q_rope device bf16 [U][R][H][64].
+ *           |q| must stay below 65504 (the kernel computes in fp16 operands
+ *           with fp32 accumulation); larger values set DSA_DEVERR_QRANGE.
+ *   rows    device u8 [U][R][K][656] (hot_gather's output).
+ *   topk_idx device int32 [U][R][K] (only the sign is used: -1 = padding).
+ *   out     device float [U][R][H][512];  lse device float [U][R][H] or NULL.
+ *   ws      device workspace of mla_decode_attn_workspace(U, R, H, K) bytes.
+ * Shapes: H in {16, 32, 48, 64, 80, 96, 112, 128}, 1 <= K <= 4096.
+ */
+size_t mla_decode_attn_workspace(int32_t U, int32_t R, int32_t H, int32_t K);
+int mla_decode_attn(int32_t U, int32_t R, int32_t H, int32_t K,
+                    const uint16_t* q_lat, const uint16_t* q_rope,
+                    const uint8_t* rows, const int32_t* topk_idx, float scale,
+                    float* out, float* lse, void* ws, size_t ws_bytes,
+                    int32_t* dev_err, void* stream);
+
+/* ------------------------------------------- A6: append and batched write-back */
+
+/*
+ * [P3] section "第三次决策": new KV goes to a GPU recent ring and is written
+ * back to the RAM history in batches; section "第二次决策" (second decision):
+ * 64-row batches replaced per-row, per-layer transfers; small logs are copied
+ * by compute kernels rather than DMA operations.
+ *
+ * For each unit and a = 0..A-1, with p = state[DSA_ST_LEN]:
+ *   ring[p % 64] = new_rows[a]; keys[p] = new_keys[a]; LEN += 1;
+ *   when LEN - state[DSA_ST_RAM] == 64, the 64 ring rows of positions
+ *   [RAM, RAM + 64) are stored to mirror (41,984 B, by the kernel) and
+ *   RAM += 64.
+ * An append with p >= lmax sets DSA_DEVERR_CAPACITY and is dropped.
+ *   new_rows device u8 [U][A][656];  new_keys device bf16 [U][A][64].
+ * Shapes: 1 <= U, 1 <= A <= 64.
+ */
+int kv_append_writeback(const dsa_unit* units, int32_t U, int32_t A,
+                        const uint8_t* new_rows, const uint16_t* new_keys,
+                        int32_t* dev_err, void* stream);
+
+/*
+ * [P3] section "容量优化必须通过会话生命周期" (capacity work must survive the
+ * session lifecycle): before exporting or restoring the full history, flush
+ * the log, wait for write-back, and check that the RAM row count has reached
+ * the logical row count.
+ *
+ * Stores the partial batch [RAM, LEN) from the ring to the mirror and sets
+ * RAM = LEN. After the stream completes, the mirror holds every row.
+ */
+int kv_flush(const dsa_unit* units, int32_t U, int32_t* dev_err, void* stream);
+
+#ifdef __cplusplus
+}
+#endif
+
+#endif /* DSA_DECODE_H */

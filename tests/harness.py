@@ -1,0 +1,128 @@
+"""Shared set-up for the GPU parity tests: builds the same workload on the
+CUDA path (through the C ABI) and in the oracle, from the numpy generator."""
+from __future__ import annotations
+
+import numpy as np
+
+from oracle.decode import OracleUnit, decode_step
+from oracle.hotcache import PAD
+from synth import workloads as W
+
+
+def gpu_modules():
+    import torch
+    from decode_attention_dsa_gb300 import abi
+    from decode_attention_dsa_gb300.step import DecodePath
+    from decode_attention_dsa_gb300.units import UnitSet
+    return torch, abi, UnitSet, DecodePath
+
+
+class Pair:
+    """A workload run side by side on the GPU and in the oracle."""
+
+    def __init__(self, wl: W.Workload, units=None, mirror="host", oracle_units=None):
+        torch, abi, UnitSet, DecodePath = gpu_modules()
+        self.torch, self.abi = torch, abi
+        self.wl = wl
+        self.uidx = list(range(wl.U)) if units is None else list(units)
+        self.oidx = self.uidx if oracle_units is None else list(oracle_units)
+        U = len(self.uidx)
+        self.g = UnitSet(U, wl.S, wl.lmax, mirror=mirror)
+        self.o = {}
+        hist = np.arange(wl.L0)
+        for i, u in enumerate(self.uidx):
+            keys = W.keys_bits(wl, u, hist)
+            rows = W.rows_bytes(wl, u, hist)
+            self.g.set_keys(i, 0, keys)
+            self.g.set_mirror_rows(i, 0, rows)
+            if u in self.oidx:
+                self.o[u] = OracleUnit.create(wl.S, wl.lmax, wl.L0, keys, rows, wl.warm)
+        self.g.init([wl.L0] * U, abi.WARM_LAST_S if wl.warm == "last_s" else abi.WARM_EMPTY)
+        self.p = DecodePath(self.g, wl.R, wl.K, wl.H, wl.A, wl.scale())
+        torch.cuda.synchronize()
+
+    def inputs(self, step):
+        torch = self.torch
+        per = [W.step_inputs(self.wl, u, step) for u in self.uidx]
+        dev = self.g.device
+
+        def t16(a):
+            return torch.from_numpy(np.ascontiguousarray(np.stack(a)).view(np.int16)).to(dev)
+        return per, dict(
+            q_idx=t16([x.q_idx for x in per]),
+            w=torch.from_numpy(np.stack([x.w for x in per])).to(dev),
+            q_lat=t16([x.q_lat for x in per]),
+            q_rope=t16([x.q_rope for x in per]),
+            new_rows=torch.from_numpy(np.stack([x.new_rows for x in per])).to(dev),
+            new_keys=t16([x.new_keys for x in per]),
+        )
+
+    def step(self, step, rnd=None, attention=True):
+        """Run one step on both sides; return (gpu dict, oracle dict per unit)."""
+        rnd = step if rnd is None else rnd
+        per, t = self.inputs(step)
+        p = self.p
+        p.score_topk(t["q_idx"], t["w"])
+        p.gather(rnd)
+        if attention:
+            p.attend(t["q_lat"], t["q_rope"])
+        p.append(t["new_rows"], t["new_keys"])
+        self.torch.cuda.synchronize()
+        g = dict(topk=p.topk.cpu().numpy(), cls=p.cls.cpu().numpy(), counters=p.counters.cpu().numpy())
+        if attention:
+            g["out"] = p.out.cpu().numpy()
+            g["lse"] = p.lse.cpu().numpy()
+        g["rows"] = p.rows.cpu().numpy()
+        ores = {}
+        for i, u in enumerate(self.uidx):
+            if u not in self.o:
+                continue
+            x = per[i]
+            ores[u] = decode_step(self.o[u], rnd, self.wl.K, self.wl.scale(), x.q_idx, x.w, x.q_lat,
+                                  x.q_rope, x.new_rows, x.new_keys, attention=attention)
+        return g, ores
+
+    def state(self, i):
+        g = self.g
+        return dict(slot_pos=g.slot_pos[i].cpu().numpy(), fill_round=g.fill_round[i].cpu().numpy(),
+                    pos_slot=g.pos_slot[i].cpu().numpy(), st=g.state[i].cpu().numpy(),
+                    ring=g.ring[i].cpu().numpy())
+
+
+def check_step(pair: Pair, g, ores, attention=True, rows=True, full_state=True, atol_rel=1e-3):
+    """Element-by-element comparison of one step; returns the worst attention error ratio."""
+    worst = 0.0
+    wl = pair.wl
+    for i, u in enumerate(pair.uidx):
+        if u not in ores:
+            continue
+        o = ores[u]
+        oc = pair.o[u].cache
+        assert np.array_equal(g["topk"][i], o["topk"]), f"unit {u}: Top-K differs"
+        assert np.array_equal(g["cls"][i], o["cls"]), f"unit {u}: classification differs"
+        assert np.array_equal(g["counters"][i], o["counters"]), f"unit {u}: counters differ"
+        if rows:
+            assert np.array_equal(g["rows"][i], o["rows"]), f"unit {u}: gathered rows differ"
+        s = pair.state(i)
+        assert np.array_equal(s["slot_pos"], oc.slot_pos), f"unit {u}: slot map differs"
+        assert np.array_equal(s["fill_round"], oc.fill_round), f"unit {u}: fill rounds differ"
+        assert s["st"][0] == oc.length and s["st"][1] == oc.rows_in_ram, f"unit {u}: len/ram"
+        assert s["st"][2] == oc.hand, f"unit {u}: hand differs"
+        if full_state:
+            assert np.array_equal(s["pos_slot"], oc.pos_slot[:wl.lmax]), f"unit {u}: pos_slot"
+            assert np.array_equal(s["ring"], oc.ring), f"unit {u}: ring differs"
+        if attention:
+            for r in range(wl.R):
+                ref = o["out"][r]
+                err = np.abs(g["out"][i, r].astype(np.float64) - ref).max()
+                scale = np.abs(ref).max()
+                ratio = err / (atol_rel * scale) if scale > 0 else err
+                worst = max(worst, ratio)
+                assert err <= atol_rel * scale or (scale == 0 and err == 0), \
+                    f"unit {u} row {r}: attention err {err:.3e} > {atol_rel}*{scale:.3e}"
+                valid = o["cls"][r] != PAD
+                if valid.any():
+                    assert np.allclose(g["lse"][i, r], o["lse"][r], rtol=0, atol=1e-4)
+                else:
+                    assert np.isneginf(g["lse"][i, r]).all()
+    return worst

@@ -1,0 +1,132 @@
+"""GPU parity: the CUDA path through the C ABI against the oracle, element by
+element. Index sets, classification, counters, slot map, ring and gathered
+bytes must be bit-exact; attention within max|gpu - oracle| <= 1e-3 * max|oracle|
+per (step, unit, query row), the bound the decode path is specified to."""
+import numpy as np
+import pytest
+
+from synth import workloads as W
+from tests.harness import Pair, check_step
+
+pytestmark = pytest.mark.gpu
+
+
+@pytest.fixture(autouse=True)
+def _need_gpu():
+    torch = pytest.importorskip("torch")
+    if not torch.cuda.is_available():
+        pytest.skip("no CUDA device")
+
+
+def run(wl, steps=None, rnds=None, mirror="host", check_every=1, attention_every=1,
+        full_state=True, units=None, oracle_units=None):
+    pair = Pair(wl, units=units, mirror=mirror, oracle_units=oracle_units)
+    steps = range(wl.steps) if steps is None else steps
+    worst = 0.0
+    for k, st in enumerate(steps):
+        rnd = None if rnds is None else rnds[k]
+        att = (k % attention_every) == 0 or k == len(steps) - 1
+        g, o = pair.step(st, rnd=rnd, attention=att)
+        if (k % check_every) == 0 or k == len(steps) - 1:
+            worst = max(worst, check_step(pair, g, o, attention=att, full_state=full_state))
+        assert pair.g.check() == 0, f"device error word {pair.g.check():#x}"
+    return pair, worst
+
+
+def test_config0_tiny_smoke_all_steps():
+    pair, worst = run(W.WORKLOADS[0])
+    assert worst < 1.0
+
+
+SMALL = [
+    # R=4 verify rows with duplicates, evictions every step, 4 appends per step
+    dict(L0=1500, S=64, R=4, A=4, K=128, H=64, warm="last_s", mode="mtp", steps=20),
+    # one query row, heavy eviction from an empty cache
+    dict(L0=700, S=16, R=1, A=1, K=64, H=16, warm="empty", steps=24),
+    # history shorter than K: -1 padding, then it grows past K
+    dict(L0=100, S=32, R=2, A=3, K=128, H=32, warm="empty", steps=16),
+    # ragged score tiles and cluster ranges, 48 and 128 heads
+    dict(L0=3 * 512 + 37, S=256, R=1, A=1, K=200, H=48, warm="last_s", steps=6),
+    dict(L0=9000, S=300, R=3, A=2, K=1000, H=128, warm="last_s", mode="mtp", steps=4),
+    # K = 1 and tiny history
+    dict(L0=5, S=4, R=1, A=1, K=1, H=16, warm="empty", steps=70),
+]
+
+
+@pytest.mark.parametrize("cfg", SMALL, ids=[f"L{c['L0']}_S{c['S']}_R{c['R']}_K{c['K']}" for c in SMALL])
+def test_small_variants(cfg):
+    base = W.WORKLOADS[0]
+    wl = base.with_(name="variant", **cfg)
+    run(wl)
+
+
+def test_empty_history_then_growth():
+    wl = W.WORKLOADS[0].with_(name="empty", L0=0, S=8, K=16, H=16, steps=80)
+    run(wl)
+
+
+def test_repeated_round_visibility():
+    """Calls that repeat a round number: slots filled earlier in the same round
+    are RAM (not HOT) and are not evicted in that round."""
+    wl = W.WORKLOADS[0].with_(name="rep", L0=800, S=32, K=48, H=16, steps=10, warm="empty")
+    rnds = [0, 0, 0, 1, 1, 2, 2, 2, 3, 3]
+    run(wl, rnds=rnds)
+
+
+def test_resident_mirror_same_results():
+    wl = W.WORKLOADS[0].with_(name="resident", steps=4)
+    run(wl, mirror="device")
+
+
+def test_flush_makes_ram_complete():
+    wl = W.WORKLOADS[0].with_(name="flush", L0=300, S=16, K=32, H=16, steps=30, A=3)
+    pair, _ = run(wl)
+    p = pair
+    p.abi.kv_flush(p.g.units, p.g.U, p.g.dev_err)
+    p.torch.cuda.synchronize()
+    oc = p.o[0].cache
+    oc.flush()
+    st = p.g.state[0].cpu().numpy()
+    assert st[0] == st[1] == oc.length == oc.rows_in_ram
+    got = p.g.get_mirror_rows(0, 0, oc.length)
+    want = oc.mirror.rows(np.arange(oc.length))
+    assert np.array_equal(got, want)
+
+
+def test_append_beyond_capacity_sets_device_flag():
+    wl = W.WORKLOADS[0].with_(name="cap", L0=10, S=4, K=4, H=16, steps=1, A=1)
+    pair = Pair(wl)
+    torch, abi = pair.torch, pair.abi
+    rows = torch.zeros((1, 1, 656), dtype=torch.uint8, device="cuda")
+    keys = torch.zeros((1, 1, 64), dtype=torch.int16, device="cuda")
+    abi.kv_append_writeback(pair.g.units, 1, 1, rows, keys, pair.g.dev_err)   # fills lmax
+    torch.cuda.synchronize()
+    assert pair.g.check() == 0
+    abi.kv_append_writeback(pair.g.units, 1, 1, rows, keys, pair.g.dev_err)   # one too many
+    torch.cuda.synchronize()
+    assert pair.g.check() & abi.DEVERR_CAPACITY
+    assert pair.g.state[0, 0].item() == wl.lmax
+
+
+@pytest.mark.slow
+def test_config1_full_size_first_steps():
+    """50K single stream, 4 layers, full sizes and the bench's launch shapes;
+    66 steps cross the first 64-row write-back."""
+    wl = W.WORKLOADS[1]
+    _, worst = run(wl, steps=range(66), attention_every=11)
+    assert worst < 1.0
+
+
+@pytest.mark.slow
+def test_config2_mtp_verify_first_steps():
+    wl = W.WORKLOADS[2]
+    _, worst = run(wl, steps=range(18), attention_every=6)
+    assert worst < 1.0
+
+
+@pytest.mark.slow
+def test_config3_cache_stress_first_steps():
+    wl = W.WORKLOADS[3]
+    pair, worst = run(wl, steps=range(6), attention_every=3)
+    c = pair.p.counters.cpu().numpy()[0]
+    assert c[2] / wl.K < 0.05          # phase 1: about 1% of the Top-K misses
