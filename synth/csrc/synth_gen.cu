@@ -41,7 +41,7 @@ __device__ __forceinline__ int64_t ih_num(uint64_t key, uint64_t f0) {
   return s + 6 - 6 * 65536;
 }
 
-__global__ void k_keys(uint64_t key, uint16_t* out, int64_t pos0, int64_t n, int tagged,
+__global__ void gen_keys(uint64_t key, uint16_t* out, int64_t pos0, int64_t n, int tagged,
                        int64_t hot_lo, int64_t hot_hi) {
   const int64_t i = (int64_t)blockIdx.x * blockDim.x + threadIdx.x;
   if (i >= n * 64) return;
@@ -52,7 +52,7 @@ __global__ void k_keys(uint64_t key, uint16_t* out, int64_t pos0, int64_t n, int
   out[i] = bf16_rne((float)v);
 }
 
-__global__ void k_rows(uint64_t k_lat, uint64_t k_sc, uint64_t k_rope, uint8_t* out, int64_t pos0,
+__global__ void gen_rows(uint64_t k_lat, uint64_t k_sc, uint64_t k_rope, uint8_t* out, int64_t pos0,
                        int64_t n) {
   const int64_t i = (int64_t)blockIdx.x * blockDim.x + threadIdx.x;
   // 512 latent bytes + 8 scales + 64 rope values = 584 items per row
@@ -78,7 +78,7 @@ __global__ void k_rows(uint64_t k_lat, uint64_t k_sc, uint64_t k_rope, uint8_t* 
   }
 }
 
-__global__ void k_normal(uint64_t key, uint16_t* out, int64_t item0, int64_t n_items, int per) {
+__global__ void gen_normal(uint64_t key, uint16_t* out, int64_t item0, int64_t n_items, int per) {
   const int64_t i = (int64_t)blockIdx.x * blockDim.x + threadIdx.x;
   if (i >= n_items * per) return;
   const uint64_t f0 = ((uint64_t)(item0 + i / per) * per + (uint64_t)(i % per)) * 12;
@@ -87,7 +87,7 @@ __global__ void k_normal(uint64_t key, uint16_t* out, int64_t item0, int64_t n_i
 
 // Uniform integers in [lo, hi] as bf16; with tag_every > 0 the last value of
 // every group of tag_every is replaced by tag16 / 16.
-__global__ void k_uniform_bf16(uint64_t key, uint16_t* out, int64_t item0, int64_t n_items, int per,
+__global__ void gen_uniform_bf16(uint64_t key, uint16_t* out, int64_t item0, int64_t n_items, int per,
                                int lo, int hi, int tag_every, int tag16) {
   const int64_t i = (int64_t)blockIdx.x * blockDim.x + threadIdx.x;
   if (i >= n_items * per) return;
@@ -98,7 +98,7 @@ __global__ void k_uniform_bf16(uint64_t key, uint16_t* out, int64_t item0, int64
 }
 
 // Uniform integers as float32; output item i uses generator item (item0 + i) / rep.
-__global__ void k_uniform_f32(uint64_t key, float* out, int64_t item0, int64_t n_items, int per,
+__global__ void gen_uniform_f32(uint64_t key, float* out, int64_t item0, int64_t n_items, int per,
                               int lo, int hi, int rep) {
   const int64_t i = (int64_t)blockIdx.x * blockDim.x + threadIdx.x;
   if (i >= n_items * per) return;
@@ -107,7 +107,7 @@ __global__ void k_uniform_f32(uint64_t key, float* out, int64_t item0, int64_t n
 }
 
 // MTP verify rows of one step: q16 = clip(16 * base + floor((num * sd16 + 32768) / 65536), -128, 128).
-__global__ void k_mtp(uint64_t k_base, uint64_t k_pert, uint16_t* out, int64_t step, int R, int sd16) {
+__global__ void gen_mtp(uint64_t k_base, uint64_t k_pert, uint16_t* out, int64_t step, int R, int sd16) {
   const int i = blockIdx.x * blockDim.x + threadIdx.x;
   if (i >= R * 512) return;
   const int r = i / 512, v = i % 512;
@@ -130,7 +130,7 @@ int synth_keys(uint64_t key, uint16_t* out, int64_t pos0, int64_t n, int tagged,
                int64_t hot_hi, void* stream) {
   if (n <= 0) return 0;
   cudaStream_t s = (cudaStream_t)stream;
-  k_keys<<<blocks(n * 64, 256), 256, 0, s>>>(key, out, pos0, n, tagged, hot_lo, hot_hi);
+  gen_keys<<<blocks(n * 64, 256), 256, 0, s>>>(key, out, pos0, n, tagged, hot_lo, hot_hi);
   return st(s);
 }
 
@@ -138,7 +138,7 @@ int synth_rows(uint64_t k_lat, uint64_t k_sc, uint64_t k_rope, uint8_t* out, int
                void* stream) {
   if (n <= 0) return 0;
   cudaStream_t s = (cudaStream_t)stream;
-  k_rows<<<blocks(n * 584, 256), 256, 0, s>>>(k_lat, k_sc, k_rope, out, pos0, n);
+  gen_rows<<<blocks(n * 584, 256), 256, 0, s>>>(k_lat, k_sc, k_rope, out, pos0, n);
   return st(s);
 }
 
@@ -146,7 +146,7 @@ int synth_normal_bf16(uint64_t key, uint16_t* out, int64_t item0, int64_t n_item
                       void* stream) {
   if (n_items <= 0) return 0;
   cudaStream_t s = (cudaStream_t)stream;
-  k_normal<<<blocks(n_items * per, 256), 256, 0, s>>>(key, out, item0, n_items, per);
+  gen_normal<<<blocks(n_items * per, 256), 256, 0, s>>>(key, out, item0, n_items, per);
   return st(s);
 }
 
@@ -154,7 +154,7 @@ int synth_uniform_bf16(uint64_t key, uint16_t* out, int64_t item0, int64_t n_ite
                        int hi, int tag_every, int tag16, void* stream) {
   if (n_items <= 0) return 0;
   cudaStream_t s = (cudaStream_t)stream;
-  k_uniform_bf16<<<blocks(n_items * per, 256), 256, 0, s>>>(key, out, item0, n_items, per, lo, hi,
+  gen_uniform_bf16<<<blocks(n_items * per, 256), 256, 0, s>>>(key, out, item0, n_items, per, lo, hi,
                                                             tag_every, tag16);
   return st(s);
 }
@@ -163,14 +163,14 @@ int synth_uniform_f32(uint64_t key, float* out, int64_t item0, int64_t n_items, 
                       int hi, int rep, void* stream) {
   if (n_items <= 0 || rep < 1) return 0;
   cudaStream_t s = (cudaStream_t)stream;
-  k_uniform_f32<<<blocks(n_items * per, 256), 256, 0, s>>>(key, out, item0, n_items, per, lo, hi, rep);
+  gen_uniform_f32<<<blocks(n_items * per, 256), 256, 0, s>>>(key, out, item0, n_items, per, lo, hi, rep);
   return st(s);
 }
 
 int synth_mtp_qidx(uint64_t k_base, uint64_t k_pert, uint16_t* out, int64_t step, int R, int sd16,
                    void* stream) {
   cudaStream_t s = (cudaStream_t)stream;
-  k_mtp<<<blocks((int64_t)R * 512, 256), 256, 0, s>>>(k_base, k_pert, out, step, R, sd16);
+  gen_mtp<<<blocks((int64_t)R * 512, 256), 256, 0, s>>>(k_base, k_pert, out, step, R, sd16);
   return st(s);
 }
 

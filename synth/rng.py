@@ -104,7 +104,8 @@ def uniform_int_fields(f: np.ndarray, lo: int, hi: int) -> np.ndarray:
 
 def normal_fields_f32(f: np.ndarray) -> np.ndarray:
     """Map fields ``[..., 12*m]`` to ``m`` Irwin-Hall normals per row (exact float32)."""
-    g = f.reshape(f.shape[:-1] + (-1, NORMAL_FIELDS)).astype(np.int64)
+    m = f.shape[-1] // NORMAL_FIELDS
+    g = f.reshape(f.shape[:-1] + (m, NORMAL_FIELDS)).astype(np.int64)
     num = g.sum(axis=-1) + 6 - 6 * 65536
     return (num.astype(np.float64) / 65536.0).astype(np.float32)
 
