@@ -17,7 +17,7 @@ LIB_PATH = os.path.join(PKG, "libdsa_decode.so")
 
 DSA_OK = 0
 DSA_ERR_ARG, DSA_ERR_SHAPE, DSA_ERR_WS, DSA_ERR_CUDA, DSA_ERR_DEVICE_CHECK = -1, -2, -3, -4, -6
-DEVERR_BOUNDS, DEVERR_CAPACITY, DEVERR_QRANGE = 0x1, 0x2, 0x4
+DEVERR_BOUNDS, DEVERR_CAPACITY, DEVERR_QRANGE, DEVERR_TIMEOUT = 0x1, 0x2, 0x4, 0x8
 ROW_BYTES, LAT_DIM, ROPE_DIM, IDX_HEADS, IDX_DIM, RING_ROWS = 656, 512, 64, 8, 64, 64
 MAX_K, MAX_ROWS = 4096, 8
 CLS_HOT, CLS_RING, CLS_RAM, CLS_PAD = 0, 1, 2, 3

@@ -52,7 +52,8 @@ extern "C" {
 
 #define DSA_DEVERR_BOUNDS 0x1     /* a position/slot index was out of range       */
 #define DSA_DEVERR_CAPACITY 0x2   /* append beyond the unit's lmax                */
-#define DSA_DEVERR_QRANGE 0x4     /* attention query outside the fp16 range       */
+#define DSA_DEVERR_QRANGE 0x4     /* attention operand outside the fp16 range    */
+#define DSA_DEVERR_TIMEOUT 0x8    /* a bounded wait inside a kernel gave up        */
 
 #define DSA_ROW_BYTES 656         /* Q8G64 MLA row: 512 int8 + 8 fp16 + 64 bf16   */
 #define DSA_LAT_DIM 512
@@ -242,8 +243,9 @@ int hot_gather(const dsa_unit* units, int32_t U, int32_t R, int32_t K,
  * over the entries j with topk_idx >= 0; with none, out = 0 and lse = -inf.
  *
  *   q_lat   device bf16 [U][R][H][512];  q_rope device bf16 [U][R][H][64].
- *           |q| must stay below 65504 (the kernel computes in fp16 operands
- *           with fp32 accumulation); larger values set DSA_DEVERR_QRANGE.
+ *           The tensor-core operands are fp16 with fp32 accumulation: |q| and
+ *           |int8 * scale| must stay below 65504, else DSA_DEVERR_QRANGE is
+ *           set. Each operand is rounded once to fp16 (relative error <= 2^-11).
  *   rows    device u8 [U][R][K][656] (hot_gather's output).
  *   topk_idx device int32 [U][R][K] (only the sign is used: -1 = padding).
  *   out     device float [U][R][H][512];  lse device float [U][R][H] or NULL.

@@ -61,6 +61,7 @@ class Pair:
         """Run one step on both sides; return (gpu dict, oracle dict per unit)."""
         rnd = step if rnd is None else rnd
         per, t = self.inputs(step)
+        self.last_inputs = per
         p = self.p
         p.score_topk(t["q_idx"], t["w"])
         p.gather(rnd)
@@ -87,6 +88,23 @@ class Pair:
         return dict(slot_pos=g.slot_pos[i].cpu().numpy(), fill_round=g.fill_round[i].cpu().numpy(),
                     pos_slot=g.pos_slot[i].cpu().numpy(), st=g.state[i].cpu().numpy(),
                     ring=g.ring[i].cpu().numpy())
+
+
+def lse_bound(pair, per_q, r, i):
+    """Per-head bound on |lse_gpu - lse_oracle|: the tensor-core operands are
+    rounded once to fp16 (relative error <= 2^-11 each), so every logit moves by
+    at most scale * 2^-11 * sum_d |q_d| * |k_d| * 2 (one rounding on each side
+    of the product, q is exact for these bf16 inputs but is counted anyway);
+    log-sum-exp moves by at most the largest logit change. 1e-5 covers fp32
+    accumulation and the exp/log evaluations."""
+    from oracle.q8g64 import dequant_latent, rope_values
+    from oracle.indexer import bf16_to_f64
+    wl = pair.wl
+    rows = per_q["rows"][r][per_q["cls"][r] != PAD]
+    k = np.concatenate([np.abs(dequant_latent(rows)), np.abs(rope_values(rows))], axis=1)
+    x = pair.last_inputs[i]
+    q = np.concatenate([np.abs(bf16_to_f64(x.q_lat[r])), np.abs(bf16_to_f64(x.q_rope[r]))], axis=1)
+    return wl.scale() * 2.0 ** -11 * 2 * (q @ k.T).max(axis=1) + 1e-5
 
 
 def check_step(pair: Pair, g, ores, attention=True, rows=True, full_state=True, atol_rel=1e-3):
@@ -122,7 +140,9 @@ def check_step(pair: Pair, g, ores, attention=True, rows=True, full_state=True, 
                     f"unit {u} row {r}: attention err {err:.3e} > {atol_rel}*{scale:.3e}"
                 valid = o["cls"][r] != PAD
                 if valid.any():
-                    assert np.allclose(g["lse"][i, r], o["lse"][r], rtol=0, atol=1e-4)
+                    tol = lse_bound(pair, per_q=ores[u], r=r, i=i)
+                    d = np.abs(g["lse"][i, r].astype(np.float64) - o["lse"][r])
+                    assert (d <= tol).all(), f"unit {u} row {r}: lse err {d.max():.3e}"
                 else:
                     assert np.isneginf(g["lse"][i, r]).all()
     return worst
