@@ -12,7 +12,9 @@ pinned host memory). The value is layer-steps/s (units x steps / time).
 
 Timing: W >= 3 untimed warm-up steps, then K steps; L2 is flushed (a 512 MiB
 write) before every timed step, outside its CUDA-event bracket; the sum of the
-per-step event times is the timed total. Inputs are generated on the device
+per-step event times is the timed total. The K timed steps (flushes and event
+records included) are captured once into a CUDA graph and replayed once, so
+host launch cost is off the device timeline; ``--no-graph`` launches directly. Inputs are generated on the device
 before timing. ``e2e`` repeats the K steps from the same initial state through
 the C ABI with host buffers: each step copies its inputs from pinned host
 memory and the attention output back, inside the bracket.
@@ -51,6 +53,7 @@ def parse():
     ap.add_argument("--mirror", choices=["host", "device"], default="host")
     ap.add_argument("--impl", choices=["gb300", "reference"], default="gb300")
     ap.add_argument("--no-e2e", action="store_true")
+    ap.add_argument("--no-graph", action="store_true", help="launch steps directly, no CUDA graph")
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--cpu-sample-steps", type=int, default=None)
     ap.add_argument("--oracle-child", type=str, default=None, help=argparse.SUPPRESS)
@@ -254,31 +257,49 @@ def run_gpu(args, rank: int, world: int):
     # ---- device-resident run
     units.init([wl.L0] * U, warm)
     for s in range(Wm):
-        path.step(s, *step_args(s))
+        path.step(abi.ROUND_AUTO, *step_args(s))
     torch.cuda.synchronize()
     if world > 1:
         torch.distributed.barrier()
     torch.cuda.synchronize()
-    ev = [[torch.cuda.Event(enable_timing=True) for _ in range(5)] for _ in range(K)]
+    use_graph = not args.no_graph
+    ev = [[torch.cuda.Event(enable_timing=True, external=use_graph) for _ in range(5)]
+          for _ in range(K)]
     ctr_acc = torch.zeros((U, 4), dtype=torch.int64, device=dev)
+    rnd = abi.ROUND_AUTO
+
+    def timed_steps():
+        for i in range(K):
+            s = Wm + i
+            qi, w, ql, qr, nr, nk = step_args(s)
+            flush.fill_(i & 0xFF)
+            e = ev[i]
+            e[0].record()
+            path.score_topk(qi, w)
+            e[1].record()
+            path.gather(rnd)
+            e[2].record()
+            path.attend(ql, qr)
+            e[3].record()
+            path.append(nr, nk)
+            e[4].record()
+            ctr_acc.add_(path.counters)
+
+    graph = None
+    if use_graph:
+        graph = torch.cuda.CUDAGraph()
+        cap = torch.cuda.Stream()
+        cap.wait_stream(torch.cuda.current_stream())
+        with torch.cuda.graph(graph, stream=cap):
+            timed_steps()
+        torch.cuda.synchronize()
     clocks = ClockSampler(torch.cuda.current_device())
     clocks.start()
     wall0 = time.perf_counter()
-    for i in range(K):
-        s = Wm + i
-        qi, w, ql, qr, nr, nk = step_args(s)
-        flush.fill_(i & 0xFF)
-        e = ev[i]
-        e[0].record()
-        path.score_topk(qi, w)
-        e[1].record()
-        path.gather(s)
-        e[2].record()
-        path.attend(ql, qr)
-        e[3].record()
-        path.append(nr, nk)
-        e[4].record()
-        ctr_acc += path.counters
+    if graph is not None:
+        graph.replay()
+    else:
+        timed_steps()
     torch.cuda.synchronize()
     wall = time.perf_counter() - wall0
     clk = clocks.stop()
@@ -307,20 +328,31 @@ def run_gpu(args, rank: int, world: int):
         d2h = path.out.numel() * 4
         units.init([wl.L0] * U, warm)
         for s in range(Wm):
-            path.step(s, *step_args(s))
+            path.step(abi.ROUND_AUTO, *step_args(s))
         torch.cuda.synchronize()
-        ee = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True))
-              for _ in range(K)]
-        for i in range(K):
-            s = Wm + i
-            flush.fill_(i & 0xFF)
-            ee[i][0].record()
-            for n in names:
-                dev_in[n].copy_(host[n][i], non_blocking=True)
-            path.step(s, dev_in["q_idx"], dev_in["w"], dev_in["q_lat"], dev_in["q_rope"],
-                      dev_in["new_rows"], dev_in["new_keys"])
-            out_host[i].copy_(path.out, non_blocking=True)
-            ee[i][1].record()
+        ee = [(torch.cuda.Event(enable_timing=True, external=use_graph),
+               torch.cuda.Event(enable_timing=True, external=use_graph)) for _ in range(K)]
+
+        def e2e_steps():
+            for i in range(K):
+                flush.fill_(i & 0xFF)
+                ee[i][0].record()
+                for n in names:
+                    dev_in[n].copy_(host[n][i], non_blocking=True)
+                path.step(abi.ROUND_AUTO, dev_in["q_idx"], dev_in["w"], dev_in["q_lat"],
+                          dev_in["q_rope"], dev_in["new_rows"], dev_in["new_keys"])
+                out_host[i].copy_(path.out, non_blocking=True)
+                ee[i][1].record()
+        if use_graph:
+            g2 = torch.cuda.CUDAGraph()
+            cap = torch.cuda.Stream()
+            cap.wait_stream(torch.cuda.current_stream())
+            with torch.cuda.graph(g2, stream=cap):
+                e2e_steps()
+            torch.cuda.synchronize()
+            g2.replay()
+        else:
+            e2e_steps()
         torch.cuda.synchronize()
         e2e_ms = sum(a.elapsed_time(b) for a, b in ee)
         if world > 1:
@@ -398,6 +430,7 @@ def run_gpu(args, rank: int, world: int):
                   "miss_frac": float(ctr[2] / max(1, ctr[:3].sum()))},
         "clocks": clk,
         "gpu_launches": path.launches_per_step() * K,
+        "cuda_graph": use_graph,
         "wall_s": wall,
     }
     if e2e:

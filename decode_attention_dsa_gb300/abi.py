@@ -19,7 +19,7 @@ DSA_OK = 0
 DSA_ERR_ARG, DSA_ERR_SHAPE, DSA_ERR_WS, DSA_ERR_CUDA, DSA_ERR_DEVICE_CHECK = -1, -2, -3, -4, -6
 DEVERR_BOUNDS, DEVERR_CAPACITY, DEVERR_QRANGE, DEVERR_TIMEOUT = 0x1, 0x2, 0x4, 0x8
 ROW_BYTES, LAT_DIM, ROPE_DIM, IDX_HEADS, IDX_DIM, RING_ROWS = 656, 512, 64, 8, 64, 64
-MAX_K, MAX_ROWS = 4096, 8
+MAX_K, MAX_ROWS, MAX_ATTN_K, ROUND_AUTO = 4096, 8, 2048, -1
 CLS_HOT, CLS_RING, CLS_RAM, CLS_PAD = 0, 1, 2, 3
 WARM_EMPTY, WARM_LAST_S = 0, 1
 ST_LEN, ST_RAM, ST_HAND, ST_EPOCH, ST_WRITEBACKS, ST_WORDS = 0, 1, 2, 3, 4, 8

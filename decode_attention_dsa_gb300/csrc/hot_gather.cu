@@ -70,6 +70,7 @@ k_classify(const dsa_unit* __restrict__ units, int R, int K, int round,
   const int64_t len = un.state[DSA_ST_LEN];
   const int64_t ram = un.state[DSA_ST_RAM];
   const int32_t epoch = (int32_t)(un.state[DSA_ST_EPOCH] + 1);
+  if (round < 0) round = epoch - 1;
   const int32_t p = topk[(size_t)u * R * K + e];
   uint8_t c = DSA_CLS_PAD;
   if (p >= 0) {
@@ -120,6 +121,7 @@ k_assign(const dsa_unit* __restrict__ units, int R, int K, int round,
   uint8_t* served = g.served + (size_t)u * RK;
   const int S = un.slots_n;
   const int32_t epoch = (int32_t)(un.state[DSA_ST_EPOCH] + 1);
+  if (round < 0) round = epoch - 1;
 
   if (threadIdx.x < 4) s_cnt[threadIdx.x] = 0;
   __syncthreads();

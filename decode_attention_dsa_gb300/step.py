@@ -24,7 +24,8 @@ class DecodePath:
         self.ws_gather_bytes = abi.hot_gather_workspace(U, R, K)
         self.ws_gather = torch.zeros(self.ws_gather_bytes, dtype=torch.uint8, device=dev)
         self.ws_attn_bytes = abi.mla_decode_attn_workspace(U, R, H, K)
-        self.ws_attn = torch.zeros(self.ws_attn_bytes, dtype=torch.uint8, device=dev)
+        self.ws_attn = (torch.zeros(self.ws_attn_bytes, dtype=torch.uint8, device=dev)
+                        if self.ws_attn_bytes else None)
         self.topk = torch.empty((U, R, K), dtype=torch.int32, device=dev)
         self.cls = torch.empty((U, R, K), dtype=torch.uint8, device=dev)
         self.rows = torch.empty((U, R, K, abi.ROW_BYTES), dtype=torch.uint8, device=dev)
@@ -60,5 +61,5 @@ class DecodePath:
 
     def launches_per_step(self) -> int:
         """Kernel launches one step enqueues (score, select, classify, assign,
-        copy, attention partial, attention combine, append)."""
-        return 8
+        copy, attention, append)."""
+        return 7

@@ -63,6 +63,8 @@ extern "C" {
 #define DSA_RING_ROWS 64
 #define DSA_MAX_K 4096
 #define DSA_MAX_ROWS 8            /* query rows per unit per step (MTP verify)   */
+#define DSA_MAX_ATTN_K 2048       /* selected rows per attention query row       */
+#define DSA_ROUND_AUTO (-1)       /* hot_gather: use the unit's gather-call count */
 
 #define DSA_CLS_HOT 0             /* read from an HBM hot slot                    */
 #define DSA_CLS_RING 1            /* read from the GPU recent ring                */
@@ -219,7 +221,10 @@ int dsa_score_topk(const dsa_unit* units, int32_t U, int32_t R, int32_t K,
  *   counters  device int32 [U][4]: HOT, RING, RAM entries, slots filled.
  *   ws        device workspace of hot_gather_workspace(U, R, K) bytes.
  * Shapes: 1 <= U, 1 <= R <= 8, 1 <= K <= 4096. `round` should not decrease
- * from call to call on a unit (a repeated round is allowed).
+ * from call to call on a unit (a repeated round is allowed). A negative
+ * `round` (DSA_ROUND_AUTO) uses each unit's state[DSA_ST_EPOCH], the number of
+ * earlier hot_gather calls on it, so one call per decode step gives rounds
+ * 0, 1, 2, ... with fixed arguments (e.g. inside a captured CUDA graph).
  */
 size_t hot_gather_workspace(int32_t U, int32_t R, int32_t K);
 int hot_gather(const dsa_unit* units, int32_t U, int32_t R, int32_t K,
@@ -249,8 +254,10 @@ int hot_gather(const dsa_unit* units, int32_t U, int32_t R, int32_t K,
  *   rows    device u8 [U][R][K][656] (hot_gather's output).
  *   topk_idx device int32 [U][R][K] (only the sign is used: -1 = padding).
  *   out     device float [U][R][H][512];  lse device float [U][R][H] or NULL.
- *   ws      device workspace of mla_decode_attn_workspace(U, R, H, K) bytes.
- * Shapes: H in {16, 32, 48, 64, 80, 96, 112, 128}, 1 <= K <= 4096.
+ *   ws      device workspace of mla_decode_attn_workspace() bytes (0: the
+ *           chunk results are merged on chip; pass NULL).
+ * Shapes: H in {16, 32, 48, 64}, 1 <= K <= DSA_MAX_ATTN_K, U * R <= 65535.
+ * One thread-block cluster of ceil(K / 128) CTAs per (unit, query row).
  */
 size_t mla_decode_attn_workspace(int32_t U, int32_t R, int32_t H, int32_t K);
 int mla_decode_attn(int32_t U, int32_t R, int32_t H, int32_t K,

@@ -57,9 +57,10 @@ class Pair:
             new_keys=t16([x.new_keys for x in per]),
         )
 
-    def step(self, step, rnd=None, attention=True):
+    def step(self, step, rnd=None, attention=True, oracle_rnd=None):
         """Run one step on both sides; return (gpu dict, oracle dict per unit)."""
         rnd = step if rnd is None else rnd
+        ornd = rnd if oracle_rnd is None else oracle_rnd
         per, t = self.inputs(step)
         self.last_inputs = per
         p = self.p
@@ -79,7 +80,7 @@ class Pair:
             if u not in self.o:
                 continue
             x = per[i]
-            ores[u] = decode_step(self.o[u], rnd, self.wl.K, self.wl.scale(), x.q_idx, x.w, x.q_lat,
+            ores[u] = decode_step(self.o[u], ornd, self.wl.K, self.wl.scale(), x.q_idx, x.w, x.q_lat,
                                   x.q_rope, x.new_rows, x.new_keys, attention=attention)
         return g, ores
 

@@ -19,14 +19,15 @@ def _need_gpu():
 
 
 def run(wl, steps=None, rnds=None, mirror="host", check_every=1, attention_every=1,
-        full_state=True, units=None, oracle_units=None):
+        full_state=True, units=None, oracle_units=None, oracle_rnds=None):
     pair = Pair(wl, units=units, mirror=mirror, oracle_units=oracle_units)
     steps = range(wl.steps) if steps is None else steps
     worst = 0.0
     for k, st in enumerate(steps):
         rnd = None if rnds is None else rnds[k]
+        ornd = None if oracle_rnds is None else oracle_rnds[k]
         att = (k % attention_every) == 0 or k == len(steps) - 1
-        g, o = pair.step(st, rnd=rnd, attention=att)
+        g, o = pair.step(st, rnd=rnd, attention=att, oracle_rnd=ornd)
         if (k % check_every) == 0 or k == len(steps) - 1:
             worst = max(worst, check_step(pair, g, o, attention=att, full_state=full_state))
         assert pair.g.check() == 0, f"device error word {pair.g.check():#x}"
@@ -45,9 +46,9 @@ SMALL = [
     dict(L0=700, S=16, R=1, A=1, K=64, H=16, warm="empty", steps=24),
     # history shorter than K: -1 padding, then it grows past K
     dict(L0=100, S=32, R=2, A=3, K=128, H=32, warm="empty", steps=16),
-    # ragged score tiles and cluster ranges, 48 and 128 heads
+    # ragged score tiles and cluster ranges, 48 heads, ragged attention clusters
     dict(L0=3 * 512 + 37, S=256, R=1, A=1, K=200, H=48, warm="last_s", steps=6),
-    dict(L0=9000, S=300, R=3, A=2, K=1000, H=128, warm="last_s", mode="mtp", steps=4),
+    dict(L0=9000, S=300, R=3, A=2, K=1000, H=64, warm="last_s", mode="mtp", steps=4),
     # K = 1 and tiny history
     dict(L0=5, S=4, R=1, A=1, K=1, H=16, warm="empty", steps=70),
 ]
@@ -71,6 +72,12 @@ def test_repeated_round_visibility():
     wl = W.WORKLOADS[0].with_(name="rep", L0=800, S=32, K=48, H=16, steps=10, warm="empty")
     rnds = [0, 0, 0, 1, 1, 2, 2, 2, 3, 3]
     run(wl, rnds=rnds)
+
+
+def test_round_auto_matches_explicit_rounds():
+    """hot_gather with DSA_ROUND_AUTO uses the call count as the round."""
+    wl = W.WORKLOADS[0].with_(name="auto", L0=900, S=48, K=64, H=16, steps=12, warm="empty")
+    run(wl, rnds=[-1] * 12, oracle_rnds=list(range(12)))
 
 
 def test_resident_mirror_same_results():
