@@ -17,6 +17,7 @@ LIB_PATH = os.path.join(PKG, "libdsa_decode.so")
 
 DSA_OK = 0
 DSA_ERR_ARG, DSA_ERR_SHAPE, DSA_ERR_WS, DSA_ERR_CUDA, DSA_ERR_DEVICE_CHECK = -1, -2, -3, -4, -6
+DSA_ERR_SCRATCH_LIMIT = -7
 DEVERR_BOUNDS, DEVERR_CAPACITY, DEVERR_QRANGE, DEVERR_TIMEOUT = 0x1, 0x2, 0x4, 0x8
 ROW_BYTES, LAT_DIM, ROPE_DIM, IDX_HEADS, IDX_DIM, RING_ROWS = 656, 512, 64, 8, 64, 64
 MAX_K, MAX_ROWS, MAX_ATTN_K, ROUND_AUTO = 4096, 8, 2048, -1
@@ -56,6 +57,7 @@ SIGNATURES = {
     "hc_init": (ctypes.c_int, [_VP, _I32, _I32, _VP, _I32, _I64, _VP, _VP]),
     "dsa_score_topk_workspace": (_SZ, [_I32, _I32, _I64]),
     "dsa_score_topk": (ctypes.c_int, [_VP, _I32, _I32, _I32, _VP, _VP, _VP, _I64, _VP, _SZ, _VP, _VP]),
+    "dsa_score_topk_noalloc": (ctypes.c_int, [_VP, _I32, _I32, _I32, _VP, _VP, _VP, _I64, _VP, _VP]),
     "hot_gather_workspace": (_SZ, [_I32, _I32, _I32]),
     "hot_gather": (ctypes.c_int, [_VP, _I32, _I32, _I32, _I32, _VP, _VP, _VP, _VP, _VP, _SZ, _VP, _VP]),
     "mla_decode_attn_workspace": (_SZ, [_I32, _I32, _I32, _I32]),
@@ -147,6 +149,12 @@ def dsa_score_topk(units, U, R, K, q, w, topk_idx, max_len, ws, ws_bytes, dev_er
     return _ok("dsa_score_topk", load().dsa_score_topk(
         _p(units), U, R, K, _p(q), _p(w), _p(topk_idx), max_len, _p(ws), ws_bytes, _p(dev_err),
         _s(stream)))
+
+
+def dsa_score_topk_noalloc(units, U, R, K, q, w, topk_idx, max_len, dev_err, stream=None):
+    """dsa_score_topk with the library's fixed built-in scratch (no workspace)."""
+    return _ok("dsa_score_topk_noalloc", load().dsa_score_topk_noalloc(
+        _p(units), U, R, K, _p(q), _p(w), _p(topk_idx), max_len, _p(dev_err), _s(stream)))
 
 
 def hot_gather_workspace(U, R, K) -> int:

@@ -147,6 +147,7 @@ extern "C" const char* dsa_status_string(int status) {
     case DSA_ERR_WS: return "workspace missing or too small";
     case DSA_ERR_CUDA: return "CUDA runtime or launch error";
     case DSA_ERR_DEVICE_CHECK: return "device-side check failed (see the dev_err bits)";
+    case DSA_ERR_SCRATCH_LIMIT: return "problem exceeds the fixed built-in scratch of this entry point";
     default: return "unknown status";
   }
 }

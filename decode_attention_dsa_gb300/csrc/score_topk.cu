@@ -353,3 +353,52 @@ extern "C" int dsa_score_topk(const dsa_unit* units, int32_t U, int32_t R, int32
                                                                   dev_err);
   return dsa_launch_status();
 }
+
+// ---------------------------------------------------------------------------
+// dsa_score_topk_noalloc: the same scoring and selection for callers that may
+// not allocate device memory. Its scratch (selection histograms and ordered
+// score keys) lives in one fixed array compiled into this library.
+
+namespace {
+
+constexpr int64_t NOALLOC_MAX_UR = 16;          // units x query rows per call
+constexpr int64_t NOALLOC_MAX_LEN = 65536;      // history positions per unit
+constexpr size_t NOALLOC_HIST_BYTES = (size_t)NOALLOC_MAX_UR * HIST1_BINS * 4;   // 256 KiB
+constexpr size_t NOALLOC_BYTES =
+    NOALLOC_HIST_BYTES + (size_t)NOALLOC_MAX_UR * NOALLOC_MAX_LEN * 4;           // 4.25 MiB
+constexpr int NOALLOC_MAX_DEVICES = 64;
+
+static __device__ __align__(256) uint8_t g_topk_scratch[NOALLOC_BYTES];
+
+// Device address of g_topk_scratch, per device ordinal (looked up once).
+void* g_topk_scratch_addr[NOALLOC_MAX_DEVICES];
+
+}  // namespace
+
+extern "C" int dsa_score_topk_noalloc(const dsa_unit* units, int32_t U, int32_t R, int32_t K,
+                                      const uint16_t* q, const float* w, int32_t* topk_idx,
+                                      int64_t max_len, int32_t* dev_err, void* stream) {
+  if (!units || !q || !w || !topk_idx) return DSA_ERR_ARG;
+  if (U < 1 || R < 1 || R > DSA_MAX_ROWS || max_len < 0) return DSA_ERR_ARG;
+  if (K < 1 || K > DSA_MAX_K) return DSA_ERR_SHAPE;
+  if ((int64_t)U * R > NOALLOC_MAX_UR || max_len > NOALLOC_MAX_LEN) return DSA_ERR_SCRATCH_LIMIT;
+  int dev = -1;
+  if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= NOALLOC_MAX_DEVICES) return DSA_ERR_CUDA;
+  if (!g_topk_scratch_addr[dev]) {
+    // First call on this device: host code cannot use the array's name as a
+    // device address, so ask the runtime for it (the device must be current).
+    void* p = nullptr;
+    if (cudaGetSymbolAddress(&p, g_topk_scratch) != cudaSuccess || !p) return DSA_ERR_CUDA;
+    g_topk_scratch_addr[dev] = p;
+  }
+  void* scratch = g_topk_scratch_addr[dev];
+  const size_t need = dsa_score_topk_workspace(U, R, max_len);
+  if (need > NOALLOC_BYTES) return DSA_ERR_SCRATCH_LIMIT;
+  // The array keeps whatever the previous call left; the histograms must
+  // start at zero, so clear them (an interrupted earlier call may have left
+  // counts behind).
+  if (cudaMemsetAsync(scratch, 0, (size_t)U * R * HIST1_BINS * 4, static_cast<cudaStream_t>(stream)) !=
+      cudaSuccess)
+    return DSA_ERR_CUDA;
+  return dsa_score_topk(units, U, R, K, q, w, topk_idx, max_len, scratch, NOALLOC_BYTES, dev_err, stream);
+}

@@ -49,6 +49,7 @@ extern "C" {
 #define DSA_ERR_WS (-3)           /* workspace missing or too small               */
 #define DSA_ERR_CUDA (-4)         /* a CUDA runtime call or launch failed         */
 #define DSA_ERR_DEVICE_CHECK (-6) /* dsa_check(): the device word is non-zero     */
+#define DSA_ERR_SCRATCH_LIMIT (-7) /* problem larger than a fixed built-in scratch */
 
 #define DSA_DEVERR_BOUNDS 0x1     /* a position/slot index was out of range       */
 #define DSA_DEVERR_CAPACITY 0x2   /* append beyond the unit's lmax                */
@@ -191,6 +192,31 @@ int dsa_score_topk(const dsa_unit* units, int32_t U, int32_t R, int32_t K,
                    const uint16_t* q, const float* w, int32_t* topk_idx,
                    int64_t max_len, void* ws, size_t ws_bytes,
                    int32_t* dev_err, void* stream);
+
+/*
+ * dsa_score_topk without a caller workspace, for callers that cannot
+ * allocate device memory: for example code that runs inside a host framework
+ * which owns every device allocation and forbids cudaMalloc, or a loop that
+ * must never stall on the allocator. The pages have no counterpart to this
+ * entry point; it computes exactly what dsa_score_topk computes (same
+ * arguments minus ws/ws_bytes) and enqueues the same kernels.
+ *
+ * Its scratch is one array of 4.25 MiB compiled into this library (device
+ * memory that every GPU which loads the library keeps until the process
+ * exits). Limits: U * R <= 16 and max_len <= 65,536; larger problems return
+ * DSA_ERR_SCRATCH_LIMIT and enqueue nothing.
+ *   - The first call on a device looks up the array's device address with
+ *     cudaGetSymbolAddress (the device must be current). Make that first call
+ *     before capturing any stream into a CUDA graph.
+ *   - Every call shares the one array: calls that may overlap on the GPU (two
+ *     streams, or two host threads) race and give wrong results. Calls in one
+ *     stream are ordered and safe.
+ *   - Each call clears the histogram part of the array (a cudaMemsetAsync on
+ *     `stream`) before scoring; no call allocates or frees memory.
+ */
+int dsa_score_topk_noalloc(const dsa_unit* units, int32_t U, int32_t R, int32_t K,
+                           const uint16_t* q, const float* w, int32_t* topk_idx,
+                           int64_t max_len, int32_t* dev_err, void* stream);
 
 /* -------------------------------------------------------- A3: hot gather */
 
