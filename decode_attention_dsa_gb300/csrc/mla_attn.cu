@@ -22,10 +22,11 @@
 //     completion through tcgen05.commit on an mbarrier;
 //  5. softmax of the CTA's 128 columns per head in registers; P (fp16) goes to
 //     X as the A operand of PV;
-//  6. O (64 x 512 fp32) is staged in Y; after a cluster barrier CTA c merges
-//     columns [c*W, c*W + W) of every CTA's O through distributed shared
-//     memory with the max/sum rescaling of split softmax, and writes the final
-//     out (and lse) directly. No partial outputs leave the chip.
+//  6. each CTA stores its O (64 x 512 fp32) to its workspace slot (it stays in
+//     L2) and its max/sum to shared memory; after a cluster barrier CTA c
+//     merges columns [c*W, c*W + W) of every CTA's O with the max/sum
+//     rescaling of split softmax (maxima and sums read through distributed
+//     shared memory) and writes the final out (and lse) directly.
 // fp16 operands keep 11 significant bits: each operand's rounding is <= 2^-11
 // relative, far inside the 1e-3 * max|out| budget. Waits are bounded; on a
 // timeout the kernel sets DSA_DEVERR_TIMEOUT, frees its tensor memory and
@@ -67,12 +68,22 @@ struct Misc {
   int fail;
   float m[64];
   float l[64];
-  uint8_t valid[NC];
+  uint32_t vmask[NC / 32];    // validity of this CTA's rows
 };
+
+// Softmax partials, in region X beyond the P atoms (the query block is dead
+// once S is computed).
+struct SoftmaxScratch {
+  float pm[2][64];            // partial max per column half
+  float pl[2][64];            // partial sum per column half
+};
+constexpr int SMX_OFF = 4 * QATOM;
 static_assert(sizeof(Misc) <= 1024, "misc block");
 
 // Merge-phase scratch, placed in region X once P is no longer needed.
 struct MergeScratch {
+  float rm[MAX_CLUSTER][64];  // every source CTA's max per head
+  float rl[MAX_CLUSTER][64];  // every source CTA's sum per head
   float f[MAX_CLUSTER][64];   // exp(m_c - M) per source CTA and head
   float inv[64];              // 1 / L per head
 };
@@ -86,7 +97,7 @@ __device__ __forceinline__ uint32_t pack_h2(float a, float b) {
 __global__ void __launch_bounds__(THREADS, 1)
 k_mla_attn(int R, int H, int K, const uint16_t* __restrict__ q_lat, const uint16_t* __restrict__ q_rope,
            const uint8_t* __restrict__ rows, const int32_t* __restrict__ topk, float scale,
-           float* __restrict__ out, float* __restrict__ lse, int32_t* dev_err) {
+           float* __restrict__ out, float* __restrict__ lse, float* __restrict__ ws_o, int32_t* dev_err) {
   extern __shared__ __align__(1024) uint8_t sm[];
   cg::cluster_group cluster = cg::this_cluster();
   const int C = (int)cluster.num_blocks();
@@ -117,7 +128,11 @@ k_mla_attn(int R, int H, int K, const uint16_t* __restrict__ q_lat, const uint16
     tc::mbar_arrive_expect_tx(&ms->bar[0], bytes);
     tc::bulk_g2s(sX, rows + ((size_t)ur * K + j0) * DSA_ROW_BYTES, bytes, &ms->bar[0]);
   }
-  if (tid < NC) ms->valid[tid] = (tid < nrows) && topk[(size_t)ur * K + j0 + tid] >= 0;
+  if (tid < NC) {
+    const bool v = (tid < nrows) && topk[(size_t)ur * K + j0 + tid] >= 0;
+    const unsigned b = __ballot_sync(0xffffffffu, v);
+    if (lane == 0) ms->vmask[warp] = b;
+  }
 
   // query block loads, in flight while the rows arrive: 64 heads x 72 chunks of 8 dims
   constexpr int QCH = 64 * 72 / THREADS;        // 18 chunks per thread
@@ -141,7 +156,7 @@ k_mla_attn(int R, int H, int K, const uint16_t* __restrict__ q_lat, const uint16
   if (!failed) {
     bool bad = false;
     for (int t = tid; t < NC * 36; t += THREADS) {
-      const int j = t / 36, c = t % 36;
+      const int j = t % NC, c = t / NC;     // consecutive threads: consecutive rows
       uint4 lo = make_uint4(0, 0, 0, 0), hi = make_uint4(0, 0, 0, 0);
       if (j < nrows) {
         const uint8_t* row = sX + j * DSA_ROW_BYTES;
@@ -221,42 +236,57 @@ k_mla_attn(int R, int H, int K, const uint16_t* __restrict__ q_lat, const uint16
   __syncthreads();
   failed = ms->fail != 0;
 
-  // ---- softmax over this CTA's columns: warps 0, 1 hold head rows 0..63
-  if (warp < 2 && !failed) {
-    float s[NC];
+  // ---- softmax over this CTA's columns. Warps 0,1,4,5 can read TMEM lanes
+  // 0..63 (head rows); warp w takes lane quarter w & 3 and column half w >> 2.
+  const bool sm_warp = (warp & 3) < 2;
+  const int hr = 32 * (warp & 3) + lane;      // head row of this thread (sm_warp only)
+  const int half = warp >> 2;
+  SoftmaxScratch* sx = reinterpret_cast<SoftmaxScratch*>(sX + SMX_OFF);
+  float s[64];
+  if (sm_warp && !failed) {
 #pragma unroll
-    for (int c = 0; c < NC / 32; ++c) {
+    for (int c = 0; c < 2; ++c) {
       float v[32];
-      tc::tmem_ld32(tmem + ((uint32_t)(32 * warp) << 16) + 32 * c, v);
+      tc::tmem_ld32(tmem + ((uint32_t)(32 * (warp & 3)) << 16) + 64 * half + 32 * c, v);
+      const uint32_t vm = ms->vmask[2 * half + c];
 #pragma unroll
-      for (int i = 0; i < 32; ++i) s[32 * c + i] = v[i];
+      for (int i = 0; i < 32; ++i) s[32 * c + i] = ((vm >> i) & 1u) ? v[i] * scale : -INFINITY;
     }
-    float m = -INFINITY;
+    float m0 = -INFINITY, m1 = -INFINITY, m2 = -INFINITY, m3 = -INFINITY;
 #pragma unroll
-    for (int j = 0; j < NC; ++j) {
-      s[j] = ms->valid[j] ? s[j] * scale : -INFINITY;
-      m = fmaxf(m, s[j]);
+    for (int j = 0; j < 64; j += 4) {
+      m0 = fmaxf(m0, s[j]);
+      m1 = fmaxf(m1, s[j + 1]);
+      m2 = fmaxf(m2, s[j + 2]);
+      m3 = fmaxf(m3, s[j + 3]);
     }
-    float l = 0.f;
+    sx->pm[half][hr] = fmaxf(fmaxf(m0, m1), fmaxf(m2, m3));
+  }
+  __syncthreads();
+  if (sm_warp && !failed) {
+    const float m = fmaxf(sx->pm[0][hr], sx->pm[1][hr]);
+    float l0 = 0.f, l1 = 0.f;
 #pragma unroll
-    for (int j = 0; j < NC; ++j) {
+    for (int j = 0; j < 64; j += 2) {
       s[j] = (m == -INFINITY) ? 0.f : __expf(s[j] - m);
-      l += s[j];
+      s[j + 1] = (m == -INFINITY) ? 0.f : __expf(s[j + 1] - m);
+      l0 += s[j];
+      l1 += s[j + 1];
     }
-    const int hr = 32 * warp + lane;
+    sx->pl[half][hr] = l0 + l1;
 #pragma unroll
-    for (int c8 = 0; c8 < NC / 8; ++c8) {
+    for (int c8 = 0; c8 < 8; ++c8) {
       const uint4 v = make_uint4(pack_h2(s[8 * c8], s[8 * c8 + 1]), pack_h2(s[8 * c8 + 2], s[8 * c8 + 3]),
                                  pack_h2(s[8 * c8 + 4], s[8 * c8 + 5]), pack_h2(s[8 * c8 + 6], s[8 * c8 + 7]));
-      *reinterpret_cast<uint4*>(sX + (c8 >> 3) * QATOM + tc::sw128_off(hr, (8 * c8) & 63)) = v;
+      *reinterpret_cast<uint4*>(sX + half * QATOM + tc::sw128_off(hr, 8 * c8)) = v;
     }
-    ms->m[hr] = m;
-    ms->l[hr] = l;
+    if (half == 0) ms->m[hr] = m;
   }
   tc::fence_async_shared();
   tc::fence_before_sync();
   __syncthreads();
   tc::fence_after_sync();
+  if (tid < 64) ms->l[tid] = sx->pl[0][tid] + sx->pl[1][tid];
 
   // ---- O = P V: TMEM columns [0, 512)
   if (tid == 0 && !failed) {
@@ -276,15 +306,16 @@ k_mla_attn(int R, int H, int K, const uint16_t* __restrict__ q_lat, const uint16
   __syncthreads();
   failed = ms->fail != 0;
 
-  // ---- stage O (64 x 512 fp32) in Y: warps 0,1,4,5 (lane quarters 0 and 1)
-  float* sO = reinterpret_cast<float*>(sY);
+  // ---- this CTA's O (64 x 512 fp32) to its slot of the workspace (L2):
+  //      warps 0,1,4,5 (lane quarters 0 and 1), 128 contiguous bytes per store run
+  float* gO = ws_o + ((size_t)ur * MAX_CLUSTER + crank) * 64 * 512;
   if ((warp & 3) < 2 && !failed) {
     const int hr = 32 * (warp & 3) + lane;
     const int c0 = 256 * (warp >> 2);
     for (int c = 0; c < 8; ++c) {
       float v[32];
       tc::tmem_ld32(tmem + ((uint32_t)(32 * (warp & 3)) << 16) + c0 + 32 * c, v);
-      float4* dst = reinterpret_cast<float4*>(sO + hr * OSTR + c0 + 32 * c);
+      float4* dst = reinterpret_cast<float4*>(gO + hr * 512 + c0 + 32 * c);
 #pragma unroll
       for (int i = 0; i < 8; ++i) dst[i] = make_float4(v[4 * i], v[4 * i + 1], v[4 * i + 2], v[4 * i + 3]);
     }
@@ -303,16 +334,22 @@ k_mla_attn(int R, int H, int K, const uint16_t* __restrict__ q_lat, const uint16
     const int c0 = crank * W, c1 = min(512, c0 + W);
     const int nq = max(0, (c1 - c0) / 4);
     MergeScratch* mg = reinterpret_cast<MergeScratch*>(sX);
+    // one round of remote loads: every source CTA's (m, l) for every head
+    for (int t = tid; t < C * 64; t += THREADS) {
+      const Misc* rm = cluster.map_shared_rank(ms, t >> 6);
+      mg->rm[t >> 6][t & 63] = rm->m[t & 63];
+      mg->rl[t >> 6][t & 63] = rm->l[t & 63];
+    }
+    __syncthreads();
     if (tid < 64) {
       const int h = tid;
       float M = -INFINITY;
-      for (int c = 0; c < C; ++c) M = fmaxf(M, cluster.map_shared_rank(ms, c)->m[h]);
+      for (int c = 0; c < C; ++c) M = fmaxf(M, mg->rm[c][h]);
       float L = 0.f;
       for (int c = 0; c < C; ++c) {
-        const Misc* rm = cluster.map_shared_rank(ms, c);
-        const float f = rm->m[h] == -INFINITY ? 0.f : __expf(rm->m[h] - M);
+        const float f = mg->rm[c][h] == -INFINITY ? 0.f : __expf(mg->rm[c][h] - M);
         mg->f[c][h] = f;
-        L += f * rm->l[h];
+        L += f * mg->rl[c][h];
       }
       mg->inv[h] = L > 0.f ? 1.f / L : 0.f;
       if (crank == 0 && lse && h < H) lse[(size_t)ur * H + h] = L > 0.f ? M + logf(L) : -INFINITY;
@@ -322,15 +359,22 @@ k_mla_attn(int R, int H, int K, const uint16_t* __restrict__ q_lat, const uint16
       const int h = t / nq, q4 = t % nq;
       if (h >= H) continue;
       const int d = c0 + 4 * q4;
+      float4 v[MAX_CLUSTER];
+#pragma unroll
+      for (int c = 0; c < MAX_CLUSTER; ++c)
+        if (c < C && mg->f[c][h] != 0.f)
+          v[c] = __ldcg(reinterpret_cast<const float4*>(
+              ws_o + (((size_t)ur * MAX_CLUSTER + c) * 64 + h) * 512 + d));
       float4 acc = make_float4(0.f, 0.f, 0.f, 0.f);
-      for (int c = 0; c < C; ++c) {
-        const float f = mg->f[c][h];
-        if (f == 0.f) continue;
-        const float4 v = *reinterpret_cast<const float4*>(cluster.map_shared_rank(sO, c) + h * OSTR + d);
-        acc.x = fmaf(f, v.x, acc.x);
-        acc.y = fmaf(f, v.y, acc.y);
-        acc.z = fmaf(f, v.z, acc.z);
-        acc.w = fmaf(f, v.w, acc.w);
+#pragma unroll
+      for (int c = 0; c < MAX_CLUSTER; ++c) {
+        const float f = c < C ? mg->f[c][h] : 0.f;
+        if (f != 0.f) {   // skip empty sources (their staged O may be undefined)
+          acc.x = fmaf(f, v[c].x, acc.x);
+          acc.y = fmaf(f, v[c].y, acc.y);
+          acc.z = fmaf(f, v[c].z, acc.z);
+          acc.w = fmaf(f, v[c].w, acc.w);
+        }
       }
       const float inv = mg->inv[h];
       *reinterpret_cast<float4*>(out + ((size_t)ur * H + h) * 512 + d) =
@@ -346,19 +390,20 @@ k_mla_attn(int R, int H, int K, const uint16_t* __restrict__ q_lat, const uint16
 }  // namespace
 
 extern "C" size_t mla_decode_attn_workspace(int32_t U, int32_t R, int32_t H, int32_t K) {
-  (void)U; (void)R; (void)H; (void)K;
-  return 0;   // the cluster merge keeps every partial result on chip
+  (void)H; (void)K;
+  if (U < 1 || R < 1) return 0;
+  return (size_t)U * R * MAX_CLUSTER * 64 * 512 * 4;   // one 64 x 512 fp32 partial per CTA
 }
 
 extern "C" int mla_decode_attn(int32_t U, int32_t R, int32_t H, int32_t K, const uint16_t* q_lat,
                                const uint16_t* q_rope, const uint8_t* rows,
                                const int32_t* topk_idx, float scale, float* out, float* lse,
                                void* ws, size_t ws_bytes, int32_t* dev_err, void* stream) {
-  (void)ws; (void)ws_bytes;
   if (!q_lat || !q_rope || !rows || !topk_idx || !out) return DSA_ERR_ARG;
   if (U < 1 || U > 65535 || R < 1 || R > DSA_MAX_ROWS || !(scale > 0.0f)) return DSA_ERR_ARG;
   if (K < 1 || K > NC * MAX_CLUSTER || H < 16 || H > 64 || (H % 16) != 0) return DSA_ERR_SHAPE;
   if ((size_t)U * R > 65535) return DSA_ERR_ARG;
+  if (!ws || ws_bytes < mla_decode_attn_workspace(U, R, H, K)) return DSA_ERR_WS;
   static bool attr_done = false;
   if (!attr_done) {
     DSA_CUDA_TRY(cudaFuncSetAttribute(k_mla_attn, cudaFuncAttributeMaxDynamicSharedMemorySize, SMEM_BYTES));
@@ -379,7 +424,7 @@ extern "C" int mla_decode_attn(int32_t U, int32_t R, int32_t H, int32_t K, const
   cfg.attrs = attr;
   cfg.numAttrs = 1;
   if (cudaLaunchKernelEx(&cfg, k_mla_attn, (int)R, (int)H, (int)K, q_lat, q_rope, rows, topk_idx, scale,
-                         out, lse, dev_err) != cudaSuccess)
+                         out, lse, static_cast<float*>(ws), dev_err) != cudaSuccess)
     return DSA_ERR_CUDA;
   return dsa_launch_status();
 }

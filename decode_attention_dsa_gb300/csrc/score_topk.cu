@@ -10,32 +10,48 @@
 // kernel time they saved, so here the whole select is one clustered launch.
 //
 // Design (GB300):
-//  * k_dsa_score: one CTA per (tile of positions, unit). Keys stream from HBM
-//    with 16-byte read-only loads; the R query rows and head weights sit
-//    in shared memory as fp32; scores accumulate in fp32 FMA (exact for
-//    integer-grid data). Each score becomes an order-preserving uint32 key,
-//    written to the workspace, and a 4096-bin histogram of its top 12 bits is
-//    built in shared memory and merged into a global per-(unit,row) histogram.
+//  * k_dsa_score: a persistent grid (one CTA per SM) walks the flattened
+//    (unit, tile) space. Each 128-position tile of bf16 keys (16 KB,
+//    contiguous) arrives by a 1-D bulk TMA copy into one of two staging
+//    buffers while the previous tile is computed; it is widened once into an
+//    fp32 tile in shared memory (rows padded to 68 floats so the positions a
+//    warp reads together sit 4 banks apart). A lane owns one (query row,
+//    indexer head) and keeps that head's 64 query values in registers as
+//    packed pairs; the 8 head lanes of a position read the key row as
+//    shared-memory broadcasts and accumulate with packed fma.rn.f32x2 (exact
+//    fp32 arithmetic for integer-grid data), two positions per lane at a
+//    time, then apply ReLU and the head weight and reduce over heads with
+//    three shuffles. Each score
+//    becomes an order-preserving uint32 key (staged, then written coalesced)
+//    and feeds a 4096-bin shared histogram of its top 12 bits, merged into a
+//    global per-(unit, row) histogram when the CTA leaves a unit.
 //  * k_topk_select: one 8-CTA thread-block cluster per (unit, row). The global
-//    histogram gives the top digit of the K-th largest key; three refinement
-//    passes (8, 8 and 4 bits) over the cluster's key ranges, with histograms
-//    summed through distributed shared memory, give the exact threshold key T
-//    and how many keys equal to T are taken. A last pass writes the selected
-//    positions in ascending order (ballot-based ordered compaction); keys equal
-//    to T are taken lowest position first.
+//    histogram gives the bin b1 of the K-th largest key. One pass over the
+//    cluster's key ranges (cached in shared memory when they fit) counts keys
+//    above b1 and collects the candidates inside b1; the cluster shares the
+//    candidates through distributed shared memory and every CTA finds the
+//    exact threshold key T (and how many keys equal to T are taken) by a
+//    local radix select over them. If the candidates do not fit, three
+//    refinement passes with cluster-summed histograms find T instead. A last
+//    pass writes the selected positions in ascending order (ballot-based
+//    ordered compaction); keys equal to T are taken lowest position first.
+#include <algorithm>
 #include <cooperative_groups.h>
 
 #include "common.cuh"
+#include "tc.cuh"
 
 namespace cg = cooperative_groups;
 
 namespace {
 
 constexpr int SCORE_THREADS = 256;
-constexpr int SCORE_TILE = 512;          // positions per CTA
 constexpr int HIST1_BINS = 4096;         // top 12 bits of the ordered key
 constexpr int SEL_CLUSTER = 8;
 constexpr int SEL_THREADS = 512;
+constexpr int SEL_KEY_CACHE = 16384;     // keys of a CTA's range kept in shared memory
+constexpr int SEL_CAND_CAP = 4096;       // candidates per CTA (fast path)
+constexpr int SEL_ALL_CAP = 8192;        // candidates per cluster (fast path)
 
 struct TopkWs {
   uint32_t* hist;   // [U*R][4096]
@@ -60,72 +76,235 @@ __device__ __forceinline__ uint32_t ordered_key(float s) {
   return (b & 0x80000000u) ? ~b : (b | 0x80000000u);
 }
 
-__global__ void __launch_bounds__(SCORE_THREADS)
-k_dsa_score(const dsa_unit* __restrict__ units, int R, int K,
-            const uint16_t* __restrict__ q, const float* __restrict__ w,
-            uint32_t* __restrict__ hist, uint32_t* __restrict__ okeys, int64_t stride,
-            int64_t max_len) {
-  const int u = blockIdx.y;
-  const int64_t L = min(units[u].state[DSA_ST_LEN], max_len);
-  const int64_t p0 = (int64_t)blockIdx.x * SCORE_TILE;
-  if (p0 >= L || L <= K) return;   // L <= K: the select emits 0..L-1 directly
+constexpr int SCORE_TP = 128;           // positions per tile
+constexpr int KT_STRIDE = 68;           // fp32 key row stride: 4-bank offset per row
+inline int score_tile(int) { return SCORE_TP; }
 
-  extern __shared__ float sm[];
-  float* sq = sm;                                  // [R][8][64]
-  float* sw = sq + R * 512;                        // [R][8]
-  uint32_t* sh = reinterpret_cast<uint32_t*>(sw + R * 8);  // [R][4096]
+inline size_t score_smem(int R) {
+  return (size_t)2 * SCORE_TP * 128 + (size_t)SCORE_TP * KT_STRIDE * 4 + (size_t)R * SCORE_TP * 4 +
+         (size_t)R * HIST1_BINS * 4 + 64;
+}
 
-  const uint16_t* qu = q + (size_t)u * R * 512;
-  for (int i = threadIdx.x; i < R * 512; i += SCORE_THREADS) sq[i] = bf16f(qu[i]);
-  for (int i = threadIdx.x; i < R * 8; i += SCORE_THREADS) sw[i] = w[(size_t)u * R * 8 + i];
-  for (int i = threadIdx.x; i < R * HIST1_BINS; i += SCORE_THREADS) sh[i] = 0;
+__device__ __forceinline__ unsigned long long pack_f2(float lo, float hi) {
+  return ((unsigned long long)__float_as_uint(hi) << 32) | __float_as_uint(lo);
+}
+
+// d = a * b + d on two packed fp32 lanes (round to nearest, per lane)
+__device__ __forceinline__ void fma2(unsigned long long& d, unsigned long long a, unsigned long long b) {
+  asm("fma.rn.f32x2 %0, %1, %2, %0;" : "+l"(d) : "l"(a), "l"(b));
+}
+
+__device__ __forceinline__ float sum2(unsigned long long v) {
+  return __uint_as_float((uint32_t)v) + __uint_as_float((uint32_t)(v >> 32));
+}
+
+struct ScoreArgs {
+  const dsa_unit* units;
+  const uint16_t* q;
+  const float* w;
+  uint32_t* hist;
+  uint32_t* okeys;
+  int64_t stride;
+  int64_t max_len;
+  int64_t tpu;          // tiles per unit
+  int64_t total;        // U * tpu
+  int R, K, TP;
+};
+
+__global__ void __launch_bounds__(SCORE_THREADS, 2) k_dsa_score(ScoreArgs a) {
+  extern __shared__ __align__(128) uint8_t sm[];
+  const int TP = a.TP, R = a.R;
+  uint8_t* stg0 = sm;
+  float* kt = reinterpret_cast<float*>(sm + 2 * TP * 128);            // [TP][KT_STRIDE]
+  uint32_t* sc = reinterpret_cast<uint32_t*>(kt + TP * KT_STRIDE);    // [R][TP]
+  uint32_t* hs = sc + R * TP;                                          // [R][4096]
+  uint64_t* bar = reinterpret_cast<uint64_t*>(hs + R * HIST1_BINS);   // [2]
+  const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
+
+  const int64_t per = (a.total + gridDim.x - 1) / gridDim.x;
+  const int64_t f0 = (int64_t)blockIdx.x * per;
+  const int64_t f1 = min(f0 + per, a.total);
+
+  // history length and key pointer of the units this CTA's tiles touch
+  constexpr int UCACHE = 8;
+  __shared__ int64_t s_len[UCACHE];
+  __shared__ const uint16_t* s_keys[UCACHE];
+  const int u_first = (int)(f0 / a.tpu);
+  if (tid < UCACHE) {
+    const int u = u_first + tid;
+    if ((int64_t)u * a.tpu < f1) {
+      s_len[tid] = min(a.units[u].state[DSA_ST_LEN], a.max_len);
+      s_keys[tid] = a.units[u].keys;
+    }
+  }
+  __syncthreads();
+  auto unit_len = [&](int u) -> int64_t {
+    return u - u_first < UCACHE ? s_len[u - u_first] : min(a.units[u].state[DSA_ST_LEN], a.max_len);
+  };
+  auto unit_keys = [&](int u) -> const uint16_t* {
+    return u - u_first < UCACHE ? s_keys[u - u_first] : a.units[u].keys;
+  };
+
+  // first valid tile at or after f (a tile is valid if it starts inside a
+  // history longer than K); f1 if none
+  auto next_valid = [&](int64_t f) -> int64_t {
+    while (f < f1) {
+      const int u = (int)(f / a.tpu);
+      const int64_t t = f % a.tpu;
+      const int64_t L = unit_len(u);
+      if (L > a.K && t * TP < L) return f;
+      f = (int64_t)(u + 1) * a.tpu;
+    }
+    return f1;
+  };
+  auto issue = [&](int64_t f, int stage) {
+    const int u = (int)(f / a.tpu);
+    const int64_t t = f % a.tpu;
+    const int64_t L = unit_len(u);
+    const uint32_t n = (uint32_t)min((int64_t)TP, L - t * TP);
+    tc::mbar_arrive_expect_tx(&bar[stage], n * 128);
+    tc::bulk_g2s(stg0 + stage * TP * 128, unit_keys(u) + t * TP * 64, n * 128, &bar[stage]);
+  };
+
+  if (tid == 0) {
+    tc::mbar_init(&bar[0], 1);
+    tc::mbar_init(&bar[1], 1);
+    tc::fence_mbar_init();
+  }
+  for (int i = tid; i < R * HIST1_BINS; i += SCORE_THREADS) hs[i] = 0;
   __syncthreads();
 
-  const uint4* kp = reinterpret_cast<const uint4*>(units[u].keys);
-  const int64_t pend = min(p0 + (int64_t)SCORE_TILE, L);
-  uint32_t* ok = okeys + (size_t)u * R * stride;
-  for (int64_t p = p0 + threadIdx.x; p < pend; p += SCORE_THREADS) {
-    uint4 v[8];
-#pragma unroll
-    for (int c = 0; c < 8; ++c) v[c] = ldg_v4(kp + p * 8 + c);
-    float k[64];
-#pragma unroll
-    for (int c = 0; c < 8; ++c) {
-      const uint32_t ww[4] = {v[c].x, v[c].y, v[c].z, v[c].w};
-#pragma unroll
-      for (int e = 0; e < 4; ++e) {
-        k[c * 8 + 2 * e] = bf16_lo(ww[e]);
-        k[c * 8 + 2 * e + 1] = bf16_hi(ww[e]);
+  int64_t nxt[2];
+  nxt[0] = next_valid(f0);
+  nxt[1] = nxt[0] < f1 ? next_valid(nxt[0] + 1) : f1;
+  if (tid == 0) {
+    if (nxt[0] < f1) issue(nxt[0], 0);
+    if (nxt[1] < f1) issue(nxt[1], 1);
+  }
+  uint32_t parity[2] = {0u, 0u};
+  int stage = 0;
+  int cur_u = -1;
+
+  // lane roles: rows are processed in groups of up to 4
+  const int h = lane & 7;
+  unsigned long long q2[32];      // this lane's head row of the query, packed pairs
+  float wv = 0.f;
+  int RP = 1, pp = 0, rr = 0, Rg = 0, loaded_rg = -1;
+
+  auto flush_hist = [&](int u) {
+    uint32_t* gh = a.hist + (size_t)u * R * HIST1_BINS;
+    for (int i = tid; i < R * HIST1_BINS; i += SCORE_THREADS) {
+      const uint32_t c = hs[i];
+      if (c) {
+        atomicAdd(&gh[i], c);
+        hs[i] = 0;
       }
     }
-    for (int r = 0; r < R; ++r) {
-      float acc = 0.0f;
+  };
+  auto load_q = [&](int u, int rg) {
+    Rg = min(4, R - 4 * rg);
+    RP = Rg == 1 ? 1 : (Rg == 2 ? 2 : 4);
+    pp = lane / (8 * RP);
+    rr = (lane >> 3) % RP;
+    const int row = 4 * rg + rr;
+    if (rr < Rg) {
+      const uint16_t* qh = a.q + (((size_t)u * R + row) * 8 + h) * 64;
 #pragma unroll
-      for (int h = 0; h < 8; ++h) {
-        const float4* qh = reinterpret_cast<const float4*>(sq + (r * 8 + h) * 64);
-        float d0 = 0.f, d1 = 0.f, d2 = 0.f, d3 = 0.f;
+      for (int c = 0; c < 16; ++c) {
+        const uint2 b = *reinterpret_cast<const uint2*>(qh + 4 * c);
+        q2[2 * c] = pack_f2(bf16_lo(b.x), bf16_hi(b.x));
+        q2[2 * c + 1] = pack_f2(bf16_lo(b.y), bf16_hi(b.y));
+      }
+      wv = a.w[((size_t)u * R + row) * 8 + h];
+    } else {
 #pragma unroll
-        for (int i = 0; i < 16; ++i) {
-          const float4 qq = qh[i];
-          d0 = fmaf(qq.x, k[4 * i + 0], d0);
-          d1 = fmaf(qq.y, k[4 * i + 1], d1);
-          d2 = fmaf(qq.z, k[4 * i + 2], d2);
-          d3 = fmaf(qq.w, k[4 * i + 3], d3);
+      for (int c = 0; c < 32; ++c) q2[c] = 0ull;
+      wv = 0.f;
+    }
+    loaded_rg = rg;
+  };
+
+  while (nxt[stage] < f1) {
+    const int64_t f = nxt[stage];
+    const int u = (int)(f / a.tpu);
+    const int64_t t = f % a.tpu;
+    const int64_t L = unit_len(u);
+    const int n = (int)min((int64_t)TP, L - t * TP);
+    if (u != cur_u) {
+      if (cur_u >= 0) flush_hist(cur_u);
+      cur_u = u;
+      loaded_rg = -1;
+    }
+    if (!tc::mbar_wait(&bar[stage], parity[stage])) break;   // bounded; cannot happen normally
+    parity[stage] ^= 1u;
+    // widen the staged bf16 keys to fp32
+    const uint8_t* stg = stg0 + stage * TP * 128;
+    for (int i = tid; i < n * 8; i += SCORE_THREADS) {
+      const uint4 v = *reinterpret_cast<const uint4*>(stg + 16 * i);
+      float4* d = reinterpret_cast<float4*>(kt + (i >> 3) * KT_STRIDE + 8 * (i & 7));
+      d[0] = make_float4(bf16_lo(v.x), bf16_hi(v.x), bf16_lo(v.y), bf16_hi(v.y));
+      d[1] = make_float4(bf16_lo(v.z), bf16_hi(v.z), bf16_lo(v.w), bf16_hi(v.w));
+    }
+    __syncthreads();
+    // the staging buffer is free: prefetch the tile after the other stage's
+    {
+      const int64_t other = nxt[stage ^ 1];
+      const int64_t fn = other < f1 ? next_valid(other + 1) : f1;
+      nxt[stage] = fn;
+      if (tid == 0 && fn < f1) issue(fn, stage);
+    }
+    const int ngroups = (R + 3) / 4;
+    for (int rg = 0; rg < ngroups; ++rg) {
+      if (loaded_rg != rg) load_q(u, rg);
+      // lanes: pp (position in a group of P), rr (row), h (head); each lane
+      // takes two positions, p0 + pp and p0 + pp + P, per iteration
+      const int P = 4 / RP;
+      const int per_warp = TP / (SCORE_THREADS / 32);
+      for (int p0 = warp * per_warp; p0 < warp * per_warp + per_warp; p0 += 2 * P) {
+        const int pa = p0 + pp, pb = pa + P;
+        const ulonglong2* ka = reinterpret_cast<const ulonglong2*>(kt + pa * KT_STRIDE);
+        const ulonglong2* kb = reinterpret_cast<const ulonglong2*>(kt + pb * KT_STRIDE);
+        unsigned long long a0 = 0ull, a1 = 0ull, b0 = 0ull, b1 = 0ull;
+#pragma unroll
+        for (int c = 0; c < 16; ++c) {
+          const ulonglong2 x = ka[c];
+          const ulonglong2 y = kb[c];
+          fma2(a0, q2[2 * c], x.x);
+          fma2(a1, q2[2 * c + 1], x.y);
+          fma2(b0, q2[2 * c], y.x);
+          fma2(b1, q2[2 * c + 1], y.y);
         }
-        const float dot = (d0 + d1) + (d2 + d3);
-        acc = fmaf(sw[r * 8 + h], fmaxf(dot, 0.0f), acc);
+        float va = wv * fmaxf(sum2(a0) + sum2(a1), 0.f);
+        float vb = wv * fmaxf(sum2(b0) + sum2(b1), 0.f);
+#pragma unroll
+        for (int o = 1; o < 8; o <<= 1) {
+          va += __shfl_xor_sync(0xffffffffu, va, o);
+          vb += __shfl_xor_sync(0xffffffffu, vb, o);
+        }
+        if (h == 0 && rr < Rg) {
+          const int row = 4 * rg + rr;
+          if (pa < n) {
+            const uint32_t key = ordered_key(va);
+            sc[row * TP + pa] = key;
+            atomicAdd(&hs[row * HIST1_BINS + (key >> 20)], 1u);
+          }
+          if (pb < n) {
+            const uint32_t key = ordered_key(vb);
+            sc[row * TP + pb] = key;
+            atomicAdd(&hs[row * HIST1_BINS + (key >> 20)], 1u);
+          }
+        }
       }
-      const uint32_t key = ordered_key(acc);
-      ok[(size_t)r * stride + p] = key;
-      atomicAdd(&sh[r * HIST1_BINS + (key >> 20)], 1u);
     }
+    __syncthreads();
+    for (int i = tid; i < R * TP; i += SCORE_THREADS) {
+      const int row = i / TP, pl = i % TP;
+      if (pl < n) a.okeys[((size_t)u * R + row) * a.stride + t * TP + pl] = sc[i];
+    }
+    stage ^= 1;
   }
   __syncthreads();
-  uint32_t* gh = hist + (size_t)u * R * HIST1_BINS;
-  for (int i = threadIdx.x; i < R * HIST1_BINS; i += SCORE_THREADS) {
-    const uint32_t c = sh[i];
-    if (c) atomicAdd(&gh[i], c);
-  }
+  if (cur_u >= 0) flush_hist(cur_u);
 }
 
 // Among `nb` histogram bins (held by threads 0..nb-1, thread t <-> bin
@@ -145,7 +324,47 @@ __device__ __forceinline__ void find_digit(const uint32_t* h, int nb, int need, 
   __syncthreads();
 }
 
-__global__ void __cluster_dims__(SEL_CLUSTER, 1, 1) __launch_bounds__(SEL_THREADS)
+// Like find_digit, for up to 8 * NT bins: thread t sums the bins
+// [nb - per*(t+1), nb - per*t) and scans them highest first.
+template <int NT>
+__device__ __forceinline__ void find_digit_wide(const uint32_t* h, int nb, int need, int* tmp,
+                                                int* s_bin, int* s_above) {
+  const int per = (nb + NT - 1) / NT;
+  const int t = threadIdx.x;
+  const int hi = nb - 1 - per * t;
+  int c = 0;
+  for (int i = 0; i < per; ++i)
+    if (hi - i >= 0) c += (int)h[hi - i];
+  const int inc = block_inclusive_scan<NT>(c, tmp);
+  int exc = inc - c;
+  if (c > 0 && exc < need && need <= inc) {
+    for (int i = 0; i < per; ++i) {
+      const int cb = hi - i >= 0 ? (int)h[hi - i] : 0;
+      if (exc + cb >= need) {
+        *s_bin = hi - i;
+        *s_above = exc;
+        break;
+      }
+      exc += cb;
+    }
+  }
+  __syncthreads();
+}
+
+struct SelShared {
+  uint32_t h1[HIST1_BINS];
+  uint32_t hl[2][256];
+  uint32_t hg[256];
+  int tmp[32];
+  int wsum[SEL_THREADS / 32];
+  int bin, above;
+  int ncand, overflow;
+  int any_over;               // some CTA of the cluster overflowed
+  int coff[SEL_CLUSTER + 1];  // candidate offsets of the cluster's CTAs
+  long long cnt[2];           // this CTA's (gt, eq) counts
+};
+
+__global__ void __cluster_dims__(SEL_CLUSTER, 1, 1) __launch_bounds__(SEL_THREADS, 1)
 k_topk_select(const dsa_unit* __restrict__ units, int R, int K, uint32_t* __restrict__ hist,
               const uint32_t* __restrict__ okeys, int64_t stride, int32_t* __restrict__ topk_idx,
               int64_t max_len, int32_t* dev_err) {
@@ -164,157 +383,228 @@ k_topk_select(const dsa_unit* __restrict__ units, int R, int K, uint32_t* __rest
     return;
   }
 
-  __shared__ uint32_t s_h1[HIST1_BINS];
-  __shared__ uint32_t s_hl[2][256];   // local refinement histograms (double buffer)
-  __shared__ uint32_t s_hg[256];      // cluster-summed refinement histogram
-  __shared__ int s_tmp[32];
-  __shared__ int s_bin, s_above;
-  __shared__ long long s_cnt[2];      // this CTA's (gt, eq) counts
-  __shared__ int s_wsum[SEL_THREADS / 32];
-  if (threadIdx.x == 0) {
-    s_bin = 0;
-    s_above = 0;
+  extern __shared__ __align__(16) uint8_t smem_sel[];
+  SelShared* S = reinterpret_cast<SelShared*>(smem_sel);
+  uint32_t* kc = reinterpret_cast<uint32_t*>(smem_sel + sizeof(SelShared));   // [SEL_KEY_CACHE]
+  uint32_t* cand = kc + SEL_KEY_CACHE;                                        // [SEL_CAND_CAP]
+  uint32_t* allc = cand + SEL_CAND_CAP;                                       // [SEL_ALL_CAP]
+  const int tid = threadIdx.x;
+  if (tid == 0) {
+    S->bin = 0;
+    S->above = 0;
+    S->ncand = 0;
+    S->overflow = 0;
   }
 
   // ---- level 1: top 12 bits from the global histogram
   uint32_t* gh = hist + (size_t)ur * HIST1_BINS;
-  for (int i = threadIdx.x; i < HIST1_BINS; i += SEL_THREADS) s_h1[i] = gh[i];
+  for (int i = tid; i < HIST1_BINS / 4; i += SEL_THREADS)
+    reinterpret_cast<uint4*>(S->h1)[i] = reinterpret_cast<const uint4*>(gh)[i];
   __syncthreads();
-  // 4096 bins over 512 threads: each thread sums 8 bins, highest first.
-  {
-    const int t = threadIdx.x;
-    int c = 0;
-    const int hi = HIST1_BINS - 1 - 8 * t;
-#pragma unroll
-    for (int i = 0; i < 8; ++i) c += (int)s_h1[hi - i];
-    const int inc = block_inclusive_scan<SEL_THREADS>(c, s_tmp);
-    int exc = inc - c;
-    if (exc < K && K <= inc) {
-      for (int i = 0; i < 8; ++i) {
-        const int cb = (int)s_h1[hi - i];
-        if (exc + cb >= K) {
-          s_bin = hi - i;
-          s_above = exc;
-          break;
-        }
-        exc += cb;
-      }
-    }
-    __syncthreads();
-  }
-  const uint32_t b1 = (uint32_t)s_bin;
-  int need = K - s_above;
+  find_digit_wide<SEL_THREADS>(S->h1, HIST1_BINS, K, S->tmp, &S->bin, &S->above);
+  const uint32_t b1 = (uint32_t)S->bin;
+  int need = K - S->above;
 
   const int64_t chunk = (L + SEL_CLUSTER - 1) / SEL_CLUSTER;
   const int64_t beg = min((int64_t)crank * chunk, L);
   const int64_t end = min(beg + chunk, L);
   const uint32_t* kk = okeys + (size_t)ur * stride;
+  const bool cached = (end - beg) <= SEL_KEY_CACHE;
+  auto key_at = [&](int64_t p) -> uint32_t { return cached ? kc[p - beg] : kk[p]; };
 
-  long long local_gt = 0;
-  uint32_t prefix = b1 << 20, mask = 0xFFF00000u;
-  const int shifts[3] = {12, 4, 0};
-  const int nbins[3] = {256, 256, 16};
-  for (int lvl = 0; lvl < 3; ++lvl) {
-    uint32_t* hl = s_hl[lvl & 1];
-    for (int i = threadIdx.x; i < 256; i += SEL_THREADS) hl[i] = 0;
+  // ---- one pass: cache keys, count keys above b1, collect candidates in b1
+  if (cached) {
+    const int64_t n = end - beg;
+#pragma unroll 4
+    for (int64_t i = tid; i < n; i += SEL_THREADS) kc[i] = kk[beg + i];
     __syncthreads();
-    const int sh = shifts[lvl];
-    const uint32_t dm = (uint32_t)nbins[lvl] - 1;
-    long long gt_top = 0;   // level 1 only: keys whose top digit is above b1
-    for (int64_t p = beg + threadIdx.x; p < end; p += SEL_THREADS) {
-      const uint32_t key = kk[p];
-      if ((key & mask) == prefix) atomicAdd(&hl[(key >> sh) & dm], 1u);
-      else if (lvl == 0 && (key >> 20) > b1) ++gt_top;
-    }
-    if (lvl == 0) {
-      int tot;
-      block_inclusive_scan<SEL_THREADS>((int)gt_top, s_tmp, &tot);
-      local_gt += tot;
-    }
-    __syncthreads();
-    cluster.sync();
-    // sum the cluster's histograms of this level
-    for (int i = threadIdx.x; i < nbins[lvl]; i += SEL_THREADS) {
-      uint32_t s = 0;
-      for (int c = 0; c < SEL_CLUSTER; ++c) s += cluster.map_shared_rank(hl, c)[i];
-      s_hg[i] = s;
-    }
-    if (lvl == 0 && crank == 0) {
-      // every CTA of the cluster read the global histogram before the
-      // cluster barrier above: clear it for the next call
-      for (int i = threadIdx.x; i < HIST1_BINS; i += SEL_THREADS) gh[i] = 0;
-    }
-    __syncthreads();
-    find_digit<SEL_THREADS>(s_hg, nbins[lvl], need, s_tmp, &s_bin, &s_above);
-    const uint32_t b = (uint32_t)s_bin;
-    need -= s_above;
-    // this CTA's keys above the digit at this level
-    {
-      const int t = threadIdx.x;
-      int c = (t < nbins[lvl] && (uint32_t)t > b) ? (int)hl[t] : 0;
-      int tot;
-      block_inclusive_scan<SEL_THREADS>(c, s_tmp, &tot);
-      local_gt += tot;
-      if (lvl == 2 && t == 0) s_cnt[1] = hl[b];
-    }
-    prefix |= b << sh;
-    mask |= dm << sh;
   }
-  const uint32_t T = prefix;
-  const int ties = need;            // keys equal to T that are taken
-  if (threadIdx.x == 0) s_cnt[0] = local_gt;
+  long long gt1 = 0;
+  for (int64_t p = beg + tid; p < end; p += SEL_THREADS) {
+    const uint32_t key = key_at(p);
+    const uint32_t d1 = key >> 20;
+    if (d1 > b1) {
+      ++gt1;
+    } else if (d1 == b1) {
+      const int i = atomicAdd(&S->ncand, 1);
+      if (i < SEL_CAND_CAP) cand[i] = key;
+    }
+  }
+  int gt1_cta;
+  block_inclusive_scan<SEL_THREADS>((int)gt1, S->tmp, &gt1_cta);
+  if (tid == 0) S->overflow = S->ncand > SEL_CAND_CAP;
+  __syncthreads();
+  cluster.sync();
+  if (crank == 0) {
+    // every CTA read the global histogram before the barrier: clear it for the next call
+    for (int i = tid; i < HIST1_BINS; i += SEL_THREADS) gh[i] = 0;
+  }
+  if (tid < SEL_CLUSTER) {
+    const SelShared* rs = cluster.map_shared_rank(S, tid);
+    S->coff[tid + 1] = rs->overflow ? -1 : min(rs->ncand, SEL_CAND_CAP);
+  }
+  __syncthreads();
+  int total = 0, any_over = 0;
+  if (tid == 0) {
+    S->coff[0] = 0;
+    for (int c = 0; c < SEL_CLUSTER; ++c) {
+      const int nc = S->coff[c + 1];
+      any_over |= nc < 0;
+      S->coff[c + 1] = S->coff[c] + max(nc, 0);
+    }
+    S->any_over = any_over;
+  }
+  __syncthreads();
+  any_over = S->any_over;
+  total = S->coff[SEL_CLUSTER];
+  const bool fast = !any_over && total <= SEL_ALL_CAP;
+
+  uint32_t T;
+  int ties;
+  long long gt_cta, eq_cta;
+  if (fast) {
+    // ---- all candidates to every CTA (one round of remote loads), then an
+    //      exact local radix select on bits 19..8 and 7..0
+    for (int i = tid; i < total; i += SEL_THREADS) {
+      int c = 0;
+      while (c + 1 < SEL_CLUSTER && i >= S->coff[c + 1]) ++c;
+      allc[i] = cluster.map_shared_rank(cand, c)[i - S->coff[c]];
+    }
+    for (int i = tid; i < HIST1_BINS; i += SEL_THREADS) S->h1[i] = 0;
+    __syncthreads();
+    const uint32_t p1 = b1 << 20;
+    for (int i = tid; i < total; i += SEL_THREADS) {
+      const uint32_t key = allc[i];
+      if ((key & 0xFFF00000u) == p1) atomicAdd(&S->h1[(key >> 8) & 0xFFF], 1u);
+    }
+    __syncthreads();
+    find_digit_wide<SEL_THREADS>(S->h1, HIST1_BINS, need, S->tmp, &S->bin, &S->above);
+    need -= S->above;
+    const uint32_t p2 = p1 | ((uint32_t)S->bin << 8);
+    for (int i = tid; i < 256; i += SEL_THREADS) S->hg[i] = 0;
+    __syncthreads();
+    for (int i = tid; i < total; i += SEL_THREADS) {
+      const uint32_t key = allc[i];
+      if ((key & 0xFFFFFF00u) == p2) atomicAdd(&S->hg[key & 0xFF], 1u);
+    }
+    __syncthreads();
+    find_digit<SEL_THREADS>(S->hg, 256, need, S->tmp, &S->bin, &S->above);
+    need -= S->above;
+    T = p2 | (uint32_t)S->bin;
+    ties = need;
+    // this CTA's counts from its own candidates
+    const int nc = min(S->ncand, SEL_CAND_CAP);
+    int g = 0, e = 0;
+    for (int i = tid; i < nc; i += SEL_THREADS) {
+      g += cand[i] > T;
+      e += cand[i] == T;
+    }
+    int gtot, etot;
+    block_inclusive_scan<SEL_THREADS>(g, S->tmp, &gtot);
+    block_inclusive_scan<SEL_THREADS>(e, S->tmp, &etot);
+    gt_cta = (long long)gt1_cta + gtot;
+    eq_cta = etot;
+  } else {
+    // ---- refinement passes with cluster-summed histograms (8, 8, 4 bits)
+    long long local_gt = gt1_cta;
+    long long local_eq = 0;
+    uint32_t prefix = b1 << 20, mask = 0xFFF00000u;
+    const int shifts[3] = {12, 4, 0};
+    const int nbins[3] = {256, 256, 16};
+    for (int lvl = 0; lvl < 3; ++lvl) {
+      uint32_t* hl = S->hl[lvl & 1];
+      for (int i = tid; i < 256; i += SEL_THREADS) hl[i] = 0;
+      __syncthreads();
+      const int sh = shifts[lvl];
+      const uint32_t dm = (uint32_t)nbins[lvl] - 1;
+      for (int64_t p = beg + tid; p < end; p += SEL_THREADS) {
+        const uint32_t key = key_at(p);
+        if ((key & mask) == prefix) atomicAdd(&hl[(key >> sh) & dm], 1u);
+      }
+      __syncthreads();
+      cluster.sync();
+      for (int i = tid; i < nbins[lvl]; i += SEL_THREADS) {
+        uint32_t s = 0;
+        for (int c = 0; c < SEL_CLUSTER; ++c) s += cluster.map_shared_rank(hl, c)[i];
+        S->hg[i] = s;
+      }
+      __syncthreads();
+      find_digit<SEL_THREADS>(S->hg, nbins[lvl], need, S->tmp, &S->bin, &S->above);
+      const uint32_t b = (uint32_t)S->bin;
+      need -= S->above;
+      {
+        const int c = (tid < nbins[lvl] && (uint32_t)tid > b) ? (int)hl[tid] : 0;
+        int tot;
+        block_inclusive_scan<SEL_THREADS>(c, S->tmp, &tot);
+        local_gt += tot;
+        if (lvl == 2) local_eq = hl[b];
+      }
+      prefix |= b << sh;
+      mask |= dm << sh;
+    }
+    T = prefix;
+    ties = need;
+    gt_cta = local_gt;
+    eq_cta = local_eq;
+  }
+  if (tid == 0) {
+    S->cnt[0] = gt_cta;
+    S->cnt[1] = eq_cta;
+  }
   __syncthreads();
   cluster.sync();
   long long eq_before = 0, sel_before = 0;
-  {
-    for (int c = 0; c < crank; ++c) {
-      const long long* rc = cluster.map_shared_rank(s_cnt, c);
-      const long long g = rc[0], e = rc[1];
-      long long take = (long long)ties - eq_before;
-      take = take < 0 ? 0 : (take > e ? e : take);
-      sel_before += g + take;
-      eq_before += e;
-    }
+  for (int c = 0; c < crank; ++c) {
+    const SelShared* rs = cluster.map_shared_rank(S, c);
+    const long long g = rs->cnt[0], e = rs->cnt[1];
+    long long take = (long long)ties - eq_before;
+    take = take < 0 ? 0 : (take > e ? e : take);
+    sel_before += g + take;
+    eq_before += e;
   }
-  // ordered compaction of this CTA's range
-  const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
-  long long run_eq = eq_before, run_sel = sel_before;
-  for (int64_t base = beg; base < end; base += SEL_THREADS) {
-    const int64_t p = base + threadIdx.x;
-    const uint32_t key = p < end ? kk[p] : 0u;
-    const bool gt = p < end && key > T;
-    const bool eq = p < end && key == T;
-    const unsigned beq = __ballot_sync(0xffffffffu, eq);
-    if (lane == 0) s_wsum[warp] = __popc(beq);
-    __syncthreads();
-    int weq = 0, teq = 0;
-    for (int i = 0; i < SEL_THREADS / 32; ++i) {
-      const int v = s_wsum[i];
-      if (i < warp) weq += v;
-      teq += v;
+  // ---- ordered compaction of this CTA's range: every thread owns a
+  //      contiguous run of positions; two block scans give each run its tie
+  //      rank and output offset
+  {
+    const int64_t n = end - beg;
+    const int64_t run = (n + SEL_THREADS - 1) / SEL_THREADS;
+    const int64_t r0 = beg + min((int64_t)tid * run, n);
+    const int64_t r1 = beg + min((int64_t)(tid + 1) * run, n);
+    int g = 0, e = 0;
+    for (int64_t p = r0; p < r1; ++p) {
+      const uint32_t key = key_at(p);
+      g += key > T;
+      e += key == T;
     }
-    const long long eq_rank = run_eq + weq + __popc(beq & ((1u << lane) - 1u));
-    const bool sel = gt || (eq && eq_rank < ties);
-    __syncthreads();
-    const unsigned bs = __ballot_sync(0xffffffffu, sel);
-    if (lane == 0) s_wsum[warp] = __popc(bs);
-    __syncthreads();
-    int wsel = 0, tsel = 0;
-    for (int i = 0; i < SEL_THREADS / 32; ++i) {
-      const int v = s_wsum[i];
-      if (i < warp) wsel += v;
-      tsel += v;
+    const int einc = block_inclusive_scan<SEL_THREADS>(e, S->tmp);
+    const long long estart = eq_before + einc - e;
+    long long take = (long long)ties - estart;
+    take = take < 0 ? 0 : (take > e ? e : take);
+    const int sel = g + (int)take;
+    const int sinc = block_inclusive_scan<SEL_THREADS>(sel, S->tmp);
+    long long o = sel_before + sinc - sel;
+    long long er = estart;
+    for (int64_t p = r0; p < r1; ++p) {
+      const uint32_t key = key_at(p);
+      bool pick = key > T;
+      if (key == T) {
+        pick = er < ties;
+        ++er;
+      }
+      if (pick) {
+        if (o < K) out[o] = (int32_t)p;
+        ++o;
+      }
     }
-    if (sel) {
-      const long long o = run_sel + wsel + __popc(bs & ((1u << lane) - 1u));
-      if (o < K) out[o] = (int32_t)p;
-    }
-    run_eq += teq;
-    run_sel += tsel;
-    __syncthreads();
   }
   cluster.sync();   // keep this CTA's shared memory alive for its peers
 }
+
+inline size_t select_smem() {
+  return sizeof(SelShared) + (size_t)(SEL_KEY_CACHE + SEL_CAND_CAP + SEL_ALL_CAP) * 4;
+}
+
+int g_num_sms = 0;
 
 }  // namespace
 
@@ -330,27 +620,46 @@ extern "C" int dsa_score_topk(const dsa_unit* units, int32_t U, int32_t R, int32
                               void* stream) {
   if (!units || !q || !w || !topk_idx) return DSA_ERR_ARG;
   if (U < 1 || U > 65535 || R < 1 || R > DSA_MAX_ROWS || max_len < 0) return DSA_ERR_ARG;
+  if ((int64_t)U * R > 65535) return DSA_ERR_ARG;
   if (K < 1 || K > DSA_MAX_K) return DSA_ERR_SHAPE;
   if (!ws || ws_bytes < dsa_score_topk_workspace(U, R, max_len)) return DSA_ERR_WS;
   cudaStream_t st = static_cast<cudaStream_t>(stream);
   TopkWs tw = topk_ws(ws, U, R, max_len);
-  const int64_t tiles = (max_len + SCORE_TILE - 1) / SCORE_TILE;
-  if (tiles > 0) {
-    const size_t smem = (size_t)R * (512 + 8) * 4 + (size_t)R * HIST1_BINS * 4;
-    static bool attr_done = false;
-    if (!attr_done) {
-      DSA_CUDA_TRY(cudaFuncSetAttribute(k_dsa_score, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                                        (int)((size_t)DSA_MAX_ROWS * (520 + HIST1_BINS) * 4)));
-      attr_done = true;
-    }
-    if (tiles > 0x7fffffff) return DSA_ERR_ARG;
-    k_dsa_score<<<dim3((unsigned)tiles, U), SCORE_THREADS, smem, st>>>(units, R, K, q, w, tw.hist,
-                                                                     tw.keys, tw.stride, max_len);
+  static bool attr_done = false;
+  if (!attr_done) {
+    size_t mx = 0;
+    for (int r = 1; r <= DSA_MAX_ROWS; ++r) mx = std::max(mx, score_smem(r));
+    DSA_CUDA_TRY(cudaFuncSetAttribute(k_dsa_score, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)mx));
+    DSA_CUDA_TRY(cudaFuncSetAttribute(k_topk_select, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                      (int)select_smem()));
+    int dev = 0;
+    DSA_CUDA_TRY(cudaGetDevice(&dev));
+    DSA_CUDA_TRY(cudaDeviceGetAttribute(&g_num_sms, cudaDevAttrMultiProcessorCount, dev));
+    attr_done = true;
+  }
+  const int TP = score_tile(R);
+  const int64_t tpu = (max_len + TP - 1) / TP;
+  if (tpu > 0) {
+    ScoreArgs a;
+    a.units = units;
+    a.q = q;
+    a.w = w;
+    a.hist = tw.hist;
+    a.okeys = tw.keys;
+    a.stride = tw.stride;
+    a.max_len = max_len;
+    a.tpu = tpu;
+    a.total = tpu * U;
+    a.R = R;
+    a.K = K;
+    a.TP = TP;
+    const int per_sm = score_smem(R) <= 113 * 1024 ? 2 : 1;
+    const int64_t grid = std::min<int64_t>(a.total, (int64_t)per_sm * (g_num_sms > 0 ? g_num_sms : 148));
+    k_dsa_score<<<(unsigned)grid, SCORE_THREADS, score_smem(R), st>>>(a);
     if (dsa_launch_status() != DSA_OK) return DSA_ERR_CUDA;
   }
-  k_topk_select<<<dim3(SEL_CLUSTER, U * R), SEL_THREADS, 0, st>>>(units, R, K, tw.hist, tw.keys,
-                                                                  tw.stride, topk_idx, max_len,
-                                                                  dev_err);
+  k_topk_select<<<dim3(SEL_CLUSTER, U * R), SEL_THREADS, select_smem(), st>>>(
+      units, R, K, tw.hist, tw.keys, tw.stride, topk_idx, max_len, dev_err);
   return dsa_launch_status();
 }
 

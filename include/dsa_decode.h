@@ -280,8 +280,9 @@ int hot_gather(const dsa_unit* units, int32_t U, int32_t R, int32_t K,
  *   rows    device u8 [U][R][K][656] (hot_gather's output).
  *   topk_idx device int32 [U][R][K] (only the sign is used: -1 = padding).
  *   out     device float [U][R][H][512];  lse device float [U][R][H] or NULL.
- *   ws      device workspace of mla_decode_attn_workspace() bytes (0: the
- *           chunk results are merged on chip; pass NULL).
+ *   ws      device workspace of mla_decode_attn_workspace(U, R, H, K) bytes:
+ *           one 64 x 512 fp32 partial output per CTA, written and read back
+ *           within the launch (it stays in L2).
  * Shapes: H in {16, 32, 48, 64}, 1 <= K <= DSA_MAX_ATTN_K, U * R <= 65535.
  * One thread-block cluster of ceil(K / 128) CTAs per (unit, query row).
  */

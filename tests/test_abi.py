@@ -52,7 +52,7 @@ def test_workspace_sizes(lib):
     b = lib.dsa_score_topk_workspace(4, 1, 100000)
     assert 0 < a < b and a % 256 == 0
     assert lib.hot_gather_workspace(1, 4, 2048) > lib.hot_gather_workspace(1, 1, 2048) > 0
-    assert lib.mla_decode_attn_workspace(1, 1, 64, 2048) == 0
+    assert lib.mla_decode_attn_workspace(1, 1, 64, 2048) > 0
 
 
 def _raw(lib, fn, *args):
@@ -72,6 +72,7 @@ def test_host_side_validation(lib):
     assert L.mla_decode_attn(1, 1, 24, 8, fake, fake, fake, fake, 0.04, fake, None, fake, 1 << 30, None, None) == lib.DSA_ERR_SHAPE
     assert L.mla_decode_attn(1, 1, 64, 8, fake, fake, fake, fake, -1.0, fake, None, fake, 1 << 30, None, None) == lib.DSA_ERR_ARG
     assert L.mla_decode_attn(1, 1, 64, 4096, fake, fake, fake, fake, 0.04, fake, None, None, 0, None, None) == lib.DSA_ERR_SHAPE
+    assert L.mla_decode_attn(1, 1, 64, 64, fake, fake, fake, fake, 0.04, fake, None, None, 0, None, None) == lib.DSA_ERR_WS
     assert L.mla_decode_attn(1, 1, 128, 64, fake, fake, fake, fake, 0.04, fake, None, None, 0, None, None) == lib.DSA_ERR_SHAPE
     assert L.kv_append_writeback(fake, 1, 0, fake, fake, None, None) == lib.DSA_ERR_ARG
     assert L.kv_append_writeback(fake, 1, 65, fake, fake, None, None) == lib.DSA_ERR_ARG

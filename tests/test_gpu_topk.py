@@ -1,0 +1,89 @@
+"""GPU score + Top-K against the oracle on hand-shaped inputs that exercise
+the select's two paths (candidates gathered on chip, or refinement passes
+when the threshold bin is too crowded), ties, ragged tiles and row groups."""
+import numpy as np
+import pytest
+
+from oracle.indexer import score_topk
+from synth.rng import f32_to_bf16_bits
+
+pytestmark = pytest.mark.gpu
+
+
+@pytest.fixture(autouse=True)
+def _need_gpu():
+    torch = pytest.importorskip("torch")
+    if not torch.cuda.is_available():
+        pytest.skip("no CUDA device")
+
+
+def _run(keys_list, q, w, K):
+    """keys_list: per unit bf16 bits [L_u, 64]; q: bf16 bits [U, R, 8, 64]; w: [U, R, 8]."""
+    import torch
+    from decode_attention_dsa_gb300 import abi
+    from decode_attention_dsa_gb300.units import UnitSet
+    U = len(keys_list)
+    R = q.shape[1]
+    lmax = max(k.shape[0] for k in keys_list) + 8
+    g = UnitSet(U, 4, lmax, mirror="device")
+    for u, k in enumerate(keys_list):
+        g.set_keys(u, 0, k)
+    g.init([k.shape[0] for k in keys_list], abi.WARM_EMPTY)
+    ws_b = abi.dsa_score_topk_workspace(U, R, lmax)
+    ws = torch.zeros(ws_b, dtype=torch.uint8, device="cuda")
+    out = torch.empty((U, R, K), dtype=torch.int32, device="cuda")
+    qt = torch.from_numpy(np.ascontiguousarray(q).view(np.int16)).cuda()
+    wt = torch.from_numpy(np.ascontiguousarray(w, dtype=np.float32)).cuda()
+    for _ in range(2):          # twice: the workspace must come back clean
+        out.fill_(-5)
+        abi.dsa_score_topk(g.units, U, R, K, qt, wt, out, lmax, ws, ws_b, g.dev_err)
+        torch.cuda.synchronize()
+        got = out.cpu().numpy()
+        for u, k in enumerate(keys_list):
+            _, want = score_topk(k, q[u], w[u], K)
+            assert np.array_equal(got[u], want), f"unit {u}"
+    assert g.check() == 0
+    g.close()
+
+
+def _bits(a):
+    return f32_to_bf16_bits(np.asarray(a, dtype=np.float32))
+
+
+def test_all_scores_equal_takes_lowest_positions():
+    rng = np.random.default_rng(0)
+    keys = [_bits(rng.integers(-4, 5, size=(40000, 64)))]
+    q = _bits(np.zeros((1, 1, 8, 64)))
+    _run(keys, q, np.ones((1, 1, 8)), 2048)
+
+
+def test_few_distinct_values_many_ties():
+    rng = np.random.default_rng(1)
+    keys = [_bits(rng.integers(0, 2, size=(30000, 64))) for _ in range(2)]
+    q = _bits(np.ones((2, 2, 8, 64)))
+    q[:, :, :, 5:] = _bits(np.zeros(1))[0]
+    _run(keys, q, np.ones((2, 2, 8)), 1000)
+
+
+def test_long_ragged_history_three_rows():
+    rng = np.random.default_rng(2)
+    keys = [_bits(rng.integers(-4, 5, size=(131072 + 77, 64)))]
+    q = _bits(rng.integers(-4, 5, size=(1, 3, 8, 64)))
+    w = rng.integers(1, 5, size=(1, 3, 8))
+    _run(keys, q, w, 2048)
+
+
+def test_six_rows_two_row_groups_and_unequal_units():
+    rng = np.random.default_rng(3)
+    keys = [_bits(rng.integers(-4, 5, size=(n, 64))) for n in (5000, 12345, 300)]
+    q = _bits(rng.integers(-4, 5, size=(3, 6, 8, 64)))
+    w = rng.integers(1, 5, size=(3, 6, 8))
+    _run(keys, q, w, 512)
+
+
+def test_negative_weights_and_fractional_queries():
+    rng = np.random.default_rng(4)
+    keys = [_bits(rng.integers(-4, 5, size=(20000, 64)))]
+    q = _bits(rng.integers(-64, 65, size=(1, 2, 8, 64)) / 16.0)
+    w = rng.integers(-4, 5, size=(1, 2, 8))
+    _run(keys, q, w, 777)
