@@ -308,16 +308,27 @@ k_mla_attn(int R, int H, int K, const uint16_t* __restrict__ q_lat, const uint16
 
   // ---- this CTA's O (64 x 512 fp32) to its slot of the workspace (L2):
   //      warps 0,1,4,5 (lane quarters 0 and 1), 128 contiguous bytes per store run
+  //      each 32 x 32 block goes through a padded shared-memory transpose so
+  //      every store instruction writes four whole 128-byte rows
   float* gO = ws_o + ((size_t)ur * MAX_CLUSTER + crank) * 64 * 512;
   if ((warp & 3) < 2 && !failed) {
-    const int hr = 32 * (warp & 3) + lane;
+    const int q = warp & 3;                              // lane quarter: head rows 32q..32q+31
     const int c0 = 256 * (warp >> 2);
+    float* tb = reinterpret_cast<float*>(sY) + (2 * (warp >> 2) + q) * 32 * 36;   // [32][36]
     for (int c = 0; c < 8; ++c) {
       float v[32];
-      tc::tmem_ld32(tmem + ((uint32_t)(32 * (warp & 3)) << 16) + c0 + 32 * c, v);
-      float4* dst = reinterpret_cast<float4*>(gO + hr * 512 + c0 + 32 * c);
+      tc::tmem_ld32(tmem + ((uint32_t)(32 * q) << 16) + c0 + 32 * c, v);
 #pragma unroll
-      for (int i = 0; i < 8; ++i) dst[i] = make_float4(v[4 * i], v[4 * i + 1], v[4 * i + 2], v[4 * i + 3]);
+      for (int i = 0; i < 8; ++i)
+        reinterpret_cast<float4*>(tb + lane * 36)[i] = make_float4(v[4 * i], v[4 * i + 1], v[4 * i + 2], v[4 * i + 3]);
+      __syncwarp();
+#pragma unroll
+      for (int r4 = 0; r4 < 8; ++r4) {
+        const int r = 4 * r4 + (lane >> 3);              // row within the block
+        const float4 x = reinterpret_cast<const float4*>(tb + r * 36)[lane & 7];
+        reinterpret_cast<float4*>(gO + (32 * q + r) * 512 + c0 + 32 * c)[lane & 7] = x;
+      }
+      __syncwarp();
     }
   }
   if (failed && tid < 64) {   // an empty contribution keeps the peers' merge well defined

@@ -11,17 +11,15 @@
 //
 // Design (GB300):
 //  * k_dsa_score: a persistent grid (one CTA per SM) walks the flattened
-//    (unit, tile) space. Each 128-position tile of bf16 keys (16 KB,
+//    (unit, tile) space. Each 256-position tile of bf16 keys (32 KB,
 //    contiguous) arrives by a 1-D bulk TMA copy into one of two staging
 //    buffers while the previous tile is computed; it is widened once into an
-//    fp32 tile in shared memory (rows padded to 68 floats so the positions a
-//    warp reads together sit 4 banks apart). A lane owns one (query row,
-//    indexer head) and keeps that head's 64 query values in registers as
-//    packed pairs; the 8 head lanes of a position read the key row as
-//    shared-memory broadcasts and accumulate with packed fma.rn.f32x2 (exact
-//    fp32 arithmetic for integer-grid data), two positions per lane at a
-//    time, then apply ReLU and the head weight and reduce over heads with
-//    three shuffles. Each score
+//    fp32 tile in shared memory (chunk c of position p at slot c ^ (p & 7),
+//    so quarter-warps read disjoint banks). A thread owns one position: its
+//    64 key values sit in registers as packed pairs, the query rows are
+//    shared-memory broadcasts, and the 8 heads accumulate in 8 independent
+//    packed fma.rn.f32x2 chains (exact fp32 arithmetic for integer-grid
+//    data); ReLU, head weights and the sum over heads stay in the thread. Each score
 //    becomes an order-preserving uint32 key (staged, then written coalesced)
 //    and feeds a 4096-bin shared histogram of its top 12 bits, merged into a
 //    global per-(unit, row) histogram when the CTA leaves a unit.
@@ -76,13 +74,14 @@ __device__ __forceinline__ uint32_t ordered_key(float s) {
   return (b & 0x80000000u) ? ~b : (b | 0x80000000u);
 }
 
-constexpr int SCORE_TP = 128;           // positions per tile
-constexpr int KT_STRIDE = 68;           // fp32 key row stride: 4-bank offset per row
-inline int score_tile(int) { return SCORE_TP; }
+// positions per tile: 256 (one per thread) up to 4 query rows, 128 above
+// (the per-row histograms need the room)
+inline int score_tile(int R) { return R <= 4 ? 256 : 128; }
 
 inline size_t score_smem(int R) {
-  return (size_t)2 * SCORE_TP * 128 + (size_t)SCORE_TP * KT_STRIDE * 4 + (size_t)R * SCORE_TP * 4 +
-         (size_t)R * HIST1_BINS * 4 + 64;
+  // bf16 staging x2, fp32 key tile, fp32 query rows, histograms, barriers
+  const int TP = score_tile(R);
+  return (size_t)2 * TP * 128 + (size_t)TP * 256 + (size_t)R * 512 * 4 + (size_t)R * HIST1_BINS * 4 + 64;
 }
 
 __device__ __forceinline__ unsigned long long pack_f2(float lo, float hi) {
@@ -106,66 +105,49 @@ struct ScoreArgs {
   uint32_t* okeys;
   int64_t stride;
   int64_t max_len;
-  int64_t tpu;          // tiles per unit
-  int64_t total;        // U * tpu
+  int tpu;              // tiles per unit
+  int U;
   int R, K, TP;
 };
 
+// One lane per history position. The fp32 key tile holds 16 four-float
+// chunks per position; chunk c of position p sits at slot c ^ (p & 7), so the
+// eight lanes of a quarter-warp read eight different bank groups.
 __global__ void __launch_bounds__(SCORE_THREADS, 2) k_dsa_score(ScoreArgs a) {
   extern __shared__ __align__(128) uint8_t sm[];
-  const int TP = a.TP, R = a.R;
-  uint8_t* stg0 = sm;
-  float* kt = reinterpret_cast<float*>(sm + 2 * TP * 128);            // [TP][KT_STRIDE]
-  uint32_t* sc = reinterpret_cast<uint32_t*>(kt + TP * KT_STRIDE);    // [R][TP]
-  uint32_t* hs = sc + R * TP;                                          // [R][4096]
-  uint64_t* bar = reinterpret_cast<uint64_t*>(hs + R * HIST1_BINS);   // [2]
-  const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
+  const int TP = a.TP;
+  const int R = a.R;
+  uint8_t* stg0 = sm;                                                  // [2][TP][128 B]
+  float* kt = reinterpret_cast<float*>(sm + 2 * TP * 128);            // [TP][64] swizzled
+  float* sq = kt + TP * 64;                                            // [R][8][64]
+  uint32_t* hs = reinterpret_cast<uint32_t*>(sq + R * 512);            // [R][4096]
+  uint64_t* bar = reinterpret_cast<uint64_t*>(hs + R * HIST1_BINS);    // [2]
+  const int tid = threadIdx.x;
 
-  const int64_t per = (a.total + gridDim.x - 1) / gridDim.x;
-  const int64_t f0 = (int64_t)blockIdx.x * per;
-  const int64_t f1 = min(f0 + per, a.total);
+  // this CTA's tiles: [f0, f1) of the flattened (unit, tile) space
+  const long long total = (long long)a.U * a.tpu;
+  const long long per = (total + gridDim.x - 1) / gridDim.x;
+  const long long f0 = (long long)blockIdx.x * per;
+  const long long f1 = min(f0 + per, total);
+  if (f0 >= f1) return;
+  const int u0 = (int)(f0 / a.tpu);
+  const int t0 = (int)(f0 - (long long)u0 * a.tpu);
+  const int ntiles = (int)(f1 - f0);
 
-  // history length and key pointer of the units this CTA's tiles touch
   constexpr int UCACHE = 8;
-  __shared__ int64_t s_len[UCACHE];
+  __shared__ int s_ntv[UCACHE];               // valid tiles of the unit (0 if L <= K)
+  __shared__ int s_len[UCACHE];
   __shared__ const uint16_t* s_keys[UCACHE];
-  const int u_first = (int)(f0 / a.tpu);
   if (tid < UCACHE) {
-    const int u = u_first + tid;
-    if ((int64_t)u * a.tpu < f1) {
-      s_len[tid] = min(a.units[u].state[DSA_ST_LEN], a.max_len);
+    const int u = u0 + tid;
+    s_ntv[tid] = 0;
+    if (u < a.U && (long long)(u - u0) * a.tpu <= (long long)t0 + ntiles) {
+      const int64_t L = min(a.units[u].state[DSA_ST_LEN], a.max_len);
+      s_len[tid] = (int)L;
       s_keys[tid] = a.units[u].keys;
+      s_ntv[tid] = L > a.K ? (int)((L + TP - 1) / TP) : 0;
     }
   }
-  __syncthreads();
-  auto unit_len = [&](int u) -> int64_t {
-    return u - u_first < UCACHE ? s_len[u - u_first] : min(a.units[u].state[DSA_ST_LEN], a.max_len);
-  };
-  auto unit_keys = [&](int u) -> const uint16_t* {
-    return u - u_first < UCACHE ? s_keys[u - u_first] : a.units[u].keys;
-  };
-
-  // first valid tile at or after f (a tile is valid if it starts inside a
-  // history longer than K); f1 if none
-  auto next_valid = [&](int64_t f) -> int64_t {
-    while (f < f1) {
-      const int u = (int)(f / a.tpu);
-      const int64_t t = f % a.tpu;
-      const int64_t L = unit_len(u);
-      if (L > a.K && t * TP < L) return f;
-      f = (int64_t)(u + 1) * a.tpu;
-    }
-    return f1;
-  };
-  auto issue = [&](int64_t f, int stage) {
-    const int u = (int)(f / a.tpu);
-    const int64_t t = f % a.tpu;
-    const int64_t L = unit_len(u);
-    const uint32_t n = (uint32_t)min((int64_t)TP, L - t * TP);
-    tc::mbar_arrive_expect_tx(&bar[stage], n * 128);
-    tc::bulk_g2s(stg0 + stage * TP * 128, unit_keys(u) + t * TP * 64, n * 128, &bar[stage]);
-  };
-
   if (tid == 0) {
     tc::mbar_init(&bar[0], 1);
     tc::mbar_init(&bar[1], 1);
@@ -174,22 +156,60 @@ __global__ void __launch_bounds__(SCORE_THREADS, 2) k_dsa_score(ScoreArgs a) {
   for (int i = tid; i < R * HIST1_BINS; i += SCORE_THREADS) hs[i] = 0;
   __syncthreads();
 
-  int64_t nxt[2];
-  nxt[0] = next_valid(f0);
-  nxt[1] = nxt[0] < f1 ? next_valid(nxt[0] + 1) : f1;
+  // walk the tile list: index k in [0, ntiles) -> (unit, tile); a tile is
+  // valid when it starts inside a history longer than K
+  auto tile_of = [&](int k, int& u, int& t) {
+    int tt = t0 + k;
+    u = u0;
+    while (tt >= a.tpu) {
+      tt -= a.tpu;
+      ++u;
+    }
+    t = tt;
+  };
+  auto unit_len = [&](int u) -> int {
+    return u - u0 < UCACHE ? s_len[u - u0] : (int)min(a.units[u].state[DSA_ST_LEN], a.max_len);
+  };
+  auto unit_keys = [&](int u) -> const uint16_t* {
+    return u - u0 < UCACHE ? s_keys[u - u0] : a.units[u].keys;
+  };
+  auto valid = [&](int u, int t) -> bool {
+    const int i = u - u0;
+    int ntv;
+    if (i < UCACHE) {
+      ntv = s_ntv[i];
+    } else {
+      const int L = unit_len(u);
+      ntv = L > a.K ? (L + TP - 1) / TP : 0;
+    }
+    return t < ntv;
+  };
+  auto next_valid = [&](int k) -> int {
+    for (; k < ntiles; ++k) {
+      int u, t;
+      tile_of(k, u, t);
+      if (valid(u, t)) return k;
+    }
+    return ntiles;
+  };
+  auto issue = [&](int k, int stage) {
+    int u, t;
+    tile_of(k, u, t);
+    const int n = min(TP, unit_len(u) - t * TP);
+    tc::mbar_arrive_expect_tx(&bar[stage], (uint32_t)n * 128);
+    tc::bulk_g2s(stg0 + stage * TP * 128, unit_keys(u) + (size_t)t * TP * 64, (uint32_t)n * 128, &bar[stage]);
+  };
+
+  int nxt[2];
+  nxt[0] = next_valid(0);
+  nxt[1] = nxt[0] < ntiles ? next_valid(nxt[0] + 1) : ntiles;
   if (tid == 0) {
-    if (nxt[0] < f1) issue(nxt[0], 0);
-    if (nxt[1] < f1) issue(nxt[1], 1);
+    if (nxt[0] < ntiles) issue(nxt[0], 0);
+    if (nxt[1] < ntiles) issue(nxt[1], 1);
   }
-  uint32_t parity[2] = {0u, 0u};
+  uint32_t parity0 = 0u, parity1 = 0u;
   int stage = 0;
   int cur_u = -1;
-
-  // lane roles: rows are processed in groups of up to 4
-  const int h = lane & 7;
-  unsigned long long q2[32];      // this lane's head row of the query, packed pairs
-  float wv = 0.f;
-  int RP = 1, pp = 0, rr = 0, Rg = 0, loaded_rg = -1;
 
   auto flush_hist = [&](int u) {
     uint32_t* gh = a.hist + (size_t)u * R * HIST1_BINS;
@@ -201,106 +221,74 @@ __global__ void __launch_bounds__(SCORE_THREADS, 2) k_dsa_score(ScoreArgs a) {
       }
     }
   };
-  auto load_q = [&](int u, int rg) {
-    Rg = min(4, R - 4 * rg);
-    RP = Rg == 1 ? 1 : (Rg == 2 ? 2 : 4);
-    pp = lane / (8 * RP);
-    rr = (lane >> 3) % RP;
-    const int row = 4 * rg + rr;
-    if (rr < Rg) {
-      const uint16_t* qh = a.q + (((size_t)u * R + row) * 8 + h) * 64;
-#pragma unroll
-      for (int c = 0; c < 16; ++c) {
-        const uint2 b = *reinterpret_cast<const uint2*>(qh + 4 * c);
-        q2[2 * c] = pack_f2(bf16_lo(b.x), bf16_hi(b.x));
-        q2[2 * c + 1] = pack_f2(bf16_lo(b.y), bf16_hi(b.y));
-      }
-      wv = a.w[((size_t)u * R + row) * 8 + h];
-    } else {
-#pragma unroll
-      for (int c = 0; c < 32; ++c) q2[c] = 0ull;
-      wv = 0.f;
-    }
-    loaded_rg = rg;
-  };
 
-  while (nxt[stage] < f1) {
-    const int64_t f = nxt[stage];
-    const int u = (int)(f / a.tpu);
-    const int64_t t = f % a.tpu;
-    const int64_t L = unit_len(u);
-    const int n = (int)min((int64_t)TP, L - t * TP);
+  while (true) {
+    const int k = stage == 0 ? nxt[0] : nxt[1];
+    if (k >= ntiles) break;
+    int u, t;
+    tile_of(k, u, t);
+    const int n = min(TP, unit_len(u) - t * TP);
     if (u != cur_u) {
       if (cur_u >= 0) flush_hist(cur_u);
       cur_u = u;
-      loaded_rg = -1;
+      // query rows (fp32) and head weights of this unit
+      for (int i = tid; i < R * 512; i += SCORE_THREADS) sq[i] = bf16f(a.q[(size_t)u * R * 512 + i]);
     }
-    if (!tc::mbar_wait(&bar[stage], parity[stage])) break;   // bounded; cannot happen normally
-    parity[stage] ^= 1u;
-    // widen the staged bf16 keys to fp32
+    const bool ok = tc::mbar_wait(&bar[stage], stage == 0 ? parity0 : parity1);
+    if (stage == 0) parity0 ^= 1u; else parity1 ^= 1u;
+    if (!ok) break;                       // bounded wait; does not happen in normal runs
+    // widen the staged bf16 keys into the swizzled fp32 tile
     const uint8_t* stg = stg0 + stage * TP * 128;
     for (int i = tid; i < n * 8; i += SCORE_THREADS) {
+      const int p = i >> 3, cb = i & 7;
       const uint4 v = *reinterpret_cast<const uint4*>(stg + 16 * i);
-      float4* d = reinterpret_cast<float4*>(kt + (i >> 3) * KT_STRIDE + 8 * (i & 7));
-      d[0] = make_float4(bf16_lo(v.x), bf16_hi(v.x), bf16_lo(v.y), bf16_hi(v.y));
-      d[1] = make_float4(bf16_lo(v.z), bf16_hi(v.z), bf16_lo(v.w), bf16_hi(v.w));
+      float4* row = reinterpret_cast<float4*>(kt + p * 64);
+      row[(2 * cb) ^ (p & 7)] = make_float4(bf16_lo(v.x), bf16_hi(v.x), bf16_lo(v.y), bf16_hi(v.y));
+      row[(2 * cb + 1) ^ (p & 7)] = make_float4(bf16_lo(v.z), bf16_hi(v.z), bf16_lo(v.w), bf16_hi(v.w));
     }
     __syncthreads();
-    // the staging buffer is free: prefetch the tile after the other stage's
     {
-      const int64_t other = nxt[stage ^ 1];
-      const int64_t fn = other < f1 ? next_valid(other + 1) : f1;
-      nxt[stage] = fn;
-      if (tid == 0 && fn < f1) issue(fn, stage);
+      const int other = stage == 0 ? nxt[1] : nxt[0];
+      const int kn = other < ntiles ? next_valid(other + 1) : ntiles;
+      if (stage == 0) nxt[0] = kn; else nxt[1] = kn;
+      if (tid == 0 && kn < ntiles) issue(kn, stage);
     }
-    const int ngroups = (R + 3) / 4;
-    for (int rg = 0; rg < ngroups; ++rg) {
-      if (loaded_rg != rg) load_q(u, rg);
-      // lanes: pp (position in a group of P), rr (row), h (head); each lane
-      // takes two positions, p0 + pp and p0 + pp + P, per iteration
-      const int P = 4 / RP;
-      const int per_warp = TP / (SCORE_THREADS / 32);
-      for (int p0 = warp * per_warp; p0 < warp * per_warp + per_warp; p0 += 2 * P) {
-        const int pa = p0 + pp, pb = pa + P;
-        const ulonglong2* ka = reinterpret_cast<const ulonglong2*>(kt + pa * KT_STRIDE);
-        const ulonglong2* kb = reinterpret_cast<const ulonglong2*>(kt + pb * KT_STRIDE);
-        unsigned long long a0 = 0ull, a1 = 0ull, b0 = 0ull, b1 = 0ull;
+    // ---- scores: thread = position
+    const int p = tid;
+    if (p < n) {
+      unsigned long long kr[32];
+      const float4* row = reinterpret_cast<const float4*>(kt + p * 64);
+      const int sw = p & 7;
+#pragma unroll
+      for (int c = 0; c < 16; ++c) {
+        const float4 v = row[c ^ sw];
+        kr[2 * c] = pack_f2(v.x, v.y);
+        kr[2 * c + 1] = pack_f2(v.z, v.w);
+      }
+      const float* wr = a.w + (size_t)u * R * 8;
+      for (int r = 0; r < R; ++r) {
+        const ulonglong2* qr = reinterpret_cast<const ulonglong2*>(sq + r * 512);
+        unsigned long long acc[8];
+#pragma unroll
+        for (int h = 0; h < 8; ++h) acc[h] = 0ull;
 #pragma unroll
         for (int c = 0; c < 16; ++c) {
-          const ulonglong2 x = ka[c];
-          const ulonglong2 y = kb[c];
-          fma2(a0, q2[2 * c], x.x);
-          fma2(a1, q2[2 * c + 1], x.y);
-          fma2(b0, q2[2 * c], y.x);
-          fma2(b1, q2[2 * c + 1], y.y);
-        }
-        float va = wv * fmaxf(sum2(a0) + sum2(a1), 0.f);
-        float vb = wv * fmaxf(sum2(b0) + sum2(b1), 0.f);
 #pragma unroll
-        for (int o = 1; o < 8; o <<= 1) {
-          va += __shfl_xor_sync(0xffffffffu, va, o);
-          vb += __shfl_xor_sync(0xffffffffu, vb, o);
-        }
-        if (h == 0 && rr < Rg) {
-          const int row = 4 * rg + rr;
-          if (pa < n) {
-            const uint32_t key = ordered_key(va);
-            sc[row * TP + pa] = key;
-            atomicAdd(&hs[row * HIST1_BINS + (key >> 20)], 1u);
-          }
-          if (pb < n) {
-            const uint32_t key = ordered_key(vb);
-            sc[row * TP + pb] = key;
-            atomicAdd(&hs[row * HIST1_BINS + (key >> 20)], 1u);
+          for (int h = 0; h < 8; ++h) {
+            const ulonglong2 qq = qr[h * 16 + c];     // broadcast: every lane, same address
+            fma2(acc[h], qq.x, kr[2 * c]);
+            fma2(acc[h], qq.y, kr[2 * c + 1]);
           }
         }
+        float sc = 0.f;
+#pragma unroll
+        for (int h = 0; h < 8; ++h) sc = fmaf(__ldg(wr + r * 8 + h), fmaxf(sum2(acc[h]), 0.f), sc);
+        const uint32_t key = ordered_key(sc);
+        a.okeys[((size_t)u * R + r) * a.stride + (size_t)t * TP + p] = key;
+        atomicAdd(&hs[r * HIST1_BINS + (key >> 20)], 1u);
       }
     }
     __syncthreads();
-    for (int i = tid; i < R * TP; i += SCORE_THREADS) {
-      const int row = i / TP, pl = i % TP;
-      if (pl < n) a.okeys[((size_t)u * R + row) * a.stride + t * TP + pl] = sc[i];
-    }
     stage ^= 1;
   }
   __syncthreads();
@@ -640,6 +628,7 @@ extern "C" int dsa_score_topk(const dsa_unit* units, int32_t U, int32_t R, int32
   const int TP = score_tile(R);
   const int64_t tpu = (max_len + TP - 1) / TP;
   if (tpu > 0) {
+    if (tpu * U > 0x7fffffffLL) return DSA_ERR_ARG;
     ScoreArgs a;
     a.units = units;
     a.q = q;
@@ -648,13 +637,13 @@ extern "C" int dsa_score_topk(const dsa_unit* units, int32_t U, int32_t R, int32
     a.okeys = tw.keys;
     a.stride = tw.stride;
     a.max_len = max_len;
-    a.tpu = tpu;
-    a.total = tpu * U;
+    a.tpu = (int)tpu;
+    a.U = U;
     a.R = R;
     a.K = K;
     a.TP = TP;
     const int per_sm = score_smem(R) <= 113 * 1024 ? 2 : 1;
-    const int64_t grid = std::min<int64_t>(a.total, (int64_t)per_sm * (g_num_sms > 0 ? g_num_sms : 148));
+    const int64_t grid = std::min<int64_t>(tpu * U, (int64_t)per_sm * (g_num_sms > 0 ? g_num_sms : 148));
     k_dsa_score<<<(unsigned)grid, SCORE_THREADS, score_smem(R), st>>>(a);
     if (dsa_launch_status() != DSA_OK) return DSA_ERR_CUDA;
   }
