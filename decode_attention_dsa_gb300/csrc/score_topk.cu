@@ -10,19 +10,21 @@
 // kernel time they saved, so here the whole select is one clustered launch.
 //
 // Design (GB300):
-//  * k_dsa_score: a persistent grid (one CTA per SM) walks the flattened
-//    (unit, tile) space. Each 256-position tile of bf16 keys (32 KB,
+//  * k_dsa_score: a persistent grid (up to four CTAs per SM) walks the flattened
+//    (unit, tile) space. Each 128-position tile of bf16 keys (16 KB,
 //    contiguous) arrives by a 1-D bulk TMA copy into one of two staging
-//    buffers while the previous tile is computed; it is widened once into an
-//    fp32 tile in shared memory (chunk c of position p at slot c ^ (p & 7),
-//    so quarter-warps read disjoint banks). A thread owns one position: its
-//    64 key values sit in registers as packed pairs, the query rows are
-//    shared-memory broadcasts, and the 8 heads accumulate in 8 independent
-//    packed fma.rn.f32x2 chains (exact fp32 arithmetic for integer-grid
-//    data); ReLU, head weights and the sum over heads stay in the thread. Each score
-//    becomes an order-preserving uint32 key (staged, then written coalesced)
-//    and feeds a 4096-bin shared histogram of its top 12 bits, merged into a
-//    global per-(unit, row) histogram when the CTA leaves a unit.
+//    buffers while the previous tile is computed. A thread owns one
+//    position: it reads the position's 128-byte bf16 row from the staged tile
+//    (chunk order rotated by position so a quarter-warp hits eight bank
+//    groups), widens it into registers as 32 packed fp32 pairs, reads the
+//    query rows as shared-memory broadcasts, and accumulates the 8 heads in
+//    independent packed fma.rn.f32x2 chains (exact fp32 arithmetic for
+//    integer-grid data); ReLU, head weights and the sum over heads stay in
+//    the thread. Histogram updates are aggregated per warp (one shared atomic
+//    per distinct bin). Each score becomes an order-preserving uint32 key
+//    (written coalesced, one per thread) and feeds a 4096-bin shared
+//    histogram of its top 12 bits, merged into a global per-(unit, row)
+//    histogram when the CTA leaves a unit.
 //  * k_topk_select: one 8-CTA thread-block cluster per (unit, row). The global
 //    histogram gives the bin b1 of the K-th largest key. One pass over the
 //    cluster's key ranges (cached in shared memory when they fit) counts keys
@@ -43,7 +45,7 @@ namespace cg = cooperative_groups;
 
 namespace {
 
-constexpr int SCORE_THREADS = 256;
+constexpr int SCORE_THREADS = 128;      // one position per thread
 constexpr int HIST1_BINS = 4096;         // top 12 bits of the ordered key
 constexpr int SEL_CLUSTER = 8;
 constexpr int SEL_THREADS = 512;
@@ -74,14 +76,32 @@ __device__ __forceinline__ uint32_t ordered_key(float s) {
   return (b & 0x80000000u) ? ~b : (b | 0x80000000u);
 }
 
-// positions per tile: 256 (one per thread) up to 4 query rows, 128 above
-// (the per-row histograms need the room)
-inline int score_tile(int R) { return R <= 4 ? 256 : 128; }
+// positions per tile (one per thread)
+inline int score_tile(int) { return 128; }
 
 inline size_t score_smem(int R) {
-  // bf16 staging x2, fp32 key tile, fp32 query rows, histograms, barriers
+  // bf16 staging x2, fp32 query rows, histograms, barriers
   const int TP = score_tile(R);
-  return (size_t)2 * TP * 128 + (size_t)TP * 256 + (size_t)R * 512 * 4 + (size_t)R * HIST1_BINS * 4 + 64;
+  return (size_t)2 * TP * 128 + (size_t)R * 512 * 4 + (size_t)R * HIST1_BINS * 4 + 64;
+}
+
+// Chunk c of a 128-byte key row is read as chunk (c + s) & 7, s = position & 7,
+// so the eight threads of a quarter-warp touch eight different bank groups;
+// this puts the chunks back in order with static register indices.
+__device__ __forceinline__ void unrotate8(uint4 (&x)[8], int s) {
+  uint4 y[8];
+#pragma unroll
+  for (int c = 0; c < 8; ++c) y[c] = x[c];
+  switch (s) {
+#define DSA_ROT_CASE(S)                                                     \
+    case S:                                                                 \
+      _Pragma("unroll") for (int c = 0; c < 8; ++c) x[(c + S) & 7] = y[c]; \
+      break;
+    DSA_ROT_CASE(0) DSA_ROT_CASE(1) DSA_ROT_CASE(2) DSA_ROT_CASE(3)
+    DSA_ROT_CASE(4) DSA_ROT_CASE(5) DSA_ROT_CASE(6) DSA_ROT_CASE(7)
+#undef DSA_ROT_CASE
+    default: break;
+  }
 }
 
 __device__ __forceinline__ unsigned long long pack_f2(float lo, float hi) {
@@ -113,13 +133,12 @@ struct ScoreArgs {
 // One lane per history position. The fp32 key tile holds 16 four-float
 // chunks per position; chunk c of position p sits at slot c ^ (p & 7), so the
 // eight lanes of a quarter-warp read eight different bank groups.
-__global__ void __launch_bounds__(SCORE_THREADS, 2) k_dsa_score(ScoreArgs a) {
+__global__ void __launch_bounds__(SCORE_THREADS, 4) k_dsa_score(ScoreArgs a) {
   extern __shared__ __align__(128) uint8_t sm[];
   const int TP = a.TP;
   const int R = a.R;
   uint8_t* stg0 = sm;                                                  // [2][TP][128 B]
-  float* kt = reinterpret_cast<float*>(sm + 2 * TP * 128);            // [TP][64] swizzled
-  float* sq = kt + TP * 64;                                            // [R][8][64]
+  float* sq = reinterpret_cast<float*>(sm + 2 * TP * 128);            // [R][8][64]
   uint32_t* hs = reinterpret_cast<uint32_t*>(sq + R * 512);            // [R][4096]
   uint64_t* bar = reinterpret_cast<uint64_t*>(hs + R * HIST1_BINS);    // [2]
   const int tid = threadIdx.x;
@@ -233,37 +252,29 @@ __global__ void __launch_bounds__(SCORE_THREADS, 2) k_dsa_score(ScoreArgs a) {
       cur_u = u;
       // query rows (fp32) and head weights of this unit
       for (int i = tid; i < R * 512; i += SCORE_THREADS) sq[i] = bf16f(a.q[(size_t)u * R * 512 + i]);
+      __syncthreads();   // the new query rows are complete before any thread reads them
     }
     const bool ok = tc::mbar_wait(&bar[stage], stage == 0 ? parity0 : parity1);
     if (stage == 0) parity0 ^= 1u; else parity1 ^= 1u;
     if (!ok) break;                       // bounded wait; does not happen in normal runs
-    // widen the staged bf16 keys into the swizzled fp32 tile
     const uint8_t* stg = stg0 + stage * TP * 128;
-    for (int i = tid; i < n * 8; i += SCORE_THREADS) {
-      const int p = i >> 3, cb = i & 7;
-      const uint4 v = *reinterpret_cast<const uint4*>(stg + 16 * i);
-      float4* row = reinterpret_cast<float4*>(kt + p * 64);
-      row[(2 * cb) ^ (p & 7)] = make_float4(bf16_lo(v.x), bf16_hi(v.x), bf16_lo(v.y), bf16_hi(v.y));
-      row[(2 * cb + 1) ^ (p & 7)] = make_float4(bf16_lo(v.z), bf16_hi(v.z), bf16_lo(v.w), bf16_hi(v.w));
-    }
-    __syncthreads();
-    {
-      const int other = stage == 0 ? nxt[1] : nxt[0];
-      const int kn = other < ntiles ? next_valid(other + 1) : ntiles;
-      if (stage == 0) nxt[0] = kn; else nxt[1] = kn;
-      if (tid == 0 && kn < ntiles) issue(kn, stage);
-    }
-    // ---- scores: thread = position
+    // ---- scores: thread = position; its key row comes straight from the
+    //      staged tile and is widened in registers
     const int p = tid;
+    float score[DSA_MAX_ROWS];
     if (p < n) {
-      unsigned long long kr[32];
-      const float4* row = reinterpret_cast<const float4*>(kt + p * 64);
-      const int sw = p & 7;
+      uint4 ch[8];
+      const uint4* row = reinterpret_cast<const uint4*>(stg + p * 128);
+      const int s = p & 7;
 #pragma unroll
-      for (int c = 0; c < 16; ++c) {
-        const float4 v = row[c ^ sw];
-        kr[2 * c] = pack_f2(v.x, v.y);
-        kr[2 * c + 1] = pack_f2(v.z, v.w);
+      for (int c = 0; c < 8; ++c) ch[c] = row[(c + s) & 7];
+      unrotate8(ch, s);
+      unsigned long long kr[32];
+#pragma unroll
+      for (int c = 0; c < 8; ++c) {
+        const uint32_t w4[4] = {ch[c].x, ch[c].y, ch[c].z, ch[c].w};
+#pragma unroll
+        for (int e = 0; e < 4; ++e) kr[4 * c + e] = pack_f2(bf16_lo(w4[e]), bf16_hi(w4[e]));
       }
       const float* wr = a.w + (size_t)u * R * 8;
       for (int r = 0; r < R; ++r) {
@@ -272,20 +283,35 @@ __global__ void __launch_bounds__(SCORE_THREADS, 2) k_dsa_score(ScoreArgs a) {
 #pragma unroll
         for (int h = 0; h < 8; ++h) acc[h] = 0ull;
 #pragma unroll
-        for (int c = 0; c < 16; ++c) {
+        for (int j = 0; j < 16; ++j) {
 #pragma unroll
           for (int h = 0; h < 8; ++h) {
-            const ulonglong2 qq = qr[h * 16 + c];     // broadcast: every lane, same address
-            fma2(acc[h], qq.x, kr[2 * c]);
-            fma2(acc[h], qq.y, kr[2 * c + 1]);
+            const ulonglong2 qq = qr[h * 16 + j];     // broadcast: every lane, same address
+            fma2(acc[h], qq.x, kr[2 * j]);
+            fma2(acc[h], qq.y, kr[2 * j + 1]);
           }
         }
         float sc = 0.f;
 #pragma unroll
         for (int h = 0; h < 8; ++h) sc = fmaf(__ldg(wr + r * 8 + h), fmaxf(sum2(acc[h]), 0.f), sc);
-        const uint32_t key = ordered_key(sc);
+        if (r < DSA_MAX_ROWS) score[r] = sc;
+      }
+    }
+    __syncthreads();
+    {
+      const int other = stage == 0 ? nxt[1] : nxt[0];
+      const int kn = other < ntiles ? next_valid(other + 1) : ntiles;
+      if (stage == 0) nxt[0] = kn; else nxt[1] = kn;
+      if (tid == 0 && kn < ntiles) issue(kn, stage);
+    }
+    if (p < n) {
+      const unsigned amask = __activemask();
+      for (int r = 0; r < R; ++r) {
+        const uint32_t key = ordered_key(score[r]);
         a.okeys[((size_t)u * R + r) * a.stride + (size_t)t * TP + p] = key;
-        atomicAdd(&hs[r * HIST1_BINS + (key >> 20)], 1u);
+        const uint32_t bin = key >> 20;
+        const unsigned peers = __match_any_sync(amask, bin);
+        if ((int)(threadIdx.x & 31) == __ffs(peers) - 1) atomicAdd(&hs[r * HIST1_BINS + bin], (uint32_t)__popc(peers));
       }
     }
     __syncthreads();
@@ -642,7 +668,7 @@ extern "C" int dsa_score_topk(const dsa_unit* units, int32_t U, int32_t R, int32
     a.R = R;
     a.K = K;
     a.TP = TP;
-    const int per_sm = score_smem(R) <= 113 * 1024 ? 2 : 1;
+    const int per_sm = (int)std::max<size_t>(1, std::min<size_t>(4, 232448 / (score_smem(R) + 1024)));
     const int64_t grid = std::min<int64_t>(tpu * U, (int64_t)per_sm * (g_num_sms > 0 ? g_num_sms : 148));
     k_dsa_score<<<(unsigned)grid, SCORE_THREADS, score_smem(R), st>>>(a);
     if (dsa_launch_status() != DSA_OK) return DSA_ERR_CUDA;
