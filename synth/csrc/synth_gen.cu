@@ -5,7 +5,6 @@
 // kernels write byte-for-byte what the numpy generator writes. This library
 // draws inputs only; it holds none of the decode path's arithmetic.
 #include <cstdint>
-#include <cuda_fp16.h>
 #include <cuda_runtime.h>
 
 namespace {
@@ -66,9 +65,12 @@ __global__ void gen_rows(uint64_t k_lat, uint64_t k_sc, uint64_t k_rope, uint8_t
   } else if (c < 520) {
     const int g = c - 512;
     const int k = uni(field(k_sc, p * 8 + g), 328, 1311);
-    const __half_raw h = __float2half_rn((float)k * (1.0f / 65536.0f));
-    row[512 + 2 * g] = (uint8_t)(h.x & 0xFF);
-    row[512 + 2 * g + 1] = (uint8_t)(h.x >> 8);
+    // k * 2^-16 is exact in fp16: with 2^e <= k < 2^(e+1) (e in 8..10) the
+    // biased exponent is e - 16 + 15 and the 10-bit fraction (k - 2^e) << (10 - e)
+    const int e = 31 - __clz(k);
+    const uint16_t h = (uint16_t)(((e - 1) << 10) | ((k << (10 - e)) & 0x3FF));
+    row[512 + 2 * g] = (uint8_t)(h & 0xFF);
+    row[512 + 2 * g + 1] = (uint8_t)(h >> 8);
   } else {
     const int e = c - 520;
     const float z = (float)ih_num(k_rope, (p * 64 + e) * 12) * (1.0f / 65536.0f);

@@ -20,7 +20,7 @@ def gpu_modules():
 class Pair:
     """A workload run side by side on the GPU and in the oracle."""
 
-    def __init__(self, wl: W.Workload, units=None, mirror="host", oracle_units=None):
+    def __init__(self, wl: W.Workload, units=None, mirror="host", oracle_units=None, gpu_gen=False):
         torch, abi, UnitSet, DecodePath = gpu_modules()
         self.torch, self.abi = torch, abi
         self.wl = wl
@@ -30,7 +30,19 @@ class Pair:
         self.g = UnitSet(U, wl.S, wl.lmax, mirror=mirror)
         self.o = {}
         hist = np.arange(wl.L0)
+        if gpu_gen:
+            # history drawn on the device (same bytes as the numpy generator);
+            # the oracle regenerates its units with numpy, mirror rows on demand
+            from synth import gpu as sg
+            assert self.uidx == list(range(wl.U))
+            sg.history(wl, self.g)
+            for u in self.oidx:
+                keys = W.keys_bits(wl, u, hist)
+                self.o[u] = OracleUnit.create(wl.S, wl.lmax, wl.L0, keys,
+                                              (lambda pos, u=u: W.rows_bytes(wl, u, pos)), wl.warm)
         for i, u in enumerate(self.uidx):
+            if gpu_gen:
+                break
             keys = W.keys_bits(wl, u, hist)
             rows = W.rows_bytes(wl, u, hist)
             self.g.set_keys(i, 0, keys)

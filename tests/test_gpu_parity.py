@@ -19,8 +19,8 @@ def _need_gpu():
 
 
 def run(wl, steps=None, rnds=None, mirror="host", check_every=1, attention_every=1,
-        full_state=True, units=None, oracle_units=None, oracle_rnds=None):
-    pair = Pair(wl, units=units, mirror=mirror, oracle_units=oracle_units)
+        full_state=True, units=None, oracle_units=None, oracle_rnds=None, gpu_gen=False):
+    pair = Pair(wl, units=units, mirror=mirror, oracle_units=oracle_units, gpu_gen=gpu_gen)
     steps = range(wl.steps) if steps is None else steps
     worst = 0.0
     for k, st in enumerate(steps):
@@ -137,3 +137,16 @@ def test_config3_cache_stress_first_steps():
     pair, worst = run(wl, steps=range(6), attention_every=3)
     c = pair.p.counters.cpu().numpy()[0]
     assert c[2] / wl.K < 0.05          # phase 1: about 1% of the Top-K misses
+
+
+@pytest.mark.slow
+def test_config4_capacity_batch_sampled_units():
+    """16 sessions x 2 layers x 1,048,576-position histories in one launch per
+    call (32 units, 20.5 GiB pinned host mirror); units 0 and 31 are compared
+    with the oracle element by element on the first steps."""
+    import torch
+    free, _ = torch.cuda.mem_get_info()
+    if free < 12 * 2**30:
+        pytest.skip("not enough device memory")
+    wl = W.WORKLOADS[4].with_(steps=3)
+    run(wl, steps=range(3), oracle_units=[0, 31], gpu_gen=True, attention_every=2)
