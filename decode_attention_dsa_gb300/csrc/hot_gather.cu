@@ -24,10 +24,13 @@
 //                 (block scans over 1024-slot windows), and the map update.
 //                 The parallel assignment reproduces the sequential rule
 //                 "i-th miss takes the i-th eligible slot" exactly.
-//  3. k_copy      one warp per 656-byte row: fills read the mirror row once
-//                 (zero-copy over the host link) and write both the victim
-//                 slot and the owner entry's compact row; every other entry
-//                 copies from its source (slot / ring / mirror).
+//  3. k_copy      one warp per 656-byte row: a fill reads the mirror row once
+//                 (zero-copy over the host link) and writes the victim slot,
+//                 the compact row of the position's first occurrence and the
+//                 compact rows of its later occurrences in the other query
+//                 rows (all RAM-class: they get the RAM bytes, never the slot
+//                 being filled); every other entry copies from its source
+//                 (slot / ring / mirror).
 #include "common.cuh"
 
 namespace {
@@ -44,6 +47,7 @@ struct GatherWs {
   int32_t* opc;         // [U][RK] per-row exclusive prefix count of owner entries
   int32_t* nfill;       // [U]
   uint8_t* served;      // [U][RK] 1 if the entry's row is written by a fill
+  int32_t* dup;         // [U][RK][MAX_ROWS-1] later occurrences of the i-th inserted miss
 };
 
 inline GatherWs gather_ws(void* ws, int32_t U, int32_t R, int32_t K) {
@@ -57,6 +61,7 @@ inline GatherWs gather_ws(void* ws, int32_t U, int32_t R, int32_t K) {
   g.opc = reinterpret_cast<int32_t*>(b + 3 * a);
   g.nfill = reinterpret_cast<int32_t*>(b + 4 * a);
   g.served = reinterpret_cast<uint8_t*>(b + 4 * a + dsa_align((size_t)U * 4, 256));
+  g.dup = reinterpret_cast<int32_t*>(b + 4 * a + dsa_align((size_t)U * 4, 256) + dsa_align((size_t)U * rk, 256));
   return g;
 }
 
@@ -192,6 +197,14 @@ k_assign(const dsa_unit* __restrict__ units, int R, int K, int round,
     if (rank < RK) {
       fill_pos[rank] = p;
       fill_entry[rank] = e;
+      int32_t* dp = g.dup + ((size_t)u * RK + rank) * (DSA_MAX_ROWS - 1);
+      for (int k = 0; k < DSA_MAX_ROWS - 1; ++k) dp[k] = -1;
+      int nd = 0;
+      for (int r2 = r + 1; r2 < R; ++r2) {
+        const int32_t* o = topk + (size_t)r2 * K;
+        const int lb = row_lower_bound(o, K, p);
+        if (lb < K && o[lb] == p) dp[nd++] = r2 * K + lb;
+      }
     } else {
       dsa_flag(dev_err, DSA_DEVERR_BOUNDS);
     }
@@ -232,9 +245,16 @@ k_assign(const dsa_unit* __restrict__ units, int R, int K, int round,
     un.pos_slot[p] = s;
     un.fill_round[s] = round;
   }
-  // served[e] = 1 only for owners that received a slot
+  // served[e] = 1 for owners that received a slot and for the later
+  // occurrences of their position: the fill reads the mirror row once and
+  // hands the same RAM bytes to every occurrence
   for (int i = threadIdx.x; i < nM; i += ASSIGN_THREADS) {
-    if (i >= n) served[fill_entry[i]] = 0;
+    if (i >= n) {
+      served[fill_entry[i]] = 0;
+    } else {
+      const int32_t* dp = g.dup + ((size_t)u * RK + i) * (DSA_MAX_ROWS - 1);
+      for (int k = 0; k < R - 1 && dp[k] >= 0; ++k) served[dp[k]] = 1;
+    }
   }
   if (threadIdx.x == 0) {
     if (n > 0) {
@@ -294,6 +314,14 @@ k_copy(const dsa_unit* __restrict__ units, int R, int K, const int32_t* __restri
       d1[32 + lane] = b;
       d2[32 + lane] = b;
     }
+    const int32_t* dp = g.dup + o * (DSA_MAX_ROWS - 1);
+    for (int k = 0; k < R - 1; ++k) {
+      const int32_t ed = dp[k];
+      if (ed < 0) break;
+      uint4* d3 = reinterpret_cast<uint4*>(rows + (size_t)ed * DSA_ROW_BYTES);
+      d3[lane] = a;
+      if (lane < 9) d3[32 + lane] = b;
+    }
   }
 }
 
@@ -303,7 +331,7 @@ extern "C" size_t hot_gather_workspace(int32_t U, int32_t R, int32_t K) {
   if (U < 1 || R < 1 || K < 1) return 0;
   const size_t rk = (size_t)R * K;
   return 4 * dsa_align((size_t)U * rk * 4, 256) + dsa_align((size_t)U * 4, 256) +
-         dsa_align((size_t)U * rk, 256);
+         dsa_align((size_t)U * rk, 256) + dsa_align((size_t)U * rk * (DSA_MAX_ROWS - 1) * 4, 256);
 }
 
 extern "C" int hot_gather(const dsa_unit* units, int32_t U, int32_t R, int32_t K, int32_t round,
