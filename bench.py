@@ -259,60 +259,92 @@ def run_gpu(args, rank: int, world: int):
     for s in range(Wm):
         path.step(abi.ROUND_AUTO, *step_args(s))
     torch.cuda.synchronize()
-    if world > 1:
-        torch.distributed.barrier()
-    torch.cuda.synchronize()
     use_graph = not args.no_graph
-    ev = [[torch.cuda.Event(enable_timing=True, external=use_graph) for _ in range(5)]
-          for _ in range(K)]
-    ctr_acc = torch.zeros((U, 4), dtype=torch.int64, device=dev)
     rnd = abi.ROUND_AUTO
 
-    def timed_steps():
-        for i in range(K):
+    def record_steps(nsteps, per_call, ctr_acc=None):
+        """Enqueue nsteps timed steps; returns the events. per_call adds
+        events between the four calls (a separate breakdown run)."""
+        nev = 5 if per_call else 2
+        ev = [[torch.cuda.Event(enable_timing=True, external=use_graph) for _ in range(nev)]
+              for _ in range(nsteps)]
+        for i in range(nsteps):
             s = Wm + i
             qi, w, ql, qr, nr, nk = step_args(s)
             flush.fill_(i & 0xFF)
             e = ev[i]
             e[0].record()
             path.score_topk(qi, w)
-            e[1].record()
+            if per_call:
+                e[1].record()
             path.gather(rnd)
-            e[2].record()
+            if per_call:
+                e[2].record()
             path.attend(ql, qr)
-            e[3].record()
+            if per_call:
+                e[3].record()
             path.append(nr, nk)
-            e[4].record()
-            ctr_acc.add_(path.counters)
+            e[-1].record()
+            if ctr_acc is not None:
+                ctr_acc.add_(path.counters)
+        return ev
 
-    graph = None
-    if use_graph:
-        graph = torch.cuda.CUDAGraph()
-        cap = torch.cuda.Stream()
-        cap.wait_stream(torch.cuda.current_stream())
-        with torch.cuda.graph(graph, stream=cap):
-            timed_steps()
+    def run_steps(nsteps, per_call, ctr_acc=None):
+        if use_graph:
+            graph = torch.cuda.CUDAGraph()
+            cap = torch.cuda.Stream()
+            cap.wait_stream(torch.cuda.current_stream())
+            with torch.cuda.graph(graph, stream=cap):
+                ev = record_steps(nsteps, per_call, ctr_acc)
+            torch.cuda.synchronize()
+            return ev, graph
+        return None, None
+
+    def warm_start():
+        units.init([wl.L0] * U, warm)
+        for s in range(Wm):
+            path.step(rnd, *step_args(s))
         torch.cuda.synchronize()
+
+    # ---- headline run: events only at step boundaries
+    ctr_acc = torch.zeros((U, 4), dtype=torch.int64, device=dev)
+    ev, graph = run_steps(K, False, ctr_acc)
+    if world > 1:
+        torch.distributed.barrier()
+    torch.cuda.synchronize()
     clocks = ClockSampler(torch.cuda.current_device())
     clocks.start()
     wall0 = time.perf_counter()
     if graph is not None:
         graph.replay()
     else:
-        timed_steps()
+        ev = record_steps(K, False, ctr_acc)
     torch.cuda.synchronize()
     wall = time.perf_counter() - wall0
     clk = clocks.stop()
     err = units.check()
     if err:
         raise RuntimeError(f"device error word {err:#x}")
-    step_ms = [e[0].elapsed_time(e[4]) for e in ev]
-    call_ms = [statistics.mean(e[j].elapsed_time(e[j + 1]) for e in ev) for j in range(4)]
+    step_ms = [e[0].elapsed_time(e[-1]) for e in ev]
     total_ms = sum(step_ms)
     if world > 1:
         t = torch.tensor([total_ms], dtype=torch.float64, device=dev)
         torch.distributed.all_reduce(t, op=torch.distributed.ReduceOp.MAX)
         total_ms = float(t.item())
+    del graph
+
+    # ---- breakdown run (same start state): events around each call
+    KB = min(K, 256)
+    warm_start()
+    evb, gb = run_steps(KB, True)
+    if gb is not None:
+        gb.replay()
+    else:
+        evb = record_steps(KB, True)
+    torch.cuda.synchronize()
+    call_ms = [statistics.mean(e[j].elapsed_time(e[j + 1]) for e in evb) for j in range(4)]
+    breakdown_step_ms = statistics.mean(e[0].elapsed_time(e[4]) for e in evb)
+    del gb
     ctr = ctr_acc.cpu().numpy().sum(axis=0)    # HOT, RING, RAM entries, fills over K steps
 
     # ---- end to end through the C ABI with host buffers (same K steps, same start state)
@@ -426,6 +458,8 @@ def run_gpu(args, rank: int, world: int):
                           "host_link_gbs": host_gbs, "host_link_kind": "DMA pinned->device copy",
                           "peak_source": peak_kind},
         "per_call": per_call,
+        "per_call_note": (f"mean over a separate replay of {KB} steps from the same start with "
+                          f"events around each call ({breakdown_step_ms:.4f} ms/step there)"),
         "cache": {"hot": int(ctr[0]), "ring": int(ctr[1]), "ram": int(ctr[2]), "fills": int(ctr[3]),
                   "miss_frac": float(ctr[2] / max(1, ctr[:3].sum()))},
         "clocks": clk,
