@@ -12,19 +12,20 @@
 // the recent ring; replacement is a ring that skips pinned slots (the
 // reference-bit clock's long sweeps cost ~1 ms per gather).
 //
-// Three launches per call, each over all units:
-//  1. k_classify  one thread per selected entry: classify with the state as
-//                 it is at call start and pin HOT slots (pin_epoch = call id).
-//                 Nothing is filled yet, so no entry can see a slot filled in
-//                 this call: the visibility rule holds by construction.
-//  2. k_assign    one 1024-thread CTA per unit: counts, the ascending list of
+// Two launches per call, each over all units:
+//  1. k_assign    one 1024-thread CTA per unit: classification of every
+//                 selected entry with the state as it is at call start and
+//                 pins of the HOT slots (pin_epoch = call id) -- nothing is
+//                 filled before a block barrier, so no entry can see a slot
+//                 filled in this call and the visibility rule holds by
+//                 construction -- then counts, the ascending list of
 //                 distinct unmapped misses (first occurrence across rows found
 //                 by binary search in the lower rows, rank by per-row prefix
 //                 counts), the eligible slots in cyclic order from the hand
 //                 (block scans over 1024-slot windows), and the map update.
 //                 The parallel assignment reproduces the sequential rule
 //                 "i-th miss takes the i-th eligible slot" exactly.
-//  3. k_copy      one warp per 656-byte row: a fill reads the mirror row once
+//  2. k_copy      one warp per 656-byte row: a fill reads the mirror row once
 //                 (zero-copy over the host link) and writes the victim slot,
 //                 the compact row of the position's first occurrence and the
 //                 compact rows of its later occurrences in the other query
@@ -35,7 +36,6 @@
 
 namespace {
 
-constexpr int CLS_THREADS = 256;
 constexpr int ASSIGN_THREADS = 1024;
 constexpr int COPY_THREADS = 256;
 constexpr int COPY_WARPS = COPY_THREADS / 32;
@@ -65,37 +65,6 @@ inline GatherWs gather_ws(void* ws, int32_t U, int32_t R, int32_t K) {
   return g;
 }
 
-__global__ void __launch_bounds__(CLS_THREADS)
-k_classify(const dsa_unit* __restrict__ units, int R, int K, int round,
-           const int32_t* __restrict__ topk, uint8_t* __restrict__ cls, int32_t* dev_err) {
-  const int u = blockIdx.y;
-  const int e = blockIdx.x * CLS_THREADS + threadIdx.x;
-  if (e >= R * K) return;
-  const dsa_unit& un = units[u];
-  const int64_t len = un.state[DSA_ST_LEN];
-  const int64_t ram = un.state[DSA_ST_RAM];
-  const int32_t epoch = (int32_t)(un.state[DSA_ST_EPOCH] + 1);
-  if (round < 0) round = epoch - 1;
-  const int32_t p = topk[(size_t)u * R * K + e];
-  uint8_t c = DSA_CLS_PAD;
-  if (p >= 0) {
-    if (p >= len) {
-      dsa_flag(dev_err, DSA_DEVERR_BOUNDS);
-    } else if (p >= ram) {
-      c = DSA_CLS_RING;
-    } else {
-      const int32_t s = un.pos_slot[p];
-      if (s >= 0 && s < un.slots_n && un.fill_round[s] < round) {
-        c = DSA_CLS_HOT;
-        un.pin_epoch[s] = epoch;
-      } else {
-        c = DSA_CLS_RAM;
-      }
-    }
-  }
-  cls[(size_t)u * R * K + e] = c;
-}
-
 // lower_bound of p in an ascending row whose tail is -1 padding (-1 = +inf).
 __device__ __forceinline__ int row_lower_bound(const int32_t* row, int K, int32_t p) {
   int lo = 0, hi = K;
@@ -110,7 +79,7 @@ __device__ __forceinline__ int row_lower_bound(const int32_t* row, int K, int32_
 
 __global__ void __launch_bounds__(ASSIGN_THREADS)
 k_assign(const dsa_unit* __restrict__ units, int R, int K, int round,
-         const int32_t* __restrict__ topk_all, const uint8_t* __restrict__ cls_all,
+         const int32_t* __restrict__ topk_all, uint8_t* cls_all,
          int32_t* __restrict__ counters, GatherWs g, int32_t* dev_err) {
   __shared__ int s_tmp[32];
   __shared__ int s_cnt[4];
@@ -118,7 +87,7 @@ k_assign(const dsa_unit* __restrict__ units, int R, int K, int round,
   const dsa_unit& un = units[u];
   const int RK = R * K;
   const int32_t* topk = topk_all + (size_t)u * RK;
-  const uint8_t* cls = cls_all + (size_t)u * RK;
+  uint8_t* cls = cls_all + (size_t)u * RK;   // written in phase 0, read after a barrier
   int32_t* fill_pos = g.fill_pos + (size_t)u * RK;
   int32_t* fill_slot = g.fill_slot + (size_t)u * RK;
   int32_t* fill_entry = g.fill_entry + (size_t)u * RK;
@@ -129,6 +98,35 @@ k_assign(const dsa_unit* __restrict__ units, int R, int K, int round,
   if (round < 0) round = epoch - 1;
 
   if (threadIdx.x < 4) s_cnt[threadIdx.x] = 0;
+
+  // 0. classify every entry with the state as it is now, pinning HOT slots
+  //    (nothing is filled before the block barrier below, so no entry can see
+  //    a slot filled in this call)
+  {
+    const int64_t len = un.state[DSA_ST_LEN];
+    const int64_t ram = un.state[DSA_ST_RAM];
+    uint8_t* cls_w = cls;
+    for (int e = threadIdx.x; e < RK; e += ASSIGN_THREADS) {
+      const int32_t p = topk[e];
+      uint8_t c = DSA_CLS_PAD;
+      if (p >= 0) {
+        if (p >= len) {
+          dsa_flag(dev_err, DSA_DEVERR_BOUNDS);
+        } else if (p >= ram) {
+          c = DSA_CLS_RING;
+        } else {
+          const int32_t sl = un.pos_slot[p];
+          if (sl >= 0 && sl < S && un.fill_round[sl] < round) {
+            c = DSA_CLS_HOT;
+            un.pin_epoch[sl] = epoch;
+          } else {
+            c = DSA_CLS_RAM;
+          }
+        }
+      }
+      cls_w[e] = c;
+    }
+  }
   __syncthreads();
 
   // 1. counts, owner flags (first occurrence of an unmapped RAM position) and
@@ -344,9 +342,6 @@ extern "C" int hot_gather(const dsa_unit* units, int32_t U, int32_t R, int32_t K
   cudaStream_t st = static_cast<cudaStream_t>(stream);
   GatherWs g = gather_ws(ws, U, R, K);
   const int RK = R * K;
-  k_classify<<<dim3((RK + CLS_THREADS - 1) / CLS_THREADS, U), CLS_THREADS, 0, st>>>(
-      units, R, K, round, topk_idx, cls, dev_err);
-  if (dsa_launch_status() != DSA_OK) return DSA_ERR_CUDA;
   k_assign<<<U, ASSIGN_THREADS, 0, st>>>(units, R, K, round, topk_idx, cls, counters, g, dev_err);
   if (dsa_launch_status() != DSA_OK) return DSA_ERR_CUDA;
   k_copy<<<dim3((2 * RK + COPY_WARPS - 1) / COPY_WARPS, U), COPY_THREADS, 0, st>>>(

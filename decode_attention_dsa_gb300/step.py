@@ -60,6 +60,6 @@ class DecodePath:
         self.append(new_rows, new_keys, stream)
 
     def launches_per_step(self) -> int:
-        """Kernel launches one step enqueues (score, select, classify, assign,
+        """Kernel launches one step enqueues (score, select, classify+assign,
         copy, attention, append)."""
-        return 7
+        return 6
