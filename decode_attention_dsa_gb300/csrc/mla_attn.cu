@@ -308,8 +308,11 @@ k_mla_attn(int R, int H, int K, const uint16_t* __restrict__ q_lat, const uint16
 
   // ---- this CTA's O (64 x 512 fp32) to its slot of the workspace (L2):
   //      warps 0,1,4,5 (lane quarters 0 and 1), 128 contiguous bytes per store run
-  //      each 32 x 32 block goes through a padded shared-memory transpose so
-  //      every store instruction writes four whole 128-byte rows
+  //      The slot is slice-major: the W = 512 / C columns that CTA c merges
+  //      form one contiguous [64][W] block, so the merge fetches each source's
+  //      block with one bulk copy. Each 32 x 32 block goes through a padded
+  //      shared-memory transpose so every store writes whole 128-byte rows.
+  const int W = 512 / C;                                 // C in {1, 2, 4, 8, 16}
   float* gO = ws_o + ((size_t)ur * MAX_CLUSTER + crank) * 64 * 512;
   if ((warp & 3) < 2 && !failed) {
     const int q = warp & 3;                              // lane quarter: head rows 32q..32q+31
@@ -322,11 +325,13 @@ k_mla_attn(int R, int H, int K, const uint16_t* __restrict__ q_lat, const uint16
       for (int i = 0; i < 8; ++i)
         reinterpret_cast<float4*>(tb + lane * 36)[i] = make_float4(v[4 * i], v[4 * i + 1], v[4 * i + 2], v[4 * i + 3]);
       __syncwarp();
+      const int col = c0 + 32 * c;                       // first column of the block
+      float* blk = gO + (size_t)(col / W) * 64 * W + (col % W);
 #pragma unroll
       for (int r4 = 0; r4 < 8; ++r4) {
         const int r = 4 * r4 + (lane >> 3);              // row within the block
         const float4 x = reinterpret_cast<const float4*>(tb + r * 36)[lane & 7];
-        reinterpret_cast<float4*>(gO + (32 * q + r) * 512 + c0 + 32 * c)[lane & 7] = x;
+        reinterpret_cast<float4*>(blk + (size_t)(32 * q + r) * W)[lane & 7] = x;
       }
       __syncwarp();
     }
@@ -335,16 +340,25 @@ k_mla_attn(int R, int H, int K, const uint16_t* __restrict__ q_lat, const uint16
     ms->m[tid] = -INFINITY;
     ms->l[tid] = 0.f;
   }
+  tc::fence_async_global();   // the partial stores are read by bulk copies
   tc::fence_before_sync();
   __syncthreads();
   cluster.sync();
+  tc::fence_async_global();
 
-  // ---- merge columns [c0, c1) of all C CTAs' outputs
+  // ---- merge columns [crank*W, crank*W + W) of all C CTAs' outputs: one
+  //      bulk copy per source brings its contiguous [64][W] block into Y
   {
-    const int W = ((512 / C) + 3) & ~3;
-    const int c0 = crank * W, c1 = min(512, c0 + W);
-    const int nq = max(0, (c1 - c0) / 4);
     MergeScratch* mg = reinterpret_cast<MergeScratch*>(sX);
+    float* buf = reinterpret_cast<float*>(sY);           // [C][64][W] = 128 KB
+    const uint32_t blk_bytes = 64u * (uint32_t)W * 4u;
+    if (tid == 0) {
+      tc::mbar_arrive_expect_tx(&ms->bar[0], blk_bytes * (uint32_t)C);
+      for (int c = 0; c < C; ++c)
+        tc::bulk_g2s(buf + (size_t)c * 64 * W,
+                     ws_o + (((size_t)ur * MAX_CLUSTER + c) * 64 * 512 + (size_t)crank * 64 * W), blk_bytes,
+                     &ms->bar[0]);
+    }
     // one round of remote loads: every source CTA's (m, l) for every head
     for (int t = tid; t < C * 64; t += THREADS) {
       const Misc* rm = cluster.map_shared_rank(ms, t >> 6);
@@ -365,32 +379,28 @@ k_mla_attn(int R, int H, int K, const uint16_t* __restrict__ q_lat, const uint16
       mg->inv[h] = L > 0.f ? 1.f / L : 0.f;
       if (crank == 0 && lse && h < H) lse[(size_t)ur * H + h] = L > 0.f ? M + logf(L) : -INFINITY;
     }
+    const bool got = tc::mbar_wait(&ms->bar[0], 1);    // second phase of the TMA barrier
+    if (!got) atomicOr(&ms->fail, 1);
     __syncthreads();
-    for (int t = tid; t < 64 * nq; t += THREADS) {
+    const int nq = W / 4;
+    for (int t = tid; t < 64 * nq && got; t += THREADS) {
       const int h = t / nq, q4 = t % nq;
       if (h >= H) continue;
-      const int d = c0 + 4 * q4;
-      float4 v[MAX_CLUSTER];
-#pragma unroll
-      for (int c = 0; c < MAX_CLUSTER; ++c)
-        if (c < C && mg->f[c][h] != 0.f)
-          v[c] = __ldcg(reinterpret_cast<const float4*>(
-              ws_o + (((size_t)ur * MAX_CLUSTER + c) * 64 + h) * 512 + d));
       float4 acc = make_float4(0.f, 0.f, 0.f, 0.f);
-#pragma unroll
-      for (int c = 0; c < MAX_CLUSTER; ++c) {
-        const float f = c < C ? mg->f[c][h] : 0.f;
-        if (f != 0.f) {   // skip empty sources (their staged O may be undefined)
-          acc.x = fmaf(f, v[c].x, acc.x);
-          acc.y = fmaf(f, v[c].y, acc.y);
-          acc.z = fmaf(f, v[c].z, acc.z);
-          acc.w = fmaf(f, v[c].w, acc.w);
-        }
+      for (int c = 0; c < C; ++c) {
+        const float f = mg->f[c][h];
+        if (f == 0.f) continue;   // skip empty sources (their blocks may be undefined)
+        const float4 v = reinterpret_cast<const float4*>(buf + ((size_t)c * 64 + h) * W)[q4];
+        acc.x = fmaf(f, v.x, acc.x);
+        acc.y = fmaf(f, v.y, acc.y);
+        acc.z = fmaf(f, v.z, acc.z);
+        acc.w = fmaf(f, v.w, acc.w);
       }
       const float inv = mg->inv[h];
-      *reinterpret_cast<float4*>(out + ((size_t)ur * H + h) * 512 + d) =
+      *reinterpret_cast<float4*>(out + ((size_t)ur * H + h) * 512 + crank * W + 4 * q4) =
           make_float4(acc.x * inv, acc.y * inv, acc.z * inv, acc.w * inv);
     }
+    failed = ms->fail != 0;
   }
   if (failed && tid == 0) dsa_flag(dev_err, DSA_DEVERR_TIMEOUT);
   tc::fence_before_sync();
