@@ -40,6 +40,7 @@ __global__ void __launch_bounds__(APP_THREADS)
 k_append(const dsa_unit* __restrict__ units, int A, const uint8_t* __restrict__ new_rows,
          const uint16_t* __restrict__ new_keys, int32_t* dev_err) {
   const int u = blockIdx.x;
+  pdl_wait();
   const dsa_unit& un = units[u];
   __shared__ int64_t s_len, s_ram;
   if (threadIdx.x == 0) {
@@ -201,9 +202,8 @@ extern "C" int kv_append_writeback(const dsa_unit* units, int32_t U, int32_t A,
                                    int32_t* dev_err, void* stream) {
   if (!units || !new_rows || !new_keys || U < 1 || U > 65535 || A < 1 || A > DSA_RING_ROWS)
     return DSA_ERR_ARG;
-  k_append<<<U, APP_THREADS, 0, static_cast<cudaStream_t>(stream)>>>(units, A, new_rows, new_keys,
-                                                                     dev_err);
-  return dsa_launch_status();
+  return launch_pdl(k_append, dim3(U), dim3(APP_THREADS), 0, static_cast<cudaStream_t>(stream), units, A,
+                    new_rows, new_keys, dev_err);
 }
 
 extern "C" int kv_flush(const dsa_unit* units, int32_t U, int32_t* dev_err, void* stream) {

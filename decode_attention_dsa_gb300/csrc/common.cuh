@@ -91,3 +91,25 @@ __device__ __forceinline__ int block_inclusive_scan(int v, int* tmp, int* total 
   __syncthreads();
   return v;
 }
+
+// Programmatic dependent launch. Every hot-path kernel is launched with
+// programmatic stream serialization, so it may start while the previous
+// kernel in the stream is still finishing; it must call pdl_wait() before it
+// reads or writes any global memory (inputs may come from that kernel).
+__device__ __forceinline__ void pdl_wait() { asm volatile("griddepcontrol.wait;" ::: "memory"); }
+
+template <typename... KArgs, typename... Args>
+static inline int launch_pdl(void (*kernel)(KArgs...), dim3 grid, dim3 block, size_t smem,
+                             cudaStream_t st, Args... args) {
+  cudaLaunchConfig_t cfg = {};
+  cfg.gridDim = grid;
+  cfg.blockDim = block;
+  cfg.dynamicSmemBytes = smem;
+  cfg.stream = st;
+  cudaLaunchAttribute attr[1];
+  attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+  attr[0].val.programmaticStreamSerializationAllowed = 1;
+  cfg.attrs = attr;
+  cfg.numAttrs = 1;
+  return cudaLaunchKernelEx(&cfg, kernel, args...) == cudaSuccess ? DSA_OK : DSA_ERR_CUDA;
+}

@@ -77,95 +77,73 @@ __device__ __forceinline__ int row_lower_bound(const int32_t* row, int K, int32_
   return lo;
 }
 
+// Shared working set of k_assign for R*K entries: the selected rows (when
+// they fit), classes, owner flags and per-row owner prefix counts.
+constexpr int ASSIGN_TK_SMEM_MAX = 16384;   // entries whose rows are kept in shared memory
+
+inline size_t assign_smem(int RK) {
+  return (size_t)RK * (1 + 1 + 2) + (RK <= ASSIGN_TK_SMEM_MAX ? (size_t)RK * 4 : 0) + 64;
+}
+
 __global__ void __launch_bounds__(ASSIGN_THREADS)
 k_assign(const dsa_unit* __restrict__ units, int R, int K, int round,
          const int32_t* __restrict__ topk_all, uint8_t* cls_all,
          int32_t* __restrict__ counters, GatherWs g, int32_t* dev_err) {
   __shared__ int s_tmp[32];
   __shared__ int s_cnt[4];
+  extern __shared__ __align__(16) uint8_t asm_[];
   const int u = blockIdx.x;
-  const dsa_unit& un = units[u];
   const int RK = R * K;
-  const int32_t* topk = topk_all + (size_t)u * RK;
-  uint8_t* cls = cls_all + (size_t)u * RK;   // written in phase 0, read after a barrier
+  const bool tk_in_smem = RK <= ASSIGN_TK_SMEM_MAX;
+  int32_t* s_tk = reinterpret_cast<int32_t*>(asm_);                          // [RK] if it fits
+  uint16_t* s_opc = reinterpret_cast<uint16_t*>(asm_ + (tk_in_smem ? (size_t)RK * 4 : 0));   // [RK]
+  uint8_t* s_cl = reinterpret_cast<uint8_t*>(s_opc + RK);                      // [RK]
+  uint8_t* s_fl = s_cl + RK;                                                   // [RK] owner flags
+  pdl_wait();
+  const dsa_unit& un = units[u];
+  const int32_t* gtopk = topk_all + (size_t)u * RK;
+  const int32_t* tk = tk_in_smem ? s_tk : gtopk;
+  uint8_t* cls = cls_all + (size_t)u * RK;
   int32_t* fill_pos = g.fill_pos + (size_t)u * RK;
   int32_t* fill_slot = g.fill_slot + (size_t)u * RK;
   int32_t* fill_entry = g.fill_entry + (size_t)u * RK;
-  int32_t* opc = g.opc + (size_t)u * RK;
   uint8_t* served = g.served + (size_t)u * RK;
   const int S = un.slots_n;
   const int32_t epoch = (int32_t)(un.state[DSA_ST_EPOCH] + 1);
   if (round < 0) round = epoch - 1;
-
-  if (threadIdx.x < 4) s_cnt[threadIdx.x] = 0;
+  const int64_t len = un.state[DSA_ST_LEN];
+  const int64_t ram = un.state[DSA_ST_RAM];
 
   // 0. classify every entry with the state as it is now, pinning HOT slots
-  //    (nothing is filled before the block barrier below, so no entry can see
-  //    a slot filled in this call)
-  {
-    const int64_t len = un.state[DSA_ST_LEN];
-    const int64_t ram = un.state[DSA_ST_RAM];
-    uint8_t* cls_w = cls;
-    for (int e = threadIdx.x; e < RK; e += ASSIGN_THREADS) {
-      const int32_t p = topk[e];
-      uint8_t c = DSA_CLS_PAD;
-      if (p >= 0) {
-        if (p >= len) {
-          dsa_flag(dev_err, DSA_DEVERR_BOUNDS);
-        } else if (p >= ram) {
-          c = DSA_CLS_RING;
-        } else {
-          const int32_t sl = un.pos_slot[p];
-          if (sl >= 0 && sl < S && un.fill_round[sl] < round) {
-            c = DSA_CLS_HOT;
-            un.pin_epoch[sl] = epoch;
-          } else {
-            c = DSA_CLS_RAM;
-          }
-        }
-      }
-      cls_w[e] = c;
-    }
-  }
-  __syncthreads();
-
-  // 1. counts, owner flags (first occurrence of an unmapped RAM position) and
-  //    the per-row exclusive prefix count of owners.
+  //    (nothing is filled before the block barriers below, so no entry can see
+  //    a slot filled in this call); flag RAM positions that hold no slot
   int hot = 0, ring = 0, rm = 0;
-  for (int r = 0; r < R; ++r) {
-    const int32_t* row = topk + (size_t)r * K;
-    const int per = (K + ASSIGN_THREADS - 1) / ASSIGN_THREADS;   // contiguous run per thread
-    const int j0 = threadIdx.x * per;
-    const int j1 = min(j0 + per, K);
-    int own = 0;
-    for (int j = j0; j < j1; ++j) {
-      const uint8_t c = cls[(size_t)r * K + j];
-      hot += c == DSA_CLS_HOT;
-      ring += c == DSA_CLS_RING;
-      rm += c == DSA_CLS_RAM;
-      bool owner = false;
-      if (c == DSA_CLS_RAM) {
-        const int32_t p = row[j];
-        if (un.pos_slot[p] < 0) {
-          owner = true;
-          for (int r2 = 0; r2 < r && owner; ++r2) {
-            const int32_t* o = topk + (size_t)r2 * K;
-            const int lb = row_lower_bound(o, K, p);
-            if (lb < K && o[lb] == p) owner = false;
-          }
+  for (int e = threadIdx.x; e < RK; e += ASSIGN_THREADS) {
+    const int32_t p = gtopk[e];
+    if (tk_in_smem) s_tk[e] = p;
+    uint8_t c = DSA_CLS_PAD, unmapped = 0;
+    if (p >= 0) {
+      if (p >= len) {
+        dsa_flag(dev_err, DSA_DEVERR_BOUNDS);
+      } else if (p >= ram) {
+        c = DSA_CLS_RING;
+      } else {
+        const int32_t sl = un.pos_slot[p];
+        if (sl >= 0 && sl < S && un.fill_round[sl] < round) {
+          c = DSA_CLS_HOT;
+          un.pin_epoch[sl] = epoch;
+        } else {
+          c = DSA_CLS_RAM;
+          unmapped = sl < 0;
         }
       }
-      served[(size_t)r * K + j] = owner ? 1 : 0;   // provisional: 1 = owner
-      own += owner;
     }
-    int tot;
-    const int inc = block_inclusive_scan<ASSIGN_THREADS>(own, s_tmp, &tot);
-    int run = inc - own;
-    for (int j = j0; j < j1; ++j) {
-      opc[(size_t)r * K + j] = run;
-      run += served[(size_t)r * K + j];
-    }
-    __syncthreads();
+    cls[e] = c;
+    s_cl[e] = c;
+    s_fl[e] = unmapped;
+    hot += c == DSA_CLS_HOT;
+    ring += c == DSA_CLS_RING;
+    rm += c == DSA_CLS_RAM;
   }
   {
     int t;
@@ -176,22 +154,53 @@ k_assign(const dsa_unit* __restrict__ units, int R, int K, int round,
     block_inclusive_scan<ASSIGN_THREADS>(rm, s_tmp, &t);
     if (threadIdx.x == 0) s_cnt[2] = t;
   }
+  // (the scans end with a block barrier: s_tk, s_cl, s_fl are complete)
+
+  // 1. owners: the first occurrence (lowest query row) of an unmapped RAM
+  //    position; per-row exclusive prefix counts of owners
+  if (R > 1) {
+    for (int e = threadIdx.x; e < RK; e += ASSIGN_THREADS) {
+      if (!s_fl[e]) continue;
+      const int r = e / K;
+      const int32_t p = tk[e];
+      for (int r2 = 0; r2 < r; ++r2) {
+        const int32_t* o = tk + (size_t)r2 * K;
+        const int lb = row_lower_bound(o, K, p);
+        if (lb < K && o[lb] == p) {
+          s_fl[e] = 0;
+          break;
+        }
+      }
+    }
+    __syncthreads();
+  }
+  const int per = (K + ASSIGN_THREADS - 1) / ASSIGN_THREADS;   // contiguous run per thread
+  for (int r = 0; r < R; ++r) {
+    const int j0 = min(threadIdx.x * per, K), j1 = min(j0 + per, K);
+    int own = 0;
+    for (int j = j0; j < j1; ++j) own += s_fl[r * K + j];
+    const int inc = block_inclusive_scan<ASSIGN_THREADS>(own, s_tmp);
+    int run = inc - own;
+    for (int j = j0; j < j1; ++j) {
+      s_opc[r * K + j] = (uint16_t)run;
+      run += s_fl[r * K + j];
+    }
+  }
   __syncthreads();
 
   // 2. rank of each owner among all owners (ascending position)
   int nM_local = 0;
   for (int e = threadIdx.x; e < RK; e += ASSIGN_THREADS) {
-    if (!served[e]) continue;
-    const int r = e / K, j = e % K;
-    const int32_t p = topk[e];
-    int rank = opc[e];
+    if (!s_fl[e]) continue;
+    const int r = e / K;
+    const int32_t p = tk[e];
+    int rank = s_opc[e];
     for (int r2 = 0; r2 < R; ++r2) {
       if (r2 == r) continue;
-      const int32_t* o = topk + (size_t)r2 * K;
+      const int32_t* o = tk + (size_t)r2 * K;
       const int lb = row_lower_bound(o, K, p);
-      rank += lb < K ? opc[(size_t)r2 * K + lb] : (opc[(size_t)r2 * K + K - 1] + served[(size_t)r2 * K + K - 1]);
+      rank += lb < K ? s_opc[r2 * K + lb] : (s_opc[r2 * K + K - 1] + s_fl[r2 * K + K - 1]);
     }
-    (void)j;
     if (rank < RK) {
       fill_pos[rank] = p;
       fill_entry[rank] = e;
@@ -199,7 +208,7 @@ k_assign(const dsa_unit* __restrict__ units, int R, int K, int round,
       for (int k = 0; k < DSA_MAX_ROWS - 1; ++k) dp[k] = -1;
       int nd = 0;
       for (int r2 = r + 1; r2 < R; ++r2) {
-        const int32_t* o = topk + (size_t)r2 * K;
+        const int32_t* o = tk + (size_t)r2 * K;
         const int lb = row_lower_bound(o, K, p);
         if (lb < K && o[lb] == p) dp[nd++] = r2 * K + lb;
       }
@@ -216,17 +225,17 @@ k_assign(const dsa_unit* __restrict__ units, int R, int K, int round,
   int found = 0;
   for (int base = 0; base < S && found < nM; base += ASSIGN_THREADS) {
     const int t = base + threadIdx.x;
-    int s = -1;
+    int sidx = -1;
     int elig = 0;
     if (t < S) {
-      s = hand0 + t;
-      if (s >= S) s -= S;
-      elig = (un.pin_epoch[s] != epoch) && (un.fill_round[s] < round);
+      sidx = hand0 + t;
+      if (sidx >= S) sidx -= S;
+      elig = (un.pin_epoch[sidx] != epoch) && (un.fill_round[sidx] < round);
     }
     int tot;
     const int inc = block_inclusive_scan<ASSIGN_THREADS>(elig, s_tmp, &tot);
     const int rank = found + inc - elig;
-    if (elig && rank < nM) fill_slot[rank] = s;
+    if (elig && rank < nM) fill_slot[rank] = sidx;
     found += tot;
   }
   const int n = min(found, nM);
@@ -235,24 +244,23 @@ k_assign(const dsa_unit* __restrict__ units, int R, int K, int round,
   // 4. map update (distinct slots, distinct new positions, and old positions
   //    that are neither new positions nor pinned: safe in parallel)
   for (int i = threadIdx.x; i < n; i += ASSIGN_THREADS) {
-    const int s = fill_slot[i];
+    const int sl = fill_slot[i];
     const int32_t p = fill_pos[i];
-    const int32_t old = un.slot_pos[s];
+    const int32_t old = un.slot_pos[sl];
     if (old >= 0 && old < un.lmax) un.pos_slot[old] = -1;
-    un.slot_pos[s] = p;
-    un.pos_slot[p] = s;
-    un.fill_round[s] = round;
+    un.slot_pos[sl] = p;
+    un.pos_slot[p] = sl;
+    un.fill_round[sl] = round;
   }
   // served[e] = 1 for owners that received a slot and for the later
   // occurrences of their position: the fill reads the mirror row once and
   // hands the same RAM bytes to every occurrence
-  for (int i = threadIdx.x; i < nM; i += ASSIGN_THREADS) {
-    if (i >= n) {
-      served[fill_entry[i]] = 0;
-    } else {
-      const int32_t* dp = g.dup + ((size_t)u * RK + i) * (DSA_MAX_ROWS - 1);
-      for (int k = 0; k < R - 1 && dp[k] >= 0; ++k) served[dp[k]] = 1;
-    }
+  for (int e = threadIdx.x; e < RK; e += ASSIGN_THREADS) served[e] = 0;
+  __syncthreads();
+  for (int i = threadIdx.x; i < n; i += ASSIGN_THREADS) {
+    served[fill_entry[i]] = 1;
+    const int32_t* dp = g.dup + ((size_t)u * RK + i) * (DSA_MAX_ROWS - 1);
+    for (int k = 0; k < R - 1 && dp[k] >= 0; ++k) served[dp[k]] = 1;
   }
   if (threadIdx.x == 0) {
     if (n > 0) {
@@ -275,6 +283,7 @@ k_copy(const dsa_unit* __restrict__ units, int R, int K, const int32_t* __restri
   const int u = blockIdx.y;
   const int lane = threadIdx.x & 31;
   const int item = blockIdx.x * COPY_WARPS + (threadIdx.x >> 5);
+  pdl_wait();
   const int RK = R * K;
   const dsa_unit& un = units[u];
   uint8_t* rows = rows_all + (size_t)u * RK * DSA_ROW_BYTES;
@@ -342,9 +351,15 @@ extern "C" int hot_gather(const dsa_unit* units, int32_t U, int32_t R, int32_t K
   cudaStream_t st = static_cast<cudaStream_t>(stream);
   GatherWs g = gather_ws(ws, U, R, K);
   const int RK = R * K;
-  k_assign<<<U, ASSIGN_THREADS, 0, st>>>(units, R, K, round, topk_idx, cls, counters, g, dev_err);
-  if (dsa_launch_status() != DSA_OK) return DSA_ERR_CUDA;
-  k_copy<<<dim3((2 * RK + COPY_WARPS - 1) / COPY_WARPS, U), COPY_THREADS, 0, st>>>(
-      units, R, K, topk_idx, cls, rows, g);
-  return dsa_launch_status();
+  static bool attr_done = false;
+  if (!attr_done) {
+    DSA_CUDA_TRY(cudaFuncSetAttribute(k_assign, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                      (int)assign_smem(DSA_MAX_ROWS * DSA_MAX_K)));
+    attr_done = true;
+  }
+  if (launch_pdl(k_assign, dim3(U), dim3(ASSIGN_THREADS), assign_smem(RK), st, units, R, K, round, topk_idx, cls,
+                 counters, g, dev_err) != DSA_OK)
+    return DSA_ERR_CUDA;
+  return launch_pdl(k_copy, dim3((2 * RK + COPY_WARPS - 1) / COPY_WARPS, U), dim3(COPY_THREADS), 0, st, units, R,
+                    K, topk_idx, cls, rows, g);
 }

@@ -122,6 +122,7 @@ k_mla_attn(int R, int H, int K, const uint16_t* __restrict__ q_lat, const uint16
   tc::fence_after_sync();
   const uint32_t tmem = ms->tmem;
   bool failed = ms->fail != 0;
+  pdl_wait();   // everything above touched only this CTA's shared and tensor memory
 
   if (tid == 0 && !failed && nrows > 0) {
     const uint32_t bytes = (uint32_t)nrows * DSA_ROW_BYTES;
@@ -437,13 +438,15 @@ extern "C" int mla_decode_attn(int32_t U, int32_t R, int32_t H, int32_t K, const
   cfg.blockDim = dim3(THREADS, 1, 1);
   cfg.dynamicSmemBytes = SMEM_BYTES;
   cfg.stream = static_cast<cudaStream_t>(stream);
-  cudaLaunchAttribute attr[1];
+  cudaLaunchAttribute attr[2];
   attr[0].id = cudaLaunchAttributeClusterDimension;
   attr[0].val.clusterDim.x = C;
   attr[0].val.clusterDim.y = 1;
   attr[0].val.clusterDim.z = 1;
+  attr[1].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+  attr[1].val.programmaticStreamSerializationAllowed = 1;
   cfg.attrs = attr;
-  cfg.numAttrs = 1;
+  cfg.numAttrs = 2;
   if (cudaLaunchKernelEx(&cfg, k_mla_attn, (int)R, (int)H, (int)K, q_lat, q_rope, rows, topk_idx, scale,
                          out, lse, static_cast<float*>(ws), dev_err) != cudaSuccess)
     return DSA_ERR_CUDA;

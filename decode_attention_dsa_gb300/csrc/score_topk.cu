@@ -157,6 +157,8 @@ __global__ void __launch_bounds__(SCORE_THREADS, 4) k_dsa_score(ScoreArgs a) {
   __shared__ int s_ntv[UCACHE];               // valid tiles of the unit (0 if L <= K)
   __shared__ int s_len[UCACHE];
   __shared__ const uint16_t* s_keys[UCACHE];
+  for (int i = tid; i < R * HIST1_BINS; i += SCORE_THREADS) hs[i] = 0;
+  pdl_wait();
   if (tid < UCACHE) {
     const int u = u0 + tid;
     s_ntv[tid] = 0;
@@ -172,7 +174,6 @@ __global__ void __launch_bounds__(SCORE_THREADS, 4) k_dsa_score(ScoreArgs a) {
     tc::mbar_init(&bar[1], 1);
     tc::fence_mbar_init();
   }
-  for (int i = tid; i < R * HIST1_BINS; i += SCORE_THREADS) hs[i] = 0;
   __syncthreads();
 
   // walk the tile list: index k in [0, ntiles) -> (unit, tile); a tile is
@@ -386,6 +387,7 @@ k_topk_select(const dsa_unit* __restrict__ units, int R, int K, uint32_t* __rest
   const int crank = (int)cluster.block_rank();
   const int ur = blockIdx.y;
   const int u = ur / R;
+  pdl_wait();
   const int64_t Lu = units[u].state[DSA_ST_LEN];
   const int64_t L = min(Lu, max_len);
   if (Lu > max_len && crank == 0 && threadIdx.x == 0) dsa_flag(dev_err, DSA_DEVERR_BOUNDS);
@@ -670,12 +672,11 @@ extern "C" int dsa_score_topk(const dsa_unit* units, int32_t U, int32_t R, int32
     a.TP = TP;
     const int per_sm = (int)std::max<size_t>(1, std::min<size_t>(4, 232448 / (score_smem(R) + 1024)));
     const int64_t grid = std::min<int64_t>(tpu * U, (int64_t)per_sm * (g_num_sms > 0 ? g_num_sms : 148));
-    k_dsa_score<<<(unsigned)grid, SCORE_THREADS, score_smem(R), st>>>(a);
-    if (dsa_launch_status() != DSA_OK) return DSA_ERR_CUDA;
+    if (launch_pdl(k_dsa_score, dim3((unsigned)grid), dim3(SCORE_THREADS), score_smem(R), st, a) != DSA_OK)
+      return DSA_ERR_CUDA;
   }
-  k_topk_select<<<dim3(SEL_CLUSTER, U * R), SEL_THREADS, select_smem(), st>>>(
-      units, R, K, tw.hist, tw.keys, tw.stride, topk_idx, max_len, dev_err);
-  return dsa_launch_status();
+  return launch_pdl(k_topk_select, dim3(SEL_CLUSTER, U * R), dim3(SEL_THREADS), select_smem(), st, units, R,
+                    K, tw.hist, tw.keys, tw.stride, topk_idx, max_len, dev_err);
 }
 
 // ---------------------------------------------------------------------------
