@@ -42,6 +42,10 @@ k_append(const dsa_unit* __restrict__ units, int A, const uint8_t* __restrict__ 
   const int u = blockIdx.x;
   pdl_wait();
   const dsa_unit& un = units[u];
+  if (!unit_aligned(un)) {
+    if (threadIdx.x == 0) dsa_flag(dev_err, DSA_DEVERR_BOUNDS);
+    return;
+  }
   __shared__ int64_t s_len, s_ram;
   if (threadIdx.x == 0) {
     s_len = un.state[DSA_ST_LEN];
@@ -81,6 +85,7 @@ k_append(const dsa_unit* __restrict__ units, int A, const uint8_t* __restrict__ 
 __global__ void __launch_bounds__(APP_THREADS) k_flush(const dsa_unit* __restrict__ units) {
   const int u = blockIdx.x;
   const dsa_unit& un = units[u];
+  if (!unit_aligned(un)) return;
   const int64_t len = un.state[DSA_ST_LEN];
   const int64_t ram = un.state[DSA_ST_RAM];
   if (len <= ram) return;
@@ -129,7 +134,7 @@ k_init_slots(const dsa_unit* __restrict__ units, int warm, const int64_t* __rest
   const int64_t i = (int64_t)blockIdx.x * (INIT_THREADS / 32) + (threadIdx.x >> 5);
   const int64_t l0 = l0v[u];
   const int S = un.slots_n;
-  if (warm != DSA_WARM_LAST_S || l0 < 0 || l0 > un.lmax || S < 1) return;
+  if (warm != DSA_WARM_LAST_S || l0 < 0 || l0 > un.lmax || S < 1 || !unit_aligned(un)) return;
   const int64_t n = min((int64_t)S, l0);
   if (i >= n) return;
   warp_copy_row(un.slots + i * DSA_ROW_BYTES, un.mirror + (l0 - n + i) * DSA_ROW_BYTES,

@@ -113,3 +113,11 @@ static inline int launch_pdl(void (*kernel)(KArgs...), dim3 grid, dim3 block, si
   cfg.numAttrs = 1;
   return cudaLaunchKernelEx(&cfg, kernel, args...) == cudaSuccess ? DSA_OK : DSA_ERR_CUDA;
 }
+
+// The row and key arrays of a unit are moved with 16-byte vector loads and
+// bulk copies; a unit whose arrays are not 16-byte aligned is skipped.
+__device__ __forceinline__ bool unit_aligned(const dsa_unit& un) {
+  const uintptr_t a = reinterpret_cast<uintptr_t>(un.keys) | reinterpret_cast<uintptr_t>(un.slots) |
+                      reinterpret_cast<uintptr_t>(un.ring) | reinterpret_cast<uintptr_t>(un.mirror);
+  return (a & 15u) == 0;
+}

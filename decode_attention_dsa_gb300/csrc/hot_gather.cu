@@ -101,6 +101,17 @@ k_assign(const dsa_unit* __restrict__ units, int R, int K, int round,
   uint8_t* s_fl = s_cl + RK;                                                   // [RK] owner flags
   pdl_wait();
   const dsa_unit& un = units[u];
+  if (!unit_aligned(un)) {
+    if (threadIdx.x == 0) {
+      dsa_flag(dev_err, DSA_DEVERR_BOUNDS);
+      g.nfill[u] = 0;
+    }
+    for (int e = threadIdx.x; e < RK; e += ASSIGN_THREADS) {
+      cls_all[(size_t)u * RK + e] = DSA_CLS_PAD;
+      g.served[(size_t)u * RK + e] = 1;   // nothing for k_copy to read
+    }
+    return;
+  }
   const int32_t* gtopk = topk_all + (size_t)u * RK;
   const int32_t* tk = tk_in_smem ? s_tk : gtopk;
   uint8_t* cls = cls_all + (size_t)u * RK;
@@ -117,33 +128,55 @@ k_assign(const dsa_unit* __restrict__ units, int R, int K, int round,
   // 0. classify every entry with the state as it is now, pinning HOT slots
   //    (nothing is filled before the block barriers below, so no entry can see
   //    a slot filled in this call); flag RAM positions that hold no slot
+  // batches of CB entries per thread: the three dependent lookups of an
+  // entry (position -> slot -> fill round) are issued for the whole batch at
+  // once, so a thread waits three memory latencies per batch, not per entry
   int hot = 0, ring = 0, rm = 0;
-  for (int e = threadIdx.x; e < RK; e += ASSIGN_THREADS) {
-    const int32_t p = gtopk[e];
-    if (tk_in_smem) s_tk[e] = p;
-    uint8_t c = DSA_CLS_PAD, unmapped = 0;
-    if (p >= 0) {
-      if (p >= len) {
-        dsa_flag(dev_err, DSA_DEVERR_BOUNDS);
-      } else if (p >= ram) {
-        c = DSA_CLS_RING;
-      } else {
-        const int32_t sl = un.pos_slot[p];
-        if (sl >= 0 && sl < S && un.fill_round[sl] < round) {
-          c = DSA_CLS_HOT;
-          un.pin_epoch[sl] = epoch;
+  constexpr int CB = 8;
+  for (int e0 = threadIdx.x; e0 < RK; e0 += CB * ASSIGN_THREADS) {
+    int32_t pv[CB], sv[CB], fv[CB];
+#pragma unroll
+    for (int b = 0; b < CB; ++b) {
+      const int e = e0 + b * ASSIGN_THREADS;
+      pv[b] = e < RK ? gtopk[e] : -1;
+    }
+#pragma unroll
+    for (int b = 0; b < CB; ++b) {
+      const int32_t p = pv[b];
+      sv[b] = (p >= 0 && p < ram) ? un.pos_slot[p] : -1;
+    }
+#pragma unroll
+    for (int b = 0; b < CB; ++b) fv[b] = (sv[b] >= 0 && sv[b] < S) ? un.fill_round[sv[b]] : 0;
+#pragma unroll
+    for (int b = 0; b < CB; ++b) {
+      const int e = e0 + b * ASSIGN_THREADS;
+      if (e >= RK) break;
+      const int32_t p = pv[b];
+      if (tk_in_smem) s_tk[e] = p;
+      uint8_t c = DSA_CLS_PAD, unmapped = 0;
+      if (p >= 0) {
+        if (p >= len) {
+          dsa_flag(dev_err, DSA_DEVERR_BOUNDS);
+        } else if (p >= ram) {
+          c = DSA_CLS_RING;
         } else {
-          c = DSA_CLS_RAM;
-          unmapped = sl < 0;
+          const int32_t sl = sv[b];
+          if (sl >= 0 && sl < S && fv[b] < round) {
+            c = DSA_CLS_HOT;
+            un.pin_epoch[sl] = epoch;
+          } else {
+            c = DSA_CLS_RAM;
+            unmapped = sl < 0;
+          }
         }
       }
+      cls[e] = c;
+      s_cl[e] = c;
+      s_fl[e] = unmapped;
+      hot += c == DSA_CLS_HOT;
+      ring += c == DSA_CLS_RING;
+      rm += c == DSA_CLS_RAM;
     }
-    cls[e] = c;
-    s_cl[e] = c;
-    s_fl[e] = unmapped;
-    hot += c == DSA_CLS_HOT;
-    ring += c == DSA_CLS_RING;
-    rm += c == DSA_CLS_RAM;
   }
   {
     int t;
@@ -205,7 +238,7 @@ k_assign(const dsa_unit* __restrict__ units, int R, int K, int round,
       fill_pos[rank] = p;
       fill_entry[rank] = e;
       int32_t* dp = g.dup + ((size_t)u * RK + rank) * (DSA_MAX_ROWS - 1);
-      for (int k = 0; k < DSA_MAX_ROWS - 1; ++k) dp[k] = -1;
+      for (int k = 0; k < R - 1; ++k) dp[k] = -1;     // only the first R - 1 are ever read
       int nd = 0;
       for (int r2 = r + 1; r2 < R; ++r2) {
         const int32_t* o = tk + (size_t)r2 * K;

@@ -426,6 +426,8 @@ extern "C" int mla_decode_attn(int32_t U, int32_t R, int32_t H, int32_t K, const
   if (K < 1 || K > NC * MAX_CLUSTER || H < 16 || H > 64 || (H % 16) != 0) return DSA_ERR_SHAPE;
   if ((size_t)U * R > 65535) return DSA_ERR_ARG;
   if (!ws || ws_bytes < mla_decode_attn_workspace(U, R, H, K)) return DSA_ERR_WS;
+  // rows and the workspace are read by bulk copies: 16-byte alignment
+  if ((reinterpret_cast<uintptr_t>(rows) | reinterpret_cast<uintptr_t>(ws)) & 15u) return DSA_ERR_ARG;
   static bool attr_done = false;
   if (!attr_done) {
     DSA_CUDA_TRY(cudaFuncSetAttribute(k_mla_attn, cudaFuncAttributeMaxDynamicSharedMemorySize, SMEM_BYTES));

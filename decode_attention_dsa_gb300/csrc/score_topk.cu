@@ -128,6 +128,7 @@ struct ScoreArgs {
   int tpu;              // tiles per unit
   int U;
   int R, K, TP;
+  int32_t* dev_err;
 };
 
 // One lane per history position. The fp32 key tile holds 16 four-float
@@ -164,9 +165,11 @@ __global__ void __launch_bounds__(SCORE_THREADS, 4) k_dsa_score(ScoreArgs a) {
     s_ntv[tid] = 0;
     if (u < a.U && (long long)(u - u0) * a.tpu <= (long long)t0 + ntiles) {
       const int64_t L = min(a.units[u].state[DSA_ST_LEN], a.max_len);
+      const bool ok = unit_aligned(a.units[u]);
       s_len[tid] = (int)L;
       s_keys[tid] = a.units[u].keys;
-      s_ntv[tid] = L > a.K ? (int)((L + TP - 1) / TP) : 0;
+      s_ntv[tid] = (L > a.K && ok) ? (int)((L + TP - 1) / TP) : 0;
+      if (!ok) dsa_flag(a.dev_err, DSA_DEVERR_BOUNDS);
     }
   }
   if (tid == 0) {
@@ -200,7 +203,7 @@ __global__ void __launch_bounds__(SCORE_THREADS, 4) k_dsa_score(ScoreArgs a) {
       ntv = s_ntv[i];
     } else {
       const int L = unit_len(u);
-      ntv = L > a.K ? (L + TP - 1) / TP : 0;
+      ntv = (L > a.K && unit_aligned(a.units[u])) ? (L + TP - 1) / TP : 0;
     }
     return t < ntv;
   };
@@ -375,9 +378,13 @@ struct SelShared {
   int bin, above;
   int ncand, overflow;
   int any_over;               // some CTA of the cluster overflowed
+  uint64_t kbar;              // bulk copy of this CTA's key range
   int coff[SEL_CLUSTER + 1];  // candidate offsets of the cluster's CTAs
   long long cnt[2];           // this CTA's (gt, eq) counts
 };
+// The key cache (a bulk-copy destination) starts 128-byte aligned after it.
+constexpr size_t SEL_KC_OFF = (sizeof(SelShared) + 127) / 128 * 128;
+static_assert(SEL_KC_OFF % 16 == 0 && SEL_KC_OFF >= sizeof(SelShared), "bulk-copy destination alignment");
 
 __global__ void __cluster_dims__(SEL_CLUSTER, 1, 1) __launch_bounds__(SEL_THREADS, 1)
 k_topk_select(const dsa_unit* __restrict__ units, int R, int K, uint32_t* __restrict__ hist,
@@ -388,6 +395,7 @@ k_topk_select(const dsa_unit* __restrict__ units, int R, int K, uint32_t* __rest
   const int ur = blockIdx.y;
   const int u = ur / R;
   pdl_wait();
+  tc::fence_async_global();   // score keys are read by bulk copies below
   const int64_t Lu = units[u].state[DSA_ST_LEN];
   const int64_t L = min(Lu, max_len);
   if (Lu > max_len && crank == 0 && threadIdx.x == 0) dsa_flag(dev_err, DSA_DEVERR_BOUNDS);
@@ -399,17 +407,33 @@ k_topk_select(const dsa_unit* __restrict__ units, int R, int K, uint32_t* __rest
     return;
   }
 
-  extern __shared__ __align__(16) uint8_t smem_sel[];
+  extern __shared__ __align__(128) uint8_t smem_sel[];
   SelShared* S = reinterpret_cast<SelShared*>(smem_sel);
-  uint32_t* kc = reinterpret_cast<uint32_t*>(smem_sel + sizeof(SelShared));   // [SEL_KEY_CACHE]
+  uint32_t* kc = reinterpret_cast<uint32_t*>(smem_sel + SEL_KC_OFF);          // [SEL_KEY_CACHE]
   uint32_t* cand = kc + SEL_KEY_CACHE;                                        // [SEL_CAND_CAP]
   uint32_t* allc = cand + SEL_CAND_CAP;                                       // [SEL_ALL_CAP]
   const int tid = threadIdx.x;
+  // this CTA's key range, a multiple of 4 keys (16-byte aligned bulk copies)
+  const int64_t chunk = ((L + SEL_CLUSTER - 1) / SEL_CLUSTER + 3) / 4 * 4;
+  const int64_t beg = min((int64_t)crank * chunk, L);
+  const int64_t end = min(beg + chunk, L);
+  const uint32_t* kk = okeys + (size_t)ur * stride;
+  const bool cached = (end - beg) + 4 <= SEL_KEY_CACHE;
   if (tid == 0) {
     S->bin = 0;
     S->above = 0;
     S->ncand = 0;
     S->overflow = 0;
+    tc::mbar_init(&S->kbar, 1);
+    tc::fence_mbar_init();
+    if (cached && end > beg && (tc::smem_u32(kc) & 15u) == 0 &&
+        ((reinterpret_cast<uintptr_t>(kk + beg)) & 15u) == 0) {
+      // the keys were written by k_dsa_score; the bulk copy reads them through
+      // the async proxy (rounded up to 16 bytes: the rows are padded to 4 keys)
+      const uint32_t bytes = (uint32_t)(((end - beg) * 4 + 15) / 16 * 16);
+      tc::mbar_arrive_expect_tx(&S->kbar, bytes);
+      tc::bulk_g2s(kc, kk + beg, bytes, &S->kbar);
+    }
   }
 
   // ---- level 1: top 12 bits from the global histogram
@@ -421,19 +445,17 @@ k_topk_select(const dsa_unit* __restrict__ units, int R, int K, uint32_t* __rest
   const uint32_t b1 = (uint32_t)S->bin;
   int need = K - S->above;
 
-  const int64_t chunk = (L + SEL_CLUSTER - 1) / SEL_CLUSTER;
-  const int64_t beg = min((int64_t)crank * chunk, L);
-  const int64_t end = min(beg + chunk, L);
-  const uint32_t* kk = okeys + (size_t)ur * stride;
-  const bool cached = (end - beg) <= SEL_KEY_CACHE;
   auto key_at = [&](int64_t p) -> uint32_t { return cached ? kc[p - beg] : kk[p]; };
 
   // ---- one pass: cache keys, count keys above b1, collect candidates in b1
-  if (cached) {
-    const int64_t n = end - beg;
-#pragma unroll 4
-    for (int64_t i = tid; i < n; i += SEL_THREADS) kc[i] = kk[beg + i];
-    __syncthreads();
+  if (cached && end > beg) {
+    if ((tc::smem_u32(kc) & 15u) != 0 || ((reinterpret_cast<uintptr_t>(kk + beg)) & 15u) != 0) {
+      // no bulk copy was issued: stage the keys with plain loads
+      for (int64_t i = tid; i < end - beg; i += SEL_THREADS) kc[i] = kk[beg + i];
+      __syncthreads();
+    } else if (!tc::mbar_wait(&S->kbar, 0)) {
+      dsa_flag(dev_err, DSA_DEVERR_TIMEOUT);
+    }
   }
   long long gt1 = 0;
   for (int64_t p = beg + tid; p < end; p += SEL_THREADS) {
@@ -617,7 +639,7 @@ k_topk_select(const dsa_unit* __restrict__ units, int R, int K, uint32_t* __rest
 }
 
 inline size_t select_smem() {
-  return sizeof(SelShared) + (size_t)(SEL_KEY_CACHE + SEL_CAND_CAP + SEL_ALL_CAP) * 4;
+  return SEL_KC_OFF + (size_t)(SEL_KEY_CACHE + SEL_CAND_CAP + SEL_ALL_CAP) * 4;
 }
 
 int g_num_sms = 0;
@@ -670,6 +692,7 @@ extern "C" int dsa_score_topk(const dsa_unit* units, int32_t U, int32_t R, int32
     a.R = R;
     a.K = K;
     a.TP = TP;
+    a.dev_err = dev_err;
     const int per_sm = (int)std::max<size_t>(1, std::min<size_t>(4, 232448 / (score_smem(R) + 1024)));
     const int64_t grid = std::min<int64_t>(tpu * U, (int64_t)per_sm * (g_num_sms > 0 ? g_num_sms : 148));
     if (launch_pdl(k_dsa_score, dim3((unsigned)grid), dim3(SCORE_THREADS), score_smem(R), st, a) != DSA_OK)

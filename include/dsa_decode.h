@@ -102,7 +102,8 @@ extern "C" {
  *   state      i64  [8]          DSA_ST_* words.
  *   slots_n    S (>= 1).
  *   lmax       capacity in positions (history + all appends).
- * 16-byte alignment is required for keys, slots, ring and mirror.
+ * 16-byte alignment is required for keys, slots, ring and mirror: a unit
+ * that breaks it is skipped by every kernel and sets DSA_DEVERR_BOUNDS.
  */
 typedef struct dsa_unit {
   uint16_t* keys;
@@ -277,7 +278,9 @@ int hot_gather(const dsa_unit* units, int32_t U, int32_t R, int32_t K,
  *           The tensor-core operands are fp16 with fp32 accumulation: |q| and
  *           |int8 * scale| must stay below 65504, else DSA_DEVERR_QRANGE is
  *           set. Each operand is rounded once to fp16 (relative error <= 2^-11).
- *   rows    device u8 [U][R][K][656] (hot_gather's output).
+ *   rows    device u8 [U][R][K][656] (hot_gather's output), 16-byte aligned;
+ *           the workspace too (both are read with bulk copies; otherwise
+ *           DSA_ERR_ARG).
  *   topk_idx device int32 [U][R][K] (only the sign is used: -1 = padding).
  *   out     device float [U][R][H][512];  lse device float [U][R][H] or NULL.
  *   ws      device workspace of mla_decode_attn_workspace(U, R, H, K) bytes:
