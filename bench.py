@@ -262,9 +262,13 @@ def run_gpu(args, rank: int, world: int):
     use_graph = not args.no_graph
     rnd = abi.ROUND_AUTO
 
+    side = torch.cuda.Stream()
+
     def record_steps(nsteps, per_call, ctr_acc=None):
         """Enqueue nsteps timed steps; returns the events. per_call adds
-        events between the four calls (a separate breakdown run)."""
+        events between the four calls and runs them one after another (a
+        separate breakdown run); otherwise the append runs on a side stream
+        concurrently with the attention, as the API allows."""
         nev = 5 if per_call else 2
         ev = [[torch.cuda.Event(enable_timing=True, external=use_graph) for _ in range(nev)]
               for _ in range(nsteps)]
@@ -274,16 +278,16 @@ def run_gpu(args, rank: int, world: int):
             flush.fill_(i & 0xFF)
             e = ev[i]
             e[0].record()
-            path.score_topk(qi, w)
             if per_call:
+                path.score_topk(qi, w)
                 e[1].record()
-            path.gather(rnd)
-            if per_call:
+                path.gather(rnd)
                 e[2].record()
-            path.attend(ql, qr)
-            if per_call:
+                path.attend(ql, qr)
                 e[3].record()
-            path.append(nr, nk)
+                path.append(nr, nk)
+            else:
+                path.step(rnd, qi, w, ql, qr, nr, nk, side=side)
             e[-1].record()
             if ctr_acc is not None:
                 ctr_acc.add_(path.counters)
@@ -372,7 +376,7 @@ def run_gpu(args, rank: int, world: int):
                 for n in names:
                     dev_in[n].copy_(host[n][i], non_blocking=True)
                 path.step(abi.ROUND_AUTO, dev_in["q_idx"], dev_in["w"], dev_in["q_lat"],
-                          dev_in["q_rope"], dev_in["new_rows"], dev_in["new_keys"])
+                          dev_in["q_rope"], dev_in["new_rows"], dev_in["new_keys"], side=side)
                 out_host[i].copy_(path.out, non_blocking=True)
                 ee[i][1].record()
         if use_graph:

@@ -53,11 +53,20 @@ class DecodePath:
         u = self.u
         abi.kv_append_writeback(u.units, u.U, self.A, new_rows, new_keys, u.dev_err, stream)
 
-    def step(self, rnd, q_idx, w, q_lat, q_rope, new_rows, new_keys, stream=None):
+    def step(self, rnd, q_idx, w, q_lat, q_rope, new_rows, new_keys, stream=None, side=None):
+        """One decode step. With a ``side`` stream, the append runs there,
+        concurrently with the attention (allowed once the gather is done)."""
         self.score_topk(q_idx, w, stream)
         self.gather(rnd, stream)
-        self.attend(q_lat, q_rope, stream)
-        self.append(new_rows, new_keys, stream)
+        if side is None:
+            self.attend(q_lat, q_rope, stream)
+            self.append(new_rows, new_keys, stream)
+            return
+        main = stream if stream is not None else torch.cuda.current_stream()
+        side.wait_stream(main)
+        self.append(new_rows, new_keys, side)
+        self.attend(q_lat, q_rope, main)
+        main.wait_stream(side)
 
     def launches_per_step(self) -> int:
         """Kernel launches one step enqueues (score, select, classify+assign,

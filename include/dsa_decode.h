@@ -312,6 +312,10 @@ int mla_decode_attn(int32_t U, int32_t R, int32_t H, int32_t K,
  * An append with p >= lmax sets DSA_DEVERR_CAPACITY and is dropped.
  *   new_rows device u8 [U][A][656];  new_keys device bf16 [U][A][64].
  * Shapes: 1 <= U, 1 <= A <= 64.
+ * Ordering: it must follow the step's hot_gather (which reads LEN and RAM),
+ * and may run concurrently with the step's mla_decode_attn (on another
+ * stream): it writes only the ring row and key of position LEN and mirror
+ * rows >= RAM, none of which this step's gathered rows came from.
  */
 int kv_append_writeback(const dsa_unit* units, int32_t U, int32_t A,
                         const uint8_t* new_rows, const uint16_t* new_keys,

@@ -69,18 +69,24 @@ class Pair:
             new_keys=t16([x.new_keys for x in per]),
         )
 
-    def step(self, step, rnd=None, attention=True, oracle_rnd=None):
-        """Run one step on both sides; return (gpu dict, oracle dict per unit)."""
+    def step(self, step, rnd=None, attention=True, oracle_rnd=None, side=None):
+        """Run one step on both sides; return (gpu dict, oracle dict per unit).
+        With a ``side`` stream the append runs there, concurrently with the
+        attention."""
         rnd = step if rnd is None else rnd
         ornd = rnd if oracle_rnd is None else oracle_rnd
         per, t = self.inputs(step)
         self.last_inputs = per
         p = self.p
-        p.score_topk(t["q_idx"], t["w"])
-        p.gather(rnd)
-        if attention:
-            p.attend(t["q_lat"], t["q_rope"])
-        p.append(t["new_rows"], t["new_keys"])
+        if side is not None:
+            assert attention
+            p.step(rnd, t["q_idx"], t["w"], t["q_lat"], t["q_rope"], t["new_rows"], t["new_keys"], side=side)
+        else:
+            p.score_topk(t["q_idx"], t["w"])
+            p.gather(rnd)
+            if attention:
+                p.attend(t["q_lat"], t["q_rope"])
+            p.append(t["new_rows"], t["new_keys"])
         self.torch.cuda.synchronize()
         g = dict(topk=p.topk.cpu().numpy(), cls=p.cls.cpu().numpy(), counters=p.counters.cpu().numpy())
         if attention:

@@ -19,15 +19,17 @@ def _need_gpu():
 
 
 def run(wl, steps=None, rnds=None, mirror="host", check_every=1, attention_every=1,
-        full_state=True, units=None, oracle_units=None, oracle_rnds=None, gpu_gen=False):
+        full_state=True, units=None, oracle_units=None, oracle_rnds=None, gpu_gen=False,
+        side_stream=False):
     pair = Pair(wl, units=units, mirror=mirror, oracle_units=oracle_units, gpu_gen=gpu_gen)
+    side = pair.torch.cuda.Stream() if side_stream else None
     steps = range(wl.steps) if steps is None else steps
     worst = 0.0
     for k, st in enumerate(steps):
         rnd = None if rnds is None else rnds[k]
         ornd = None if oracle_rnds is None else oracle_rnds[k]
         att = (k % attention_every) == 0 or k == len(steps) - 1
-        g, o = pair.step(st, rnd=rnd, attention=att, oracle_rnd=ornd)
+        g, o = pair.step(st, rnd=rnd, attention=att or side is not None, oracle_rnd=ornd, side=side)
         if (k % check_every) == 0 or k == len(steps) - 1:
             worst = max(worst, check_step(pair, g, o, attention=att, full_state=full_state))
         assert pair.g.check() == 0, f"device error word {pair.g.check():#x}"
@@ -78,6 +80,13 @@ def test_round_auto_matches_explicit_rounds():
     """hot_gather with DSA_ROUND_AUTO uses the call count as the round."""
     wl = W.WORKLOADS[0].with_(name="auto", L0=900, S=48, K=64, H=16, steps=12, warm="empty")
     run(wl, rnds=[-1] * 12, oracle_rnds=list(range(12)))
+
+
+def test_append_concurrent_with_attention():
+    """The append on a side stream, concurrent with the attention, across
+    several 64-row write-backs: results identical to the serial order."""
+    wl = W.WORKLOADS[0].with_(name="side", L0=700, S=48, K=64, H=16, steps=140, A=1, warm="last_s")
+    run(wl, side_stream=True)
 
 
 def test_resident_mirror_same_results():
