@@ -54,6 +54,9 @@ def parse():
     ap.add_argument("--impl", choices=["gb300", "reference"], default="gb300")
     ap.add_argument("--no-e2e", action="store_true")
     ap.add_argument("--no-graph", action="store_true", help="launch steps directly, no CUDA graph")
+    ap.add_argument("--path", choices=["fused", "split"], default=None,
+                    help="fused: hot_gather_attn; split: hot_gather + mla_decode_attn with the append "
+                         "overlapping the attention (default: split, the faster one measured)")
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--cpu-sample-steps", type=int, default=None)
     ap.add_argument("--oracle-child", type=str, default=None, help=argparse.SUPPRESS)
@@ -263,6 +266,7 @@ def run_gpu(args, rank: int, world: int):
     rnd = abi.ROUND_AUTO
 
     side = torch.cuda.Stream()
+    fused = args.path == "fused"
 
     def record_steps(nsteps, per_call, ctr_acc=None):
         """Enqueue nsteps timed steps; returns the events. per_call adds
@@ -286,6 +290,8 @@ def run_gpu(args, rank: int, world: int):
                 path.attend(ql, qr)
                 e[3].record()
                 path.append(nr, nk)
+            elif fused:
+                path.step(rnd, qi, w, ql, qr, nr, nk, fused=True)
             else:
                 path.step(rnd, qi, w, ql, qr, nr, nk, side=side)
             e[-1].record()
@@ -376,7 +382,7 @@ def run_gpu(args, rank: int, world: int):
                 for n in names:
                     dev_in[n].copy_(host[n][i], non_blocking=True)
                 path.step(abi.ROUND_AUTO, dev_in["q_idx"], dev_in["w"], dev_in["q_lat"],
-                          dev_in["q_rope"], dev_in["new_rows"], dev_in["new_keys"], side=side)
+                          dev_in["q_rope"], dev_in["new_rows"], dev_in["new_keys"], side=side, fused=fused)
                 out_host[i].copy_(path.out, non_blocking=True)
                 ee[i][1].record()
         if use_graph:
@@ -452,6 +458,8 @@ def run_gpu(args, rank: int, world: int):
         "vs_baseline": None, "dtype": "fp32 score / u8 rows / fp32 attention",
         "data": "synthetic (seeded counter-based generator, generated on the device)",
         "config": workload_config(wl, {"mirror": args.mirror, "l2": "flushed before every timed step",
+                                       "path": "hot_gather_attn (fused)" if fused else
+                                               "hot_gather + mla_decode_attn, append concurrent",
                                        "parallelism": "replicas" if world > 1 else "single GPU"}),
         "tok_per_s": value * A / wl.layers,
         "roofline": {"kernel": name, "bound": bound, "achieved": achieved, "peak": peak,

@@ -63,6 +63,9 @@ SIGNATURES = {
     "mla_decode_attn_workspace": (_SZ, [_I32, _I32, _I32, _I32]),
     "mla_decode_attn": (ctypes.c_int, [_I32, _I32, _I32, _I32, _VP, _VP, _VP, _VP, _F, _VP, _VP, _VP,
                                        _SZ, _VP, _VP]),
+    "hot_gather_attn_workspace": (_SZ, [_I32, _I32, _I32, _I32]),
+    "hot_gather_attn": (ctypes.c_int, [_VP, _I32, _I32, _I32, _I32, _I32, _VP, _VP, _VP, _F, _VP, _VP, _VP,
+                                       _VP, _VP, _SZ, _VP, _VP]),
     "kv_append_writeback": (ctypes.c_int, [_VP, _I32, _I32, _VP, _VP, _VP, _VP]),
     "kv_flush": (ctypes.c_int, [_VP, _I32, _VP, _VP]),
 }
@@ -177,6 +180,17 @@ def mla_decode_attn(U, R, H, K, q_lat, q_rope, rows, topk_idx, scale, out, lse, 
     return _ok("mla_decode_attn", load().mla_decode_attn(
         U, R, H, K, _p(q_lat), _p(q_rope), _p(rows), _p(topk_idx), float(scale), _p(out), _p(lse),
         _p(ws), ws_bytes, _p(dev_err), _s(stream)))
+
+
+def hot_gather_attn_workspace(U, R, H, K) -> int:
+    return load().hot_gather_attn_workspace(U, R, H, K)
+
+
+def hot_gather_attn(units, U, R, K, H, round_, topk_idx, q_lat, q_rope, scale, cls, counters, out, lse,
+                    ws, ws_bytes, dev_err, stream=None):
+    return _ok("hot_gather_attn", load().hot_gather_attn(
+        _p(units), U, R, K, H, round_, _p(topk_idx), _p(q_lat), _p(q_rope), float(scale), _p(cls),
+        _p(counters), _p(out), _p(lse), _p(ws), ws_bytes, _p(dev_err), _s(stream)))
 
 
 def kv_append_writeback(units, U, A, new_rows, new_keys, dev_err, stream=None):

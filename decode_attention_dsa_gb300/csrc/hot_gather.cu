@@ -33,37 +33,13 @@
 //                 being filled); every other entry copies from its source
 //                 (slot / ring / mirror).
 #include "common.cuh"
+#include "gather_internal.cuh"
 
 namespace {
 
 constexpr int ASSIGN_THREADS = 1024;
 constexpr int COPY_THREADS = 256;
 constexpr int COPY_WARPS = COPY_THREADS / 32;
-
-struct GatherWs {
-  int32_t* fill_pos;    // [U][RK] position of the i-th inserted miss (ascending)
-  int32_t* fill_slot;   // [U][RK] its slot
-  int32_t* fill_entry;  // [U][RK] entry (r*K + j) whose compact row it also writes
-  int32_t* opc;         // [U][RK] per-row exclusive prefix count of owner entries
-  int32_t* nfill;       // [U]
-  uint8_t* served;      // [U][RK] 1 if the entry's row is written by a fill
-  int32_t* dup;         // [U][RK][MAX_ROWS-1] later occurrences of the i-th inserted miss
-};
-
-inline GatherWs gather_ws(void* ws, int32_t U, int32_t R, int32_t K) {
-  const size_t rk = (size_t)R * K;
-  const size_t a = dsa_align((size_t)U * rk * 4, 256);
-  char* b = static_cast<char*>(ws);
-  GatherWs g;
-  g.fill_pos = reinterpret_cast<int32_t*>(b);
-  g.fill_slot = reinterpret_cast<int32_t*>(b + a);
-  g.fill_entry = reinterpret_cast<int32_t*>(b + 2 * a);
-  g.opc = reinterpret_cast<int32_t*>(b + 3 * a);
-  g.nfill = reinterpret_cast<int32_t*>(b + 4 * a);
-  g.served = reinterpret_cast<uint8_t*>(b + 4 * a + dsa_align((size_t)U * 4, 256));
-  g.dup = reinterpret_cast<int32_t*>(b + 4 * a + dsa_align((size_t)U * 4, 256) + dsa_align((size_t)U * rk, 256));
-  return g;
-}
 
 // lower_bound of p in an ascending row whose tail is -1 padding (-1 = +inf).
 __device__ __forceinline__ int row_lower_bound(const int32_t* row, int K, int32_t p) {
@@ -109,6 +85,7 @@ k_assign(const dsa_unit* __restrict__ units, int R, int K, int round,
     for (int e = threadIdx.x; e < RK; e += ASSIGN_THREADS) {
       cls_all[(size_t)u * RK + e] = DSA_CLS_PAD;
       g.served[(size_t)u * RK + e] = 1;   // nothing for k_copy to read
+      g.fill_of[(size_t)u * RK + e] = -1;
     }
     return;
   }
@@ -288,10 +265,15 @@ k_assign(const dsa_unit* __restrict__ units, int R, int K, int round,
   // served[e] = 1 for owners that received a slot and for the later
   // occurrences of their position: the fill reads the mirror row once and
   // hands the same RAM bytes to every occurrence
-  for (int e = threadIdx.x; e < RK; e += ASSIGN_THREADS) served[e] = 0;
+  int32_t* fill_of = g.fill_of + (size_t)u * RK;
+  for (int e = threadIdx.x; e < RK; e += ASSIGN_THREADS) {
+    served[e] = 0;
+    fill_of[e] = -1;
+  }
   __syncthreads();
   for (int i = threadIdx.x; i < n; i += ASSIGN_THREADS) {
     served[fill_entry[i]] = 1;
+    fill_of[fill_entry[i]] = i;
     const int32_t* dp = g.dup + ((size_t)u * RK + i) * (DSA_MAX_ROWS - 1);
     for (int k = 0; k < R - 1 && dp[k] >= 0; ++k) served[dp[k]] = 1;
   }
@@ -374,14 +356,9 @@ extern "C" size_t hot_gather_workspace(int32_t U, int32_t R, int32_t K) {
          dsa_align((size_t)U * rk, 256) + dsa_align((size_t)U * rk * (DSA_MAX_ROWS - 1) * 4, 256);
 }
 
-extern "C" int hot_gather(const dsa_unit* units, int32_t U, int32_t R, int32_t K, int32_t round,
-                          const int32_t* topk_idx, uint8_t* cls, uint8_t* rows, int32_t* counters,
-                          void* ws, size_t ws_bytes, int32_t* dev_err, void* stream) {
-  if (!units || !topk_idx || !cls || !rows || !counters) return DSA_ERR_ARG;
-  if (U < 1 || U > 65535 || R < 1 || R > DSA_MAX_ROWS) return DSA_ERR_ARG;
-  if (K < 1 || K > DSA_MAX_K) return DSA_ERR_SHAPE;
-  if (!ws || ws_bytes < hot_gather_workspace(U, R, K)) return DSA_ERR_WS;
-  cudaStream_t st = static_cast<cudaStream_t>(stream);
+int dsa_launch_assign(const dsa_unit* units, int32_t U, int32_t R, int32_t K, int32_t round,
+                      const int32_t* topk_idx, uint8_t* cls, int32_t* counters, void* ws, int32_t* dev_err,
+                      cudaStream_t st) {
   GatherWs g = gather_ws(ws, U, R, K);
   const int RK = R * K;
   static bool attr_done = false;
@@ -390,8 +367,22 @@ extern "C" int hot_gather(const dsa_unit* units, int32_t U, int32_t R, int32_t K
                                       (int)assign_smem(DSA_MAX_ROWS * DSA_MAX_K)));
     attr_done = true;
   }
-  if (launch_pdl(k_assign, dim3(U), dim3(ASSIGN_THREADS), assign_smem(RK), st, units, R, K, round, topk_idx, cls,
-                 counters, g, dev_err) != DSA_OK)
+  return launch_pdl(k_assign, dim3(U), dim3(ASSIGN_THREADS), assign_smem(RK), st, units, R, K, round, topk_idx,
+                    cls, counters, g, dev_err);
+}
+
+extern "C" int hot_gather(const dsa_unit* units, int32_t U, int32_t R, int32_t K, int32_t round,
+                          const int32_t* topk_idx, uint8_t* cls, uint8_t* rows, int32_t* counters,
+                          void* ws, size_t ws_bytes, int32_t* dev_err, void* stream) {
+  if (!units || !topk_idx || !cls || !rows || !counters) return DSA_ERR_ARG;
+  if (U < 1 || U > 65535 || R < 1 || R > DSA_MAX_ROWS) return DSA_ERR_ARG;
+  if (K < 1 || K > DSA_MAX_K) return DSA_ERR_SHAPE;
+  if (!ws || ws_bytes < hot_gather_workspace(U, R, K)) return DSA_ERR_WS;
+  if (reinterpret_cast<uintptr_t>(rows) & 15u) return DSA_ERR_ARG;
+  cudaStream_t st = static_cast<cudaStream_t>(stream);
+  GatherWs g = gather_ws(ws, U, R, K);
+  const int RK = R * K;
+  if (dsa_launch_assign(units, U, R, K, round, topk_idx, cls, counters, ws, dev_err, st) != DSA_OK)
     return DSA_ERR_CUDA;
   return launch_pdl(k_copy, dim3((2 * RK + COPY_WARPS - 1) / COPY_WARPS, U), dim3(COPY_THREADS), 0, st, units, R,
                     K, topk_idx, cls, rows, g);

@@ -36,6 +36,7 @@
 #include <math.h>
 
 #include "common.cuh"
+#include "gather_internal.cuh"
 #include "tc.cuh"
 
 namespace cg = cooperative_groups;
@@ -94,10 +95,20 @@ __device__ __forceinline__ uint32_t pack_h2(float a, float b) {
   return *reinterpret_cast<const uint32_t*>(&h);
 }
 
+__device__ __forceinline__ void cp_async16(void* dst_smem, const void* src) {
+  asm volatile("cp.async.cg.shared.global [%0], [%1], 16;" ::"r"(tc::smem_u32(dst_smem)), "l"(src) : "memory");
+}
+
+// GATHER = false: the rows come compact from hot_gather (one bulk copy).
+// GATHER = true: the rows are read from their sources (HOT slot, ring, RAM
+// mirror) as classified by the gather's assign kernel, and each inserted
+// miss's row is also written to its victim slot.
+template <bool GATHER>
 __global__ void __launch_bounds__(THREADS, 1)
 k_mla_attn(int R, int H, int K, const uint16_t* __restrict__ q_lat, const uint16_t* __restrict__ q_rope,
            const uint8_t* __restrict__ rows, const int32_t* __restrict__ topk, float scale,
-           float* __restrict__ out, float* __restrict__ lse, float* __restrict__ ws_o, int32_t* dev_err) {
+           float* __restrict__ out, float* __restrict__ lse, float* __restrict__ ws_o, int32_t* dev_err,
+           const dsa_unit* __restrict__ units, const uint8_t* __restrict__ cls, GatherWs g) {
   extern __shared__ __align__(1024) uint8_t sm[];
   cg::cluster_group cluster = cg::this_cluster();
   const int C = (int)cluster.num_blocks();
@@ -124,10 +135,59 @@ k_mla_attn(int R, int H, int K, const uint16_t* __restrict__ q_lat, const uint16
   bool failed = ms->fail != 0;
   pdl_wait();   // everything above touched only this CTA's shared and tensor memory
 
-  if (tid == 0 && !failed && nrows > 0) {
+  if (!GATHER && tid == 0 && !failed && nrows > 0) {
     const uint32_t bytes = (uint32_t)nrows * DSA_ROW_BYTES;
     tc::mbar_arrive_expect_tx(&ms->bar[0], bytes);
     tc::bulk_g2s(sX, rows + ((size_t)ur * K + j0) * DSA_ROW_BYTES, bytes, &ms->bar[0]);
+  }
+  if (GATHER && !failed) {
+    // source and fill destination of each of this CTA's rows (kept in Y, which
+    // is free until the dequantised tile is written)
+    const uint8_t** s_src = reinterpret_cast<const uint8_t**>(sY);
+    uint8_t** s_dst = reinterpret_cast<uint8_t**>(sY + NC * sizeof(void*));
+    if (tid < NC) {
+      const uint8_t* src = nullptr;
+      uint8_t* dst = nullptr;
+      if (tid < nrows) {
+        const size_t e = (size_t)ur * K + j0 + tid;    // = u * R * K + entry
+        const int u = ur / R;
+        const dsa_unit& un = units[u];
+        const int32_t p = topk[e];
+        const uint8_t c = cls[e];
+        if (c == DSA_CLS_HOT) {
+          const int32_t sl = un.pos_slot[p];
+          if (sl >= 0 && sl < un.slots_n) src = un.slots + (size_t)sl * DSA_ROW_BYTES;
+        } else if (c == DSA_CLS_RING) {
+          src = un.ring + (size_t)(p & (DSA_RING_ROWS - 1)) * DSA_ROW_BYTES;
+        } else if (c == DSA_CLS_RAM) {
+          src = un.mirror + (size_t)p * DSA_ROW_BYTES;
+          const int32_t f = g.fill_of[e];
+          if (f >= 0) {
+            const int32_t sl = g.fill_slot[(size_t)u * R * K + f];
+            if (sl >= 0 && sl < un.slots_n) dst = un.slots + (size_t)sl * DSA_ROW_BYTES;
+          }
+        }
+      }
+      s_src[tid] = src;
+      s_dst[tid] = dst;
+    }
+    __syncthreads();
+    // every 16-byte piece of every row in flight at once (no registers held)
+    for (int t = tid; t < nrows * 41; t += THREADS) {
+      const int jj = t / 41, c = t % 41;
+      const uint8_t* src = s_src[jj];
+      uint8_t* d = sX + jj * DSA_ROW_BYTES + 16 * c;
+      if (src) cp_async16(d, src + 16 * c);
+      else *reinterpret_cast<uint4*>(d) = make_uint4(0, 0, 0, 0);
+    }
+    asm volatile("cp.async.commit_group;\ncp.async.wait_group 0;" ::: "memory");
+    __syncthreads();
+    // inserted misses: their RAM bytes also go to the victim slot
+    for (int t = tid; t < nrows * 41; t += THREADS) {
+      const int jj = t / 41, c = t % 41;
+      uint8_t* dst = s_dst[jj];
+      if (dst) *reinterpret_cast<uint4*>(dst + 16 * c) = *reinterpret_cast<const uint4*>(sX + jj * DSA_ROW_BYTES + 16 * c);
+    }
   }
   if (tid < NC) {
     const bool v = (tid < nrows) && topk[(size_t)ur * K + j0 + tid] >= 0;
@@ -149,7 +209,7 @@ k_mla_attn(int R, int H, int K, const uint16_t* __restrict__ q_lat, const uint16
                      : *reinterpret_cast<const uint4*>(q_rope + qo * 64 + 8 * (c - 64));
     }
   }
-  if (!failed && nrows > 0 && !tc::mbar_wait(&ms->bar[0], 0)) atomicOr(&ms->fail, 1);
+  if (!GATHER && !failed && nrows > 0 && !tc::mbar_wait(&ms->bar[0], 0)) atomicOr(&ms->fail, 1);
   __syncthreads();
   failed = ms->fail != 0;
 
@@ -380,7 +440,7 @@ k_mla_attn(int R, int H, int K, const uint16_t* __restrict__ q_lat, const uint16
       mg->inv[h] = L > 0.f ? 1.f / L : 0.f;
       if (crank == 0 && lse && h < H) lse[(size_t)ur * H + h] = L > 0.f ? M + logf(L) : -INFINITY;
     }
-    const bool got = tc::mbar_wait(&ms->bar[0], 1);    // second phase of the TMA barrier
+    const bool got = tc::mbar_wait(&ms->bar[0], GATHER ? 0 : 1);   // the merge copy's phase of the TMA barrier
     if (!got) atomicOr(&ms->fail, 1);
     __syncthreads();
     const int nq = W / 4;
@@ -417,6 +477,48 @@ extern "C" size_t mla_decode_attn_workspace(int32_t U, int32_t R, int32_t H, int
   return (size_t)U * R * MAX_CLUSTER * 64 * 512 * 4;   // one 64 x 512 fp32 partial per CTA
 }
 
+namespace {
+
+template <bool GATHER>
+int launch_attn(int32_t U, int32_t R, int32_t H, int32_t K, const uint16_t* q_lat, const uint16_t* q_rope,
+                const uint8_t* rows, const int32_t* topk_idx, float scale, float* out, float* lse, float* ws_o,
+                int32_t* dev_err, const dsa_unit* units, const uint8_t* cls, GatherWs g, cudaStream_t st) {
+  static bool attr_done = false;
+  if (!attr_done) {
+    DSA_CUDA_TRY(cudaFuncSetAttribute(k_mla_attn<GATHER>, cudaFuncAttributeMaxDynamicSharedMemorySize, SMEM_BYTES));
+    DSA_CUDA_TRY(cudaFuncSetAttribute(k_mla_attn<GATHER>, cudaFuncAttributeNonPortableClusterSizeAllowed, 1));
+    attr_done = true;
+  }
+  const int C = (K + NC - 1) / NC;
+  cudaLaunchConfig_t cfg = {};
+  cfg.gridDim = dim3(C, U * R, 1);
+  cfg.blockDim = dim3(THREADS, 1, 1);
+  cfg.dynamicSmemBytes = SMEM_BYTES;
+  cfg.stream = st;
+  cudaLaunchAttribute attr[2];
+  attr[0].id = cudaLaunchAttributeClusterDimension;
+  attr[0].val.clusterDim.x = C;
+  attr[0].val.clusterDim.y = 1;
+  attr[0].val.clusterDim.z = 1;
+  attr[1].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+  attr[1].val.programmaticStreamSerializationAllowed = 1;
+  cfg.attrs = attr;
+  cfg.numAttrs = 2;
+  if (cudaLaunchKernelEx(&cfg, k_mla_attn<GATHER>, (int)R, (int)H, (int)K, q_lat, q_rope, rows, topk_idx, scale,
+                         out, lse, ws_o, dev_err, units, cls, g) != cudaSuccess)
+    return DSA_ERR_CUDA;
+  return dsa_launch_status();
+}
+
+// K <= 2048 needs C = ceil(K / 128) CTAs per cluster; the merge splits the
+// 512 output columns evenly, so C must divide 512 (1, 2, 4, 8, 16)
+inline bool cluster_ok(int K) {
+  const int C = (K + NC - 1) / NC;
+  return C == 1 || C == 2 || C == 4 || C == 8 || C == 16;
+}
+
+}  // namespace
+
 extern "C" int mla_decode_attn(int32_t U, int32_t R, int32_t H, int32_t K, const uint16_t* q_lat,
                                const uint16_t* q_rope, const uint8_t* rows,
                                const int32_t* topk_idx, float scale, float* out, float* lse,
@@ -428,29 +530,31 @@ extern "C" int mla_decode_attn(int32_t U, int32_t R, int32_t H, int32_t K, const
   if (!ws || ws_bytes < mla_decode_attn_workspace(U, R, H, K)) return DSA_ERR_WS;
   // rows and the workspace are read by bulk copies: 16-byte alignment
   if ((reinterpret_cast<uintptr_t>(rows) | reinterpret_cast<uintptr_t>(ws)) & 15u) return DSA_ERR_ARG;
-  static bool attr_done = false;
-  if (!attr_done) {
-    DSA_CUDA_TRY(cudaFuncSetAttribute(k_mla_attn, cudaFuncAttributeMaxDynamicSharedMemorySize, SMEM_BYTES));
-    DSA_CUDA_TRY(cudaFuncSetAttribute(k_mla_attn, cudaFuncAttributeNonPortableClusterSizeAllowed, 1));
-    attr_done = true;
-  }
-  const int C = (K + NC - 1) / NC;
-  cudaLaunchConfig_t cfg = {};
-  cfg.gridDim = dim3(C, U * R, 1);
-  cfg.blockDim = dim3(THREADS, 1, 1);
-  cfg.dynamicSmemBytes = SMEM_BYTES;
-  cfg.stream = static_cast<cudaStream_t>(stream);
-  cudaLaunchAttribute attr[2];
-  attr[0].id = cudaLaunchAttributeClusterDimension;
-  attr[0].val.clusterDim.x = C;
-  attr[0].val.clusterDim.y = 1;
-  attr[0].val.clusterDim.z = 1;
-  attr[1].id = cudaLaunchAttributeProgrammaticStreamSerialization;
-  attr[1].val.programmaticStreamSerializationAllowed = 1;
-  cfg.attrs = attr;
-  cfg.numAttrs = 2;
-  if (cudaLaunchKernelEx(&cfg, k_mla_attn, (int)R, (int)H, (int)K, q_lat, q_rope, rows, topk_idx, scale,
-                         out, lse, static_cast<float*>(ws), dev_err) != cudaSuccess)
+  GatherWs none = {};
+  return launch_attn<false>(U, R, H, K, q_lat, q_rope, rows, topk_idx, scale, out, lse, static_cast<float*>(ws),
+                            dev_err, nullptr, nullptr, none, static_cast<cudaStream_t>(stream));
+}
+
+extern "C" size_t hot_gather_attn_workspace(int32_t U, int32_t R, int32_t H, int32_t K) {
+  if (U < 1 || R < 1 || H < 1 || K < 1) return 0;
+  return dsa_align(hot_gather_workspace(U, R, K), 256) + mla_decode_attn_workspace(U, R, H, K);
+}
+
+extern "C" int hot_gather_attn(const dsa_unit* units, int32_t U, int32_t R, int32_t K, int32_t H, int32_t round,
+                               const int32_t* topk_idx, const uint16_t* q_lat, const uint16_t* q_rope,
+                               float scale, uint8_t* cls, int32_t* counters, float* out, float* lse, void* ws,
+                               size_t ws_bytes, int32_t* dev_err, void* stream) {
+  if (!units || !topk_idx || !q_lat || !q_rope || !cls || !counters || !out) return DSA_ERR_ARG;
+  if (U < 1 || U > 65535 || R < 1 || R > DSA_MAX_ROWS || !(scale > 0.0f)) return DSA_ERR_ARG;
+  if (K < 1 || K > NC * MAX_CLUSTER || H < 16 || H > 64 || (H % 16) != 0) return DSA_ERR_SHAPE;
+  if ((size_t)U * R > 65535) return DSA_ERR_ARG;
+  if (!ws || ws_bytes < hot_gather_attn_workspace(U, R, H, K)) return DSA_ERR_WS;
+  if (reinterpret_cast<uintptr_t>(ws) & 255u) return DSA_ERR_ARG;
+  cudaStream_t st = static_cast<cudaStream_t>(stream);
+  void* gws = ws;
+  float* aws = reinterpret_cast<float*>(static_cast<char*>(ws) + dsa_align(hot_gather_workspace(U, R, K), 256));
+  if (dsa_launch_assign(units, U, R, K, round, topk_idx, cls, counters, gws, dev_err, st) != DSA_OK)
     return DSA_ERR_CUDA;
-  return dsa_launch_status();
+  return launch_attn<true>(U, R, H, K, q_lat, q_rope, nullptr, topk_idx, scale, out, lse, aws, dev_err, units,
+                           cls, gather_ws(gws, U, R, K), st);
 }

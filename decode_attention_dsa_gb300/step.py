@@ -49,13 +49,31 @@ class DecodePath:
                             self.scale, self.out, self.lse, self.ws_attn, self.ws_attn_bytes,
                             u.dev_err, stream)
 
+    def gather_attend(self, rnd: int, q_lat, q_rope, stream=None):
+        """hot_gather + attention in one call (rows read from their sources)."""
+        u = self.u
+        if not hasattr(self, "ws_fused"):
+            self.ws_fused_bytes = abi.hot_gather_attn_workspace(u.U, self.R, self.H, self.K)
+            self.ws_fused = torch.zeros(self.ws_fused_bytes, dtype=torch.uint8, device=u.device)
+        abi.hot_gather_attn(u.units, u.U, self.R, self.K, self.H, rnd, self.topk, q_lat, q_rope, self.scale,
+                            self.cls, self.counters, self.out, self.lse, self.ws_fused, self.ws_fused_bytes,
+                            u.dev_err, stream)
+
     def append(self, new_rows, new_keys, stream=None):
         u = self.u
         abi.kv_append_writeback(u.units, u.U, self.A, new_rows, new_keys, u.dev_err, stream)
 
-    def step(self, rnd, q_idx, w, q_lat, q_rope, new_rows, new_keys, stream=None, side=None):
-        """One decode step. With a ``side`` stream, the append runs there,
-        concurrently with the attention (allowed once the gather is done)."""
+    def step(self, rnd, q_idx, w, q_lat, q_rope, new_rows, new_keys, stream=None, side=None,
+             fused=False):
+        """One decode step. ``fused`` uses hot_gather_attn (no compact rows; the
+        append follows it). Otherwise, with a ``side`` stream, the append runs
+        there, concurrently with the attention (allowed once the gather is
+        done)."""
+        if fused:
+            self.score_topk(q_idx, w, stream)
+            self.gather_attend(rnd, q_lat, q_rope, stream)
+            self.append(new_rows, new_keys, stream)
+            return
         self.score_topk(q_idx, w, stream)
         self.gather(rnd, stream)
         if side is None:

@@ -296,6 +296,29 @@ int mla_decode_attn(int32_t U, int32_t R, int32_t H, int32_t K,
                     float* out, float* lse, void* ws, size_t ws_bytes,
                     int32_t* dev_err, void* stream);
 
+/*
+ * hot_gather followed by mla_decode_attn in one call, without the compact
+ * rows: the attention kernel reads each selected row straight from its
+ * source (HOT slot, ring, RAM mirror) as this call's classification found it,
+ * and writes each inserted miss's row to its victim slot ([P3] section
+ * "第三次决策": hits read VRAM, misses read the registered RAM mirror, and
+ * attention consumes the gathered set). Classification, pins, visibility,
+ * replacement, counters, cache state and out/lse are exactly those of
+ * hot_gather + mla_decode_attn; only the compact `rows` buffer is not
+ * produced. Duplicate misses of different query rows each read the mirror.
+ *   Arguments as in hot_gather and mla_decode_attn; ws holds
+ *   hot_gather_attn_workspace(U, R, H, K) bytes, 256-byte aligned.
+ *   Shapes: those of mla_decode_attn.
+ * Ordering: the step's kv_append_writeback must not run concurrently with
+ * this call (the call reads ring rows that an append of several rows may
+ * overwrite).
+ */
+size_t hot_gather_attn_workspace(int32_t U, int32_t R, int32_t H, int32_t K);
+int hot_gather_attn(const dsa_unit* units, int32_t U, int32_t R, int32_t K, int32_t H, int32_t round,
+                    const int32_t* topk_idx, const uint16_t* q_lat, const uint16_t* q_rope, float scale,
+                    uint8_t* cls, int32_t* counters, float* out, float* lse, void* ws, size_t ws_bytes,
+                    int32_t* dev_err, void* stream);
+
 /* ------------------------------------------- A6: append and batched write-back */
 
 /*

@@ -78,7 +78,9 @@ class Pair:
         per, t = self.inputs(step)
         self.last_inputs = per
         p = self.p
-        if side is not None:
+        if side == "fused":
+            p.step(rnd, t["q_idx"], t["w"], t["q_lat"], t["q_rope"], t["new_rows"], t["new_keys"], fused=True)
+        elif side is not None:
             assert attention
             p.step(rnd, t["q_idx"], t["w"], t["q_lat"], t["q_rope"], t["new_rows"], t["new_keys"], side=side)
         else:
@@ -140,6 +142,10 @@ def check_step(pair: Pair, g, ores, attention=True, rows=True, full_state=True, 
         assert np.array_equal(g["counters"][i], o["counters"]), f"unit {u}: counters differ"
         if rows:
             assert np.array_equal(g["rows"][i], o["rows"]), f"unit {u}: gathered rows differ"
+        if full_state and getattr(pair, "check_slots", False):
+            gs = pair.g.slots[i].cpu().numpy()
+            occ = oc.slot_pos >= 0
+            assert np.array_equal(gs[occ], oc.slots[occ]), f"unit {u}: slot bytes differ"
         s = pair.state(i)
         assert np.array_equal(s["slot_pos"], oc.slot_pos), f"unit {u}: slot map differs"
         assert np.array_equal(s["fill_round"], oc.fill_round), f"unit {u}: fill rounds differ"

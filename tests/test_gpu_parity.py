@@ -22,7 +22,8 @@ def run(wl, steps=None, rnds=None, mirror="host", check_every=1, attention_every
         full_state=True, units=None, oracle_units=None, oracle_rnds=None, gpu_gen=False,
         side_stream=False):
     pair = Pair(wl, units=units, mirror=mirror, oracle_units=oracle_units, gpu_gen=gpu_gen)
-    side = pair.torch.cuda.Stream() if side_stream else None
+    side = pair.torch.cuda.Stream() if side_stream is True else side_stream or None
+    pair.check_slots = True
     steps = range(wl.steps) if steps is None else steps
     worst = 0.0
     for k, st in enumerate(steps):
@@ -31,7 +32,8 @@ def run(wl, steps=None, rnds=None, mirror="host", check_every=1, attention_every
         att = (k % attention_every) == 0 or k == len(steps) - 1
         g, o = pair.step(st, rnd=rnd, attention=att or side is not None, oracle_rnd=ornd, side=side)
         if (k % check_every) == 0 or k == len(steps) - 1:
-            worst = max(worst, check_step(pair, g, o, attention=att, full_state=full_state))
+            worst = max(worst, check_step(pair, g, o, attention=att or side is not None,
+                                          full_state=full_state, rows=side != "fused"))
         assert pair.g.check() == 0, f"device error word {pair.g.check():#x}"
     return pair, worst
 
@@ -87,6 +89,27 @@ def test_append_concurrent_with_attention():
     several 64-row write-backs: results identical to the serial order."""
     wl = W.WORKLOADS[0].with_(name="side", L0=700, S=48, K=64, H=16, steps=140, A=1, warm="last_s")
     run(wl, side_stream=True)
+
+
+FUSED = [
+    W.WORKLOADS[0],
+    W.WORKLOADS[0].with_(name="fused-mtp", L0=1500, S=64, R=4, A=4, K=128, H=64, warm="last_s", mode="mtp",
+                         steps=20),
+    W.WORKLOADS[0].with_(name="fused-ragged", L0=3 * 512 + 37, S=256, K=200, H=48, warm="last_s", steps=6),
+    W.WORKLOADS[0].with_(name="fused-evict", L0=700, S=16, K=64, H=16, warm="empty", steps=70),
+]
+
+
+@pytest.mark.parametrize("wl", FUSED, ids=[w.name[:12] for w in FUSED])
+def test_fused_gather_attention(wl):
+    """hot_gather_attn: same classification, state, slot bytes and attention
+    as hot_gather + mla_decode_attn (compared with the oracle)."""
+    run(wl, side_stream="fused")
+
+
+@pytest.mark.slow
+def test_fused_config1_full_size_first_steps():
+    run(W.WORKLOADS[1], steps=range(66), side_stream="fused", attention_every=1)
 
 
 def test_resident_mirror_same_results():
