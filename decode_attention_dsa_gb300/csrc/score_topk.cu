@@ -52,6 +52,7 @@ constexpr int SEL_THREADS = 512;
 constexpr int SEL_KEY_CACHE = 16384;     // keys of a CTA's range kept in shared memory
 constexpr int SEL_CAND_CAP = 4096;       // candidates per CTA (fast path)
 constexpr int SEL_ALL_CAP = 8192;        // candidates per cluster (fast path)
+constexpr int SEL_PER_SRC = SEL_ALL_CAP / SEL_CLUSTER;   // candidates each CTA may push
 
 struct TopkWs {
   uint32_t* hist;   // [U*R][4096]
@@ -379,7 +380,9 @@ struct SelShared {
   int ncand, overflow;
   int any_over;               // some CTA of the cluster overflowed
   uint64_t kbar;              // bulk copy of this CTA's key range
-  int coff[SEL_CLUSTER + 1];  // candidate offsets of the cluster's CTAs
+  int coff[SEL_CLUSTER + 1];  // (fallback bookkeeping)
+  int srcn[SEL_CLUSTER];      // candidates pushed here by each CTA (-1: it overflowed)
+  long long rcnt[SEL_CLUSTER][2];   // (gt, eq) of each CTA, read once for the prefix
   long long cnt[2];           // this CTA's (gt, eq) counts
 };
 // The key cache (a bulk-copy destination) starts 128-byte aligned after it.
@@ -407,6 +410,9 @@ k_topk_select(const dsa_unit* __restrict__ units, int R, int K, uint32_t* __rest
     return;
   }
 
+  // every CTA of the cluster must be running before any remote shared store:
+  // arrive now, wait just before the first one
+  asm volatile("barrier.cluster.arrive.relaxed.aligned;" ::: "memory");
   extern __shared__ __align__(128) uint8_t smem_sel[];
   SelShared* S = reinterpret_cast<SelShared*>(smem_sel);
   uint32_t* kc = reinterpret_cast<uint32_t*>(smem_sel + SEL_KC_OFF);          // [SEL_KEY_CACHE]
@@ -457,6 +463,11 @@ k_topk_select(const dsa_unit* __restrict__ units, int R, int K, uint32_t* __rest
       dsa_flag(dev_err, DSA_DEVERR_TIMEOUT);
     }
   }
+  asm volatile("barrier.cluster.wait.aligned;" ::: "memory");
+  // candidates go to region [crank] of every CTA's candidate buffer
+  uint32_t* dst[SEL_CLUSTER];
+#pragma unroll
+  for (int c = 0; c < SEL_CLUSTER; ++c) dst[c] = cluster.map_shared_rank(allc, c) + crank * SEL_PER_SRC;
   long long gt1 = 0;
   for (int64_t p = beg + tid; p < end; p += SEL_THREADS) {
     const uint32_t key = key_at(p);
@@ -465,53 +476,42 @@ k_topk_select(const dsa_unit* __restrict__ units, int R, int K, uint32_t* __rest
       ++gt1;
     } else if (d1 == b1) {
       const int i = atomicAdd(&S->ncand, 1);
-      if (i < SEL_CAND_CAP) cand[i] = key;
+      if (i < SEL_PER_SRC) {
+#pragma unroll
+        for (int c = 0; c < SEL_CLUSTER; ++c) dst[c][i] = key;
+      }
     }
   }
   int gt1_cta;
   block_inclusive_scan<SEL_THREADS>((int)gt1, S->tmp, &gt1_cta);
-  if (tid == 0) S->overflow = S->ncand > SEL_CAND_CAP;
+  if (tid == 0) S->overflow = S->ncand > SEL_PER_SRC;
+  if (tid < SEL_CLUSTER)
+    cluster.map_shared_rank(S, tid)->srcn[crank] = S->ncand > SEL_PER_SRC ? -1 : S->ncand;
   __syncthreads();
   cluster.sync();
   if (crank == 0) {
     // every CTA read the global histogram before the barrier: clear it for the next call
     for (int i = tid; i < HIST1_BINS; i += SEL_THREADS) gh[i] = 0;
   }
-  if (tid < SEL_CLUSTER) {
-    const SelShared* rs = cluster.map_shared_rank(S, tid);
-    S->coff[tid + 1] = rs->overflow ? -1 : min(rs->ncand, SEL_CAND_CAP);
-  }
-  __syncthreads();
   int total = 0, any_over = 0;
-  if (tid == 0) {
-    S->coff[0] = 0;
-    for (int c = 0; c < SEL_CLUSTER; ++c) {
-      const int nc = S->coff[c + 1];
-      any_over |= nc < 0;
-      S->coff[c + 1] = S->coff[c] + max(nc, 0);
-    }
-    S->any_over = any_over;
+  for (int c = 0; c < SEL_CLUSTER; ++c) {
+    const int nc = S->srcn[c];
+    any_over |= nc < 0;
+    total += max(nc, 0);
   }
-  __syncthreads();
-  any_over = S->any_over;
-  total = S->coff[SEL_CLUSTER];
   const bool fast = !any_over && total <= SEL_ALL_CAP;
 
   uint32_t T;
   int ties;
   long long gt_cta, eq_cta;
   if (fast) {
-    // ---- all candidates to every CTA (one round of remote loads), then an
+    // ---- every CTA holds all candidates (pushed into per-source regions):
     //      exact local radix select on bits 19..8 and 7..0
-    for (int i = tid; i < total; i += SEL_THREADS) {
-      int c = 0;
-      while (c + 1 < SEL_CLUSTER && i >= S->coff[c + 1]) ++c;
-      allc[i] = cluster.map_shared_rank(cand, c)[i - S->coff[c]];
-    }
     for (int i = tid; i < HIST1_BINS; i += SEL_THREADS) S->h1[i] = 0;
     __syncthreads();
     const uint32_t p1 = b1 << 20;
-    for (int i = tid; i < total; i += SEL_THREADS) {
+    for (int i = tid; i < SEL_ALL_CAP; i += SEL_THREADS) {
+      if ((i % SEL_PER_SRC) >= S->srcn[i / SEL_PER_SRC]) continue;
       const uint32_t key = allc[i];
       if ((key & 0xFFF00000u) == p1) atomicAdd(&S->h1[(key >> 8) & 0xFFF], 1u);
     }
@@ -521,7 +521,8 @@ k_topk_select(const dsa_unit* __restrict__ units, int R, int K, uint32_t* __rest
     const uint32_t p2 = p1 | ((uint32_t)S->bin << 8);
     for (int i = tid; i < 256; i += SEL_THREADS) S->hg[i] = 0;
     __syncthreads();
-    for (int i = tid; i < total; i += SEL_THREADS) {
+    for (int i = tid; i < SEL_ALL_CAP; i += SEL_THREADS) {
+      if ((i % SEL_PER_SRC) >= S->srcn[i / SEL_PER_SRC]) continue;
       const uint32_t key = allc[i];
       if ((key & 0xFFFFFF00u) == p2) atomicAdd(&S->hg[key & 0xFF], 1u);
     }
@@ -531,11 +532,12 @@ k_topk_select(const dsa_unit* __restrict__ units, int R, int K, uint32_t* __rest
     T = p2 | (uint32_t)S->bin;
     ties = need;
     // this CTA's counts from its own candidates
-    const int nc = min(S->ncand, SEL_CAND_CAP);
+    const int nc = S->srcn[crank];
+    const uint32_t* own = allc + crank * SEL_PER_SRC;
     int g = 0, e = 0;
     for (int i = tid; i < nc; i += SEL_THREADS) {
-      g += cand[i] > T;
-      e += cand[i] == T;
+      g += own[i] > T;
+      e += own[i] == T;
     }
     int gtot, etot;
     block_inclusive_scan<SEL_THREADS>(g, S->tmp, &gtot);
@@ -591,10 +593,15 @@ k_topk_select(const dsa_unit* __restrict__ units, int R, int K, uint32_t* __rest
   }
   __syncthreads();
   cluster.sync();
+  if (tid < SEL_CLUSTER) {   // one round of remote loads
+    const SelShared* rs = cluster.map_shared_rank(S, tid);
+    S->rcnt[tid][0] = rs->cnt[0];
+    S->rcnt[tid][1] = rs->cnt[1];
+  }
+  __syncthreads();
   long long eq_before = 0, sel_before = 0;
   for (int c = 0; c < crank; ++c) {
-    const SelShared* rs = cluster.map_shared_rank(S, c);
-    const long long g = rs->cnt[0], e = rs->cnt[1];
+    const long long g = S->rcnt[c][0], e = S->rcnt[c][1];
     long long take = (long long)ties - eq_before;
     take = take < 0 ? 0 : (take > e ? e : take);
     sel_before += g + take;
