@@ -452,6 +452,35 @@ k_topk_select(const dsa_unit* __restrict__ units, int R, int K, uint32_t* __rest
   int need = K - S->above;
 
   auto key_at = [&](int64_t p) -> uint32_t { return cached ? kc[p - beg] : kk[p]; };
+  // four keys [4q, 4q + 4) of the range, one 16-byte load (shared or global)
+  auto key4 = [&](int64_t q) -> uint4 {
+    return cached ? *reinterpret_cast<const uint4*>(kc + (4 * q - beg))
+                  : __ldcg(reinterpret_cast<const uint4*>(kk + 4 * q));
+  };
+  // quads covering [beg, end); beg is a multiple of 4 whenever the range is
+  // not empty (a trailing CTA whose range is empty gets no quads)
+  const int64_t q0 = beg / 4, q1 = end > beg ? (end + 3) / 4 : q0;
+  // visit every key of the range with coalesced 16-byte loads, UNR quads in
+  // flight per thread
+  auto for_keys = [&](auto&& f) {
+    constexpr int UNR = 4;
+    for (int64_t qb = q0 + tid; qb < q1; qb += (int64_t)UNR * SEL_THREADS) {
+      uint4 v[UNR];
+#pragma unroll
+      for (int k = 0; k < UNR; ++k) {
+        const int64_t q = qb + (int64_t)k * SEL_THREADS;
+        v[k] = q < q1 ? key4(q) : make_uint4(0, 0, 0, 0);
+      }
+#pragma unroll
+      for (int k = 0; k < UNR; ++k) {
+        const int64_t q = qb + (int64_t)k * SEL_THREADS;
+        const uint32_t w[4] = {v[k].x, v[k].y, v[k].z, v[k].w};
+#pragma unroll
+        for (int e = 0; e < 4; ++e)
+          if (q < q1 && 4 * q + e < end) f(4 * q + e, w[e]);
+      }
+    }
+  };
 
   // ---- one pass: cache keys, count keys above b1, collect candidates in b1
   if (cached && end > beg) {
@@ -469,8 +498,7 @@ k_topk_select(const dsa_unit* __restrict__ units, int R, int K, uint32_t* __rest
 #pragma unroll
   for (int c = 0; c < SEL_CLUSTER; ++c) dst[c] = cluster.map_shared_rank(allc, c) + crank * SEL_PER_SRC;
   long long gt1 = 0;
-  for (int64_t p = beg + tid; p < end; p += SEL_THREADS) {
-    const uint32_t key = key_at(p);
+  for_keys([&](int64_t, uint32_t key) {
     const uint32_t d1 = key >> 20;
     if (d1 > b1) {
       ++gt1;
@@ -481,7 +509,7 @@ k_topk_select(const dsa_unit* __restrict__ units, int R, int K, uint32_t* __rest
         for (int c = 0; c < SEL_CLUSTER; ++c) dst[c][i] = key;
       }
     }
-  }
+  });
   int gt1_cta;
   block_inclusive_scan<SEL_THREADS>((int)gt1, S->tmp, &gt1_cta);
   if (tid == 0) S->overflow = S->ncand > SEL_PER_SRC;
@@ -557,10 +585,9 @@ k_topk_select(const dsa_unit* __restrict__ units, int R, int K, uint32_t* __rest
       __syncthreads();
       const int sh = shifts[lvl];
       const uint32_t dm = (uint32_t)nbins[lvl] - 1;
-      for (int64_t p = beg + tid; p < end; p += SEL_THREADS) {
-        const uint32_t key = key_at(p);
+      for_keys([&](int64_t, uint32_t key) {
         if ((key & mask) == prefix) atomicAdd(&hl[(key >> sh) & dm], 1u);
-      }
+      });
       __syncthreads();
       cluster.sync();
       for (int i = tid; i < nbins[lvl]; i += SEL_THREADS) {
@@ -607,39 +634,53 @@ k_topk_select(const dsa_unit* __restrict__ units, int R, int K, uint32_t* __rest
     sel_before += g + take;
     eq_before += e;
   }
-  // ---- ordered compaction of this CTA's range: every thread owns a
-  //      contiguous run of positions; two block scans give each run its tie
-  //      rank and output offset
+  // ---- ordered compaction of this CTA's range, in tiles of 8 x SEL_THREADS
+  //      keys: thread t owns 8 consecutive keys of the tile (two 16-byte
+  //      loads); two block scans give each thread its tie rank and output
+  //      offset
   {
-    const int64_t n = end - beg;
-    const int64_t run = (n + SEL_THREADS - 1) / SEL_THREADS;
-    const int64_t r0 = beg + min((int64_t)tid * run, n);
-    const int64_t r1 = beg + min((int64_t)(tid + 1) * run, n);
-    int g = 0, e = 0;
-    for (int64_t p = r0; p < r1; ++p) {
-      const uint32_t key = key_at(p);
-      g += key > T;
-      e += key == T;
-    }
-    const int einc = block_inclusive_scan<SEL_THREADS>(e, S->tmp);
-    const long long estart = eq_before + einc - e;
-    long long take = (long long)ties - estart;
-    take = take < 0 ? 0 : (take > e ? e : take);
-    const int sel = g + (int)take;
-    const int sinc = block_inclusive_scan<SEL_THREADS>(sel, S->tmp);
-    long long o = sel_before + sinc - sel;
-    long long er = estart;
-    for (int64_t p = r0; p < r1; ++p) {
-      const uint32_t key = key_at(p);
-      bool pick = key > T;
-      if (key == T) {
-        pick = er < ties;
-        ++er;
+    long long run_eq = eq_before, run_sel = sel_before;
+    for (int64_t tb = q0; tb < q1; tb += 2 * SEL_THREADS) {
+      const int64_t qa = tb + 2 * tid;
+      uint32_t w[8];
+      {
+        const uint4 a = qa < q1 ? key4(qa) : make_uint4(0, 0, 0, 0);
+        const uint4 b = qa + 1 < q1 ? key4(qa + 1) : make_uint4(0, 0, 0, 0);
+        w[0] = a.x; w[1] = a.y; w[2] = a.z; w[3] = a.w;
+        w[4] = b.x; w[5] = b.y; w[6] = b.z; w[7] = b.w;
       }
-      if (pick) {
-        if (o < K) out[o] = (int32_t)p;
-        ++o;
+      const int64_t p0 = 4 * qa;
+      int g = 0, e = 0;
+#pragma unroll
+      for (int k = 0; k < 8; ++k) {
+        const bool in = p0 + k >= beg && p0 + k < end;
+        g += in && w[k] > T;
+        e += in && w[k] == T;
       }
+      int etot, stot;
+      const int einc = block_inclusive_scan<SEL_THREADS>(e, S->tmp, &etot);
+      const long long estart = run_eq + einc - e;
+      long long take = (long long)ties - estart;
+      take = take < 0 ? 0 : (take > e ? e : take);
+      const int sel = g + (int)take;
+      const int sinc = block_inclusive_scan<SEL_THREADS>(sel, S->tmp, &stot);
+      long long o = run_sel + sinc - sel;
+      long long er = estart;
+#pragma unroll
+      for (int k = 0; k < 8; ++k) {
+        const bool in = p0 + k >= beg && p0 + k < end;
+        bool pick = in && w[k] > T;
+        if (in && w[k] == T) {
+          pick = er < ties;
+          ++er;
+        }
+        if (pick) {
+          if (o < K) out[o] = (int32_t)(p0 + k);
+          ++o;
+        }
+      }
+      run_eq += etot;
+      run_sel += stot;
     }
   }
   cluster.sync();   // keep this CTA's shared memory alive for its peers
