@@ -67,6 +67,7 @@ SIGNATURES = {
     "hot_gather_attn": (ctypes.c_int, [_VP, _I32, _I32, _I32, _I32, _I32, _VP, _VP, _VP, _F, _VP, _VP, _VP,
                                        _VP, _VP, _SZ, _VP, _VP]),
     "kv_append_writeback": (ctypes.c_int, [_VP, _I32, _I32, _VP, _VP, _VP, _VP]),
+    "kv_append_quantize": (ctypes.c_int, [_VP, _I32, _I32, _VP, _VP, _VP, _VP, _VP]),
     "kv_flush": (ctypes.c_int, [_VP, _I32, _VP, _VP]),
 }
 
@@ -196,6 +197,11 @@ def hot_gather_attn(units, U, R, K, H, round_, topk_idx, q_lat, q_rope, scale, c
 def kv_append_writeback(units, U, A, new_rows, new_keys, dev_err, stream=None):
     return _ok("kv_append_writeback", load().kv_append_writeback(
         _p(units), U, A, _p(new_rows), _p(new_keys), _p(dev_err), _s(stream)))
+
+
+def kv_append_quantize(units, U, A, new_latent, new_rope, new_keys, dev_err, stream=None):
+    return _ok("kv_append_quantize", load().kv_append_quantize(
+        _p(units), U, A, _p(new_latent), _p(new_rope), _p(new_keys), _p(dev_err), _s(stream)))
 
 
 def kv_flush(units, U, dev_err, stream=None):

@@ -16,6 +16,8 @@
 #include <algorithm>
 #include <cstring>
 
+#include <cuda_fp16.h>
+
 #include "common.cuh"
 
 namespace {
@@ -36,9 +38,42 @@ __device__ void write_back(const dsa_unit& un, int64_t from, int64_t to) {
   }
 }
 
+// Q8G64-quantise one bf16 row into `dst` (656 bytes): warp g handles latent
+// group g (threads 32g..32g+31, two values each). Symmetric group scale
+// fp16_rn(amax / 127) and codes clamp(rint(w / scale), -127, 127), IEEE fp32
+// division; a zero (or unrepresentable) scale gives all-zero codes.
+__device__ void quantize_row_q8g64(uint8_t* dst, const uint16_t* lat, const uint16_t* rope) {
+  const int t = threadIdx.x, lane = t & 31, g = t >> 5;
+  if (t < 256) {
+    const float x0 = bf16f(lat[2 * t]), x1 = bf16f(lat[2 * t + 1]);
+    float m = fmaxf(fabsf(x0), fabsf(x1));
+#pragma unroll
+    for (int o = 16; o > 0; o >>= 1) m = fmaxf(m, __shfl_xor_sync(0xffffffffu, m, o));
+    const __half h = __float2half_rn(m / 127.0f);
+    float sc = __half2float(h);
+    const bool zero = !(sc > 0.0f) || isinf(sc);
+    int8_t q0 = 0, q1 = 0;
+    if (!zero) {
+      q0 = (int8_t)fminf(fmaxf(rintf(x0 / sc), -127.0f), 127.0f);
+      q1 = (int8_t)fminf(fmaxf(rintf(x1 / sc), -127.0f), 127.0f);
+    }
+    dst[2 * t] = (uint8_t)q0;
+    dst[2 * t + 1] = (uint8_t)q1;
+    if (lane == 0) {
+      const uint16_t hb = zero ? (uint16_t)0 : __half_as_ushort(h);
+      dst[DSA_LAT_DIM + 2 * g] = (uint8_t)(hb & 0xFF);
+      dst[DSA_LAT_DIM + 2 * g + 1] = (uint8_t)(hb >> 8);
+    }
+  }
+  if (t < DSA_ROPE_DIM) reinterpret_cast<uint16_t*>(dst + DSA_LAT_DIM + 16)[t] = rope[t];
+}
+
+// QUANT = false: new_rows holds ready 656-byte rows. QUANT = true: new_rows
+// holds bf16 latents [A][512] and new_rope bf16 RoPE parts [A][64].
+template <bool QUANT>
 __global__ void __launch_bounds__(APP_THREADS)
 k_append(const dsa_unit* __restrict__ units, int A, const uint8_t* __restrict__ new_rows,
-         const uint16_t* __restrict__ new_keys, int32_t* dev_err) {
+         const uint16_t* __restrict__ new_keys, int32_t* dev_err, const uint16_t* __restrict__ new_rope) {
   const int u = blockIdx.x;
   pdl_wait();
   const dsa_unit& un = units[u];
@@ -60,9 +95,15 @@ k_append(const dsa_unit* __restrict__ units, int A, const uint8_t* __restrict__ 
       if (threadIdx.x == 0) dsa_flag(dev_err, DSA_DEVERR_CAPACITY);
       break;
     }
-    const uint4* src = reinterpret_cast<const uint4*>(new_rows + ((size_t)u * A + a) * DSA_ROW_BYTES);
-    uint4* dst = reinterpret_cast<uint4*>(un.ring + (p & (DSA_RING_ROWS - 1)) * DSA_ROW_BYTES);
-    for (int c = threadIdx.x; c < DSA_ROW_BYTES / 16; c += APP_THREADS) dst[c] = src[c];
+    uint8_t* ring_row = un.ring + (p & (DSA_RING_ROWS - 1)) * DSA_ROW_BYTES;
+    if (QUANT) {
+      const uint16_t* lat = reinterpret_cast<const uint16_t*>(new_rows) + ((size_t)u * A + a) * DSA_LAT_DIM;
+      quantize_row_q8g64(ring_row, lat, new_rope + ((size_t)u * A + a) * DSA_ROPE_DIM);
+    } else {
+      const uint4* src = reinterpret_cast<const uint4*>(new_rows + ((size_t)u * A + a) * DSA_ROW_BYTES);
+      uint4* dst = reinterpret_cast<uint4*>(ring_row);
+      for (int c = threadIdx.x; c < DSA_ROW_BYTES / 16; c += APP_THREADS) dst[c] = src[c];
+    }
     const uint4* ks = reinterpret_cast<const uint4*>(new_keys + ((size_t)u * A + a) * DSA_IDX_DIM);
     uint4* kd = reinterpret_cast<uint4*>(un.keys + p * DSA_IDX_DIM);
     if (threadIdx.x < 8) kd[threadIdx.x] = ks[threadIdx.x];
@@ -207,8 +248,17 @@ extern "C" int kv_append_writeback(const dsa_unit* units, int32_t U, int32_t A,
                                    int32_t* dev_err, void* stream) {
   if (!units || !new_rows || !new_keys || U < 1 || U > 65535 || A < 1 || A > DSA_RING_ROWS)
     return DSA_ERR_ARG;
-  return launch_pdl(k_append, dim3(U), dim3(APP_THREADS), 0, static_cast<cudaStream_t>(stream), units, A,
-                    new_rows, new_keys, dev_err);
+  return launch_pdl(k_append<false>, dim3(U), dim3(APP_THREADS), 0, static_cast<cudaStream_t>(stream), units, A,
+                    new_rows, new_keys, dev_err, (const uint16_t*)nullptr);
+}
+
+extern "C" int kv_append_quantize(const dsa_unit* units, int32_t U, int32_t A, const uint16_t* new_latent,
+                                  const uint16_t* new_rope, const uint16_t* new_keys, int32_t* dev_err,
+                                  void* stream) {
+  if (!units || !new_latent || !new_rope || !new_keys || U < 1 || U > 65535 || A < 1 || A > DSA_RING_ROWS)
+    return DSA_ERR_ARG;
+  return launch_pdl(k_append<true>, dim3(U), dim3(APP_THREADS), 0, static_cast<cudaStream_t>(stream), units, A,
+                    reinterpret_cast<const uint8_t*>(new_latent), new_keys, dev_err, new_rope);
 }
 
 extern "C" int kv_flush(const dsa_unit* units, int32_t U, int32_t* dev_err, void* stream) {

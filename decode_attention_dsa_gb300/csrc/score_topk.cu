@@ -105,8 +105,11 @@ __device__ __forceinline__ void unrotate8(uint4 (&x)[8], int s) {
   }
 }
 
+// Two fp32 values as one 64-bit register pair (no arithmetic: register pairing).
 __device__ __forceinline__ unsigned long long pack_f2(float lo, float hi) {
-  return ((unsigned long long)__float_as_uint(hi) << 32) | __float_as_uint(lo);
+  unsigned long long r;
+  asm("mov.b64 %0, {%1, %2};" : "=l"(r) : "f"(lo), "f"(hi));
+  return r;
 }
 
 // d = a * b + d on two packed fp32 lanes (round to nearest, per lane)
@@ -115,7 +118,9 @@ __device__ __forceinline__ void fma2(unsigned long long& d, unsigned long long a
 }
 
 __device__ __forceinline__ float sum2(unsigned long long v) {
-  return __uint_as_float((uint32_t)v) + __uint_as_float((uint32_t)(v >> 32));
+  float lo, hi;
+  asm("mov.b64 {%0, %1}, %2;" : "=f"(lo), "=f"(hi) : "l"(v));
+  return lo + hi;
 }
 
 struct ScoreArgs {

@@ -345,6 +345,22 @@ int kv_append_writeback(const dsa_unit* units, int32_t U, int32_t A,
                         int32_t* dev_err, void* stream);
 
 /*
+ * kv_append_writeback for new rows given in bf16: each row is Q8G64-quantised
+ * once on the GPU before it enters the ring ([P3] section "第二次决策": the
+ * owner quantises a new KV row once and moves the 656-byte packed row; [QNT]
+ * section "三、基本思路": symmetric q = round(w / scale), one scale per 64
+ * values). Per group of 64 latent values: scale = fp16_rn(max|w| / 127) and
+ * q = clamp(rint(w / scale), -127, 127), both divisions IEEE fp32; a group
+ * whose scale is 0 or not finite in fp16 gets scale 0 and zero codes. The
+ * RoPE part is stored as given. Everything else as kv_append_writeback.
+ *   new_latent device bf16 [U][A][512]; new_rope device bf16 [U][A][64];
+ *   new_keys device bf16 [U][A][64].
+ */
+int kv_append_quantize(const dsa_unit* units, int32_t U, int32_t A, const uint16_t* new_latent,
+                       const uint16_t* new_rope, const uint16_t* new_keys, int32_t* dev_err,
+                       void* stream);
+
+/*
  * [P3] section "容量优化必须通过会话生命周期" (capacity work must survive the
  * session lifecycle): before exporting or restoring the full history, flush
  * the log, wait for write-back, and check that the RAM row count has reached

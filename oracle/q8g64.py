@@ -60,3 +60,40 @@ def dequant_latent(rows: np.ndarray) -> np.ndarray:
     q = latent_int8(rows).astype(np.float64)
     s = np.repeat(group_scales(rows), GROUP, axis=-1)
     return q * s
+
+
+def quantize_row(latent_bf16, rope_bf16) -> np.ndarray:
+    """Q8G64-quantise one new KV row (the owner quantises once).
+
+    [QNT] section "三、基本思路": symmetric quantisation ``q = round(w / scale)``,
+    one scale per group of 64. Readings (the pages give the formula only): the
+    group scale is ``fp16_rn(amax / 127)`` with ``amax = max |w|`` over the group
+    (division in float32); ``q = clamp(rint(w / scale), -127, 127)`` with the
+    division in float32 and round-half-to-even; a group with ``amax = 0`` (or a
+    scale that rounds to 0) gets scale 0 and all codes 0; the RoPE part is
+    stored as given. Every rounding is an IEEE float32/float16 operation, the
+    same ones the kernel performs, so both sides take identical integer
+    decisions.
+
+    latent_bf16: uint16 bf16 bits [512]; rope_bf16: uint16 bf16 bits [64].
+    Returns the 656-byte row.
+    """
+    lat = (np.asarray(latent_bf16, dtype=np.uint16).astype(np.uint32) << np.uint32(16)).view(np.float32)
+    row = np.zeros(ROW_BYTES, dtype=np.uint8)
+    q = np.zeros(LAT_DIM, dtype=np.int8)
+    scales = np.zeros(N_GROUPS, dtype="<f2")
+    for g in range(N_GROUPS):
+        x = lat[g * GROUP:(g + 1) * GROUP]
+        amax = np.float32(np.max(np.abs(x)))
+        s16 = np.float16(np.float32(amax) / np.float32(127.0))
+        s = np.float32(s16)
+        scales[g] = s16
+        if s == 0 or not np.isfinite(s):
+            scales[g] = np.float16(0.0)
+            continue
+        r = np.rint(x / s).astype(np.float32)
+        q[g * GROUP:(g + 1) * GROUP] = np.clip(r, -127, 127).astype(np.int8)
+    row[:LAT_DIM] = q.view(np.uint8)
+    row[OFF_SCALES:OFF_ROPE] = scales.view(np.uint8)
+    row[OFF_ROPE:] = np.asarray(rope_bf16, dtype="<u2").view(np.uint8)
+    return row
