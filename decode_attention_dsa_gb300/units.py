@@ -87,6 +87,29 @@ class UnitSet:
         self._l0 = l0t
         abi.hc_init(self.units, self.U, warm, l0t, self.S, self.lmax, self.dev_err, stream)
 
+    STATE_FIELDS = ("keys", "slots", "slot_pos", "pos_slot", "fill_round", "pin_epoch", "ring", "state")
+
+    def export_state(self) -> dict:
+        """Host snapshot of every unit's cache state and mirror. Call kv_flush
+        and let the stream finish first, so that the mirror holds every row
+        (rows_in_ram == len) and the snapshot is complete."""
+        torch.cuda.synchronize(self.device)
+        d = {f: getattr(self, f).cpu().clone() for f in self.STATE_FIELDS}
+        d["mirror"] = (np.array(self.mirror_host) if self.mirror_host is not None
+                       else self.mirror_dev_tensor.cpu().numpy())
+        return d
+
+    def import_state(self, d: dict) -> None:
+        """Restore a snapshot taken by export_state into a unit set of the same
+        shape (plain copies; the unit descriptors stay this set's own)."""
+        for f in self.STATE_FIELDS:
+            getattr(self, f).copy_(d[f].to(self.device))
+        if self.mirror_host is not None:
+            self.mirror_host[...] = d["mirror"]
+        else:
+            self.mirror_dev_tensor.copy_(torch.from_numpy(d["mirror"]).to(self.device))
+        torch.cuda.synchronize(self.device)
+
     def check(self) -> int:
         return int(self.dev_err.item())
 

@@ -132,6 +132,34 @@ def test_flush_makes_ram_complete():
     assert np.array_equal(got, want)
 
 
+def test_export_restore_round_trip():
+    """Flush, export to the host, rebuild a fresh unit set from the snapshot and
+    continue: every later step matches the oracle, which flushed at the same
+    point (the export/restore barrier: RAM rows equal logical rows first)."""
+    from decode_attention_dsa_gb300.step import DecodePath
+    from decode_attention_dsa_gb300.units import UnitSet
+    wl = W.WORKLOADS[0].with_(name="restore", L0=900, S=64, K=96, H=16, steps=50, A=1, warm="last_s")
+    pair = Pair(wl)
+    pair.check_slots = True
+    for st in range(25):
+        g, o = pair.step(st)
+        check_step(pair, g, o)
+    pair.abi.kv_flush(pair.g.units, pair.g.U, pair.g.dev_err)
+    pair.o[0].cache.flush()
+    snap = pair.g.export_state()
+    st0 = snap["state"][0].numpy()
+    assert st0[0] == st0[1] == pair.o[0].cache.length, "flush must bring RAM rows to the logical rows"
+    fresh = UnitSet(pair.g.U, wl.S, wl.lmax, mirror="host")
+    fresh.import_state(snap)
+    pair.g.close()
+    pair.g = fresh
+    pair.p = DecodePath(fresh, wl.R, wl.K, wl.H, wl.A, wl.scale())
+    for st in range(25, 50):
+        g, o = pair.step(st)
+        check_step(pair, g, o)
+    assert fresh.check() == 0
+
+
 def test_append_beyond_capacity_sets_device_flag():
     wl = W.WORKLOADS[0].with_(name="cap", L0=10, S=4, K=4, H=16, steps=1, A=1)
     pair = Pair(wl)
