@@ -54,6 +54,8 @@ def parse():
     ap.add_argument("--impl", choices=["gb300", "reference"], default="gb300")
     ap.add_argument("--no-e2e", action="store_true")
     ap.add_argument("--no-graph", action="store_true", help="launch steps directly, no CUDA graph")
+    ap.add_argument("--reuse-every", type=int, default=1,
+                    help="layer l reuses the selection of layer l - l %% N (1: every layer scores)")
     ap.add_argument("--path", choices=["fused", "split"], default=None,
                     help="fused: hot_gather_attn; split: hot_gather + mla_decode_attn with the append "
                          "overlapping the attention (default: split, the faster one measured)")
@@ -239,6 +241,8 @@ def run_gpu(args, rank: int, world: int):
     from synth import workloads as W
 
     wl = W.WORKLOADS[args.config]
+    if args.reuse_every > 1:
+        wl = wl.with_(reuse_every=args.reuse_every)
     K = args.steps or wl.steps
     Wm = max(3, args.warmup)
     total = Wm + K
@@ -246,9 +250,14 @@ def run_gpu(args, rank: int, world: int):
     U, R, A = wl.U, wl.R, wl.A
     dev = torch.device("cuda")
     units = UnitSet(U, wl.S, wlr.lmax, mirror=args.mirror)
-    path = DecodePath(units, R, wl.K, wl.H, A, wl.scale())
+    src = [wl.selection_source(u) for u in range(U)] if wl.reuse_every > 1 else None
+    path = DecodePath(units, R, wl.K, wl.H, A, wl.scale(), selection_source=src)
     sg.history(wlr, units)
     inp = sg.step_inputs(wlr, 0, total)
+    if path.sources:
+        # only the source units' indexer queries are scored (set up before timing)
+        inp["q_idx"] = inp["q_idx"][:, path.sources].contiguous()
+        inp["w"] = inp["w"][:, path.sources].contiguous()
     torch.cuda.synchronize()
     flush = torch.empty(512 << 20, dtype=torch.uint8, device=dev)
     warm = abi.WARM_LAST_S if wl.warm == "last_s" else abi.WARM_EMPTY
@@ -424,7 +433,7 @@ def run_gpu(args, rank: int, world: int):
     hbm_peak = float(peaks.get("hbm_gbs", FALLBACK_PEAKS["hbm_gbs"]))
     tc_peak = float(peaks.get("bf16_tflops", FALLBACK_PEAKS["bf16_tflops"]))
     mean_L = wl.L0 + (Wm + (K - 1) / 2.0) * A
-    key_bytes = U * mean_L * 128.0                          # per score_topk launch
+    key_bytes = (path.Us if path.sources else U) * mean_L * 128.0   # per score_topk launch
     ent = ctr[:3].sum() / K
     ram_b = ctr[2] / K * 656.0                              # host-link bytes per step
     hbm_rows_b = (ctr[0] + ctr[1]) / K * 656.0 + ctr[3] / K * 656.0
@@ -458,6 +467,7 @@ def run_gpu(args, rank: int, world: int):
         "vs_baseline": None, "dtype": "fp32 score / u8 rows / fp32 attention",
         "data": "synthetic (seeded counter-based generator, generated on the device)",
         "config": workload_config(wl, {"mirror": args.mirror, "l2": "flushed before every timed step",
+                                       "selection_reuse_every": wl.reuse_every,
                                        "path": "hot_gather_attn (fused)" if fused else
                                                "hot_gather + mla_decode_attn, append concurrent",
                                        "parallelism": "replicas" if world > 1 else "single GPU"}),

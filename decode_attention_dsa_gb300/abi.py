@@ -58,6 +58,7 @@ SIGNATURES = {
     "dsa_score_topk_workspace": (_SZ, [_I32, _I32, _I64]),
     "dsa_score_topk": (ctypes.c_int, [_VP, _I32, _I32, _I32, _VP, _VP, _VP, _I64, _VP, _SZ, _VP, _VP]),
     "dsa_score_topk_noalloc": (ctypes.c_int, [_VP, _I32, _I32, _I32, _VP, _VP, _VP, _I64, _VP, _VP]),
+    "dsa_reuse_selection": (ctypes.c_int, [_VP, _VP, _I32, _I32, _I32, _I32, _VP, _VP, _VP]),
     "hot_gather_workspace": (_SZ, [_I32, _I32, _I32]),
     "hot_gather": (ctypes.c_int, [_VP, _I32, _I32, _I32, _I32, _VP, _VP, _VP, _VP, _VP, _SZ, _VP, _VP]),
     "mla_decode_attn_workspace": (_SZ, [_I32, _I32, _I32, _I32]),
@@ -159,6 +160,11 @@ def dsa_score_topk_noalloc(units, U, R, K, q, w, topk_idx, max_len, dev_err, str
     """dsa_score_topk with the library's fixed built-in scratch (no workspace)."""
     return _ok("dsa_score_topk_noalloc", load().dsa_score_topk_noalloc(
         _p(units), U, R, K, _p(q), _p(w), _p(topk_idx), max_len, _p(dev_err), _s(stream)))
+
+
+def dsa_reuse_selection(topk_idx, src_topk, U, Us, R, K, src_of, dev_err, stream=None):
+    return _ok("dsa_reuse_selection", load().dsa_reuse_selection(
+        _p(topk_idx), _p(src_topk), U, Us, R, K, _p(src_of), _p(dev_err), _s(stream)))
 
 
 def hot_gather_workspace(U, R, K) -> int:

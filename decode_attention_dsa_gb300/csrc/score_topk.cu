@@ -756,6 +756,39 @@ extern "C" int dsa_score_topk(const dsa_unit* units, int32_t U, int32_t R, int32
 }
 
 // ---------------------------------------------------------------------------
+// Selection reuse across layers: unit u takes the selection held in row
+// src_of[u] of a compact buffer of the scored (source) units.
+
+namespace {
+
+__global__ void __launch_bounds__(256)
+k_reuse_selection(int32_t* __restrict__ topk, const int32_t* __restrict__ src_topk, int Us, int R, int K,
+                  const int32_t* __restrict__ src_of, int32_t* dev_err) {
+  const int u = blockIdx.y;
+  pdl_wait();
+  const int s = src_of[u];
+  if (s < 0 || s >= Us) {
+    if (blockIdx.x == 0 && threadIdx.x == 0) dsa_flag(dev_err, DSA_DEVERR_BOUNDS);
+    return;
+  }
+  const size_t n = (size_t)R * K;
+  for (size_t i = (size_t)blockIdx.x * blockDim.x + threadIdx.x; i < n; i += (size_t)gridDim.x * blockDim.x)
+    topk[(size_t)u * n + i] = src_topk[(size_t)s * n + i];
+}
+
+}  // namespace
+
+extern "C" int dsa_reuse_selection(int32_t* topk_idx, const int32_t* src_topk, int32_t U, int32_t Us, int32_t R,
+                                   int32_t K, const int32_t* src_of, int32_t* dev_err, void* stream) {
+  if (!topk_idx || !src_topk || !src_of || U < 1 || U > 65535 || Us < 1 || R < 1 || R > DSA_MAX_ROWS)
+    return DSA_ERR_ARG;
+  if (K < 1 || K > DSA_MAX_K) return DSA_ERR_SHAPE;
+  const int bx = (int)std::min<int64_t>(((int64_t)R * K + 255) / 256, 64);
+  return launch_pdl(k_reuse_selection, dim3(bx, U), dim3(256), 0, static_cast<cudaStream_t>(stream), topk_idx,
+                    src_topk, Us, R, K, src_of, dev_err);
+}
+
+// ---------------------------------------------------------------------------
 // dsa_score_topk_noalloc: the same scoring and selection for callers that may
 // not allocate device memory. Its scratch (selection histograms and ordered
 // score keys) lives in one fixed array compiled into this library.

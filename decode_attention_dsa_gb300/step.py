@@ -2,6 +2,8 @@
 persistent workspaces and outputs (marshalling only)."""
 from __future__ import annotations
 
+import ctypes
+
 import torch
 
 from . import abi
@@ -13,13 +15,27 @@ class DecodePath:
     heads and ``A`` appended rows per unit per step."""
 
     def __init__(self, units: UnitSet, R: int, K: int, H: int, A: int, scale: float,
-                 max_len: int | None = None):
+                 max_len: int | None = None, selection_source=None):
+        """``selection_source[u]``: the unit whose selection unit u reuses (a
+        later layer reusing an earlier layer's selection); None: every unit is
+        scored. With reuse, score_topk takes the query rows of the source
+        units only, in ascending unit order."""
         self.u = units
         U = units.U
         self.R, self.K, self.H, self.A, self.scale = R, K, H, A, float(scale)
         self.max_len = units.lmax if max_len is None else max_len
         dev = units.device
-        self.ws_topk_bytes = abi.dsa_score_topk_workspace(U, R, self.max_len)
+        self.sources = None
+        if selection_source is not None and any(int(x) != u for u, x in enumerate(selection_source)):
+            self.sources = sorted(set(int(x) for x in selection_source))
+            self.Us = len(self.sources)
+            raw = units.units.view(-1, ctypes.sizeof(abi.DsaUnit))
+            self.src_units = raw[self.sources].contiguous().view(-1)
+            self.src_of = torch.tensor([self.sources.index(int(x)) for x in selection_source],
+                                       dtype=torch.int32, device=dev)
+            self.src_topk = torch.empty((self.Us, R, K), dtype=torch.int32, device=dev)
+        n_scored = self.Us if self.sources else U
+        self.ws_topk_bytes = abi.dsa_score_topk_workspace(n_scored, R, self.max_len)
         self.ws_topk = torch.zeros(self.ws_topk_bytes, dtype=torch.uint8, device=dev)
         self.ws_gather_bytes = abi.hot_gather_workspace(U, R, K)
         self.ws_gather = torch.zeros(self.ws_gather_bytes, dtype=torch.uint8, device=dev)
@@ -35,6 +51,12 @@ class DecodePath:
 
     def score_topk(self, q_idx, w, stream=None):
         u = self.u
+        if self.sources:
+            abi.dsa_score_topk(self.src_units, self.Us, self.R, self.K, q_idx, w, self.src_topk, self.max_len,
+                               self.ws_topk, self.ws_topk_bytes, u.dev_err, stream)
+            abi.dsa_reuse_selection(self.topk, self.src_topk, u.U, self.Us, self.R, self.K, self.src_of,
+                                    u.dev_err, stream)
+            return
         abi.dsa_score_topk(u.units, u.U, self.R, self.K, q_idx, w, self.topk, self.max_len,
                            self.ws_topk, self.ws_topk_bytes, u.dev_err, stream)
 
@@ -87,6 +109,6 @@ class DecodePath:
         main.wait_stream(side)
 
     def launches_per_step(self) -> int:
-        """Kernel launches one step enqueues (score, select, classify+assign,
-        copy, attention, append)."""
-        return 6
+        """Kernel launches one step enqueues (score, select, [reuse copy],
+        classify+assign, copy, attention, append)."""
+        return 7 if self.sources else 6

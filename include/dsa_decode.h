@@ -219,6 +219,21 @@ int dsa_score_topk_noalloc(const dsa_unit* units, int32_t U, int32_t R, int32_t 
                            const uint16_t* q, const float* w, int32_t* topk_idx,
                            int64_t max_len, int32_t* dev_err, void* stream);
 
+/*
+ * Selection reuse across layers ([P3] section "起点": some later layers reuse
+ * the selection, while every layer keeps its own KV). Score only the source
+ * units (dsa_score_topk on a units array holding just them, output src_topk),
+ * then fill every unit's selection: rows of unit u of topk_idx <- rows of
+ * unit src_of[u] of src_topk. A unit reuses another's selection when its
+ * src_of points at that unit's scored rows; src_of outside [0, Us) sets
+ * DSA_DEVERR_BOUNDS and leaves the unit unchanged. A source should share the
+ * consumer's history (same session).
+ *   topk_idx device int32 [U][R][K] (written); src_topk device int32 [Us][R][K];
+ *   src_of   device int32 [U].
+ */
+int dsa_reuse_selection(int32_t* topk_idx, const int32_t* src_topk, int32_t U, int32_t Us, int32_t R,
+                        int32_t K, const int32_t* src_of, int32_t* dev_err, void* stream);
+
 /* -------------------------------------------------------- A3: hot gather */
 
 /*

@@ -29,10 +29,18 @@ class OracleUnit:
 
 
 def decode_step(unit: OracleUnit, rnd: int, K: int, scale: float, q_idx, w,
-                q_lat, q_rope, new_rows, new_keys, attention: bool = True):
-    """Run one step; returns a dict with scores, topk, cls, rows, counters, out, lse."""
+                q_lat, q_rope, new_rows, new_keys, attention: bool = True, topk=None):
+    """Run one step; returns a dict with scores, topk, cls, rows, counters, out, lse.
+
+    ``topk`` given: the unit reuses that selection (made by an earlier layer of
+    the same session, [P3] section "起点": some later layers reuse the
+    selection while every layer keeps its own KV) and does not score.
+    """
     L = unit.cache.length
-    scores, topk = score_topk(unit.keys[:L], q_idx, w, K)
+    if topk is None:
+        scores, topk = score_topk(unit.keys[:L], q_idx, w, K)
+    else:
+        scores = None
     cls, rows, counters = unit.cache.gather(rnd, topk)
     res = dict(L=L, scores=scores, topk=topk, cls=cls, rows=rows, counters=counters)
     if attention:

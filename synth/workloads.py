@@ -73,11 +73,17 @@ class Workload:
     mode: str = "iid"  # 'iid' | 'mtp' | 'tagged'
     mtp_sd16: int = 8  # perturbation sd in 1/16 units (8 -> sd 0.5, variance 0.25)
     phases: tuple = field(default=())  # tagged: ((steps, bias in 1/16 units), ...)
+    reuse_every: int = 1   # layer l reuses the selection of layer l - l % reuse_every (1: none)
     seed: int = 0
 
     @property
     def U(self) -> int:
         return self.sessions * self.layers
+
+    def selection_source(self, u: int) -> int:
+        """Unit whose selection unit u uses (itself unless it reuses one)."""
+        layer = u % self.layers
+        return u - layer % self.reuse_every
 
     @property
     def lmax(self) -> int:

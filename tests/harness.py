@@ -50,7 +50,8 @@ class Pair:
             if u in self.oidx:
                 self.o[u] = OracleUnit.create(wl.S, wl.lmax, wl.L0, keys, rows, wl.warm)
         self.g.init([wl.L0] * U, abi.WARM_LAST_S if wl.warm == "last_s" else abi.WARM_EMPTY)
-        self.p = DecodePath(self.g, wl.R, wl.K, wl.H, wl.A, wl.scale())
+        src = [wl.selection_source(u) for u in self.uidx] if wl.reuse_every > 1 else None
+        self.p = DecodePath(self.g, wl.R, wl.K, wl.H, wl.A, wl.scale(), selection_source=src)
         torch.cuda.synchronize()
 
     def inputs(self, step):
@@ -60,9 +61,11 @@ class Pair:
 
         def t16(a):
             return torch.from_numpy(np.ascontiguousarray(np.stack(a)).view(np.int16)).to(dev)
+        sel = (lambda a: [a[i] for i, u in enumerate(self.uidx) if self.wl.selection_source(u) == u]) \
+            if self.wl.reuse_every > 1 else (lambda a: a)
         return per, dict(
-            q_idx=t16([x.q_idx for x in per]),
-            w=torch.from_numpy(np.stack([x.w for x in per])).to(dev),
+            q_idx=t16(sel([x.q_idx for x in per])),
+            w=torch.from_numpy(np.stack(sel([x.w for x in per]))).to(dev),
             q_lat=t16([x.q_lat for x in per]),
             q_rope=t16([x.q_rope for x in per]),
             new_rows=torch.from_numpy(np.stack([x.new_rows for x in per])).to(dev),
@@ -100,8 +103,11 @@ class Pair:
             if u not in self.o:
                 continue
             x = per[i]
+            given = None
+            if self.wl.reuse_every > 1 and self.wl.selection_source(u) != u:
+                given = ores[self.wl.selection_source(u)]["topk"]   # sources come first in unit order
             ores[u] = decode_step(self.o[u], ornd, self.wl.K, self.wl.scale(), x.q_idx, x.w, x.q_lat,
-                                  x.q_rope, x.new_rows, x.new_keys, attention=attention)
+                                  x.q_rope, x.new_rows, x.new_keys, attention=attention, topk=given)
         return g, ores
 
     def state(self, i):

@@ -132,6 +132,19 @@ def test_flush_makes_ram_complete():
     assert np.array_equal(got, want)
 
 
+def test_selection_reuse_across_layers():
+    """Layers 1 and 3 reuse the selections of layers 0 and 2 (same session);
+    every layer keeps its own cache."""
+    wl = W.WORKLOADS[0].with_(name="reuse", sessions=2, layers=4, L0=2000, S=128, K=128, H=16, steps=8,
+                              warm="last_s", reuse_every=2)
+    run(wl)
+
+
+@pytest.mark.slow
+def test_selection_reuse_config1_first_steps():
+    run(W.WORKLOADS[1].with_(reuse_every=2), steps=range(8), attention_every=4)
+
+
 def test_export_restore_round_trip():
     """Flush, export to the host, rebuild a fresh unit set from the snapshot and
     continue: every later step matches the oracle, which flushed at the same
