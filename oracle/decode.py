@@ -4,6 +4,11 @@ Order within a step (the pages' per-layer path, [P3] "第三次决策" diagram):
 score all history positions and keep the Top-K ([P3] "起点"), hot gather
 (``hotcache``), dequantise and attend (``attention``), then append the step's
 new rows to the recent ring with batched write-back (``hotcache`` C7).
+
+Pinned by ``tests/test_oracle_decode.py``: a row appended in step t is not a
+candidate before step t + 1, the gather sees the state of the step start (not
+the step's own append or write-back), attention reads the gathered rows, and
+the selection-reuse branch does not score.
 """
 from __future__ import annotations
 
