@@ -18,12 +18,12 @@ LIB_PATH = os.path.join(PKG, "libdsa_decode.so")
 DSA_OK = 0
 DSA_ERR_ARG, DSA_ERR_SHAPE, DSA_ERR_WS, DSA_ERR_CUDA, DSA_ERR_DEVICE_CHECK = -1, -2, -3, -4, -6
 DSA_ERR_SCRATCH_LIMIT = -7
-DEVERR_BOUNDS, DEVERR_CAPACITY, DEVERR_QRANGE, DEVERR_TIMEOUT = 0x1, 0x2, 0x4, 0x8
+DEVERR_BOUNDS, DEVERR_CAPACITY, DEVERR_QRANGE, DEVERR_TIMEOUT, DEVERR_ROUND = 0x1, 0x2, 0x4, 0x8, 0x10
 ROW_BYTES, LAT_DIM, ROPE_DIM, IDX_HEADS, IDX_DIM, RING_ROWS = 656, 512, 64, 8, 64, 64
 MAX_K, MAX_ROWS, MAX_ATTN_K, ROUND_AUTO = 4096, 8, 2048, -1
 CLS_HOT, CLS_RING, CLS_RAM, CLS_PAD = 0, 1, 2, 3
 WARM_EMPTY, WARM_LAST_S = 0, 1
-ST_LEN, ST_RAM, ST_HAND, ST_EPOCH, ST_WRITEBACKS, ST_WORDS = 0, 1, 2, 3, 4, 8
+ST_LEN, ST_RAM, ST_HAND, ST_EPOCH, ST_WRITEBACKS, ST_ROUND, ST_WORDS = 0, 1, 2, 3, 4, 5, 8
 
 
 class DsaError(RuntimeError):
@@ -52,6 +52,7 @@ SIGNATURES = {
     "dsa_abi_version": (ctypes.c_int, []),
     "dsa_status_string": (ctypes.c_char_p, [ctypes.c_int]),
     "dsa_check": (ctypes.c_int, [_I32]),
+    "dsa_wait_selftest": (ctypes.c_int, [_I64, _I32, _VP, _VP]),
     "dsa_host_alloc": (ctypes.c_int, [ctypes.POINTER(_VP), ctypes.POINTER(_VP), _SZ]),
     "dsa_host_free": (ctypes.c_int, [_VP]),
     "hc_init": (ctypes.c_int, [_VP, _I32, _I32, _VP, _I32, _I64, _VP, _VP]),
@@ -128,6 +129,11 @@ dsa_status_string = status_string
 
 def dsa_check(dev_err_value: int) -> int:
     return load().dsa_check(int(dev_err_value))
+
+
+def dsa_wait_selftest(limit_cycles, complete, dev_err, stream=None):
+    return _ok("dsa_wait_selftest", load().dsa_wait_selftest(int(limit_cycles), int(bool(complete)),
+                                                             _p(dev_err), _s(stream)))
 
 
 def dsa_host_alloc(nbytes: int) -> tuple[int, int]:

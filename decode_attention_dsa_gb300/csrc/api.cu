@@ -19,6 +19,7 @@
 #include <cuda_fp16.h>
 
 #include "common.cuh"
+#include "tc.cuh"
 
 namespace {
 
@@ -182,7 +183,28 @@ k_init_slots(const dsa_unit* __restrict__ units, int warm, const int64_t* __rest
                 threadIdx.x & 31);
 }
 
+// The bounded wait every kernel uses, alone: one CTA waits on a barrier
+// phase that completes only if `complete` is set, for at most `limit` cycles.
+__global__ void k_wait_selftest(long long limit, int complete, int32_t* dev_err) {
+  __shared__ uint64_t bar;
+  if (threadIdx.x == 0) {
+    tc::mbar_init(&bar, 1);
+    tc::fence_mbar_init();
+  }
+  __syncthreads();
+  if (complete && threadIdx.x == 0) tc::mbar_arrive(&bar);
+  const bool ok = tc::mbar_wait(&bar, 0, limit);
+  if (__syncthreads_or(!ok) && threadIdx.x == 0) dsa_flag(dev_err, DSA_DEVERR_TIMEOUT);
+}
+
 }  // namespace
+
+extern "C" int dsa_wait_selftest(int64_t limit_cycles, int32_t complete, int32_t* dev_err, void* stream) {
+  if (!dev_err || limit_cycles < 0) return DSA_ERR_ARG;
+  k_wait_selftest<<<1, 32, 0, static_cast<cudaStream_t>(stream)>>>((long long)limit_cycles, complete ? 1 : 0,
+                                                                   dev_err);
+  return dsa_launch_status();
+}
 
 extern "C" int dsa_abi_version(void) { return 1; }
 

@@ -1,7 +1,10 @@
 // Shared helpers of the decode-path kernels (device code for sm_103a).
 #pragma once
 
+#include <atomic>
 #include <cstdint>
+#include <mutex>
+
 #include <cuda_runtime.h>
 
 #include "dsa_decode.h"
@@ -18,6 +21,35 @@ static inline int dsa_launch_status() {
 }
 
 static inline size_t dsa_align(size_t x, size_t a) { return (x + a - 1) / a * a; }
+
+// One-time set-up per device (kernel attributes, SM count), keyed by the
+// current device ordinal: a process that uses several GPUs sets every one up,
+// and host threads that make their first calls at the same time are
+// serialised. `init(dev)` returns a DSA_ status; a failed set-up is retried
+// on the next call.
+constexpr int DSA_MAX_DEVICES = 64;
+struct DsaPerDevice {
+  std::mutex mu;
+  std::atomic<bool> ready[DSA_MAX_DEVICES] = {};
+  int num_sms[DSA_MAX_DEVICES] = {};
+};
+
+template <typename F>
+static inline int dsa_device_setup(DsaPerDevice& pd, int* dev_out, F&& init) {
+  int dev = -1;
+  if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= DSA_MAX_DEVICES) return DSA_ERR_CUDA;
+  *dev_out = dev;
+  if (pd.ready[dev].load(std::memory_order_acquire)) return DSA_OK;
+  std::lock_guard<std::mutex> lock(pd.mu);
+  if (pd.ready[dev].load(std::memory_order_relaxed)) return DSA_OK;
+  int sms = 0;
+  if (cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess) return DSA_ERR_CUDA;
+  const int st = init(dev);
+  if (st != DSA_OK) return st;
+  pd.num_sms[dev] = sms;
+  pd.ready[dev].store(true, std::memory_order_release);
+  return DSA_OK;
+}
 
 __device__ __forceinline__ void dsa_flag(int32_t* dev_err, int32_t bit) {
   if (dev_err) atomicOr(dev_err, bit);

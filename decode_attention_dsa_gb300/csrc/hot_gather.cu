@@ -77,14 +77,21 @@ k_assign(const dsa_unit* __restrict__ units, int R, int K, int round,
   uint8_t* s_fl = s_cl + RK;                                                   // [RK] owner flags
   pdl_wait();
   const dsa_unit& un = units[u];
-  if (!unit_aligned(un)) {
+  const int32_t epoch = (int32_t)(un.state[DSA_ST_EPOCH] + 1);
+  if (round < 0) round = epoch - 1;
+  // a unit whose arrays are misaligned, or a round below the unit's previous
+  // one (it would break the visibility rule), is skipped: every entry PAD
+  // (k_copy zeroes its compact row), no fill, state untouched
+  const bool misaligned = !unit_aligned(un);
+  if (misaligned || (int64_t)round + 1 < un.state[DSA_ST_ROUND]) {
     if (threadIdx.x == 0) {
-      dsa_flag(dev_err, DSA_DEVERR_BOUNDS);
+      dsa_flag(dev_err, misaligned ? DSA_DEVERR_BOUNDS : DSA_DEVERR_ROUND);
       g.nfill[u] = 0;
+      for (int i = 0; i < 4; ++i) counters[(size_t)u * 4 + i] = 0;
     }
     for (int e = threadIdx.x; e < RK; e += ASSIGN_THREADS) {
       cls_all[(size_t)u * RK + e] = DSA_CLS_PAD;
-      g.served[(size_t)u * RK + e] = 1;   // nothing for k_copy to read
+      g.served[(size_t)u * RK + e] = 0;
       g.fill_of[(size_t)u * RK + e] = -1;
     }
     return;
@@ -97,8 +104,6 @@ k_assign(const dsa_unit* __restrict__ units, int R, int K, int round,
   int32_t* fill_entry = g.fill_entry + (size_t)u * RK;
   uint8_t* served = g.served + (size_t)u * RK;
   const int S = un.slots_n;
-  const int32_t epoch = (int32_t)(un.state[DSA_ST_EPOCH] + 1);
-  if (round < 0) round = epoch - 1;
   const int64_t len = un.state[DSA_ST_LEN];
   const int64_t ram = un.state[DSA_ST_RAM];
 
@@ -283,6 +288,7 @@ k_assign(const dsa_unit* __restrict__ units, int R, int K, int round,
       un.state[DSA_ST_HAND] = h >= S ? 0 : h;
     }
     un.state[DSA_ST_EPOCH] = epoch;
+    un.state[DSA_ST_ROUND] = (int64_t)round + 1;
     g.nfill[u] = n;
     int32_t* cu = counters + (size_t)u * 4;
     cu[0] = s_cnt[0];
@@ -361,12 +367,14 @@ int dsa_launch_assign(const dsa_unit* units, int32_t U, int32_t R, int32_t K, in
                       cudaStream_t st) {
   GatherWs g = gather_ws(ws, U, R, K);
   const int RK = R * K;
-  static bool attr_done = false;
-  if (!attr_done) {
+  static DsaPerDevice pd;
+  int dev = 0;
+  const int ok = dsa_device_setup(pd, &dev, [](int) {
     DSA_CUDA_TRY(cudaFuncSetAttribute(k_assign, cudaFuncAttributeMaxDynamicSharedMemorySize,
                                       (int)assign_smem(DSA_MAX_ROWS * DSA_MAX_K)));
-    attr_done = true;
-  }
+    return DSA_OK;
+  });
+  if (ok != DSA_OK) return ok;
   return launch_pdl(k_assign, dim3(U), dim3(ASSIGN_THREADS), assign_smem(RK), st, units, R, K, round, topk_idx,
                     cls, counters, g, dev_err);
 }

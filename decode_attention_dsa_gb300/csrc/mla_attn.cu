@@ -7,8 +7,9 @@
 // w_hat = scale * q, one scale per group of 64 (G64). [P3] "From 1M total to
 // 15+ x 1M", section "起点": a row is 512 B latent + 16 B scales + 128 B RoPE.
 //
-// One thread-block cluster per (unit, query row); CTA c of the cluster owns
-// selected rows [128c, 128c + 128):
+// One thread-block cluster per (unit, query row), of ceil(K / 128) CTAs
+// rounded up to a power of two; CTA c of the cluster owns selected rows
+// [128c, 128c + 128) (none for the padding CTAs):
 //  1. one 1-D bulk TMA copy brings the CTA's rows (up to 128 x 656 B) into
 //     shared memory region X;
 //  2. dequantisation writes an fp16 tile [128 rows][576] (latent int8 * fp16
@@ -90,6 +91,17 @@ struct MergeScratch {
 };
 static_assert(sizeof(MergeScratch) <= X_BYTES, "merge scratch");
 
+// CTAs per cluster for K selected rows: ceil(K / 128) rounded up to a power
+// of two (at most 16 for K <= 2048). The merge splits the 512 output columns
+// evenly over the cluster, so the count must divide 512; the CTAs past the
+// last row hold no rows and add an empty softmax part (max -inf, sum 0).
+inline int cluster_ctas(int K) {
+  const int need = (K + NC - 1) / NC;
+  int C = 1;
+  while (C < need) C *= 2;
+  return C;
+}
+
 __device__ __forceinline__ uint32_t pack_h2(float a, float b) {
   const __half2 h = __floats2half2_rn(a, b);
   return *reinterpret_cast<const uint32_t*>(&h);
@@ -135,7 +147,11 @@ k_mla_attn(int R, int H, int K, const uint16_t* __restrict__ q_lat, const uint16
   bool failed = ms->fail != 0;
   pdl_wait();   // everything above touched only this CTA's shared and tensor memory
 
-  if (!GATHER && tid == 0 && !failed && nrows > 0) {
+  // The rows of a CTA arrive by one bulk copy on phase 0 of bar[0]; a CTA
+  // without rows (the cluster is padded to a power of two) issues none, so
+  // the merge's copies below complete phase 0 there and phase 1 elsewhere.
+  const bool rows_copy = !GATHER && !failed && nrows > 0;
+  if (rows_copy && tid == 0) {
     const uint32_t bytes = (uint32_t)nrows * DSA_ROW_BYTES;
     tc::mbar_arrive_expect_tx(&ms->bar[0], bytes);
     tc::bulk_g2s(sX, rows + ((size_t)ur * K + j0) * DSA_ROW_BYTES, bytes, &ms->bar[0]);
@@ -209,7 +225,7 @@ k_mla_attn(int R, int H, int K, const uint16_t* __restrict__ q_lat, const uint16
                      : *reinterpret_cast<const uint4*>(q_rope + qo * 64 + 8 * (c - 64));
     }
   }
-  if (!GATHER && !failed && nrows > 0 && !tc::mbar_wait(&ms->bar[0], 0)) atomicOr(&ms->fail, 1);
+  if (rows_copy && !tc::mbar_wait(&ms->bar[0], 0)) atomicOr(&ms->fail, 1);
   __syncthreads();
   failed = ms->fail != 0;
 
@@ -413,7 +429,8 @@ k_mla_attn(int R, int H, int K, const uint16_t* __restrict__ q_lat, const uint16
     MergeScratch* mg = reinterpret_cast<MergeScratch*>(sX);
     float* buf = reinterpret_cast<float*>(sY);           // [C][64][W] = 128 KB
     const uint32_t blk_bytes = 64u * (uint32_t)W * 4u;
-    if (tid == 0) {
+    // (a CTA that already failed issues no copy: nothing of it stays in flight)
+    if (tid == 0 && !failed) {
       tc::mbar_arrive_expect_tx(&ms->bar[0], blk_bytes * (uint32_t)C);
       for (int c = 0; c < C; ++c)
         tc::bulk_g2s(buf + (size_t)c * 64 * W,
@@ -440,7 +457,7 @@ k_mla_attn(int R, int H, int K, const uint16_t* __restrict__ q_lat, const uint16
       mg->inv[h] = L > 0.f ? 1.f / L : 0.f;
       if (crank == 0 && lse && h < H) lse[(size_t)ur * H + h] = L > 0.f ? M + logf(L) : -INFINITY;
     }
-    const bool got = tc::mbar_wait(&ms->bar[0], GATHER ? 0 : 1);   // the merge copy's phase of the TMA barrier
+    const bool got = !failed && tc::mbar_wait(&ms->bar[0], rows_copy ? 1u : 0u);   // the merge copies' phase
     if (!got) atomicOr(&ms->fail, 1);
     __syncthreads();
     const int nq = W / 4;
@@ -483,13 +500,15 @@ template <bool GATHER>
 int launch_attn(int32_t U, int32_t R, int32_t H, int32_t K, const uint16_t* q_lat, const uint16_t* q_rope,
                 const uint8_t* rows, const int32_t* topk_idx, float scale, float* out, float* lse, float* ws_o,
                 int32_t* dev_err, const dsa_unit* units, const uint8_t* cls, GatherWs g, cudaStream_t st) {
-  static bool attr_done = false;
-  if (!attr_done) {
+  static DsaPerDevice pd;
+  int dev = 0;
+  const int ok = dsa_device_setup(pd, &dev, [](int) {
     DSA_CUDA_TRY(cudaFuncSetAttribute(k_mla_attn<GATHER>, cudaFuncAttributeMaxDynamicSharedMemorySize, SMEM_BYTES));
     DSA_CUDA_TRY(cudaFuncSetAttribute(k_mla_attn<GATHER>, cudaFuncAttributeNonPortableClusterSizeAllowed, 1));
-    attr_done = true;
-  }
-  const int C = (K + NC - 1) / NC;
+    return DSA_OK;
+  });
+  if (ok != DSA_OK) return ok;
+  const int C = cluster_ctas(K);
   cudaLaunchConfig_t cfg = {};
   cfg.gridDim = dim3(C, U * R, 1);
   cfg.blockDim = dim3(THREADS, 1, 1);
@@ -508,13 +527,6 @@ int launch_attn(int32_t U, int32_t R, int32_t H, int32_t K, const uint16_t* q_la
                          out, lse, ws_o, dev_err, units, cls, g) != cudaSuccess)
     return DSA_ERR_CUDA;
   return dsa_launch_status();
-}
-
-// K <= 2048 needs C = ceil(K / 128) CTAs per cluster; the merge splits the
-// 512 output columns evenly, so C must divide 512 (1, 2, 4, 8, 16)
-inline bool cluster_ok(int K) {
-  const int C = (K + NC - 1) / NC;
-  return C == 1 || C == 2 || C == 4 || C == 8 || C == 16;
 }
 
 }  // namespace

@@ -264,15 +264,14 @@ __global__ void __launch_bounds__(SCORE_THREADS, 4) k_dsa_score(ScoreArgs a) {
       for (int i = tid; i < R * 512; i += SCORE_THREADS) sq[i] = bf16f(a.q[(size_t)u * R * 512 + i]);
       __syncthreads();   // the new query rows are complete before any thread reads them
     }
-    const bool ok = tc::mbar_wait(&bar[stage], stage == 0 ? parity0 : parity1);
-    if (stage == 0) parity0 ^= 1u; else parity1 ^= 1u;
-    if (!ok) break;                       // bounded wait; does not happen in normal runs
+    const uint32_t par = stage == 0 ? parity0 : parity1;
+    const bool ok = tc::mbar_wait(&bar[stage], par);   // bounded
     const uint8_t* stg = stg0 + stage * TP * 128;
     // ---- scores: thread = position; its key row comes straight from the
     //      staged tile and is widened in registers
     const int p = tid;
     float score[DSA_MAX_ROWS];
-    if (p < n) {
+    if (p < n && ok) {
       uint4 ch[8];
       const uint4* row = reinterpret_cast<const uint4*>(stg + p * 128);
       const int s = p & 7;
@@ -307,7 +306,21 @@ __global__ void __launch_bounds__(SCORE_THREADS, 4) k_dsa_score(ScoreArgs a) {
         if (r < DSA_MAX_ROWS) score[r] = sc;
       }
     }
-    __syncthreads();
+    if (__syncthreads_or(!ok)) {
+      // A copy did not land in time (this does not happen in normal runs).
+      // Every thread leaves together; the copies in flight get one more
+      // bounded wait so that none lands after the CTA is gone, and the
+      // unit's histogram is not flushed (the call's selection is void).
+      if (tid == 0) {
+        dsa_flag(a.dev_err, DSA_DEVERR_TIMEOUT);
+        tc::mbar_wait(&bar[stage], par);
+        const int o = stage ^ 1;
+        if (nxt[o] < ntiles) tc::mbar_wait(&bar[o], o == 0 ? parity0 : parity1);
+      }
+      __syncthreads();
+      return;
+    }
+    if (stage == 0) parity0 ^= 1u; else parity1 ^= 1u;
     {
       const int other = stage == 0 ? nxt[1] : nxt[0];
       const int kn = other < ntiles ? next_valid(other + 1) : ntiles;
@@ -695,7 +708,7 @@ inline size_t select_smem() {
   return SEL_KC_OFF + (size_t)(SEL_KEY_CACHE + SEL_CAND_CAP + SEL_ALL_CAP) * 4;
 }
 
-int g_num_sms = 0;
+DsaPerDevice g_setup;   // kernel attributes and SM count, per device
 
 }  // namespace
 
@@ -716,18 +729,17 @@ extern "C" int dsa_score_topk(const dsa_unit* units, int32_t U, int32_t R, int32
   if (!ws || ws_bytes < dsa_score_topk_workspace(U, R, max_len)) return DSA_ERR_WS;
   cudaStream_t st = static_cast<cudaStream_t>(stream);
   TopkWs tw = topk_ws(ws, U, R, max_len);
-  static bool attr_done = false;
-  if (!attr_done) {
+  int dev = 0;
+  const int ok = dsa_device_setup(g_setup, &dev, [](int) {
     size_t mx = 0;
     for (int r = 1; r <= DSA_MAX_ROWS; ++r) mx = std::max(mx, score_smem(r));
     DSA_CUDA_TRY(cudaFuncSetAttribute(k_dsa_score, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)mx));
     DSA_CUDA_TRY(cudaFuncSetAttribute(k_topk_select, cudaFuncAttributeMaxDynamicSharedMemorySize,
                                       (int)select_smem()));
-    int dev = 0;
-    DSA_CUDA_TRY(cudaGetDevice(&dev));
-    DSA_CUDA_TRY(cudaDeviceGetAttribute(&g_num_sms, cudaDevAttrMultiProcessorCount, dev));
-    attr_done = true;
-  }
+    return DSA_OK;
+  });
+  if (ok != DSA_OK) return ok;
+  const int num_sms = g_setup.num_sms[dev];
   const int TP = score_tile(R);
   const int64_t tpu = (max_len + TP - 1) / TP;
   if (tpu > 0) {
@@ -747,7 +759,7 @@ extern "C" int dsa_score_topk(const dsa_unit* units, int32_t U, int32_t R, int32
     a.TP = TP;
     a.dev_err = dev_err;
     const int per_sm = (int)std::max<size_t>(1, std::min<size_t>(4, 232448 / (score_smem(R) + 1024)));
-    const int64_t grid = std::min<int64_t>(tpu * U, (int64_t)per_sm * (g_num_sms > 0 ? g_num_sms : 148));
+    const int64_t grid = std::min<int64_t>(tpu * U, (int64_t)per_sm * num_sms);
     if (launch_pdl(k_dsa_score, dim3((unsigned)grid), dim3(SCORE_THREADS), score_smem(R), st, a) != DSA_OK)
       return DSA_ERR_CUDA;
   }
@@ -800,12 +812,12 @@ constexpr int64_t NOALLOC_MAX_LEN = 65536;      // history positions per unit
 constexpr size_t NOALLOC_HIST_BYTES = (size_t)NOALLOC_MAX_UR * HIST1_BINS * 4;   // 256 KiB
 constexpr size_t NOALLOC_BYTES =
     NOALLOC_HIST_BYTES + (size_t)NOALLOC_MAX_UR * NOALLOC_MAX_LEN * 4;           // 4.25 MiB
-constexpr int NOALLOC_MAX_DEVICES = 64;
-
 static __device__ __align__(256) uint8_t g_topk_scratch[NOALLOC_BYTES];
 
-// Device address of g_topk_scratch, per device ordinal (looked up once).
-void* g_topk_scratch_addr[NOALLOC_MAX_DEVICES];
+// Device address of g_topk_scratch, per device ordinal (looked up once, under
+// a lock so that host threads making first calls at the same time agree).
+std::atomic<void*> g_topk_scratch_addr[DSA_MAX_DEVICES];
+std::mutex g_topk_scratch_mu;
 
 }  // namespace
 
@@ -817,15 +829,20 @@ extern "C" int dsa_score_topk_noalloc(const dsa_unit* units, int32_t U, int32_t 
   if (K < 1 || K > DSA_MAX_K) return DSA_ERR_SHAPE;
   if ((int64_t)U * R > NOALLOC_MAX_UR || max_len > NOALLOC_MAX_LEN) return DSA_ERR_SCRATCH_LIMIT;
   int dev = -1;
-  if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= NOALLOC_MAX_DEVICES) return DSA_ERR_CUDA;
-  if (!g_topk_scratch_addr[dev]) {
+  if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= DSA_MAX_DEVICES) return DSA_ERR_CUDA;
+  void* scratch = g_topk_scratch_addr[dev].load(std::memory_order_acquire);
+  if (!scratch) {
     // First call on this device: host code cannot use the array's name as a
     // device address, so ask the runtime for it (the device must be current).
-    void* p = nullptr;
-    if (cudaGetSymbolAddress(&p, g_topk_scratch) != cudaSuccess || !p) return DSA_ERR_CUDA;
-    g_topk_scratch_addr[dev] = p;
+    std::lock_guard<std::mutex> lock(g_topk_scratch_mu);
+    scratch = g_topk_scratch_addr[dev].load(std::memory_order_relaxed);
+    if (!scratch) {
+      void* p = nullptr;
+      if (cudaGetSymbolAddress(&p, g_topk_scratch) != cudaSuccess || !p) return DSA_ERR_CUDA;
+      g_topk_scratch_addr[dev].store(p, std::memory_order_release);
+      scratch = p;
+    }
   }
-  void* scratch = g_topk_scratch_addr[dev];
   const size_t need = dsa_score_topk_workspace(U, R, max_len);
   if (need > NOALLOC_BYTES) return DSA_ERR_SCRATCH_LIMIT;
   // The array keeps whatever the previous call left; the histograms must

@@ -55,6 +55,7 @@ extern "C" {
 #define DSA_DEVERR_CAPACITY 0x2   /* append beyond the unit's lmax                */
 #define DSA_DEVERR_QRANGE 0x4     /* attention operand outside the fp16 range    */
 #define DSA_DEVERR_TIMEOUT 0x8    /* a bounded wait inside a kernel gave up        */
+#define DSA_DEVERR_ROUND 0x10     /* hot_gather round below the unit's last round */
 
 #define DSA_ROW_BYTES 656         /* Q8G64 MLA row: 512 int8 + 8 fp16 + 64 bf16   */
 #define DSA_LAT_DIM 512
@@ -81,6 +82,7 @@ extern "C" {
 #define DSA_ST_HAND 2             /* ring-replacement hand                        */
 #define DSA_ST_EPOCH 3            /* gather-call counter (pins are per call)      */
 #define DSA_ST_WRITEBACKS 4       /* number of write-back batches issued          */
+#define DSA_ST_ROUND 5            /* last hot_gather round + 1 (0: none yet)      */
 #define DSA_ST_WORDS 8
 
 /*
@@ -131,6 +133,17 @@ const char* dsa_status_string(int status);
 /* Map a device error word read back from `dev_err` to a status:
  * DSA_OK if it is 0, else DSA_ERR_DEVICE_CHECK. */
 int dsa_check(int32_t dev_err_value);
+
+/*
+ * Diagnostic of the failure path that every kernel's bounded waits share: a
+ * one-CTA kernel waits on a barrier phase for at most `limit_cycles` SM
+ * cycles. With `complete` = 0 nothing completes the phase, the wait gives up
+ * and DSA_DEVERR_TIMEOUT is OR-ed into *dev_err (so dsa_check reports
+ * DSA_ERR_DEVICE_CHECK) while the context stays usable; with `complete` != 0
+ * the phase completes first and the word is untouched. Nothing is left in
+ * flight either way.
+ */
+int dsa_wait_selftest(int64_t limit_cycles, int32_t complete, int32_t* dev_err, void* stream);
 
 /*
  * Pinned, mapped host memory for a unit's RAM mirror ([P3] section
@@ -262,8 +275,11 @@ int dsa_reuse_selection(int32_t* topk_idx, const int32_t* src_topk, int32_t U, i
  *             exactly as read from their source (PAD entries are zeroed).
  *   counters  device int32 [U][4]: HOT, RING, RAM entries, slots filled.
  *   ws        device workspace of hot_gather_workspace(U, R, K) bytes.
- * Shapes: 1 <= U, 1 <= R <= 8, 1 <= K <= 4096. `round` should not decrease
- * from call to call on a unit (a repeated round is allowed). A negative
+ * Shapes: 1 <= U, 1 <= R <= 8, 1 <= K <= 4096. `round` must not decrease
+ * from call to call on a unit (a repeated round is allowed): a call whose
+ * round is below the unit's previous one would break the visibility rule, so
+ * it sets DSA_DEVERR_ROUND and leaves that unit's state unchanged (its
+ * entries come back DSA_CLS_PAD with zeroed rows and zero counters). A negative
  * `round` (DSA_ROUND_AUTO) uses each unit's state[DSA_ST_EPOCH], the number of
  * earlier hot_gather calls on it, so one call per decode step gives rounds
  * 0, 1, 2, ... with fixed arguments (e.g. inside a captured CUDA graph).
@@ -302,7 +318,8 @@ int hot_gather(const dsa_unit* units, int32_t U, int32_t R, int32_t K,
  *           one 64 x 512 fp32 partial output per CTA, written and read back
  *           within the launch (it stays in L2).
  * Shapes: H in {16, 32, 48, 64}, 1 <= K <= DSA_MAX_ATTN_K, U * R <= 65535.
- * One thread-block cluster of ceil(K / 128) CTAs per (unit, query row).
+ * One thread-block cluster per (unit, query row) of ceil(K / 128) CTAs
+ * rounded up to a power of two (CTAs past the last row hold none).
  */
 size_t mla_decode_attn_workspace(int32_t U, int32_t R, int32_t H, int32_t K);
 int mla_decode_attn(int32_t U, int32_t R, int32_t H, int32_t K,

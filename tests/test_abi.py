@@ -78,6 +78,14 @@ def test_host_side_validation(lib):
     assert L.kv_append_writeback(fake, 1, 65, fake, fake, None, None) == lib.DSA_ERR_ARG
     assert L.kv_flush(None, 1, None, None) == lib.DSA_ERR_ARG
     assert L.hc_init(fake, 1, 7, fake, 4, 10, None, None) == lib.DSA_ERR_ARG
+    assert L.dsa_wait_selftest(100, 0, None, None) == lib.DSA_ERR_ARG
+    assert L.dsa_wait_selftest(-1, 0, fake, None) == lib.DSA_ERR_ARG
+    # attention: K beyond 2048 or H off the 16-grid are refused before any launch
+    for K in (0, 2049, 4096):
+        assert L.mla_decode_attn(1, 1, 64, K, fake, fake, fake, fake, 0.04, fake, None, fake, 1 << 30,
+                                 None, None) == lib.DSA_ERR_SHAPE
+        assert L.hot_gather_attn(fake, 1, 1, K, 64, 0, fake, fake, fake, 0.04, fake, fake, fake, None,
+                                 fake, 1 << 30, None, None) == lib.DSA_ERR_SHAPE
     h, d = ctypes.c_void_p(), ctypes.c_void_p()
     assert L.dsa_host_alloc(None, ctypes.byref(d), 16) == lib.DSA_ERR_ARG
     assert L.dsa_host_alloc(ctypes.byref(h), ctypes.byref(d), 0) == lib.DSA_ERR_ARG

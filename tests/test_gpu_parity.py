@@ -55,6 +55,11 @@ SMALL = [
     dict(L0=9000, S=300, R=3, A=2, K=1000, H=64, warm="last_s", mode="mtp", steps=4),
     # K = 1 and tiny history
     dict(L0=5, S=4, R=1, A=1, K=1, H=16, warm="empty", steps=70),
+    # cluster sizes that are not powers of two before padding: 3 -> 4, 5 -> 8,
+    # 12 -> 16 CTAs (the padding CTAs hold no rows)
+    dict(L0=2500, S=512, R=1, A=1, K=300, H=16, warm="last_s", steps=4),
+    dict(L0=3000, S=700, R=2, A=2, K=640, H=32, warm="empty", steps=3),
+    dict(L0=5000, S=2048, R=1, A=1, K=1500, H=64, warm="last_s", steps=3),
 ]
 
 
@@ -97,6 +102,7 @@ FUSED = [
                          steps=20),
     W.WORKLOADS[0].with_(name="fused-ragged", L0=3 * 512 + 37, S=256, K=200, H=48, warm="last_s", steps=6),
     W.WORKLOADS[0].with_(name="fused-evict", L0=700, S=16, K=64, H=16, warm="empty", steps=70),
+    W.WORKLOADS[0].with_(name="fused-pad3", L0=2500, S=512, K=300, H=16, warm="last_s", steps=4),
 ]
 
 
@@ -171,6 +177,42 @@ def test_export_restore_round_trip():
         g, o = pair.step(st)
         check_step(pair, g, o)
     assert fresh.check() == 0
+
+
+def test_decreasing_round_is_refused_on_the_device():
+    """A gather whose round is below the unit's previous round would break the
+    visibility rule: the unit is left unchanged and DSA_DEVERR_ROUND is set."""
+    wl = W.WORKLOADS[0].with_(name="round", L0=600, S=32, K=48, H=16, steps=4, warm="empty")
+    pair, _ = run(wl, rnds=[0, 1, 2, 3])
+    torch, abi, g, p = pair.torch, pair.abi, pair.g, pair.p
+    before = {k: getattr(g, k).clone() for k in ("slot_pos", "pos_slot", "fill_round", "state", "slots")}
+    p.gather(2)
+    torch.cuda.synchronize()
+    assert g.check() == abi.DEVERR_ROUND
+    assert (p.cls == abi.CLS_PAD).all() and (p.counters == 0).all() and (p.rows == 0).all()
+    for k, v in before.items():
+        assert torch.equal(getattr(g, k), v), f"{k} changed"
+    g.dev_err.zero_()
+    p.gather(3)                      # the same round again is allowed
+    torch.cuda.synchronize()
+    assert g.check() == 0
+
+
+def test_bounded_wait_gives_up_with_an_error_status():
+    """The bounded wait every kernel uses: a phase that nothing completes makes
+    it give up after its limit and report DSA_DEVERR_TIMEOUT; the context stays
+    usable (a completed phase right after reports nothing)."""
+    import torch
+    from decode_attention_dsa_gb300 import abi
+    err = torch.zeros(1, dtype=torch.int32, device="cuda")
+    abi.dsa_wait_selftest(1 << 16, False, err)
+    torch.cuda.synchronize()
+    assert int(err.item()) == abi.DEVERR_TIMEOUT
+    assert abi.dsa_check(int(err.item())) == abi.DSA_ERR_DEVICE_CHECK
+    err.zero_()
+    abi.dsa_wait_selftest(1 << 16, True, err)
+    torch.cuda.synchronize()
+    assert int(err.item()) == 0
 
 
 def test_append_beyond_capacity_sets_device_flag():
