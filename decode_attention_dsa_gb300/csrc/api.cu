@@ -16,6 +16,8 @@
 #include <algorithm>
 #include <cstring>
 
+#include <unistd.h>
+
 #include <cuda_fp16.h>
 
 #include "common.cuh"
@@ -183,6 +185,22 @@ k_init_slots(const dsa_unit* __restrict__ units, int warm, const int64_t* __rest
                 threadIdx.x & 31);
 }
 
+// One 16-byte read per `stride` bytes of each unit's mirror: the GPU's
+// address translations for the whole mirror are set up here, at set-up time,
+// instead of by the first decode steps' misses (random rows spread over
+// gigabytes of host memory paid several milliseconds per step for them).
+__global__ void __launch_bounds__(INIT_THREADS)
+k_touch_mirror(const dsa_unit* __restrict__ units, int64_t stride) {
+  const dsa_unit& un = units[blockIdx.y];
+  if (!unit_aligned(un) || un.lmax <= 0) return;
+  const int64_t bytes = un.lmax * DSA_ROW_BYTES;
+  for (int64_t i = (int64_t)blockIdx.x * INIT_THREADS + threadIdx.x; i * stride < bytes;
+       i += (int64_t)gridDim.x * INIT_THREADS) {
+    uint32_t v;
+    asm volatile("ld.global.nc.L1::no_allocate.u32 %0, [%1];" : "=r"(v) : "l"(un.mirror + i * stride));
+  }
+}
+
 // The bounded wait every kernel uses, alone: one CTA waits on a barrier
 // phase that completes only if `complete` is set, for at most `limit` cycles.
 __global__ void k_wait_selftest(long long limit, int complete, int32_t* dev_err) {
@@ -262,6 +280,13 @@ extern "C" int hc_init(const dsa_unit* units, int32_t U, int32_t warm, const int
     k_init_slots<<<dim3((unsigned)gs, U), INIT_THREADS, 0, st>>>(units, warm, l0);
     if (dsa_launch_status() != DSA_OK) return DSA_ERR_CUDA;
   }
+  // touch every host page of the mirrors (page size of this host)
+  const long pg = sysconf(_SC_PAGESIZE);
+  const int64_t stride = pg >= 16 ? (int64_t)pg / 16 * 16 : 4096;
+  const int64_t pages = (max_lmax * DSA_ROW_BYTES + stride - 1) / stride;
+  const int64_t gt = std::min<int64_t>(std::max<int64_t>((pages + INIT_THREADS - 1) / INIT_THREADS, 1), 1024);
+  k_touch_mirror<<<dim3((unsigned)gt, U), INIT_THREADS, 0, st>>>(units, stride);
+  if (dsa_launch_status() != DSA_OK) return DSA_ERR_CUDA;
   return DSA_OK;
 }
 

@@ -20,7 +20,7 @@ static inline int dsa_launch_status() {
   return cudaGetLastError() == cudaSuccess ? DSA_OK : DSA_ERR_CUDA;
 }
 
-static inline size_t dsa_align(size_t x, size_t a) { return (x + a - 1) / a * a; }
+__host__ __device__ static inline size_t dsa_align(size_t x, size_t a) { return (x + a - 1) / a * a; }
 
 // One-time set-up per device (kernel attributes, SM count), keyed by the
 // current device ordinal: a process that uses several GPUs sets every one up,

@@ -10,21 +10,20 @@
 // kernel time they saved, so here the whole select is one clustered launch.
 //
 // Design (GB300):
-//  * k_dsa_score: a persistent grid (up to four CTAs per SM) walks the flattened
-//    (unit, tile) space. Each 128-position tile of bf16 keys (16 KB,
-//    contiguous) arrives by a 1-D bulk TMA copy into one of two staging
-//    buffers while the previous tile is computed. A thread owns one
-//    position: it reads the position's 128-byte bf16 row from the staged tile
-//    (chunk order rotated by position so a quarter-warp hits eight bank
-//    groups), widens it into registers as 32 packed fp32 pairs, reads the
-//    query rows as shared-memory broadcasts, and accumulates the 8 heads in
-//    independent packed fma.rn.f32x2 chains (exact fp32 arithmetic for
-//    integer-grid data); ReLU, head weights and the sum over heads stay in
-//    the thread. Histogram updates are aggregated per warp (one shared atomic
-//    per distinct bin). Each score becomes an order-preserving uint32 key
-//    (written coalesced, one per thread) and feeds a 4096-bin shared
-//    histogram of its top 12 bits, merged into a global per-(unit, row)
-//    histogram when the CTA leaves a unit.
+//  * k_dsa_score: a persistent grid (two to four CTAs per SM) walks the
+//    flattened (unit, tile) space. Each 128-position tile of bf16 keys (16 KB,
+//    contiguous) arrives by a 1-D bulk TMA copy into one of several stages;
+//    each thread rewrites its position's 128-byte row in place into the
+//    128-byte-swizzled K-major operand layout (bank-conflict-free order), and
+//    one thread issues four tcgen05.mma kind::f16 (bf16 x bf16 -> fp32, M = 128
+//    positions, N = 8 heads per query row padded to 16, K = 64) against the
+//    unit's query rows held as operand B. The epilogue reads the thread's TMEM
+//    lane (its position), applies ReLU and the head weights, and turns each
+//    score into an order-preserving uint32 key (written coalesced) that feeds a
+//    4096-bin shared histogram of its top 12 bits (one shared atomic per
+//    distinct bin per warp), merged into a global per-(unit, row) histogram
+//    when the CTA leaves a unit. The next copy into a stage is issued as soon
+//    as the MMA that read it completes.
 //  * k_topk_select: one 8-CTA thread-block cluster per (unit, row). The global
 //    histogram gives the bin b1 of the K-th largest key. One pass over the
 //    cluster's key ranges (cached in shared memory when they fit) counts keys
@@ -45,7 +44,6 @@ namespace cg = cooperative_groups;
 
 namespace {
 
-constexpr int SCORE_THREADS = 128;      // one position per thread
 constexpr int HIST1_BINS = 4096;         // top 12 bits of the ordered key
 constexpr int SEL_CLUSTER = 8;
 constexpr int SEL_THREADS = 512;
@@ -77,51 +75,89 @@ __device__ __forceinline__ uint32_t ordered_key(float s) {
   return (b & 0x80000000u) ? ~b : (b | 0x80000000u);
 }
 
-// positions per tile (one per thread)
-inline int score_tile(int) { return 128; }
+// ---------------------------------------------------------------------------
+// Scores on the tensor cores. For a tile of 128 positions the 8 indexer heads
+// of every query row are one small contraction:
+//     D[p][8r + h] = sum_d keys[p][d] * q[r][h][d]       (M = 128, N = 8R, K = 64)
+// issued as tcgen05.mma kind::f16 with bf16 operands and an fp32 accumulator
+// in tensor memory. With the workloads' integer-grid values every product and
+// partial sum is exactly representable in fp32, so the result equals the
+// CUDA-core fp32 (and the fp64) dot products bit for bit. ReLU, head weights
+// and the sum over heads follow on the CUDA cores, one thread per position.
 
-inline size_t score_smem(int R) {
-  // bf16 staging x2, fp32 query rows, histograms, barriers
-  const int TP = score_tile(R);
-  return (size_t)2 * TP * 128 + (size_t)R * 512 * 4 + (size_t)R * HIST1_BINS * 4 + 64;
+constexpr int SCORE_THREADS = 128;       // one position (TMEM lane) per thread
+constexpr int SCORE_TILE = 128;          // positions per tile = MMA M
+constexpr int SCORE_STAGE = SCORE_TILE * 128;   // 16 KB of bf16 keys
+constexpr int SCORE_MAX_STAGES = 4;
+constexpr int SCORE_TMEM_COLS = 64;      // N <= 64 (R <= 8)
+
+// N of the MMA: 8 heads per query row, padded to a multiple of 16.
+__host__ __device__ inline int score_npad(int R) { return (8 * R + 15) / 16 * 16; }
+
+struct ScoreLayout {
+  int nst;            // key stages (bulk-copy destination, then MMA operand A)
+  size_t b_off;       // query operand B: npad rows x 128 B
+  size_t hist_off;    // R x 4096 bins
+  size_t w_off;       // R x 8 head weights
+  size_t bar_off;     // nst copy barriers + 1 MMA barrier + TMEM address
+  size_t bytes;
+};
+
+__host__ __device__ inline ScoreLayout score_layout(int R, int nst) {
+  ScoreLayout l;
+  l.nst = nst;
+  l.b_off = (size_t)nst * SCORE_STAGE;
+  l.hist_off = l.b_off + dsa_align((size_t)score_npad(R) * 128, 1024);
+  l.w_off = l.hist_off + (size_t)R * HIST1_BINS * 4;
+  l.bar_off = dsa_align(l.w_off + (size_t)R * 8 * 4, 16);
+  l.bytes = l.bar_off + (SCORE_MAX_STAGES + 2) * 8;
+  return l;
 }
 
-// Chunk c of a 128-byte key row is read as chunk (c + s) & 7, s = position & 7,
-// so the eight threads of a quarter-warp touch eight different bank groups;
-// this puts the chunks back in order with static register indices.
-__device__ __forceinline__ void unrotate8(uint4 (&x)[8], int s) {
-  uint4 y[8];
-#pragma unroll
-  for (int c = 0; c < 8; ++c) y[c] = x[c];
-  switch (s) {
-#define DSA_ROT_CASE(S)                                                     \
-    case S:                                                                 \
-      _Pragma("unroll") for (int c = 0; c < 8; ++c) x[(c + S) & 7] = y[c]; \
-      break;
-    DSA_ROT_CASE(0) DSA_ROT_CASE(1) DSA_ROT_CASE(2) DSA_ROT_CASE(3)
-    DSA_ROT_CASE(4) DSA_ROT_CASE(5) DSA_ROT_CASE(6) DSA_ROT_CASE(7)
-#undef DSA_ROT_CASE
-    default: break;
+// The stage count and CTAs per SM for R query rows: the most key bytes in
+// flight per SM, with at least two stages per CTA.
+inline void score_config(int R, int* nst, int* per_sm) {
+  constexpr size_t SM_BYTES = 228 * 1024;
+  int best = -1;
+  for (int s = 2; s <= SCORE_MAX_STAGES; ++s) {
+    // dynamic bytes + alignment slack, static shared memory, the per-CTA reserve
+    const size_t b = score_layout(R, s).bytes + 1024 + 256 + 1024;
+    const int c = (int)std::min<size_t>(4, SM_BYTES / b);
+    if (c >= 1 && c * s > best) {
+      best = c * s;
+      *nst = s;
+      *per_sm = c;
+    }
   }
 }
 
-// Two fp32 values as one 64-bit register pair (no arithmetic: register pairing).
-__device__ __forceinline__ unsigned long long pack_f2(float lo, float hi) {
-  unsigned long long r;
-  asm("mov.b64 %0, {%1, %2};" : "=l"(r) : "f"(lo), "f"(hi));
-  return r;
+// GF(2^3) multiplication by x (modulus x^3 + x + 1): t -> x*t is a bijection,
+// and so is t -> (x + 1)*t.
+__device__ __forceinline__ uint32_t gf8_mulx(uint32_t t) { return ((t << 1) & 7u) ^ ((t & 4u) ? 3u : 0u); }
+
+// Rewrite a staged 128-byte key row (row p of the stage, 1024-aligned base)
+// into the 128-byte-swizzled K-major layout in place: logical 16-byte chunk j
+// goes to slot j ^ (p & 7). Chunk j_c = c ^ mulx(p & 7) is read at step c and
+// its slot j_c ^ (p & 7) = c ^ (x + 1)(p & 7) is written at step c, so the
+// eight rows of a quarter-warp touch eight different 16-byte bank groups on
+// both the reads and the writes.
+__device__ __forceinline__ void swizzle_row_in_place(uint8_t* row, uint32_t p) {
+  const uint32_t s = p & 7u, m = gf8_mulx(s);
+  uint4 v[8];
+#pragma unroll
+  for (int c = 0; c < 8; ++c) v[c] = reinterpret_cast<const uint4*>(row)[(uint32_t)c ^ m];
+#pragma unroll
+  for (int c = 0; c < 8; ++c) reinterpret_cast<uint4*>(row)[((uint32_t)c ^ m) ^ s] = v[c];
 }
 
-// d = a * b + d on two packed fp32 lanes (round to nearest, per lane)
-__device__ __forceinline__ void fma2(unsigned long long& d, unsigned long long a, unsigned long long b) {
-  asm("fma.rn.f32x2 %0, %1, %2, %0;" : "+l"(d) : "l"(a), "l"(b));
+// 8 consecutive fp32 TMEM columns of this thread's lane (no wait).
+__device__ __forceinline__ void tmem_ld8_nowait(uint32_t taddr, uint32_t (&r)[8]) {
+  asm volatile("tcgen05.ld.sync.aligned.32x32b.x8.b32 {%0,%1,%2,%3,%4,%5,%6,%7}, [%8];"
+               : "=r"(r[0]), "=r"(r[1]), "=r"(r[2]), "=r"(r[3]), "=r"(r[4]), "=r"(r[5]), "=r"(r[6]), "=r"(r[7])
+               : "r"(taddr)
+               : "memory");
 }
-
-__device__ __forceinline__ float sum2(unsigned long long v) {
-  float lo, hi;
-  asm("mov.b64 {%0, %1}, %2;" : "=f"(lo), "=f"(hi) : "l"(v));
-  return lo + hi;
-}
+__device__ __forceinline__ void tmem_ld_wait() { asm volatile("tcgen05.wait::ld.sync.aligned;" ::: "memory"); }
 
 struct ScoreArgs {
   const dsa_unit* units;
@@ -133,22 +169,26 @@ struct ScoreArgs {
   int64_t max_len;
   int tpu;              // tiles per unit
   int U;
-  int R, K, TP;
+  int R, K;
+  int nst;
+  uint32_t idesc;
   int32_t* dev_err;
 };
 
-// One lane per history position. The fp32 key tile holds 16 four-float
-// chunks per position; chunk c of position p sits at slot c ^ (p & 7), so the
-// eight lanes of a quarter-warp read eight different bank groups.
-__global__ void __launch_bounds__(SCORE_THREADS, 4) k_dsa_score(ScoreArgs a) {
-  extern __shared__ __align__(128) uint8_t sm[];
-  const int TP = a.TP;
-  const int R = a.R;
-  uint8_t* stg0 = sm;                                                  // [2][TP][128 B]
-  float* sq = reinterpret_cast<float*>(sm + 2 * TP * 128);            // [R][8][64]
-  uint32_t* hs = reinterpret_cast<uint32_t*>(sq + R * 512);            // [R][4096]
-  uint64_t* bar = reinterpret_cast<uint64_t*>(hs + R * HIST1_BINS);    // [2]
-  const int tid = threadIdx.x;
+__global__ void __launch_bounds__(SCORE_THREADS) k_dsa_score(ScoreArgs a) {
+  extern __shared__ __align__(1024) uint8_t sm_raw[];
+  // the swizzled operand layouts need a 1024-byte aligned base
+  uint8_t* sm = sm_raw + ((1024u - (tc::smem_u32(sm_raw) & 1023u)) & 1023u);
+  const int R = a.R, NST = a.nst;
+  const ScoreLayout lay = score_layout(R, NST);
+  const int npad = score_npad(R);
+  uint8_t* sB = sm + lay.b_off;
+  uint32_t* hs = reinterpret_cast<uint32_t*>(sm + lay.hist_off);
+  float* sw = reinterpret_cast<float*>(sm + lay.w_off);
+  uint64_t* full = reinterpret_cast<uint64_t*>(sm + lay.bar_off);     // [NST]
+  uint64_t* mma_bar = full + SCORE_MAX_STAGES;
+  uint32_t* s_tmem = reinterpret_cast<uint32_t*>(mma_bar + 1);
+  const int tid = threadIdx.x, warp = tid >> 5;
 
   // this CTA's tiles: [f0, f1) of the flattened (unit, tile) space
   const long long total = (long long)a.U * a.tpu;
@@ -165,6 +205,16 @@ __global__ void __launch_bounds__(SCORE_THREADS, 4) k_dsa_score(ScoreArgs a) {
   __shared__ int s_len[UCACHE];
   __shared__ const uint16_t* s_keys[UCACHE];
   for (int i = tid; i < R * HIST1_BINS; i += SCORE_THREADS) hs[i] = 0;
+  if (tid == 0) {
+    for (int s = 0; s < NST; ++s) tc::mbar_init(&full[s], 1);
+    tc::mbar_init(mma_bar, 1);
+    tc::fence_mbar_init();
+  }
+  if (warp == 0) tc::tmem_alloc(s_tmem, SCORE_TMEM_COLS);
+  tc::fence_before_sync();
+  __syncthreads();
+  tc::fence_after_sync();
+  const uint32_t tmem = *s_tmem;
   pdl_wait();
   if (tid < UCACHE) {
     const int u = u0 + tid;
@@ -174,19 +224,12 @@ __global__ void __launch_bounds__(SCORE_THREADS, 4) k_dsa_score(ScoreArgs a) {
       const bool ok = unit_aligned(a.units[u]);
       s_len[tid] = (int)L;
       s_keys[tid] = a.units[u].keys;
-      s_ntv[tid] = (L > a.K && ok) ? (int)((L + TP - 1) / TP) : 0;
+      s_ntv[tid] = (L > a.K && ok) ? (int)((L + SCORE_TILE - 1) / SCORE_TILE) : 0;
       if (!ok) dsa_flag(a.dev_err, DSA_DEVERR_BOUNDS);
     }
   }
-  if (tid == 0) {
-    tc::mbar_init(&bar[0], 1);
-    tc::mbar_init(&bar[1], 1);
-    tc::fence_mbar_init();
-  }
   __syncthreads();
 
-  // walk the tile list: index k in [0, ntiles) -> (unit, tile); a tile is
-  // valid when it starts inside a history longer than K
   auto tile_of = [&](int k, int& u, int& t) {
     int tt = t0 + k;
     u = u0;
@@ -209,7 +252,7 @@ __global__ void __launch_bounds__(SCORE_THREADS, 4) k_dsa_score(ScoreArgs a) {
       ntv = s_ntv[i];
     } else {
       const int L = unit_len(u);
-      ntv = (L > a.K && unit_aligned(a.units[u])) ? (L + TP - 1) / TP : 0;
+      ntv = (L > a.K && unit_aligned(a.units[u])) ? (L + SCORE_TILE - 1) / SCORE_TILE : 0;
     }
     return t < ntv;
   };
@@ -224,22 +267,11 @@ __global__ void __launch_bounds__(SCORE_THREADS, 4) k_dsa_score(ScoreArgs a) {
   auto issue = [&](int k, int stage) {
     int u, t;
     tile_of(k, u, t);
-    const int n = min(TP, unit_len(u) - t * TP);
-    tc::mbar_arrive_expect_tx(&bar[stage], (uint32_t)n * 128);
-    tc::bulk_g2s(stg0 + stage * TP * 128, unit_keys(u) + (size_t)t * TP * 64, (uint32_t)n * 128, &bar[stage]);
+    const int n = min(SCORE_TILE, unit_len(u) - t * SCORE_TILE);
+    tc::mbar_arrive_expect_tx(&full[stage], (uint32_t)n * 128);
+    tc::bulk_g2s(sm + stage * SCORE_STAGE, unit_keys(u) + (size_t)t * SCORE_TILE * 64, (uint32_t)n * 128,
+                 &full[stage]);
   };
-
-  int nxt[2];
-  nxt[0] = next_valid(0);
-  nxt[1] = nxt[0] < ntiles ? next_valid(nxt[0] + 1) : ntiles;
-  if (tid == 0) {
-    if (nxt[0] < ntiles) issue(nxt[0], 0);
-    if (nxt[1] < ntiles) issue(nxt[1], 1);
-  }
-  uint32_t parity0 = 0u, parity1 = 0u;
-  int stage = 0;
-  int cur_u = -1;
-
   auto flush_hist = [&](int u) {
     uint32_t* gh = a.hist + (size_t)u * R * HIST1_BINS;
     for (int i = tid; i < R * HIST1_BINS; i += SCORE_THREADS) {
@@ -251,97 +283,114 @@ __global__ void __launch_bounds__(SCORE_THREADS, 4) k_dsa_score(ScoreArgs a) {
     }
   };
 
-  while (true) {
-    const int k = stage == 0 ? nxt[0] : nxt[1];
-    if (k >= ntiles) break;
+  // the valid tiles of this CTA in order; tile j goes to stage j % NST
+  int k_iss = -1;      // last tile issued
+  long long issued = 0;
+  for (int s = 0; s < NST; ++s) {
+    k_iss = next_valid(k_iss + 1);
+    if (k_iss >= ntiles) break;
+    if (tid == 0) issue(k_iss, s);
+    ++issued;
+  }
+  int k = next_valid(0);
+  long long j = 0;     // index of tile k in the valid sequence
+  int stage = 0;
+  int cur_u = -1;
+  bool failed = false;
+  const int p = tid;
+  while (k < ntiles) {
     int u, t;
     tile_of(k, u, t);
-    const int n = min(TP, unit_len(u) - t * TP);
+    const int n = min(SCORE_TILE, unit_len(u) - t * SCORE_TILE);
     if (u != cur_u) {
+      // (the previous tile's MMA is complete: its barrier was waited below)
       if (cur_u >= 0) flush_hist(cur_u);
       cur_u = u;
-      // query rows (fp32) and head weights of this unit
-      for (int i = tid; i < R * 512; i += SCORE_THREADS) sq[i] = bf16f(a.q[(size_t)u * R * 512 + i]);
-      __syncthreads();   // the new query rows are complete before any thread reads them
-    }
-    const uint32_t par = stage == 0 ? parity0 : parity1;
-    const bool ok = tc::mbar_wait(&bar[stage], par);   // bounded
-    const uint8_t* stg = stg0 + stage * TP * 128;
-    // ---- scores: thread = position; its key row comes straight from the
-    //      staged tile and is widened in registers
-    const int p = tid;
-    float score[DSA_MAX_ROWS];
-    if (p < n && ok) {
-      uint4 ch[8];
-      const uint4* row = reinterpret_cast<const uint4*>(stg + p * 128);
-      const int s = p & 7;
-#pragma unroll
-      for (int c = 0; c < 8; ++c) ch[c] = row[(c + s) & 7];
-      unrotate8(ch, s);
-      unsigned long long kr[32];
-#pragma unroll
-      for (int c = 0; c < 8; ++c) {
-        const uint32_t w4[4] = {ch[c].x, ch[c].y, ch[c].z, ch[c].w};
-#pragma unroll
-        for (int e = 0; e < 4; ++e) kr[4 * c + e] = pack_f2(bf16_lo(w4[e]), bf16_hi(w4[e]));
+      // query rows as operand B: row 8r + h holds q[r][h][0..63]; rows past 8R are zero
+      const uint16_t* qu = a.q + (size_t)u * R * 512;
+      for (int i = tid; i < npad * 8; i += SCORE_THREADS) {
+        const int row = i >> 3, c = i & 7;
+        uint4 v = make_uint4(0, 0, 0, 0);
+        if (row < 8 * R) v = *reinterpret_cast<const uint4*>(qu + (size_t)row * 64 + 8 * c);
+        *reinterpret_cast<uint4*>(sB + (row >> 3) * 1024 + (row & 7) * 128 + ((c ^ (row & 7)) << 4)) = v;
       }
-      const float* wr = a.w + (size_t)u * R * 8;
-      for (int r = 0; r < R; ++r) {
-        const ulonglong2* qr = reinterpret_cast<const ulonglong2*>(sq + r * 512);
-        unsigned long long acc[8];
+      for (int i = tid; i < R * 8; i += SCORE_THREADS) sw[i] = a.w[(size_t)u * R * 8 + i];
+    }
+    uint8_t* st = sm + stage * SCORE_STAGE;
+    const bool ok = tc::mbar_wait(&full[stage], (uint32_t)((j / NST) & 1));
+    if (ok && p < n) swizzle_row_in_place(st + p * 128, (uint32_t)p);
+    tc::fence_async_shared();
+    if (__syncthreads_or(!ok)) {
+      failed = true;
+      break;
+    }
+    tc::fence_after_sync();
+    if (tid == 0) {
+      const uint32_t aa = tc::smem_u32(st), bb = tc::smem_u32(sB);
 #pragma unroll
-        for (int h = 0; h < 8; ++h) acc[h] = 0ull;
-#pragma unroll
-        for (int j = 0; j < 16; ++j) {
-#pragma unroll
-          for (int h = 0; h < 8; ++h) {
-            const ulonglong2 qq = qr[h * 16 + j];     // broadcast: every lane, same address
-            fma2(acc[h], qq.x, kr[2 * j]);
-            fma2(acc[h], qq.y, kr[2 * j + 1]);
-          }
-        }
+      for (int kk = 0; kk < 4; ++kk)
+        tc::mma_f16(tmem, tc::sdesc_sw128(aa + kk * 32, 16, 1024), tc::sdesc_sw128(bb + kk * 32, 16, 1024), a.idesc,
+                    kk > 0);
+      tc::mma_commit(mma_bar);
+    }
+    const bool ok2 = tc::mbar_wait(mma_bar, (uint32_t)(j & 1));
+    tc::fence_after_sync();
+    if (__syncthreads_or(!ok2)) {
+      failed = true;
+      ++j;           // this tile's copy was consumed; its MMA may still run
+      break;
+    }
+    // the stage is free again: the next valid tile goes into it
+    {
+      const int kn = k_iss < ntiles ? next_valid(k_iss + 1) : ntiles;
+      if (kn < ntiles) {
+        k_iss = kn;
+        if (tid == 0) issue(kn, stage);
+        ++issued;
+      } else {
+        k_iss = ntiles;
+      }
+    }
+    // ---- epilogue: this thread's position, every query row
+    for (int r = 0; r < R; ++r) {
+      uint32_t d[8];
+      tmem_ld8_nowait(tmem + ((uint32_t)(32 * warp) << 16) + 8 * r, d);
+      tmem_ld_wait();
+      if (p < n) {
         float sc = 0.f;
 #pragma unroll
-        for (int h = 0; h < 8; ++h) sc = fmaf(__ldg(wr + r * 8 + h), fmaxf(sum2(acc[h]), 0.f), sc);
-        if (r < DSA_MAX_ROWS) score[r] = sc;
-      }
-    }
-    if (__syncthreads_or(!ok)) {
-      // A copy did not land in time (this does not happen in normal runs).
-      // Every thread leaves together; the copies in flight get one more
-      // bounded wait so that none lands after the CTA is gone, and the
-      // unit's histogram is not flushed (the call's selection is void).
-      if (tid == 0) {
-        dsa_flag(a.dev_err, DSA_DEVERR_TIMEOUT);
-        tc::mbar_wait(&bar[stage], par);
-        const int o = stage ^ 1;
-        if (nxt[o] < ntiles) tc::mbar_wait(&bar[o], o == 0 ? parity0 : parity1);
-      }
-      __syncthreads();
-      return;
-    }
-    if (stage == 0) parity0 ^= 1u; else parity1 ^= 1u;
-    {
-      const int other = stage == 0 ? nxt[1] : nxt[0];
-      const int kn = other < ntiles ? next_valid(other + 1) : ntiles;
-      if (stage == 0) nxt[0] = kn; else nxt[1] = kn;
-      if (tid == 0 && kn < ntiles) issue(kn, stage);
-    }
-    if (p < n) {
-      const unsigned amask = __activemask();
-      for (int r = 0; r < R; ++r) {
-        const uint32_t key = ordered_key(score[r]);
-        a.okeys[((size_t)u * R + r) * a.stride + (size_t)t * TP + p] = key;
+        for (int h = 0; h < 8; ++h) sc = fmaf(sw[r * 8 + h], fmaxf(__uint_as_float(d[h]), 0.f), sc);
+        const uint32_t key = ordered_key(sc);
+        a.okeys[((size_t)u * R + r) * a.stride + (size_t)t * SCORE_TILE + p] = key;
         const uint32_t bin = key >> 20;
+        const unsigned amask = __activemask();
         const unsigned peers = __match_any_sync(amask, bin);
         if ((int)(threadIdx.x & 31) == __ffs(peers) - 1) atomicAdd(&hs[r * HIST1_BINS + bin], (uint32_t)__popc(peers));
       }
     }
-    __syncthreads();
-    stage ^= 1;
+    tc::fence_before_sync();
+    __syncthreads();   // TMEM read and B used before the next MMA or query load
+    ++j;
+    stage = stage + 1 == NST ? 0 : stage + 1;
+    k = next_valid(k + 1);
   }
+  if (failed) {
+    // A wait gave up (this does not happen in normal runs): the call's
+    // selection is void. Every thread left the loop together; the copies
+    // and the MMA still in flight get one more bounded wait each so that
+    // nothing lands after the CTA is gone.
+    if (tid == 0) {
+      dsa_flag(a.dev_err, DSA_DEVERR_TIMEOUT);
+      tc::mbar_wait(mma_bar, (uint32_t)((j - 1) & 1));
+      for (long long i = j; i < issued; ++i) tc::mbar_wait(&full[i % NST], (uint32_t)((i / NST) & 1));
+    }
+  } else if (cur_u >= 0) {
+    flush_hist(cur_u);
+  }
+  tc::fence_before_sync();
   __syncthreads();
-  if (cur_u >= 0) flush_hist(cur_u);
+  tc::fence_after_sync();
+  if (warp == 0) tc::tmem_dealloc(tmem, SCORE_TMEM_COLS);
 }
 
 // Among `nb` histogram bins (held by threads 0..nb-1, thread t <-> bin
@@ -469,7 +518,6 @@ k_topk_select(const dsa_unit* __restrict__ units, int R, int K, uint32_t* __rest
   const uint32_t b1 = (uint32_t)S->bin;
   int need = K - S->above;
 
-  auto key_at = [&](int64_t p) -> uint32_t { return cached ? kc[p - beg] : kk[p]; };
   // four keys [4q, 4q + 4) of the range, one 16-byte load (shared or global)
   auto key4 = [&](int64_t q) -> uint4 {
     return cached ? *reinterpret_cast<const uint4*>(kc + (4 * q - beg))
@@ -729,10 +777,15 @@ extern "C" int dsa_score_topk(const dsa_unit* units, int32_t U, int32_t R, int32
   if (!ws || ws_bytes < dsa_score_topk_workspace(U, R, max_len)) return DSA_ERR_WS;
   cudaStream_t st = static_cast<cudaStream_t>(stream);
   TopkWs tw = topk_ws(ws, U, R, max_len);
+  if (reinterpret_cast<uintptr_t>(q) & 15u) return DSA_ERR_ARG;   // query rows are read as 16-byte vectors
   int dev = 0;
   const int ok = dsa_device_setup(g_setup, &dev, [](int) {
     size_t mx = 0;
-    for (int r = 1; r <= DSA_MAX_ROWS; ++r) mx = std::max(mx, score_smem(r));
+    for (int r = 1; r <= DSA_MAX_ROWS; ++r) {
+      int nst = 2, per_sm = 1;
+      score_config(r, &nst, &per_sm);
+      mx = std::max(mx, score_layout(r, nst).bytes + 1024);
+    }
     DSA_CUDA_TRY(cudaFuncSetAttribute(k_dsa_score, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)mx));
     DSA_CUDA_TRY(cudaFuncSetAttribute(k_topk_select, cudaFuncAttributeMaxDynamicSharedMemorySize,
                                       (int)select_smem()));
@@ -740,10 +793,11 @@ extern "C" int dsa_score_topk(const dsa_unit* units, int32_t U, int32_t R, int32
   });
   if (ok != DSA_OK) return ok;
   const int num_sms = g_setup.num_sms[dev];
-  const int TP = score_tile(R);
-  const int64_t tpu = (max_len + TP - 1) / TP;
+  const int64_t tpu = (max_len + SCORE_TILE - 1) / SCORE_TILE;
   if (tpu > 0) {
     if (tpu * U > 0x7fffffffLL) return DSA_ERR_ARG;
+    int nst = 2, per_sm = 1;
+    score_config(R, &nst, &per_sm);
     ScoreArgs a;
     a.units = units;
     a.q = q;
@@ -756,11 +810,12 @@ extern "C" int dsa_score_topk(const dsa_unit* units, int32_t U, int32_t R, int32
     a.U = U;
     a.R = R;
     a.K = K;
-    a.TP = TP;
+    a.nst = nst;
+    a.idesc = tc::idesc_bf16_f32(SCORE_TILE, score_npad(R));
     a.dev_err = dev_err;
-    const int per_sm = (int)std::max<size_t>(1, std::min<size_t>(4, 232448 / (score_smem(R) + 1024)));
     const int64_t grid = std::min<int64_t>(tpu * U, (int64_t)per_sm * num_sms);
-    if (launch_pdl(k_dsa_score, dim3((unsigned)grid), dim3(SCORE_THREADS), score_smem(R), st, a) != DSA_OK)
+    if (launch_pdl(k_dsa_score, dim3((unsigned)grid), dim3(SCORE_THREADS), score_layout(R, nst).bytes + 1024, st,
+                   a) != DSA_OK)
       return DSA_ERR_CUDA;
   }
   return launch_pdl(k_topk_select, dim3(SEL_CLUSTER, U * R), dim3(SEL_THREADS), select_smem(), st, units, R,
