@@ -88,18 +88,19 @@ __device__ __forceinline__ uint32_t ordered_key(float s) {
 constexpr int SCORE_THREADS = 128;       // one position (TMEM lane) per thread
 constexpr int SCORE_TILE = 128;          // positions per tile = MMA M
 constexpr int SCORE_STAGE = SCORE_TILE * 128;   // 16 KB of bf16 keys
-constexpr int SCORE_MAX_STAGES = 4;
-constexpr int SCORE_TMEM_COLS = 64;      // N <= 64 (R <= 8)
+constexpr int SCORE_MAX_STAGES = 6;
+constexpr int SCORE_TMEM_COLS = 128;     // two accumulators of N <= 64 columns
 
 // N of the MMA: 8 heads per query row, padded to a multiple of 16.
 __host__ __device__ inline int score_npad(int R) { return (8 * R + 15) / 16 * 16; }
 
 struct ScoreLayout {
-  int nst;            // key stages (bulk-copy destination, then MMA operand A)
-  size_t b_off;       // query operand B: npad rows x 128 B
+  int nst;            // key stages (operand A of one tile each)
+  size_t b_off;       // query operand B, two buffers of npad rows x 128 B
+  size_t b_bytes;
   size_t hist_off;    // R x 4096 bins
-  size_t w_off;       // R x 8 head weights
-  size_t bar_off;     // nst copy barriers + 1 MMA barrier + TMEM address
+  size_t w_off;       // head weights, two buffers of R x 8
+  size_t bar_off;     // nst copy barriers, 2 MMA barriers, TMEM address, fail flag
   size_t bytes;
 };
 
@@ -107,47 +108,36 @@ __host__ __device__ inline ScoreLayout score_layout(int R, int nst) {
   ScoreLayout l;
   l.nst = nst;
   l.b_off = (size_t)nst * SCORE_STAGE;
-  l.hist_off = l.b_off + dsa_align((size_t)score_npad(R) * 128, 1024);
+  l.b_bytes = dsa_align((size_t)score_npad(R) * 128, 1024);
+  l.hist_off = l.b_off + 2 * l.b_bytes;
   l.w_off = l.hist_off + (size_t)R * HIST1_BINS * 4;
-  l.bar_off = dsa_align(l.w_off + (size_t)R * 8 * 4, 16);
-  l.bytes = l.bar_off + (SCORE_MAX_STAGES + 2) * 8;
+  l.bar_off = dsa_align(l.w_off + 2 * (size_t)R * 8 * 4, 16);
+  l.bytes = l.bar_off + (SCORE_MAX_STAGES + 2) * 8 + 16;
   return l;
 }
 
-// The stage count and CTAs per SM for R query rows: the most key bytes in
-// flight per SM, with at least two stages per CTA.
+// The stage count and CTAs per SM for R query rows: as many CTAs per SM as
+// fit (up to four; each CTA's tile loop is a latency chain, so more CTAs hide
+// more of it than more stages per CTA do), then as many stages as still fit.
 inline void score_config(int R, int* nst, int* per_sm) {
   constexpr size_t SM_BYTES = 228 * 1024;
-  int best = -1;
-  for (int s = 2; s <= SCORE_MAX_STAGES; ++s) {
-    // dynamic bytes + alignment slack, static shared memory, the per-CTA reserve
-    const size_t b = score_layout(R, s).bytes + 1024 + 256 + 1024;
-    const int c = (int)std::min<size_t>(4, SM_BYTES / b);
-    if (c >= 1 && c * s > best) {
-      best = c * s;
-      *nst = s;
-      *per_sm = c;
-    }
-  }
+  // dynamic bytes + alignment slack, static shared memory, the per-CTA reserve
+  auto cta_bytes = [R](int s) { return score_layout(R, s).bytes + 1024 + 256 + 1024; };
+  int c = (int)std::max<size_t>(1, std::min<size_t>(4, SM_BYTES / cta_bytes(2)));
+  int s = 2;
+  while (s < SCORE_MAX_STAGES && (size_t)c * cta_bytes(s + 1) <= SM_BYTES) ++s;
+  *nst = s;
+  *per_sm = c;
 }
 
-// GF(2^3) multiplication by x (modulus x^3 + x + 1): t -> x*t is a bijection,
-// and so is t -> (x + 1)*t.
-__device__ __forceinline__ uint32_t gf8_mulx(uint32_t t) { return ((t << 1) & 7u) ^ ((t & 4u) ? 3u : 0u); }
-
-// Rewrite a staged 128-byte key row (row p of the stage, 1024-aligned base)
-// into the 128-byte-swizzled K-major layout in place: logical 16-byte chunk j
-// goes to slot j ^ (p & 7). Chunk j_c = c ^ mulx(p & 7) is read at step c and
-// its slot j_c ^ (p & 7) = c ^ (x + 1)(p & 7) is written at step c, so the
-// eight rows of a quarter-warp touch eight different 16-byte bank groups on
-// both the reads and the writes.
-__device__ __forceinline__ void swizzle_row_in_place(uint8_t* row, uint32_t p) {
-  const uint32_t s = p & 7u, m = gf8_mulx(s);
-  uint4 v[8];
-#pragma unroll
-  for (int c = 0; c < 8; ++c) v[c] = reinterpret_cast<const uint4*>(row)[(uint32_t)c ^ m];
-#pragma unroll
-  for (int c = 0; c < 8; ++c) reinterpret_cast<uint4*>(row)[((uint32_t)c ^ m) ^ s] = v[c];
+// 16-byte asynchronous copy global -> shared (L1 bypassed).
+__device__ __forceinline__ void cp_async16(uint32_t dst_smem, const void* src) {
+  asm volatile("cp.async.cg.shared.global [%0], [%1], 16;" ::"r"(dst_smem), "l"(src) : "memory");
+}
+// Arrive on `bar` once every cp.async this thread issued so far has landed
+// (the barrier counts one arrival per thread, no pending-count increment).
+__device__ __forceinline__ void cp_async_arrive(uint64_t* bar) {
+  asm volatile("cp.async.mbarrier.arrive.noinc.shared::cta.b64 [%0];" ::"r"(tc::smem_u32(bar)) : "memory");
 }
 
 // 8 consecutive fp32 TMEM columns of this thread's lane (no wait).
@@ -175,19 +165,32 @@ struct ScoreArgs {
   int32_t* dev_err;
 };
 
+// Per CTA: a contiguous range of the flattened (unit, tile) space, software
+// pipelined over its valid tiles j = 0, 1, ...:
+//   copies   every thread issues 16-byte cp.async for tile j + NST - 1 straight
+//            into the 128-byte-swizzled K-major layout (row p, chunk c at
+//            p*128 + ((c ^ (p & 7)) << 4)), then arrives on the stage's
+//            barrier; a warp's 32 copies cover 512 contiguous bytes;
+//   MMA      thread 0 waits for tile j's stage, issues its four MMAs into
+//            accumulator j & 1 and commits them to MMA barrier j & 1;
+//   epilogue meanwhile every thread finishes tile j - 1 from the other
+//            accumulator (its stage is then free for the next copy).
+// The query rows sit in operand B buffer (unit change count & 1), so a unit
+// change never overwrites a B that an MMA in flight may read.
 __global__ void __launch_bounds__(SCORE_THREADS) k_dsa_score(ScoreArgs a) {
   extern __shared__ __align__(1024) uint8_t sm_raw[];
   // the swizzled operand layouts need a 1024-byte aligned base
   uint8_t* sm = sm_raw + ((1024u - (tc::smem_u32(sm_raw) & 1023u)) & 1023u);
   const int R = a.R, NST = a.nst;
+  if (NST < 2 || NST > SCORE_MAX_STAGES) return;   // the launch never passes these (barrier slots)
   const ScoreLayout lay = score_layout(R, NST);
   const int npad = score_npad(R);
-  uint8_t* sB = sm + lay.b_off;
   uint32_t* hs = reinterpret_cast<uint32_t*>(sm + lay.hist_off);
-  float* sw = reinterpret_cast<float*>(sm + lay.w_off);
+  float* sw0 = reinterpret_cast<float*>(sm + lay.w_off);              // [2][R * 8]
   uint64_t* full = reinterpret_cast<uint64_t*>(sm + lay.bar_off);     // [NST]
-  uint64_t* mma_bar = full + SCORE_MAX_STAGES;
-  uint32_t* s_tmem = reinterpret_cast<uint32_t*>(mma_bar + 1);
+  uint64_t* mma_bar = full + SCORE_MAX_STAGES;                        // [2]
+  uint32_t* s_tmem = reinterpret_cast<uint32_t*>(mma_bar + 2);
+  int* s_fail = reinterpret_cast<int*>(s_tmem + 1);
   const int tid = threadIdx.x, warp = tid >> 5;
 
   // this CTA's tiles: [f0, f1) of the flattened (unit, tile) space
@@ -206,8 +209,10 @@ __global__ void __launch_bounds__(SCORE_THREADS) k_dsa_score(ScoreArgs a) {
   __shared__ const uint16_t* s_keys[UCACHE];
   for (int i = tid; i < R * HIST1_BINS; i += SCORE_THREADS) hs[i] = 0;
   if (tid == 0) {
-    for (int s = 0; s < NST; ++s) tc::mbar_init(&full[s], 1);
-    tc::mbar_init(mma_bar, 1);
+    for (int s = 0; s < NST; ++s) tc::mbar_init(&full[s], SCORE_THREADS);
+    tc::mbar_init(&mma_bar[0], 1);
+    tc::mbar_init(&mma_bar[1], 1);
+    *s_fail = 0;
     tc::fence_mbar_init();
   }
   if (warp == 0) tc::tmem_alloc(s_tmem, SCORE_TMEM_COLS);
@@ -264,13 +269,20 @@ __global__ void __launch_bounds__(SCORE_THREADS) k_dsa_score(ScoreArgs a) {
     }
     return ntiles;
   };
-  auto issue = [&](int k, int stage) {
+  // every thread: its 8 chunks of tile k into `stage`, then one arrival
+  auto copy_tile = [&](int k, int stage) {
     int u, t;
     tile_of(k, u, t);
     const int n = min(SCORE_TILE, unit_len(u) - t * SCORE_TILE);
-    tc::mbar_arrive_expect_tx(&full[stage], (uint32_t)n * 128);
-    tc::bulk_g2s(sm + stage * SCORE_STAGE, unit_keys(u) + (size_t)t * SCORE_TILE * 64, (uint32_t)n * 128,
-                 &full[stage]);
+    const uint8_t* src = reinterpret_cast<const uint8_t*>(unit_keys(u) + (size_t)t * SCORE_TILE * 64);
+    const uint32_t dst = tc::smem_u32(sm + stage * SCORE_STAGE);
+#pragma unroll
+    for (int i = 0; i < 8; ++i) {
+      const int lin = i * SCORE_THREADS + tid;           // 16-byte chunk of the tile
+      const int row = lin >> 3, c = lin & 7;
+      if (row < n) cp_async16(dst + row * 128 + ((c ^ (row & 7)) << 4), src + (size_t)lin * 16);
+    }
+    cp_async_arrive(&full[stage]);
   };
   auto flush_hist = [&](int u) {
     uint32_t* gh = a.hist + (size_t)u * R * HIST1_BINS;
@@ -283,109 +295,142 @@ __global__ void __launch_bounds__(SCORE_THREADS) k_dsa_score(ScoreArgs a) {
     }
   };
 
-  // the valid tiles of this CTA in order; tile j goes to stage j % NST
-  int k_iss = -1;      // last tile issued
+  // prologue: the first NST valid tiles
+  int k_iss = -1;      // last tile whose copy was issued
   long long issued = 0;
   for (int s = 0; s < NST; ++s) {
-    k_iss = next_valid(k_iss + 1);
-    if (k_iss >= ntiles) break;
-    if (tid == 0) issue(k_iss, s);
+    const int kn = next_valid(k_iss + 1);
+    k_iss = kn;
+    if (kn >= ntiles) break;
+    copy_tile(kn, s);
     ++issued;
   }
-  int k = next_valid(0);
-  long long j = 0;     // index of tile k in the valid sequence
-  int stage = 0;
-  int cur_u = -1;
+
+  int k = next_valid(0);          // tile of this iteration (its MMA)
+  long long j = 0;                // its index in the valid sequence
+  int stage = 0;                  // its stage
+  int bsel = 1, mma_u = -1;       // operand-B buffer of the unit being multiplied
+  // the tile whose epilogue runs in this iteration (the previous one)
+  int pu = -1, pt = 0, pn = 0, pstage = 0, pbsel = 0;
+  int hist_u = -1;                // unit whose counts the shared histogram holds
   bool failed = false;
-  const int p = tid;
-  while (k < ntiles) {
-    int u, t;
-    tile_of(k, u, t);
-    const int n = min(SCORE_TILE, unit_len(u) - t * SCORE_TILE);
-    if (u != cur_u) {
-      // (the previous tile's MMA is complete: its barrier was waited below)
-      if (cur_u >= 0) flush_hist(cur_u);
-      cur_u = u;
-      // query rows as operand B: row 8r + h holds q[r][h][0..63]; rows past 8R are zero
-      const uint16_t* qu = a.q + (size_t)u * R * 512;
-      for (int i = tid; i < npad * 8; i += SCORE_THREADS) {
-        const int row = i >> 3, c = i & 7;
-        uint4 v = make_uint4(0, 0, 0, 0);
-        if (row < 8 * R) v = *reinterpret_cast<const uint4*>(qu + (size_t)row * 64 + 8 * c);
-        *reinterpret_cast<uint4*>(sB + (row >> 3) * 1024 + (row & 7) * 128 + ((c ^ (row & 7)) << 4)) = v;
+  long long last_mma = -1;        // (thread 0) the last tile whose MMAs were issued
+  while (true) {
+    const bool have = k < ntiles;
+    int u = 0, t = 0, n = 0;
+    if (have) {
+      tile_of(k, u, t);
+      n = min(SCORE_TILE, unit_len(u) - t * SCORE_TILE);
+      if (u != mma_u) {
+        // new unit: its query rows into the other B buffer (the MMAs in
+        // flight read this one at most), its head weights likewise
+        mma_u = u;
+        bsel ^= 1;
+        uint8_t* sB = sm + lay.b_off + bsel * lay.b_bytes;
+        const uint16_t* qu = a.q + (size_t)u * R * 512;
+        for (int i = tid; i < npad * 8; i += SCORE_THREADS) {
+          const int row = i >> 3, c = i & 7;
+          uint4 v = make_uint4(0, 0, 0, 0);
+          if (row < 8 * R) v = *reinterpret_cast<const uint4*>(qu + (size_t)row * 64 + 8 * c);
+          *reinterpret_cast<uint4*>(sB + (row >> 3) * 1024 + (row & 7) * 128 + ((c ^ (row & 7)) << 4)) = v;
+        }
+        for (int i = tid; i < R * 8; i += SCORE_THREADS) sw0[bsel * R * 8 + i] = a.w[(size_t)u * R * 8 + i];
+        tc::fence_async_shared();
+        __syncthreads();
       }
-      for (int i = tid; i < R * 8; i += SCORE_THREADS) sw[i] = a.w[(size_t)u * R * 8 + i];
-    }
-    uint8_t* st = sm + stage * SCORE_STAGE;
-    const bool ok = tc::mbar_wait(&full[stage], (uint32_t)((j / NST) & 1));
-    if (ok && p < n) swizzle_row_in_place(st + p * 128, (uint32_t)p);
-    tc::fence_async_shared();
-    if (__syncthreads_or(!ok)) {
-      failed = true;
-      break;
-    }
-    tc::fence_after_sync();
-    if (tid == 0) {
-      const uint32_t aa = tc::smem_u32(st), bb = tc::smem_u32(sB);
+      if (tid == 0) {
+        // tile j's keys have landed: issue its MMAs into accumulator j & 1
+        if (tc::mbar_wait(&full[stage], (uint32_t)((j / NST) & 1))) {
+          last_mma = j;
+          tc::fence_async_shared();
+          tc::fence_after_sync();
+          const uint32_t aa = tc::smem_u32(sm + stage * SCORE_STAGE);
+          const uint32_t bb = tc::smem_u32(sm + lay.b_off + bsel * lay.b_bytes);
+          const uint32_t d = tmem + (uint32_t)(j & 1) * 64;
 #pragma unroll
-      for (int kk = 0; kk < 4; ++kk)
-        tc::mma_f16(tmem, tc::sdesc_sw128(aa + kk * 32, 16, 1024), tc::sdesc_sw128(bb + kk * 32, 16, 1024), a.idesc,
-                    kk > 0);
-      tc::mma_commit(mma_bar);
+          for (int kk = 0; kk < 4; ++kk)
+            tc::mma_f16(d, tc::sdesc_sw128(aa + kk * 32, 16, 1024), tc::sdesc_sw128(bb + kk * 32, 16, 1024),
+                        a.idesc, kk > 0);
+          tc::mma_commit(&mma_bar[j & 1]);
+        } else {
+          atomicOr(s_fail, 1);
+        }
+      }
     }
-    const bool ok2 = tc::mbar_wait(mma_bar, (uint32_t)(j & 1));
-    tc::fence_after_sync();
-    if (__syncthreads_or(!ok2)) {
-      failed = true;
-      ++j;           // this tile's copy was consumed; its MMA may still run
-      break;
-    }
-    // the stage is free again: the next valid tile goes into it
-    {
-      const int kn = k_iss < ntiles ? next_valid(k_iss + 1) : ntiles;
-      if (kn < ntiles) {
+    if (pu >= 0) {
+      // ---- previous tile: its MMAs are done, its stage takes the next copy,
+      //      then its epilogue
+      if (pu != hist_u) {
+        // the shared histogram moves to the new unit (every thread flushes and
+        // clears its own bins; the barrier keeps the epilogue's counts out)
+        if (hist_u >= 0) flush_hist(hist_u);
+        hist_u = pu;
+        __syncthreads();
+      }
+      const long long jp = j - 1;
+      bool ok = tc::mbar_wait(&mma_bar[jp & 1], (uint32_t)((jp >> 1) & 1));
+      ok = __all_sync(0xffffffffu, ok);
+      tc::fence_after_sync();
+      if (ok) {
+        const int kn = k_iss < ntiles ? next_valid(k_iss + 1) : ntiles;
         k_iss = kn;
-        if (tid == 0) issue(kn, stage);
-        ++issued;
-      } else {
-        k_iss = ntiles;
-      }
-    }
-    // ---- epilogue: this thread's position, every query row
-    for (int r = 0; r < R; ++r) {
-      uint32_t d[8];
-      tmem_ld8_nowait(tmem + ((uint32_t)(32 * warp) << 16) + 8 * r, d);
-      tmem_ld_wait();
-      if (p < n) {
-        float sc = 0.f;
+        if (kn < ntiles) {
+          copy_tile(kn, pstage);
+          ++issued;
+        }
+        const float* sw = sw0 + pbsel * R * 8;
+        const int p = tid;
+        for (int r = 0; r < R; ++r) {
+          uint32_t d[8];
+          tmem_ld8_nowait(tmem + ((uint32_t)(32 * warp) << 16) + (uint32_t)(jp & 1) * 64 + 8 * r, d);
+          tmem_ld_wait();
+          if (p < pn) {
+            float sc = 0.f;
 #pragma unroll
-        for (int h = 0; h < 8; ++h) sc = fmaf(sw[r * 8 + h], fmaxf(__uint_as_float(d[h]), 0.f), sc);
-        const uint32_t key = ordered_key(sc);
-        a.okeys[((size_t)u * R + r) * a.stride + (size_t)t * SCORE_TILE + p] = key;
-        const uint32_t bin = key >> 20;
-        const unsigned amask = __activemask();
-        const unsigned peers = __match_any_sync(amask, bin);
-        if ((int)(threadIdx.x & 31) == __ffs(peers) - 1) atomicAdd(&hs[r * HIST1_BINS + bin], (uint32_t)__popc(peers));
+            for (int h = 0; h < 8; ++h) sc = fmaf(sw[r * 8 + h], fmaxf(__uint_as_float(d[h]), 0.f), sc);
+            const uint32_t key = ordered_key(sc);
+            a.okeys[((size_t)pu * R + r) * a.stride + (size_t)pt * SCORE_TILE + p] = key;
+            const uint32_t bin = key >> 20;
+            const unsigned amask = __activemask();
+            const unsigned peers = __match_any_sync(amask, bin);
+            if ((int)(threadIdx.x & 31) == __ffs(peers) - 1)
+              atomicAdd(&hs[r * HIST1_BINS + bin], (uint32_t)__popc(peers));
+          }
+        }
+      } else {
+        atomicOr(s_fail, 1);
       }
     }
     tc::fence_before_sync();
-    __syncthreads();   // TMEM read and B used before the next MMA or query load
+    __syncthreads();   // accumulator (j - 1) & 1 is read before the next MMA writes it
+    if (*s_fail) {
+      failed = true;
+      break;
+    }
+    if (!have) break;
+    pu = u;
+    pt = t;
+    pn = n;
+    pstage = stage;
+    pbsel = bsel;
     ++j;
     stage = stage + 1 == NST ? 0 : stage + 1;
     k = next_valid(k + 1);
   }
   if (failed) {
     // A wait gave up (this does not happen in normal runs): the call's
-    // selection is void. Every thread left the loop together; the copies
-    // and the MMA still in flight get one more bounded wait each so that
-    // nothing lands after the CTA is gone.
+    // selection is void. Every thread left the loop together; the MMAs and
+    // copies that may still be in flight get one more bounded wait each so
+    // that nothing lands after the CTA is gone.
     if (tid == 0) {
       dsa_flag(a.dev_err, DSA_DEVERR_TIMEOUT);
-      tc::mbar_wait(mma_bar, (uint32_t)((j - 1) & 1));
+      for (long long i = last_mma - 1; i <= last_mma; ++i)
+        if (i >= 0) tc::mbar_wait(&mma_bar[i & 1], (uint32_t)((i >> 1) & 1));
       for (long long i = j; i < issued; ++i) tc::mbar_wait(&full[i % NST], (uint32_t)((i / NST) & 1));
     }
-  } else if (cur_u >= 0) {
-    flush_hist(cur_u);
+  } else if (hist_u >= 0) {
+    __syncthreads();
+    flush_hist(hist_u);
   }
   tc::fence_before_sync();
   __syncthreads();
