@@ -3,30 +3,39 @@
 
 One *step* is one decode step of every unit of the workload through the whole
 path: DSA score + Top-K, hot gather, Q8G64 dequant + MLA attention, append with
-batched write-back. The default workload is the 50K single stream (50,023-token
-history, 4 layers, 1 query row, Top-2048, 64 heads, 32,768 hot slots, mirror in
-pinned host memory). The value is layer-steps/s (units x steps / time).
+batched write-back. The headline workload is the capacity batch (16 sessions x
+2 layers, 1,048,576-position histories, Top-2048, 64 heads, 32,768 hot slots
+per unit, mirror in pinned host memory): the largest single-GPU workload. The
+value is layer-steps/s (units x steps / time).
 
-  python bench.py [--gpus N] [--steps K] [--warmup W] [--config C]
-                  [--mirror host|device] [--impl gb300|reference]
+  python bench.py [--gpus N] [--steps K] [--warmup W] [--config C] [--sessions S]
+                  [--mirror host|device] [--impl gb300|reference] [--reps R]
 
-Timing: W >= 3 untimed warm-up steps, then K steps; L2 is flushed (a 512 MiB
-write) before every timed step, outside its CUDA-event bracket; the sum of the
-per-step event times is the timed total. The K timed steps (flushes and event
-records included) are captured once into a CUDA graph and replayed once, so
-host launch cost is off the device timeline; ``--no-graph`` launches directly. Inputs are generated on the device
-before timing. ``e2e`` repeats the K steps from the same initial state through
-the C ABI with host buffers: each step copies its inputs from pinned host
-memory and the attention output back, inside the bracket.
+Timing: every timed repetition starts from the same state (cache initialised,
+then W >= 3 untimed warm-up steps), then K steps run from one CUDA graph; L2
+is flushed (a 512 MiB write) before every timed step, outside its CUDA-event
+bracket, and the sum of the per-step event times is the repetition's total.
+The value is the median over R repetitions. Clocks are sampled through NVML
+every ~2 ms and only samples inside the timed replays are kept. ``e2e`` runs
+the same K steps through the C ABI with host buffers: each step copies its
+inputs from pinned host memory and the attention output back, inside the
+bracket.
 
-``--impl reference`` times the CPU oracle (the only reference there is: the
-pages publish no code) on the host cores, on one unit-step per step.
-Under torchrun (N > 1) every rank runs an independent replica of the workload
-(the path runs on one GPU; there is no collective on the data path).
+Beside the headline the same line carries the 50K single-stream workload
+(``secondary``), and the offload gate (``gate``): the MTP=3 verify workload
+with the mirror in pinned host memory and in HBM, in interleaved repetitions,
+and the gap between them. The CPU baseline (the oracle, float64, one host
+thread, on a bounded sample) runs after all GPU work.
+
+``--impl reference`` times the oracle (the only reference there is: the pages
+publish no code) on the host cores, on one unit-step per step. Under torchrun
+(N > 1) every rank runs an independent replica of the workload (the path runs
+on one GPU; there is no collective on the data path).
 """
 from __future__ import annotations
 
 import argparse
+import ctypes
 import hashlib
 import json
 import os
@@ -42,23 +51,29 @@ if ROOT not in sys.path:
 
 METRIC = "DSA+gather+MLA-attn layer-steps/s; tok/s; achieved GB/s vs HBM/PCIe roofline"
 FALLBACK_PEAKS = {"hbm_gbs": 6800.0, "bf16_tflops": 1900.0, "bf16_tflops_sustained": 1700.0}
+DTYPE = "bf16 indexer operands, fp32 scores / Q8G64 rows / fp16 MMA operands, fp32 accumulate"
 
 
 def parse():
     ap = argparse.ArgumentParser()
     ap.add_argument("--gpus", type=int, default=1)
     ap.add_argument("--steps", type=int, default=None)
-    ap.add_argument("--warmup", type=int, default=8)
-    ap.add_argument("--config", type=int, default=1)
+    ap.add_argument("--warmup", type=int, default=5)
+    ap.add_argument("--config", type=int, default=4)
+    ap.add_argument("--sessions", type=int, default=None,
+                    help="run the workload with fewer sessions (a reduced case for profiling)")
+    ap.add_argument("--reps", type=int, default=5, help="timed repetitions of the K steps (median reported)")
     ap.add_argument("--mirror", choices=["host", "device"], default="host")
     ap.add_argument("--impl", choices=["gb300", "reference"], default="gb300")
     ap.add_argument("--no-e2e", action="store_true")
     ap.add_argument("--no-graph", action="store_true", help="launch steps directly, no CUDA graph")
+    ap.add_argument("--no-secondary", action="store_true", help="skip the 50K single-stream line")
+    ap.add_argument("--no-gate", action="store_true", help="skip the offloaded-vs-resident gate")
     ap.add_argument("--reuse-every", type=int, default=1,
                     help="layer l reuses the selection of layer l - l %% N (1: every layer scores)")
     ap.add_argument("--path", choices=["fused", "split"], default=None,
                     help="fused: hot_gather_attn; split: hot_gather + mla_decode_attn with the append "
-                         "overlapping the attention (default: split, the faster one measured)")
+                         "overlapping the attention (default: split)")
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--cpu-sample-steps", type=int, default=None)
     ap.add_argument("--oracle-child", type=str, default=None, help=argparse.SUPPRESS)
@@ -75,20 +90,38 @@ def load_peaks():
         return dict(FALLBACK_PEAKS), "fallback"
 
 
+def workload(args, cid=None):
+    from synth import workloads as W
+    wl = W.WORKLOADS[args.config if cid is None else cid]
+    if cid is None and args.sessions:
+        wl = wl.with_(sessions=args.sessions)
+    if args.reuse_every > 1:
+        wl = wl.with_(reuse_every=args.reuse_every)
+    return wl
+
+
+def default_steps(wl):
+    return min(wl.steps, 64)
+
+
 # ---------------------------------------------------------------- CPU oracle leg
+
+# The oracle replays unit 0 of the workload: each unit-step is one decode step
+# of one (session, layer) history, exactly as the GPU computes it.
+CPU_UNITS = (0,)
+
 
 def oracle_child(spec: str) -> None:
     """Run in a fresh interpreter: time the oracle on a bounded sample."""
-    os.environ.setdefault("OPENBLAS_NUM_THREADS", "1")
-    os.environ.setdefault("OMP_NUM_THREADS", "1")
-    os.environ.setdefault("MKL_NUM_THREADS", "1")
     import numpy as np
     from oracle.decode import OracleUnit, decode_step
     from synth import workloads as W
     cfg = json.loads(spec)
     wl = W.WORKLOADS[cfg["config"]]
+    if cfg.get("sessions"):
+        wl = wl.with_(sessions=cfg["sessions"])
     nsteps, warm = cfg["steps"], cfg["warmup"]
-    units = list(range(wl.U))
+    units = [u for u in CPU_UNITS if u < wl.U]
     wl2 = wl.with_(steps=max(wl.steps, nsteps + warm + 1))
     ous = {}
     t0 = time.time()
@@ -97,8 +130,6 @@ def oracle_child(spec: str) -> None:
         ous[u] = OracleUnit.create(wl.S, wl2.lmax, wl.L0, keys,
                                    (lambda pos, u=u: W.rows_bytes(wl2, u, pos)), wl.warm)
     setup = time.time() - t0
-    # one unit-step per bench step, units round robin; each unit keeps its own
-    # step counter so every unit replays its own decode sequence
     nxt = {u: 0 for u in units}
 
     def one(i):
@@ -114,12 +145,13 @@ def oracle_child(spec: str) -> None:
     for i in range(nsteps):
         one(warm + i)
     dt = time.perf_counter() - t0
-    print(json.dumps({"seconds": dt, "unit_steps": nsteps, "setup_s": setup, "threads": 1}))
+    print(json.dumps({"seconds": dt, "unit_steps": nsteps, "setup_s": setup, "threads": 1,
+                      "units": units}))
 
 
-def run_oracle(config: int, steps: int, warmup: int) -> dict:
+def run_oracle(config: int, sessions, steps: int, warmup: int) -> dict:
     env = dict(os.environ, OPENBLAS_NUM_THREADS="1", OMP_NUM_THREADS="1", MKL_NUM_THREADS="1")
-    spec = json.dumps({"config": config, "steps": steps, "warmup": warmup})
+    spec = json.dumps({"config": config, "sessions": sessions, "steps": steps, "warmup": warmup})
     r = subprocess.run([sys.executable, os.path.abspath(__file__), "--oracle-child", spec],
                        capture_output=True, text=True, env=env, cwd=ROOT)
     if r.returncode != 0:
@@ -136,15 +168,19 @@ def workload_config(wl, extra=None):
     return d
 
 
+def sample_text(wl, n, r):
+    return (f"{n} unit-steps of unit(s) {r['units']} of the {wl.name} workload (each replaying its own "
+            f"decode steps from the start), float64 oracle, 1 host thread ({r['seconds']:.1f} s; "
+            f"history set-up {r['setup_s']:.1f} s untimed)")
+
+
 def reference_arm(args) -> dict:
-    from synth import workloads as W
-    wl = W.WORKLOADS[args.config]
-    steps = args.steps or wl.steps
+    wl = workload(args)
+    steps = args.steps or default_steps(wl)
     warm = max(3, args.warmup)
-    r = run_oracle(args.config, steps, warm)
+    r = run_oracle(args.config, args.sessions, steps, warm)
     value = r["unit_steps"] / r["seconds"]
-    sample = (f"{steps} unit-steps (units round robin, each replaying its own decode steps from "
-              f"the start) of the {wl.name} workload, float64 oracle, 1 thread")
+    sample = sample_text(wl, steps, r)
     return {
         "impl": "reference", "metric": METRIC, "value": value, "unit": "layer-steps/s",
         "n_gpus": args.gpus, "steps": steps, "warmup": warm,
@@ -162,57 +198,97 @@ def reference_arm(args) -> dict:
 # ---------------------------------------------------------------- clocks
 
 class ClockSampler:
-    QUERY = ("index,clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
-             "clocks_event_reasons.hw_slowdown,clocks_event_reasons.hw_thermal_slowdown,"
-             "clocks_event_reasons.sw_thermal_slowdown,clocks_event_reasons.sw_power_cap")
+    """SM clock, power and clock-event reasons every ~2 ms through NVML (read
+    only), with host timestamps so that samples can be matched to the timed
+    replays; nvidia-smi at 50 ms if NVML cannot be loaded."""
 
-    def __init__(self, index: int):
-        self.index = index
-        self.proc = None
-        self.lines = []
-        self.t = None
+    REASONS = {0x4: "sw_power_cap", 0x8: "hw_slowdown", 0x20: "sw_thermal_slowdown",
+               0x40: "hw_thermal_slowdown", 0x80: "hw_power_brake_slowdown"}
+
+    def __init__(self, torch_index: int):
+        self.samples = []          # (t, sm_mhz, reasons_mask)
+        self.max_mhz = None
+        self.source = None
+        self._stop = threading.Event()
+        self._thread = None
+        self._proc = None
+        self.windows = []
+        try:
+            import torch
+            lib = ctypes.CDLL("libnvidia-ml.so.1")
+            if lib.nvmlInit_v2() != 0:
+                raise RuntimeError("nvmlInit")
+            h = ctypes.c_void_p()
+            uuid = "GPU-" + str(torch.cuda.get_device_properties(torch_index).uuid)
+            if lib.nvmlDeviceGetHandleByUUID(uuid.encode(), ctypes.byref(h)) != 0:
+                if lib.nvmlDeviceGetHandleByIndex_v2(torch_index, ctypes.byref(h)) != 0:
+                    raise RuntimeError("nvml handle")
+            self.lib, self.h = lib, h
+            mx = ctypes.c_uint()
+            if lib.nvmlDeviceGetMaxClockInfo(h, 1, ctypes.byref(mx)) == 0:
+                self.max_mhz = float(mx.value)
+            self._reasons = getattr(lib, "nvmlDeviceGetCurrentClocksEventReasons", None) or \
+                lib.nvmlDeviceGetCurrentClocksThrottleReasons
+            self.source = "nvml"
+        except Exception:
+            self.lib = None
+            self.torch_index = torch_index
+            self.source = "nvidia-smi"
+
+    def _poll_nvml(self):
+        c, r = ctypes.c_uint(), ctypes.c_ulonglong()
+        while not self._stop.is_set():
+            ok = self.lib.nvmlDeviceGetClockInfo(self.h, 1, ctypes.byref(c)) == 0
+            ok = ok and self._reasons(self.h, ctypes.byref(r)) == 0
+            if ok:
+                self.samples.append((time.perf_counter(), float(c.value), int(r.value)))
+            time.sleep(0.002)
+
+    def _poll_smi(self):
+        q = ("clocks.sm,clocks.max.sm,clocks_event_reasons.hw_slowdown,clocks_event_reasons.hw_thermal_slowdown,"
+             "clocks_event_reasons.sw_thermal_slowdown,clocks_event_reasons.sw_power_cap")
+        self._proc = subprocess.Popen(["nvidia-smi", f"--id={self.torch_index}", f"--query-gpu={q}",
+                                       "--format=csv,noheader,nounits", "-lms", "50"],
+                                      stdout=subprocess.PIPE, stderr=subprocess.DEVNULL, text=True)
+        bits = [0x8, 0x40, 0x20, 0x4]
+        for ln in self._proc.stdout:
+            f = [x.strip() for x in ln.split(",")]
+            try:
+                mask = sum(b for b, v in zip(bits, f[2:6]) if v.lower() == "active")
+                self.max_mhz = float(f[1])
+                self.samples.append((time.perf_counter(), float(f[0]), mask))
+            except (ValueError, IndexError):
+                continue
 
     def start(self):
+        target = self._poll_nvml if self.lib is not None else self._poll_smi
+        self._thread = threading.Thread(target=target, daemon=True)
         try:
-            self.proc = subprocess.Popen(
-                ["nvidia-smi", f"--id={self.index}", f"--query-gpu={self.QUERY}",
-                 "--format=csv,noheader,nounits", "-lms", "50"],
-                stdout=subprocess.PIPE, stderr=subprocess.DEVNULL, text=True)
-            self.t = threading.Thread(target=self._read, daemon=True)
-            self.t.start()
-            time.sleep(0.3)
+            self._thread.start()
         except Exception:
-            self.proc = None
+            self._thread = None
+        time.sleep(0.05)
 
-    def _read(self):
-        for ln in self.proc.stdout:
-            self.lines.append(ln.strip())
+    def window(self, t0, t1):
+        self.windows.append((t0, t1))
 
     def stop(self) -> dict:
-        if self.proc is None:
-            return {"sm_mhz": None, "sm_max_mhz": None, "reasons": ["nvidia-smi unavailable"]}
-        time.sleep(0.2)
-        self.proc.terminate()
-        try:
-            self.proc.wait(timeout=5)
-        except Exception:
-            self.proc.kill()
-        sm, mx, reasons = [], None, set()
-        names = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
-        for ln in self.lines:
-            f = [x.strip() for x in ln.split(",")]
-            if len(f) < 9:
-                continue
+        self._stop.set()
+        if self._proc is not None:
+            self._proc.terminate()
             try:
-                sm.append(float(f[1]))
-                mx = float(f[2])
-            except ValueError:
-                continue
-            for n, v in zip(names, f[5:9]):
-                if v.lower() == "active":
-                    reasons.add(n)
-        return {"sm_mhz": statistics.median(sm) if sm else None, "sm_max_mhz": mx,
-                "reasons": sorted(reasons), "samples": len(sm)}
+                self._proc.wait(timeout=5)
+            except Exception:
+                self._proc.kill()
+        if self._thread is not None:
+            self._thread.join(timeout=5)
+        inside = [s for s in self.samples if any(a <= s[0] <= b for a, b in self.windows)]
+        use = inside if inside else self.samples
+        reasons = sorted({n for s in use for b, n in self.REASONS.items() if s[2] & b})
+        return {"sm_mhz": statistics.median(s[1] for s in use) if use else None,
+                "sm_max_mhz": self.max_mhz, "reasons": reasons, "samples": len(use),
+                "samples_in_timed_region": len(inside), "source": self.source,
+                "timed_region_s": round(sum(b - a for a, b in self.windows), 4)}
 
 
 # ---------------------------------------------------------------- GPU arm
@@ -232,63 +308,56 @@ def traffic_for(kernel: str):
         return None
 
 
-def run_gpu(args, rank: int, world: int):
-    import torch
-    from decode_attention_dsa_gb300 import abi
-    from decode_attention_dsa_gb300.step import DecodePath
-    from decode_attention_dsa_gb300.units import UnitSet
-    from synth import gpu as sg
-    from synth import workloads as W
+class WorkloadRun:
+    """One workload on the device: unit set, decode path, inputs for W + K
+    steps (generated on the device), and K-step CUDA graphs."""
 
-    wl = W.WORKLOADS[args.config]
-    if args.reuse_every > 1:
-        wl = wl.with_(reuse_every=args.reuse_every)
-    K = args.steps or wl.steps
-    Wm = max(3, args.warmup)
-    total = Wm + K
-    wlr = wl.with_(steps=total)
-    U, R, A = wl.U, wl.R, wl.A
-    dev = torch.device("cuda")
-    units = UnitSet(U, wl.S, wlr.lmax, mirror=args.mirror)
-    src = [wl.selection_source(u) for u in range(U)] if wl.reuse_every > 1 else None
-    path = DecodePath(units, R, wl.K, wl.H, A, wl.scale(), selection_source=src)
-    sg.history(wlr, units)
-    inp = sg.step_inputs(wlr, 0, total)
-    if path.sources:
-        # only the source units' indexer queries are scored (set up before timing)
-        inp["q_idx"] = inp["q_idx"][:, path.sources].contiguous()
-        inp["w"] = inp["w"][:, path.sources].contiguous()
-    torch.cuda.synchronize()
-    flush = torch.empty(512 << 20, dtype=torch.uint8, device=dev)
-    warm = abi.WARM_LAST_S if wl.warm == "last_s" else abi.WARM_EMPTY
+    def __init__(self, wl, K, Wm, mirror, fused, use_graph):
+        import torch
+        from decode_attention_dsa_gb300 import abi
+        from decode_attention_dsa_gb300.step import DecodePath
+        from decode_attention_dsa_gb300.units import UnitSet
+        from synth import gpu as sg
+        self.torch, self.abi = torch, abi
+        self.wl, self.K, self.Wm, self.fused, self.use_graph = wl, K, Wm, fused, use_graph
+        self.mirror = mirror
+        wlr = wl.with_(steps=Wm + K)
+        U = wl.U
+        self.units = UnitSet(U, wl.S, wlr.lmax, mirror=mirror)
+        src = [wl.selection_source(u) for u in range(U)] if wl.reuse_every > 1 else None
+        self.path = DecodePath(self.units, wl.R, wl.K, wl.H, wl.A, wl.scale(), selection_source=src)
+        sg.history(wlr, self.units)
+        self.inp = sg.step_inputs(wlr, 0, Wm + K)
+        if self.path.sources:
+            # only the source units' indexer queries are scored (set up before timing)
+            self.inp["q_idx"] = self.inp["q_idx"][:, self.path.sources].contiguous()
+            self.inp["w"] = self.inp["w"][:, self.path.sources].contiguous()
+        self.flush = torch.empty(512 << 20, dtype=torch.uint8, device="cuda")
+        self.side = torch.cuda.Stream()
+        self.warm = abi.WARM_LAST_S if wl.warm == "last_s" else abi.WARM_EMPTY
+        self.ctr = torch.zeros((U, 4), dtype=torch.int64, device="cuda")
+        torch.cuda.synchronize()
 
-    def step_args(s):
-        return (inp["q_idx"][s], inp["w"][s], inp["q_lat"][s], inp["q_rope"][s],
-                inp["new_rows"][s], inp["new_keys"][s])
+    def step_args(self, s):
+        i = self.inp
+        return (i["q_idx"][s], i["w"][s], i["q_lat"][s], i["q_rope"][s], i["new_rows"][s], i["new_keys"][s])
 
-    # ---- device-resident run
-    units.init([wl.L0] * U, warm)
-    for s in range(Wm):
-        path.step(abi.ROUND_AUTO, *step_args(s))
-    torch.cuda.synchronize()
-    use_graph = not args.no_graph
-    rnd = abi.ROUND_AUTO
+    def reset(self):
+        """Initialise the cache, run the W warm-up steps, wait."""
+        self.units.init([self.wl.L0] * self.wl.U, self.warm)
+        for s in range(self.Wm):
+            self.path.step(self.abi.ROUND_AUTO, *self.step_args(s))
+        self.ctr.zero_()
+        self.torch.cuda.synchronize()
 
-    side = torch.cuda.Stream()
-    fused = args.path == "fused"
-
-    def record_steps(nsteps, per_call, ctr_acc=None):
-        """Enqueue nsteps timed steps; returns the events. per_call adds
-        events between the four calls and runs them one after another (a
-        separate breakdown run); otherwise the append runs on a side stream
-        concurrently with the attention, as the API allows."""
+    def _record(self, per_call):
+        torch, path, rnd = self.torch, self.path, self.abi.ROUND_AUTO
         nev = 5 if per_call else 2
-        ev = [[torch.cuda.Event(enable_timing=True, external=use_graph) for _ in range(nev)]
-              for _ in range(nsteps)]
-        for i in range(nsteps):
-            s = Wm + i
-            qi, w, ql, qr, nr, nk = step_args(s)
-            flush.fill_(i & 0xFF)
+        ev = [[torch.cuda.Event(enable_timing=True, external=self.use_graph) for _ in range(nev)]
+              for _ in range(self.K)]
+        for i in range(self.K):
+            qi, w, ql, qr, nr, nk = self.step_args(self.Wm + i)
+            self.flush.fill_(i & 0xFF)
             e = ev[i]
             e[0].record()
             if per_call:
@@ -299,124 +368,104 @@ def run_gpu(args, rank: int, world: int):
                 path.attend(ql, qr)
                 e[3].record()
                 path.append(nr, nk)
-            elif fused:
+            elif self.fused:
                 path.step(rnd, qi, w, ql, qr, nr, nk, fused=True)
             else:
-                path.step(rnd, qi, w, ql, qr, nr, nk, side=side)
+                path.step(rnd, qi, w, ql, qr, nr, nk, side=self.side)
             e[-1].record()
-            if ctr_acc is not None:
-                ctr_acc.add_(path.counters)
+            if not per_call:
+                self.ctr.add_(path.counters)
         return ev
 
-    def run_steps(nsteps, per_call, ctr_acc=None):
-        if use_graph:
+    def capture(self, per_call=False):
+        """A K-step graph (or, without graphs, a function that launches the steps)."""
+        torch = self.torch
+        if not self.use_graph:
+            return None, None
+        graph = torch.cuda.CUDAGraph()
+        cap = torch.cuda.Stream()
+        cap.wait_stream(torch.cuda.current_stream())
+        with torch.cuda.graph(graph, stream=cap):
+            ev = self._record(per_call)
+        torch.cuda.synchronize()
+        return graph, ev
+
+    def timed(self, graph, ev, per_call=False, clocks=None):
+        """Reset, replay the K steps once; returns per-step event lists."""
+        torch = self.torch
+        self.reset()
+        t0 = time.perf_counter()
+        if graph is not None:
+            graph.replay()
+        else:
+            ev = self._record(per_call)
+        torch.cuda.synchronize()
+        t1 = time.perf_counter()
+        if clocks is not None:
+            clocks.window(t0, t1)
+        err = self.units.check()
+        if err:
+            raise RuntimeError(f"device error word {err:#x}")
+        return ev
+
+    def e2e(self, reps):
+        """The K steps through the C ABI with pinned host buffers: per step the
+        inputs are copied in and the attention output copied out inside the
+        bracket. Returns (ms per K steps per rep, h2d bytes/step, d2h bytes/step)."""
+        torch = self.torch
+        names = ["q_idx", "w", "q_lat", "q_rope", "new_rows", "new_keys"]
+        K, Wm, path = self.K, self.Wm, self.path
+        host = {n: torch.empty_like(self.inp[n][Wm:], device="cpu").pin_memory() for n in names}
+        for n in names:
+            host[n].copy_(self.inp[n][Wm:])
+        dev_in = {n: torch.empty_like(self.inp[n][0]) for n in names}
+        out_host = torch.empty((K,) + tuple(path.out.shape), dtype=torch.float32).pin_memory()
+        h2d = sum(host[n][0].numel() * host[n][0].element_size() for n in names)
+        d2h = path.out.numel() * 4
+        ee = [(torch.cuda.Event(enable_timing=True, external=self.use_graph),
+               torch.cuda.Event(enable_timing=True, external=self.use_graph)) for _ in range(K)]
+
+        def steps():
+            for i in range(K):
+                self.flush.fill_(i & 0xFF)
+                ee[i][0].record()
+                for n in names:
+                    dev_in[n].copy_(host[n][i], non_blocking=True)
+                path.step(self.abi.ROUND_AUTO, dev_in["q_idx"], dev_in["w"], dev_in["q_lat"], dev_in["q_rope"],
+                          dev_in["new_rows"], dev_in["new_keys"], side=self.side, fused=self.fused)
+                out_host[i].copy_(path.out, non_blocking=True)
+                ee[i][1].record()
+        graph = None
+        if self.use_graph:
             graph = torch.cuda.CUDAGraph()
             cap = torch.cuda.Stream()
             cap.wait_stream(torch.cuda.current_stream())
             with torch.cuda.graph(graph, stream=cap):
-                ev = record_steps(nsteps, per_call, ctr_acc)
+                steps()
             torch.cuda.synchronize()
-            return ev, graph
-        return None, None
-
-    def warm_start():
-        units.init([wl.L0] * U, warm)
-        for s in range(Wm):
-            path.step(rnd, *step_args(s))
-        torch.cuda.synchronize()
-
-    # ---- headline run: events only at step boundaries
-    ctr_acc = torch.zeros((U, 4), dtype=torch.int64, device=dev)
-    ev, graph = run_steps(K, False, ctr_acc)
-    if world > 1:
-        torch.distributed.barrier()
-    torch.cuda.synchronize()
-    clocks = ClockSampler(torch.cuda.current_device())
-    clocks.start()
-    wall0 = time.perf_counter()
-    if graph is not None:
-        graph.replay()
-    else:
-        ev = record_steps(K, False, ctr_acc)
-    torch.cuda.synchronize()
-    wall = time.perf_counter() - wall0
-    clk = clocks.stop()
-    err = units.check()
-    if err:
-        raise RuntimeError(f"device error word {err:#x}")
-    step_ms = [e[0].elapsed_time(e[-1]) for e in ev]
-    total_ms = sum(step_ms)
-    if world > 1:
-        t = torch.tensor([total_ms], dtype=torch.float64, device=dev)
-        torch.distributed.all_reduce(t, op=torch.distributed.ReduceOp.MAX)
-        total_ms = float(t.item())
-    del graph
-
-    # ---- breakdown run (same start state): events around each call
-    KB = min(K, 256)
-    warm_start()
-    evb, gb = run_steps(KB, True)
-    if gb is not None:
-        gb.replay()
-    else:
-        evb = record_steps(KB, True)
-    torch.cuda.synchronize()
-    call_ms = [statistics.mean(e[j].elapsed_time(e[j + 1]) for e in evb) for j in range(4)]
-    breakdown_step_ms = statistics.mean(e[0].elapsed_time(e[4]) for e in evb)
-    del gb
-    ctr = ctr_acc.cpu().numpy().sum(axis=0)    # HOT, RING, RAM entries, fills over K steps
-
-    # ---- end to end through the C ABI with host buffers (same K steps, same start state)
-    e2e = None
-    if not args.no_e2e:
-        names = ["q_idx", "w", "q_lat", "q_rope", "new_rows", "new_keys"]
-        host = {n: torch.empty_like(inp[n][Wm:], device="cpu").pin_memory() for n in names}
-        for n in names:
-            host[n].copy_(inp[n][Wm:])
-        dev_in = {n: torch.empty_like(inp[n][0]) for n in names}
-        out_host = torch.empty((K,) + tuple(path.out.shape), dtype=torch.float32).pin_memory()
-        h2d = sum(host[n][0].numel() * host[n][0].element_size() for n in names)
-        d2h = path.out.numel() * 4
-        units.init([wl.L0] * U, warm)
-        for s in range(Wm):
-            path.step(abi.ROUND_AUTO, *step_args(s))
-        torch.cuda.synchronize()
-        ee = [(torch.cuda.Event(enable_timing=True, external=use_graph),
-               torch.cuda.Event(enable_timing=True, external=use_graph)) for _ in range(K)]
-
-        def e2e_steps():
-            for i in range(K):
-                flush.fill_(i & 0xFF)
-                ee[i][0].record()
-                for n in names:
-                    dev_in[n].copy_(host[n][i], non_blocking=True)
-                path.step(abi.ROUND_AUTO, dev_in["q_idx"], dev_in["w"], dev_in["q_lat"],
-                          dev_in["q_rope"], dev_in["new_rows"], dev_in["new_keys"], side=side, fused=fused)
-                out_host[i].copy_(path.out, non_blocking=True)
-                ee[i][1].record()
-        if use_graph:
-            g2 = torch.cuda.CUDAGraph()
-            cap = torch.cuda.Stream()
-            cap.wait_stream(torch.cuda.current_stream())
-            with torch.cuda.graph(g2, stream=cap):
-                e2e_steps()
+        res = []
+        for _ in range(reps):
+            self.reset()
+            if graph is not None:
+                graph.replay()
+            else:
+                steps()
             torch.cuda.synchronize()
-            g2.replay()
-        else:
-            e2e_steps()
-        torch.cuda.synchronize()
-        e2e_ms = sum(a.elapsed_time(b) for a, b in ee)
-        if world > 1:
-            t = torch.tensor([e2e_ms], dtype=torch.float64, device=dev)
-            torch.distributed.all_reduce(t, op=torch.distributed.ReduceOp.MAX)
-            e2e_ms = float(t.item())
-        e2e = {"value": world * U * K / (e2e_ms / 1e3), "unit": "layer-steps/s",
-               "h2d_bytes_per_step": int(h2d), "d2h_bytes_per_step": int(d2h),
-               "ms_per_step": e2e_ms / K}
+            res.append(sum(a.elapsed_time(b) for a, b in ee))
+        del graph
+        return res, h2d, d2h
 
-    # ---- host-link copy bandwidth (DMA, pinned -> device), for the roofline's host term
+    def close(self):
+        self.units.close()
+        del self.inp, self.flush
+        self.torch.cuda.synchronize()
+        self.torch.cuda.empty_cache()
+
+
+def host_link_gbs(torch):
+    """Pinned host -> device copy bandwidth (DMA), the host link's rate."""
     hb = torch.empty(256 << 20, dtype=torch.uint8).pin_memory()
-    db = torch.empty(256 << 20, dtype=torch.uint8, device=dev)
+    db = torch.empty(256 << 20, dtype=torch.uint8, device="cuda")
     for _ in range(2):
         db.copy_(hb, non_blocking=True)
     torch.cuda.synchronize()
@@ -426,73 +475,181 @@ def run_gpu(args, rank: int, world: int):
         db.copy_(hb, non_blocking=True)
     b.record()
     torch.cuda.synchronize()
-    host_gbs = 4 * hb.numel() / (a.elapsed_time(b) * 1e6)
+    gbs = 4 * hb.numel() / (a.elapsed_time(b) * 1e6)
     del hb, db
+    return gbs
 
+
+def measure(args, wl, K, Wm, mirror, reps, world, clocks=None, e2e=False, breakdown=True):
+    """Time one workload: median of `reps` K-step replays, the per-call
+    breakdown, the cache counters and (optionally) e2e. Returns a dict."""
+    import torch
+    use_graph = not args.no_graph
+    fused = args.path == "fused"
+    run = WorkloadRun(wl, K, Wm, mirror, fused, use_graph)
+    path, U = run.path, wl.U
+    graph, ev = run.capture(per_call=False)
+    totals = []
+    ctr = None
+    for r in range(reps):
+        ev = run.timed(graph, ev, clocks=clocks)
+        totals.append(sum(e[0].elapsed_time(e[-1]) for e in ev))
+        if ctr is None:
+            ctr = run.ctr.cpu().numpy().sum(axis=0)      # HOT, RING, RAM entries, fills over K steps
+    del graph
+    total_ms = statistics.median(totals)
+    if world > 1:
+        t = torch.tensor([total_ms], dtype=torch.float64, device="cuda")
+        torch.distributed.all_reduce(t, op=torch.distributed.ReduceOp.MAX)
+        total_ms = float(t.item())
+    res = {"run": run, "totals_ms": totals, "total_ms": total_ms, "ctr": ctr,
+           "launches_per_step": path.launches_per_step()}
+    if breakdown:
+        gb, evb = run.capture(per_call=True)
+        evb = run.timed(gb, evb, per_call=True)
+        res["call_ms"] = [statistics.mean(e[j].elapsed_time(e[j + 1]) for e in evb) for j in range(4)]
+        res["breakdown_step_ms"] = statistics.mean(e[0].elapsed_time(e[4]) for e in evb)
+        del gb
+    if e2e:
+        ms, h2d, d2h = run.e2e(max(1, min(3, reps)))
+        e2e_ms = statistics.median(ms)
+        if world > 1:
+            t = torch.tensor([e2e_ms], dtype=torch.float64, device="cuda")
+            torch.distributed.all_reduce(t, op=torch.distributed.ReduceOp.MAX)
+            e2e_ms = float(t.item())
+        res["e2e"] = {"value": world * U * K / (e2e_ms / 1e3), "unit": "layer-steps/s",
+                      "h2d_bytes_per_step": int(h2d), "d2h_bytes_per_step": int(d2h), "ms_per_step": e2e_ms / K}
+    return res
+
+
+def roofline(wl, res, K, Wm, host_gbs, path):
+    """Per-call achieved rates, the dominant call's roofline fraction and the
+    step roofline (the slower of HBM bytes, host-link bytes and attention
+    FLOPs at their peaks)."""
     peaks, peak_kind = load_peaks()
     hbm_peak = float(peaks.get("hbm_gbs", FALLBACK_PEAKS["hbm_gbs"]))
     tc_peak = float(peaks.get("bf16_tflops", FALLBACK_PEAKS["bf16_tflops"]))
+    U, R, A = wl.U, wl.R, wl.A
+    ctr = res["ctr"]
     mean_L = wl.L0 + (Wm + (K - 1) / 2.0) * A
-    key_bytes = (path.Us if path.sources else U) * mean_L * 128.0   # per score_topk launch
-    ent = ctr[:3].sum() / K
-    ram_b = ctr[2] / K * 656.0                              # host-link bytes per step
+    key_bytes = (path.Us if path.sources else U) * mean_L * 128.0   # per score_topk call
+    ram_b = ctr[2] / K * 656.0                                      # host-link bytes per step
     hbm_rows_b = (ctr[0] + ctr[1]) / K * 656.0 + ctr[3] / K * 656.0
     attn_flops = U * R * wl.H * wl.K * (576 + 512) * 2.0
-    calls = [
-        ("dsa_score_topk", "hbm", key_bytes, call_ms[0]),
-        ("hot_gather", "hbm", hbm_rows_b + ram_b, call_ms[1]),
-        ("mla_decode_attn", "tensor", attn_flops, call_ms[2]),
-        ("kv_append_writeback", "hbm", U * A * (656 + 128.0), call_ms[3]),
-    ]
-    dom = max(calls, key=lambda c: c[3])
-    name, bound, work, ms = dom
-    if bound == "hbm":
-        achieved, peak, unit = work / (ms * 1e6), hbm_peak, "GB/s"
-    else:
-        achieved, peak, unit = work / (ms * 1e9), tc_peak, "TFLOP/s"
-    per_call = {}
-    for n, bd, wk, m in calls:
-        if bd == "hbm":
-            per_call[n] = {"ms": m, "GB/s": wk / (m * 1e6)}
+    out = {}
+    if "call_ms" in res:
+        cm = res["call_ms"]
+        calls = [
+            ("dsa_score_topk", "hbm", key_bytes, cm[0]),
+            ("hot_gather", "hbm", hbm_rows_b + ram_b, cm[1]),
+            ("mla_decode_attn", "tensor", attn_flops, cm[2]),
+            ("kv_append_writeback", "hbm", U * A * (656 + 128.0), cm[3]),
+        ]
+        name, bound, work, ms = max(calls, key=lambda c: c[3])
+        if bound == "hbm":
+            achieved, peak, unit = work / (ms * 1e6), hbm_peak, "GB/s"
         else:
-            per_call[n] = {"ms": m, "TFLOP/s": wk / (m * 1e9)}
-    ms_step = total_ms / K
+            achieved, peak, unit = work / (ms * 1e9), tc_peak, "TFLOP/s"
+        out["roofline"] = {"kernel": name, "bound": bound, "achieved": achieved, "peak": peak, "unit": unit,
+                           "frac": achieved / peak, "peak_source": peak_kind, "traffic": traffic_for(name),
+                           "work_per_launch": work,
+                           "note": "achieved = algorithmic bytes (or FLOPs) per call / mean call time "
+                                   "(CUDA events around the call, serial replay)"}
+        out["per_call"] = {n: ({"ms": m, "GB/s": wk / (m * 1e6)} if bd == "hbm" else
+                               {"ms": m, "TFLOP/s": wk / (m * 1e9)}) for n, bd, wk, m in calls}
+    ms_step = res["total_ms"] / K
     hbm_step_b = key_bytes + hbm_rows_b
-    t_roof_ms = max(hbm_step_b / (hbm_peak * 1e6), ram_b / (host_gbs * 1e6),
-                    attn_flops / (tc_peak * 1e9))
-    value = world * U * K / (total_ms / 1e3)
+    t_roof = max(hbm_step_b / (hbm_peak * 1e6), ram_b / (host_gbs * 1e6), attn_flops / (tc_peak * 1e9))
+    out["step_roofline"] = {"t_roof_ms": t_roof, "frac": t_roof / ms_step, "hbm_bytes": hbm_step_b,
+                            "host_bytes": ram_b, "attn_flops": attn_flops, "host_link_gbs": host_gbs,
+                            "host_link_kind": "DMA pinned->device copy", "peak_source": peak_kind}
+    out["cache"] = {"hot": int(ctr[0]), "ring": int(ctr[1]), "ram": int(ctr[2]), "fills": int(ctr[3]),
+                    "miss_frac": float(ctr[2] / max(1, ctr[:3].sum()))}
+    return out
+
+
+def run_gpu(args, rank: int, world: int):
+    import torch
+    wl = workload(args)
+    K = args.steps or default_steps(wl)
+    Wm = max(3, args.warmup)
+    reps = max(1, args.reps)
+    host_gbs = host_link_gbs(torch)
+    clocks = ClockSampler(torch.cuda.current_device())
+    if world > 1:
+        torch.distributed.barrier()
+    clocks.start()
+    res = measure(args, wl, K, Wm, args.mirror, reps, world, clocks=clocks, e2e=not args.no_e2e)
+    clk = clocks.stop()
+    run = res.pop("run")
+    value = world * wl.U * K / (res["total_ms"] / 1e3)
     line = {
         "metric": METRIC, "value": value, "unit": "layer-steps/s", "n_gpus": world, "steps": K,
-        "warmup": Wm, "ms_per_step": ms_step, "higher_is_better": True, "scaling": "weak",
-        "vs_baseline": None, "dtype": "fp32 score / u8 rows / fp32 attention",
+        "warmup": Wm, "ms_per_step": res["total_ms"] / K, "higher_is_better": True, "scaling": "weak",
+        "vs_baseline": None, "dtype": DTYPE,
         "data": "synthetic (seeded counter-based generator, generated on the device)",
-        "config": workload_config(wl, {"mirror": args.mirror, "l2": "flushed before every timed step",
-                                       "selection_reuse_every": wl.reuse_every,
-                                       "path": "hot_gather_attn (fused)" if fused else
-                                               "hot_gather + mla_decode_attn, append concurrent",
-                                       "parallelism": "replicas" if world > 1 else "single GPU"}),
-        "tok_per_s": value * A / wl.layers,
-        "roofline": {"kernel": name, "bound": bound, "achieved": achieved, "peak": peak,
-                     "unit": unit, "frac": achieved / peak, "peak_source": peak_kind,
-                     "traffic": traffic_for(name)},
-        "step_roofline": {"t_roof_ms": t_roof_ms, "frac": t_roof_ms / ms_step,
-                          "hbm_bytes": hbm_step_b, "host_bytes": ram_b, "attn_flops": attn_flops,
-                          "host_link_gbs": host_gbs, "host_link_kind": "DMA pinned->device copy",
-                          "peak_source": peak_kind},
-        "per_call": per_call,
-        "per_call_note": (f"mean over a separate replay of {KB} steps from the same start with "
-                          f"events around each call ({breakdown_step_ms:.4f} ms/step there)"),
-        "cache": {"hot": int(ctr[0]), "ring": int(ctr[1]), "ram": int(ctr[2]), "fills": int(ctr[3]),
-                  "miss_frac": float(ctr[2] / max(1, ctr[:3].sum()))},
-        "clocks": clk,
-        "gpu_launches": path.launches_per_step() * K,
-        "cuda_graph": use_graph,
-        "wall_s": wall,
+        "config": workload_config(wl, {
+            "mirror": args.mirror, "l2": "flushed before every timed step (512 MiB write outside the bracket)",
+            "selection_reuse_every": wl.reuse_every,
+            "path": "hot_gather_attn (fused)" if args.path == "fused" else
+                    "hot_gather + mla_decode_attn, append concurrent",
+            "timing": f"median of {reps} replays of one {K}-step CUDA graph, each from the same state",
+            "parallelism": "replicas" if world > 1 else "single GPU"}),
+        "tok_per_s": value * wl.A / wl.layers,
+        "reps_ms_per_step": [t / K for t in res["totals_ms"]],
     }
-    if e2e:
-        line["e2e"] = e2e
-    units.close()
+    line.update(roofline(wl, res, K, Wm, host_gbs, run.path))
+    line["per_call_note"] = (f"mean over a separate replay of {K} steps from the same start with events around "
+                             f"each call, calls serial ({res['breakdown_step_ms']:.4f} ms/step there)")
+    line["clocks"] = clk
+    line["gpu_launches"] = res["launches_per_step"] * K
+    line["cuda_graph"] = not args.no_graph
+    if "e2e" in res:
+        line["e2e"] = res["e2e"]
+    run.close()
+    del run
+
+    if rank == 0 and world == 1 and not args.no_secondary and args.config != 1:
+        wl1 = workload(args, 1)
+        r1 = measure(args, wl1, K, Wm, "host", reps, 1)
+        run1 = r1.pop("run")
+        v1 = wl1.U * K / (r1["total_ms"] / 1e3)
+        sec = {"workload": wl1.name, "value": v1, "unit": "layer-steps/s", "ms_per_step": r1["total_ms"] / K,
+               "tok_per_s": v1 * wl1.A / wl1.layers, "steps": K}
+        rf = roofline(wl1, r1, K, Wm, host_gbs, run1.path)
+        sec.update({k: rf[k] for k in ("step_roofline", "per_call", "cache")})
+        line["secondary"] = sec
+        run1.close()
+        del run1
+    if rank == 0 and world == 1 and not args.no_gate:
+        line["gate"] = offload_gate(args, K, Wm)
     return line
+
+
+def offload_gate(args, K, Wm):
+    """The MTP=3 verify workload with the mirror in pinned host memory
+    (offloaded) and in HBM (resident), same kernels, interleaved repetitions;
+    the gap is (offloaded - resident) / resident in step time (best of each)."""
+    import torch
+    wl2 = workload(args, 2)
+    use_graph = not args.no_graph
+    runs = {m: WorkloadRun(wl2, K, Wm, m, args.path == "fused", use_graph) for m in ("host", "device")}
+    graphs = {m: r.capture(per_call=False) for m, r in runs.items()}
+    ms = {"host": [], "device": []}
+    for _ in range(max(3, min(5, args.reps))):
+        for m in ("host", "device"):
+            g, ev = graphs[m]
+            ev = runs[m].timed(g, ev)
+            ms[m].append(sum(e[0].elapsed_time(e[-1]) for e in ev) / K)
+    for m in runs:
+        runs[m].close()
+    del graphs, runs
+    torch.cuda.empty_cache()
+    best = {m: min(v) for m, v in ms.items()}
+    gap = (best["host"] - best["device"]) / best["device"] * 100.0
+    return {"workload": wl2.name, "steps": K, "offloaded_ms_per_step": best["host"],
+            "resident_ms_per_step": best["device"], "gap_pct": gap, "within_5pct": gap <= 5.0,
+            "reps_ms_per_step": ms, "note": "best of interleaved repetitions (host, device, host, ...)"}
 
 
 def main():
@@ -508,37 +665,23 @@ def main():
             return 0
         print(json.dumps(reference_arm(args)), flush=True)
         return 0
-    cpu = None
-    if rank == 0 and world == 1 and not args.no_cpu_baseline:
-        # the CPU leg runs in a child process started before any CUDA work
-        from synth import workloads as W
-        wl = W.WORKLOADS[args.config]
-        n = args.cpu_sample_steps or min(64, wl.steps) * 1
-        cpu_res = {}
-
-        def go():
-            try:
-                cpu_res.update(run_oracle(args.config, n, 2))
-            except Exception as e:  # reported, not fatal
-                cpu_res["error"] = str(e)[-300:]
-        th = threading.Thread(target=go)
-        th.start()
     import torch
     torch.cuda.set_device(local)
     if world > 1:
         torch.distributed.init_process_group("nccl")
     line = run_gpu(args, rank, world)
     if rank == 0 and world == 1 and not args.no_cpu_baseline:
-        th.join()
-        if "seconds" in cpu_res:
-            v = cpu_res["unit_steps"] / cpu_res["seconds"]
-            cpu = {"value": v, "unit": "layer-steps/s", "cores": cpu_res["threads"], "kind": "oracle",
-                   "sample": f"{cpu_res['unit_steps']} unit-steps of the same workload, units round "
-                             f"robin, float64 oracle, 1 thread ({cpu_res['seconds']:.1f} s)"}
-        else:
-            cpu = {"value": None, "unit": "layer-steps/s", "cores": 1, "kind": "oracle",
-                   "sample": "failed: " + cpu_res.get("error", "?")}
-        line["cpu_baseline"] = cpu
+        # after all GPU work: the oracle on a bounded sample of the same workload
+        wl = workload(args)
+        n = args.cpu_sample_steps or 12
+        try:
+            r = run_oracle(args.config, args.sessions, n, 1)
+            v = r["unit_steps"] / r["seconds"]
+            line["cpu_baseline"] = {"value": v, "unit": "layer-steps/s", "cores": r["threads"], "kind": "oracle",
+                                    "sample": sample_text(wl, n, r)}
+        except Exception as e:  # reported, not fatal
+            line["cpu_baseline"] = {"value": None, "unit": "layer-steps/s", "cores": 1, "kind": "oracle",
+                                    "sample": "failed: " + str(e)[-300:]}
     if rank == 0:
         print(json.dumps(line), flush=True)
     if world > 1:
