@@ -25,15 +25,17 @@
 //    when the CTA leaves a unit. The next copy into a stage is issued as soon
 //    as the MMA that read it completes.
 //  * k_topk_select: one 8-CTA thread-block cluster per (unit, row). The global
-//    histogram gives the bin b1 of the K-th largest key. One pass over the
-//    cluster's key ranges (cached in shared memory when they fit) counts keys
-//    above b1 and collects the candidates inside b1; the cluster shares the
-//    candidates through distributed shared memory and every CTA finds the
+//    histogram gives the bin b1 of the K-th largest key. One pass streams each
+//    CTA's key range through shared memory (1-D bulk TMA copies of 4096-key
+//    tiles, two in flight) in position order: it counts the keys above b1,
+//    pushes the candidates inside b1 to every CTA of the cluster through
+//    distributed shared memory, and keeps every key of bin >= b1 with its
+//    position in an ordered list (block scans per tile). Every CTA finds the
 //    exact threshold key T (and how many keys equal to T are taken) by a
-//    local radix select over them. If the candidates do not fit, three
-//    refinement passes with cluster-summed histograms find T instead. A last
-//    pass writes the selected positions in ascending order (ballot-based
-//    ordered compaction); keys equal to T are taken lowest position first.
+//    local radix select over the candidates; if they do not fit, three
+//    refinement passes with cluster-summed histograms find T instead. The
+//    output is compacted from the ordered list (or, if it overflowed, from
+//    the whole range): keys above T, and keys equal to T lowest position first.
 #include <algorithm>
 #include <cooperative_groups.h>
 
@@ -47,8 +49,9 @@ namespace {
 constexpr int HIST1_BINS = 4096;         // top 12 bits of the ordered key
 constexpr int SEL_CLUSTER = 8;
 constexpr int SEL_THREADS = 512;
-constexpr int SEL_KEY_CACHE = 16384;     // keys of a CTA's range kept in shared memory
-constexpr int SEL_CAND_CAP = 4096;       // candidates per CTA (fast path)
+constexpr int SEL_TILE = 4096;           // keys per streamed tile (16 KB)
+constexpr int SEL_STAGES = 2;            // tiles in flight per CTA
+constexpr int SEL_LIST_CAP = 2048;       // keys of bin >= b1 kept per CTA, in order
 constexpr int SEL_ALL_CAP = 8192;        // candidates per cluster (fast path)
 constexpr int SEL_PER_SRC = SEL_ALL_CAP / SEL_CLUSTER;   // candidates each CTA may push
 
@@ -483,25 +486,30 @@ __device__ __forceinline__ void find_digit_wide(const uint32_t* h, int nb, int n
 }
 
 struct SelShared {
-  uint32_t h1[HIST1_BINS];
   uint32_t hl[2][256];
   uint32_t hg[256];
   int tmp[32];
-  int wsum[SEL_THREADS / 32];
   int bin, above;
-  int ncand, overflow;
-  int any_over;               // some CTA of the cluster overflowed
-  uint64_t kbar;              // bulk copy of this CTA's key range
-  int coff[SEL_CLUSTER + 1];  // (fallback bookkeeping)
+  int ncand;
+  int list_n;                 // entries of this CTA's list (above the cap: it overflowed)
+  uint64_t sbar[SEL_STAGES];  // streamed key tiles
   int srcn[SEL_CLUSTER];      // candidates pushed here by each CTA (-1: it overflowed)
   long long rcnt[SEL_CLUSTER][2];   // (gt, eq) of each CTA, read once for the prefix
   long long cnt[2];           // this CTA's (gt, eq) counts
 };
-// The key cache (a bulk-copy destination) starts 128-byte aligned after it.
-constexpr size_t SEL_KC_OFF = (sizeof(SelShared) + 127) / 128 * 128;
-static_assert(SEL_KC_OFF % 16 == 0 && SEL_KC_OFF >= sizeof(SelShared), "bulk-copy destination alignment");
+// Shared memory after SelShared (each part 128-byte aligned): region U holds
+// the streamed key tiles during the pass and the 4096-bin radix histogram
+// after it; then the ordered list (positions, keys); then the candidates of
+// the whole cluster.
+constexpr size_t SEL_U_OFF = (sizeof(SelShared) + 127) / 128 * 128;
+constexpr size_t SEL_U_BYTES = (size_t)SEL_STAGES * SEL_TILE * 4;
+constexpr size_t SEL_LIST_OFF = SEL_U_OFF + SEL_U_BYTES;
+constexpr size_t SEL_ALLC_OFF = SEL_LIST_OFF + (size_t)SEL_LIST_CAP * 8;
+constexpr size_t SEL_SMEM = SEL_ALLC_OFF + (size_t)SEL_ALL_CAP * 4;
+static_assert(SEL_U_OFF % 16 == 0 && SEL_TILE * 4 % 16 == 0, "bulk-copy destination alignment");
+static_assert(SEL_U_BYTES >= HIST1_BINS * 4, "region U also holds the radix histogram");
 
-__global__ void __cluster_dims__(SEL_CLUSTER, 1, 1) __launch_bounds__(SEL_THREADS, 1)
+__global__ void __cluster_dims__(SEL_CLUSTER, 1, 1) __launch_bounds__(SEL_THREADS, 2)
 k_topk_select(const dsa_unit* __restrict__ units, int R, int K, uint32_t* __restrict__ hist,
               const uint32_t* __restrict__ okeys, int64_t stride, int32_t* __restrict__ topk_idx,
               int64_t max_len, int32_t* dev_err) {
@@ -527,47 +535,50 @@ k_topk_select(const dsa_unit* __restrict__ units, int R, int K, uint32_t* __rest
   asm volatile("barrier.cluster.arrive.relaxed.aligned;" ::: "memory");
   extern __shared__ __align__(128) uint8_t smem_sel[];
   SelShared* S = reinterpret_cast<SelShared*>(smem_sel);
-  uint32_t* kc = reinterpret_cast<uint32_t*>(smem_sel + SEL_KC_OFF);          // [SEL_KEY_CACHE]
-  uint32_t* cand = kc + SEL_KEY_CACHE;                                        // [SEL_CAND_CAP]
-  uint32_t* allc = cand + SEL_CAND_CAP;                                       // [SEL_ALL_CAP]
+  uint8_t* regU = smem_sel + SEL_U_OFF;
+  uint32_t* h1 = reinterpret_cast<uint32_t*>(regU);                           // [4096], after the pass
+  int32_t* lpos = reinterpret_cast<int32_t*>(smem_sel + SEL_LIST_OFF);        // [SEL_LIST_CAP]
+  uint32_t* lkey = reinterpret_cast<uint32_t*>(lpos + SEL_LIST_CAP);          // [SEL_LIST_CAP]
+  uint32_t* allc = reinterpret_cast<uint32_t*>(smem_sel + SEL_ALLC_OFF);      // [SEL_ALL_CAP]
   const int tid = threadIdx.x;
   // this CTA's key range, a multiple of 4 keys (16-byte aligned bulk copies)
   const int64_t chunk = ((L + SEL_CLUSTER - 1) / SEL_CLUSTER + 3) / 4 * 4;
   const int64_t beg = min((int64_t)crank * chunk, L);
   const int64_t end = min(beg + chunk, L);
+  const int64_t nkeys = end - beg;
+  const int ntile = (int)((nkeys + SEL_TILE - 1) / SEL_TILE);
   const uint32_t* kk = okeys + (size_t)ur * stride;
-  const bool cached = (end - beg) + 4 <= SEL_KEY_CACHE;
+  // bulk copies need 16-byte aligned sources (always true for workspaces from
+  // dsa_score_topk_workspace; otherwise the keys are read from global memory)
+  const bool stream = ((reinterpret_cast<uintptr_t>(kk + beg)) & 15u) == 0;
+  // tile i: keys [beg + i*SEL_TILE, +n) into stage i % SEL_STAGES; the copy
+  // is rounded up to 4 keys (rows are padded to a multiple of 4)
+  auto issue = [&](int i) {
+    const int64_t k0 = (int64_t)i * SEL_TILE;
+    const int64_t n = min((int64_t)SEL_TILE, nkeys - k0);
+    const uint32_t bytes = (uint32_t)((n + 3) / 4 * 16);
+    const int st = i % SEL_STAGES;
+    tc::mbar_arrive_expect_tx(&S->sbar[st], bytes);
+    tc::bulk_g2s(regU + (size_t)st * SEL_TILE * 4, kk + beg + k0, bytes, &S->sbar[st]);
+  };
   if (tid == 0) {
     S->bin = 0;
     S->above = 0;
     S->ncand = 0;
-    S->overflow = 0;
-    tc::mbar_init(&S->kbar, 1);
+    for (int i = 0; i < SEL_STAGES; ++i) tc::mbar_init(&S->sbar[i], 1);
     tc::fence_mbar_init();
-    if (cached && end > beg && (tc::smem_u32(kc) & 15u) == 0 &&
-        ((reinterpret_cast<uintptr_t>(kk + beg)) & 15u) == 0) {
-      // the keys were written by k_dsa_score; the bulk copy reads them through
-      // the async proxy (rounded up to 16 bytes: the rows are padded to 4 keys)
-      const uint32_t bytes = (uint32_t)(((end - beg) * 4 + 15) / 16 * 16);
-      tc::mbar_arrive_expect_tx(&S->kbar, bytes);
-      tc::bulk_g2s(kc, kk + beg, bytes, &S->kbar);
-    }
+    if (stream)
+      for (int i = 0; i < SEL_STAGES && i < ntile; ++i) issue(i);
   }
 
-  // ---- level 1: top 12 bits from the global histogram
+  // ---- level 1: top 12 bits from the global histogram (read in place)
   uint32_t* gh = hist + (size_t)ur * HIST1_BINS;
-  for (int i = tid; i < HIST1_BINS / 4; i += SEL_THREADS)
-    reinterpret_cast<uint4*>(S->h1)[i] = reinterpret_cast<const uint4*>(gh)[i];
-  __syncthreads();
-  find_digit_wide<SEL_THREADS>(S->h1, HIST1_BINS, K, S->tmp, &S->bin, &S->above);
+  find_digit_wide<SEL_THREADS>(gh, HIST1_BINS, K, S->tmp, &S->bin, &S->above);
   const uint32_t b1 = (uint32_t)S->bin;
   int need = K - S->above;
 
-  // four keys [4q, 4q + 4) of the range, one 16-byte load (shared or global)
-  auto key4 = [&](int64_t q) -> uint4 {
-    return cached ? *reinterpret_cast<const uint4*>(kc + (4 * q - beg))
-                  : __ldcg(reinterpret_cast<const uint4*>(kk + 4 * q));
-  };
+  // four keys [4q, 4q + 4) of the range from global memory (the fallbacks)
+  auto key4 = [&](int64_t q) -> uint4 { return __ldcg(reinterpret_cast<const uint4*>(kk + 4 * q)); };
   // quads covering [beg, end); beg is a multiple of 4 whenever the range is
   // not empty (a trailing CTA whose range is empty gets no quads)
   const int64_t q0 = beg / 4, q1 = end > beg ? (end + 3) / 4 : q0;
@@ -593,37 +604,79 @@ k_topk_select(const dsa_unit* __restrict__ units, int R, int K, uint32_t* __rest
     }
   };
 
-  // ---- one pass: cache keys, count keys above b1, collect candidates in b1
-  if (cached && end > beg) {
-    if ((tc::smem_u32(kc) & 15u) != 0 || ((reinterpret_cast<uintptr_t>(kk + beg)) & 15u) != 0) {
-      // no bulk copy was issued: stage the keys with plain loads
-      for (int64_t i = tid; i < end - beg; i += SEL_THREADS) kc[i] = kk[beg + i];
-      __syncthreads();
-    } else if (!tc::mbar_wait(&S->kbar, 0)) {
-      dsa_flag(dev_err, DSA_DEVERR_TIMEOUT);
-    }
-  }
   asm volatile("barrier.cluster.wait.aligned;" ::: "memory");
   // candidates go to region [crank] of every CTA's candidate buffer
   uint32_t* dst[SEL_CLUSTER];
 #pragma unroll
   for (int c = 0; c < SEL_CLUSTER; ++c) dst[c] = cluster.map_shared_rank(allc, c) + crank * SEL_PER_SRC;
+
+  // ---- one pass over the range, tile by tile in position order: count the
+  //      keys above bin b1, push the candidates inside b1 to the cluster, and
+  //      keep every key of bin >= b1 (position and key) in an ordered list;
+  //      thread t owns keys [8t, 8t + 8) of a tile
   long long gt1 = 0;
-  for_keys([&](int64_t, uint32_t key) {
-    const uint32_t d1 = key >> 20;
-    if (d1 > b1) {
-      ++gt1;
-    } else if (d1 == b1) {
-      const int i = atomicAdd(&S->ncand, 1);
-      if (i < SEL_PER_SRC) {
+  int lbase = 0;       // list entries so far (may pass the cap)
+  bool timed_out = false;
+  for (int i = 0; i < ntile; ++i) {
+    const int st = i % SEL_STAGES;
+    const int64_t p0 = beg + (int64_t)i * SEL_TILE + 8 * tid;
+    uint32_t w[8];
+    bool ok = true;
+    if (stream) {
+      ok = tc::mbar_wait(&S->sbar[st], (uint32_t)((i / SEL_STAGES) & 1));
+      const uint4* t4 = reinterpret_cast<const uint4*>(regU + (size_t)st * SEL_TILE * 4) + 2 * tid;
+      const uint4 a = ok ? t4[0] : make_uint4(0, 0, 0, 0);
+      const uint4 b = ok ? t4[1] : make_uint4(0, 0, 0, 0);
+      w[0] = a.x; w[1] = a.y; w[2] = a.z; w[3] = a.w; w[4] = b.x; w[5] = b.y; w[6] = b.z; w[7] = b.w;
+    } else {
 #pragma unroll
-        for (int c = 0; c < SEL_CLUSTER; ++c) dst[c][i] = key;
+      for (int e = 0; e < 8; ++e) w[e] = p0 + e < end ? __ldcg(kk + p0 + e) : 0u;
+    }
+    timed_out |= !ok;
+    int c = 0;
+#pragma unroll
+    for (int e = 0; e < 8; ++e) {
+      const bool in = p0 + e < end;
+      const uint32_t d1 = w[e] >> 20;
+      gt1 += in && d1 > b1;
+      c += in && d1 >= b1;
+      if (in && d1 == b1) {
+        const int k = atomicAdd(&S->ncand, 1);
+        if (k < SEL_PER_SRC) {
+#pragma unroll
+          for (int cc = 0; cc < SEL_CLUSTER; ++cc) dst[cc][k] = w[e];
+        }
       }
     }
-  });
+    int tot;
+    const int inc = block_inclusive_scan<SEL_THREADS>(c, S->tmp, &tot);   // ends with a barrier
+    int o = lbase + inc - c;
+#pragma unroll
+    for (int e = 0; e < 8; ++e) {
+      if (p0 + e < end && (w[e] >> 20) >= b1) {
+        if (o < SEL_LIST_CAP) {
+          lpos[o] = (int32_t)(p0 + e);
+          lkey[o] = w[e];
+        }
+        ++o;
+      }
+    }
+    lbase += tot;
+    // every thread has read the stage (the scan's barriers): refill it
+    if (stream && tid == 0 && i + SEL_STAGES < ntile) issue(i + SEL_STAGES);
+  }
+  if (__syncthreads_or(timed_out) && tid == 0) {
+    // (does not happen in normal runs) the selection is void; every stage's
+    // last copy gets one more bounded wait so that none lands later
+    dsa_flag(dev_err, DSA_DEVERR_TIMEOUT);
+    for (int st = 0; st < SEL_STAGES; ++st) {
+      const int last = st < ntile ? st + (ntile - 1 - st) / SEL_STAGES * SEL_STAGES : -1;
+      if (last >= 0) tc::mbar_wait(&S->sbar[st], (uint32_t)((last / SEL_STAGES) & 1));
+    }
+  }
+  __syncthreads();
   int gt1_cta;
   block_inclusive_scan<SEL_THREADS>((int)gt1, S->tmp, &gt1_cta);
-  if (tid == 0) S->overflow = S->ncand > SEL_PER_SRC;
   if (tid < SEL_CLUSTER)
     cluster.map_shared_rank(S, tid)->srcn[crank] = S->ncand > SEL_PER_SRC ? -1 : S->ncand;
   __syncthreads();
@@ -646,16 +699,16 @@ k_topk_select(const dsa_unit* __restrict__ units, int R, int K, uint32_t* __rest
   if (fast) {
     // ---- every CTA holds all candidates (pushed into per-source regions):
     //      exact local radix select on bits 19..8 and 7..0
-    for (int i = tid; i < HIST1_BINS; i += SEL_THREADS) S->h1[i] = 0;
+    for (int i = tid; i < HIST1_BINS; i += SEL_THREADS) h1[i] = 0;
     __syncthreads();
     const uint32_t p1 = b1 << 20;
     for (int i = tid; i < SEL_ALL_CAP; i += SEL_THREADS) {
       if ((i % SEL_PER_SRC) >= S->srcn[i / SEL_PER_SRC]) continue;
       const uint32_t key = allc[i];
-      if ((key & 0xFFF00000u) == p1) atomicAdd(&S->h1[(key >> 8) & 0xFFF], 1u);
+      if ((key & 0xFFF00000u) == p1) atomicAdd(&h1[(key >> 8) & 0xFFF], 1u);
     }
     __syncthreads();
-    find_digit_wide<SEL_THREADS>(S->h1, HIST1_BINS, need, S->tmp, &S->bin, &S->above);
+    find_digit_wide<SEL_THREADS>(h1, HIST1_BINS, need, S->tmp, &S->bin, &S->above);
     need -= S->above;
     const uint32_t p2 = p1 | ((uint32_t)S->bin << 8);
     for (int i = tid; i < 256; i += SEL_THREADS) S->hg[i] = 0;
@@ -745,28 +798,24 @@ k_topk_select(const dsa_unit* __restrict__ units, int R, int K, uint32_t* __rest
     sel_before += g + take;
     eq_before += e;
   }
-  // ---- ordered compaction of this CTA's range, in tiles of 8 x SEL_THREADS
-  //      keys: thread t owns 8 consecutive keys of the tile (two 16-byte
-  //      loads); two block scans give each thread its tie rank and output
-  //      offset
-  {
+  // ---- ordered compaction: keys above T, and keys equal to T lowest position
+  //      first, written at the CTA's offset. From the ordered list when it
+  //      held every key of bin >= b1 (all selected keys are among them), else
+  //      from the whole range. Per group of entries: thread t owns NPT
+  //      consecutive entries; two block scans give its tie rank and offset.
+  auto compact = [&](int64_t nent, auto&& entry) {
+    constexpr int NPT = 8;
     long long run_eq = eq_before, run_sel = sel_before;
-    for (int64_t tb = q0; tb < q1; tb += 2 * SEL_THREADS) {
-      const int64_t qa = tb + 2 * tid;
-      uint32_t w[8];
-      {
-        const uint4 a = qa < q1 ? key4(qa) : make_uint4(0, 0, 0, 0);
-        const uint4 b = qa + 1 < q1 ? key4(qa + 1) : make_uint4(0, 0, 0, 0);
-        w[0] = a.x; w[1] = a.y; w[2] = a.z; w[3] = a.w;
-        w[4] = b.x; w[5] = b.y; w[6] = b.z; w[7] = b.w;
-      }
-      const int64_t p0 = 4 * qa;
+    for (int64_t gb = 0; gb < nent; gb += (int64_t)NPT * SEL_THREADS) {
+      const int64_t e0 = gb + (int64_t)NPT * tid;
+      int32_t pos[NPT];
+      uint32_t key[NPT];
       int g = 0, e = 0;
 #pragma unroll
-      for (int k = 0; k < 8; ++k) {
-        const bool in = p0 + k >= beg && p0 + k < end;
-        g += in && w[k] > T;
-        e += in && w[k] == T;
+      for (int k = 0; k < NPT; ++k) {
+        entry(e0 + k, pos[k], key[k]);           // pos < 0: no entry
+        g += pos[k] >= 0 && key[k] > T;
+        e += pos[k] >= 0 && key[k] == T;
       }
       int etot, stot;
       const int einc = block_inclusive_scan<SEL_THREADS>(e, S->tmp, &etot);
@@ -778,28 +827,39 @@ k_topk_select(const dsa_unit* __restrict__ units, int R, int K, uint32_t* __rest
       long long o = run_sel + sinc - sel;
       long long er = estart;
 #pragma unroll
-      for (int k = 0; k < 8; ++k) {
-        const bool in = p0 + k >= beg && p0 + k < end;
-        bool pick = in && w[k] > T;
-        if (in && w[k] == T) {
+      for (int k = 0; k < NPT; ++k) {
+        bool pick = pos[k] >= 0 && key[k] > T;
+        if (pos[k] >= 0 && key[k] == T) {
           pick = er < ties;
           ++er;
         }
         if (pick) {
-          if (o < K) out[o] = (int32_t)(p0 + k);
+          if (o < K) out[o] = pos[k];
           ++o;
         }
       }
       run_eq += etot;
       run_sel += stot;
     }
+  };
+  if (lbase <= SEL_LIST_CAP) {
+    compact(lbase, [&](int64_t i, int32_t& p, uint32_t& k) {
+      p = i < lbase ? lpos[i] : -1;
+      k = i < lbase ? lkey[i] : 0u;
+    });
+  } else {
+    const int64_t nq = q1 - q0;   // the whole range, 4 keys per quad from global memory
+    compact(4 * nq, [&](int64_t i, int32_t& p, uint32_t& k) {
+      const int64_t pp = 4 * q0 + i;
+      const bool in = pp >= beg && pp < end;
+      p = in ? (int32_t)pp : -1;
+      k = in ? __ldcg(kk + pp) : 0u;
+    });
   }
   cluster.sync();   // keep this CTA's shared memory alive for its peers
 }
 
-inline size_t select_smem() {
-  return SEL_KC_OFF + (size_t)(SEL_KEY_CACHE + SEL_CAND_CAP + SEL_ALL_CAP) * 4;
-}
+inline size_t select_smem() { return SEL_SMEM; }
 
 DsaPerDevice g_setup;   // kernel attributes and SM count, per device
 
@@ -820,6 +880,7 @@ extern "C" int dsa_score_topk(const dsa_unit* units, int32_t U, int32_t R, int32
   if ((int64_t)U * R > 65535) return DSA_ERR_ARG;
   if (K < 1 || K > DSA_MAX_K) return DSA_ERR_SHAPE;
   if (!ws || ws_bytes < dsa_score_topk_workspace(U, R, max_len)) return DSA_ERR_WS;
+  if (reinterpret_cast<uintptr_t>(ws) & 15u) return DSA_ERR_ARG;   // its keys are read by bulk copies
   cudaStream_t st = static_cast<cudaStream_t>(stream);
   TopkWs tw = topk_ws(ws, U, R, max_len);
   if (reinterpret_cast<uintptr_t>(q) & 15u) return DSA_ERR_ARG;   // query rows are read as 16-byte vectors

@@ -202,8 +202,9 @@ int hc_init(const dsa_unit* units, int32_t U, int32_t warm, const int64_t* l0,
  *   topk_idx  device int32 [U][R][K] (written).
  *   max_len   host bound: max over units of L (sizes the grid).
  *   ws        device workspace of dsa_score_topk_workspace(U, R, max_len)
- *             bytes. It must be zero-filled once before its first use; every
- *             call leaves it ready for the next.
+ *             bytes, 16-byte aligned. It must be zero-filled once before its
+ *             first use; every call leaves it ready for the next.
+ *   q         must be 16-byte aligned as well (read as 16-byte vectors).
  * Shapes: 1 <= U, 1 <= R <= 8, 1 <= K <= 4096.
  */
 size_t dsa_score_topk_workspace(int32_t U, int32_t R, int64_t max_len);

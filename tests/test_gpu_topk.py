@@ -87,3 +87,23 @@ def test_negative_weights_and_fractional_queries():
     q = _bits(rng.integers(-64, 65, size=(1, 2, 8, 64)) / 16.0)
     w = rng.integers(-4, 5, size=(1, 2, 8))
     _run(keys, q, w, 777)
+
+
+def test_many_selected_keys_in_one_cluster_range():
+    """Most of a large Top-K lies in the first CTA's part of the history, so
+    that CTA's ordered list of keys at or above the threshold bin overflows
+    and the output is compacted from its whole range instead."""
+    rng = np.random.default_rng(5)
+    k = np.zeros((40000, 64))
+    k[:6000] = rng.integers(1, 5, size=(6000, 64))
+    keys = [_bits(k)]
+    q = _bits(np.ones((1, 1, 8, 64)))
+    _run(keys, q, np.ones((1, 1, 8)), 4096)
+
+
+def test_short_history_in_few_tiles_and_empty_cluster_ranges():
+    rng = np.random.default_rng(6)
+    keys = [_bits(rng.integers(-4, 5, size=(n, 64))) for n in (2049, 2051, 4100, 9)]
+    q = _bits(rng.integers(-4, 5, size=(4, 1, 8, 64)))
+    w = rng.integers(1, 5, size=(4, 1, 8))
+    _run(keys, q, w, 2048)
