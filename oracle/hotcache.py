@@ -49,6 +49,20 @@ C7 append: the row at position ``p = len`` goes to ring row ``p % 64`` and its
 
 The ascending assignment order of C5, the hand update and the insertion filter
 of C3 are readings of "ring replacement skipping pinned slots".
+
+C8 clock with reference bits (the policy the pages replaced by the ring; a
+   unit built with ``policy="clock"``). Section "GPU 管缓存也会犯错" describes
+   it only by its cost: with a full window, every reference bit set and 1%
+   misses, the few missing blocks had to sweep far. Readings: each slot has a
+   reference bit; a HOT hit sets it; warm slots start with it set, empty ones
+   clear. To find victims for M (same list as C3), the hand walks the slots
+   cyclically from ``hand``: a slot pinned in this call, filled in this round
+   or already taken in this walk is passed over; a slot whose bit is set gets
+   it cleared and is passed over; a slot whose bit is clear is the next
+   victim. The walk stops when every position of M has a victim or after two
+   turns (after one turn every eligible bit is clear). A fill sets the bit
+   (the row was just referenced). ``hand`` = last victim + 1; ``last_sweep``
+   is the number of slots the hand visited.
 """
 from __future__ import annotations
 
@@ -92,7 +106,10 @@ class MirrorStore:
 
 
 class UnitCache:
-    def __init__(self, S: int, lmax: int, L0: int, mirror_initial, warm: str):
+    def __init__(self, S: int, lmax: int, L0: int, mirror_initial, warm: str, policy: str = "ring"):
+        if policy not in ("ring", "clock"):
+            raise ValueError(policy)
+        self.policy = policy
         self.S = S
         self.lmax = lmax
         self.slot_pos = np.full(S, -1, dtype=np.int64)
@@ -105,12 +122,15 @@ class UnitCache:
         self.rows_in_ram = L0
         self.length = L0
         self.writebacks = 0
+        self.ref = np.zeros(S, dtype=np.uint8)      # C8 reference bits
+        self.last_sweep = 0
         if warm == "last_s":
             n = min(S, L0)
             pos = np.arange(L0 - n, L0, dtype=np.int64)
             self.slot_pos[:n] = pos
             self.pos_slot[pos] = np.arange(n)
             self.slots[:n] = self.mirror.rows(pos)
+            self.ref[:n] = 1
         elif warm != "empty":
             raise ValueError(warm)
 
@@ -143,6 +163,7 @@ class UnitCache:
                 cls[i, j] = c
                 if c == HOT:
                     pinned.add(int(self.pos_slot[p]))
+                    self.ref[self.pos_slot[p]] = 1
         # rows as read at call start (pinned HOT slots and the ring do not change below)
         for i in range(R):
             for j in range(K):
@@ -157,14 +178,17 @@ class UnitCache:
         # C3
         M = sorted({int(topk[i, j]) for i in range(R) for j in range(K)
                     if cls[i, j] == RAM and self.pos_slot[int(topk[i, j])] < 0})
-        # C5
-        E = []
-        for t in range(self.S):
-            if len(E) == len(M):
-                break
-            s = (self.hand + t) % self.S
-            if s not in pinned and self.fill_round[s] < r:
-                E.append(s)
+        if self.policy == "ring":
+            # C5
+            E = []
+            for t in range(self.S):
+                if len(E) == len(M):
+                    break
+                s = (self.hand + t) % self.S
+                if s not in pinned and self.fill_round[s] < r:
+                    E.append(s)
+        else:
+            E = self._clock_victims(pinned, r, len(M))
         n = min(len(M), len(E))
         for i in range(n):
             s, p = E[i], M[i]
@@ -175,11 +199,29 @@ class UnitCache:
             self.pos_slot[p] = s
             self.fill_round[s] = r
             self.slots[s] = self.mirror.rows([p])[0]
+            self.ref[s] = 1
         if n > 0:
             self.hand = (E[n - 1] + 1) % self.S
         counters = np.array([(cls == HOT).sum(), (cls == RING).sum(), (cls == RAM).sum(), n],
                             dtype=np.int64)
         return cls, rows, counters
+
+    # -- C8
+    def _clock_victims(self, pinned, r: int, m: int) -> list:
+        """The clock hand's walk for m victims (see C8); one slot per visit."""
+        E, taken = [], set()
+        s, visits = self.hand, 0
+        while len(E) < m and visits < 2 * self.S:
+            visits += 1
+            if s not in pinned and s not in taken and self.fill_round[s] < r:
+                if self.ref[s]:
+                    self.ref[s] = 0
+                else:
+                    E.append(s)
+                    taken.add(s)
+            s = (s + 1) % self.S
+        self.last_sweep = visits
+        return E
 
     # -- C7
     def append(self, new_rows: np.ndarray, keys=None, new_keys=None) -> None:
