@@ -64,6 +64,8 @@ def parse():
                     help="run the workload with fewer sessions (a reduced case for profiling)")
     ap.add_argument("--reps", type=int, default=5, help="timed repetitions of the K steps (median reported)")
     ap.add_argument("--mirror", choices=["host", "device"], default="host")
+    ap.add_argument("--policy", choices=["ring", "clock"], default="ring",
+                    help="hot-cache replacement of the headline workload")
     ap.add_argument("--impl", choices=["gb300", "reference"], default="gb300")
     ap.add_argument("--no-e2e", action="store_true")
     ap.add_argument("--no-graph", action="store_true", help="launch steps directly, no CUDA graph")
@@ -97,6 +99,8 @@ def workload(args, cid=None):
         wl = wl.with_(sessions=args.sessions)
     if args.reuse_every > 1:
         wl = wl.with_(reuse_every=args.reuse_every)
+    if cid is None and args.policy != "ring":
+        wl = wl.with_(policy=args.policy)
     return wl
 
 
@@ -323,7 +327,7 @@ class WorkloadRun:
         self.mirror = mirror
         wlr = wl.with_(steps=Wm + K)
         U = wl.U
-        self.units = UnitSet(U, wl.S, wlr.lmax, mirror=mirror)
+        self.units = UnitSet(U, wl.S, wlr.lmax, mirror=mirror, policy=wl.policy)
         src = [wl.selection_source(u) for u in range(U)] if wl.reuse_every > 1 else None
         self.path = DecodePath(self.units, wl.R, wl.K, wl.H, wl.A, wl.scale(), selection_source=src)
         sg.history(wlr, self.units)
@@ -589,7 +593,8 @@ def run_gpu(args, rank: int, world: int):
         "vs_baseline": None, "dtype": DTYPE,
         "data": "synthetic (seeded counter-based generator, generated on the device)",
         "config": workload_config(wl, {
-            "mirror": args.mirror, "l2": "flushed before every timed step (512 MiB write outside the bracket)",
+            "mirror": args.mirror, "replacement": wl.policy,
+            "l2": "flushed before every timed step (512 MiB write outside the bracket)",
             "selection_reuse_every": wl.reuse_every,
             "path": "hot_gather_attn (fused)" if args.path == "fused" else
                     "hot_gather + mla_decode_attn, append concurrent",

@@ -23,6 +23,7 @@ ROW_BYTES, LAT_DIM, ROPE_DIM, IDX_HEADS, IDX_DIM, RING_ROWS = 656, 512, 64, 8, 6
 MAX_K, MAX_ROWS, MAX_ATTN_K, ROUND_AUTO = 4096, 8, 2048, -1
 CLS_HOT, CLS_RING, CLS_RAM, CLS_PAD = 0, 1, 2, 3
 WARM_EMPTY, WARM_LAST_S = 0, 1
+POLICY_RING, POLICY_CLOCK = 0, 1
 ST_LEN, ST_RAM, ST_HAND, ST_EPOCH, ST_WRITEBACKS, ST_ROUND, ST_WORDS = 0, 1, 2, 3, 4, 5, 8
 
 
@@ -38,12 +39,12 @@ class DsaUnit(ctypes.Structure):
         ("keys", ctypes.c_void_p), ("slots", ctypes.c_void_p), ("slot_pos", ctypes.c_void_p),
         ("pos_slot", ctypes.c_void_p), ("fill_round", ctypes.c_void_p),
         ("pin_epoch", ctypes.c_void_p), ("ring", ctypes.c_void_p), ("mirror", ctypes.c_void_p),
-        ("state", ctypes.c_void_p), ("slots_n", ctypes.c_int32), ("reserved0", ctypes.c_int32),
-        ("lmax", ctypes.c_int64),
+        ("state", ctypes.c_void_p), ("slots_n", ctypes.c_int32), ("policy", ctypes.c_int32),
+        ("lmax", ctypes.c_int64), ("ref", ctypes.c_void_p),
     ]
 
 
-assert ctypes.sizeof(DsaUnit) == 88
+assert ctypes.sizeof(DsaUnit) == 96
 
 _VP, _I32, _I64, _SZ, _F = ctypes.c_void_p, ctypes.c_int32, ctypes.c_int64, ctypes.c_size_t, ctypes.c_float
 

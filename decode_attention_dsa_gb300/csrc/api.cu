@@ -162,6 +162,7 @@ k_init_map(const dsa_unit* __restrict__ units, int warm, const int64_t* __restri
     un.slot_pos[i] = i < n ? (int32_t)(first + i) : -1;
     un.fill_round[i] = -1;
     un.pin_epoch[i] = -1;
+    if (un.ref) un.ref[i] = i < n ? 1 : 0;
   }
   if (i < DSA_ST_WORDS) {
     int64_t v = 0;
@@ -224,7 +225,7 @@ extern "C" int dsa_wait_selftest(int64_t limit_cycles, int32_t complete, int32_t
   return dsa_launch_status();
 }
 
-extern "C" int dsa_abi_version(void) { return 1; }
+extern "C" int dsa_abi_version(void) { return 2; }
 
 extern "C" const char* dsa_status_string(int status) {
   switch (status) {

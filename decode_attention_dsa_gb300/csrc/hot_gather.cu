@@ -82,7 +82,9 @@ k_assign(const dsa_unit* __restrict__ units, int R, int K, int round,
   // a unit whose arrays are misaligned, or a round below the unit's previous
   // one (it would break the visibility rule), is skipped: every entry PAD
   // (k_copy zeroes its compact row), no fill, state untouched
-  const bool misaligned = !unit_aligned(un);
+  const bool clock = un.policy == DSA_POLICY_CLOCK;
+  const bool misaligned = !unit_aligned(un) || (clock && !un.ref) ||
+                          (un.policy != DSA_POLICY_RING && !clock);   // (or an unknown policy)
   if (misaligned || (int64_t)round + 1 < un.state[DSA_ST_ROUND]) {
     if (threadIdx.x == 0) {
       dsa_flag(dev_err, misaligned ? DSA_DEVERR_BOUNDS : DSA_DEVERR_ROUND);
@@ -146,6 +148,7 @@ k_assign(const dsa_unit* __restrict__ units, int R, int K, int round,
           if (sl >= 0 && sl < S && fv[b] < round) {
             c = DSA_CLS_HOT;
             un.pin_epoch[sl] = epoch;
+            if (clock) un.ref[sl] = 1;        // a hit sets the reference bit
           } else {
             c = DSA_CLS_RAM;
             unmapped = sl < 0;
@@ -235,26 +238,48 @@ k_assign(const dsa_unit* __restrict__ units, int R, int K, int round,
   int nM;
   block_inclusive_scan<ASSIGN_THREADS>(nM_local, s_tmp, &nM);
 
-  // 3. eligible slots in cyclic order from the hand
+  // 3. victims in cyclic order from the hand. Ring: the eligible slots (not
+  //    pinned in this call, not filled in this round). Clock: the eligible
+  //    slots whose reference bit is clear (the hand's first turn), then those
+  //    whose bit is set (its second turn, after the first cleared them).
   const int hand0 = (int)un.state[DSA_ST_HAND];
-  int found = 0;
-  for (int base = 0; base < S && found < nM; base += ASSIGN_THREADS) {
-    const int t = base + threadIdx.x;
-    int sidx = -1;
-    int elig = 0;
-    if (t < S) {
-      sidx = hand0 + t;
-      if (sidx >= S) sidx -= S;
-      elig = (un.pin_epoch[sidx] != epoch) && (un.fill_round[sidx] < round);
+  int found = 0, found_first = 0;
+  for (int pass = 0; pass < (clock ? 2 : 1) && found < nM; ++pass) {
+    for (int base = 0; base < S && found < nM; base += ASSIGN_THREADS) {
+      const int t = base + threadIdx.x;
+      int sidx = -1;
+      int elig = 0;
+      if (t < S) {
+        sidx = hand0 + t;
+        if (sidx >= S) sidx -= S;
+        elig = (un.pin_epoch[sidx] != epoch) && (un.fill_round[sidx] < round);
+        if (clock && elig) elig = (un.ref[sidx] != 0) == (pass == 1);
+      }
+      int tot;
+      const int inc = block_inclusive_scan<ASSIGN_THREADS>(elig, s_tmp, &tot);
+      const int rank = found + inc - elig;
+      if (elig && rank < nM) fill_slot[rank] = sidx;
+      found += tot;
     }
-    int tot;
-    const int inc = block_inclusive_scan<ASSIGN_THREADS>(elig, s_tmp, &tot);
-    const int rank = found + inc - elig;
-    if (elig && rank < nM) fill_slot[rank] = sidx;
-    found += tot;
+    if (pass == 0) found_first = found;
   }
   const int n = min(found, nM);
   __syncthreads();
+  if (clock && n > 0) {
+    // the bits the first turn passed are cleared: up to the last victim if
+    // the first turn found them all, else every eligible slot's
+    int limit = S;
+    if (n <= found_first) {
+      const int last = fill_slot[n - 1];
+      limit = last >= hand0 ? last - hand0 : last + S - hand0;
+    }
+    for (int t = threadIdx.x; t < limit; t += ASSIGN_THREADS) {
+      int sidx = hand0 + t;
+      if (sidx >= S) sidx -= S;
+      if (un.pin_epoch[sidx] != epoch && un.fill_round[sidx] < round && un.ref[sidx]) un.ref[sidx] = 0;
+    }
+    __syncthreads();
+  }
 
   // 4. map update (distinct slots, distinct new positions, and old positions
   //    that are neither new positions nor pinned: safe in parallel)
@@ -266,6 +291,7 @@ k_assign(const dsa_unit* __restrict__ units, int R, int K, int round,
     un.slot_pos[sl] = p;
     un.pos_slot[p] = sl;
     un.fill_round[sl] = round;
+    if (clock) un.ref[sl] = 1;                // a fill sets the reference bit
   }
   // served[e] = 1 for owners that received a slot and for the later
   // occurrences of their position: the fill reads the mirror row once and

@@ -22,9 +22,10 @@ class UnitSet:
     fully resident run of the same kernels).
     """
 
-    def __init__(self, U: int, S: int, lmax: int, mirror: str = "host", device="cuda"):
+    def __init__(self, U: int, S: int, lmax: int, mirror: str = "host", device="cuda", policy: str = "ring"):
         abi.load()
         self.U, self.S, self.lmax, self.mirror_kind = U, S, lmax, mirror
+        self.policy = {"ring": abi.POLICY_RING, "clock": abi.POLICY_CLOCK}[policy]
         dev = torch.device(device)
         self.device = dev
         self.keys = torch.zeros((U, lmax, abi.IDX_DIM), dtype=torch.int16, device=dev)
@@ -35,6 +36,7 @@ class UnitSet:
         self.pin_epoch = torch.full((U, S), -1, dtype=torch.int32, device=dev)
         self.ring = torch.zeros((U, abi.RING_ROWS, abi.ROW_BYTES), dtype=torch.uint8, device=dev)
         self.state = torch.zeros((U, abi.ST_WORDS), dtype=torch.int64, device=dev)
+        self.ref = torch.zeros((U, S), dtype=torch.uint8, device=dev)
         nbytes = U * lmax * abi.ROW_BYTES
         self._host_ptr = None
         if mirror == "host":
@@ -56,7 +58,8 @@ class UnitSet:
                 self.keys[u].data_ptr(), self.slots[u].data_ptr(), self.slot_pos[u].data_ptr(),
                 self.pos_slot[u].data_ptr(), self.fill_round[u].data_ptr(),
                 self.pin_epoch[u].data_ptr(), self.ring[u].data_ptr(),
-                self._mirror_dev + u * lmax * abi.ROW_BYTES, self.state[u].data_ptr(), S, 0, lmax)
+                self._mirror_dev + u * lmax * abi.ROW_BYTES, self.state[u].data_ptr(), S, self.policy, lmax,
+                self.ref[u].data_ptr())
         raw = np.frombuffer(bytes(arr), dtype=np.uint8).copy()
         self.units = torch.from_numpy(raw).to(dev)
         self.dev_err = torch.zeros(1, dtype=torch.int32, device=dev)
@@ -87,7 +90,7 @@ class UnitSet:
         self._l0 = l0t
         abi.hc_init(self.units, self.U, warm, l0t, self.S, self.lmax, self.dev_err, stream)
 
-    STATE_FIELDS = ("keys", "slots", "slot_pos", "pos_slot", "fill_round", "pin_epoch", "ring", "state")
+    STATE_FIELDS = ("keys", "slots", "slot_pos", "pos_slot", "fill_round", "pin_epoch", "ring", "state", "ref")
 
     def export_state(self) -> dict:
         """Host snapshot of every unit's cache state and mirror. Call kv_flush

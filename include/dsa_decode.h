@@ -76,6 +76,9 @@ extern "C" {
 #define DSA_WARM_EMPTY 0
 #define DSA_WARM_LAST_S 1
 
+#define DSA_POLICY_RING 0         /* ring replacement skipping pinned slots      */
+#define DSA_POLICY_CLOCK 1        /* clock with reference bits (needs `ref`)    */
+
 /* state[] word indices of a unit (int64 each) */
 #define DSA_ST_LEN 0              /* logical rows (history length)               */
 #define DSA_ST_RAM 1              /* positions < this are in the RAM mirror       */
@@ -103,7 +106,10 @@ extern "C" {
  *                                HBM (the fully resident variant).
  *   state      i64  [8]          DSA_ST_* words.
  *   slots_n    S (>= 1).
+ *   policy     DSA_POLICY_RING or DSA_POLICY_CLOCK (see hot_gather).
  *   lmax       capacity in positions (history + all appends).
+ *   ref        u8   [S]          reference bits (clock policy; may be NULL
+ *                                for the ring policy).
  * 16-byte alignment is required for keys, slots, ring and mirror: a unit
  * that breaks it is skipped by every kernel and sets DSA_DEVERR_BOUNDS.
  */
@@ -118,13 +124,14 @@ typedef struct dsa_unit {
   uint8_t* mirror;
   int64_t* state;
   int32_t slots_n;
-  int32_t reserved0;
+  int32_t policy;
   int64_t lmax;
+  uint8_t* ref;
 } dsa_unit;
 
 /* ------------------------------------------------------------ housekeeping */
 
-/* ABI version of this header (returns 1). */
+/* ABI version of this header (returns 2). */
 int dsa_abi_version(void);
 
 /* Static text for a DSA_* status code. */
@@ -167,7 +174,8 @@ int dsa_host_free(void* host_ptr);
  *   l0       device int64 [U]; 0 <= l0[u] <= lmax.
  *   warm     DSA_WARM_EMPTY: every slot empty. DSA_WARM_LAST_S: slot i holds
  *            position l0 - n + i for n = min(S, l0), fill_round -1, and its
- *            bytes are copied from the mirror.
+ *            bytes are copied from the mirror. Reference bits (when `ref` is
+ *            set) start set for the occupied slots and clear for the others.
  *   max_slots, max_lmax  host bounds: max over units of S and of lmax
  *            (they size the grid).
  * Also clears pin_epoch and the DSA_ST_* words. A unit whose l0 is outside
@@ -281,6 +289,16 @@ int dsa_reuse_selection(int32_t* topk_idx, const int32_t* src_topk, int32_t U, i
  *             exactly as read from their source (PAD entries are zeroed).
  *   counters  device int32 [U][4]: HOT, RING, RAM entries, slots filled.
  *   ws        device workspace of hot_gather_workspace(U, R, K) bytes.
+ * With DSA_POLICY_CLOCK (the policy the pages replaced; [P3] section "GPU 管缓存
+ * 也会犯错": with a full window, every reference bit set and 1% misses, the few
+ * missing blocks swept far), each slot has a reference bit: a HOT hit sets
+ * it; the victims are found by the clock hand's walk from `hand`, which
+ * passes over pinned slots, slots filled in this round and slots already
+ * taken, clears a set bit and passes on, and takes a slot whose bit is
+ * clear; after two turns it stops. A fill sets the bit; hand = last victim +
+ * 1. (Computed with two block scans over the cyclic order, not a serial walk:
+ * the eligible slots with a clear bit come first, then those with a set
+ * bit; the bits the first turn passes are cleared.)
  * Shapes: 1 <= U, 1 <= R <= 8, 1 <= K <= 4096. `round` must not decrease
  * from call to call on a unit (a repeated round is allowed): a call whose
  * round is below the unit's previous one would break the visibility rule, so

@@ -27,10 +27,10 @@ class OracleUnit:
     keys: np.ndarray          # bf16 bits [lmax, 64]; rows >= length are unused
 
     @classmethod
-    def create(cls, S, lmax, L0, keys_initial, mirror_initial, warm):
+    def create(cls, S, lmax, L0, keys_initial, mirror_initial, warm, policy="ring"):
         keys = np.zeros((lmax, keys_initial.shape[1]), dtype=np.uint16)
         keys[:L0] = keys_initial[:L0]
-        return cls(UnitCache(S, lmax, L0, mirror_initial, warm), keys)
+        return cls(UnitCache(S, lmax, L0, mirror_initial, warm, policy=policy), keys)
 
 
 def decode_step(unit: OracleUnit, rnd: int, K: int, scale: float, q_idx, w,

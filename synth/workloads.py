@@ -75,6 +75,7 @@ class Workload:
     phases: tuple = field(default=())  # tagged: ((steps, bias in 1/16 units), ...)
     reuse_every: int = 1   # layer l reuses the selection of layer l - l % reuse_every (1: none)
     seed: int = 0
+    policy: str = "ring"   # hot-cache replacement: 'ring' or 'clock' (reference bits)
 
     @property
     def U(self) -> int:

@@ -27,7 +27,7 @@ class Pair:
         self.uidx = list(range(wl.U)) if units is None else list(units)
         self.oidx = self.uidx if oracle_units is None else list(oracle_units)
         U = len(self.uidx)
-        self.g = UnitSet(U, wl.S, wl.lmax, mirror=mirror)
+        self.g = UnitSet(U, wl.S, wl.lmax, mirror=mirror, policy=wl.policy)
         self.o = {}
         hist = np.arange(wl.L0)
         if gpu_gen:
@@ -39,7 +39,8 @@ class Pair:
             for u in self.oidx:
                 keys = W.keys_bits(wl, u, hist)
                 self.o[u] = OracleUnit.create(wl.S, wl.lmax, wl.L0, keys,
-                                              (lambda pos, u=u: W.rows_bytes(wl, u, pos)), wl.warm)
+                                              (lambda pos, u=u: W.rows_bytes(wl, u, pos)), wl.warm,
+                                              policy=wl.policy)
         for i, u in enumerate(self.uidx):
             if gpu_gen:
                 break
@@ -48,7 +49,7 @@ class Pair:
             self.g.set_keys(i, 0, keys)
             self.g.set_mirror_rows(i, 0, rows)
             if u in self.oidx:
-                self.o[u] = OracleUnit.create(wl.S, wl.lmax, wl.L0, keys, rows, wl.warm)
+                self.o[u] = OracleUnit.create(wl.S, wl.lmax, wl.L0, keys, rows, wl.warm, policy=wl.policy)
         self.g.init([wl.L0] * U, abi.WARM_LAST_S if wl.warm == "last_s" else abi.WARM_EMPTY)
         src = [wl.selection_source(u) for u in self.uidx] if wl.reuse_every > 1 else None
         self.p = DecodePath(self.g, wl.R, wl.K, wl.H, wl.A, wl.scale(), selection_source=src)
@@ -114,7 +115,7 @@ class Pair:
         g = self.g
         return dict(slot_pos=g.slot_pos[i].cpu().numpy(), fill_round=g.fill_round[i].cpu().numpy(),
                     pos_slot=g.pos_slot[i].cpu().numpy(), st=g.state[i].cpu().numpy(),
-                    ring=g.ring[i].cpu().numpy())
+                    ring=g.ring[i].cpu().numpy(), ref=g.ref[i].cpu().numpy())
 
 
 def lse_bound(pair, per_q, r, i):
@@ -157,6 +158,8 @@ def check_step(pair: Pair, g, ores, attention=True, rows=True, full_state=True, 
         assert np.array_equal(s["fill_round"], oc.fill_round), f"unit {u}: fill rounds differ"
         assert s["st"][0] == oc.length and s["st"][1] == oc.rows_in_ram, f"unit {u}: len/ram"
         assert s["st"][2] == oc.hand, f"unit {u}: hand differs"
+        if wl.policy == "clock":
+            assert np.array_equal(s["ref"], oc.ref), f"unit {u}: reference bits differ"
         if full_state:
             assert np.array_equal(s["pos_slot"], oc.pos_slot[:wl.lmax]), f"unit {u}: pos_slot"
             assert np.array_equal(s["ring"], oc.ring), f"unit {u}: ring differs"

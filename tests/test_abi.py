@@ -40,7 +40,7 @@ def test_every_declared_symbol_is_exported(lib):
 
 
 def test_housekeeping(lib):
-    assert lib.dsa_abi_version() == 1
+    assert lib.dsa_abi_version() == 2
     assert lib.dsa_check(0) == 0
     assert lib.dsa_check(0x4) == lib.DSA_ERR_DEVICE_CHECK
     assert "workspace" in lib.status_string(lib.DSA_ERR_WS)

@@ -179,6 +179,39 @@ def test_export_restore_round_trip():
     assert fresh.check() == 0
 
 
+CLOCK = [
+    # every warm slot referenced, few misses: long first turns of the hand
+    dict(L0=1500, S=512, R=1, A=1, K=256, H=16, warm="last_s", steps=12),
+    # MTP rows with duplicates and evictions from an empty cache
+    dict(L0=1500, S=64, R=4, A=4, K=128, H=64, warm="last_s", mode="mtp", steps=16),
+    dict(L0=700, S=16, R=1, A=1, K=64, H=16, warm="empty", steps=40),
+    # more misses than eligible slots (the second turn runs out)
+    dict(L0=900, S=8, R=2, A=1, K=48, H=16, warm="last_s", steps=10),
+]
+
+
+@pytest.mark.parametrize("cfg", CLOCK, ids=[f"clock_L{c['L0']}_S{c['S']}_R{c['R']}" for c in CLOCK])
+def test_clock_policy_matches_oracle(cfg):
+    """Clock replacement with reference bits: classification, victims, bits,
+    hand and slot bytes identical to the oracle's walk of the hand."""
+    wl = W.WORKLOADS[0].with_(name="clock", policy="clock", **cfg)
+    run(wl)
+
+
+def test_clock_policy_fused_path():
+    wl = W.WORKLOADS[0].with_(name="clock-fused", policy="clock", L0=1500, S=64, R=4, A=4, K=128, H=64,
+                              warm="last_s", mode="mtp", steps=10)
+    run(wl, side_stream="fused")
+
+
+@pytest.mark.slow
+def test_config3_clock_policy_first_steps():
+    """The cache-stress workload (full window, every slot referenced, 1% of
+    the Top-2048 outside the hot set) under the clock policy."""
+    wl = W.WORKLOADS[3].with_(policy="clock")
+    run(wl, steps=range(6), attention_every=3)
+
+
 def test_decreasing_round_is_refused_on_the_device():
     """A gather whose round is below the unit's previous round would break the
     visibility rule: the unit is left unchanged and DSA_DEVERR_ROUND is set."""
