@@ -484,6 +484,35 @@ def host_link_gbs(torch):
     return gbs
 
 
+def measure_restore(run, n_units):
+    """kv_restore_full on the first n units after the timed steps: their whole
+    history as dense rows, almost all of it read from the mirror over the host
+    link with zero-copy 16-byte loads (the append-prefill restore)."""
+    import torch
+    from decode_attention_dsa_gb300 import abi
+    g = run.units
+    st = g.state[:n_units].cpu().numpy()
+    rows = int(st[:, abi.ST_LEN].max())
+    dst = torch.empty((n_units, rows, abi.ROW_BYTES), dtype=torch.uint8, device="cuda")
+    sub = g.units[:n_units * ctypes.sizeof(abi.DsaUnit)]
+    ms = []
+    for _ in range(3):
+        a, b = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        a.record()
+        abi.kv_restore_full(sub, n_units, dst, rows, g.dev_err)
+        b.record()
+        torch.cuda.synchronize()
+        ms.append(a.elapsed_time(b))
+    nbytes = float(st[:, abi.ST_LEN].sum()) * abi.ROW_BYTES
+    host_b = float(st[:, abi.ST_RAM].sum()) * abi.ROW_BYTES
+    t = min(ms)
+    del dst
+    return {"units": n_units, "rows": int(st[:, abi.ST_LEN].sum()), "bytes": nbytes, "ms": t,
+            "GB/s": nbytes / (t * 1e6), "host_GB/s": host_b / (t * 1e6),
+            "note": "kv_restore_full (append-prefill restore) of the first units' whole history, best of 3; "
+                    "rows below RAM are zero-copy reads of the pinned mirror"}
+
+
 def measure(args, wl, K, Wm, mirror, reps, world, clocks=None, e2e=False, breakdown=True):
     """Time one workload: median of `reps` K-step replays, the per-call
     breakdown, the cache counters and (optionally) e2e. Returns a dict."""
@@ -526,7 +555,7 @@ def measure(args, wl, K, Wm, mirror, reps, world, clocks=None, e2e=False, breakd
     return res
 
 
-def roofline(wl, res, K, Wm, host_gbs, path):
+def roofline(wl, res, K, Wm, host_gbs, path, host_kind="DMA pinned->device copy"):
     """Per-call achieved rates, the dominant call's roofline fraction and the
     step roofline (the slower of HBM bytes, host-link bytes and attention
     FLOPs at their peaks)."""
@@ -566,7 +595,7 @@ def roofline(wl, res, K, Wm, host_gbs, path):
     t_roof = max(hbm_step_b / (hbm_peak * 1e6), ram_b / (host_gbs * 1e6), attn_flops / (tc_peak * 1e9))
     out["step_roofline"] = {"t_roof_ms": t_roof, "frac": t_roof / ms_step, "hbm_bytes": hbm_step_b,
                             "host_bytes": ram_b, "attn_flops": attn_flops, "host_link_gbs": host_gbs,
-                            "host_link_kind": "DMA pinned->device copy", "peak_source": peak_kind}
+                            "host_link_kind": host_kind, "peak_source": peak_kind}
     out["cache"] = {"hot": int(ctr[0]), "ring": int(ctr[1]), "ram": int(ctr[2]), "fills": int(ctr[3]),
                     "miss_frac": float(ctr[2] / max(1, ctr[:3].sum()))}
     return out
@@ -586,6 +615,12 @@ def run_gpu(args, rank: int, world: int):
     res = measure(args, wl, K, Wm, args.mirror, reps, world, clocks=clocks, e2e=not args.no_e2e)
     clk = clocks.stop()
     run = res.pop("run")
+    restore = measure_restore(run, min(4, wl.U)) if args.mirror == "host" else None
+    # the host link's rate as the kernels meet it: the better of the DMA copy
+    # and the zero-copy sequential read of the restore
+    link, link_kind = host_gbs, "DMA pinned->device copy"
+    if restore and restore["host_GB/s"] > link:
+        link, link_kind = restore["host_GB/s"], "zero-copy sequential read (kv_restore_full)"
     value = world * wl.U * K / (res["total_ms"] / 1e3)
     line = {
         "metric": METRIC, "value": value, "unit": "layer-steps/s", "n_gpus": world, "steps": K,
@@ -603,7 +638,8 @@ def run_gpu(args, rank: int, world: int):
         "tok_per_s": value * wl.A / wl.layers,
         "reps_ms_per_step": [t / K for t in res["totals_ms"]],
     }
-    line.update(roofline(wl, res, K, Wm, host_gbs, run.path))
+    line.update(roofline(wl, res, K, Wm, link, run.path, link_kind))
+    line["host_link"] = {"dma_copy_gbs": host_gbs, "restore": restore}
     line["per_call_note"] = (f"mean over a separate replay of {K} steps from the same start with events around "
                              f"each call, calls serial ({res['breakdown_step_ms']:.4f} ms/step there)")
     line["clocks"] = clk
@@ -621,7 +657,7 @@ def run_gpu(args, rank: int, world: int):
         v1 = wl1.U * K / (r1["total_ms"] / 1e3)
         sec = {"workload": wl1.name, "value": v1, "unit": "layer-steps/s", "ms_per_step": r1["total_ms"] / K,
                "tok_per_s": v1 * wl1.A / wl1.layers, "steps": K}
-        rf = roofline(wl1, r1, K, Wm, host_gbs, run1.path)
+        rf = roofline(wl1, r1, K, Wm, link, run1.path, link_kind)
         sec.update({k: rf[k] for k in ("step_roofline", "per_call", "cache")})
         line["secondary"] = sec
         run1.close()

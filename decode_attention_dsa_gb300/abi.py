@@ -19,6 +19,7 @@ DSA_OK = 0
 DSA_ERR_ARG, DSA_ERR_SHAPE, DSA_ERR_WS, DSA_ERR_CUDA, DSA_ERR_DEVICE_CHECK = -1, -2, -3, -4, -6
 DSA_ERR_SCRATCH_LIMIT = -7
 DEVERR_BOUNDS, DEVERR_CAPACITY, DEVERR_QRANGE, DEVERR_TIMEOUT, DEVERR_ROUND = 0x1, 0x2, 0x4, 0x8, 0x10
+DEVERR_STATE = 0x20
 ROW_BYTES, LAT_DIM, ROPE_DIM, IDX_HEADS, IDX_DIM, RING_ROWS = 656, 512, 64, 8, 64, 64
 MAX_K, MAX_ROWS, MAX_ATTN_K, ROUND_AUTO = 4096, 8, 2048, -1
 CLS_HOT, CLS_RING, CLS_RAM, CLS_PAD = 0, 1, 2, 3
@@ -72,6 +73,10 @@ SIGNATURES = {
     "kv_append_writeback": (ctypes.c_int, [_VP, _I32, _I32, _VP, _VP, _VP, _VP]),
     "kv_append_quantize": (ctypes.c_int, [_VP, _I32, _I32, _VP, _VP, _VP, _VP, _VP]),
     "kv_flush": (ctypes.c_int, [_VP, _I32, _VP, _VP]),
+    "dsa_snapshot_bytes": (_SZ, [_I32, _I64]),
+    "dsa_export": (ctypes.c_int, [_VP, _I32, _VP, _SZ, _I32, _I64, _VP, _VP]),
+    "dsa_restore": (ctypes.c_int, [_VP, _I32, _VP, _SZ, _I32, _I64, _VP, _VP]),
+    "kv_restore_full": (ctypes.c_int, [_VP, _I32, _VP, _I64, _VP, _VP]),
 }
 
 _lib = None
@@ -219,3 +224,22 @@ def kv_append_quantize(units, U, A, new_latent, new_rope, new_keys, dev_err, str
 
 def kv_flush(units, U, dev_err, stream=None):
     return _ok("kv_flush", load().kv_flush(_p(units), U, _p(dev_err), _s(stream)))
+
+
+def dsa_snapshot_bytes(S, lmax) -> int:
+    return load().dsa_snapshot_bytes(S, lmax)
+
+
+def dsa_export(units, U, snap, snap_stride, max_slots, max_lmax, dev_err, stream=None):
+    return _ok("dsa_export", load().dsa_export(_p(units), U, _p(snap), snap_stride, max_slots, max_lmax,
+                                               _p(dev_err), _s(stream)))
+
+
+def dsa_restore(units, U, snap, snap_stride, max_slots, max_lmax, dev_err, stream=None):
+    return _ok("dsa_restore", load().dsa_restore(_p(units), U, _p(snap), snap_stride, max_slots, max_lmax,
+                                                 _p(dev_err), _s(stream)))
+
+
+def kv_restore_full(units, U, dst, dst_rows, dev_err, stream=None):
+    return _ok("kv_restore_full", load().kv_restore_full(_p(units), U, _p(dst), dst_rows, _p(dev_err),
+                                                         _s(stream)))

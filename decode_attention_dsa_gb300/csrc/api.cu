@@ -216,7 +216,177 @@ __global__ void k_wait_selftest(long long limit, int complete, int32_t* dev_err)
   if (__syncthreads_or(!ok) && threadIdx.x == 0) dsa_flag(dev_err, DSA_DEVERR_TIMEOUT);
 }
 
+// ---- session snapshot (export / restore) and the full-history restore
+
+// Byte layout of one unit's snapshot (every part 16-byte aligned).
+struct SnapLayout {
+  size_t slot_pos, fill_round, ref, ring, keys, bytes;
+};
+__host__ __device__ inline SnapLayout snap_layout(int32_t S, int64_t lmax) {
+  SnapLayout l;
+  l.slot_pos = 128;                                   // [0, 64) state words, [64, 80) S, policy, lmax
+  l.fill_round = l.slot_pos + dsa_align((size_t)S * 4, 16);
+  l.ref = l.fill_round + dsa_align((size_t)S * 4, 16);
+  l.ring = l.ref + dsa_align((size_t)S, 16);
+  l.keys = l.ring + (size_t)DSA_RING_ROWS * DSA_ROW_BYTES;
+  l.bytes = l.keys + (size_t)lmax * DSA_IDX_DIM * 2;
+  return l;
+}
+
+// 16-byte copy loop over a block's part of [0, n16) chunks (grid x stride).
+__device__ __forceinline__ void copy16(void* dst, const void* src, int64_t n16) {
+  const uint4* s = reinterpret_cast<const uint4*>(src);
+  uint4* d = reinterpret_cast<uint4*>(dst);
+  for (int64_t i = (int64_t)blockIdx.x * blockDim.x + threadIdx.x; i < n16; i += (int64_t)gridDim.x * blockDim.x)
+    d[i] = s[i];
+}
+
+// Export: unit u's state into snap + u * stride. Needs RAM == LEN (flushed).
+__global__ void __launch_bounds__(INIT_THREADS)
+k_export(const dsa_unit* __restrict__ units, uint8_t* __restrict__ snap, size_t stride, int32_t* dev_err) {
+  const dsa_unit& un = units[blockIdx.y];
+  const int64_t len = un.state[DSA_ST_LEN];
+  if (!unit_aligned(un) || un.state[DSA_ST_RAM] != len) {
+    if (blockIdx.x == 0 && threadIdx.x == 0) dsa_flag(dev_err, DSA_DEVERR_STATE);
+    return;
+  }
+  const int S = un.slots_n;
+  const SnapLayout l = snap_layout(S, un.lmax);
+  if (l.bytes > stride) {   // this unit is larger than the host bounds said
+    if (blockIdx.x == 0 && threadIdx.x == 0) dsa_flag(dev_err, DSA_DEVERR_STATE);
+    return;
+  }
+  uint8_t* o = snap + (size_t)blockIdx.y * stride;
+  const int64_t gt = (int64_t)blockIdx.x * blockDim.x + threadIdx.x, gs = (int64_t)gridDim.x * blockDim.x;
+  if (gt < DSA_ST_WORDS) reinterpret_cast<int64_t*>(o)[gt] = un.state[gt];
+  if (gt == 0) {
+    reinterpret_cast<int32_t*>(o + 64)[0] = S;
+    reinterpret_cast<int32_t*>(o + 64)[1] = un.policy;
+    reinterpret_cast<int64_t*>(o + 72)[0] = un.lmax;
+  }
+  for (int64_t i = gt; i < S; i += gs) {
+    reinterpret_cast<int32_t*>(o + l.slot_pos)[i] = un.slot_pos[i];
+    reinterpret_cast<int32_t*>(o + l.fill_round)[i] = un.fill_round[i];
+    o[l.ref + i] = un.ref ? un.ref[i] : 0;
+  }
+  copy16(o + l.ring, un.ring, (int64_t)DSA_RING_ROWS * DSA_ROW_BYTES / 16);
+  copy16(o + l.keys, un.keys, len * DSA_IDX_DIM * 2 / 16);
+}
+
+// Restore, part 1: state words, slot arrays, ring, keys; pos_slot cleared.
+__global__ void __launch_bounds__(INIT_THREADS)
+k_restore_a(const dsa_unit* __restrict__ units, const uint8_t* __restrict__ snap, size_t stride, int32_t* dev_err) {
+  const dsa_unit& un = units[blockIdx.y];
+  const uint8_t* o = snap + (size_t)blockIdx.y * stride;
+  const int64_t* st = reinterpret_cast<const int64_t*>(o);
+  const int S = reinterpret_cast<const int32_t*>(o + 64)[0];
+  const int64_t slmax = reinterpret_cast<const int64_t*>(o + 72)[0];
+  const int64_t len = st[DSA_ST_LEN];
+  if (!unit_aligned(un) || S != un.slots_n || len < 0 || len > un.lmax || len > slmax || st[DSA_ST_RAM] != len ||
+      snap_layout(S, slmax).bytes > stride) {
+    if (blockIdx.x == 0 && threadIdx.x == 0) dsa_flag(dev_err, DSA_DEVERR_STATE);
+    return;
+  }
+  const SnapLayout l = snap_layout(S, slmax);
+  const int64_t gt = (int64_t)blockIdx.x * blockDim.x + threadIdx.x, gs = (int64_t)gridDim.x * blockDim.x;
+  if (gt < DSA_ST_WORDS) un.state[gt] = st[gt];
+  for (int64_t i = gt; i < S; i += gs) {
+    un.slot_pos[i] = reinterpret_cast<const int32_t*>(o + l.slot_pos)[i];
+    un.fill_round[i] = reinterpret_cast<const int32_t*>(o + l.fill_round)[i];
+    un.pin_epoch[i] = -1;
+    if (un.ref) un.ref[i] = o[l.ref + i];
+  }
+  for (int64_t i = gt; i < un.lmax; i += gs) un.pos_slot[i] = -1;
+  copy16(un.ring, o + l.ring, (int64_t)DSA_RING_ROWS * DSA_ROW_BYTES / 16);
+  copy16(un.keys, o + l.keys, len * DSA_IDX_DIM * 2 / 16);
+}
+
+// Restore, part 2: the position -> slot index and the slot bytes (one warp
+// per slot, from the mirror, which holds every row of the flushed history).
+__global__ void __launch_bounds__(INIT_THREADS)
+k_restore_b(const dsa_unit* __restrict__ units, const uint8_t* __restrict__ snap, size_t stride) {
+  const dsa_unit& un = units[blockIdx.y];
+  const uint8_t* o = snap + (size_t)blockIdx.y * stride;
+  const int64_t len = reinterpret_cast<const int64_t*>(o)[DSA_ST_LEN];
+  const int S = reinterpret_cast<const int32_t*>(o + 64)[0];
+  const int64_t slmax = reinterpret_cast<const int64_t*>(o + 72)[0];
+  if (!unit_aligned(un) || S != un.slots_n || len < 0 || len > un.lmax || len > slmax ||
+      reinterpret_cast<const int64_t*>(o)[DSA_ST_RAM] != len || snap_layout(S, slmax).bytes > stride)
+    return;
+  const int lane = threadIdx.x & 31;
+  for (int64_t i = ((int64_t)blockIdx.x * blockDim.x + threadIdx.x) >> 5; i < S;
+       i += ((int64_t)gridDim.x * blockDim.x) >> 5) {
+    const int32_t p = un.slot_pos[i];
+    if (p < 0 || p >= len) continue;
+    if (lane == 0) un.pos_slot[p] = (int32_t)i;
+    warp_copy_row(un.slots + i * DSA_ROW_BYTES, un.mirror + (int64_t)p * DSA_ROW_BYTES, lane);
+  }
+}
+
+// The full history of each unit as dense rows: [0, RAM) from the mirror,
+// [RAM, LEN) from the ring. Each warp copies whole rows.
+__global__ void __launch_bounds__(INIT_THREADS)
+k_restore_full(const dsa_unit* __restrict__ units, uint8_t* __restrict__ dst, int64_t dst_rows) {
+  const dsa_unit& un = units[blockIdx.y];
+  if (!unit_aligned(un)) return;
+  const int64_t len = min(un.state[DSA_ST_LEN], dst_rows);
+  const int64_t ram = un.state[DSA_ST_RAM];
+  uint8_t* d = dst + (size_t)blockIdx.y * dst_rows * DSA_ROW_BYTES;
+  const int lane = threadIdx.x & 31;
+  for (int64_t p = ((int64_t)blockIdx.x * blockDim.x + threadIdx.x) >> 5; p < len;
+       p += ((int64_t)gridDim.x * blockDim.x) >> 5) {
+    const uint8_t* src = p < ram ? un.mirror + p * DSA_ROW_BYTES : un.ring + (p & (DSA_RING_ROWS - 1)) * DSA_ROW_BYTES;
+    warp_copy_row(d + p * DSA_ROW_BYTES, src, lane);
+  }
+}
+
 }  // namespace
+
+extern "C" size_t dsa_snapshot_bytes(int32_t S, int64_t lmax) {
+  if (S < 1 || lmax < 0) return 0;
+  return snap_layout(S, lmax).bytes;
+}
+
+static int grid_for(int64_t items, int per_block) {
+  const int64_t b = (items + per_block - 1) / per_block;
+  return (int)std::min<int64_t>(std::max<int64_t>(b, 1), 4096);
+}
+
+extern "C" int dsa_export(const dsa_unit* units, int32_t U, uint8_t* snap, size_t snap_stride, int32_t max_slots,
+                          int64_t max_lmax, int32_t* dev_err, void* stream) {
+  if (!units || !snap || U < 1 || U > 65535 || max_slots < 1 || max_lmax < 0) return DSA_ERR_ARG;
+  if (snap_stride < dsa_snapshot_bytes(max_slots, max_lmax) || (snap_stride & 15u) ||
+      (reinterpret_cast<uintptr_t>(snap) & 15u))
+    return DSA_ERR_ARG;
+  const int64_t n16 = std::max<int64_t>(max_lmax * DSA_IDX_DIM * 2 / 16, max_slots);
+  k_export<<<dim3(grid_for(n16, INIT_THREADS), U), INIT_THREADS, 0, static_cast<cudaStream_t>(stream)>>>(
+      units, snap, snap_stride, dev_err);
+  return dsa_launch_status();
+}
+
+extern "C" int dsa_restore(const dsa_unit* units, int32_t U, const uint8_t* snap, size_t snap_stride,
+                           int32_t max_slots, int64_t max_lmax, int32_t* dev_err, void* stream) {
+  if (!units || !snap || U < 1 || U > 65535 || max_slots < 1 || max_lmax < 0) return DSA_ERR_ARG;
+  if (snap_stride < dsa_snapshot_bytes(max_slots, max_lmax) || (snap_stride & 15u) ||
+      (reinterpret_cast<uintptr_t>(snap) & 15u))
+    return DSA_ERR_ARG;
+  cudaStream_t st = static_cast<cudaStream_t>(stream);
+  const int64_t n = std::max<int64_t>(max_lmax * DSA_IDX_DIM * 2 / 16, std::max<int64_t>(max_lmax, max_slots));
+  k_restore_a<<<dim3(grid_for(n, INIT_THREADS), U), INIT_THREADS, 0, st>>>(units, snap, snap_stride, dev_err);
+  if (dsa_launch_status() != DSA_OK) return DSA_ERR_CUDA;
+  k_restore_b<<<dim3(grid_for(max_slots, INIT_THREADS / 32), U), INIT_THREADS, 0, st>>>(units, snap, snap_stride);
+  return dsa_launch_status();
+}
+
+extern "C" int kv_restore_full(const dsa_unit* units, int32_t U, uint8_t* dst, int64_t dst_rows,
+                               int32_t* dev_err, void* stream) {
+  (void)dev_err;
+  if (!units || !dst || U < 1 || U > 65535 || dst_rows < 1) return DSA_ERR_ARG;
+  if (reinterpret_cast<uintptr_t>(dst) & 15u) return DSA_ERR_ARG;
+  k_restore_full<<<dim3(grid_for(dst_rows, INIT_THREADS / 32), U), INIT_THREADS, 0,
+                   static_cast<cudaStream_t>(stream)>>>(units, dst, dst_rows);
+  return dsa_launch_status();
+}
 
 extern "C" int dsa_wait_selftest(int64_t limit_cycles, int32_t complete, int32_t* dev_err, void* stream) {
   if (!dev_err || limit_cycles < 0) return DSA_ERR_ARG;

@@ -90,27 +90,38 @@ class UnitSet:
         self._l0 = l0t
         abi.hc_init(self.units, self.U, warm, l0t, self.S, self.lmax, self.dev_err, stream)
 
-    STATE_FIELDS = ("keys", "slots", "slot_pos", "pos_slot", "fill_round", "pin_epoch", "ring", "state", "ref")
+    # ----------------------------------------------------------- snapshots
+    def snapshot_stride(self) -> int:
+        return abi.dsa_snapshot_bytes(self.S, self.lmax)
 
-    def export_state(self) -> dict:
-        """Host snapshot of every unit's cache state and mirror. Call kv_flush
-        and let the stream finish first, so that the mirror holds every row
-        (rows_in_ram == len) and the snapshot is complete."""
-        torch.cuda.synchronize(self.device)
-        d = {f: getattr(self, f).cpu().clone() for f in self.STATE_FIELDS}
-        d["mirror"] = (np.array(self.mirror_host) if self.mirror_host is not None
-                       else self.mirror_dev_tensor.cpu().numpy())
-        return d
+    def export_state(self, stream=None) -> dict:
+        """Host snapshot of every unit: dsa_export into pinned, mapped host
+        memory (slot map, bits, ring, keys, state words) plus a copy of the
+        mirror. Call kv_flush first on the same stream; a unit that was not
+        flushed is not exported (DSA_DEVERR_STATE)."""
+        stride = self.snapshot_stride()
+        h, d = abi.dsa_host_alloc(self.U * stride)
+        try:
+            abi.dsa_export(self.units, self.U, d, stride, self.S, self.lmax, self.dev_err, stream)
+            torch.cuda.synchronize(self.device)
+            buf = (ctypes.c_uint8 * (self.U * stride)).from_address(h)
+            snap = np.array(np.ctypeslib.as_array(buf))
+        finally:
+            abi.dsa_host_free(h)
+        mirror = (np.array(self.mirror_host) if self.mirror_host is not None
+                  else self.mirror_dev_tensor.cpu().numpy())
+        return {"snapshot": snap, "stride": stride, "mirror": mirror}
 
-    def import_state(self, d: dict) -> None:
-        """Restore a snapshot taken by export_state into a unit set of the same
-        shape (plain copies; the unit descriptors stay this set's own)."""
-        for f in self.STATE_FIELDS:
-            getattr(self, f).copy_(d[f].to(self.device))
+    def import_state(self, d: dict, stream=None) -> None:
+        """Restore a snapshot from export_state into a unit set of the same
+        shape: the mirror rows are put back, then dsa_restore rebuilds the
+        cache state (and re-reads every slot's bytes from the mirror)."""
         if self.mirror_host is not None:
             self.mirror_host[...] = d["mirror"]
         else:
             self.mirror_dev_tensor.copy_(torch.from_numpy(d["mirror"]).to(self.device))
+        snap = torch.from_numpy(d["snapshot"]).to(self.device)
+        abi.dsa_restore(self.units, self.U, snap, d["stride"], self.S, self.lmax, self.dev_err, stream)
         torch.cuda.synchronize(self.device)
 
     def check(self) -> int:

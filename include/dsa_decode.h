@@ -56,6 +56,7 @@ extern "C" {
 #define DSA_DEVERR_QRANGE 0x4     /* attention operand outside the fp16 range    */
 #define DSA_DEVERR_TIMEOUT 0x8    /* a bounded wait inside a kernel gave up        */
 #define DSA_DEVERR_ROUND 0x10     /* hot_gather round below the unit's last round */
+#define DSA_DEVERR_STATE 0x20     /* export/restore of a unit not flushed / not matching */
 
 #define DSA_ROW_BYTES 656         /* Q8G64 MLA row: 512 int8 + 8 fp16 + 64 bf16   */
 #define DSA_LAT_DIM 512
@@ -426,6 +427,51 @@ int kv_append_quantize(const dsa_unit* units, int32_t U, int32_t A, const uint16
  * RAM = LEN. After the stream completes, the mirror holds every row.
  */
 int kv_flush(const dsa_unit* units, int32_t U, int32_t* dev_err, void* stream);
+
+/* ------------------------------------------------- session export and restore */
+
+/*
+ * [P3] section "容量优化必须通过会话生命周期" (capacity work must survive the
+ * session lifecycle): a session is saved and restored, and before exporting
+ * or restoring the full history the log is flushed, the write-back waited
+ * for, and the RAM row count checked against the logical row count.
+ *
+ * A unit's snapshot holds its DSA_ST_* words, slot map (slot_pos,
+ * fill_round), reference bits, recent ring and indexer keys [0, LEN); the
+ * RAM mirror is the caller's own host memory and is not copied. Its size is
+ * dsa_snapshot_bytes(S, lmax); unit u's snapshot is at snap + u * snap_stride
+ * (snap_stride >= the size for the largest S and lmax, a multiple of 16;
+ * snap 16-byte aligned; device memory or a mapped host alias from
+ * dsa_host_alloc).
+ *
+ * dsa_export: call after kv_flush on the same stream. A unit whose RAM row
+ * count is not its logical row count (not flushed) is not exported and sets
+ * DSA_DEVERR_STATE.
+ * dsa_restore: into units with the same S and lmax >= LEN whose mirrors hold
+ * the exported history rows [0, LEN). Restores the words, slot map, bits,
+ * ring and keys, rebuilds pos_slot, clears the pins and re-reads every slot's
+ * bytes from the mirror. A unit whose S differs, whose lmax is too small or
+ * whose snapshot was not flushed is left as it is and sets DSA_DEVERR_STATE.
+ * max_slots, max_lmax: host bounds over the units (they size the grids).
+ */
+size_t dsa_snapshot_bytes(int32_t S, int64_t lmax);
+int dsa_export(const dsa_unit* units, int32_t U, uint8_t* snap, size_t snap_stride, int32_t max_slots,
+               int64_t max_lmax, int32_t* dev_err, void* stream);
+int dsa_restore(const dsa_unit* units, int32_t U, const uint8_t* snap, size_t snap_stride, int32_t max_slots,
+                int64_t max_lmax, int32_t* dev_err, void* stream);
+
+/*
+ * [P3] section "容量优化必须通过会话生命周期": a large append (prefill of many
+ * new rows) first restores the full history of GPU MLA KV from RAM, appends,
+ * and decode then returns to the hot cache.
+ *
+ * Copies each unit's history [0, LEN) as dense 656-byte rows into
+ * dst + u * dst_rows * 656: rows below RAM from the mirror (over the host
+ * link), the rest from the recent ring. Rows at or past dst_rows are not
+ * copied. dst: device memory, 16-byte aligned, U * dst_rows * 656 bytes.
+ */
+int kv_restore_full(const dsa_unit* units, int32_t U, uint8_t* dst, int64_t dst_rows, int32_t* dev_err,
+                    void* stream);
 
 #ifdef __cplusplus
 }

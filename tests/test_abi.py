@@ -79,6 +79,13 @@ def test_host_side_validation(lib):
     assert L.kv_flush(None, 1, None, None) == lib.DSA_ERR_ARG
     assert L.hc_init(fake, 1, 7, fake, 4, 10, None, None) == lib.DSA_ERR_ARG
     assert L.dsa_wait_selftest(100, 0, None, None) == lib.DSA_ERR_ARG
+    sb = lib.dsa_snapshot_bytes(64, 1000)
+    assert sb % 16 == 0 and sb > 1000 * 128 and lib.dsa_snapshot_bytes(0, 10) == 0
+    assert L.dsa_export(fake, 1, fake, sb - 16, 64, 1000, None, None) == lib.DSA_ERR_ARG     # stride too small
+    assert L.dsa_export(fake, 1, fake + 8, sb, 64, 1000, None, None) == lib.DSA_ERR_ARG      # misaligned
+    assert L.dsa_restore(None, 1, fake, sb, 64, 1000, None, None) == lib.DSA_ERR_ARG
+    assert L.kv_restore_full(fake, 1, fake + 4, 100, None, None) == lib.DSA_ERR_ARG
+    assert L.kv_restore_full(fake, 1, fake, 0, None, None) == lib.DSA_ERR_ARG
     assert L.dsa_wait_selftest(-1, 0, fake, None) == lib.DSA_ERR_ARG
     # attention: K beyond 2048 or H off the 16-grid are refused before any launch
     for K in (0, 2049, 4096):

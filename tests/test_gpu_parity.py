@@ -166,7 +166,7 @@ def test_export_restore_round_trip():
     pair.abi.kv_flush(pair.g.units, pair.g.U, pair.g.dev_err)
     pair.o[0].cache.flush()
     snap = pair.g.export_state()
-    st0 = snap["state"][0].numpy()
+    st0 = snap["snapshot"][:64].view(np.int64)
     assert st0[0] == st0[1] == pair.o[0].cache.length, "flush must bring RAM rows to the logical rows"
     fresh = UnitSet(pair.g.U, wl.S, wl.lmax, mirror="host")
     fresh.import_state(snap)
@@ -246,6 +246,71 @@ def test_bounded_wait_gives_up_with_an_error_status():
     abi.dsa_wait_selftest(1 << 16, True, err)
     torch.cuda.synchronize()
     assert int(err.item()) == 0
+
+
+@pytest.mark.parametrize("policy", ["ring", "clock"])
+def test_snapshot_restore_is_bit_exact(policy):
+    """dsa_export after kv_flush, dsa_restore into a fresh unit set whose
+    mirror holds the same rows: every array of the cache state comes back
+    bit for bit, and slot bytes are re-read from the mirror."""
+    from decode_attention_dsa_gb300.units import UnitSet
+    wl = W.WORKLOADS[0].with_(name="snap", sessions=2, layers=2, L0=1200, S=96, K=64, H=16, steps=70, A=1,
+                              warm="last_s", policy=policy)
+    pair, _ = run(wl, steps=range(37), check_every=12, attention_every=12)
+    g, abi, torch = pair.g, pair.abi, pair.torch
+    before = {f: getattr(g, f).clone() for f in ("slot_pos", "fill_round", "ref", "ring", "state", "keys")}
+    abi.kv_flush(g.units, g.U, g.dev_err)
+    snap = g.export_state()
+    assert g.check() == 0
+    fresh = UnitSet(g.U, wl.S, wl.lmax, mirror="host", policy=policy)
+    fresh.import_state(snap)
+    assert fresh.check() == 0
+    st = g.state.cpu().numpy()
+    for f in ("slot_pos", "fill_round", "ref", "ring"):
+        assert torch.equal(getattr(fresh, f), getattr(g, f)), f
+    assert torch.equal(fresh.state, g.state)
+    assert torch.equal(g.slot_pos, before["slot_pos"]) and torch.equal(g.ring, before["ring"])
+    for u in range(g.U):
+        L = int(st[u, 0])
+        assert st[u, 1] == L
+        assert torch.equal(fresh.keys[u, :L], g.keys[u, :L])
+        assert torch.equal(fresh.pos_slot[u], g.pos_slot[u])
+        occ = g.slot_pos[u] >= 0
+        assert torch.equal(fresh.slots[u][occ], g.slots[u][occ])
+    assert (fresh.pin_epoch == -1).all()
+    fresh.close()
+
+
+def test_export_of_an_unflushed_unit_is_refused():
+    wl = W.WORKLOADS[0].with_(name="noflush", L0=300, S=16, K=32, H=16, steps=5, A=1)
+    pair, _ = run(wl)
+    g, abi, torch = pair.g, pair.abi, pair.torch
+    stride = g.snapshot_stride()
+    snap = torch.zeros(stride, dtype=torch.uint8, device="cuda")
+    abi.dsa_export(g.units, g.U, snap, stride, g.S, g.lmax, g.dev_err)
+    torch.cuda.synchronize()
+    assert g.check() == abi.DEVERR_STATE
+    assert int(snap.sum().item()) == 0
+
+
+def test_full_history_restore_for_append_prefill():
+    """kv_restore_full: the dense history [0, LEN) of every unit, rows below
+    RAM from the mirror and the rest from the ring, equals the oracle's rows."""
+    wl = W.WORKLOADS[0].with_(name="prefill", sessions=3, layers=1, L0=2000, S=64, K=64, H=16, steps=50, A=3)
+    pair, _ = run(wl, steps=range(50), check_every=25, attention_every=25)
+    g, abi, torch = pair.g, pair.abi, pair.torch
+    dst = torch.full((g.U, wl.lmax, 656), 0xAB, dtype=torch.uint8, device="cuda")
+    abi.kv_restore_full(g.units, g.U, dst, wl.lmax, g.dev_err)
+    torch.cuda.synchronize()
+    got = dst.cpu().numpy()
+    for u in range(g.U):
+        oc = pair.o[u].cache
+        L = oc.length
+        assert oc.rows_in_ram < L, "the case must leave rows in the ring"
+        want = np.concatenate([oc.mirror.rows(np.arange(oc.rows_in_ram)),
+                               np.stack([oc.ring[p % 64] for p in range(oc.rows_in_ram, L)])])
+        assert np.array_equal(got[u, :L], want), f"unit {u}"
+        assert (got[u, L:] == 0xAB).all()
 
 
 def test_append_beyond_capacity_sets_device_flag():
