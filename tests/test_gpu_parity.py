@@ -339,8 +339,10 @@ def test_config1_full_size_first_steps():
 
 @pytest.mark.slow
 def test_config2_mtp_verify_first_steps():
+    """34 steps of 4 appended rows cross two 64-row write-backs (steps 15 and
+    31) with steps after each."""
     wl = W.WORKLOADS[2]
-    _, worst = run(wl, steps=range(18), attention_every=6)
+    _, worst = run(wl, steps=range(34), attention_every=8)
     assert worst < 1.0
 
 
@@ -350,6 +352,30 @@ def test_config3_cache_stress_first_steps():
     pair, worst = run(wl, steps=range(6), attention_every=3)
     c = pair.p.counters.cpu().numpy()[0]
     assert c[2] / wl.K < 0.05          # phase 1: about 1% of the Top-K misses
+
+
+@pytest.mark.slow
+def test_config3_cache_stress_high_miss_phase():
+    """The second phase of the cache-stress workload (about 30% of the
+    Top-2048 outside the hot set: eviction scans and miss bandwidth), started
+    at step 0 from the full warm cache, compared for 10 steps."""
+    wl = W.WORKLOADS[3].with_(phases=((0, 88), (1024, 36)))
+    pair, worst = run(wl, steps=range(10), attention_every=3)
+    c = pair.p.counters.cpu().numpy()[0]
+    assert 0.15 < c[2] / wl.K < 0.5
+    assert worst < 1.0
+
+
+@pytest.mark.slow
+def test_config4_capacity_batch_other_units_more_steps():
+    """Units 5 (session 2, layer 1) and 22 (session 11, layer 0) of the
+    capacity batch, 9 steps, in the full 32-unit launch."""
+    import torch
+    free, _ = torch.cuda.mem_get_info()
+    if free < 12 * 2**30:
+        pytest.skip("not enough device memory")
+    wl = W.WORKLOADS[4].with_(steps=9)
+    run(wl, steps=range(9), oracle_units=[5, 22], gpu_gen=True, attention_every=4)
 
 
 @pytest.mark.slow
