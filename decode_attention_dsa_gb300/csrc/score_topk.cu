@@ -38,6 +38,8 @@
 //    the whole range): keys above T, and keys equal to T lowest position first.
 #include <algorithm>
 #include <cooperative_groups.h>
+#include <cuda.h>
+#include <cudaTypedefs.h>
 
 #include "common.cuh"
 #include "tc.cuh"
@@ -58,6 +60,7 @@ constexpr int SEL_PER_SRC = SEL_ALL_CAP / SEL_CLUSTER;   // candidates each CTA 
 struct TopkWs {
   uint32_t* hist;   // [U*R][4096]
   uint32_t* keys;   // [U*R][stride]
+  uint8_t* tmaps;   // tensor-map slots of the score kernel's CTAs
   int64_t stride;
 };
 
@@ -69,6 +72,7 @@ inline TopkWs topk_ws(void* ws, int32_t U, int32_t R, int64_t max_len) {
   size_t hb = dsa_align((size_t)U * R * HIST1_BINS * 4, 256);
   w.keys = reinterpret_cast<uint32_t*>(static_cast<char*>(ws) + hb);
   w.stride = key_stride(max_len);
+  w.tmaps = reinterpret_cast<uint8_t*>(w.keys) + dsa_align((size_t)U * R * w.stride * 4, 256);
   return w;
 }
 
@@ -133,14 +137,32 @@ inline void score_config(int R, int* nst, int* per_sm) {
   *per_sm = c;
 }
 
-// 16-byte asynchronous copy global -> shared (L1 bypassed).
-__device__ __forceinline__ void cp_async16(uint32_t dst_smem, const void* src) {
-  asm volatile("cp.async.cg.shared.global [%0], [%1], 16;" ::"r"(dst_smem), "l"(src) : "memory");
+// Per-unit tensor maps. The keys of a unit are a bf16 [L][64] tensor whose
+// 128-position boxes a tiled TMA copy lands in shared memory already in the
+// 128-byte-swizzled K-major layout of the MMA's operand A. The units' key
+// pointers live in device memory, so the maps are made on the device: a
+// template encoded on the host (128 B, passed as a kernel parameter) is
+// copied into a CTA-private slot in the workspace, and tensormap.replace
+// sets the unit's address and row count.
+constexpr int SCORE_TMAP_SLOTS = 8;              // per CTA, reused cyclically by unit
+static_assert(SCORE_TMAP_SLOTS > SCORE_MAX_STAGES, "a map slot outlives the copies in flight");
+constexpr int SCORE_MAX_GRID = 1024;
+constexpr size_t SCORE_TMAP_BYTES = (size_t)SCORE_MAX_GRID * SCORE_TMAP_SLOTS * 128;
+
+__device__ __forceinline__ void tmap_set_unit(uint8_t* slot, const void* keys, int rows) {
+  asm volatile("tensormap.replace.tile.global_address.global.b1024.b64 [%0], %1;" ::"l"(slot), "l"(keys) : "memory");
+  asm volatile("tensormap.replace.tile.global_dim.global.b1024.b32 [%0], 1, %1;" ::"l"(slot), "r"(rows) : "memory");
+  asm volatile("fence.proxy.tensormap::generic.release.gpu;" ::: "memory");
+  asm volatile("fence.proxy.tensormap::generic.acquire.gpu [%0], 128;" ::"l"(slot) : "memory");
 }
-// Arrive on `bar` once every cp.async this thread issued so far has landed
-// (the barrier counts one arrival per thread, no pending-count increment).
-__device__ __forceinline__ void cp_async_arrive(uint64_t* bar) {
-  asm volatile("cp.async.mbarrier.arrive.noinc.shared::cta.b64 [%0];" ::"r"(tc::smem_u32(bar)) : "memory");
+
+// One 128 x 64 bf16 box (rows y .. y + 127; rows past the map's row count
+// read as zeros) into shared memory, completion counted on `bar` (16 KB).
+__device__ __forceinline__ void tma_tile(void* dst, const uint8_t* tmap, int y, uint64_t* bar) {
+  asm volatile(
+      "cp.async.bulk.tensor.2d.shared::cluster.global.tile.mbarrier::complete_tx::bytes [%0], [%1, {%2, %3}], [%4];" ::
+          "r"(tc::smem_u32(dst)), "l"(tmap), "r"(0), "r"(y), "r"(tc::smem_u32(bar))
+      : "memory");
 }
 
 // 8 consecutive fp32 TMEM columns of this thread's lane (no wait).
@@ -165,22 +187,22 @@ struct ScoreArgs {
   int R, K;
   int nst;
   uint32_t idesc;
+  uint8_t* tmaps;       // [grid][SCORE_TMAP_SLOTS][128 B]
   int32_t* dev_err;
 };
 
 // Per CTA: a contiguous range of the flattened (unit, tile) space, software
 // pipelined over its valid tiles j = 0, 1, ...:
-//   copies   every thread issues 16-byte cp.async for tile j + NST - 1 straight
-//            into the 128-byte-swizzled K-major layout (row p, chunk c at
-//            p*128 + ((c ^ (p & 7)) << 4)), then arrives on the stage's
-//            barrier; a warp's 32 copies cover 512 contiguous bytes;
+//   copies   thread 0 issues one tiled TMA copy for tile j + NST - 1 (the
+//            keys land swizzled, ready for the MMA) as soon as the MMA that
+//            read that stage completes;
 //   MMA      thread 0 waits for tile j's stage, issues its four MMAs into
 //            accumulator j & 1 and commits them to MMA barrier j & 1;
 //   epilogue meanwhile every thread finishes tile j - 1 from the other
 //            accumulator (its stage is then free for the next copy).
 // The query rows sit in operand B buffer (unit change count & 1), so a unit
 // change never overwrites a B that an MMA in flight may read.
-__global__ void __launch_bounds__(SCORE_THREADS) k_dsa_score(ScoreArgs a) {
+__global__ void __launch_bounds__(SCORE_THREADS) k_dsa_score(const __grid_constant__ CUtensorMap tmpl, ScoreArgs a) {
   extern __shared__ __align__(1024) uint8_t sm_raw[];
   // the swizzled operand layouts need a 1024-byte aligned base
   uint8_t* sm = sm_raw + ((1024u - (tc::smem_u32(sm_raw) & 1023u)) & 1023u);
@@ -211,8 +233,9 @@ __global__ void __launch_bounds__(SCORE_THREADS) k_dsa_score(ScoreArgs a) {
   __shared__ int s_len[UCACHE];
   __shared__ const uint16_t* s_keys[UCACHE];
   for (int i = tid; i < R * HIST1_BINS; i += SCORE_THREADS) hs[i] = 0;
+  uint8_t* my_tmaps = a.tmaps + (size_t)blockIdx.x * SCORE_TMAP_SLOTS * 128;
   if (tid == 0) {
-    for (int s = 0; s < NST; ++s) tc::mbar_init(&full[s], SCORE_THREADS);
+    for (int s = 0; s < NST; ++s) tc::mbar_init(&full[s], 1);
     tc::mbar_init(&mma_bar[0], 1);
     tc::mbar_init(&mma_bar[1], 1);
     *s_fail = 0;
@@ -224,6 +247,9 @@ __global__ void __launch_bounds__(SCORE_THREADS) k_dsa_score(ScoreArgs a) {
   tc::fence_after_sync();
   const uint32_t tmem = *s_tmem;
   pdl_wait();
+  // every slot starts as a copy of the template (8 x 16 B each)
+  for (int i = tid; i < SCORE_TMAP_SLOTS * 8; i += SCORE_THREADS)
+    reinterpret_cast<uint4*>(my_tmaps)[i] = reinterpret_cast<const uint4*>(&tmpl)[i & 7];
   if (tid < UCACHE) {
     const int u = u0 + tid;
     s_ntv[tid] = 0;
@@ -272,20 +298,22 @@ __global__ void __launch_bounds__(SCORE_THREADS) k_dsa_score(ScoreArgs a) {
     }
     return ntiles;
   };
-  // every thread: its 8 chunks of tile k into `stage`, then one arrival
-  auto copy_tile = [&](int k, int stage) {
+  // thread 0: tile k into `stage` by one TMA copy. A unit's map is made when
+  // its first tile is issued, in the next slot in turn: every unit issued has
+  // at least one tile, so a slot is rewritten only SCORE_TMAP_SLOTS units (and
+  // as many tiles, more than the NST copies in flight) after its last use.
+  int tmap_u = -1, tmap_n = -1;
+  auto issue = [&](int k, int stage) {
     int u, t;
     tile_of(k, u, t);
-    const int n = min(SCORE_TILE, unit_len(u) - t * SCORE_TILE);
-    const uint8_t* src = reinterpret_cast<const uint8_t*>(unit_keys(u) + (size_t)t * SCORE_TILE * 64);
-    const uint32_t dst = tc::smem_u32(sm + stage * SCORE_STAGE);
-#pragma unroll
-    for (int i = 0; i < 8; ++i) {
-      const int lin = i * SCORE_THREADS + tid;           // 16-byte chunk of the tile
-      const int row = lin >> 3, c = lin & 7;
-      if (row < n) cp_async16(dst + row * 128 + ((c ^ (row & 7)) << 4), src + (size_t)lin * 16);
+    if (u != tmap_u) {
+      tmap_u = u;
+      ++tmap_n;
+      tmap_set_unit(my_tmaps + (size_t)(tmap_n & (SCORE_TMAP_SLOTS - 1)) * 128, unit_keys(u), unit_len(u));
     }
-    cp_async_arrive(&full[stage]);
+    tc::mbar_arrive_expect_tx(&full[stage], (uint32_t)SCORE_STAGE);
+    tma_tile(sm + stage * SCORE_STAGE, my_tmaps + (size_t)(tmap_n & (SCORE_TMAP_SLOTS - 1)) * 128, t * SCORE_TILE,
+             &full[stage]);
   };
   auto flush_hist = [&](int u) {
     uint32_t* gh = a.hist + (size_t)u * R * HIST1_BINS;
@@ -298,15 +326,18 @@ __global__ void __launch_bounds__(SCORE_THREADS) k_dsa_score(ScoreArgs a) {
     }
   };
 
-  // prologue: the first NST valid tiles
+  // prologue: the first NST valid tiles (thread 0 tracks the copies)
   int k_iss = -1;      // last tile whose copy was issued
   long long issued = 0;
-  for (int s = 0; s < NST; ++s) {
-    const int kn = next_valid(k_iss + 1);
-    k_iss = kn;
-    if (kn >= ntiles) break;
-    copy_tile(kn, s);
-    ++issued;
+  __syncthreads();     // the map slots hold the template
+  if (tid == 0) {
+    for (int s = 0; s < NST; ++s) {
+      const int kn = next_valid(k_iss + 1);
+      k_iss = kn;
+      if (kn >= ntiles) break;
+      issue(kn, s);
+      ++issued;
+    }
   }
 
   int k = next_valid(0);          // tile of this iteration (its MMA)
@@ -345,7 +376,6 @@ __global__ void __launch_bounds__(SCORE_THREADS) k_dsa_score(ScoreArgs a) {
         // tile j's keys have landed: issue its MMAs into accumulator j & 1
         if (tc::mbar_wait(&full[stage], (uint32_t)((j / NST) & 1))) {
           last_mma = j;
-          tc::fence_async_shared();
           tc::fence_after_sync();
           const uint32_t aa = tc::smem_u32(sm + stage * SCORE_STAGE);
           const uint32_t bb = tc::smem_u32(sm + lay.b_off + bsel * lay.b_bytes);
@@ -375,12 +405,15 @@ __global__ void __launch_bounds__(SCORE_THREADS) k_dsa_score(ScoreArgs a) {
       ok = __all_sync(0xffffffffu, ok);
       tc::fence_after_sync();
       if (ok) {
-        const int kn = k_iss < ntiles ? next_valid(k_iss + 1) : ntiles;
-        k_iss = kn;
-        if (kn < ntiles) {
-          copy_tile(kn, pstage);
-          ++issued;
+        if (tid == 0) {
+          const int kn = k_iss < ntiles ? next_valid(k_iss + 1) : ntiles;
+          k_iss = kn;
+          if (kn < ntiles) {
+            issue(kn, pstage);
+            ++issued;
+          }
         }
+        __syncwarp();   // warp 0 converges before the warp-wide TMEM loads
         const float* sw = sw0 + pbsel * R * 8;
         const int p = tid;
         for (int r = 0; r < R; ++r) {
@@ -863,12 +896,38 @@ inline size_t select_smem() { return SEL_SMEM; }
 
 DsaPerDevice g_setup;   // kernel attributes and SM count, per device
 
+// The tensor-map template of the score kernel, per device: bf16 [rows][64],
+// 128-byte rows, 64 x 128 boxes, 128-byte swizzle. It is encoded over a
+// small array of this library (the kernels always replace the address and
+// the row count before a copy).
+static __device__ __align__(256) uint8_t g_tmap_dummy[SCORE_STAGE];
+CUtensorMap g_tmpl[DSA_MAX_DEVICES];
+
+int encode_template(int dev) {
+  void* fn = nullptr;
+  cudaDriverEntryPointQueryResult q;
+  if (cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &fn, 12000, cudaEnableDefault, &q) != cudaSuccess ||
+      q != cudaDriverEntryPointSuccess || !fn)
+    return DSA_ERR_CUDA;
+  void* base = nullptr;
+  if (cudaGetSymbolAddress(&base, g_tmap_dummy) != cudaSuccess) return DSA_ERR_CUDA;
+  const cuuint64_t dims[2] = {64, SCORE_TILE};
+  const cuuint64_t strides[1] = {128};
+  const cuuint32_t box[2] = {64, SCORE_TILE};
+  const cuuint32_t estr[2] = {1, 1};
+  const CUresult r = reinterpret_cast<PFN_cuTensorMapEncodeTiled_v12000>(fn)(
+      &g_tmpl[dev], CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, base, dims, strides, box, estr,
+      CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
+      CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+  return r == CUDA_SUCCESS ? DSA_OK : DSA_ERR_CUDA;
+}
+
 }  // namespace
 
 extern "C" size_t dsa_score_topk_workspace(int32_t U, int32_t R, int64_t max_len) {
   if (U < 1 || R < 1 || max_len < 0) return 0;
   return dsa_align((size_t)U * R * HIST1_BINS * 4, 256) +
-         dsa_align((size_t)U * R * key_stride(max_len) * 4, 256);
+         dsa_align((size_t)U * R * key_stride(max_len) * 4, 256) + SCORE_TMAP_BYTES;
 }
 
 extern "C" int dsa_score_topk(const dsa_unit* units, int32_t U, int32_t R, int32_t K,
@@ -885,7 +944,8 @@ extern "C" int dsa_score_topk(const dsa_unit* units, int32_t U, int32_t R, int32
   TopkWs tw = topk_ws(ws, U, R, max_len);
   if (reinterpret_cast<uintptr_t>(q) & 15u) return DSA_ERR_ARG;   // query rows are read as 16-byte vectors
   int dev = 0;
-  const int ok = dsa_device_setup(g_setup, &dev, [](int) {
+  const int ok = dsa_device_setup(g_setup, &dev, [](int d) {
+    if (encode_template(d) != DSA_OK) return DSA_ERR_CUDA;
     size_t mx = 0;
     for (int r = 1; r <= DSA_MAX_ROWS; ++r) {
       int nst = 2, per_sm = 1;
@@ -918,10 +978,11 @@ extern "C" int dsa_score_topk(const dsa_unit* units, int32_t U, int32_t R, int32
     a.K = K;
     a.nst = nst;
     a.idesc = tc::idesc_bf16_f32(SCORE_TILE, score_npad(R));
+    a.tmaps = tw.tmaps;
     a.dev_err = dev_err;
-    const int64_t grid = std::min<int64_t>(tpu * U, (int64_t)per_sm * num_sms);
+    const int64_t grid = std::min<int64_t>(std::min<int64_t>(tpu * U, (int64_t)per_sm * num_sms), SCORE_MAX_GRID);
     if (launch_pdl(k_dsa_score, dim3((unsigned)grid), dim3(SCORE_THREADS), score_layout(R, nst).bytes + 1024, st,
-                   a) != DSA_OK)
+                   g_tmpl[dev], a) != DSA_OK)
       return DSA_ERR_CUDA;
   }
   return launch_pdl(k_topk_select, dim3(SEL_CLUSTER, U * R), dim3(SEL_THREADS), select_smem(), st, units, R,
@@ -972,7 +1033,7 @@ constexpr int64_t NOALLOC_MAX_UR = 16;          // units x query rows per call
 constexpr int64_t NOALLOC_MAX_LEN = 65536;      // history positions per unit
 constexpr size_t NOALLOC_HIST_BYTES = (size_t)NOALLOC_MAX_UR * HIST1_BINS * 4;   // 256 KiB
 constexpr size_t NOALLOC_BYTES =
-    NOALLOC_HIST_BYTES + (size_t)NOALLOC_MAX_UR * NOALLOC_MAX_LEN * 4;           // 4.25 MiB
+    NOALLOC_HIST_BYTES + (size_t)NOALLOC_MAX_UR * NOALLOC_MAX_LEN * 4 + SCORE_TMAP_BYTES;   // 5.25 MiB
 static __device__ __align__(256) uint8_t g_topk_scratch[NOALLOC_BYTES];
 
 // Device address of g_topk_scratch, per device ordinal (looked up once, under
