@@ -11,15 +11,16 @@ value is layer-steps/s (units x steps / time).
   python bench.py [--gpus N] [--steps K] [--warmup W] [--config C] [--sessions S]
                   [--mirror host|device] [--impl gb300|reference] [--reps R]
 
-Timing: every timed repetition starts from the same state (cache initialised,
-then W >= 3 untimed warm-up steps), then K steps run from one CUDA graph; L2
-is flushed (a 512 MiB write) before every timed step, outside its CUDA-event
-bracket, and the sum of the per-step event times is the repetition's total.
-The value is the median over R repetitions. Clocks are sampled through NVML
-every ~2 ms and only samples inside the timed replays are kept. ``e2e`` runs
-the same K steps through the C ABI with host buffers: each step copies its
-inputs from pinned host memory and the attention output back, inside the
-bracket.
+Timing: the cache is initialised and W >= 3 untimed warm-up steps run; then
+R consecutive K-step segments of the same decode run, each from its own CUDA
+graph, so every timed step selects rows that no earlier step has read; L2 is
+flushed (a 512 MiB write) before every timed step, outside its CUDA-event
+bracket, and the sum of the per-step event times is a segment's total. The
+value is the median over the R segments. Clocks are sampled through NVML
+every ~2 ms and only samples inside the timed segments are kept. Three more
+segments give the per-call breakdown (events around each call, calls serial)
+and three more ``e2e``: each step copies its inputs from pinned host memory
+and the attention output back, inside the bracket, through the C ABI.
 
 Beside the headline the same line carries the 50K single-stream workload
 (``secondary``), and the offload gate (``gate``): the MTP=3 verify workload
@@ -313,10 +314,12 @@ def traffic_for(kernel: str):
 
 
 class WorkloadRun:
-    """One workload on the device: unit set, decode path, inputs for W + K
-    steps (generated on the device), and K-step CUDA graphs."""
+    """One workload on the device: unit set, decode path, inputs for W + n*K
+    steps (generated on the device), and one CUDA graph per K-step segment.
+    The timed segments are consecutive parts of one continuous decode, so
+    every timed step selects rows no earlier step has read."""
 
-    def __init__(self, wl, K, Wm, mirror, fused, use_graph):
+    def __init__(self, wl, K, Wm, nseg, mirror, fused, use_graph):
         import torch
         from decode_attention_dsa_gb300 import abi
         from decode_attention_dsa_gb300.step import DecodePath
@@ -325,13 +328,14 @@ class WorkloadRun:
         self.torch, self.abi = torch, abi
         self.wl, self.K, self.Wm, self.fused, self.use_graph = wl, K, Wm, fused, use_graph
         self.mirror = mirror
-        wlr = wl.with_(steps=Wm + K)
+        self.total = Wm + nseg * K
+        wlr = wl.with_(steps=self.total)
         U = wl.U
         self.units = UnitSet(U, wl.S, wlr.lmax, mirror=mirror, policy=wl.policy)
         src = [wl.selection_source(u) for u in range(U)] if wl.reuse_every > 1 else None
         self.path = DecodePath(self.units, wl.R, wl.K, wl.H, wl.A, wl.scale(), selection_source=src)
         sg.history(wlr, self.units)
-        self.inp = sg.step_inputs(wlr, 0, Wm + K)
+        self.inp = sg.step_inputs(wlr, 0, self.total)
         if self.path.sources:
             # only the source units' indexer queries are scored (set up before timing)
             self.inp["q_idx"] = self.inp["q_idx"][:, self.path.sources].contiguous()
@@ -340,30 +344,36 @@ class WorkloadRun:
         self.side = torch.cuda.Stream()
         self.warm = abi.WARM_LAST_S if wl.warm == "last_s" else abi.WARM_EMPTY
         self.ctr = torch.zeros((U, 4), dtype=torch.int64, device="cuda")
+        self.next_seg = 0
         torch.cuda.synchronize()
 
     def step_args(self, s):
         i = self.inp
         return (i["q_idx"][s], i["w"][s], i["q_lat"][s], i["q_rope"][s], i["new_rows"][s], i["new_keys"][s])
 
-    def reset(self):
-        """Initialise the cache, run the W warm-up steps, wait."""
+    def start(self):
+        """Initialise the cache and run the W warm-up steps."""
         self.units.init([self.wl.L0] * self.wl.U, self.warm)
         for s in range(self.Wm):
             self.path.step(self.abi.ROUND_AUTO, *self.step_args(s))
-        self.ctr.zero_()
         self.torch.cuda.synchronize()
 
-    def _record(self, per_call):
+    def _record(self, s0, per_call, e2e=None):
         torch, path, rnd = self.torch, self.path, self.abi.ROUND_AUTO
         nev = 5 if per_call else 2
         ev = [[torch.cuda.Event(enable_timing=True, external=self.use_graph) for _ in range(nev)]
               for _ in range(self.K)]
         for i in range(self.K):
-            qi, w, ql, qr, nr, nk = self.step_args(self.Wm + i)
+            s = s0 + i
+            qi, w, ql, qr, nr, nk = self.step_args(s)
             self.flush.fill_(i & 0xFF)
             e = ev[i]
             e[0].record()
+            if e2e is not None:
+                host, dev_in, out_host = e2e
+                for n in dev_in:
+                    dev_in[n].copy_(host[n][s], non_blocking=True)
+                qi, w, ql, qr, nr, nk = (dev_in[n] for n in ("q_idx", "w", "q_lat", "q_rope", "new_rows", "new_keys"))
             if per_call:
                 path.score_topk(qi, w)
                 e[1].record()
@@ -376,33 +386,41 @@ class WorkloadRun:
                 path.step(rnd, qi, w, ql, qr, nr, nk, fused=True)
             else:
                 path.step(rnd, qi, w, ql, qr, nr, nk, side=self.side)
+            if e2e is not None:
+                e2e[2][i].copy_(path.out, non_blocking=True)
             e[-1].record()
             if not per_call:
                 self.ctr.add_(path.counters)
         return ev
 
-    def capture(self, per_call=False):
-        """A K-step graph (or, without graphs, a function that launches the steps)."""
+    def segment(self, per_call=False, e2e=None):
+        """The next K-step segment of the decode, captured as a graph (or, with
+        --no-graph, a closure that launches it). Segments must be run in the
+        order they were made."""
+        s0 = self.Wm + self.next_seg * self.K
+        self.next_seg += 1
+        assert s0 + self.K <= self.total
         torch = self.torch
         if not self.use_graph:
-            return None, None
+            return (None, lambda: self._record(s0, per_call, e2e))
         graph = torch.cuda.CUDAGraph()
         cap = torch.cuda.Stream()
         cap.wait_stream(torch.cuda.current_stream())
         with torch.cuda.graph(graph, stream=cap):
-            ev = self._record(per_call)
+            ev = self._record(s0, per_call, e2e)
         torch.cuda.synchronize()
-        return graph, ev
+        return (graph, ev)
 
-    def timed(self, graph, ev, per_call=False, clocks=None):
-        """Reset, replay the K steps once; returns per-step event lists."""
+    def run_segment(self, seg, clocks=None):
+        """Run a segment; returns its per-step events."""
         torch = self.torch
-        self.reset()
+        graph, ev = seg
+        self.ctr.zero_()
         t0 = time.perf_counter()
         if graph is not None:
             graph.replay()
         else:
-            ev = self._record(per_call)
+            ev = ev()
         torch.cuda.synchronize()
         t1 = time.perf_counter()
         if clocks is not None:
@@ -412,52 +430,18 @@ class WorkloadRun:
             raise RuntimeError(f"device error word {err:#x}")
         return ev
 
-    def e2e(self, reps):
-        """The K steps through the C ABI with pinned host buffers: per step the
-        inputs are copied in and the attention output copied out inside the
-        bracket. Returns (ms per K steps per rep, h2d bytes/step, d2h bytes/step)."""
+    def e2e_buffers(self):
+        """Pinned host copies of every step's inputs, device staging buffers
+        and pinned host outputs (the inputs a caller hands over per step)."""
         torch = self.torch
         names = ["q_idx", "w", "q_lat", "q_rope", "new_rows", "new_keys"]
-        K, Wm, path = self.K, self.Wm, self.path
-        host = {n: torch.empty_like(self.inp[n][Wm:], device="cpu").pin_memory() for n in names}
+        host = {n: torch.empty_like(self.inp[n], device="cpu").pin_memory() for n in names}
         for n in names:
-            host[n].copy_(self.inp[n][Wm:])
+            host[n].copy_(self.inp[n])
         dev_in = {n: torch.empty_like(self.inp[n][0]) for n in names}
-        out_host = torch.empty((K,) + tuple(path.out.shape), dtype=torch.float32).pin_memory()
+        out_host = torch.empty((self.K,) + tuple(self.path.out.shape), dtype=torch.float32).pin_memory()
         h2d = sum(host[n][0].numel() * host[n][0].element_size() for n in names)
-        d2h = path.out.numel() * 4
-        ee = [(torch.cuda.Event(enable_timing=True, external=self.use_graph),
-               torch.cuda.Event(enable_timing=True, external=self.use_graph)) for _ in range(K)]
-
-        def steps():
-            for i in range(K):
-                self.flush.fill_(i & 0xFF)
-                ee[i][0].record()
-                for n in names:
-                    dev_in[n].copy_(host[n][i], non_blocking=True)
-                path.step(self.abi.ROUND_AUTO, dev_in["q_idx"], dev_in["w"], dev_in["q_lat"], dev_in["q_rope"],
-                          dev_in["new_rows"], dev_in["new_keys"], side=self.side, fused=self.fused)
-                out_host[i].copy_(path.out, non_blocking=True)
-                ee[i][1].record()
-        graph = None
-        if self.use_graph:
-            graph = torch.cuda.CUDAGraph()
-            cap = torch.cuda.Stream()
-            cap.wait_stream(torch.cuda.current_stream())
-            with torch.cuda.graph(graph, stream=cap):
-                steps()
-            torch.cuda.synchronize()
-        res = []
-        for _ in range(reps):
-            self.reset()
-            if graph is not None:
-                graph.replay()
-            else:
-                steps()
-            torch.cuda.synchronize()
-            res.append(sum(a.elapsed_time(b) for a, b in ee))
-        del graph
-        return res, h2d, d2h
+        return (host, dev_in, out_host), h2d, self.path.out.numel() * 4
 
     def close(self):
         self.units.close()
@@ -513,38 +497,54 @@ def measure_restore(run, n_units):
                     "rows below RAM are zero-copy reads of the pinned mirror"}
 
 
+BREAKDOWN_SEGS = 3
+E2E_SEGS = 3
+
+
 def measure(args, wl, K, Wm, mirror, reps, world, clocks=None, e2e=False, breakdown=True):
-    """Time one workload: median of `reps` K-step replays, the per-call
-    breakdown, the cache counters and (optionally) e2e. Returns a dict."""
+    """Time one workload: `reps` consecutive K-step segments of one decode
+    (median reported), then the per-call breakdown (median over 3 segments
+    with events around each call, calls serial), the cache counters and
+    (optionally) e2e over 3 more segments. Returns a dict."""
     import torch
     use_graph = not args.no_graph
     fused = args.path == "fused"
-    run = WorkloadRun(wl, K, Wm, mirror, fused, use_graph)
+    nseg = reps + (BREAKDOWN_SEGS if breakdown else 0) + (E2E_SEGS if e2e else 0)
+    run = WorkloadRun(wl, K, Wm, nseg, mirror, fused, use_graph)
     path, U = run.path, wl.U
-    graph, ev = run.capture(per_call=False)
-    totals = []
-    ctr = None
-    for r in range(reps):
-        ev = run.timed(graph, ev, clocks=clocks)
+    heads = [run.segment() for _ in range(reps)]
+    bds = [run.segment(per_call=True) for _ in range(BREAKDOWN_SEGS)] if breakdown else []
+    e2e_bufs = None
+    if e2e:
+        e2e_bufs, h2d, d2h = run.e2e_buffers()
+        e2es = [run.segment(e2e=e2e_bufs) for _ in range(E2E_SEGS)]
+    run.start()
+    totals, ctrs = [], []
+    for seg in heads:
+        ev = run.run_segment(seg, clocks=clocks)
         totals.append(sum(e[0].elapsed_time(e[-1]) for e in ev))
-        if ctr is None:
-            ctr = run.ctr.cpu().numpy().sum(axis=0)      # HOT, RING, RAM entries, fills over K steps
-    del graph
+        ctrs.append(run.ctr.cpu().numpy().sum(axis=0))      # HOT, RING, RAM entries, fills over K steps
     total_ms = statistics.median(totals)
     if world > 1:
         t = torch.tensor([total_ms], dtype=torch.float64, device="cuda")
         torch.distributed.all_reduce(t, op=torch.distributed.ReduceOp.MAX)
         total_ms = float(t.item())
-    res = {"run": run, "totals_ms": totals, "total_ms": total_ms, "ctr": ctr,
+    import numpy as np
+    res = {"run": run, "totals_ms": totals, "total_ms": total_ms, "ctr": np.mean(ctrs, axis=0),
            "launches_per_step": path.launches_per_step()}
     if breakdown:
-        gb, evb = run.capture(per_call=True)
-        evb = run.timed(gb, evb, per_call=True)
-        res["call_ms"] = [statistics.mean(e[j].elapsed_time(e[j + 1]) for e in evb) for j in range(4)]
-        res["breakdown_step_ms"] = statistics.mean(e[0].elapsed_time(e[4]) for e in evb)
-        del gb
+        per = []
+        for seg in bds:
+            evb = run.run_segment(seg)
+            per.append([statistics.mean(e[j].elapsed_time(e[j + 1]) for e in evb) for j in range(4)] +
+                       [statistics.mean(e[0].elapsed_time(e[4]) for e in evb)])
+        res["call_ms"] = [statistics.median(p[j] for p in per) for j in range(4)]
+        res["breakdown_step_ms"] = statistics.median(p[4] for p in per)
     if e2e:
-        ms, h2d, d2h = run.e2e(max(1, min(3, reps)))
+        ms = []
+        for seg in e2es:
+            ee = run.run_segment(seg)
+            ms.append(sum(e[0].elapsed_time(e[-1]) for e in ee))
         e2e_ms = statistics.median(ms)
         if world > 1:
             t = torch.tensor([e2e_ms], dtype=torch.float64, device="cuda")
@@ -552,6 +552,9 @@ def measure(args, wl, K, Wm, mirror, reps, world, clocks=None, e2e=False, breakd
             e2e_ms = float(t.item())
         res["e2e"] = {"value": world * U * K / (e2e_ms / 1e3), "unit": "layer-steps/s",
                       "h2d_bytes_per_step": int(h2d), "d2h_bytes_per_step": int(d2h), "ms_per_step": e2e_ms / K}
+    del heads, bds
+    if e2e:
+        del e2es
     return res
 
 
@@ -633,15 +636,16 @@ def run_gpu(args, rank: int, world: int):
             "selection_reuse_every": wl.reuse_every,
             "path": "hot_gather_attn (fused)" if args.path == "fused" else
                     "hot_gather + mla_decode_attn, append concurrent",
-            "timing": f"median of {reps} replays of one {K}-step CUDA graph, each from the same state",
+            "timing": f"median of {reps} consecutive {K}-step segments of one decode (one CUDA graph each) "
+                      f"after {Wm} warm-up steps",
             "parallelism": "replicas" if world > 1 else "single GPU"}),
         "tok_per_s": value * wl.A / wl.layers,
-        "reps_ms_per_step": [t / K for t in res["totals_ms"]],
+        "segments_ms_per_step": [t / K for t in res["totals_ms"]],
     }
     line.update(roofline(wl, res, K, Wm, link, run.path, link_kind))
     line["host_link"] = {"dma_copy_gbs": host_gbs, "restore": restore}
-    line["per_call_note"] = (f"mean over a separate replay of {K} steps from the same start with events around "
-                             f"each call, calls serial ({res['breakdown_step_ms']:.4f} ms/step there)")
+    line["per_call_note"] = (f"median over {BREAKDOWN_SEGS} further {K}-step segments with events around each "
+                             f"call, calls serial ({res['breakdown_step_ms']:.4f} ms/step there)")
     line["clocks"] = clk
     line["gpu_launches"] = res["launches_per_step"] * K
     line["cuda_graph"] = not args.no_graph
@@ -669,28 +673,33 @@ def run_gpu(args, rank: int, world: int):
 
 def offload_gate(args, K, Wm):
     """The MTP=3 verify workload with the mirror in pinned host memory
-    (offloaded) and in HBM (resident), same kernels, interleaved repetitions;
-    the gap is (offloaded - resident) / resident in step time (best of each)."""
+    (offloaded) and in HBM (resident), same kernels; the two decodes run
+    their segments interleaved (host, device, host, ...); the gap is
+    (offloaded - resident) / resident in step time (best segment of each)."""
     import torch
     wl2 = workload(args, 2)
     use_graph = not args.no_graph
-    runs = {m: WorkloadRun(wl2, K, Wm, m, args.path == "fused", use_graph) for m in ("host", "device")}
-    graphs = {m: r.capture(per_call=False) for m, r in runs.items()}
+    nrep = max(3, min(5, args.reps))
+    runs = {m: WorkloadRun(wl2, K, Wm, nrep, m, args.path == "fused", use_graph) for m in ("host", "device")}
+    segs = {m: [r.segment() for _ in range(nrep)] for m, r in runs.items()}
+    for r in runs.values():
+        r.start()
     ms = {"host": [], "device": []}
-    for _ in range(max(3, min(5, args.reps))):
+    for i in range(nrep):
         for m in ("host", "device"):
-            g, ev = graphs[m]
-            ev = runs[m].timed(g, ev)
+            ev = runs[m].run_segment(segs[m][i])
             ms[m].append(sum(e[0].elapsed_time(e[-1]) for e in ev) / K)
+    del segs
     for m in runs:
         runs[m].close()
-    del graphs, runs
+    del runs
     torch.cuda.empty_cache()
     best = {m: min(v) for m, v in ms.items()}
     gap = (best["host"] - best["device"]) / best["device"] * 100.0
     return {"workload": wl2.name, "steps": K, "offloaded_ms_per_step": best["host"],
             "resident_ms_per_step": best["device"], "gap_pct": gap, "within_5pct": gap <= 5.0,
-            "reps_ms_per_step": ms, "note": "best of interleaved repetitions (host, device, host, ...)"}
+            "segments_ms_per_step": ms,
+            "note": "best of interleaved segments of two continuous decodes (host, device, host, ...)"}
 
 
 def main():

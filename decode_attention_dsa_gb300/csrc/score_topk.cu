@@ -193,9 +193,9 @@ struct ScoreArgs {
 
 // Per CTA: a contiguous range of the flattened (unit, tile) space, software
 // pipelined over its valid tiles j = 0, 1, ...:
-//   copies   thread 0 issues one tiled TMA copy for tile j + NST - 1 (the
-//            keys land swizzled, ready for the MMA) as soon as the MMA that
-//            read that stage completes;
+//   copies   lane 0 of warp 1 issues one tiled TMA copy for tile j + NST - 1
+//            (the keys land swizzled, ready for the MMA) as soon as the MMA
+//            that read that stage completes;
 //   MMA      thread 0 waits for tile j's stage, issues its four MMAs into
 //            accumulator j & 1 and commits them to MMA barrier j & 1;
 //   epilogue meanwhile every thread finishes tile j - 1 from the other
@@ -326,11 +326,14 @@ __global__ void __launch_bounds__(SCORE_THREADS) k_dsa_score(const __grid_consta
     }
   };
 
-  // prologue: the first NST valid tiles (thread 0 tracks the copies)
+  // prologue: the first NST valid tiles. The copies are issued (and
+  // tracked) by lane 0 of warp 1, so that warp 0, whose lane 0 issues the
+  // MMAs, carries no more than its share of the per-tile chain.
+  constexpr int COPY_TID = 32;
   int k_iss = -1;      // last tile whose copy was issued
   long long issued = 0;
   __syncthreads();     // the map slots hold the template
-  if (tid == 0) {
+  if (tid == COPY_TID) {
     for (int s = 0; s < NST; ++s) {
       const int kn = next_valid(k_iss + 1);
       k_iss = kn;
@@ -405,7 +408,7 @@ __global__ void __launch_bounds__(SCORE_THREADS) k_dsa_score(const __grid_consta
       ok = __all_sync(0xffffffffu, ok);
       tc::fence_after_sync();
       if (ok) {
-        if (tid == 0) {
+        if (tid == COPY_TID) {
           const int kn = k_iss < ntiles ? next_valid(k_iss + 1) : ntiles;
           k_iss = kn;
           if (kn < ntiles) {
@@ -413,7 +416,7 @@ __global__ void __launch_bounds__(SCORE_THREADS) k_dsa_score(const __grid_consta
             ++issued;
           }
         }
-        __syncwarp();   // warp 0 converges before the warp-wide TMEM loads
+        __syncwarp();   // warp 1 converges before the warp-wide TMEM loads
         const float* sw = sw0 + pbsel * R * 8;
         const int p = tid;
         for (int r = 0; r < R; ++r) {
@@ -462,8 +465,9 @@ __global__ void __launch_bounds__(SCORE_THREADS) k_dsa_score(const __grid_consta
       dsa_flag(a.dev_err, DSA_DEVERR_TIMEOUT);
       for (long long i = last_mma - 1; i <= last_mma; ++i)
         if (i >= 0) tc::mbar_wait(&mma_bar[i & 1], (uint32_t)((i >> 1) & 1));
-      for (long long i = j; i < issued; ++i) tc::mbar_wait(&full[i % NST], (uint32_t)((i / NST) & 1));
     }
+    if (tid == COPY_TID)
+      for (long long i = j; i < issued; ++i) tc::mbar_wait(&full[i % NST], (uint32_t)((i / NST) & 1));
   } else if (hist_u >= 0) {
     __syncthreads();
     flush_hist(hist_u);
