@@ -77,6 +77,9 @@ def parse():
     ap.add_argument("--path", choices=["fused", "split"], default=None,
                     help="fused: hot_gather_attn; split: hot_gather + mla_decode_attn with the append "
                          "overlapping the attention (default: split)")
+    ap.add_argument("--no-pipeline", action="store_true",
+                    help="run every step serially (no overlap of a step's gather copy and attention "
+                         "with the next step's scoring)")
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--cpu-sample-steps", type=int, default=None)
     ap.add_argument("--oracle-child", type=str, default=None, help=argparse.SUPPRESS)
@@ -319,7 +322,7 @@ class WorkloadRun:
     The timed segments are consecutive parts of one continuous decode, so
     every timed step selects rows no earlier step has read."""
 
-    def __init__(self, wl, K, Wm, nseg, mirror, fused, use_graph):
+    def __init__(self, wl, K, Wm, nseg, mirror, fused, use_graph, pipeline=False):
         import torch
         from decode_attention_dsa_gb300 import abi
         from decode_attention_dsa_gb300.step import DecodePath
@@ -345,6 +348,9 @@ class WorkloadRun:
         self.warm = abi.WARM_LAST_S if wl.warm == "last_s" else abi.WARM_EMPTY
         self.ctr = torch.zeros((U, 4), dtype=torch.int64, device="cuda")
         self.next_seg = 0
+        self.pipeline = pipeline
+        if pipeline:
+            self.path.enable_pipeline()
         torch.cuda.synchronize()
 
     def step_args(self, s):
@@ -358,8 +364,36 @@ class WorkloadRun:
             self.path.step(self.abi.ROUND_AUTO, *self.step_args(s))
         self.torch.cuda.synchronize()
 
+    def _record_pipelined(self, s0, e2e=None):
+        """K steps with each step's gather copy and attention overlapping the
+        next step's scoring (no L2 flush between steps: every step streams
+        far more than L2 holds); one event pair brackets the K steps."""
+        torch, path, rnd = self.torch, self.path, self.abi.ROUND_AUTO
+        path.begin_graph()
+        ev = [torch.cuda.Event(enable_timing=True, external=self.use_graph) for _ in range(2)]
+        ev[0].record()
+        for i in range(self.K):
+            s = s0 + i
+            if e2e is None:
+                path.step_pipelined(rnd, *self.step_args(s))
+            else:
+                host, dev_in2, out_host = e2e
+                names = ("q_idx", "w", "q_lat", "q_rope", "new_rows", "new_keys")
+
+                def stage(b, s=s):
+                    for n in names:
+                        dev_in2[b][n].copy_(host[n][s], non_blocking=True)
+                    return tuple(dev_in2[b][n] for n in names)
+                path.step_pipelined(rnd, *self.step_args(s), out_host=out_host[i], stage_inputs=stage)
+            self.ctr.add_(path.counters)
+        path.join()
+        ev[1].record()
+        return [ev]
+
     def _record(self, s0, per_call, e2e=None):
         torch, path, rnd = self.torch, self.path, self.abi.ROUND_AUTO
+        if self.pipeline and not per_call:
+            return self._record_pipelined(s0, e2e)
         nev = 5 if per_call else 2
         ev = [[torch.cuda.Event(enable_timing=True, external=self.use_graph) for _ in range(nev)]
               for _ in range(self.K)]
@@ -370,7 +404,8 @@ class WorkloadRun:
             e = ev[i]
             e[0].record()
             if e2e is not None:
-                host, dev_in, out_host = e2e
+                host, dev_in2, out_host = e2e
+                dev_in = dev_in2[0]
                 for n in dev_in:
                     dev_in[n].copy_(host[n][s], non_blocking=True)
                 qi, w, ql, qr, nr, nk = (dev_in[n] for n in ("q_idx", "w", "q_lat", "q_rope", "new_rows", "new_keys"))
@@ -438,7 +473,7 @@ class WorkloadRun:
         host = {n: torch.empty_like(self.inp[n], device="cpu").pin_memory() for n in names}
         for n in names:
             host[n].copy_(self.inp[n])
-        dev_in = {n: torch.empty_like(self.inp[n][0]) for n in names}
+        dev_in = [{n: torch.empty_like(self.inp[n][0]) for n in names} for _ in range(2)]
         out_host = torch.empty((self.K,) + tuple(self.path.out.shape), dtype=torch.float32).pin_memory()
         h2d = sum(host[n][0].numel() * host[n][0].element_size() for n in names)
         return (host, dev_in, out_host), h2d, self.path.out.numel() * 4
@@ -499,6 +534,16 @@ def measure_restore(run, n_units):
 
 BREAKDOWN_SEGS = 3
 E2E_SEGS = 3
+L2_BYTES = 126 << 20
+
+
+def use_pipeline(args, wl):
+    """Steps overlap (gather copy and attention with the next step's scoring)
+    where the path allows it (one appended row, no selection reuse, split
+    path) and every step streams more than L2 holds, so that no L2 flush is
+    needed between the steps."""
+    return (not args.no_pipeline and wl.A == 1 and wl.reuse_every == 1 and args.path != "fused"
+            and wl.U * wl.L0 * 128 > 4 * L2_BYTES)
 
 
 def measure(args, wl, K, Wm, mirror, reps, world, clocks=None, e2e=False, breakdown=True):
@@ -510,7 +555,7 @@ def measure(args, wl, K, Wm, mirror, reps, world, clocks=None, e2e=False, breakd
     use_graph = not args.no_graph
     fused = args.path == "fused"
     nseg = reps + (BREAKDOWN_SEGS if breakdown else 0) + (E2E_SEGS if e2e else 0)
-    run = WorkloadRun(wl, K, Wm, nseg, mirror, fused, use_graph)
+    run = WorkloadRun(wl, K, Wm, nseg, mirror, fused, use_graph, pipeline=use_pipeline(args, wl))
     path, U = run.path, wl.U
     heads = [run.segment() for _ in range(reps)]
     bds = [run.segment(per_call=True) for _ in range(BREAKDOWN_SEGS)] if breakdown else []
@@ -615,6 +660,7 @@ def run_gpu(args, rank: int, world: int):
     if world > 1:
         torch.distributed.barrier()
     clocks.start()
+    pipe = use_pipeline(args, wl)
     res = measure(args, wl, K, Wm, args.mirror, reps, world, clocks=clocks, e2e=not args.no_e2e)
     clk = clocks.stop()
     run = res.pop("run")
@@ -632,10 +678,12 @@ def run_gpu(args, rank: int, world: int):
         "data": "synthetic (seeded counter-based generator, generated on the device)",
         "config": workload_config(wl, {
             "mirror": args.mirror, "replacement": wl.policy,
-            "l2": "flushed before every timed step (512 MiB write outside the bracket)",
+            "l2": ("not flushed: every step streams more than L2 holds (keys of all units)" if pipe else
+                   "flushed before every timed step (512 MiB write outside the bracket)"),
             "selection_reuse_every": wl.reuse_every,
             "path": "hot_gather_attn (fused)" if args.path == "fused" else
-                    "hot_gather + mla_decode_attn, append concurrent",
+                    ("pipelined: each step's gather copy and attention (side stream) overlap the next "
+                     "step's score and select" if pipe else "hot_gather + mla_decode_attn, append concurrent"),
             "timing": f"median of {reps} consecutive {K}-step segments of one decode (one CUDA graph each) "
                       f"after {Wm} warm-up steps",
             "parallelism": "replicas" if world > 1 else "single GPU"}),

@@ -64,6 +64,8 @@ SIGNATURES = {
     "dsa_reuse_selection": (ctypes.c_int, [_VP, _VP, _I32, _I32, _I32, _I32, _VP, _VP, _VP]),
     "hot_gather_workspace": (_SZ, [_I32, _I32, _I32]),
     "hot_gather": (ctypes.c_int, [_VP, _I32, _I32, _I32, _I32, _VP, _VP, _VP, _VP, _VP, _SZ, _VP, _VP]),
+    "hot_gather_assign": (ctypes.c_int, [_VP, _I32, _I32, _I32, _I32, _VP, _VP, _VP, _VP, _SZ, _VP, _VP]),
+    "hot_gather_copy": (ctypes.c_int, [_VP, _I32, _I32, _I32, _VP, _VP, _VP, _VP, _SZ, _VP, _VP]),
     "mla_decode_attn_workspace": (_SZ, [_I32, _I32, _I32, _I32]),
     "mla_decode_attn": (ctypes.c_int, [_I32, _I32, _I32, _I32, _VP, _VP, _VP, _VP, _F, _VP, _VP, _VP,
                                        _SZ, _VP, _VP]),
@@ -188,6 +190,17 @@ def hot_gather(units, U, R, K, round_, topk_idx, cls, rows, counters, ws, ws_byt
     return _ok("hot_gather", load().hot_gather(
         _p(units), U, R, K, round_, _p(topk_idx), _p(cls), _p(rows), _p(counters), _p(ws), ws_bytes,
         _p(dev_err), _s(stream)))
+
+
+def hot_gather_assign(units, U, R, K, round_, topk_idx, cls, counters, ws, ws_bytes, dev_err, stream=None):
+    return _ok("hot_gather_assign", load().hot_gather_assign(
+        _p(units), U, R, K, round_, _p(topk_idx), _p(cls), _p(counters), _p(ws), ws_bytes, _p(dev_err),
+        _s(stream)))
+
+
+def hot_gather_copy(units, U, R, K, topk_idx, cls, rows, ws, ws_bytes, dev_err, stream=None):
+    return _ok("hot_gather_copy", load().hot_gather_copy(
+        _p(units), U, R, K, _p(topk_idx), _p(cls), _p(rows), _p(ws), ws_bytes, _p(dev_err), _s(stream)))
 
 
 def mla_decode_attn_workspace(U, R, H, K) -> int:

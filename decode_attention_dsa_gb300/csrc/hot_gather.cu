@@ -326,7 +326,7 @@ k_assign(const dsa_unit* __restrict__ units, int R, int K, int round,
 
 __global__ void __launch_bounds__(COPY_THREADS)
 k_copy(const dsa_unit* __restrict__ units, int R, int K, const int32_t* __restrict__ topk_all,
-       const uint8_t* __restrict__ cls_all, uint8_t* __restrict__ rows_all, GatherWs g) {
+       const uint8_t* __restrict__ cls_all, uint8_t* __restrict__ rows_all, GatherWs g, int32_t* dev_err) {
   const int u = blockIdx.y;
   const int lane = threadIdx.x & 31;
   const int item = blockIdx.x * COPY_WARPS + (threadIdx.x >> 5);
@@ -341,7 +341,13 @@ k_copy(const dsa_unit* __restrict__ units, int R, int K, const int32_t* __restri
     const int32_t p = topk_all[(size_t)u * RK + e];
     uint8_t* dst = rows + (size_t)e * DSA_ROW_BYTES;
     if (c == DSA_CLS_HOT) {
-      warp_copy_row(dst, un.slots + (size_t)un.pos_slot[p] * DSA_ROW_BYTES, lane);
+      const int32_t sl = un.pos_slot[p];
+      if (sl >= 0 && sl < un.slots_n) {
+        warp_copy_row(dst, un.slots + (size_t)sl * DSA_ROW_BYTES, lane);
+      } else {   // the map changed under this copy (a later assign ran first)
+        warp_zero_row(dst, lane);
+        if (lane == 0) dsa_flag(dev_err, DSA_DEVERR_BOUNDS);
+      }
     } else if (c == DSA_CLS_RING) {
       warp_copy_row(dst, un.ring + (size_t)(p & (DSA_RING_ROWS - 1)) * DSA_ROW_BYTES, lane);
     } else if (c == DSA_CLS_RAM) {
@@ -405,19 +411,43 @@ int dsa_launch_assign(const dsa_unit* units, int32_t U, int32_t R, int32_t K, in
                     cls, counters, g, dev_err);
 }
 
-extern "C" int hot_gather(const dsa_unit* units, int32_t U, int32_t R, int32_t K, int32_t round,
-                          const int32_t* topk_idx, uint8_t* cls, uint8_t* rows, int32_t* counters,
-                          void* ws, size_t ws_bytes, int32_t* dev_err, void* stream) {
-  if (!units || !topk_idx || !cls || !rows || !counters) return DSA_ERR_ARG;
+static int gather_args_ok(const dsa_unit* units, int32_t U, int32_t R, int32_t K, const int32_t* topk_idx,
+                          const void* cls, void* ws, size_t ws_bytes) {
+  if (!units || !topk_idx || !cls) return DSA_ERR_ARG;
   if (U < 1 || U > 65535 || R < 1 || R > DSA_MAX_ROWS) return DSA_ERR_ARG;
   if (K < 1 || K > DSA_MAX_K) return DSA_ERR_SHAPE;
   if (!ws || ws_bytes < hot_gather_workspace(U, R, K)) return DSA_ERR_WS;
-  if (reinterpret_cast<uintptr_t>(rows) & 15u) return DSA_ERR_ARG;
-  cudaStream_t st = static_cast<cudaStream_t>(stream);
-  GatherWs g = gather_ws(ws, U, R, K);
+  return DSA_OK;
+}
+
+extern "C" int hot_gather_assign(const dsa_unit* units, int32_t U, int32_t R, int32_t K, int32_t round,
+                                 const int32_t* topk_idx, uint8_t* cls, int32_t* counters, void* ws,
+                                 size_t ws_bytes, int32_t* dev_err, void* stream) {
+  const int st = gather_args_ok(units, U, R, K, topk_idx, cls, ws, ws_bytes);
+  if (st != DSA_OK) return st;
+  if (!counters) return DSA_ERR_ARG;
+  return dsa_launch_assign(units, U, R, K, round, topk_idx, cls, counters, ws, dev_err,
+                           static_cast<cudaStream_t>(stream));
+}
+
+extern "C" int hot_gather_copy(const dsa_unit* units, int32_t U, int32_t R, int32_t K, const int32_t* topk_idx,
+                               const uint8_t* cls, uint8_t* rows, void* ws, size_t ws_bytes, int32_t* dev_err,
+                               void* stream) {
+  const int st = gather_args_ok(units, U, R, K, topk_idx, cls, ws, ws_bytes);
+  if (st != DSA_OK) return st;
+  if (!rows || (reinterpret_cast<uintptr_t>(rows) & 15u)) return DSA_ERR_ARG;
   const int RK = R * K;
-  if (dsa_launch_assign(units, U, R, K, round, topk_idx, cls, counters, ws, dev_err, st) != DSA_OK)
-    return DSA_ERR_CUDA;
-  return launch_pdl(k_copy, dim3((2 * RK + COPY_WARPS - 1) / COPY_WARPS, U), dim3(COPY_THREADS), 0, st, units, R,
-                    K, topk_idx, cls, rows, g);
+  return launch_pdl(k_copy, dim3((2 * RK + COPY_WARPS - 1) / COPY_WARPS, U), dim3(COPY_THREADS), 0,
+                    static_cast<cudaStream_t>(stream), units, R, K, topk_idx, cls, rows, gather_ws(ws, U, R, K),
+                    dev_err);
+}
+
+extern "C" int hot_gather(const dsa_unit* units, int32_t U, int32_t R, int32_t K, int32_t round,
+                          const int32_t* topk_idx, uint8_t* cls, uint8_t* rows, int32_t* counters,
+                          void* ws, size_t ws_bytes, int32_t* dev_err, void* stream) {
+  if (!rows || !counters) return DSA_ERR_ARG;
+  if (reinterpret_cast<uintptr_t>(rows) & 15u) return DSA_ERR_ARG;
+  const int st = hot_gather_assign(units, U, R, K, round, topk_idx, cls, counters, ws, ws_bytes, dev_err, stream);
+  if (st != DSA_OK) return st;
+  return hot_gather_copy(units, U, R, K, topk_idx, cls, rows, ws, ws_bytes, dev_err, stream);
 }

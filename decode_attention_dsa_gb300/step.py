@@ -108,6 +108,80 @@ class DecodePath:
         self.attend(q_lat, q_rope, main)
         main.wait_stream(side)
 
+    # ------------------------------------------------------ pipelined steps
+    def enable_pipeline(self):
+        """Buffers and streams for step_pipelined: a second selection buffer,
+        a side stream and the events that order the two halves of the gather."""
+        if self.A != 1 or self.sources:
+            raise ValueError("pipelined steps need one appended row per step and no selection reuse")
+        dev = self.u.device
+        self.topk_pipe = [self.topk, torch.empty_like(self.topk)]
+        self.pipe_i = 0
+        self.side = torch.cuda.Stream(dev)
+        self.ev_assigned = torch.cuda.Event()
+        self.ev_copied = torch.cuda.Event()
+        self.ev_used = [torch.cuda.Event(), torch.cuda.Event()]   # attention done with topk_pipe[i]
+        self.ev_done = torch.cuda.Event()
+        self.copy_pending = False
+        self.used_pending = [False, False]
+
+    def step_pipelined(self, rnd, q_idx, w, q_lat, q_rope, new_rows, new_keys, stream=None, out_host=None,
+                       stage_inputs=None):
+        """One decode step whose gather copy and attention run on a side stream,
+        overlapping the next step's scoring and selection (main stream). The
+        order the C ABI requires is kept with events: the next step's
+        hot_gather_assign waits for this step's hot_gather_copy (it may evict
+        slots the copy reads); the append (one row) follows the assign on the
+        main stream. Selections alternate between two buffers; ``cur_topk`` is
+        this step's. ``out`` is this step's output once ``join()`` has made the
+        main stream wait for the side stream (or, with ``out_host``, it is
+        copied there on the side stream). ``stage_inputs(b)``, if given, is
+        called on the main stream once the step before last has finished with
+        input set b (b = step parity) and returns the six input tensors it has
+        staged there (e.g. copies from host memory)."""
+        u = self.u
+        main = stream if stream is not None else torch.cuda.current_stream()
+        b = self.pipe_i
+        topk = self.topk_pipe[b]
+        self.pipe_i ^= 1
+        if self.used_pending[b]:
+            main.wait_event(self.ev_used[b])     # the attention two steps back read this buffer
+        if stage_inputs is not None:
+            q_idx, w, q_lat, q_rope, new_rows, new_keys = stage_inputs(b)
+        abi.dsa_score_topk(u.units, u.U, self.R, self.K, q_idx, w, topk, self.max_len,
+                           self.ws_topk, self.ws_topk_bytes, u.dev_err, main)
+        if self.copy_pending:
+            main.wait_event(self.ev_copied)
+        abi.hot_gather_assign(u.units, u.U, self.R, self.K, rnd, topk, self.cls, self.counters, self.ws_gather,
+                              self.ws_gather_bytes, u.dev_err, main)
+        self.ev_assigned.record(main)
+        abi.kv_append_writeback(u.units, u.U, self.A, new_rows, new_keys, u.dev_err, main)
+        self.side.wait_event(self.ev_assigned)
+        abi.hot_gather_copy(u.units, u.U, self.R, self.K, topk, self.cls, self.rows, self.ws_gather,
+                            self.ws_gather_bytes, u.dev_err, self.side)
+        self.ev_copied.record(self.side)
+        abi.mla_decode_attn(u.U, self.R, self.H, self.K, q_lat, q_rope, self.rows, topk, self.scale, self.out,
+                            self.lse, self.ws_attn, self.ws_attn_bytes, u.dev_err, self.side)
+        self.ev_used[b].record(self.side)
+        self.used_pending[b] = True
+        if out_host is not None:
+            with torch.cuda.stream(self.side):
+                out_host.copy_(self.out, non_blocking=True)
+        self.ev_done.record(self.side)
+        self.copy_pending = True
+        self.cur_topk = topk
+
+    def begin_graph(self):
+        """The steps before this point have completed (e.g. an earlier CUDA
+        graph replay on the same stream); steps captured from here on do not
+        wait on their events (a graph capture cannot)."""
+        self.copy_pending = False
+        self.used_pending = [False, False]
+
+    def join(self, stream=None):
+        """Make `stream` (default: the current stream) wait for the side stream."""
+        (stream if stream is not None else torch.cuda.current_stream()).wait_event(self.ev_done)
+
     def launches_per_step(self) -> int:
         """Kernel launches one step enqueues (score, select, [reuse copy],
         classify+assign, copy, attention, append)."""

@@ -315,6 +315,31 @@ int hot_gather(const dsa_unit* units, int32_t U, int32_t R, int32_t K,
                uint8_t* rows, int32_t* counters, void* ws, size_t ws_bytes,
                int32_t* dev_err, void* stream);
 
+/*
+ * The two halves of hot_gather, for callers that overlap them with other work:
+ * hot_gather_assign classifies, pins and assigns victims and updates the
+ * cache state (cls, counters, the workspace's fill list); hot_gather_copy
+ * then writes the compact rows (and the inserted misses' slot bytes) from
+ * that workspace. hot_gather = hot_gather_assign + hot_gather_copy on one
+ * stream. Ordering:
+ *   - the copy must follow its assign (same units, topk_idx, cls, ws), and must
+ *     finish before the next hot_gather_assign on the same units starts (that
+ *     assign may evict slots this copy reads; a HOT row whose slot mapping
+ *     changed under the copy is zeroed and sets DSA_DEVERR_BOUNDS);
+ *   - after the assign, kv_append_writeback with A = 1 may run concurrently
+ *     with the copy: it writes the ring row of position LEN - 64 (below RAM,
+ *     never RING in this round), the key of position LEN and mirror rows at
+ *     or above RAM (read from the ring in this round), none of which the copy
+ *     reads; the next step's dsa_score_topk (into another topk buffer) may then
+ *     overlap the copy and the attention as well.
+ */
+int hot_gather_assign(const dsa_unit* units, int32_t U, int32_t R, int32_t K, int32_t round,
+                      const int32_t* topk_idx, uint8_t* cls, int32_t* counters, void* ws, size_t ws_bytes,
+                      int32_t* dev_err, void* stream);
+int hot_gather_copy(const dsa_unit* units, int32_t U, int32_t R, int32_t K, const int32_t* topk_idx,
+                    const uint8_t* cls, uint8_t* rows, void* ws, size_t ws_bytes, int32_t* dev_err,
+                    void* stream);
+
 /* ---------------------------------- A4 + A5: dequant and MLA decode attention */
 
 /*

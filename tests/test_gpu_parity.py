@@ -5,6 +5,7 @@ per (step, unit, query row), the bound the decode path is specified to."""
 import numpy as np
 import pytest
 
+from oracle.decode import decode_step
 from synth import workloads as W
 from tests.harness import Pair, check_step
 
@@ -389,3 +390,85 @@ def test_config4_capacity_batch_sampled_units():
         pytest.skip("not enough device memory")
     wl = W.WORKLOADS[4].with_(steps=3)
     run(wl, steps=range(3), oracle_units=[0, 31], gpu_gen=True, attention_every=2)
+
+
+def _run_pipelined(wl, nsteps, units=None, oracle_units=None, gpu_gen=False):
+    """Enqueue nsteps pipelined steps back to back (no synchronisation in
+    between, so each step's copy and attention overlap the next step's score),
+    keeping each step's outputs on the stream that orders them, then compare
+    every step with the oracle."""
+    pair = Pair(wl, units=units, oracle_units=oracle_units, gpu_gen=gpu_gen)
+    torch, p = pair.torch, pair.p
+    p.enable_pipeline()
+    U, R, K = pair.g.U, wl.R, wl.K
+    keep = {k: [] for k in ("topk", "cls", "ctr", "out", "rows")}
+    inputs = []
+    for st in range(nsteps):
+        per, t = pair.inputs(st)
+        inputs.append((per, t))
+        p.step_pipelined(st, t["q_idx"], t["w"], t["q_lat"], t["q_rope"], t["new_rows"], t["new_keys"])
+        keep["cls"].append(p.cls.clone())              # main stream: before the next assign
+        keep["ctr"].append(p.counters.clone())
+        with torch.cuda.stream(p.side):                # side stream: after this step's attention
+            keep["out"].append(p.out.clone())
+            keep["topk"].append(p.cur_topk.clone())
+            keep["rows"].append(p.rows.clone())
+    p.join()
+    torch.cuda.synchronize()
+    assert pair.g.check() == 0, f"device error word {pair.g.check():#x}"
+    worst = 0.0
+    for st in range(nsteps):
+        per, _ = inputs[st]
+        pair.last_inputs = per
+        g = {k: v[st].cpu().numpy() for k, v in keep.items()}
+        g["counters"] = g.pop("ctr")
+        g["lse"] = None
+        for i, u in enumerate(pair.uidx):
+            if u not in pair.o:
+                continue
+            x = per[i]
+            o = decode_step(pair.o[u], st, wl.K, wl.scale(), x.q_idx, x.w, x.q_lat, x.q_rope, x.new_rows, x.new_keys)
+            assert np.array_equal(g["topk"][i], o["topk"]), f"step {st} unit {u}: Top-K"
+            assert np.array_equal(g["cls"][i], o["cls"]), f"step {st} unit {u}: classification"
+            assert np.array_equal(g["counters"][i], o["counters"]), f"step {st} unit {u}: counters"
+            assert np.array_equal(g["rows"][i], o["rows"]), f"step {st} unit {u}: gathered rows"
+            for r in range(R):
+                ref = o["out"][r]
+                err = np.abs(g["out"][i, r].astype(np.float64) - ref).max()
+                assert err <= 1e-3 * np.abs(ref).max(), f"step {st} unit {u} row {r}: attention"
+                worst = max(worst, err / (1e-3 * np.abs(ref).max()))
+    # the final cache state
+    for i, u in enumerate(pair.uidx):
+        if u not in pair.o:
+            continue
+        oc, s = pair.o[u].cache, pair.state(i)
+        assert np.array_equal(s["slot_pos"], oc.slot_pos) and s["st"][2] == oc.hand
+        assert s["st"][0] == oc.length and s["st"][1] == oc.rows_in_ram
+    return worst
+
+
+def test_pipelined_steps_match_oracle():
+    """Steps whose gather copy and attention run on a side stream while the
+    next step scores: results identical to the serial path's (the oracle)."""
+    wl = W.WORKLOADS[0].with_(name="pipe", sessions=2, layers=1, L0=3000, S=128, K=256, H=64, steps=70, A=1,
+                              warm="last_s")
+    from decode_attention_dsa_gb300 import abi  # noqa: F401
+    assert _run_pipelined(wl, 70) < 1.0
+
+
+def test_pipelined_steps_mtp_rows():
+    wl = W.WORKLOADS[0].with_(name="pipe-mtp", L0=1500, S=64, R=4, A=1, K=128, H=16, warm="last_s", mode="mtp",
+                              steps=24)
+    _run_pipelined(wl, 24)
+
+
+@pytest.mark.slow
+def test_config4_capacity_batch_pipelined_steps():
+    """The bench's launch shape of the capacity batch (pipelined steps),
+    units 0 and 31 against the oracle for 6 steps."""
+    import torch
+    free, _ = torch.cuda.mem_get_info()
+    if free < 12 * 2**30:
+        pytest.skip("not enough device memory")
+    wl = W.WORKLOADS[4].with_(steps=6)
+    _run_pipelined(wl, 6, oracle_units=[0, 31], gpu_gen=True)
