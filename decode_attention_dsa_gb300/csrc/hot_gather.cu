@@ -32,6 +32,8 @@
 //                 rows (all RAM-class: they get the RAM bytes, never the slot
 //                 being filled); every other entry copies from its source
 //                 (slot / ring / mirror).
+#include <algorithm>
+
 #include "common.cuh"
 #include "gather_internal.cuh"
 
@@ -40,6 +42,10 @@ namespace {
 constexpr int ASSIGN_THREADS = 1024;
 constexpr int COPY_THREADS = 256;
 constexpr int COPY_WARPS = COPY_THREADS / 32;
+// The row copies run on at most COPY_BLOCKS_PER_SM blocks per SM (grid-stride
+// beyond): enough host reads in flight for the link, while a full-width grid
+// of waiting warps measured slower and crowded out kernels running beside it.
+constexpr int COPY_BLOCKS_PER_SM = 4;
 
 // lower_bound of p in an ascending row whose tail is -1 padding (-1 = +inf).
 __device__ __forceinline__ int row_lower_bound(const int32_t* row, int K, int32_t p) {
@@ -325,62 +331,70 @@ k_assign(const dsa_unit* __restrict__ units, int R, int K, int round,
 }
 
 __global__ void __launch_bounds__(COPY_THREADS)
-k_copy(const dsa_unit* __restrict__ units, int R, int K, const int32_t* __restrict__ topk_all,
+k_copy(const dsa_unit* __restrict__ units, int U, int R, int K, const int32_t* __restrict__ topk_all,
        const uint8_t* __restrict__ cls_all, uint8_t* __restrict__ rows_all, GatherWs g, int32_t* dev_err) {
-  const int u = blockIdx.y;
   const int lane = threadIdx.x & 31;
-  const int item = blockIdx.x * COPY_WARPS + (threadIdx.x >> 5);
   pdl_wait();
   const int RK = R * K;
-  const dsa_unit& un = units[u];
-  uint8_t* rows = rows_all + (size_t)u * RK * DSA_ROW_BYTES;
-  if (item < RK) {
-    const int e = item;
-    if (g.served[(size_t)u * RK + e]) return;   // written by its fill below
-    const uint8_t c = cls_all[(size_t)u * RK + e];
-    const int32_t p = topk_all[(size_t)u * RK + e];
-    uint8_t* dst = rows + (size_t)e * DSA_ROW_BYTES;
-    if (c == DSA_CLS_HOT) {
-      const int32_t sl = un.pos_slot[p];
-      if (sl >= 0 && sl < un.slots_n) {
-        warp_copy_row(dst, un.slots + (size_t)sl * DSA_ROW_BYTES, lane);
-      } else {   // the map changed under this copy (a later assign ran first)
+  // warps walk the flattened (unit, item) space in order: per unit its RK
+  // entries, then its fills in ascending position order (mirror rows are
+  // read in position order, unit by unit, which suits the host's page
+  // translations)
+  const int64_t nitems = (int64_t)U * 2 * RK;
+  for (int64_t idx = (int64_t)blockIdx.x * COPY_WARPS + (threadIdx.x >> 5); idx < nitems;
+       idx += (int64_t)gridDim.x * COPY_WARPS) {
+    const int u = (int)(idx / (2 * RK));
+    const int item = (int)(idx - (int64_t)u * 2 * RK);
+    const dsa_unit& un = units[u];
+    uint8_t* rows = rows_all + (size_t)u * RK * DSA_ROW_BYTES;
+    if (item < RK) {
+      const int e = item;
+      if (g.served[(size_t)u * RK + e]) continue;   // written by its fill
+      const uint8_t c = cls_all[(size_t)u * RK + e];
+      const int32_t p = topk_all[(size_t)u * RK + e];
+      uint8_t* dst = rows + (size_t)e * DSA_ROW_BYTES;
+      if (c == DSA_CLS_HOT) {
+        const int32_t sl = un.pos_slot[p];
+        if (sl >= 0 && sl < un.slots_n) {
+          warp_copy_row(dst, un.slots + (size_t)sl * DSA_ROW_BYTES, lane);
+        } else {   // the map changed under this copy (a later assign ran first)
+          warp_zero_row(dst, lane);
+          if (lane == 0) dsa_flag(dev_err, DSA_DEVERR_BOUNDS);
+        }
+      } else if (c == DSA_CLS_RING) {
+        warp_copy_row(dst, un.ring + (size_t)(p & (DSA_RING_ROWS - 1)) * DSA_ROW_BYTES, lane);
+      } else if (c == DSA_CLS_RAM) {
+        warp_copy_row(dst, un.mirror + (size_t)p * DSA_ROW_BYTES, lane);
+      } else {
         warp_zero_row(dst, lane);
-        if (lane == 0) dsa_flag(dev_err, DSA_DEVERR_BOUNDS);
       }
-    } else if (c == DSA_CLS_RING) {
-      warp_copy_row(dst, un.ring + (size_t)(p & (DSA_RING_ROWS - 1)) * DSA_ROW_BYTES, lane);
-    } else if (c == DSA_CLS_RAM) {
-      warp_copy_row(dst, un.mirror + (size_t)p * DSA_ROW_BYTES, lane);
     } else {
-      warp_zero_row(dst, lane);
-    }
-  } else {
-    const int f = item - RK;
-    if (f >= g.nfill[u]) return;
-    const size_t o = (size_t)u * RK + f;
-    const int32_t p = g.fill_pos[o];
-    const int32_t s = g.fill_slot[o];
-    const int32_t e = g.fill_entry[o];
-    const uint4* src = reinterpret_cast<const uint4*>(un.mirror + (size_t)p * DSA_ROW_BYTES);
-    uint4* d1 = reinterpret_cast<uint4*>(un.slots + (size_t)s * DSA_ROW_BYTES);
-    uint4* d2 = reinterpret_cast<uint4*>(rows + (size_t)e * DSA_ROW_BYTES);
-    const uint4 a = ldg_nc_v4(src + lane);
-    uint4 b;
-    if (lane < 9) b = ldg_nc_v4(src + 32 + lane);
-    d1[lane] = a;
-    d2[lane] = a;
-    if (lane < 9) {
-      d1[32 + lane] = b;
-      d2[32 + lane] = b;
-    }
-    const int32_t* dp = g.dup + o * (DSA_MAX_ROWS - 1);
-    for (int k = 0; k < R - 1; ++k) {
-      const int32_t ed = dp[k];
-      if (ed < 0) break;
-      uint4* d3 = reinterpret_cast<uint4*>(rows + (size_t)ed * DSA_ROW_BYTES);
-      d3[lane] = a;
-      if (lane < 9) d3[32 + lane] = b;
+      const int f = item - RK;
+      if (f >= g.nfill[u]) continue;
+      const size_t o = (size_t)u * RK + f;
+      const int32_t p = g.fill_pos[o];
+      const int32_t s = g.fill_slot[o];
+      const int32_t e = g.fill_entry[o];
+      const uint4* src = reinterpret_cast<const uint4*>(un.mirror + (size_t)p * DSA_ROW_BYTES);
+      uint4* d1 = reinterpret_cast<uint4*>(un.slots + (size_t)s * DSA_ROW_BYTES);
+      uint4* d2 = reinterpret_cast<uint4*>(rows + (size_t)e * DSA_ROW_BYTES);
+      const uint4 a = ldg_nc_v4(src + lane);
+      uint4 b;
+      if (lane < 9) b = ldg_nc_v4(src + 32 + lane);
+      d1[lane] = a;
+      d2[lane] = a;
+      if (lane < 9) {
+        d1[32 + lane] = b;
+        d2[32 + lane] = b;
+      }
+      const int32_t* dp = g.dup + o * (DSA_MAX_ROWS - 1);
+      for (int k = 0; k < R - 1; ++k) {
+        const int32_t ed = dp[k];
+        if (ed < 0) break;
+        uint4* d3 = reinterpret_cast<uint4*>(rows + (size_t)ed * DSA_ROW_BYTES);
+        d3[lane] = a;
+        if (lane < 9) d3[32 + lane] = b;
+      }
     }
   }
 }
@@ -436,10 +450,16 @@ extern "C" int hot_gather_copy(const dsa_unit* units, int32_t U, int32_t R, int3
   const int st = gather_args_ok(units, U, R, K, topk_idx, cls, ws, ws_bytes);
   if (st != DSA_OK) return st;
   if (!rows || (reinterpret_cast<uintptr_t>(rows) & 15u)) return DSA_ERR_ARG;
-  const int RK = R * K;
-  return launch_pdl(k_copy, dim3((2 * RK + COPY_WARPS - 1) / COPY_WARPS, U), dim3(COPY_THREADS), 0,
-                    static_cast<cudaStream_t>(stream), units, R, K, topk_idx, cls, rows, gather_ws(ws, U, R, K),
-                    dev_err);
+  static DsaPerDevice pd;
+  int dev = 0;
+  const int ok = dsa_device_setup(pd, &dev, [](int) { return DSA_OK; });
+  if (ok != DSA_OK) return ok;
+  const int64_t nitems = (int64_t)U * 2 * R * K;
+  const int64_t blocks =
+      std::max<int64_t>(1, std::min<int64_t>((nitems + COPY_WARPS - 1) / COPY_WARPS,
+                                             (int64_t)COPY_BLOCKS_PER_SM * pd.num_sms[dev]));
+  return launch_pdl(k_copy, dim3((unsigned)blocks), dim3(COPY_THREADS), 0, static_cast<cudaStream_t>(stream),
+                    units, (int)U, (int)R, (int)K, topk_idx, cls, rows, gather_ws(ws, U, R, K), dev_err);
 }
 
 extern "C" int hot_gather(const dsa_unit* units, int32_t U, int32_t R, int32_t K, int32_t round,
