@@ -51,9 +51,10 @@ namespace {
 constexpr int HIST1_BINS = 4096;         // top 12 bits of the ordered key
 constexpr int SEL_CLUSTER = 8;
 constexpr int SEL_THREADS = 512;
-constexpr int SEL_TILE = 4096;           // keys per streamed tile (16 KB)
-constexpr int SEL_STAGES = 2;            // tiles in flight per CTA
+constexpr int SEL_WARPS = 16;           // SEL_THREADS / 32
 constexpr int SEL_LIST_CAP = 2048;       // keys of bin >= b1 kept per CTA, in order
+constexpr int SEL_WLIST = SEL_LIST_CAP / SEL_WARPS;   // per warp
+constexpr int SEL_UNR = 4;               // 16-byte loads in flight per lane
 constexpr int SEL_ALL_CAP = 8192;        // candidates per cluster (fast path)
 constexpr int SEL_PER_SRC = SEL_ALL_CAP / SEL_CLUSTER;   // candidates each CTA may push
 
@@ -528,23 +529,20 @@ struct SelShared {
   int tmp[32];
   int bin, above;
   int ncand;
-  int list_n;                 // entries of this CTA's list (above the cap: it overflowed)
-  uint64_t sbar[SEL_STAGES];  // streamed key tiles
+  int wcnt[SEL_WARPS];        // entries of each warp's list (above SEL_WLIST: it overflowed)
+  int woff[SEL_WARPS + 1];    // their prefix: warp w's entries are list entries [woff[w], woff[w+1])
   int srcn[SEL_CLUSTER];      // candidates pushed here by each CTA (-1: it overflowed)
   long long rcnt[SEL_CLUSTER][2];   // (gt, eq) of each CTA, read once for the prefix
   long long cnt[2];           // this CTA's (gt, eq) counts
 };
-// Shared memory after SelShared (each part 128-byte aligned): region U holds
-// the streamed key tiles during the pass and the 4096-bin radix histogram
-// after it; then the ordered list (positions, keys); then the candidates of
-// the whole cluster.
-constexpr size_t SEL_U_OFF = (sizeof(SelShared) + 127) / 128 * 128;
-constexpr size_t SEL_U_BYTES = (size_t)SEL_STAGES * SEL_TILE * 4;
-constexpr size_t SEL_LIST_OFF = SEL_U_OFF + SEL_U_BYTES;
+// Shared memory after SelShared (each part 128-byte aligned): the 4096-bin
+// radix histogram, the per-warp ordered lists (positions, keys), the
+// candidates of the whole cluster.
+constexpr size_t SEL_H_OFF = (sizeof(SelShared) + 127) / 128 * 128;
+constexpr size_t SEL_LIST_OFF = SEL_H_OFF + (size_t)HIST1_BINS * 4;
 constexpr size_t SEL_ALLC_OFF = SEL_LIST_OFF + (size_t)SEL_LIST_CAP * 8;
 constexpr size_t SEL_SMEM = SEL_ALLC_OFF + (size_t)SEL_ALL_CAP * 4;
-static_assert(SEL_U_OFF % 16 == 0 && SEL_TILE * 4 % 16 == 0, "bulk-copy destination alignment");
-static_assert(SEL_U_BYTES >= HIST1_BINS * 4, "region U also holds the radix histogram");
+static_assert(SEL_WARPS * 32 == SEL_THREADS, "one list per warp");
 
 __global__ void __cluster_dims__(SEL_CLUSTER, 1, 1) __launch_bounds__(SEL_THREADS, 2)
 k_topk_select(const dsa_unit* __restrict__ units, int R, int K, uint32_t* __restrict__ hist,
@@ -572,8 +570,7 @@ k_topk_select(const dsa_unit* __restrict__ units, int R, int K, uint32_t* __rest
   asm volatile("barrier.cluster.arrive.relaxed.aligned;" ::: "memory");
   extern __shared__ __align__(128) uint8_t smem_sel[];
   SelShared* S = reinterpret_cast<SelShared*>(smem_sel);
-  uint8_t* regU = smem_sel + SEL_U_OFF;
-  uint32_t* h1 = reinterpret_cast<uint32_t*>(regU);                           // [4096], after the pass
+  uint32_t* h1 = reinterpret_cast<uint32_t*>(smem_sel + SEL_H_OFF);           // [4096]
   int32_t* lpos = reinterpret_cast<int32_t*>(smem_sel + SEL_LIST_OFF);        // [SEL_LIST_CAP]
   uint32_t* lkey = reinterpret_cast<uint32_t*>(lpos + SEL_LIST_CAP);          // [SEL_LIST_CAP]
   uint32_t* allc = reinterpret_cast<uint32_t*>(smem_sel + SEL_ALLC_OFF);      // [SEL_ALL_CAP]
@@ -582,30 +579,11 @@ k_topk_select(const dsa_unit* __restrict__ units, int R, int K, uint32_t* __rest
   const int64_t chunk = ((L + SEL_CLUSTER - 1) / SEL_CLUSTER + 3) / 4 * 4;
   const int64_t beg = min((int64_t)crank * chunk, L);
   const int64_t end = min(beg + chunk, L);
-  const int64_t nkeys = end - beg;
-  const int ntile = (int)((nkeys + SEL_TILE - 1) / SEL_TILE);
   const uint32_t* kk = okeys + (size_t)ur * stride;
-  // bulk copies need 16-byte aligned sources (always true for workspaces from
-  // dsa_score_topk_workspace; otherwise the keys are read from global memory)
-  const bool stream = ((reinterpret_cast<uintptr_t>(kk + beg)) & 15u) == 0;
-  // tile i: keys [beg + i*SEL_TILE, +n) into stage i % SEL_STAGES; the copy
-  // is rounded up to 4 keys (rows are padded to a multiple of 4)
-  auto issue = [&](int i) {
-    const int64_t k0 = (int64_t)i * SEL_TILE;
-    const int64_t n = min((int64_t)SEL_TILE, nkeys - k0);
-    const uint32_t bytes = (uint32_t)((n + 3) / 4 * 16);
-    const int st = i % SEL_STAGES;
-    tc::mbar_arrive_expect_tx(&S->sbar[st], bytes);
-    tc::bulk_g2s(regU + (size_t)st * SEL_TILE * 4, kk + beg + k0, bytes, &S->sbar[st]);
-  };
   if (tid == 0) {
     S->bin = 0;
     S->above = 0;
     S->ncand = 0;
-    for (int i = 0; i < SEL_STAGES; ++i) tc::mbar_init(&S->sbar[i], 1);
-    tc::fence_mbar_init();
-    if (stream)
-      for (int i = 0; i < SEL_STAGES && i < ntile; ++i) issue(i);
   }
 
   // ---- level 1: top 12 bits from the global histogram (read in place)
@@ -647,71 +625,81 @@ k_topk_select(const dsa_unit* __restrict__ units, int R, int K, uint32_t* __rest
 #pragma unroll
   for (int c = 0; c < SEL_CLUSTER; ++c) dst[c] = cluster.map_shared_rank(allc, c) + crank * SEL_PER_SRC;
 
-  // ---- one pass over the range, tile by tile in position order: count the
-  //      keys above bin b1, push the candidates inside b1 to the cluster, and
-  //      keep every key of bin >= b1 (position and key) in an ordered list;
-  //      thread t owns keys [8t, 8t + 8) of a tile
+  // ---- one pass over the range: count the keys above bin b1, push the
+  //      candidates inside b1 to the cluster, and keep every key of bin >= b1
+  //      with its position in an ordered list. Warp w owns a contiguous part
+  //      of the range and its own list (lane order within a group of 32
+  //      quads, groups in increasing position), so the warps' lists,
+  //      concatenated in warp order, are ordered; no block barrier is needed.
+  const int warp = tid >> 5, lane = tid & 31;
+  const int64_t nq = q1 - q0;
+  const int64_t qpw = (nq + SEL_WARPS - 1) / SEL_WARPS;
+  const int64_t wq0 = min(q0 + (int64_t)warp * qpw, q1), wq1 = min(wq0 + qpw, q1);
+  int32_t* wpos = lpos + warp * SEL_WLIST;
+  uint32_t* wkey = lkey + warp * SEL_WLIST;
   long long gt1 = 0;
-  int lbase = 0;       // list entries so far (may pass the cap)
-  bool timed_out = false;
-  for (int i = 0; i < ntile; ++i) {
-    const int st = i % SEL_STAGES;
-    const int64_t p0 = beg + (int64_t)i * SEL_TILE + 8 * tid;
-    uint32_t w[8];
-    bool ok = true;
-    if (stream) {
-      ok = tc::mbar_wait(&S->sbar[st], (uint32_t)((i / SEL_STAGES) & 1));
-      const uint4* t4 = reinterpret_cast<const uint4*>(regU + (size_t)st * SEL_TILE * 4) + 2 * tid;
-      const uint4 a = ok ? t4[0] : make_uint4(0, 0, 0, 0);
-      const uint4 b = ok ? t4[1] : make_uint4(0, 0, 0, 0);
-      w[0] = a.x; w[1] = a.y; w[2] = a.z; w[3] = a.w; w[4] = b.x; w[5] = b.y; w[6] = b.z; w[7] = b.w;
-    } else {
+  int wn = 0;          // entries of this warp's list so far (may pass SEL_WLIST)
+  for (int64_t qb = wq0; qb < wq1; qb += 32 * SEL_UNR) {
+    uint4 v[SEL_UNR];
 #pragma unroll
-      for (int e = 0; e < 8; ++e) w[e] = p0 + e < end ? __ldcg(kk + p0 + e) : 0u;
+    for (int k = 0; k < SEL_UNR; ++k) {
+      const int64_t q = qb + 32 * k + lane;
+      v[k] = q < wq1 ? key4(q) : make_uint4(0, 0, 0, 0);
     }
-    timed_out |= !ok;
-    int c = 0;
 #pragma unroll
-    for (int e = 0; e < 8; ++e) {
-      const bool in = p0 + e < end;
-      const uint32_t d1 = w[e] >> 20;
-      gt1 += in && d1 > b1;
-      c += in && d1 >= b1;
-      if (in && d1 == b1) {
-        const int k = atomicAdd(&S->ncand, 1);
-        if (k < SEL_PER_SRC) {
+    for (int k = 0; k < SEL_UNR; ++k) {
+      const int64_t q = qb + 32 * k + lane;
+      const uint32_t w[4] = {v[k].x, v[k].y, v[k].z, v[k].w};
+      int c = 0;
 #pragma unroll
-          for (int cc = 0; cc < SEL_CLUSTER; ++cc) dst[cc][k] = w[e];
+      for (int e = 0; e < 4; ++e) {
+        const bool in = q < wq1 && 4 * q + e < end;
+        const uint32_t d1 = w[e] >> 20;
+        gt1 += in && d1 > b1;
+        c += in && d1 >= b1;
+        if (in && d1 == b1) {
+          const int kc = atomicAdd(&S->ncand, 1);
+          if (kc < SEL_PER_SRC) {
+#pragma unroll
+            for (int cc = 0; cc < SEL_CLUSTER; ++cc) dst[cc][kc] = w[e];
+          }
         }
       }
-    }
-    int tot;
-    const int inc = block_inclusive_scan<SEL_THREADS>(c, S->tmp, &tot);   // ends with a barrier
-    int o = lbase + inc - c;
+      // this lane's offset in the warp's list: exclusive prefix over lanes
+      int inc = c;
 #pragma unroll
-    for (int e = 0; e < 8; ++e) {
-      if (p0 + e < end && (w[e] >> 20) >= b1) {
-        if (o < SEL_LIST_CAP) {
-          lpos[o] = (int32_t)(p0 + e);
-          lkey[o] = w[e];
-        }
-        ++o;
+      for (int o = 1; o < 32; o <<= 1) {
+        const int y = __shfl_up_sync(0xffffffffu, inc, o);
+        if (lane >= o) inc += y;
       }
+      int o = wn + inc - c;
+#pragma unroll
+      for (int e = 0; e < 4; ++e) {
+        if (q < wq1 && 4 * q + e < end && (w[e] >> 20) >= b1) {
+          if (o < SEL_WLIST) {
+            wpos[o] = (int32_t)(4 * q + e);
+            wkey[o] = w[e];
+          }
+          ++o;
+        }
+      }
+      wn += __shfl_sync(0xffffffffu, inc, 31);
     }
-    lbase += tot;
-    // every thread has read the stage (the scan's barriers): refill it
-    if (stream && tid == 0 && i + SEL_STAGES < ntile) issue(i + SEL_STAGES);
   }
-  if (__syncthreads_or(timed_out) && tid == 0) {
-    // (does not happen in normal runs) the selection is void; every stage's
-    // last copy gets one more bounded wait so that none lands later
-    dsa_flag(dev_err, DSA_DEVERR_TIMEOUT);
-    for (int st = 0; st < SEL_STAGES; ++st) {
-      const int last = st < ntile ? st + (ntile - 1 - st) / SEL_STAGES * SEL_STAGES : -1;
-      if (last >= 0) tc::mbar_wait(&S->sbar[st], (uint32_t)((last / SEL_STAGES) & 1));
+  if (lane == 0) S->wcnt[warp] = wn;
+  __syncthreads();
+  if (tid == 0) {
+    int acc = 0;
+    for (int i = 0; i < SEL_WARPS; ++i) {
+      S->woff[i] = acc;
+      acc += min(S->wcnt[i], SEL_WLIST);
     }
+    S->woff[SEL_WARPS] = acc;
   }
   __syncthreads();
+  bool list_ok = true;
+  for (int i = 0; i < SEL_WARPS; ++i) list_ok &= S->wcnt[i] <= SEL_WLIST;
+  const int lbase = S->woff[SEL_WARPS];
   int gt1_cta;
   block_inclusive_scan<SEL_THREADS>((int)gt1, S->tmp, &gt1_cta);
   if (tid < SEL_CLUSTER)
@@ -879,10 +867,18 @@ k_topk_select(const dsa_unit* __restrict__ units, int R, int K, uint32_t* __rest
       run_sel += stot;
     }
   };
-  if (lbase <= SEL_LIST_CAP) {
+  if (list_ok) {
+    // entry i of the concatenated list: warp segment w with woff[w] <= i < woff[w + 1]
     compact(lbase, [&](int64_t i, int32_t& p, uint32_t& k) {
-      p = i < lbase ? lpos[i] : -1;
-      k = i < lbase ? lkey[i] : 0u;
+      p = -1;
+      k = 0u;
+      if (i < lbase) {
+        int w = 0;
+        while (w + 1 < SEL_WARPS && S->woff[w + 1] <= i) ++w;
+        const int j = (int)(i - S->woff[w]);
+        p = lpos[w * SEL_WLIST + j];
+        k = lkey[w * SEL_WLIST + j];
+      }
     });
   } else {
     const int64_t nq = q1 - q0;   // the whole range, 4 keys per quad from global memory
