@@ -461,11 +461,24 @@ extern "C" int hc_init(const dsa_unit* units, int32_t U, int32_t warm, const int
   return DSA_OK;
 }
 
+namespace {
+DsaPerDevice g_append_setup;
+int append_setup() {
+  int dev = 0;
+  return dsa_device_setup(g_append_setup, &dev, [](int) {
+    DSA_CUDA_TRY(dsa_prefer_shared(k_append<false>));
+    DSA_CUDA_TRY(dsa_prefer_shared(k_append<true>));
+    return DSA_OK;
+  });
+}
+}  // namespace
+
 extern "C" int kv_append_writeback(const dsa_unit* units, int32_t U, int32_t A,
                                    const uint8_t* new_rows, const uint16_t* new_keys,
                                    int32_t* dev_err, void* stream) {
   if (!units || !new_rows || !new_keys || U < 1 || U > 65535 || A < 1 || A > DSA_RING_ROWS)
     return DSA_ERR_ARG;
+  if (const int ok = append_setup(); ok != DSA_OK) return ok;
   return launch_pdl(k_append<false>, dim3(U), dim3(APP_THREADS), 0, static_cast<cudaStream_t>(stream), units, A,
                     new_rows, new_keys, dev_err, (const uint16_t*)nullptr);
 }
@@ -475,6 +488,7 @@ extern "C" int kv_append_quantize(const dsa_unit* units, int32_t U, int32_t A, c
                                   void* stream) {
   if (!units || !new_latent || !new_rope || !new_keys || U < 1 || U > 65535 || A < 1 || A > DSA_RING_ROWS)
     return DSA_ERR_ARG;
+  if (const int ok = append_setup(); ok != DSA_OK) return ok;
   return launch_pdl(k_append<true>, dim3(U), dim3(APP_THREADS), 0, static_cast<cudaStream_t>(stream), units, A,
                     reinterpret_cast<const uint8_t*>(new_latent), new_keys, dev_err, new_rope);
 }

@@ -34,6 +34,17 @@ struct DsaPerDevice {
   int num_sms[DSA_MAX_DEVICES] = {};
 };
 
+// Every kernel of the library prefers the largest shared-memory carveout. An
+// SM whose L1/shared split was set for a kernel with little shared memory
+// takes a CTA that needs more only after it has drained, so a small kernel of
+// one step (row copies, append) would hold the next step's persistent score
+// CTAs off its SMs instead of running beside them.
+template <typename T>
+static inline cudaError_t dsa_prefer_shared(T* kernel) {
+  return cudaFuncSetAttribute(kernel, cudaFuncAttributePreferredSharedMemoryCarveout,
+                              (int)cudaSharedmemCarveoutMaxShared);
+}
+
 template <typename F>
 static inline int dsa_device_setup(DsaPerDevice& pd, int* dev_out, F&& init) {
   int dev = -1;

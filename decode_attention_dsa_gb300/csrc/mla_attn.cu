@@ -505,6 +505,7 @@ int launch_attn(int32_t U, int32_t R, int32_t H, int32_t K, const uint16_t* q_la
   const int ok = dsa_device_setup(pd, &dev, [](int) {
     DSA_CUDA_TRY(cudaFuncSetAttribute(k_mla_attn<GATHER>, cudaFuncAttributeMaxDynamicSharedMemorySize, SMEM_BYTES));
     DSA_CUDA_TRY(cudaFuncSetAttribute(k_mla_attn<GATHER>, cudaFuncAttributeNonPortableClusterSizeAllowed, 1));
+    DSA_CUDA_TRY(dsa_prefer_shared(k_mla_attn<GATHER>));
     return DSA_OK;
   });
   if (ok != DSA_OK) return ok;

@@ -952,6 +952,8 @@ extern "C" int dsa_score_topk(const dsa_unit* units, int32_t U, int32_t R, int32
       score_config(r, &nst, &per_sm);
       mx = std::max(mx, score_layout(r, nst).bytes + 1024);
     }
+    DSA_CUDA_TRY(dsa_prefer_shared(k_dsa_score));
+    DSA_CUDA_TRY(dsa_prefer_shared(k_topk_select));
     DSA_CUDA_TRY(cudaFuncSetAttribute(k_dsa_score, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)mx));
     DSA_CUDA_TRY(cudaFuncSetAttribute(k_topk_select, cudaFuncAttributeMaxDynamicSharedMemorySize,
                                       (int)select_smem()));
@@ -1017,6 +1019,13 @@ extern "C" int dsa_reuse_selection(int32_t* topk_idx, const int32_t* src_topk, i
   if (!topk_idx || !src_topk || !src_of || U < 1 || U > 65535 || Us < 1 || R < 1 || R > DSA_MAX_ROWS)
     return DSA_ERR_ARG;
   if (K < 1 || K > DSA_MAX_K) return DSA_ERR_SHAPE;
+  static DsaPerDevice pd;
+  int dev = 0;
+  const int ok = dsa_device_setup(pd, &dev, [](int) {
+    DSA_CUDA_TRY(dsa_prefer_shared(k_reuse_selection));
+    return DSA_OK;
+  });
+  if (ok != DSA_OK) return ok;
   const int bx = (int)std::min<int64_t>(((int64_t)R * K + 255) / 256, 64);
   return launch_pdl(k_reuse_selection, dim3(bx, U), dim3(256), 0, static_cast<cudaStream_t>(stream), topk_idx,
                     src_topk, Us, R, K, src_of, dev_err);
