@@ -7,9 +7,9 @@
 // w_hat = scale * q, one scale per group of 64 (G64). [P3] "From 1M total to
 // 15+ x 1M", section "起点": a row is 512 B latent + 16 B scales + 128 B RoPE.
 //
-// One thread-block cluster per (unit, query row), of ceil(K / 128) CTAs
-// rounded up to a power of two; CTA c of the cluster owns selected rows
-// [128c, 128c + 128) (none for the padding CTAs):
+// Two launches per call:
+//  A. k_mla_attn: ceil(K / 128) CTAs per (unit, query row); CTA c owns the
+//     selected rows [128c, 128c + 128):
 //  1. one 1-D bulk TMA copy brings the CTA's rows (up to 128 x 656 B) into
 //     shared memory region X;
 //  2. dequantisation writes an fp16 tile [128 rows][576] (latent int8 * fp16
@@ -22,17 +22,22 @@
 //     2 x 256 for O, fp32 accumulators in tensor memory, one issuing thread,
 //     completion through tcgen05.commit on an mbarrier;
 //  5. softmax of the CTA's 128 columns per head in registers; P (fp16) goes to
-//     X as the A operand of PV;
-//  6. each CTA stores its O (64 x 512 fp32) to its workspace slot (it stays in
-//     L2) and its max/sum to shared memory; after a cluster barrier CTA c
-//     merges columns [c*W, c*W + W) of every CTA's O with the max/sum
-//     rescaling of split softmax (maxima and sums read through distributed
-//     shared memory) and writes the final out (and lse) directly.
+//     X as the A operand of PV, its 64 head rows written twice (rows 64..127
+//     repeat them) so that tensor-memory lanes 64..127 of O repeat lanes
+//     0..63 and all eight warps can read O out;
+//  6. the CTA's O (64 x 512 fp32), row max and row sum go to its slot of the
+//     workspace (they stay in L2).
+//  B. k_attn_merge: one block per (unit, query row) and 32-column slice
+//     rescales the CTAs' partial outputs by exp(m_c - M) (split softmax),
+//     sums them, divides by the total L and writes out (and lse).
 // fp16 operands keep 11 significant bits: each operand's rounding is <= 2^-11
-// relative, far inside the 1e-3 * max|out| budget. Waits are bounded; on a
-// timeout the kernel sets DSA_DEVERR_TIMEOUT, frees its tensor memory and
-// still takes part in every cluster barrier so no peer is left waiting.
-#include <cooperative_groups.h>
+// relative, far inside the 1e-3 * max|out| budget. The latent is
+// dequantised in fp16 arithmetic: the byte b + 128 placed under the exponent
+// of 1024 is the fp16 number 1024 + (b + 128), exactly; subtracting 1152 gives
+// b exactly and one fp16 multiply by the scale rounds once, the same value as
+// the fp32 product rounded to fp16. Waits are bounded; on a timeout the kernel
+// sets DSA_DEVERR_TIMEOUT, frees its tensor memory and leaves an empty part
+// (max -inf, sum 0) for the merge.
 #include <cuda_fp16.h>
 #include <math.h>
 
@@ -40,14 +45,13 @@
 #include "gather_internal.cuh"
 #include "tc.cuh"
 
-namespace cg = cooperative_groups;
-
 namespace {
 
 constexpr int NC = 128;                         // selected rows per CTA
-constexpr int MAX_CLUSTER = 16;                 // -> K <= 2048
+constexpr int MAX_CTAS = 16;                    // per (unit, query row) -> K <= 2048
 constexpr int THREADS = 256;
-constexpr int QATOM = 8192;                     // 64 rows x 128 B (query and P atoms)
+constexpr int QATOM = 8192;                     // 64 rows x 128 B (query atoms)
+constexpr int PATOM = 16384;                    // 128 rows x 128 B (P atoms: the 64 rows twice)
 constexpr int BATOM = NC * 128;                 // 128 rows x 128 B (row-tile atoms)
 constexpr int X_OFF = 0;
 constexpr int X_BYTES = NC * DSA_ROW_BYTES;     // 83,968 = 82 KB
@@ -55,13 +59,19 @@ constexpr int Y_OFF = X_BYTES;
 constexpr int Y_BYTES = 9 * BATOM;              // 147,456
 constexpr int MISC_OFF = Y_OFF + Y_BYTES;
 constexpr int SMEM_BYTES = MISC_OFF + 1024;     // 232,448: the whole opt-in budget
-constexpr int OSTR = 516;                       // fp32 row stride of the staged O
 constexpr int TMEM_COLS = 512;
 constexpr uint32_t IDESC_QK = tc::idesc_f16_f32(128, NC, 0, 0);
 constexpr uint32_t IDESC_PV = tc::idesc_f16_f32(128, 256, 0, 1);
+// Partial outputs in the workspace, per (unit, query row) and CTA: O as 16
+// slices of 32 columns, each a contiguous [64 heads][32] block (the merge
+// block of a slice reads one block per CTA), then the 64 row maxima and the
+// 64 row sums.
+constexpr int SLICE = 32;
+constexpr int NSLICE = 512 / SLICE;
+constexpr size_t PART_O = (size_t)64 * 512;     // floats per CTA
+constexpr size_t PART_ML = 128;                 // floats per CTA
 
 static_assert(X_BYTES % 1024 == 0, "region X must keep Y 1024-aligned");
-static_assert(64 * OSTR * 4 <= Y_BYTES, "staged O must fit in Y");
 static_assert(SMEM_BYTES <= 232448, "shared memory budget");
 
 struct Misc {
@@ -79,33 +89,37 @@ struct SoftmaxScratch {
   float pm[2][64];            // partial max per column half
   float pl[2][64];            // partial sum per column half
 };
-constexpr int SMX_OFF = 4 * QATOM;
+constexpr int SMX_OFF = 2 * PATOM;
+static_assert(SMX_OFF + (int)sizeof(SoftmaxScratch) <= X_BYTES, "softmax scratch");
 static_assert(sizeof(Misc) <= 1024, "misc block");
+static_assert(8 * 32 * 36 * 4 <= Y_BYTES, "O transpose buffers");
 
-// Merge-phase scratch, placed in region X once P is no longer needed.
-struct MergeScratch {
-  float rm[MAX_CLUSTER][64];  // every source CTA's max per head
-  float rl[MAX_CLUSTER][64];  // every source CTA's sum per head
-  float f[MAX_CLUSTER][64];   // exp(m_c - M) per source CTA and head
-  float inv[64];              // 1 / L per head
-};
-static_assert(sizeof(MergeScratch) <= X_BYTES, "merge scratch");
-
-// CTAs per cluster for K selected rows: ceil(K / 128) rounded up to a power
-// of two (at most 16 for K <= 2048). The merge splits the 512 output columns
-// evenly over the cluster, so the count must divide 512; the CTAs past the
-// last row hold no rows and add an empty softmax part (max -inf, sum 0).
-inline int cluster_ctas(int K) {
-  const int need = (K + NC - 1) / NC;
-  int C = 1;
-  while (C < need) C *= 2;
-  return C;
-}
+// CTAs per (unit, query row) for K selected rows.
+inline int attn_ctas(int K) { return (K + NC - 1) / NC; }
 
 __device__ __forceinline__ uint32_t pack_h2(float a, float b) {
   const __half2 h = __floats2half2_rn(a, b);
   return *reinterpret_cast<const uint32_t*>(&h);
 }
+
+__device__ __forceinline__ uint32_t prmt(uint32_t a, uint32_t b, uint32_t sel) {
+  uint32_t r;
+  asm("prmt.b32 %0, %1, %2, %3;" : "=r"(r) : "r"(a), "r"(b), "r"(sel));
+  return r;
+}
+
+// Four int8 (one 32-bit word, lowest byte first) times the fp16 scale s2, as
+// two fp16 pairs (bytes 0,1 and 2,3).
+__device__ __forceinline__ void dequant4(uint32_t w, __half2 s2, __half2& lo, __half2& hi) {
+  const uint32_t x = w ^ 0x80808080u;                  // b + 128 per byte
+  const uint32_t a = prmt(x, 0x64646464u, 0x4140u);   // {0x64, b0 + 128}, {0x64, b1 + 128}
+  const uint32_t b = prmt(x, 0x64646464u, 0x4342u);
+  const __half2 off = __half2half2(__ushort_as_half((unsigned short)0x6480u));   // 1152
+  lo = __hmul2(__hsub2(*reinterpret_cast<const __half2*>(&a), off), s2);
+  hi = __hmul2(__hsub2(*reinterpret_cast<const __half2*>(&b), off), s2);
+}
+
+__device__ __forceinline__ uint32_t h2_bits(__half2 v) { return *reinterpret_cast<const uint32_t*>(&v); }
 
 __device__ __forceinline__ void cp_async16(void* dst_smem, const void* src) {
   asm volatile("cp.async.cg.shared.global [%0], [%1], 16;" ::"r"(tc::smem_u32(dst_smem)), "l"(src) : "memory");
@@ -119,12 +133,10 @@ template <bool GATHER>
 __global__ void __launch_bounds__(THREADS, 1)
 k_mla_attn(int R, int H, int K, const uint16_t* __restrict__ q_lat, const uint16_t* __restrict__ q_rope,
            const uint8_t* __restrict__ rows, const int32_t* __restrict__ topk, float scale,
-           float* __restrict__ out, float* __restrict__ lse, float* __restrict__ ws_o, int32_t* dev_err,
+           float* __restrict__ ws_o, float* __restrict__ ws_ml, int32_t* dev_err,
            const dsa_unit* __restrict__ units, const uint8_t* __restrict__ cls, GatherWs g) {
   extern __shared__ __align__(1024) uint8_t sm[];
-  cg::cluster_group cluster = cg::this_cluster();
-  const int C = (int)cluster.num_blocks();
-  const int crank = (int)cluster.block_rank();
+  const int crank = blockIdx.x;
   uint8_t* sX = sm + X_OFF;
   uint8_t* sY = sm + Y_OFF;
   Misc* ms = reinterpret_cast<Misc*>(sm + MISC_OFF);
@@ -147,9 +159,7 @@ k_mla_attn(int R, int H, int K, const uint16_t* __restrict__ q_lat, const uint16
   bool failed = ms->fail != 0;
   pdl_wait();   // everything above touched only this CTA's shared and tensor memory
 
-  // The rows of a CTA arrive by one bulk copy on phase 0 of bar[0]; a CTA
-  // without rows (the cluster is padded to a power of two) issues none, so
-  // the merge's copies below complete phase 0 there and phase 1 elsewhere.
+  // The rows of a CTA arrive by one bulk copy on phase 0 of bar[0].
   const bool rows_copy = !GATHER && !failed && nrows > 0;
   if (rows_copy && tid == 0) {
     const uint32_t bytes = (uint32_t)nrows * DSA_ROW_BYTES;
@@ -231,7 +241,7 @@ k_mla_attn(int R, int H, int K, const uint16_t* __restrict__ q_lat, const uint16
 
   // ---- dequantise the rows: region X (raw) -> region Y (fp16 tile)
   if (!failed) {
-    bool bad = false;
+    __half2 vmax = __float2half2_rn(0.f);   // largest |dequantised value| of this thread
     for (int t = tid; t < NC * 36; t += THREADS) {
       const int j = t % NC, c = t / NC;     // consecutive threads: consecutive rows
       uint4 lo = make_uint4(0, 0, 0, 0), hi = make_uint4(0, 0, 0, 0);
@@ -239,18 +249,16 @@ k_mla_attn(int R, int H, int K, const uint16_t* __restrict__ q_lat, const uint16
         const uint8_t* row = sX + j * DSA_ROW_BYTES;
         uint32_t o[8];
         if (c < 32) {
-          const float s = __half2float(__ushort_as_half(reinterpret_cast<const uint16_t*>(row + 512)[c >> 2]));
+          const __half2 s2 = __half2half2(reinterpret_cast<const __half*>(row + 512)[c >> 2]);
           const uint4 raw = *reinterpret_cast<const uint4*>(row + 16 * c);
           const uint32_t w[4] = {raw.x, raw.y, raw.z, raw.w};
 #pragma unroll
           for (int e = 0; e < 4; ++e) {
-            const float a0 = (float)(int8_t)(w[e] & 0xFF) * s;
-            const float a1 = (float)(int8_t)((w[e] >> 8) & 0xFF) * s;
-            const float a2 = (float)(int8_t)((w[e] >> 16) & 0xFF) * s;
-            const float a3 = (float)(int8_t)(w[e] >> 24) * s;
-            bad |= fmaxf(fmaxf(fabsf(a0), fabsf(a1)), fmaxf(fabsf(a2), fabsf(a3))) >= 65504.f;
-            o[2 * e] = pack_h2(a0, a1);
-            o[2 * e + 1] = pack_h2(a2, a3);
+            __half2 a, b;
+            dequant4(w[e], s2, a, b);
+            vmax = __hmax2(vmax, __hmax2(__habs2(a), __habs2(b)));
+            o[2 * e] = h2_bits(a);
+            o[2 * e + 1] = h2_bits(b);
           }
         } else {
           const uint4 r0 = *reinterpret_cast<const uint4*>(row + 528 + 32 * (c - 32));
@@ -267,7 +275,8 @@ k_mla_attn(int R, int H, int K, const uint16_t* __restrict__ q_lat, const uint16
       *reinterpret_cast<uint4*>(atom + tc::sw128_off(j, d0 & 63)) = lo;
       *reinterpret_cast<uint4*>(atom + tc::sw128_off(j, (d0 & 63) + 8)) = hi;
     }
-    if (bad) dsa_flag(dev_err, DSA_DEVERR_QRANGE);
+    // (a value whose fp16 rounding reaches 65504, including an overflow)
+    if (fmaxf(__low2float(vmax), __high2float(vmax)) >= 65504.f) dsa_flag(dev_err, DSA_DEVERR_QRANGE);
   }
   __syncthreads();   // raw rows are dead: X takes the query block
   if (!failed) {
@@ -355,7 +364,8 @@ k_mla_attn(int R, int H, int K, const uint16_t* __restrict__ q_lat, const uint16
     for (int c8 = 0; c8 < 8; ++c8) {
       const uint4 v = make_uint4(pack_h2(s[8 * c8], s[8 * c8 + 1]), pack_h2(s[8 * c8 + 2], s[8 * c8 + 3]),
                                  pack_h2(s[8 * c8 + 4], s[8 * c8 + 5]), pack_h2(s[8 * c8 + 6], s[8 * c8 + 7]));
-      *reinterpret_cast<uint4*>(sX + half * QATOM + tc::sw128_off(hr, 8 * c8)) = v;
+      *reinterpret_cast<uint4*>(sX + half * PATOM + tc::sw128_off(hr, 8 * c8)) = v;
+      *reinterpret_cast<uint4*>(sX + half * PATOM + tc::sw128_off(hr + 64, 8 * c8)) = v;
     }
     if (half == 0) ms->m[hr] = m;
   }
@@ -371,7 +381,7 @@ k_mla_attn(int R, int H, int K, const uint16_t* __restrict__ q_lat, const uint16
     for (int half = 0; half < 2; ++half) {
 #pragma unroll
       for (int kk = 0; kk < NC / 16; ++kk) {
-        const uint64_t ad = tc::sdesc_sw128(pa + (kk >> 2) * QATOM + (kk & 3) * 32, 16, 1024);
+        const uint64_t ad = tc::sdesc_sw128(pa + (kk >> 2) * PATOM + (kk & 3) * 32, 16, 1024);
         const uint64_t bd = tc::sdesc_sw128(ba + half * 4 * BATOM + kk * 2048, BATOM, 1024);
         tc::mma_f16(tmem + half * 256, ad, bd, IDESC_PV, kk > 0);
       }
@@ -383,107 +393,92 @@ k_mla_attn(int R, int H, int K, const uint16_t* __restrict__ q_lat, const uint16
   __syncthreads();
   failed = ms->fail != 0;
 
-  // ---- this CTA's O (64 x 512 fp32) to its slot of the workspace (L2):
-  //      warps 0,1,4,5 (lane quarters 0 and 1), 128 contiguous bytes per store run
-  //      The slot is slice-major: the W = 512 / C columns that CTA c merges
-  //      form one contiguous [64][W] block, so the merge fetches each source's
-  //      block with one bulk copy. Each 32 x 32 block goes through a padded
-  //      shared-memory transpose so every store writes whole 128-byte rows.
-  const int W = 512 / C;                                 // C in {1, 2, 4, 8, 16}
-  float* gO = ws_o + ((size_t)ur * MAX_CLUSTER + crank) * 64 * 512;
-  if ((warp & 3) < 2 && !failed) {
-    const int q = warp & 3;                              // lane quarter: head rows 32q..32q+31
-    const int c0 = 256 * (warp >> 2);
-    float* tb = reinterpret_cast<float*>(sY) + (2 * (warp >> 2) + q) * 32 * 36;   // [32][36]
-    for (int c = 0; c < 8; ++c) {
+  // ---- this CTA's O (64 x 512 fp32) to its slot of the workspace (L2). Warp
+  //      w reads tensor-memory lane quarter w & 3 (heads 32 * (w & 1) + lane:
+  //      lanes 64..127 repeat 0..63) and 128-column range 2 * (w >> 2) +
+  //      ((w & 3) >> 1). Each 32 x 32 block goes through a padded shared-memory
+  //      transpose so every store writes whole 128-byte rows of a slice.
+  float* gO = ws_o + ((size_t)ur * MAX_CTAS + crank) * PART_O;
+  if (!failed) {
+    const int q = warp & 3;
+    const int hb = 32 * (q & 1);
+    const int c0 = 128 * (2 * (warp >> 2) + (q >> 1));
+    float* tb = reinterpret_cast<float*>(sY) + warp * 32 * 36;   // [32][36]
+    for (int c = 0; c < 4; ++c) {
       float v[32];
-      tc::tmem_ld32(tmem + ((uint32_t)(32 * q) << 16) + c0 + 32 * c, v);
+      const int col = c0 + 32 * c;                       // first column of the block = slice start
+      tc::tmem_ld32(tmem + ((uint32_t)(32 * q) << 16) + col, v);
 #pragma unroll
       for (int i = 0; i < 8; ++i)
         reinterpret_cast<float4*>(tb + lane * 36)[i] = make_float4(v[4 * i], v[4 * i + 1], v[4 * i + 2], v[4 * i + 3]);
       __syncwarp();
-      const int col = c0 + 32 * c;                       // first column of the block
-      float* blk = gO + (size_t)(col / W) * 64 * W + (col % W);
+      float* blk = gO + (size_t)(col / SLICE) * 64 * SLICE;
 #pragma unroll
       for (int r4 = 0; r4 < 8; ++r4) {
         const int r = 4 * r4 + (lane >> 3);              // row within the block
         const float4 x = reinterpret_cast<const float4*>(tb + r * 36)[lane & 7];
-        reinterpret_cast<float4*>(blk + (size_t)(32 * q + r) * W)[lane & 7] = x;
+        reinterpret_cast<float4*>(blk + (size_t)(hb + r) * SLICE)[lane & 7] = x;
       }
       __syncwarp();
     }
   }
-  if (failed && tid < 64) {   // an empty contribution keeps the peers' merge well defined
-    ms->m[tid] = -INFINITY;
-    ms->l[tid] = 0.f;
-  }
-  tc::fence_async_global();   // the partial stores are read by bulk copies
-  tc::fence_before_sync();
-  __syncthreads();
-  cluster.sync();
-  tc::fence_async_global();
-
-  // ---- merge columns [crank*W, crank*W + W) of all C CTAs' outputs: one
-  //      bulk copy per source brings its contiguous [64][W] block into Y
-  {
-    MergeScratch* mg = reinterpret_cast<MergeScratch*>(sX);
-    float* buf = reinterpret_cast<float*>(sY);           // [C][64][W] = 128 KB
-    const uint32_t blk_bytes = 64u * (uint32_t)W * 4u;
-    // (a CTA that already failed issues no copy: nothing of it stays in flight)
-    if (tid == 0 && !failed) {
-      tc::mbar_arrive_expect_tx(&ms->bar[0], blk_bytes * (uint32_t)C);
-      for (int c = 0; c < C; ++c)
-        tc::bulk_g2s(buf + (size_t)c * 64 * W,
-                     ws_o + (((size_t)ur * MAX_CLUSTER + c) * 64 * 512 + (size_t)crank * 64 * W), blk_bytes,
-                     &ms->bar[0]);
-    }
-    // one round of remote loads: every source CTA's (m, l) for every head
-    for (int t = tid; t < C * 64; t += THREADS) {
-      const Misc* rm = cluster.map_shared_rank(ms, t >> 6);
-      mg->rm[t >> 6][t & 63] = rm->m[t & 63];
-      mg->rl[t >> 6][t & 63] = rm->l[t & 63];
-    }
-    __syncthreads();
-    if (tid < 64) {
-      const int h = tid;
-      float M = -INFINITY;
-      for (int c = 0; c < C; ++c) M = fmaxf(M, mg->rm[c][h]);
-      float L = 0.f;
-      for (int c = 0; c < C; ++c) {
-        const float f = mg->rm[c][h] == -INFINITY ? 0.f : __expf(mg->rm[c][h] - M);
-        mg->f[c][h] = f;
-        L += f * mg->rl[c][h];
-      }
-      mg->inv[h] = L > 0.f ? 1.f / L : 0.f;
-      if (crank == 0 && lse && h < H) lse[(size_t)ur * H + h] = L > 0.f ? M + logf(L) : -INFINITY;
-    }
-    const bool got = !failed && tc::mbar_wait(&ms->bar[0], rows_copy ? 1u : 0u);   // the merge copies' phase
-    if (!got) atomicOr(&ms->fail, 1);
-    __syncthreads();
-    const int nq = W / 4;
-    for (int t = tid; t < 64 * nq && got; t += THREADS) {
-      const int h = t / nq, q4 = t % nq;
-      if (h >= H) continue;
-      float4 acc = make_float4(0.f, 0.f, 0.f, 0.f);
-      for (int c = 0; c < C; ++c) {
-        const float f = mg->f[c][h];
-        if (f == 0.f) continue;   // skip empty sources (their blocks may be undefined)
-        const float4 v = reinterpret_cast<const float4*>(buf + ((size_t)c * 64 + h) * W)[q4];
-        acc.x = fmaf(f, v.x, acc.x);
-        acc.y = fmaf(f, v.y, acc.y);
-        acc.z = fmaf(f, v.z, acc.z);
-        acc.w = fmaf(f, v.w, acc.w);
-      }
-      const float inv = mg->inv[h];
-      *reinterpret_cast<float4*>(out + ((size_t)ur * H + h) * 512 + crank * W + 4 * q4) =
-          make_float4(acc.x * inv, acc.y * inv, acc.z * inv, acc.w * inv);
-    }
-    failed = ms->fail != 0;
+  failed = failed || ms->fail != 0;
+  if (tid < 64) {   // a failed CTA leaves an empty part (its O is never read)
+    float* ml = ws_ml + ((size_t)ur * MAX_CTAS + crank) * PART_ML;
+    ml[tid] = failed ? -INFINITY : ms->m[tid];
+    ml[64 + tid] = failed ? 0.f : ms->l[tid];
   }
   if (failed && tid == 0) dsa_flag(dev_err, DSA_DEVERR_TIMEOUT);
   tc::fence_before_sync();
-  cluster.sync();   // peers may still read this CTA's shared memory until here
+  __syncthreads();
+  tc::fence_after_sync();
   if (warp == 0) tc::tmem_dealloc(tmem, TMEM_COLS);
+}
+
+// B: merge of the C parts of one (unit, query row), output columns
+// [32 s, 32 s + 32) with s = blockIdx.x.
+__global__ void __launch_bounds__(256) k_attn_merge(int H, int C, const float* __restrict__ ws_o,
+                                                     const float* __restrict__ ws_ml, float* __restrict__ out,
+                                                     float* __restrict__ lse) {
+  __shared__ float f[MAX_CTAS][64];   // exp(m_c - M) per part and head
+  __shared__ float inv[64];           // 1 / L per head
+  const int s = blockIdx.x, ur = blockIdx.y, tid = threadIdx.x;
+  pdl_wait();
+  const float* ml = ws_ml + (size_t)ur * MAX_CTAS * PART_ML;
+  if (tid < 64) {
+    const int h = tid;
+    float M = -INFINITY;
+    for (int c = 0; c < C; ++c) M = fmaxf(M, ml[c * PART_ML + h]);
+    float L = 0.f;
+    for (int c = 0; c < C; ++c) {
+      const float mc = ml[c * PART_ML + h];
+      const float fc = mc == -INFINITY ? 0.f : __expf(mc - M);
+      f[c][h] = fc;
+      L += fc * ml[c * PART_ML + 64 + h];
+    }
+    inv[h] = L > 0.f ? 1.f / L : 0.f;
+    if (s == 0 && lse && h < H) lse[(size_t)ur * H + h] = L > 0.f ? M + logf(L) : -INFINITY;
+  }
+  __syncthreads();
+  // 64 heads x 8 float4 columns
+  const float* po = ws_o + (size_t)ur * MAX_CTAS * PART_O + (size_t)s * 64 * SLICE;
+  for (int t = tid; t < 64 * (SLICE / 4); t += 256) {
+    const int h = t / (SLICE / 4), q4 = t % (SLICE / 4);
+    if (h >= H) continue;
+    float4 acc = make_float4(0.f, 0.f, 0.f, 0.f);
+    for (int c = 0; c < C; ++c) {
+      const float fc = f[c][h];
+      if (fc == 0.f) continue;   // an empty part (its block may be undefined)
+      const float4 v = reinterpret_cast<const float4*>(po + (size_t)c * PART_O + h * SLICE)[q4];
+      acc.x = fmaf(fc, v.x, acc.x);
+      acc.y = fmaf(fc, v.y, acc.y);
+      acc.z = fmaf(fc, v.z, acc.z);
+      acc.w = fmaf(fc, v.w, acc.w);
+    }
+    const float iv = inv[h];
+    *reinterpret_cast<float4*>(out + ((size_t)ur * H + h) * 512 + s * SLICE + 4 * q4) =
+        make_float4(acc.x * iv, acc.y * iv, acc.z * iv, acc.w * iv);
+  }
 }
 
 }  // namespace
@@ -491,43 +486,34 @@ k_mla_attn(int R, int H, int K, const uint16_t* __restrict__ q_lat, const uint16
 extern "C" size_t mla_decode_attn_workspace(int32_t U, int32_t R, int32_t H, int32_t K) {
   (void)H; (void)K;
   if (U < 1 || R < 1) return 0;
-  return (size_t)U * R * MAX_CLUSTER * 64 * 512 * 4;   // one 64 x 512 fp32 partial per CTA
+  // per (unit, query row): MAX_CTAS partial outputs, then their maxima and sums
+  return (size_t)U * R * MAX_CTAS * (PART_O + PART_ML) * sizeof(float);
 }
 
 namespace {
 
 template <bool GATHER>
 int launch_attn(int32_t U, int32_t R, int32_t H, int32_t K, const uint16_t* q_lat, const uint16_t* q_rope,
-                const uint8_t* rows, const int32_t* topk_idx, float scale, float* out, float* lse, float* ws_o,
+                const uint8_t* rows, const int32_t* topk_idx, float scale, float* out, float* lse, float* ws,
                 int32_t* dev_err, const dsa_unit* units, const uint8_t* cls, GatherWs g, cudaStream_t st) {
   static DsaPerDevice pd;
   int dev = 0;
   const int ok = dsa_device_setup(pd, &dev, [](int) {
     DSA_CUDA_TRY(cudaFuncSetAttribute(k_mla_attn<GATHER>, cudaFuncAttributeMaxDynamicSharedMemorySize, SMEM_BYTES));
-    DSA_CUDA_TRY(cudaFuncSetAttribute(k_mla_attn<GATHER>, cudaFuncAttributeNonPortableClusterSizeAllowed, 1));
     DSA_CUDA_TRY(dsa_prefer_shared(k_mla_attn<GATHER>));
+    DSA_CUDA_TRY(dsa_prefer_shared(k_attn_merge));
     return DSA_OK;
   });
   if (ok != DSA_OK) return ok;
-  const int C = cluster_ctas(K);
-  cudaLaunchConfig_t cfg = {};
-  cfg.gridDim = dim3(C, U * R, 1);
-  cfg.blockDim = dim3(THREADS, 1, 1);
-  cfg.dynamicSmemBytes = SMEM_BYTES;
-  cfg.stream = st;
-  cudaLaunchAttribute attr[2];
-  attr[0].id = cudaLaunchAttributeClusterDimension;
-  attr[0].val.clusterDim.x = C;
-  attr[0].val.clusterDim.y = 1;
-  attr[0].val.clusterDim.z = 1;
-  attr[1].id = cudaLaunchAttributeProgrammaticStreamSerialization;
-  attr[1].val.programmaticStreamSerializationAllowed = 1;
-  cfg.attrs = attr;
-  cfg.numAttrs = 2;
-  if (cudaLaunchKernelEx(&cfg, k_mla_attn<GATHER>, (int)R, (int)H, (int)K, q_lat, q_rope, rows, topk_idx, scale,
-                         out, lse, ws_o, dev_err, units, cls, g) != cudaSuccess)
+  const int C = attn_ctas(K);
+  const size_t UR = (size_t)U * R;
+  float* ws_o = ws;
+  float* ws_ml = ws + UR * MAX_CTAS * PART_O;
+  if (launch_pdl(k_mla_attn<GATHER>, dim3(C, (unsigned)UR), dim3(THREADS), SMEM_BYTES, st, (int)R, (int)H, (int)K,
+                 q_lat, q_rope, rows, topk_idx, scale, ws_o, ws_ml, dev_err, units, cls, g) != DSA_OK)
     return DSA_ERR_CUDA;
-  return dsa_launch_status();
+  return launch_pdl(k_attn_merge, dim3(NSLICE, (unsigned)UR), dim3(256), 0, st, (int)H, C,
+                    static_cast<const float*>(ws_o), static_cast<const float*>(ws_ml), out, lse);
 }
 
 }  // namespace
@@ -538,7 +524,7 @@ extern "C" int mla_decode_attn(int32_t U, int32_t R, int32_t H, int32_t K, const
                                void* ws, size_t ws_bytes, int32_t* dev_err, void* stream) {
   if (!q_lat || !q_rope || !rows || !topk_idx || !out) return DSA_ERR_ARG;
   if (U < 1 || U > 65535 || R < 1 || R > DSA_MAX_ROWS || !(scale > 0.0f)) return DSA_ERR_ARG;
-  if (K < 1 || K > NC * MAX_CLUSTER || H < 16 || H > 64 || (H % 16) != 0) return DSA_ERR_SHAPE;
+  if (K < 1 || K > NC * MAX_CTAS || H < 16 || H > 64 || (H % 16) != 0) return DSA_ERR_SHAPE;
   if ((size_t)U * R > 65535) return DSA_ERR_ARG;
   if (!ws || ws_bytes < mla_decode_attn_workspace(U, R, H, K)) return DSA_ERR_WS;
   // rows and the workspace are read by bulk copies: 16-byte alignment
@@ -559,7 +545,7 @@ extern "C" int hot_gather_attn(const dsa_unit* units, int32_t U, int32_t R, int3
                                size_t ws_bytes, int32_t* dev_err, void* stream) {
   if (!units || !topk_idx || !q_lat || !q_rope || !cls || !counters || !out) return DSA_ERR_ARG;
   if (U < 1 || U > 65535 || R < 1 || R > DSA_MAX_ROWS || !(scale > 0.0f)) return DSA_ERR_ARG;
-  if (K < 1 || K > NC * MAX_CLUSTER || H < 16 || H > 64 || (H % 16) != 0) return DSA_ERR_SHAPE;
+  if (K < 1 || K > NC * MAX_CTAS || H < 16 || H > 64 || (H % 16) != 0) return DSA_ERR_SHAPE;
   if ((size_t)U * R > 65535) return DSA_ERR_ARG;
   if (!ws || ws_bytes < hot_gather_attn_workspace(U, R, H, K)) return DSA_ERR_WS;
   if (reinterpret_cast<uintptr_t>(ws) & 255u) return DSA_ERR_ARG;

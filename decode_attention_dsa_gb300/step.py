@@ -184,5 +184,5 @@ class DecodePath:
 
     def launches_per_step(self) -> int:
         """Kernel launches one step enqueues (score, select, [reuse copy],
-        classify+assign, copy, attention, append)."""
-        return 7 if self.sources else 6
+        classify+assign, copy, attention parts, attention merge, append)."""
+        return 8 if self.sources else 7
