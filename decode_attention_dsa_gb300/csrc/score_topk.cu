@@ -54,26 +54,39 @@ constexpr int SEL_THREADS = 512;
 constexpr int SEL_WARPS = 16;           // SEL_THREADS / 32
 constexpr int SEL_LIST_CAP = 2048;       // keys of bin >= b1 kept per CTA, in order
 constexpr int SEL_WLIST = SEL_LIST_CAP / SEL_WARPS;   // per warp
-constexpr int SEL_UNR = 4;               // 16-byte loads in flight per lane
+constexpr int SEL_GRP_INFLIGHT = 8;      // groups of 32 keys a warp reads at once
 constexpr int SEL_ALL_CAP = 8192;        // candidates per cluster (fast path)
 constexpr int SEL_PER_SRC = SEL_ALL_CAP / SEL_CLUSTER;   // candidates each CTA may push
+
+constexpr int SEL_GROUP = 32;            // keys per group (one warp of the score epilogue)
 
 struct TopkWs {
   uint32_t* hist;   // [U*R][4096]
   uint32_t* keys;   // [U*R][stride]
+  uint32_t* gmax;   // [U*R][stride / 32]: largest key of each group of 32 positions
   uint8_t* tmaps;   // tensor-map slots of the score kernel's CTAs
   int64_t stride;
 };
 
-inline int64_t key_stride(int64_t max_len) { return (max_len + 3) / 4 * 4; }
+// Keys per (unit, row): whole groups, so that every group is one 128-byte line.
+inline int64_t key_stride(int64_t max_len) { return (max_len + SEL_GROUP - 1) / SEL_GROUP * SEL_GROUP; }
+
+inline size_t topk_hist_bytes(int32_t U, int32_t R) { return dsa_align((size_t)U * R * HIST1_BINS * 4, 256); }
+inline size_t topk_keys_bytes(int32_t U, int32_t R, int64_t max_len) {
+  return dsa_align((size_t)U * R * key_stride(max_len) * 4, 256);
+}
+inline size_t topk_gmax_bytes(int32_t U, int32_t R, int64_t max_len) {
+  return dsa_align((size_t)U * R * (key_stride(max_len) / SEL_GROUP) * 4, 256);
+}
 
 inline TopkWs topk_ws(void* ws, int32_t U, int32_t R, int64_t max_len) {
   TopkWs w;
-  w.hist = static_cast<uint32_t*>(ws);
-  size_t hb = dsa_align((size_t)U * R * HIST1_BINS * 4, 256);
-  w.keys = reinterpret_cast<uint32_t*>(static_cast<char*>(ws) + hb);
+  char* b = static_cast<char*>(ws);
+  w.hist = reinterpret_cast<uint32_t*>(b);
+  w.keys = reinterpret_cast<uint32_t*>(b + topk_hist_bytes(U, R));
+  w.gmax = reinterpret_cast<uint32_t*>(b + topk_hist_bytes(U, R) + topk_keys_bytes(U, R, max_len));
   w.stride = key_stride(max_len);
-  w.tmaps = reinterpret_cast<uint8_t*>(w.keys) + dsa_align((size_t)U * R * w.stride * 4, 256);
+  w.tmaps = reinterpret_cast<uint8_t*>(w.gmax) + topk_gmax_bytes(U, R, max_len);
   return w;
 }
 
@@ -181,6 +194,7 @@ struct ScoreArgs {
   const float* w;
   uint32_t* hist;
   uint32_t* okeys;
+  uint32_t* gmax;
   int64_t stride;
   int64_t max_len;
   int tpu;              // tiles per unit
@@ -424,11 +438,12 @@ __global__ void __launch_bounds__(SCORE_THREADS) k_dsa_score(const __grid_consta
           uint32_t d[8];
           tmem_ld8_nowait(tmem + ((uint32_t)(32 * warp) << 16) + (uint32_t)(jp & 1) * 64 + 8 * r, d);
           tmem_ld_wait();
+          uint32_t key = 0u;   // positions past the history count as the smallest key
           if (p < pn) {
             float sc = 0.f;
 #pragma unroll
             for (int h = 0; h < 8; ++h) sc = fmaf(sw[r * 8 + h], fmaxf(__uint_as_float(d[h]), 0.f), sc);
-            const uint32_t key = ordered_key(sc);
+            key = ordered_key(sc);
             a.okeys[((size_t)pu * R + r) * a.stride + (size_t)pt * SCORE_TILE + p] = key;
             const uint32_t bin = key >> 20;
             const unsigned amask = __activemask();
@@ -436,6 +451,14 @@ __global__ void __launch_bounds__(SCORE_THREADS) k_dsa_score(const __grid_consta
             if ((int)(threadIdx.x & 31) == __ffs(peers) - 1)
               atomicAdd(&hs[r * HIST1_BINS + bin], (uint32_t)__popc(peers));
           }
+          // the warp's 32 positions form one group: its largest key lets the
+          // selection skip groups that hold no key of the threshold bin. A
+          // row holds stride / 32 groups; the last tile's groups past it
+          // (positions >= max_len only) have no slot and are not written.
+          const uint32_t gk = __reduce_max_sync(0xffffffffu, key);
+          const int64_t gi = (int64_t)pt * (SCORE_TILE / SEL_GROUP) + warp;
+          if ((tid & 31) == 0 && gi < a.stride / SEL_GROUP)
+            a.gmax[((size_t)pu * R + r) * (a.stride / SEL_GROUP) + gi] = gk;
         }
       } else {
         atomicOr(s_fail, 1);
@@ -546,7 +569,7 @@ static_assert(SEL_WARPS * 32 == SEL_THREADS, "one list per warp");
 
 __global__ void __cluster_dims__(SEL_CLUSTER, 1, 1) __launch_bounds__(SEL_THREADS, 2)
 k_topk_select(const dsa_unit* __restrict__ units, int R, int K, uint32_t* __restrict__ hist,
-              const uint32_t* __restrict__ okeys, int64_t stride, int32_t* __restrict__ topk_idx,
+              const uint32_t* __restrict__ okeys, const uint32_t* __restrict__ gmax, int64_t stride, int32_t* __restrict__ topk_idx,
               int64_t max_len, int32_t* dev_err) {
   cg::cluster_group cluster = cg::this_cluster();
   const int crank = (int)cluster.block_rank();
@@ -575,8 +598,8 @@ k_topk_select(const dsa_unit* __restrict__ units, int R, int K, uint32_t* __rest
   uint32_t* lkey = reinterpret_cast<uint32_t*>(lpos + SEL_LIST_CAP);          // [SEL_LIST_CAP]
   uint32_t* allc = reinterpret_cast<uint32_t*>(smem_sel + SEL_ALLC_OFF);      // [SEL_ALL_CAP]
   const int tid = threadIdx.x;
-  // this CTA's key range, a multiple of 4 keys (16-byte aligned bulk copies)
-  const int64_t chunk = ((L + SEL_CLUSTER - 1) / SEL_CLUSTER + 3) / 4 * 4;
+  // this CTA's key range: whole groups of 32 keys (a trailing range may be empty)
+  const int64_t chunk = ((L + SEL_CLUSTER - 1) / SEL_CLUSTER + SEL_GROUP - 1) / SEL_GROUP * SEL_GROUP;
   const int64_t beg = min((int64_t)crank * chunk, L);
   const int64_t end = min(beg + chunk, L);
   const uint32_t* kk = okeys + (size_t)ur * stride;
@@ -620,70 +643,71 @@ k_topk_select(const dsa_unit* __restrict__ units, int R, int K, uint32_t* __rest
   };
 
   asm volatile("barrier.cluster.wait.aligned;" ::: "memory");
-  // candidates go to region [crank] of every CTA's candidate buffer
-  uint32_t* dst[SEL_CLUSTER];
-#pragma unroll
-  for (int c = 0; c < SEL_CLUSTER; ++c) dst[c] = cluster.map_shared_rank(allc, c) + crank * SEL_PER_SRC;
+  // candidates go to region [crank] of every CTA's candidate buffer (the
+  // remote addresses are formed where a candidate is pushed: it is rare, and
+  // the pass keeps its registers for loads in flight)
+  uint32_t* const own_region = allc + crank * SEL_PER_SRC;
 
   // ---- one pass over the range: count the keys above bin b1, push the
   //      candidates inside b1 to the cluster, and keep every key of bin >= b1
-  //      with its position in an ordered list. Warp w owns a contiguous part
-  //      of the range and its own list (lane order within a group of 32
-  //      quads, groups in increasing position), so the warps' lists,
-  //      concatenated in warp order, are ordered; no block barrier is needed.
+  //      with its position in an ordered list. The range is read in groups of
+  //      32 positions (one 128-byte line each); a group whose largest key
+  //      (written by the score kernel) lies below bin b1 holds nothing of
+  //      interest and is not read at all. Warp w owns a contiguous run of
+  //      groups and its own list, filled in position order, so the warps'
+  //      lists concatenated in warp order are ordered; no block barrier is
+  //      needed.
   const int warp = tid >> 5, lane = tid & 31;
-  const int64_t nq = q1 - q0;
-  const int64_t qpw = (nq + SEL_WARPS - 1) / SEL_WARPS;
-  const int64_t wq0 = min(q0 + (int64_t)warp * qpw, q1), wq1 = min(wq0 + qpw, q1);
+  const int64_t gr0 = beg / SEL_GROUP, gr1 = (end + SEL_GROUP - 1) / SEL_GROUP;   // beg: whole groups
+  const int64_t gpw = (gr1 - gr0 + SEL_WARPS - 1) / SEL_WARPS;
+  const int64_t wg0 = min(gr0 + (int64_t)warp * gpw, gr1), wg1 = min(wg0 + gpw, gr1);
+  const uint32_t* gm = gmax + (size_t)ur * (stride / SEL_GROUP);
+  const uint32_t kb1 = b1 << 20;     // smallest key of bin b1
   int32_t* wpos = lpos + warp * SEL_WLIST;
   uint32_t* wkey = lkey + warp * SEL_WLIST;
   long long gt1 = 0;
   int wn = 0;          // entries of this warp's list so far (may pass SEL_WLIST)
-  for (int64_t qb = wq0; qb < wq1; qb += 32 * SEL_UNR) {
-    uint4 v[SEL_UNR];
+  const unsigned lt_mask = (1u << lane) - 1u;
+  for (int64_t gb = wg0; gb < wg1; gb += 32) {
+    // lane i looks at group gb + i; `pass` marks the groups to read
+    const int64_t gi = gb + lane;
+    const uint32_t gmx = gi < wg1 ? __ldcg(gm + gi) : 0u;
+    unsigned pass = __ballot_sync(0xffffffffu, gi < wg1 && gmx >= kb1);
+    while (pass) {
+      // up to SEL_GRP_INFLIGHT of the marked groups in flight at once, in order
+      int gidx[SEL_GRP_INFLIGHT];
+      uint32_t kv[SEL_GRP_INFLIGHT];
 #pragma unroll
-    for (int k = 0; k < SEL_UNR; ++k) {
-      const int64_t q = qb + 32 * k + lane;
-      v[k] = q < wq1 ? key4(q) : make_uint4(0, 0, 0, 0);
-    }
+      for (int i = 0; i < SEL_GRP_INFLIGHT; ++i) {
+        gidx[i] = pass ? __ffs(pass) - 1 : -1;
+        pass &= pass - 1u;
+        kv[i] = gidx[i] >= 0 ? __ldcg(kk + (gb + gidx[i]) * SEL_GROUP + lane) : 0u;
+      }
 #pragma unroll
-    for (int k = 0; k < SEL_UNR; ++k) {
-      const int64_t q = qb + 32 * k + lane;
-      const uint32_t w[4] = {v[k].x, v[k].y, v[k].z, v[k].w};
-      int c = 0;
-#pragma unroll
-      for (int e = 0; e < 4; ++e) {
-        const bool in = q < wq1 && 4 * q + e < end;
-        const uint32_t d1 = w[e] >> 20;
-        gt1 += in && d1 > b1;
-        c += in && d1 >= b1;
-        if (in && d1 == b1) {
+      for (int i = 0; i < SEL_GRP_INFLIGHT; ++i) {
+        if (gidx[i] < 0) break;   // warp-uniform
+        const int64_t pos = (gb + gidx[i]) * SEL_GROUP + lane;
+        const uint32_t key = kv[i];
+        const bool in = pos >= beg && pos < end;
+        gt1 += in && (key >> 20) > b1;
+        if (in && (key >> 20) == b1) {
           const int kc = atomicAdd(&S->ncand, 1);
           if (kc < SEL_PER_SRC) {
 #pragma unroll
-            for (int cc = 0; cc < SEL_CLUSTER; ++cc) dst[cc][kc] = w[e];
+            for (int cc = 0; cc < SEL_CLUSTER; ++cc) cluster.map_shared_rank(own_region, cc)[kc] = key;
           }
         }
-      }
-      // this lane's offset in the warp's list: exclusive prefix over lanes
-      int inc = c;
-#pragma unroll
-      for (int o = 1; o < 32; o <<= 1) {
-        const int y = __shfl_up_sync(0xffffffffu, inc, o);
-        if (lane >= o) inc += y;
-      }
-      int o = wn + inc - c;
-#pragma unroll
-      for (int e = 0; e < 4; ++e) {
-        if (q < wq1 && 4 * q + e < end && (w[e] >> 20) >= b1) {
+        const bool take = in && key >= kb1;
+        const unsigned tm = __ballot_sync(0xffffffffu, take);
+        if (take) {
+          const int o = wn + __popc(tm & lt_mask);
           if (o < SEL_WLIST) {
-            wpos[o] = (int32_t)(4 * q + e);
-            wkey[o] = w[e];
+            wpos[o] = (int32_t)pos;
+            wkey[o] = key;
           }
-          ++o;
         }
+        wn += __popc(tm);
       }
-      wn += __shfl_sync(0xffffffffu, inc, 31);
     }
   }
   if (lane == 0) S->wcnt[warp] = wn;
@@ -926,8 +950,8 @@ int encode_template(int dev) {
 
 extern "C" size_t dsa_score_topk_workspace(int32_t U, int32_t R, int64_t max_len) {
   if (U < 1 || R < 1 || max_len < 0) return 0;
-  return dsa_align((size_t)U * R * HIST1_BINS * 4, 256) +
-         dsa_align((size_t)U * R * key_stride(max_len) * 4, 256) + SCORE_TMAP_BYTES;
+  return topk_hist_bytes(U, R) + topk_keys_bytes(U, R, max_len) + topk_gmax_bytes(U, R, max_len) +
+         SCORE_TMAP_BYTES;
 }
 
 extern "C" int dsa_score_topk(const dsa_unit* units, int32_t U, int32_t R, int32_t K,
@@ -972,6 +996,7 @@ extern "C" int dsa_score_topk(const dsa_unit* units, int32_t U, int32_t R, int32
     a.w = w;
     a.hist = tw.hist;
     a.okeys = tw.keys;
+    a.gmax = tw.gmax;
     a.stride = tw.stride;
     a.max_len = max_len;
     a.tpu = (int)tpu;
@@ -988,7 +1013,7 @@ extern "C" int dsa_score_topk(const dsa_unit* units, int32_t U, int32_t R, int32
       return DSA_ERR_CUDA;
   }
   return launch_pdl(k_topk_select, dim3(SEL_CLUSTER, U * R), dim3(SEL_THREADS), select_smem(), st, units, R,
-                    K, tw.hist, tw.keys, tw.stride, topk_idx, max_len, dev_err);
+                    K, tw.hist, tw.keys, tw.gmax, tw.stride, topk_idx, max_len, dev_err);
 }
 
 // ---------------------------------------------------------------------------
@@ -1041,8 +1066,10 @@ namespace {
 constexpr int64_t NOALLOC_MAX_UR = 16;          // units x query rows per call
 constexpr int64_t NOALLOC_MAX_LEN = 65536;      // history positions per unit
 constexpr size_t NOALLOC_HIST_BYTES = (size_t)NOALLOC_MAX_UR * HIST1_BINS * 4;   // 256 KiB
-constexpr size_t NOALLOC_BYTES =
-    NOALLOC_HIST_BYTES + (size_t)NOALLOC_MAX_UR * NOALLOC_MAX_LEN * 4 + SCORE_TMAP_BYTES;   // 5.25 MiB
+// histograms, ordered keys (4 MiB), group maxima (128 KiB), tensor-map slots
+// (1 MiB); each part a multiple of 256 bytes at these limits
+constexpr size_t NOALLOC_BYTES = NOALLOC_HIST_BYTES + (size_t)NOALLOC_MAX_UR * NOALLOC_MAX_LEN * 4 +
+                                 (size_t)NOALLOC_MAX_UR * (NOALLOC_MAX_LEN / SEL_GROUP) * 4 + SCORE_TMAP_BYTES;
 static __device__ __align__(256) uint8_t g_topk_scratch[NOALLOC_BYTES];
 
 // Device address of g_topk_scratch, per device ordinal (looked up once, under

@@ -230,7 +230,7 @@ int dsa_score_topk(const dsa_unit* units, int32_t U, int32_t R, int32_t K,
  * entry point; it computes exactly what dsa_score_topk computes (same
  * arguments minus ws/ws_bytes) and enqueues the same kernels.
  *
- * Its scratch is one array of 4.25 MiB compiled into this library (device
+ * Its scratch is one array of 5.375 MiB compiled into this library (device
  * memory that every GPU which loads the library keeps until the process
  * exits). Limits: U * R <= 16 and max_len <= 65,536; larger problems return
  * DSA_ERR_SCRATCH_LIMIT and enqueue nothing.
