@@ -54,7 +54,8 @@ constexpr int SEL_THREADS = 512;
 constexpr int SEL_WARPS = 16;           // SEL_THREADS / 32
 constexpr int SEL_LIST_CAP = 2048;       // keys of bin >= b1 kept per CTA, in order
 constexpr int SEL_WLIST = SEL_LIST_CAP / SEL_WARPS;   // per warp
-constexpr int SEL_GRP_INFLIGHT = 8;      // groups of 32 keys a warp reads at once
+constexpr int SEL_ROUND = 256;           // groups of 32 keys a warp screens per round (8 per lane)
+constexpr int SEL_NLD = 4;               // 16-byte loads in flight per lane: 16 groups per warp
 constexpr int SEL_ALL_CAP = 8192;        // candidates per cluster (fast path)
 constexpr int SEL_PER_SRC = SEL_ALL_CAP / SEL_CLUSTER;   // candidates each CTA may push
 
@@ -553,7 +554,9 @@ struct SelShared {
   int bin, above;
   int ncand;
   int wcnt[SEL_WARPS];        // entries of each warp's list (above SEL_WLIST: it overflowed)
-  int woff[SEL_WARPS + 1];    // their prefix: warp w's entries are list entries [woff[w], woff[w+1])
+  int wgt[SEL_WARPS];         // keys of each warp's range above bin b1
+  int wg[SEL_WARPS], we[SEL_WARPS];   // entries of each warp's list above / at the threshold key
+  int csum[2];                // this CTA's candidates above / at the threshold key
   int srcn[SEL_CLUSTER];      // candidates pushed here by each CTA (-1: it overflowed)
   long long rcnt[SEL_CLUSTER][2];   // (gt, eq) of each CTA, read once for the prefix
   long long cnt[2];           // this CTA's (gt, eq) counts
@@ -564,7 +567,8 @@ struct SelShared {
 constexpr size_t SEL_H_OFF = (sizeof(SelShared) + 127) / 128 * 128;
 constexpr size_t SEL_LIST_OFF = SEL_H_OFF + (size_t)HIST1_BINS * 4;
 constexpr size_t SEL_ALLC_OFF = SEL_LIST_OFF + (size_t)SEL_LIST_CAP * 8;
-constexpr size_t SEL_SMEM = SEL_ALLC_OFF + (size_t)SEL_ALL_CAP * 4;
+constexpr size_t SEL_GL_OFF = SEL_ALLC_OFF + (size_t)SEL_ALL_CAP * 4;
+constexpr size_t SEL_SMEM = SEL_GL_OFF + (size_t)SEL_WARPS * SEL_ROUND * 4;
 static_assert(SEL_WARPS * 32 == SEL_THREADS, "one list per warp");
 
 __global__ void __cluster_dims__(SEL_CLUSTER, 1, 1) __launch_bounds__(SEL_THREADS, 2)
@@ -609,6 +613,26 @@ k_topk_select(const dsa_unit* __restrict__ units, int R, int K, uint32_t* __rest
     S->ncand = 0;
   }
 
+  // Warp w owns a contiguous run of groups of 32 positions; the largest
+  // key of each group of its first round is loaded now (8 per lane, all in
+  // flight) and lands while the histogram is scanned.
+  const int warp = tid >> 5, lane = tid & 31;
+  // (positions and group indices of one unit fit in 32 bits: L < 2^31)
+  const int begi = (int)beg, endi = (int)end;
+  const int gr0 = begi / SEL_GROUP, gr1 = (endi + SEL_GROUP - 1) / SEL_GROUP;   // beg: whole groups
+  const int gpw = (gr1 - gr0 + SEL_WARPS - 1) / SEL_WARPS;
+  const int wg0 = min(gr0 + warp * gpw, gr1), wg1 = min(wg0 + gpw, gr1);
+  const uint32_t* gm = gmax + (size_t)ur * (stride / SEL_GROUP);
+  uint32_t gmr[SEL_ROUND / 32];
+  auto load_round = [&](int rb) {
+#pragma unroll
+    for (int j = 0; j < SEL_ROUND / 32; ++j) {
+      const int gi = rb + 32 * j + lane;
+      gmr[j] = gi < wg1 ? __ldcg(gm + gi) : 0u;
+    }
+  };
+  load_round(wg0);
+
   // ---- level 1: top 12 bits from the global histogram (read in place)
   uint32_t* gh = hist + (size_t)ur * HIST1_BINS;
   find_digit_wide<SEL_THREADS>(gh, HIST1_BINS, K, S->tmp, &S->bin, &S->above);
@@ -650,85 +674,104 @@ k_topk_select(const dsa_unit* __restrict__ units, int R, int K, uint32_t* __rest
 
   // ---- one pass over the range: count the keys above bin b1, push the
   //      candidates inside b1 to the cluster, and keep every key of bin >= b1
-  //      with its position in an ordered list. The range is read in groups of
-  //      32 positions (one 128-byte line each); a group whose largest key
-  //      (written by the score kernel) lies below bin b1 holds nothing of
-  //      interest and is not read at all. Warp w owns a contiguous run of
-  //      groups and its own list, filled in position order, so the warps'
-  //      lists concatenated in warp order are ordered; no block barrier is
-  //      needed.
-  const int warp = tid >> 5, lane = tid & 31;
-  const int64_t gr0 = beg / SEL_GROUP, gr1 = (end + SEL_GROUP - 1) / SEL_GROUP;   // beg: whole groups
-  const int64_t gpw = (gr1 - gr0 + SEL_WARPS - 1) / SEL_WARPS;
-  const int64_t wg0 = min(gr0 + (int64_t)warp * gpw, gr1), wg1 = min(wg0 + gpw, gr1);
-  const uint32_t* gm = gmax + (size_t)ur * (stride / SEL_GROUP);
+  //      with its position in an ordered list. Per round of 256 groups a
+  //      warp lists, in order, the groups whose largest key reaches bin b1
+  //      (the score kernel wrote these maxima; the other groups hold nothing
+  //      of interest and are not read), then reads the listed groups 16 at
+  //      a time, 8 lanes x 16 bytes per group. The warp's own list of keys
+  //      is filled in position order, so the warps' lists concatenated in
+  //      warp order are ordered; no block barrier is needed.
   const uint32_t kb1 = b1 << 20;     // smallest key of bin b1
   int32_t* wpos = lpos + warp * SEL_WLIST;
   uint32_t* wkey = lkey + warp * SEL_WLIST;
+  int32_t* wgl = reinterpret_cast<int32_t*>(smem_sel + SEL_GL_OFF) + warp * SEL_ROUND;
   long long gt1 = 0;
   int wn = 0;          // entries of this warp's list so far (may pass SEL_WLIST)
   const unsigned lt_mask = (1u << lane) - 1u;
-  for (int64_t gb = wg0; gb < wg1; gb += 32) {
-    // lane i looks at group gb + i; `pass` marks the groups to read
-    const int64_t gi = gb + lane;
-    const uint32_t gmx = gi < wg1 ? __ldcg(gm + gi) : 0u;
-    unsigned pass = __ballot_sync(0xffffffffu, gi < wg1 && gmx >= kb1);
-    while (pass) {
-      // up to SEL_GRP_INFLIGHT of the marked groups in flight at once, in order
-      int gidx[SEL_GRP_INFLIGHT];
-      uint32_t kv[SEL_GRP_INFLIGHT];
+  const int seg = lane >> 3, sl = lane & 7;   // group slot of a load, 16-byte piece of the group
+  for (int rb = wg0; rb < wg1; rb += SEL_ROUND) {
+    if (rb != wg0) load_round(rb);
+    int ng = 0;
 #pragma unroll
-      for (int i = 0; i < SEL_GRP_INFLIGHT; ++i) {
-        gidx[i] = pass ? __ffs(pass) - 1 : -1;
-        pass &= pass - 1u;
-        kv[i] = gidx[i] >= 0 ? __ldcg(kk + (gb + gidx[i]) * SEL_GROUP + lane) : 0u;
+    for (int j = 0; j < SEL_ROUND / 32; ++j) {
+      const int gi = rb + 32 * j + lane;
+      const bool hit = gi < wg1 && gmr[j] >= kb1;
+      const unsigned m = __ballot_sync(0xffffffffu, hit);
+      if (hit) wgl[ng + __popc(m & lt_mask)] = gi - rb;
+      ng += __popc(m);
+    }
+    __syncwarp();
+    for (int e0 = 0; e0 < ng; e0 += 4 * SEL_NLD) {
+      uint4 v[SEL_NLD];
+#pragma unroll
+      for (int k = 0; k < SEL_NLD; ++k) {
+        const int e = e0 + 4 * k + seg;
+        v[k] = e < ng ? __ldcg(reinterpret_cast<const uint4*>(kk + (size_t)(rb + wgl[e]) * SEL_GROUP) + sl)
+                      : make_uint4(0u, 0u, 0u, 0u);
       }
 #pragma unroll
-      for (int i = 0; i < SEL_GRP_INFLIGHT; ++i) {
-        if (gidx[i] < 0) break;   // warp-uniform
-        const int64_t pos = (gb + gidx[i]) * SEL_GROUP + lane;
-        const uint32_t key = kv[i];
-        const bool in = pos >= beg && pos < end;
-        gt1 += in && (key >> 20) > b1;
-        if (in && (key >> 20) == b1) {
-          const int kc = atomicAdd(&S->ncand, 1);
-          if (kc < SEL_PER_SRC) {
+      for (int k = 0; k < SEL_NLD; ++k) {
+        if (e0 + 4 * k >= ng) break;   // warp-uniform
+        const int e = e0 + 4 * k + seg;
+        const int p0 = e < ng ? (rb + wgl[e]) * SEL_GROUP + 4 * sl : -1;
+        const uint32_t w[4] = {v[k].x, v[k].y, v[k].z, v[k].w};
+        int c = 0;
 #pragma unroll
-            for (int cc = 0; cc < SEL_CLUSTER; ++cc) cluster.map_shared_rank(own_region, cc)[kc] = key;
+        for (int q = 0; q < 4; ++q) {
+          const int pos = p0 + q;
+          const bool in = p0 >= 0 && pos >= begi && pos < endi;
+          gt1 += in && (w[q] >> 20) > b1;
+          c += in && w[q] >= kb1;
+          if (in && (w[q] >> 20) == b1) {
+            const int kc = atomicAdd(&S->ncand, 1);
+            if (kc < SEL_PER_SRC) {
+#pragma unroll
+              for (int cc = 0; cc < SEL_CLUSTER; ++cc) cluster.map_shared_rank(own_region, cc)[kc] = w[q];
+            }
           }
         }
-        const bool take = in && key >= kb1;
-        const unsigned tm = __ballot_sync(0xffffffffu, take);
-        if (take) {
-          const int o = wn + __popc(tm & lt_mask);
-          if (o < SEL_WLIST) {
-            wpos[o] = (int32_t)pos;
-            wkey[o] = key;
+        // lanes hold consecutive pieces of consecutive listed groups, so an
+        // exclusive prefix over the lanes gives each taken key its place
+        int inc = c;
+#pragma unroll
+        for (int o = 1; o < 32; o <<= 1) {
+          const int y = __shfl_up_sync(0xffffffffu, inc, o);
+          if (lane >= o) inc += y;
+        }
+        int o = wn + inc - c;
+#pragma unroll
+        for (int q = 0; q < 4; ++q) {
+          const int pos = p0 + q;
+          if (p0 >= 0 && pos >= begi && pos < endi && w[q] >= kb1) {
+            if (o < SEL_WLIST) {
+              wpos[o] = pos;
+              wkey[o] = w[q];
+            }
+            ++o;
           }
         }
-        wn += __popc(tm);
+        wn += __shfl_sync(0xffffffffu, inc, 31);
       }
     }
+    __syncwarp();   // the group list is rewritten by the next round
   }
-  if (lane == 0) S->wcnt[warp] = wn;
-  __syncthreads();
-  if (tid == 0) {
-    int acc = 0;
-    for (int i = 0; i < SEL_WARPS; ++i) {
-      S->woff[i] = acc;
-      acc += min(S->wcnt[i], SEL_WLIST);
+  {
+    const int gw = __reduce_add_sync(0xffffffffu, (int)gt1);
+    if (lane == 0) {
+      S->wcnt[warp] = wn;
+      S->wgt[warp] = gw;
     }
-    S->woff[SEL_WARPS] = acc;
+    if (tid < 2) S->csum[tid] = 0;
   }
   __syncthreads();
   bool list_ok = true;
-  for (int i = 0; i < SEL_WARPS; ++i) list_ok &= S->wcnt[i] <= SEL_WLIST;
-  const int lbase = S->woff[SEL_WARPS];
-  int gt1_cta;
-  block_inclusive_scan<SEL_THREADS>((int)gt1, S->tmp, &gt1_cta);
+  int gt1_cta = 0;
+  for (int i = 0; i < SEL_WARPS; ++i) {
+    list_ok &= S->wcnt[i] <= SEL_WLIST;
+    gt1_cta += S->wgt[i];
+  }
   if (tid < SEL_CLUSTER)
     cluster.map_shared_rank(S, tid)->srcn[crank] = S->ncand > SEL_PER_SRC ? -1 : S->ncand;
-  __syncthreads();
   cluster.sync();
   if (crank == 0) {
     // every CTA read the global histogram before the barrier: clear it for the next call
@@ -749,11 +792,21 @@ k_topk_select(const dsa_unit* __restrict__ units, int R, int K, uint32_t* __rest
     // ---- every CTA holds all candidates (pushed into per-source regions):
     //      exact local radix select on bits 19..8 and 7..0
     for (int i = tid; i < HIST1_BINS; i += SEL_THREADS) h1[i] = 0;
+    // the valid candidates, flattened: source c's are entries [off[c], off[c + 1])
+    int off[SEL_CLUSTER + 1];
+    off[0] = 0;
+#pragma unroll
+    for (int c = 0; c < SEL_CLUSTER; ++c) off[c + 1] = off[c] + S->srcn[c];
+    auto cand = [&](int i) -> uint32_t {
+      int c = 0;
+#pragma unroll
+      for (int cc = 1; cc < SEL_CLUSTER; ++cc) c += i >= off[cc];
+      return allc[c * SEL_PER_SRC + (i - off[c])];
+    };
     __syncthreads();
     const uint32_t p1 = b1 << 20;
-    for (int i = tid; i < SEL_ALL_CAP; i += SEL_THREADS) {
-      if ((i % SEL_PER_SRC) >= S->srcn[i / SEL_PER_SRC]) continue;
-      const uint32_t key = allc[i];
+    for (int i = tid; i < total; i += SEL_THREADS) {
+      const uint32_t key = cand(i);
       if ((key & 0xFFF00000u) == p1) atomicAdd(&h1[(key >> 8) & 0xFFF], 1u);
     }
     __syncthreads();
@@ -762,9 +815,8 @@ k_topk_select(const dsa_unit* __restrict__ units, int R, int K, uint32_t* __rest
     const uint32_t p2 = p1 | ((uint32_t)S->bin << 8);
     for (int i = tid; i < 256; i += SEL_THREADS) S->hg[i] = 0;
     __syncthreads();
-    for (int i = tid; i < SEL_ALL_CAP; i += SEL_THREADS) {
-      if ((i % SEL_PER_SRC) >= S->srcn[i / SEL_PER_SRC]) continue;
-      const uint32_t key = allc[i];
+    for (int i = tid; i < total; i += SEL_THREADS) {
+      const uint32_t key = cand(i);
       if ((key & 0xFFFFFF00u) == p2) atomicAdd(&S->hg[key & 0xFF], 1u);
     }
     __syncthreads();
@@ -780,11 +832,15 @@ k_topk_select(const dsa_unit* __restrict__ units, int R, int K, uint32_t* __rest
       g += own[i] > T;
       e += own[i] == T;
     }
-    int gtot, etot;
-    block_inclusive_scan<SEL_THREADS>(g, S->tmp, &gtot);
-    block_inclusive_scan<SEL_THREADS>(e, S->tmp, &etot);
-    gt_cta = (long long)gt1_cta + gtot;
-    eq_cta = etot;
+    g = __reduce_add_sync(0xffffffffu, g);
+    e = __reduce_add_sync(0xffffffffu, e);
+    if (lane == 0 && (g | e)) {
+      atomicAdd(&S->csum[0], g);
+      atomicAdd(&S->csum[1], e);
+    }
+    __syncthreads();
+    gt_cta = (long long)gt1_cta + S->csum[0];
+    eq_cta = S->csum[1];
   } else {
     // ---- refinement passes with cluster-summed histograms (8, 8, 4 bits)
     long long local_gt = gt1_cta;
@@ -892,18 +948,44 @@ k_topk_select(const dsa_unit* __restrict__ units, int R, int K, uint32_t* __rest
     }
   };
   if (list_ok) {
-    // entry i of the concatenated list: warp segment w with woff[w] <= i < woff[w + 1]
-    compact(lbase, [&](int64_t i, int32_t& p, uint32_t& k) {
-      p = -1;
-      k = 0u;
-      if (i < lbase) {
-        int w = 0;
-        while (w + 1 < SEL_WARPS && S->woff[w + 1] <= i) ++w;
-        const int j = (int)(i - S->woff[w]);
-        p = lpos[w * SEL_WLIST + j];
-        k = lkey[w * SEL_WLIST + j];
-      }
-    });
+    // Every warp walks its own list (in position order; the warps' lists
+    // follow each other in position order). Its place in the CTA's output
+    // and its first tie rank come from the counts of the warps before it.
+    const int nw = S->wcnt[warp];
+    int g = 0, e = 0;
+    for (int j = lane; j < nw; j += 32) {
+      const uint32_t k = wkey[j];
+      g += k > T;
+      e += k == T;
+    }
+    g = __reduce_add_sync(0xffffffffu, g);
+    e = __reduce_add_sync(0xffffffffu, e);
+    if (lane == 0) {
+      S->wg[warp] = g;
+      S->we[warp] = e;
+    }
+    __syncthreads();
+    long long eqb = eq_before, selb = sel_before;
+    for (int i = 0; i < warp; ++i) {
+      const long long ei = S->we[i];
+      long long take = (long long)ties - eqb;
+      take = take < 0 ? 0 : (take > ei ? ei : take);
+      selb += S->wg[i] + take;
+      eqb += ei;
+    }
+    for (int j0 = 0; j0 < nw; j0 += 32) {
+      const int j = j0 + lane;
+      const bool v = j < nw;
+      const uint32_t k = v ? wkey[j] : 0u;
+      const bool eq = v && k == T;
+      const unsigned em = __ballot_sync(0xffffffffu, eq);
+      const bool pick = (v && k > T) || (eq && eqb + __popc(em & lt_mask) < ties);
+      const unsigned pm = __ballot_sync(0xffffffffu, pick);
+      const long long o = selb + __popc(pm & lt_mask);
+      if (pick && o < K) out[o] = wpos[j];
+      selb += __popc(pm);
+      eqb += __popc(em);
+    }
   } else {
     const int64_t nq = q1 - q0;   // the whole range, 4 keys per quad from global memory
     compact(4 * nq, [&](int64_t i, int32_t& p, uint32_t& k) {
