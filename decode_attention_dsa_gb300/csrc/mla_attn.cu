@@ -8,36 +8,41 @@
 // 15+ x 1M", section "起点": a row is 512 B latent + 16 B scales + 128 B RoPE.
 //
 // Two launches per call:
-//  A. k_mla_attn: ceil(K / 128) CTAs per (unit, query row); CTA c owns the
-//     selected rows [128c, 128c + 128):
-//  1. one 1-D bulk TMA copy brings the CTA's rows (up to 128 x 656 B) into
-//     shared memory region X;
-//  2. dequantisation writes an fp16 tile [128 rows][576] (latent int8 * fp16
-//     scale rounded once to fp16; RoPE bf16 -> fp16) in the K-major
-//     128-byte-swizzled layout into region Y. The same bytes serve as the
-//     K-major B operand of S = Q K^T and, read as an MN-major operand, as the
-//     B operand of O = P V;
-//  3. the query block (64 heads x 576, bf16 -> fp16) goes into X;
-//  4. tcgen05.mma kind::f16, M = 128 (heads, 64 real), N = 128 for S and
-//     2 x 256 for O, fp32 accumulators in tensor memory, one issuing thread,
-//     completion through tcgen05.commit on an mbarrier;
-//  5. softmax of the CTA's 128 columns per head in registers; P (fp16) goes to
-//     X as the A operand of PV, its 64 head rows written twice (rows 64..127
-//     repeat them) so that tensor-memory lanes 64..127 of O repeat lanes
-//     0..63 and all eight warps can read O out;
-//  6. the CTA's O (64 x 512 fp32), row max and row sum go to its slot of the
-//     workspace (they stay in L2).
+//  A. k_attn_parts: the K selected rows of a (unit, query row) are cut into
+//     chunks of 64 and the chunks into `parts` contiguous runs, one CTA per
+//     run (runs sized so that all CTAs fill the GPU once). A CTA keeps the
+//     query block (64 heads x 576, fp16) in shared memory and, per chunk:
+//  1. one 1-D bulk TMA copy brings the chunk's rows (up to 64 x 656 B) into a
+//     staging buffer; the copy of the next chunk is issued as soon as this
+//     chunk is dequantised, so it lands while this chunk's products run;
+//  2. dequantisation writes an fp16 tile [64 rows][576] (latent int8 * fp16
+//     scale rounded once to fp16; RoPE bf16 -> fp16), 128-byte swizzled;
+//  3. S = Q K^T on the tensor cores (tcgen05.mma kind::f16, M = 128: the 64
+//     heads, the other 64 lanes unused; N = 64 rows, K = 576; fp32 in tensor
+//     memory);
+//  4. an online softmax per head (a thread holds one head and 32 rows). The
+//     running maximum of a head moves only when a chunk exceeds it by more
+//     than TAU, so P = exp(x - m) stays below e^TAU in fp16 and the
+//     accumulated output is rescaled only then;
+//  5. P (fp16, [64 heads][64 rows]) goes over the tile's RoPE part, which S
+//     no longer needs, and O^T += V^T P^T accumulates in tensor memory
+//     (M = 128 latent dims per block, 4 blocks, N = 64 heads, K = 64 rows):
+//     the tile is the K-major B operand of the first product and the
+//     MN-major A operand of the second.
+//     The run's O (64 x 512 fp32, unnormalised), running maxima and sums go to
+//     the run's slot of the workspace (they stay in L2).
 //  B. k_attn_merge: one block per (unit, query row) and 32-column slice
-//     rescales the CTAs' partial outputs by exp(m_c - M) (split softmax),
-//     sums them, divides by the total L and writes out (and lse).
+//     rescales the runs' outputs by exp(m_c - M) (split softmax), sums them,
+//     divides by the total L and writes out (and lse).
 // fp16 operands keep 11 significant bits: each operand's rounding is <= 2^-11
-// relative, far inside the 1e-3 * max|out| budget. The latent is
-// dequantised in fp16 arithmetic: the byte b + 128 placed under the exponent
-// of 1024 is the fp16 number 1024 + (b + 128), exactly; subtracting 1152 gives
-// b exactly and one fp16 multiply by the scale rounds once, the same value as
-// the fp32 product rounded to fp16. Waits are bounded; on a timeout the kernel
-// sets DSA_DEVERR_TIMEOUT, frees its tensor memory and leaves an empty part
-// (max -inf, sum 0) for the merge.
+// relative, far inside the 1e-3 * max|out| budget. The latent is dequantised
+// in fp16 arithmetic: the byte b + 128 placed under the exponent of 1024 is
+// the fp16 number 1024 + (b + 128), exactly; subtracting 1152 gives b exactly
+// and one fp16 multiply by the scale rounds once, the same value as the fp32
+// product rounded to fp16. Waits are bounded; on a timeout the kernel sets
+// DSA_DEVERR_TIMEOUT, frees its tensor memory and leaves an empty part (max
+// -inf, sum 0) for the merge.
+#include <algorithm>
 #include <cuda_fp16.h>
 #include <math.h>
 
@@ -47,55 +52,52 @@
 
 namespace {
 
-constexpr int NC = 128;                         // selected rows per CTA
-constexpr int MAX_CTAS = 16;                    // per (unit, query row) -> K <= 2048
+constexpr int NC = 64;                          // selected rows per chunk
+constexpr int MAX_CTAS = 16;                    // runs per (unit, query row)
 constexpr int THREADS = 256;
-constexpr int QATOM = 8192;                     // 64 rows x 128 B (query atoms)
-constexpr int PATOM = 16384;                    // 128 rows x 128 B (P atoms: the 64 rows twice)
-constexpr int BATOM = NC * 128;                 // 128 rows x 128 B (row-tile atoms)
-constexpr int X_OFF = 0;
-constexpr int X_BYTES = NC * DSA_ROW_BYTES;     // 83,968 = 82 KB
-constexpr int Y_OFF = X_BYTES;
-constexpr int Y_BYTES = 9 * BATOM;              // 147,456
-constexpr int MISC_OFF = Y_OFF + Y_BYTES;
-constexpr int SMEM_BYTES = MISC_OFF + 1024;     // 232,448: the whole opt-in budget
+constexpr int QATOM = 64 * 128;                 // 64 rows x 128 B: query and tile atoms
+constexpr int Q_OFF = 0;                        // query block: 9 atoms of 64 dims
+constexpr int T_OFF = 9 * QATOM;                // row tile: 9 atoms of 64 dims (atom 8: RoPE, then P)
+constexpr int P_OFF = T_OFF + 8 * QATOM;
+constexpr int R_OFF = T_OFF + 9 * QATOM;        // staging of the raw rows (64 x 656 B)
+constexpr int MISC_OFF = R_OFF + NC * DSA_ROW_BYTES;
+constexpr float TAU = 8.f;                      // allowed growth of a chunk maximum before a rescale
+// Tensor memory: O^T block b (latent dims 128b..128b+127 in lanes, heads in
+// columns) at columns [64b, 64b + 64); S (heads in lanes 0..63, rows in
+// columns) at columns [256, 320).
 constexpr int TMEM_COLS = 512;
+constexpr uint32_t S_COL = 256;
 constexpr uint32_t IDESC_QK = tc::idesc_f16_f32(128, NC, 0, 0);
-constexpr uint32_t IDESC_PV = tc::idesc_f16_f32(128, 256, 0, 1);
-// Partial outputs in the workspace, per (unit, query row) and CTA: O as 16
+constexpr uint32_t IDESC_PV = tc::idesc_f16_f32(128, 64, 1, 0);
+// Partial outputs in the workspace, per (unit, query row) and run: O as 16
 // slices of 32 columns, each a contiguous [64 heads][32] block (the merge
-// block of a slice reads one block per CTA), then the 64 row maxima and the
+// block of a slice reads one block per run), then the 64 row maxima and the
 // 64 row sums.
 constexpr int SLICE = 32;
 constexpr int NSLICE = 512 / SLICE;
-constexpr size_t PART_O = (size_t)64 * 512;     // floats per CTA
-constexpr size_t PART_ML = 128;                 // floats per CTA
-
-static_assert(X_BYTES % 1024 == 0, "region X must keep Y 1024-aligned");
-static_assert(SMEM_BYTES <= 232448, "shared memory budget");
+constexpr size_t PART_O = (size_t)64 * 512;     // floats per run
+constexpr size_t PART_ML = 128;                 // floats per run
 
 struct Misc {
-  uint64_t bar[2];        // [0] TMA, [1] MMA
+  uint64_t bar_t;             // rows staged (one phase per chunk, compact rows)
+  uint64_t bar_s;             // S product done (one phase per chunk)
+  uint64_t bar_o;             // O^T product done (one phase per chunk)
   uint32_t tmem;
   int fail;
-  float m[64];
-  float l[64];
-  uint32_t vmask[NC / 32];    // validity of this CTA's rows
+  int rescale;                // this chunk moved a running maximum: rescale O^T
+  uint32_t vmask[NC / 32];    // validity of the chunk's rows
+  float m_run[64];            // running maximum per head (logit units)
+  float alpha[64];            // this chunk's rescale factor per head
+  float red[2][64];           // per half of the rows: maximum, then sum, per head
+  const uint8_t* src[NC];     // (gathered rows) source of each row
+  uint8_t* dst[NC];           // (gathered rows) hot slot an inserted miss also goes to
 };
-
-// Softmax partials, in region X beyond the P atoms (the query block is dead
-// once S is computed).
-struct SoftmaxScratch {
-  float pm[2][64];            // partial max per column half
-  float pl[2][64];            // partial sum per column half
-};
-constexpr int SMX_OFF = 2 * PATOM;
-static_assert(SMX_OFF + (int)sizeof(SoftmaxScratch) <= X_BYTES, "softmax scratch");
-static_assert(sizeof(Misc) <= 1024, "misc block");
-static_assert(8 * 32 * 36 * 4 <= Y_BYTES, "O transpose buffers");
-
-// CTAs per (unit, query row) for K selected rows.
-inline int attn_ctas(int K) { return (K + NC - 1) / NC; }
+constexpr int SMEM_BYTES = MISC_OFF + (int)((sizeof(Misc) + 127) / 128 * 128);
+static_assert(SMEM_BYTES <= 232448, "shared memory budget");
+static_assert(T_OFF % 1024 == 0 && P_OFF % 1024 == 0 && R_OFF % 16 == 0, "operand alignment");
+// the M = 128 query operand reads 64 rows past each atom: the last atom's
+// extra rows fall inside the tile
+static_assert(T_OFF + QATOM <= MISC_OFF, "padded query rows stay inside shared memory");
 
 __device__ __forceinline__ uint32_t pack_h2(float a, float b) {
   const __half2 h = __floats2half2_rn(a, b);
@@ -121,36 +123,105 @@ __device__ __forceinline__ void dequant4(uint32_t w, __half2 s2, __half2& lo, __
 
 __device__ __forceinline__ uint32_t h2_bits(__half2 v) { return *reinterpret_cast<const uint32_t*>(&v); }
 
+// 32 lanes x 32 bits, 32 consecutive columns, from registers (then waits).
+__device__ __forceinline__ void tmem_st32(uint32_t taddr, const float (&v)[32]) {
+  asm volatile(
+      "tcgen05.st.sync.aligned.32x32b.x32.b32 [%0], "
+      "{%1,%2,%3,%4,%5,%6,%7,%8,%9,%10,%11,%12,%13,%14,%15,%16,"
+      "%17,%18,%19,%20,%21,%22,%23,%24,%25,%26,%27,%28,%29,%30,%31,%32};" ::"r"(taddr),
+      "r"(__float_as_uint(v[0])), "r"(__float_as_uint(v[1])), "r"(__float_as_uint(v[2])),
+      "r"(__float_as_uint(v[3])), "r"(__float_as_uint(v[4])), "r"(__float_as_uint(v[5])),
+      "r"(__float_as_uint(v[6])), "r"(__float_as_uint(v[7])), "r"(__float_as_uint(v[8])),
+      "r"(__float_as_uint(v[9])), "r"(__float_as_uint(v[10])), "r"(__float_as_uint(v[11])),
+      "r"(__float_as_uint(v[12])), "r"(__float_as_uint(v[13])), "r"(__float_as_uint(v[14])),
+      "r"(__float_as_uint(v[15])), "r"(__float_as_uint(v[16])), "r"(__float_as_uint(v[17])),
+      "r"(__float_as_uint(v[18])), "r"(__float_as_uint(v[19])), "r"(__float_as_uint(v[20])),
+      "r"(__float_as_uint(v[21])), "r"(__float_as_uint(v[22])), "r"(__float_as_uint(v[23])),
+      "r"(__float_as_uint(v[24])), "r"(__float_as_uint(v[25])), "r"(__float_as_uint(v[26])),
+      "r"(__float_as_uint(v[27])), "r"(__float_as_uint(v[28])), "r"(__float_as_uint(v[29])),
+      "r"(__float_as_uint(v[30])), "r"(__float_as_uint(v[31]))
+      : "memory");
+  asm volatile("tcgen05.wait::st.sync.aligned;" ::: "memory");
+}
+
+// Dequantise the staged raw rows [0, nrows) into the fp16 tile (rows past
+// nrows: zeros). Work item (row j, piece c): c < 32 is 16 latent bytes (one
+// fp16 scale), c >= 32 is 16 RoPE values; consecutive threads take
+// consecutive rows. Returns the largest |value| written.
+__device__ __forceinline__ float dequant_tile(const uint8_t* raw, uint8_t* tile, int nrows, int tid) {
+  __half2 vmax = __float2half2_rn(0.f);
+  for (int t = tid; t < NC * 36; t += THREADS) {
+    const int j = t % NC, c = t / NC;
+    uint4 lo = make_uint4(0u, 0u, 0u, 0u), hi = make_uint4(0u, 0u, 0u, 0u);
+    if (j < nrows) {
+      const uint8_t* row = raw + j * DSA_ROW_BYTES;
+      uint32_t o[8];
+      if (c < 32) {
+        const __half2 s2 = __half2half2(reinterpret_cast<const __half*>(row + 512)[c >> 2]);
+        const uint4 w4 = *reinterpret_cast<const uint4*>(row + 16 * c);
+        const uint32_t w[4] = {w4.x, w4.y, w4.z, w4.w};
+#pragma unroll
+        for (int e = 0; e < 4; ++e) {
+          __half2 a, b;
+          dequant4(w[e], s2, a, b);
+          vmax = __hmax2(vmax, __hmax2(__habs2(a), __habs2(b)));
+          o[2 * e] = h2_bits(a);
+          o[2 * e + 1] = h2_bits(b);
+        }
+      } else {
+        const uint4 r0 = *reinterpret_cast<const uint4*>(row + 528 + 32 * (c - 32));
+        const uint4 r1 = *reinterpret_cast<const uint4*>(row + 528 + 32 * (c - 32) + 16);
+        const uint32_t w[8] = {r0.x, r0.y, r0.z, r0.w, r1.x, r1.y, r1.z, r1.w};
+#pragma unroll
+        for (int e = 0; e < 8; ++e) o[e] = pack_h2(bf16_lo(w[e]), bf16_hi(w[e]));
+      }
+      lo = make_uint4(o[0], o[1], o[2], o[3]);
+      hi = make_uint4(o[4], o[5], o[6], o[7]);
+    }
+    const int d0 = 16 * c;   // first of the item's 16 dims
+    uint8_t* atom = tile + (d0 >> 6) * QATOM;
+    *reinterpret_cast<uint4*>(atom + tc::sw128_off(j, d0 & 63)) = lo;
+    *reinterpret_cast<uint4*>(atom + tc::sw128_off(j, (d0 & 63) + 8)) = hi;
+  }
+  return fmaxf(__low2float(vmax), __high2float(vmax));
+}
+
 __device__ __forceinline__ void cp_async16(void* dst_smem, const void* src) {
   asm volatile("cp.async.cg.shared.global [%0], [%1], 16;" ::"r"(tc::smem_u32(dst_smem)), "l"(src) : "memory");
 }
 
-// GATHER = false: the rows come compact from hot_gather (one bulk copy).
-// GATHER = true: the rows are read from their sources (HOT slot, ring, RAM
-// mirror) as classified by the gather's assign kernel, and each inserted
-// miss's row is also written to its victim slot.
+// A: one run of chunks [cpp * part, cpp * part + cpp) of (unit, query row)
+// ur = blockIdx.y, part = blockIdx.x.
 template <bool GATHER>
 __global__ void __launch_bounds__(THREADS, 1)
-k_mla_attn(int R, int H, int K, const uint16_t* __restrict__ q_lat, const uint16_t* __restrict__ q_rope,
-           const uint8_t* __restrict__ rows, const int32_t* __restrict__ topk, float scale,
-           float* __restrict__ ws_o, float* __restrict__ ws_ml, int32_t* dev_err,
-           const dsa_unit* __restrict__ units, const uint8_t* __restrict__ cls, GatherWs g) {
+k_attn_parts(int R, int H, int K, int cpp, const uint16_t* __restrict__ q_lat, const uint16_t* __restrict__ q_rope,
+             const uint8_t* __restrict__ rows, const int32_t* __restrict__ topk, float scale,
+             float* __restrict__ ws_o, float* __restrict__ ws_ml, int32_t* dev_err,
+             const dsa_unit* __restrict__ units, const uint8_t* __restrict__ cls, GatherWs g) {
   extern __shared__ __align__(1024) uint8_t sm[];
-  const int crank = blockIdx.x;
-  uint8_t* sX = sm + X_OFF;
-  uint8_t* sY = sm + Y_OFF;
+  uint8_t* sQ = sm + Q_OFF;
+  uint8_t* sT = sm + T_OFF;
+  uint8_t* sP = sm + P_OFF;
+  uint8_t* sR = sm + R_OFF;
   Misc* ms = reinterpret_cast<Misc*>(sm + MISC_OFF);
   const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
-  const int ur = blockIdx.y;
-  const int j0 = crank * NC;
-  const int nrows = max(0, min(NC, K - j0));
+  const int part = blockIdx.x, ur = blockIdx.y;
+  const int nchunks = (K + NC - 1) / NC;
+  const int c0 = part * cpp, c1 = min(c0 + cpp, nchunks);
+  // softmax threads: warps 0, 1, 4, 5 read S lanes 0..63 (the heads); head
+  // 32 * (warp & 1) + lane, rows 32 * (warp >> 2) .. + 31 of the chunk
+  const bool sm_warp = (warp & 3) < 2;
+  const int hd = 32 * (warp & 1) + lane, rh = warp >> 2;
 
   if (tid == 0) {
-    tc::mbar_init(&ms->bar[0], 1);
-    tc::mbar_init(&ms->bar[1], 1);
+    tc::mbar_init(&ms->bar_t, 1);
+    tc::mbar_init(&ms->bar_s, 1);
+    tc::mbar_init(&ms->bar_o, 1);
     tc::fence_mbar_init();
     ms->fail = (tc::smem_u32(sm) & 1023u) != 0;   // the tile layouts need 1024-byte alignment
+    ms->rescale = 0;
   }
+  if (tid < 64) ms->m_run[tid] = -INFINITY;
   if (warp == 0) tc::tmem_alloc(&ms->tmem, TMEM_COLS);
   tc::fence_before_sync();
   __syncthreads();
@@ -159,127 +230,72 @@ k_mla_attn(int R, int H, int K, const uint16_t* __restrict__ q_lat, const uint16
   bool failed = ms->fail != 0;
   pdl_wait();   // everything above touched only this CTA's shared and tensor memory
 
-  // The rows of a CTA arrive by one bulk copy on phase 0 of bar[0].
-  const bool rows_copy = !GATHER && !failed && nrows > 0;
-  if (rows_copy && tid == 0) {
-    const uint32_t bytes = (uint32_t)nrows * DSA_ROW_BYTES;
-    tc::mbar_arrive_expect_tx(&ms->bar[0], bytes);
-    tc::bulk_g2s(sX, rows + ((size_t)ur * K + j0) * DSA_ROW_BYTES, bytes, &ms->bar[0]);
-  }
-  if (GATHER && !failed) {
-    // source and fill destination of each of this CTA's rows (kept in Y, which
-    // is free until the dequantised tile is written)
-    const uint8_t** s_src = reinterpret_cast<const uint8_t**>(sY);
-    uint8_t** s_dst = reinterpret_cast<uint8_t**>(sY + NC * sizeof(void*));
-    if (tid < NC) {
-      const uint8_t* src = nullptr;
-      uint8_t* dst = nullptr;
-      if (tid < nrows) {
-        const size_t e = (size_t)ur * K + j0 + tid;    // = u * R * K + entry
-        const int u = ur / R;
-        const dsa_unit& un = units[u];
-        const int32_t p = topk[e];
-        const uint8_t c = cls[e];
-        if (c == DSA_CLS_HOT) {
-          const int32_t sl = un.pos_slot[p];
-          if (sl >= 0 && sl < un.slots_n) src = un.slots + (size_t)sl * DSA_ROW_BYTES;
-        } else if (c == DSA_CLS_RING) {
-          src = un.ring + (size_t)(p & (DSA_RING_ROWS - 1)) * DSA_ROW_BYTES;
-        } else if (c == DSA_CLS_RAM) {
-          src = un.mirror + (size_t)p * DSA_ROW_BYTES;
-          const int32_t f = g.fill_of[e];
-          if (f >= 0) {
-            const int32_t sl = g.fill_slot[(size_t)u * R * K + f];
-            if (sl >= 0 && sl < un.slots_n) dst = un.slots + (size_t)sl * DSA_ROW_BYTES;
+  // Stage chunk c's rows. Compact rows: one bulk copy (thread 0) on bar_t.
+  // Gathered rows: 16-byte async copies from each row's source (all threads;
+  // the caller waits with cp.async.wait_group and a barrier).
+  auto stage = [&](int c) {
+    const int j0 = c * NC, n = min(NC, K - j0);
+    if (!GATHER) {
+      if (tid == 0) {
+        const uint32_t bytes = (uint32_t)n * DSA_ROW_BYTES;
+        tc::mbar_arrive_expect_tx(&ms->bar_t, bytes);
+        tc::bulk_g2s(sR, rows + ((size_t)ur * K + j0) * DSA_ROW_BYTES, bytes, &ms->bar_t);
+      }
+    } else {
+      if (tid < NC) {
+        uint8_t* dst = nullptr;
+        const uint8_t* src = nullptr;
+        if (tid < n) {
+          const size_t ei = (size_t)ur * K + j0 + tid;   // = u * R * K + entry
+          const int u = ur / R;
+          const dsa_unit& un = units[u];
+          const int32_t p = topk[ei];
+          const uint8_t cl = cls[ei];
+          if (cl == DSA_CLS_HOT) {
+            const int32_t sl = un.pos_slot[p];
+            if (sl >= 0 && sl < un.slots_n) src = un.slots + (size_t)sl * DSA_ROW_BYTES;
+          } else if (cl == DSA_CLS_RING) {
+            src = un.ring + (size_t)(p & (DSA_RING_ROWS - 1)) * DSA_ROW_BYTES;
+          } else if (cl == DSA_CLS_RAM) {
+            src = un.mirror + (size_t)p * DSA_ROW_BYTES;
+            const int32_t f = g.fill_of[ei];
+            if (f >= 0) {
+              const int32_t sl = g.fill_slot[(size_t)u * R * K + f];
+              if (sl >= 0 && sl < un.slots_n) dst = un.slots + (size_t)sl * DSA_ROW_BYTES;
+            }
           }
         }
+        ms->src[tid] = src;
+        ms->dst[tid] = dst;
       }
-      s_src[tid] = src;
-      s_dst[tid] = dst;
-    }
-    __syncthreads();
-    // every 16-byte piece of every row in flight at once (no registers held)
-    for (int t = tid; t < nrows * 41; t += THREADS) {
-      const int jj = t / 41, c = t % 41;
-      const uint8_t* src = s_src[jj];
-      uint8_t* d = sX + jj * DSA_ROW_BYTES + 16 * c;
-      if (src) cp_async16(d, src + 16 * c);
-      else *reinterpret_cast<uint4*>(d) = make_uint4(0, 0, 0, 0);
-    }
-    asm volatile("cp.async.commit_group;\ncp.async.wait_group 0;" ::: "memory");
-    __syncthreads();
-    // inserted misses: their RAM bytes also go to the victim slot
-    for (int t = tid; t < nrows * 41; t += THREADS) {
-      const int jj = t / 41, c = t % 41;
-      uint8_t* dst = s_dst[jj];
-      if (dst) *reinterpret_cast<uint4*>(dst + 16 * c) = *reinterpret_cast<const uint4*>(sX + jj * DSA_ROW_BYTES + 16 * c);
-    }
-  }
-  if (tid < NC) {
-    const bool v = (tid < nrows) && topk[(size_t)ur * K + j0 + tid] >= 0;
-    const unsigned b = __ballot_sync(0xffffffffu, v);
-    if (lane == 0) ms->vmask[warp] = b;
-  }
-
-  // query block loads, in flight while the rows arrive: 64 heads x 72 chunks of 8 dims
-  constexpr int QCH = 64 * 72 / THREADS;        // 18 chunks per thread
-  uint4 qv[QCH];
-#pragma unroll
-  for (int i = 0; i < QCH; ++i) {
-    const int t = tid + i * THREADS;
-    const int h = t / 72, c = t % 72;
-    qv[i] = make_uint4(0, 0, 0, 0);
-    if (h < H) {
-      const size_t qo = (size_t)ur * H + h;
-      qv[i] = c < 64 ? *reinterpret_cast<const uint4*>(q_lat + qo * 512 + 8 * c)
-                     : *reinterpret_cast<const uint4*>(q_rope + qo * 64 + 8 * (c - 64));
-    }
-  }
-  if (rows_copy && !tc::mbar_wait(&ms->bar[0], 0)) atomicOr(&ms->fail, 1);
-  __syncthreads();
-  failed = ms->fail != 0;
-
-  // ---- dequantise the rows: region X (raw) -> region Y (fp16 tile)
-  if (!failed) {
-    __half2 vmax = __float2half2_rn(0.f);   // largest |dequantised value| of this thread
-    for (int t = tid; t < NC * 36; t += THREADS) {
-      const int j = t % NC, c = t / NC;     // consecutive threads: consecutive rows
-      uint4 lo = make_uint4(0, 0, 0, 0), hi = make_uint4(0, 0, 0, 0);
-      if (j < nrows) {
-        const uint8_t* row = sX + j * DSA_ROW_BYTES;
-        uint32_t o[8];
-        if (c < 32) {
-          const __half2 s2 = __half2half2(reinterpret_cast<const __half*>(row + 512)[c >> 2]);
-          const uint4 raw = *reinterpret_cast<const uint4*>(row + 16 * c);
-          const uint32_t w[4] = {raw.x, raw.y, raw.z, raw.w};
-#pragma unroll
-          for (int e = 0; e < 4; ++e) {
-            __half2 a, b;
-            dequant4(w[e], s2, a, b);
-            vmax = __hmax2(vmax, __hmax2(__habs2(a), __habs2(b)));
-            o[2 * e] = h2_bits(a);
-            o[2 * e + 1] = h2_bits(b);
-          }
-        } else {
-          const uint4 r0 = *reinterpret_cast<const uint4*>(row + 528 + 32 * (c - 32));
-          const uint4 r1 = *reinterpret_cast<const uint4*>(row + 528 + 32 * (c - 32) + 16);
-          const uint32_t w[8] = {r0.x, r0.y, r0.z, r0.w, r1.x, r1.y, r1.z, r1.w};
-#pragma unroll
-          for (int e = 0; e < 8; ++e) o[e] = pack_h2(bf16_lo(w[e]), bf16_hi(w[e]));
-        }
-        lo = make_uint4(o[0], o[1], o[2], o[3]);
-        hi = make_uint4(o[4], o[5], o[6], o[7]);
+      __syncthreads();
+      for (int t = tid; t < n * 41; t += THREADS) {
+        const int jj = t / 41, q = t % 41;
+        const uint8_t* src = ms->src[jj];
+        uint8_t* d = sR + jj * DSA_ROW_BYTES + 16 * q;
+        if (src) cp_async16(d, src + 16 * q);
+        else *reinterpret_cast<uint4*>(d) = make_uint4(0u, 0u, 0u, 0u);
       }
-      const int d0 = 16 * c;
-      uint8_t* atom = sY + (d0 >> 6) * BATOM;
-      *reinterpret_cast<uint4*>(atom + tc::sw128_off(j, d0 & 63)) = lo;
-      *reinterpret_cast<uint4*>(atom + tc::sw128_off(j, (d0 & 63) + 8)) = hi;
+      asm volatile("cp.async.commit_group;" ::: "memory");
     }
-    // (a value whose fp16 rounding reaches 65504, including an overflow)
-    if (fmaxf(__low2float(vmax), __high2float(vmax)) >= 65504.f) dsa_flag(dev_err, DSA_DEVERR_QRANGE);
-  }
-  __syncthreads();   // raw rows are dead: X takes the query block
+  };
+  if (!failed && c0 < c1) stage(c0);
+
+  // query block: 64 heads x 72 pieces of 8 dims, bf16 -> fp16, K-major swizzled
+  constexpr int QCH = 64 * 72 / THREADS;        // 18 pieces per thread
   if (!failed) {
+    uint4 qv[QCH];
+#pragma unroll
+    for (int i = 0; i < QCH; ++i) {
+      const int t = tid + i * THREADS;
+      const int h = t / 72, c = t % 72;
+      qv[i] = make_uint4(0u, 0u, 0u, 0u);
+      if (h < H) {
+        const size_t qo = (size_t)ur * H + h;
+        qv[i] = c < 64 ? *reinterpret_cast<const uint4*>(q_lat + qo * 512 + 8 * c)
+                       : *reinterpret_cast<const uint4*>(q_rope + qo * 64 + 8 * (c - 64));
+      }
+    }
     bool bad = false;
 #pragma unroll
     for (int i = 0; i < QCH; ++i) {
@@ -293,149 +309,214 @@ k_mla_attn(int R, int H, int K, const uint16_t* __restrict__ q_lat, const uint16
         bad |= fmaxf(fabsf(a), fabsf(b)) >= 65504.f;
         o[e] = pack_h2(a, b);
       }
-      const int d0 = 8 * c;
-      *reinterpret_cast<uint4*>(sX + (d0 >> 6) * QATOM + tc::sw128_off(h, d0 & 63)) =
+      *reinterpret_cast<uint4*>(sQ + (c >> 3) * QATOM + tc::sw128_off(h, 8 * (c & 7))) =
           make_uint4(o[0], o[1], o[2], o[3]);
     }
     if (bad) dsa_flag(dev_err, DSA_DEVERR_QRANGE);
   }
-  tc::fence_async_shared();
-  tc::fence_before_sync();
-  __syncthreads();
-  tc::fence_after_sync();
 
-  // ---- S = Q K^T: TMEM columns [0, 128)
-  if (tid == 0 && !failed) {
-    const uint32_t qa = tc::smem_u32(sX), ba = tc::smem_u32(sY);
-    for (int kb = 0; kb < 9; ++kb) {
+  float lsum = 0.f;    // (softmax threads) this thread's share of its head's row sum
+  float vmax = 0.f;
+  int ns = 0, no = 0;  // (thread 0) product groups committed on bar_s / bar_o
+  int nt = (!failed && c0 < c1) ? 1 : 0;   // (thread 0) row copies issued on bar_t
+  for (int c = c0; c < c1; ++c) {
+    const int i = c - c0;
+    const int j0 = c * NC;
+    const int nrows = min(NC, K - j0);
+    // ---- rows staged; the tile and P are free once the previous chunk's
+    //      O^T product is done
+    if (!failed) {
+      if (!GATHER) {
+        if (!tc::mbar_wait(&ms->bar_t, (uint32_t)(i & 1))) atomicOr(&ms->fail, 1);
+      } else {
+        asm volatile("cp.async.wait_group 0;" ::: "memory");
+      }
+      if (i > 0 && !tc::mbar_wait(&ms->bar_o, (uint32_t)((i - 1) & 1))) atomicOr(&ms->fail, 1);
+    }
+    if (tid < NC) {
+      const bool v = tid < nrows && topk[(size_t)ur * K + j0 + tid] >= 0;
+      const unsigned b = __ballot_sync(0xffffffffu, v);
+      if (lane == 0) ms->vmask[warp] = b;
+    }
+    tc::fence_after_sync();
+    __syncthreads();
+    failed = ms->fail != 0;
+    // ---- dequantise (an inserted miss's bytes also go to its hot slot)
+    if (!failed) {
+      if (GATHER) {
+        for (int t = tid; t < nrows * 41; t += THREADS) {
+          const int jj = t / 41, q = t % 41;
+          uint8_t* dst = ms->dst[jj];
+          if (dst) *reinterpret_cast<uint4*>(dst + 16 * q) = *reinterpret_cast<const uint4*>(sR + jj * DSA_ROW_BYTES + 16 * q);
+        }
+      }
+      vmax = fmaxf(vmax, dequant_tile(sR, sT, nrows, tid));
+    }
+    tc::fence_async_shared();
+    tc::fence_before_sync();
+    __syncthreads();   // staging consumed, tile written
+    tc::fence_after_sync();
+    failed = ms->fail != 0;
+    // ---- the next chunk's rows land while this chunk's products run
+    if (!failed && c + 1 < c1) {
+      stage(c + 1);
+      ++nt;
+    }
+
+    // ---- S = Q K^T: heads in lanes 0..63, rows in columns [S_COL, S_COL + 64)
+    if (tid == 0 && !failed) {
+      const uint32_t ta = tc::smem_u32(sT), qa = tc::smem_u32(sQ);
+      for (int kb = 0; kb < 9; ++kb) {
 #pragma unroll
-      for (int kk = 0; kk < 4; ++kk) {
-        const uint64_t ad = tc::sdesc_sw128(qa + kb * QATOM + kk * 32, 16, 1024);
-        const uint64_t bd = tc::sdesc_sw128(ba + kb * BATOM + kk * 32, 16, 1024);
-        tc::mma_f16(tmem, ad, bd, IDESC_QK, (kb | kk) != 0);
+        for (int kk = 0; kk < 4; ++kk)
+          tc::mma_f16(tmem + S_COL, tc::sdesc_sw128(qa + kb * QATOM + kk * 32, 16, 1024),
+                      tc::sdesc_sw128(ta + kb * QATOM + kk * 32, 16, 1024), IDESC_QK, (kb | kk) != 0);
+      }
+      tc::mma_commit(&ms->bar_s);
+      ++ns;
+    }
+    if (!failed && !tc::mbar_wait(&ms->bar_s, (uint32_t)(i & 1))) atomicOr(&ms->fail, 1);
+    tc::fence_after_sync();
+    __syncthreads();
+    failed = ms->fail != 0;
+
+    // ---- online softmax: head hd, rows 32 rh .. 32 rh + 31 of the chunk
+    float x[32];
+    if (sm_warp && !failed) {
+      float v[32];
+      tc::tmem_ld32(tmem + ((uint32_t)(32 * (warp & 3)) << 16) + S_COL + 32 * rh, v);
+      const uint32_t vm = ms->vmask[rh];
+      float mx = -INFINITY;
+#pragma unroll
+      for (int k = 0; k < 32; ++k) {
+        x[k] = ((vm >> k) & 1u) ? v[k] * scale : -INFINITY;
+        mx = fmaxf(mx, x[k]);
+      }
+      ms->red[rh][hd] = mx;
+    }
+    __syncthreads();
+    if (tid < 64 && !failed) {
+      const int h = tid;
+      const float cm = fmaxf(ms->red[0][h], ms->red[1][h]);
+      const float mo = ms->m_run[h];
+      float a = 1.f;
+      if (cm > -INFINITY && (mo == -INFINITY || cm > mo + TAU)) {
+        a = mo == -INFINITY ? 0.f : __expf(mo - cm);
+        ms->m_run[h] = cm;
+        if (i > 0) ms->rescale = 1;
+      }
+      ms->alpha[h] = a;
+    }
+    __syncthreads();
+    if (!failed) {
+      if (ms->rescale) {
+        // (rare) a running maximum moved: O^T *= alpha per head column. This
+        // thread owns latent dim 32 * (warp & 3) + lane of blocks
+        // 2 * (warp >> 2) and 2 * (warp >> 2) + 1.
+#pragma unroll 1
+        for (int b = 0; b < 2; ++b) {
+#pragma unroll 1
+          for (int x2 = 0; x2 < 2; ++x2) {
+            const uint32_t ta =
+                tmem + ((uint32_t)(32 * (warp & 3)) << 16) + 64 * (2 * (warp >> 2) + b) + 32 * x2;
+            float o[32];
+            tc::tmem_ld32(ta, o);
+#pragma unroll
+            for (int k = 0; k < 32; ++k) o[k] *= ms->alpha[32 * x2 + k];
+            tmem_st32(ta, o);
+          }
+        }
+      }
+      if (sm_warp) {
+        // P = exp(x - m) (0 for masked rows) -> row hd of P, columns 32 rh ..
+        const float m = ms->m_run[hd];
+        uint32_t pw[16];
+        float sum = 0.f;
+#pragma unroll
+        for (int k = 0; k < 16; ++k) {
+          const float p0 = (x[2 * k] == -INFINITY || m == -INFINITY) ? 0.f : __expf(x[2 * k] - m);
+          const float p1 = (x[2 * k + 1] == -INFINITY || m == -INFINITY) ? 0.f : __expf(x[2 * k + 1] - m);
+          sum += p0 + p1;
+          pw[k] = pack_h2(p0, p1);
+        }
+        lsum = fmaf(lsum, ms->alpha[hd], sum);
+#pragma unroll
+        for (int q4 = 0; q4 < 4; ++q4)
+          *reinterpret_cast<uint4*>(sP + tc::sw128_off(hd, 32 * rh + 8 * q4)) =
+              make_uint4(pw[4 * q4], pw[4 * q4 + 1], pw[4 * q4 + 2], pw[4 * q4 + 3]);
       }
     }
-    tc::mma_commit(&ms->bar[1]);
+    tc::fence_async_shared();
+    tc::fence_before_sync();
+    __syncthreads();
+    tc::fence_after_sync();
+    if (tid == 0) ms->rescale = 0;
+    failed = ms->fail != 0;
+
+    // ---- O^T += V^T P^T: latent dims 128 mb .. + 127 in lanes, heads in columns
+    if (tid == 0 && !failed) {
+      const uint32_t ta = tc::smem_u32(sT), pa = tc::smem_u32(sP);
+      for (int mb = 0; mb < 4; ++mb) {
+#pragma unroll
+        for (int kk = 0; kk < NC / 16; ++kk)
+          tc::mma_f16(tmem + 64 * mb, tc::sdesc_sw128(ta + 2 * mb * QATOM + kk * 2048, QATOM, 1024),
+                      tc::sdesc_sw128(pa + kk * 32, 16, 1024), IDESC_PV, (i > 0 || kk > 0));
+      }
+      tc::mma_commit(&ms->bar_o);
+      ++no;
+    }
   }
-  if (!failed && !tc::mbar_wait(&ms->bar[1], 0)) atomicOr(&ms->fail, 1);
+
+  // ---- the run's O^T, maxima and sums -> its workspace slot
+  const int nch = c1 - c0;
+  if (nch > 0 && !failed && !tc::mbar_wait(&ms->bar_o, (uint32_t)((nch - 1) & 1))) atomicOr(&ms->fail, 1);
   tc::fence_after_sync();
   __syncthreads();
   failed = ms->fail != 0;
-
-  // ---- softmax over this CTA's columns. Warps 0,1,4,5 can read TMEM lanes
-  // 0..63 (head rows); warp w takes lane quarter w & 3 and column half w >> 2.
-  const bool sm_warp = (warp & 3) < 2;
-  const int hr = 32 * (warp & 3) + lane;      // head row of this thread (sm_warp only)
-  const int half = warp >> 2;
-  SoftmaxScratch* sx = reinterpret_cast<SoftmaxScratch*>(sX + SMX_OFF);
-  float s[64];
-  if (sm_warp && !failed) {
+  if (sm_warp) ms->red[rh][hd] = lsum;
+  float* gO = ws_o + ((size_t)ur * MAX_CTAS + part) * PART_O;
+  if (!failed && nch > 0) {
+    // this thread: latent dim d = 128 mb + 32 (warp & 3) + lane of blocks
+    // mb = 2 (warp >> 2) + b; for each head the warp stores 32 consecutive
+    // floats of slice d / 32
+#pragma unroll 1
+    for (int b = 0; b < 2; ++b) {
+      const int mb = 2 * (warp >> 2) + b;
+      float* blk = gO + (size_t)(4 * mb + (warp & 3)) * 64 * SLICE;
+#pragma unroll 1
+      for (int x2 = 0; x2 < 2; ++x2) {
+        float o[32];
+        tc::tmem_ld32(tmem + ((uint32_t)(32 * (warp & 3)) << 16) + 64 * mb + 32 * x2, o);
 #pragma unroll
-    for (int c = 0; c < 2; ++c) {
-      float v[32];
-      tc::tmem_ld32(tmem + ((uint32_t)(32 * (warp & 3)) << 16) + 64 * half + 32 * c, v);
-      const uint32_t vm = ms->vmask[2 * half + c];
-#pragma unroll
-      for (int i = 0; i < 32; ++i) s[32 * c + i] = ((vm >> i) & 1u) ? v[i] * scale : -INFINITY;
-    }
-    float m0 = -INFINITY, m1 = -INFINITY, m2 = -INFINITY, m3 = -INFINITY;
-#pragma unroll
-    for (int j = 0; j < 64; j += 4) {
-      m0 = fmaxf(m0, s[j]);
-      m1 = fmaxf(m1, s[j + 1]);
-      m2 = fmaxf(m2, s[j + 2]);
-      m3 = fmaxf(m3, s[j + 3]);
-    }
-    sx->pm[half][hr] = fmaxf(fmaxf(m0, m1), fmaxf(m2, m3));
-  }
-  __syncthreads();
-  if (sm_warp && !failed) {
-    const float m = fmaxf(sx->pm[0][hr], sx->pm[1][hr]);
-    float l0 = 0.f, l1 = 0.f;
-#pragma unroll
-    for (int j = 0; j < 64; j += 2) {
-      s[j] = (m == -INFINITY) ? 0.f : __expf(s[j] - m);
-      s[j + 1] = (m == -INFINITY) ? 0.f : __expf(s[j + 1] - m);
-      l0 += s[j];
-      l1 += s[j + 1];
-    }
-    sx->pl[half][hr] = l0 + l1;
-#pragma unroll
-    for (int c8 = 0; c8 < 8; ++c8) {
-      const uint4 v = make_uint4(pack_h2(s[8 * c8], s[8 * c8 + 1]), pack_h2(s[8 * c8 + 2], s[8 * c8 + 3]),
-                                 pack_h2(s[8 * c8 + 4], s[8 * c8 + 5]), pack_h2(s[8 * c8 + 6], s[8 * c8 + 7]));
-      *reinterpret_cast<uint4*>(sX + half * PATOM + tc::sw128_off(hr, 8 * c8)) = v;
-      *reinterpret_cast<uint4*>(sX + half * PATOM + tc::sw128_off(hr + 64, 8 * c8)) = v;
-    }
-    if (half == 0) ms->m[hr] = m;
-  }
-  tc::fence_async_shared();
-  tc::fence_before_sync();
-  __syncthreads();
-  tc::fence_after_sync();
-  if (tid < 64) ms->l[tid] = sx->pl[0][tid] + sx->pl[1][tid];
-
-  // ---- O = P V: TMEM columns [0, 512)
-  if (tid == 0 && !failed) {
-    const uint32_t pa = tc::smem_u32(sX), ba = tc::smem_u32(sY);
-    for (int half = 0; half < 2; ++half) {
-#pragma unroll
-      for (int kk = 0; kk < NC / 16; ++kk) {
-        const uint64_t ad = tc::sdesc_sw128(pa + (kk >> 2) * PATOM + (kk & 3) * 32, 16, 1024);
-        const uint64_t bd = tc::sdesc_sw128(ba + half * 4 * BATOM + kk * 2048, BATOM, 1024);
-        tc::mma_f16(tmem + half * 256, ad, bd, IDESC_PV, kk > 0);
+        for (int k = 0; k < 32; ++k) blk[(32 * x2 + k) * SLICE + lane] = o[k];
       }
     }
-    tc::mma_commit(&ms->bar[1]);
   }
-  if (!failed && !tc::mbar_wait(&ms->bar[1], 1)) atomicOr(&ms->fail, 1);
-  tc::fence_after_sync();
   __syncthreads();
-  failed = ms->fail != 0;
-
-  // ---- this CTA's O (64 x 512 fp32) to its slot of the workspace (L2). Warp
-  //      w reads tensor-memory lane quarter w & 3 (heads 32 * (w & 1) + lane:
-  //      lanes 64..127 repeat 0..63) and 128-column range 2 * (w >> 2) +
-  //      ((w & 3) >> 1). Each 32 x 32 block goes through a padded shared-memory
-  //      transpose so every store writes whole 128-byte rows of a slice.
-  float* gO = ws_o + ((size_t)ur * MAX_CTAS + crank) * PART_O;
-  if (!failed) {
-    const int q = warp & 3;
-    const int hb = 32 * (q & 1);
-    const int c0 = 128 * (2 * (warp >> 2) + (q >> 1));
-    float* tb = reinterpret_cast<float*>(sY) + warp * 32 * 36;   // [32][36]
-    for (int c = 0; c < 4; ++c) {
-      float v[32];
-      const int col = c0 + 32 * c;                       // first column of the block = slice start
-      tc::tmem_ld32(tmem + ((uint32_t)(32 * q) << 16) + col, v);
-#pragma unroll
-      for (int i = 0; i < 8; ++i)
-        reinterpret_cast<float4*>(tb + lane * 36)[i] = make_float4(v[4 * i], v[4 * i + 1], v[4 * i + 2], v[4 * i + 3]);
-      __syncwarp();
-      float* blk = gO + (size_t)(col / SLICE) * 64 * SLICE;
-#pragma unroll
-      for (int r4 = 0; r4 < 8; ++r4) {
-        const int r = 4 * r4 + (lane >> 3);              // row within the block
-        const float4 x = reinterpret_cast<const float4*>(tb + r * 36)[lane & 7];
-        reinterpret_cast<float4*>(blk + (size_t)(hb + r) * SLICE)[lane & 7] = x;
-      }
-      __syncwarp();
-    }
+  if (tid < 64) {   // a failed or empty run leaves an empty part (its O is never read)
+    const bool empty = failed || nch <= 0;
+    float* ml = ws_ml + ((size_t)ur * MAX_CTAS + part) * PART_ML;
+    ml[tid] = empty ? -INFINITY : ms->m_run[tid];
+    ml[64 + tid] = empty ? 0.f : ms->red[0][tid] + ms->red[1][tid];
   }
-  failed = failed || ms->fail != 0;
-  if (tid < 64) {   // a failed CTA leaves an empty part (its O is never read)
-    float* ml = ws_ml + ((size_t)ur * MAX_CTAS + crank) * PART_ML;
-    ml[tid] = failed ? -INFINITY : ms->m[tid];
-    ml[64 + tid] = failed ? 0.f : ms->l[tid];
+  // (a value whose fp16 rounding reaches 65504, including an overflow)
+  if (vmax >= 65504.f) dsa_flag(dev_err, DSA_DEVERR_QRANGE);
+  if (GATHER) asm volatile("cp.async.wait_group 0;" ::: "memory");
+  if (failed && tid == 0) {
+    dsa_flag(dev_err, DSA_DEVERR_TIMEOUT);
+    // nothing may still land in shared memory or run on tensor memory once
+    // the CTA is gone
+    if (!GATHER && nt > 0) tc::mbar_wait(&ms->bar_t, (uint32_t)((nt - 1) & 1));
+    if (ns > 0) tc::mbar_wait(&ms->bar_s, (uint32_t)((ns - 1) & 1));
+    if (no > 0) tc::mbar_wait(&ms->bar_o, (uint32_t)((no - 1) & 1));
   }
-  if (failed && tid == 0) dsa_flag(dev_err, DSA_DEVERR_TIMEOUT);
   tc::fence_before_sync();
   __syncthreads();
   tc::fence_after_sync();
   if (warp == 0) tc::tmem_dealloc(tmem, TMEM_COLS);
 }
 
-// B: merge of the C parts of one (unit, query row), output columns
+// B: merge of the C runs of one (unit, query row), output columns
 // [32 s, 32 s + 32) with s = blockIdx.x.
 __global__ void __launch_bounds__(256) k_attn_merge(int H, int C, const float* __restrict__ ws_o,
                                                      const float* __restrict__ ws_ml, float* __restrict__ out,
@@ -499,20 +580,26 @@ int launch_attn(int32_t U, int32_t R, int32_t H, int32_t K, const uint16_t* q_la
   static DsaPerDevice pd;
   int dev = 0;
   const int ok = dsa_device_setup(pd, &dev, [](int) {
-    DSA_CUDA_TRY(cudaFuncSetAttribute(k_mla_attn<GATHER>, cudaFuncAttributeMaxDynamicSharedMemorySize, SMEM_BYTES));
-    DSA_CUDA_TRY(dsa_prefer_shared(k_mla_attn<GATHER>));
+    DSA_CUDA_TRY(cudaFuncSetAttribute(k_attn_parts<GATHER>, cudaFuncAttributeMaxDynamicSharedMemorySize, SMEM_BYTES));
+    DSA_CUDA_TRY(dsa_prefer_shared(k_attn_parts<GATHER>));
     DSA_CUDA_TRY(dsa_prefer_shared(k_attn_merge));
     return DSA_OK;
   });
   if (ok != DSA_OK) return ok;
-  const int C = attn_ctas(K);
-  const size_t UR = (size_t)U * R;
+  // runs of chunks: as many runs per (unit, query row) as one CTA per SM
+  // allows for all of them, at most MAX_CTAS, at least one chunk per run
+  const int nchunks = (K + NC - 1) / NC;
+  const int64_t UR = (int64_t)U * R;
+  const int64_t want = std::min<int64_t>(std::min<int64_t>(std::max<int64_t>(1, pd.num_sms[dev] / UR), nchunks),
+                                         MAX_CTAS);
+  const int cpp = (int)((nchunks + want - 1) / want);
+  const int parts = (nchunks + cpp - 1) / cpp;
   float* ws_o = ws;
-  float* ws_ml = ws + UR * MAX_CTAS * PART_O;
-  if (launch_pdl(k_mla_attn<GATHER>, dim3(C, (unsigned)UR), dim3(THREADS), SMEM_BYTES, st, (int)R, (int)H, (int)K,
-                 q_lat, q_rope, rows, topk_idx, scale, ws_o, ws_ml, dev_err, units, cls, g) != DSA_OK)
+  float* ws_ml = ws + (size_t)UR * MAX_CTAS * PART_O;
+  if (launch_pdl(k_attn_parts<GATHER>, dim3(parts, (unsigned)UR), dim3(THREADS), SMEM_BYTES, st, (int)R, (int)H,
+                 (int)K, cpp, q_lat, q_rope, rows, topk_idx, scale, ws_o, ws_ml, dev_err, units, cls, g) != DSA_OK)
     return DSA_ERR_CUDA;
-  return launch_pdl(k_attn_merge, dim3(NSLICE, (unsigned)UR), dim3(256), 0, st, (int)H, C,
+  return launch_pdl(k_attn_merge, dim3(NSLICE, (unsigned)UR), dim3(256), 0, st, (int)H, parts,
                     static_cast<const float*>(ws_o), static_cast<const float*>(ws_ml), out, lse);
 }
 
@@ -524,7 +611,7 @@ extern "C" int mla_decode_attn(int32_t U, int32_t R, int32_t H, int32_t K, const
                                void* ws, size_t ws_bytes, int32_t* dev_err, void* stream) {
   if (!q_lat || !q_rope || !rows || !topk_idx || !out) return DSA_ERR_ARG;
   if (U < 1 || U > 65535 || R < 1 || R > DSA_MAX_ROWS || !(scale > 0.0f)) return DSA_ERR_ARG;
-  if (K < 1 || K > NC * MAX_CTAS || H < 16 || H > 64 || (H % 16) != 0) return DSA_ERR_SHAPE;
+  if (K < 1 || K > DSA_MAX_ATTN_K || H < 16 || H > 64 || (H % 16) != 0) return DSA_ERR_SHAPE;
   if ((size_t)U * R > 65535) return DSA_ERR_ARG;
   if (!ws || ws_bytes < mla_decode_attn_workspace(U, R, H, K)) return DSA_ERR_WS;
   // rows and the workspace are read by bulk copies: 16-byte alignment
@@ -545,7 +632,7 @@ extern "C" int hot_gather_attn(const dsa_unit* units, int32_t U, int32_t R, int3
                                size_t ws_bytes, int32_t* dev_err, void* stream) {
   if (!units || !topk_idx || !q_lat || !q_rope || !cls || !counters || !out) return DSA_ERR_ARG;
   if (U < 1 || U > 65535 || R < 1 || R > DSA_MAX_ROWS || !(scale > 0.0f)) return DSA_ERR_ARG;
-  if (K < 1 || K > NC * MAX_CTAS || H < 16 || H > 64 || (H % 16) != 0) return DSA_ERR_SHAPE;
+  if (K < 1 || K > DSA_MAX_ATTN_K || H < 16 || H > 64 || (H % 16) != 0) return DSA_ERR_SHAPE;
   if ((size_t)U * R > 65535) return DSA_ERR_ARG;
   if (!ws || ws_bytes < hot_gather_attn_workspace(U, R, H, K)) return DSA_ERR_WS;
   if (reinterpret_cast<uintptr_t>(ws) & 255u) return DSA_ERR_ARG;

@@ -365,13 +365,15 @@ int hot_gather_copy(const dsa_unit* units, int32_t U, int32_t R, int32_t K, cons
  *   topk_idx device int32 [U][R][K] (only the sign is used: -1 = padding).
  *   out     device float [U][R][H][512];  lse device float [U][R][H] or NULL.
  *   ws      device workspace of mla_decode_attn_workspace(U, R, H, K) bytes:
- *           per (unit, query row) and block of 128 selected rows, one 64 x 512
- *           fp32 partial output and its 64 row maxima and sums, written by
- *           the first kernel of the call and read by the second (in L2).
+ *           per (unit, query row) and run of selected rows (at most 16), one
+ *           64 x 512 fp32 partial output and its 64 row maxima and sums,
+ *           written by the first kernel of the call and read by the second
+ *           (in L2).
  * Shapes: H in {16, 32, 48, 64}, 1 <= K <= DSA_MAX_ATTN_K, U * R <= 65535.
- * Two kernels: ceil(K / 128) CTAs per (unit, query row), each the split
- * softmax part of 128 selected rows, then a merge of the parts (one block per
- * (unit, query row) and 32 output columns).
+ * Two kernels: per (unit, query row) the selected rows are cut into chunks
+ * of 64 and the chunks into runs, one CTA per run (as many runs as fill the
+ * GPU once), each an online-softmax part over its rows; then a merge of the
+ * parts (one block per (unit, query row) and 32 output columns).
  */
 size_t mla_decode_attn_workspace(int32_t U, int32_t R, int32_t H, int32_t K);
 int mla_decode_attn(int32_t U, int32_t R, int32_t H, int32_t K,

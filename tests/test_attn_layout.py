@@ -1,86 +1,117 @@
-"""Address table of the attention kernels' split, checked on the CPU.
+"""Address table of the attention kernels, checked on the CPU.
 
-The attention runs as two kernels. The first has ceil(K / 128) CTAs per
-(unit, query row); CTA c computes the split-softmax part of selected rows
-[128c, 128c + 128) and stores its 64 x 512 fp32 partial output slice-major
-(16 slices of 32 columns, each a contiguous [64 heads][32] block) plus its 64
-row maxima and sums. The second has one block per (unit, query row) and slice
-and writes the final output. This restates both kernels' index arithmetic and
-checks, for every accepted K, that each access is 16-byte aligned, stays
-inside the workspace, that every partial element is stored exactly once, and
-that every output element is produced exactly once from every part.
+The first kernel cuts the K selected rows of a (unit, query row) into chunks
+of 64 and the chunks into at most 16 contiguous runs, one CTA per run; a CTA
+keeps the query block and a 64-row fp16 tile in shared memory, stages the raw
+rows of a chunk with one bulk copy, and stores its unnormalised 64 x 512 fp32
+output slice-major (16 slices of 32 columns, each a contiguous [64 heads][32]
+block) plus its 64 row maxima and sums. The second kernel has one block per
+(unit, query row) and slice. This restates the kernels' index arithmetic and
+checks, for every accepted K and several batch sizes, that the runs cover the
+chunks exactly once, that every shared-memory operand read of the tensor-core
+products stays inside its region, that each store is 16-byte aligned and
+inside the workspace, and that every output element is produced exactly once.
 """
 import numpy as np
 
-NC, MAX_CTAS, MAX_K = 128, 16, 2048
+NC, MAX_CTAS, MAX_K = 64, 16, 2048
 SLICE, NSLICE = 32, 16
 PART_O, PART_ML = 64 * 512, 128
+QATOM = 64 * 128
+Q_OFF, T_OFF = 0, 9 * QATOM
+P_OFF, R_OFF = T_OFF + 8 * QATOM, T_OFF + 9 * QATOM
+MISC_OFF = R_OFF + NC * 656
 
 
-def attn_ctas(K):
-    return (K + NC - 1) // NC
+def runs(K, UR, sms=152):
+    """(chunks per run, runs) as the launch chooses them."""
+    nchunks = (K + NC - 1) // NC
+    want = min(max(1, sms // UR), nchunks, MAX_CTAS)
+    cpp = (nchunks + want - 1) // want
+    return cpp, (nchunks + cpp - 1) // cpp
 
 
-def workspace_floats(U, R):
-    return U * R * MAX_CTAS * (PART_O + PART_ML)
+def test_runs_cover_every_chunk_once():
+    for UR in (1, 2, 4, 16, 32, 64, 200):
+        for K in range(1, MAX_K + 1, 7):
+            cpp, parts = runs(K, UR)
+            nchunks = (K + NC - 1) // NC
+            assert 1 <= parts <= MAX_CTAS
+            seen = np.zeros(nchunks, int)
+            for part in range(parts):
+                c0, c1 = part * cpp, min(part * cpp + cpp, nchunks)
+                assert c0 < c1
+                seen[c0:c1] += 1
+            assert (seen == 1).all()
+            rows = [min(NC, K - NC * c) for c in range(nchunks)]
+            assert sum(rows) == K and all(r > 0 for r in rows)
 
 
-def test_cta_count_and_row_ranges_for_every_accepted_k():
-    for K in range(1, MAX_K + 1):
-        C = attn_ctas(K)
-        assert 1 <= C <= MAX_CTAS
-        rows = [max(0, min(NC, K - NC * c)) for c in range(C)]
-        assert sum(rows) == K and all(r > 0 for r in rows)
-        assert all(r == NC for r in rows[:-1])
+def sw128(row, k):
+    return (row >> 3) * 1024 + (row & 7) * 128 + ((((k >> 3) ^ row) & 7) << 4) + (k & 7) * 2
+
+
+def test_operand_spans_stay_inside_their_regions():
+    # S = Q K^T: A = query atom kb read as M = 128 rows (16 groups of 1024 B;
+    # the descriptor's 32-byte steps along K stay inside each 128-byte row);
+    # B = tile atom kb, N = 64 rows (8 groups)
+    for kb in range(9):
+        a_atom = Q_OFF + kb * QATOM
+        assert a_atom + 16 * 1024 <= MISC_OFF            # padded rows stay in shared memory
+        b_atom = T_OFF + kb * QATOM
+        assert b_atom + 8 * 1024 <= T_OFF + 9 * QATOM
+        for kk in range(4):
+            assert kk * 32 + 32 <= 128
+    # O^T += V^T P^T: A = latent atoms 2mb, 2mb + 1 (MN-major, LBO = one atom),
+    # 16 rows per product (2 groups); B = P, 64 heads (8 groups)
+    for mb in range(4):
+        for kk in range(NC // 16):
+            a0 = T_OFF + 2 * mb * QATOM + kk * 2048
+            assert a0 + QATOM + 2048 <= P_OFF              # never the RoPE / P atom
+    assert P_OFF + 8 * 1024 <= R_OFF and (NC // 16 - 1) * 32 + 32 <= 128
+    # the dequantised items and P rows
+    for j in range(NC):
+        for c in range(36):
+            d0 = 16 * c
+            for half in (0, 8):   # two 16-byte stores (the swizzle separates them)
+                off = T_OFF + (d0 >> 6) * QATOM + sw128(j, (d0 & 63) + half)
+                assert off % 16 == 0 and T_OFF <= off and off + 16 <= R_OFF
+    for hd in range(64):
+        for rh in range(2):
+            for q4 in range(4):
+                off = P_OFF + sw128(hd, 32 * rh + 8 * q4)
+                assert off % 16 == 0 and P_OFF <= off < R_OFF
 
 
 def partial_store_offsets():
-    """Float offsets within one CTA's 64 x 512 slot written by the partial-O
-    stores: all 8 warps; warp w reads tensor-memory lane quarter w & 3 (heads
-    32 * (w & 1) + lane, lanes 64..127 repeating 0..63) and 128 columns from
-    128 * (2 * (w >> 2) + ((w & 3) >> 1)); each 32 x 32 block is written as
-    float4 runs of its slice."""
+    """Float offsets within one run's 64 x 512 slot written by the partial-O
+    stores: warp w, lane l hold latent dim 128 mb + 32 (w & 3) + l of blocks
+    mb = 2 (w >> 2) + b; per head the warp stores 32 consecutive floats."""
     out = []
     for warp in range(8):
-        q = warp & 3
-        hb = 32 * (q & 1)
-        c0 = 128 * (2 * (warp >> 2) + (q >> 1))
-        for c in range(4):
-            col = c0 + 32 * c
-            blk = (col // SLICE) * 64 * SLICE
-            for r4 in range(8):
-                for lane in range(32):
-                    r = 4 * r4 + (lane >> 3)
-                    off = blk + (hb + r) * SLICE + 4 * (lane & 7)
-                    out.append((off, hb + r, col + 4 * (lane & 7)))
+        for b in range(2):
+            mb = 2 * (warp >> 2) + b
+            blk = (4 * mb + (warp & 3)) * 64 * SLICE
+            for x2 in range(2):
+                for k in range(32):
+                    for lane in range(32):
+                        d = 128 * mb + 32 * (warp & 3) + lane
+                        out.append((blk + (32 * x2 + k) * SLICE + lane, 32 * x2 + k, d))
     return out
 
 
-def test_partial_output_stores_are_aligned_slice_major_and_complete():
+def test_partial_output_stores_are_slice_major_and_complete():
     seen = np.zeros(PART_O, np.int32)
-    for off, head, col in partial_store_offsets():
-        assert off % 4 == 0 and 0 <= off and off + 4 <= PART_O
-        # slice-major: column col of head h sits in slice col // 32 at [h][col % 32]
-        assert off == (col // SLICE) * 64 * SLICE + head * SLICE + col % SLICE
-        seen[off:off + 4] += 1
+    for off, head, d in partial_store_offsets():
+        assert 0 <= off < PART_O
+        assert off == (d // SLICE) * 64 * SLICE + head * SLICE + d % SLICE
+        seen[off] += 1
     assert (seen == 1).all()
 
 
-def test_part_slots_inside_the_workspace():
-    for U, R in ((1, 1), (4, 1), (32, 1), (3, 4)):
-        total = workspace_floats(U, R)
-        o_end = U * R * MAX_CTAS * PART_O
-        for ur in range(U * R):
-            for c in range(MAX_CTAS):
-                o = (ur * MAX_CTAS + c) * PART_O
-                ml = o_end + (ur * MAX_CTAS + c) * PART_ML
-                assert o % 4 == 0 and o + PART_O <= o_end
-                assert ml % 4 == 0 and ml + PART_ML <= total
-
-
-def test_merge_reads_every_part_and_writes_every_output_once():
-    for K in (1, 128, 129, 300, 640, 1500, 2048):
-        C = attn_ctas(K)
+def test_merge_reads_every_run_and_writes_every_output_once():
+    for K in (1, 64, 65, 300, 640, 1500, 2048):
+        _, C = runs(K, 4)
         out = np.zeros((64, 512), np.int32)
         for s in range(NSLICE):
             for t in range(64 * (SLICE // 4)):
@@ -88,7 +119,5 @@ def test_merge_reads_every_part_and_writes_every_output_once():
                 for c in range(C):
                     src = c * PART_O + s * 64 * SLICE + h * SLICE + 4 * q4
                     assert src % 4 == 0 and src + 4 <= MAX_CTAS * PART_O
-                dst = h * 512 + s * SLICE + 4 * q4
-                assert dst % 4 == 0
                 out[h, s * SLICE + 4 * q4:s * SLICE + 4 * q4 + 4] += 1
         assert (out == 1).all()
