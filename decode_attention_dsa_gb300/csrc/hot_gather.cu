@@ -87,6 +87,8 @@ k_assign(const dsa_unit* __restrict__ units, int R, int K, int round,
   uint16_t* s_opc = reinterpret_cast<uint16_t*>(asm_ + (tk_in_smem ? (size_t)RK * 4 : 0));   // [RK]
   uint8_t* s_cl = reinterpret_cast<uint8_t*>(s_opc + RK);                      // [RK]
   uint8_t* s_fl = s_cl + RK;                                                   // [RK] owner flags
+  if (threadIdx.x < 4) s_cnt[threadIdx.x] = 0;   // totals: HOT, RING, RAM, owners
+  __syncthreads();
   pdl_wait();
   const dsa_unit& un = units[u];
   const int32_t epoch = (int32_t)(un.state[DSA_ST_EPOCH] + 1);
@@ -176,15 +178,17 @@ k_assign(const dsa_unit* __restrict__ units, int R, int K, int round,
     }
   }
   {
-    int t;
-    block_inclusive_scan<ASSIGN_THREADS>(hot, s_tmp, &t);
-    if (threadIdx.x == 0) s_cnt[0] = t;
-    block_inclusive_scan<ASSIGN_THREADS>(ring, s_tmp, &t);
-    if (threadIdx.x == 0) s_cnt[1] = t;
-    block_inclusive_scan<ASSIGN_THREADS>(rm, s_tmp, &t);
-    if (threadIdx.x == 0) s_cnt[2] = t;
+    // per-warp totals, one shared atomic each
+    hot = __reduce_add_sync(0xffffffffu, hot);
+    ring = __reduce_add_sync(0xffffffffu, ring);
+    rm = __reduce_add_sync(0xffffffffu, rm);
+    if ((threadIdx.x & 31) == 0) {
+      if (hot) atomicAdd(&s_cnt[0], hot);
+      if (ring) atomicAdd(&s_cnt[1], ring);
+      if (rm) atomicAdd(&s_cnt[2], rm);
+    }
   }
-  // (the scans end with a block barrier: s_tk, s_cl, s_fl are complete)
+  __syncthreads();   // s_tk, s_cl, s_fl and the totals are complete
 
   // 1. owners: the first occurrence (lowest query row) of an unmapped RAM
   //    position; per-row exclusive prefix counts of owners
@@ -247,8 +251,10 @@ k_assign(const dsa_unit* __restrict__ units, int R, int K, int round,
     }
     ++nM_local;
   }
-  int nM;
-  block_inclusive_scan<ASSIGN_THREADS>(nM_local, s_tmp, &nM);
+  nM_local = __reduce_add_sync(0xffffffffu, nM_local);
+  if ((threadIdx.x & 31) == 0 && nM_local) atomicAdd(&s_cnt[3], nM_local);
+  __syncthreads();
+  const int nM = s_cnt[3];
 
   // 3. victims in cyclic order from the hand. Ring: the eligible slots (not
   //    pinned in this call, not filled in this round). Clock: the eligible
