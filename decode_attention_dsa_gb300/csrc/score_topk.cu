@@ -199,6 +199,7 @@ struct ScoreArgs {
   int64_t stride;
   int64_t max_len;
   int tpu;              // tiles per unit
+  int cpu;              // CTAs per unit (each CTA within one unit), or 0: flattened ranges
   int U;
   int R, K;
   int nst;
@@ -234,11 +235,21 @@ __global__ void __launch_bounds__(SCORE_THREADS) k_dsa_score(const __grid_consta
   int* s_fail = reinterpret_cast<int*>(s_tmem + 1);
   const int tid = threadIdx.x, warp = tid >> 5;
 
-  // this CTA's tiles: [f0, f1) of the flattened (unit, tile) space
+  // this CTA's tiles: [f0, f1) of the flattened (unit, tile) space. With
+  // a.cpu CTAs per unit every range lies inside one unit (one query operand,
+  // one histogram flush); otherwise the flattened space is cut evenly.
   const long long total = (long long)a.U * a.tpu;
-  const long long per = (total + gridDim.x - 1) / gridDim.x;
-  const long long f0 = (long long)blockIdx.x * per;
-  const long long f1 = min(f0 + per, total);
+  long long f0, f1;
+  if (a.cpu > 0) {
+    const int uu = blockIdx.x / a.cpu, sub = blockIdx.x % a.cpu;
+    const int per = (a.tpu + a.cpu - 1) / a.cpu;
+    f0 = (long long)uu * a.tpu + min(sub * per, a.tpu);
+    f1 = (long long)uu * a.tpu + min(sub * per + per, a.tpu);
+  } else {
+    const long long per = (total + gridDim.x - 1) / gridDim.x;
+    f0 = (long long)blockIdx.x * per;
+    f1 = min(f0 + per, total);
+  }
   if (f0 >= f1) return;
   const int u0 = (int)(f0 / a.tpu);
   const int t0 = (int)(f0 - (long long)u0 * a.tpu);
@@ -1089,7 +1100,16 @@ extern "C" int dsa_score_topk(const dsa_unit* units, int32_t U, int32_t R, int32
     a.idesc = tc::idesc_bf16_f32(SCORE_TILE, score_npad(R));
     a.tmaps = tw.tmaps;
     a.dev_err = dev_err;
-    const int64_t grid = std::min<int64_t>(std::min<int64_t>(tpu * U, (int64_t)per_sm * num_sms), SCORE_MAX_GRID);
+    const int64_t slots = std::min<int64_t>((int64_t)per_sm * num_sms, SCORE_MAX_GRID);
+    int64_t grid;
+    if (U <= slots) {
+      // whole CTAs per unit
+      a.cpu = (int)std::min<int64_t>(slots / U, tpu);
+      grid = (int64_t)a.cpu * U;
+    } else {
+      a.cpu = 0;
+      grid = std::min<int64_t>(tpu * U, slots);
+    }
     if (launch_pdl(k_dsa_score, dim3((unsigned)grid), dim3(SCORE_THREADS), score_layout(R, nst).bytes + 1024, st,
                    g_tmpl[dev], a) != DSA_OK)
       return DSA_ERR_CUDA;
