@@ -135,6 +135,27 @@ def lse_bound(pair, per_q, r, i):
     return wl.scale() * 2.0 ** -11 * 2 * (q @ k.T).max(axis=1) + 1e-5
 
 
+def lse_fp16_operands(pair, per_q, r, i):
+    """log-sum-exp of one query row with the tensor cores' operands: the
+    query (bf16) and the dequantised key values (int8 * fp16 scale, RoPE bf16)
+    each rounded once to fp16 (round to nearest even, as the kernel's
+    conversions do), everything else in float64. Against this the kernel's
+    lse differs only by fp32 accumulation and exp/log evaluation (well under
+    2e-4 for these magnitudes), a check ~100x tighter than lse_bound's, which
+    has to cover the fp16 roundings themselves."""
+    from oracle.q8g64 import dequant_latent, rope_values
+    from oracle.indexer import bf16_to_f64
+    wl = pair.wl
+    rows = per_q["rows"][r][per_q["cls"][r] != PAD]
+    f16 = lambda a: np.asarray(a, np.float64).astype(np.float16).astype(np.float64)
+    k = np.concatenate([f16(dequant_latent(rows)), f16(rope_values(rows))], axis=1)
+    x = pair.last_inputs[i]
+    q = np.concatenate([f16(bf16_to_f64(x.q_lat[r])), f16(bf16_to_f64(x.q_rope[r]))], axis=1)
+    lg = wl.scale() * (q @ k.T)
+    m = lg.max(axis=1)
+    return m + np.log(np.exp(lg - m[:, None]).sum(axis=1))
+
+
 def check_step(pair: Pair, g, ores, attention=True, rows=True, full_state=True, atol_rel=1e-3):
     """Element-by-element comparison of one step; returns the worst attention error ratio."""
     worst = 0.0
@@ -177,6 +198,8 @@ def check_step(pair: Pair, g, ores, attention=True, rows=True, full_state=True, 
                     tol = lse_bound(pair, per_q=ores[u], r=r, i=i)
                     d = np.abs(g["lse"][i, r].astype(np.float64) - o["lse"][r])
                     assert (d <= tol).all(), f"unit {u} row {r}: lse err {d.max():.3e}"
+                    d16 = np.abs(g["lse"][i, r].astype(np.float64) - lse_fp16_operands(pair, ores[u], r, i))
+                    assert (d16 <= 2e-4).all(), f"unit {u} row {r}: lse vs fp16-operand lse {d16.max():.3e}"
                 else:
                     assert np.isneginf(g["lse"][i, r]).all()
     return worst
