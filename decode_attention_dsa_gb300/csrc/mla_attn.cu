@@ -517,44 +517,59 @@ k_attn_parts(int R, int H, int K, int cpp, const uint16_t* __restrict__ q_lat, c
 }
 
 // B: merge of the C runs of one (unit, query row), output columns
-// [32 s, 32 s + 32) with s = blockIdx.x.
+// [32 s, 32 s + 32) with s = blockIdx.x. The loops over the runs are unrolled
+// to MAX_CTAS with predicated loads, so every run's value is in flight at
+// once (a run-time bound would chain one L2 round trip per run).
 __global__ void __launch_bounds__(256) k_attn_merge(int H, int C, const float* __restrict__ ws_o,
                                                      const float* __restrict__ ws_ml, float* __restrict__ out,
                                                      float* __restrict__ lse) {
-  __shared__ float f[MAX_CTAS][64];   // exp(m_c - M) per part and head
+  __shared__ float f[MAX_CTAS][64];   // exp(m_c - M) per run and head
   __shared__ float inv[64];           // 1 / L per head
   const int s = blockIdx.x, ur = blockIdx.y, tid = threadIdx.x;
   pdl_wait();
   const float* ml = ws_ml + (size_t)ur * MAX_CTAS * PART_ML;
   if (tid < 64) {
     const int h = tid;
+    float mc[MAX_CTAS], lc[MAX_CTAS];
+#pragma unroll
+    for (int c = 0; c < MAX_CTAS; ++c) {
+      mc[c] = c < C ? ml[c * PART_ML + h] : -INFINITY;
+      lc[c] = c < C ? ml[c * PART_ML + 64 + h] : 0.f;
+    }
     float M = -INFINITY;
-    for (int c = 0; c < C; ++c) M = fmaxf(M, ml[c * PART_ML + h]);
+#pragma unroll
+    for (int c = 0; c < MAX_CTAS; ++c) M = fmaxf(M, mc[c]);
     float L = 0.f;
-    for (int c = 0; c < C; ++c) {
-      const float mc = ml[c * PART_ML + h];
-      const float fc = mc == -INFINITY ? 0.f : __expf(mc - M);
+#pragma unroll
+    for (int c = 0; c < MAX_CTAS; ++c) {
+      const float fc = mc[c] == -INFINITY ? 0.f : __expf(mc[c] - M);
       f[c][h] = fc;
-      L += fc * ml[c * PART_ML + 64 + h];
+      L += fc * lc[c];
     }
     inv[h] = L > 0.f ? 1.f / L : 0.f;
     if (s == 0 && lse && h < H) lse[(size_t)ur * H + h] = L > 0.f ? M + logf(L) : -INFINITY;
   }
   __syncthreads();
-  // 64 heads x 8 float4 columns
+  // 64 heads x 8 float4 columns: two items per thread
   const float* po = ws_o + (size_t)ur * MAX_CTAS * PART_O + (size_t)s * 64 * SLICE;
+#pragma unroll 1
   for (int t = tid; t < 64 * (SLICE / 4); t += 256) {
     const int h = t / (SLICE / 4), q4 = t % (SLICE / 4);
     if (h >= H) continue;
+    float4 v[MAX_CTAS];
+#pragma unroll
+    for (int c = 0; c < MAX_CTAS; ++c)
+      v[c] = (c < C && f[c][h] != 0.f)   // an empty run's block may be undefined
+                 ? reinterpret_cast<const float4*>(po + (size_t)c * PART_O + h * SLICE)[q4]
+                 : make_float4(0.f, 0.f, 0.f, 0.f);
     float4 acc = make_float4(0.f, 0.f, 0.f, 0.f);
-    for (int c = 0; c < C; ++c) {
-      const float fc = f[c][h];
-      if (fc == 0.f) continue;   // an empty part (its block may be undefined)
-      const float4 v = reinterpret_cast<const float4*>(po + (size_t)c * PART_O + h * SLICE)[q4];
-      acc.x = fmaf(fc, v.x, acc.x);
-      acc.y = fmaf(fc, v.y, acc.y);
-      acc.z = fmaf(fc, v.z, acc.z);
-      acc.w = fmaf(fc, v.w, acc.w);
+#pragma unroll
+    for (int c = 0; c < MAX_CTAS; ++c) {
+      const float fc = c < C ? f[c][h] : 0.f;
+      acc.x = fmaf(fc, v[c].x, acc.x);
+      acc.y = fmaf(fc, v[c].y, acc.y);
+      acc.z = fmaf(fc, v[c].z, acc.z);
+      acc.w = fmaf(fc, v[c].w, acc.w);
     }
     const float iv = inv[h];
     *reinterpret_cast<float4*>(out + ((size_t)ur * H + h) * 512 + s * SLICE + 4 * q4) =
