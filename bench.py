@@ -351,6 +351,9 @@ class WorkloadRun:
         self.pipeline = pipeline
         if pipeline:
             self.path.enable_pipeline()
+            # (e2e) input copies of the next step, issued on a copy stream
+            self.ev_in = [torch.cuda.Event(), torch.cuda.Event()]
+            self.ev_main_prev = torch.cuda.Event()
         torch.cuda.synchronize()
 
     def step_args(self, s):
@@ -377,14 +380,29 @@ class WorkloadRun:
             if e2e is None:
                 path.step_pipelined(rnd, *self.step_args(s))
             else:
-                host, dev_in2, out_host = e2e
+                # step s's inputs arrive in buffer i & 1 (one copy, issued on
+                # the copy stream during the step before); the copy of step
+                # s + 1 goes into the other buffer once step s - 1, its last
+                # reader, is done on both streams
+                hpack, dpack, dev_in, out_host, cs = e2e
+                main = torch.cuda.current_stream()
+                b = i & 1
+                if i == 0:
+                    cs.wait_stream(main)
+                    with torch.cuda.stream(cs):
+                        dpack[0].copy_(hpack[s], non_blocking=True)
+                    self.ev_in[0].record(cs)
+                if i + 1 < self.K:
+                    if i >= 1:
+                        cs.wait_event(self.ev_main_prev)
+                        cs.wait_event(path.ev_done)
+                    with torch.cuda.stream(cs):
+                        dpack[b ^ 1].copy_(hpack[s + 1], non_blocking=True)
+                    self.ev_in[b ^ 1].record(cs)
+                main.wait_event(self.ev_in[b])
                 names = ("q_idx", "w", "q_lat", "q_rope", "new_rows", "new_keys")
-
-                def stage(b, s=s):
-                    for n in names:
-                        dev_in2[b][n].copy_(host[n][s], non_blocking=True)
-                    return tuple(dev_in2[b][n] for n in names)
-                path.step_pipelined(rnd, *self.step_args(s), out_host=out_host[i], stage_inputs=stage)
+                path.step_pipelined(rnd, *(dev_in[b][n] for n in names), out_host=out_host[i])
+                self.ev_main_prev.record(main)
             self.ctr.add_(path.counters)
         path.join()
         ev[1].record()
@@ -404,11 +422,9 @@ class WorkloadRun:
             e = ev[i]
             e[0].record()
             if e2e is not None:
-                host, dev_in2, out_host = e2e
-                dev_in = dev_in2[0]
-                for n in dev_in:
-                    dev_in[n].copy_(host[n][s], non_blocking=True)
-                qi, w, ql, qr, nr, nk = (dev_in[n] for n in ("q_idx", "w", "q_lat", "q_rope", "new_rows", "new_keys"))
+                hpack, dpack, dev_in2, out_host, _ = e2e
+                dpack[0].copy_(hpack[s], non_blocking=True)
+                qi, w, ql, qr, nr, nk = (dev_in2[0][n] for n in ("q_idx", "w", "q_lat", "q_rope", "new_rows", "new_keys"))
             if per_call:
                 path.score_topk(qi, w)
                 e[1].record()
@@ -422,7 +438,7 @@ class WorkloadRun:
             else:
                 path.step(rnd, qi, w, ql, qr, nr, nk, side=self.side)
             if e2e is not None:
-                e2e[2][i].copy_(path.out, non_blocking=True)
+                e2e[3][i].copy_(path.out, non_blocking=True)
             e[-1].record()
             if not per_call:
                 self.ctr.add_(path.counters)
@@ -466,17 +482,27 @@ class WorkloadRun:
         return ev
 
     def e2e_buffers(self):
-        """Pinned host copies of every step's inputs, device staging buffers
-        and pinned host outputs (the inputs a caller hands over per step)."""
+        """The inputs a caller hands over per step, packed per step into one
+        pinned host buffer (the six tensors at 256-byte aligned offsets), two
+        device buffers of the same layout (alternating steps) with typed views,
+        pinned host outputs, and a copy stream."""
         torch = self.torch
         names = ["q_idx", "w", "q_lat", "q_rope", "new_rows", "new_keys"]
-        host = {n: torch.empty_like(self.inp[n], device="cpu").pin_memory() for n in names}
+        nst = self.inp[names[0]].shape[0]
+        offs, nbytes, total = {}, {}, 0
         for n in names:
-            host[n].copy_(self.inp[n])
-        dev_in = [{n: torch.empty_like(self.inp[n][0]) for n in names} for _ in range(2)]
+            nb = self.inp[n][0].numel() * self.inp[n][0].element_size()
+            offs[n], nbytes[n] = total, nb
+            total += (nb + 255) // 256 * 256
+        hpack = torch.empty((nst, total), dtype=torch.uint8).pin_memory()
+        for n in names:
+            hpack[:, offs[n]:offs[n] + nbytes[n]].copy_(self.inp[n].reshape(nst, -1).view(torch.uint8))
+        dpack = [torch.empty(total, dtype=torch.uint8, device=self.inp[names[0]].device) for _ in range(2)]
+        dev_in = [{n: dpack[b][offs[n]:offs[n] + nbytes[n]].view(self.inp[n].dtype).view(self.inp[n][0].shape)
+                   for n in names} for b in range(2)]
         out_host = torch.empty((self.K,) + tuple(self.path.out.shape), dtype=torch.float32).pin_memory()
-        h2d = sum(host[n][0].numel() * host[n][0].element_size() for n in names)
-        return (host, dev_in, out_host), h2d, self.path.out.numel() * 4
+        h2d = sum(nbytes.values())
+        return (hpack, dpack, dev_in, out_host, torch.cuda.Stream()), h2d, self.path.out.numel() * 4
 
     def close(self):
         self.units.close()
