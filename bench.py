@@ -78,8 +78,14 @@ def parse():
                     help="fused: hot_gather_attn; split: hot_gather + mla_decode_attn with the append "
                          "overlapping the attention (default: split)")
     ap.add_argument("--no-pipeline", action="store_true",
-                    help="run every step serially (no overlap of a step's gather copy and attention "
-                         "with the next step's scoring)")
+                    help="run every step serially, all units in lockstep (same as --schedule serial)")
+    ap.add_argument("--schedule", choices=["groups", "lockstep", "serial"], default=None,
+                    help="groups: the sessions in two halves, each decoding step after step on its own "
+                         "stream, so one half's gather copy and attention overlap the other half's "
+                         "scoring (the default where the workload streams more than L2 and has two or "
+                         "more sessions); lockstep: all units, each step's copy and attention overlapping "
+                         "the next step's scoring (a step's next query would have to be known before "
+                         "its attention ends); serial: one step after the other")
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--cpu-sample-steps", type=int, default=None)
     ap.add_argument("--oracle-child", type=str, default=None, help=argparse.SUPPRESS)
@@ -316,13 +322,25 @@ def traffic_for(kernel: str):
         return None
 
 
+class _UnitRange:
+    """The units [lo, hi) of a UnitSet as a unit set of their own: a copy of
+    their descriptors, the same device buffers and error word."""
+
+    def __init__(self, us, lo, hi):
+        import ctypes
+        from decode_attention_dsa_gb300 import abi
+        self.U, self.lmax, self.device, self.dev_err = hi - lo, us.lmax, us.device, us.dev_err
+        raw = us.units.view(-1, ctypes.sizeof(abi.DsaUnit))
+        self.units = raw[lo:hi].contiguous().view(-1)
+
+
 class WorkloadRun:
     """One workload on the device: unit set, decode path, inputs for W + n*K
     steps (generated on the device), and one CUDA graph per K-step segment.
     The timed segments are consecutive parts of one continuous decode, so
     every timed step selects rows no earlier step has read."""
 
-    def __init__(self, wl, K, Wm, nseg, mirror, fused, use_graph, pipeline=False):
+    def __init__(self, wl, K, Wm, nseg, mirror, fused, use_graph, pipeline="serial"):
         import torch
         from decode_attention_dsa_gb300 import abi
         from decode_attention_dsa_gb300.step import DecodePath
@@ -348,8 +366,18 @@ class WorkloadRun:
         self.warm = abi.WARM_LAST_S if wl.warm == "last_s" else abi.WARM_EMPTY
         self.ctr = torch.zeros((U, 4), dtype=torch.int64, device="cuda")
         self.next_seg = 0
-        self.pipeline = pipeline
-        if pipeline:
+        self.pipeline = pipeline == "lockstep"
+        self.groups = None
+        if pipeline == "groups":
+            # sessions [0, S/2) and [S/2, S): units are session-major
+            half = (wl.sessions // 2) * wl.layers
+            self.granges = [(0, half), (half, U)]
+            self.gpaths = [DecodePath(_UnitRange(self.units, lo, hi), wl.R, wl.K, wl.H, wl.A, wl.scale())
+                           for lo, hi in self.granges]
+            self.gstreams = [torch.cuda.Stream() for _ in self.granges]
+            self.g_assigned = [torch.cuda.Event() for _ in self.granges]
+            self.groups = True
+        if self.pipeline:
             self.path.enable_pipeline()
             # (e2e) input copies of the next step, issued on a copy stream
             self.ev_in = [torch.cuda.Event(), torch.cuda.Event()]
@@ -408,8 +436,53 @@ class WorkloadRun:
         ev[1].record()
         return [ev]
 
+    def _record_groups(self, s0, e2e=None):
+        """K steps of each session group, step after step on the group's own
+        stream (score + select, gather assignment, gather copy, attention,
+        append; a step's scoring follows the group's previous attention). The
+        groups' scorings alternate: a group scores once the other group's
+        last gather assignment is done, so each group's host-link copy runs
+        beside the other group's scoring. One event pair brackets them."""
+        torch, abi, rnd = self.torch, self.abi, self.abi.ROUND_AUTO
+        main = torch.cuda.current_stream()
+        names = ("q_idx", "w", "q_lat", "q_rope", "new_rows", "new_keys")
+        ev = [torch.cuda.Event(enable_timing=True, external=self.use_graph) for _ in range(2)]
+        ev[0].record()
+        for st in self.gstreams:
+            st.wait_stream(main)
+        for i in range(self.K):
+            s = s0 + i
+            for g, ((lo, hi), p, st) in enumerate(zip(self.granges, self.gpaths, self.gstreams)):
+                u = p.u
+                with torch.cuda.stream(st):
+                    if e2e is None:
+                        qi, w, ql, qr, nr, nk = tuple(x[lo:hi] for x in self.step_args(s))
+                    else:
+                        hpack, dpack, dev_in, out_host, _ = e2e[g]
+                        dpack[0].copy_(hpack[s], non_blocking=True)
+                        qi, w, ql, qr, nr, nk = (dev_in[0][n] for n in names)
+                    if i > 0 or g > 0:
+                        st.wait_event(self.g_assigned[1 - g])
+                    p.score_topk(qi, w, st)
+                    abi.hot_gather_assign(u.units, u.U, p.R, p.K, rnd, p.topk, p.cls, p.counters, p.ws_gather,
+                                          p.ws_gather_bytes, u.dev_err, st)
+                    self.g_assigned[g].record(st)
+                    abi.hot_gather_copy(u.units, u.U, p.R, p.K, p.topk, p.cls, p.rows, p.ws_gather,
+                                        p.ws_gather_bytes, u.dev_err, st)
+                    p.attend(ql, qr, st)
+                    p.append(nr, nk, st)
+                    if e2e is not None:
+                        out_host[i].copy_(p.out, non_blocking=True)
+                    self.ctr[lo:hi].add_(p.counters)
+        for st in self.gstreams:
+            main.wait_stream(st)
+        ev[1].record()
+        return [ev]
+
     def _record(self, s0, per_call, e2e=None):
         torch, path, rnd = self.torch, self.path, self.abi.ROUND_AUTO
+        if self.groups and not per_call:
+            return self._record_groups(s0, e2e)
         if self.pipeline and not per_call:
             return self._record_pipelined(s0, e2e)
         nev = 5 if per_call else 2
@@ -481,28 +554,40 @@ class WorkloadRun:
             raise RuntimeError(f"device error word {err:#x}")
         return ev
 
-    def e2e_buffers(self):
-        """The inputs a caller hands over per step, packed per step into one
-        pinned host buffer (the six tensors at 256-byte aligned offsets), two
-        device buffers of the same layout (alternating steps) with typed views,
-        pinned host outputs, and a copy stream."""
+    def _pack(self, lo, hi, out_shape):
+        """Packed per-step inputs of units [lo, hi): one pinned host buffer
+        per step (the six tensors at 256-byte aligned offsets), two device
+        buffers of that layout with typed views, pinned host outputs, a copy
+        stream; and the bytes in and out per step."""
         torch = self.torch
         names = ["q_idx", "w", "q_lat", "q_rope", "new_rows", "new_keys"]
         nst = self.inp[names[0]].shape[0]
+        src = {n: self.inp[n][:, lo:hi] for n in names}
         offs, nbytes, total = {}, {}, 0
         for n in names:
-            nb = self.inp[n][0].numel() * self.inp[n][0].element_size()
+            nb = src[n][0].numel() * src[n][0].element_size()
             offs[n], nbytes[n] = total, nb
             total += (nb + 255) // 256 * 256
         hpack = torch.empty((nst, total), dtype=torch.uint8).pin_memory()
         for n in names:
-            hpack[:, offs[n]:offs[n] + nbytes[n]].copy_(self.inp[n].reshape(nst, -1).view(torch.uint8))
-        dpack = [torch.empty(total, dtype=torch.uint8, device=self.inp[names[0]].device) for _ in range(2)]
-        dev_in = [{n: dpack[b][offs[n]:offs[n] + nbytes[n]].view(self.inp[n].dtype).view(self.inp[n][0].shape)
+            hpack[:, offs[n]:offs[n] + nbytes[n]].copy_(src[n].reshape(nst, -1).view(torch.uint8))
+        dev = self.inp[names[0]].device
+        dpack = [torch.empty(total, dtype=torch.uint8, device=dev) for _ in range(2)]
+        dev_in = [{n: dpack[b][offs[n]:offs[n] + nbytes[n]].view(src[n].dtype).view(src[n][0].shape)
                    for n in names} for b in range(2)]
-        out_host = torch.empty((self.K,) + tuple(self.path.out.shape), dtype=torch.float32).pin_memory()
-        h2d = sum(nbytes.values())
-        return (hpack, dpack, dev_in, out_host, torch.cuda.Stream()), h2d, self.path.out.numel() * 4
+        out_host = torch.empty((self.K,) + tuple(out_shape), dtype=torch.float32).pin_memory()
+        nout = 1
+        for x in out_shape:
+            nout *= x
+        return (hpack, dpack, dev_in, out_host, torch.cuda.Stream()), sum(nbytes.values()), nout * 4
+
+    def e2e_buffers(self):
+        """The inputs a caller hands over per step and the outputs it reads
+        back (per session group with the group schedule)."""
+        if self.groups:
+            packs = [self._pack(lo, hi, p.out.shape) for (lo, hi), p in zip(self.granges, self.gpaths)]
+            return [x[0] for x in packs], sum(x[1] for x in packs), sum(x[2] for x in packs)
+        return self._pack(0, self.wl.U, self.path.out.shape)
 
     def close(self):
         self.units.close()
@@ -564,12 +649,20 @@ L2_BYTES = 126 << 20
 
 
 def use_pipeline(args, wl):
-    """Steps overlap (gather copy and attention with the next step's scoring)
-    where the path allows it (one appended row, no selection reuse, split
-    path) and every step streams more than L2 holds, so that no L2 flush is
-    needed between the steps."""
-    return (not args.no_pipeline and wl.A == 1 and wl.reuse_every == 1 and args.path != "fused"
-            and wl.U * wl.L0 * 128 > 4 * L2_BYTES)
+    """The step schedule: "groups" (two halves of the sessions, each decoding
+    step after step on its own stream, overlapping each other) or "lockstep"
+    (every unit; a step's gather copy and attention overlap the next step's
+    scoring) where the path allows it (one appended row, no selection reuse,
+    split path) and every step streams more than L2 holds, so that no L2 flush
+    is needed between the steps; else "serial" (no overlap)."""
+    if args.no_pipeline or args.schedule == "serial":
+        return "serial"
+    ok = (wl.A == 1 and wl.reuse_every == 1 and args.path != "fused" and wl.U * wl.L0 * 128 > 4 * L2_BYTES)
+    if not ok:
+        return "serial"
+    if args.schedule == "lockstep" or wl.sessions < 2:
+        return "lockstep"
+    return "groups"
 
 
 def measure(args, wl, K, Wm, mirror, reps, world, clocks=None, e2e=False, breakdown=True):
@@ -601,8 +694,9 @@ def measure(args, wl, K, Wm, mirror, reps, world, clocks=None, e2e=False, breakd
         torch.distributed.all_reduce(t, op=torch.distributed.ReduceOp.MAX)
         total_ms = float(t.item())
     import numpy as np
+    lps = sum(p.launches_per_step() for p in run.gpaths) if run.groups else path.launches_per_step()
     res = {"run": run, "totals_ms": totals, "total_ms": total_ms, "ctr": np.mean(ctrs, axis=0),
-           "launches_per_step": path.launches_per_step()}
+           "launches_per_step": lps}
     if breakdown:
         per = []
         for seg in bds:
@@ -704,12 +798,16 @@ def run_gpu(args, rank: int, world: int):
         "data": "synthetic (seeded counter-based generator, generated on the device)",
         "config": workload_config(wl, {
             "mirror": args.mirror, "replacement": wl.policy,
-            "l2": ("not flushed: every step streams more than L2 holds (keys of all units)" if pipe else
+            "l2": ("not flushed: every step streams more than L2 holds (keys of all units)" if pipe != "serial" else
                    "flushed before every timed step (512 MiB write outside the bracket)"),
             "selection_reuse_every": wl.reuse_every,
-            "path": "hot_gather_attn (fused)" if args.path == "fused" else
-                    ("pipelined: each step's gather copy and attention (side stream) overlap the next "
-                     "step's score and select" if pipe else "hot_gather + mla_decode_attn, append concurrent"),
+            "path": "hot_gather_attn (fused)" if args.path == "fused" else {
+                "groups": ("two session groups (sessions [0, S/2) and [S/2, S)), each decoding step after "
+                           "step on its own stream (score, select, gather, attention, append); one group's "
+                           "gather copy and attention overlap the other group's scoring"),
+                "lockstep": ("lockstep pipeline: each step's gather copy and attention (side stream) overlap "
+                             "the next step's score and select"),
+                "serial": "hot_gather + mla_decode_attn, append concurrent"}[pipe],
             "timing": f"median of {reps} consecutive {K}-step segments of one decode (one CUDA graph each) "
                       f"after {Wm} warm-up steps",
             "parallelism": "replicas" if world > 1 else "single GPU"}),

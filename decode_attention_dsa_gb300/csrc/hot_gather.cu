@@ -52,6 +52,12 @@ constexpr int COPY_WARPS = COPY_THREADS / 32;
 // 0.90 vs 1.02 ms per step on 32 units x Top-2048 with 1 vs 4 blocks per SM.
 constexpr int COPY_BLOCKS_PER_SM = 4;
 constexpr int64_t COPY_BW_ENTRIES = 65536;
+// Between COPY_MID_ENTRIES and COPY_BW_ENTRIES the kernel decides itself: if
+// the call's fills (rows read over the host link) reach COPY_BW_FILLS, only
+// one block per SM copies (the rest leave at once); a call with that many
+// selected entries but few misses stays latency-bound and keeps them all.
+constexpr int64_t COPY_MID_ENTRIES = 16384;
+constexpr int COPY_BW_FILLS = 16384;
 
 // lower_bound of p in an ascending row whose tail is -1 padding (-1 = +inf).
 __device__ __forceinline__ int row_lower_bound(const int32_t* row, int K, int32_t p) {
@@ -344,17 +350,33 @@ k_assign(const dsa_unit* __restrict__ units, int R, int K, int round,
 
 __global__ void __launch_bounds__(COPY_THREADS)
 k_copy(const dsa_unit* __restrict__ units, int U, int R, int K, const int32_t* __restrict__ topk_all,
-       const uint8_t* __restrict__ cls_all, uint8_t* __restrict__ rows_all, GatherWs g, int32_t* dev_err) {
+       const uint8_t* __restrict__ cls_all, uint8_t* __restrict__ rows_all, GatherWs g, int32_t* dev_err,
+       int bw_blocks) {
   const int lane = threadIdx.x & 31;
   pdl_wait();
   const int RK = R * K;
+  int nblocks = gridDim.x;
+  if (bw_blocks > 0) {
+    __shared__ int s_fills;
+    if (threadIdx.x == 0) s_fills = 0;
+    __syncthreads();
+    int f = 0;
+    for (int u = threadIdx.x; u < U; u += COPY_THREADS) f += g.nfill[u];
+    f = __reduce_add_sync(0xffffffffu, f);
+    if ((threadIdx.x & 31) == 0 && f) atomicAdd(&s_fills, f);
+    __syncthreads();
+    if (s_fills >= COPY_BW_FILLS) {
+      if ((int)blockIdx.x >= bw_blocks) return;   // (the whole block)
+      nblocks = bw_blocks;
+    }
+  }
   // warps walk the flattened (unit, item) space in order: per unit its RK
   // entries, then its fills in ascending position order (mirror rows are
   // read in position order, unit by unit, which suits the host's page
   // translations)
   const int64_t nitems = (int64_t)U * 2 * RK;
   for (int64_t idx = (int64_t)blockIdx.x * COPY_WARPS + (threadIdx.x >> 5); idx < nitems;
-       idx += (int64_t)gridDim.x * COPY_WARPS) {
+       idx += (int64_t)nblocks * COPY_WARPS) {
     const int u = (int)(idx / (2 * RK));
     const int item = (int)(idx - (int64_t)u * 2 * RK);
     const dsa_unit& un = units[u];
@@ -474,8 +496,11 @@ extern "C" int hot_gather_copy(const dsa_unit* units, int32_t U, int32_t R, int3
   const int64_t per_sm = entries >= COPY_BW_ENTRIES ? 1 : COPY_BLOCKS_PER_SM;
   const int64_t blocks = std::max<int64_t>(
       1, std::min<int64_t>((2 * entries + COPY_WARPS - 1) / COPY_WARPS, per_sm * pd.num_sms[dev]));
+  // mid-size calls: one block per SM if the fills turn out to bind on the host link
+  const int bw_blocks = (entries >= COPY_MID_ENTRIES && entries < COPY_BW_ENTRIES) ? pd.num_sms[dev] : 0;
   return launch_pdl(k_copy, dim3((unsigned)blocks), dim3(COPY_THREADS), 0, static_cast<cudaStream_t>(stream),
-                    units, (int)U, (int)R, (int)K, topk_idx, cls, rows, gather_ws(ws, U, R, K), dev_err);
+                    units, (int)U, (int)R, (int)K, topk_idx, cls, rows, gather_ws(ws, U, R, K), dev_err,
+                    bw_blocks);
 }
 
 extern "C" int hot_gather(const dsa_unit* units, int32_t U, int32_t R, int32_t K, int32_t round,
