@@ -322,18 +322,6 @@ def traffic_for(kernel: str):
         return None
 
 
-class _UnitRange:
-    """The units [lo, hi) of a UnitSet as a unit set of their own: a copy of
-    their descriptors, the same device buffers and error word."""
-
-    def __init__(self, us, lo, hi):
-        import ctypes
-        from decode_attention_dsa_gb300 import abi
-        self.U, self.lmax, self.device, self.dev_err = hi - lo, us.lmax, us.device, us.dev_err
-        raw = us.units.view(-1, ctypes.sizeof(abi.DsaUnit))
-        self.units = raw[lo:hi].contiguous().view(-1)
-
-
 class WorkloadRun:
     """One workload on the device: unit set, decode path, inputs for W + n*K
     steps (generated on the device), and one CUDA graph per K-step segment.
@@ -372,7 +360,7 @@ class WorkloadRun:
             # sessions [0, S/2) and [S/2, S): units are session-major
             half = (wl.sessions // 2) * wl.layers
             self.granges = [(0, half), (half, U)]
-            self.gpaths = [DecodePath(_UnitRange(self.units, lo, hi), wl.R, wl.K, wl.H, wl.A, wl.scale())
+            self.gpaths = [DecodePath(self.units.subset(lo, hi), wl.R, wl.K, wl.H, wl.A, wl.scale())
                            for lo, hi in self.granges]
             self.gstreams = [torch.cuda.Stream() for _ in self.granges]
             self.g_assigned = [torch.cuda.Event() for _ in self.granges]

@@ -127,6 +127,13 @@ class UnitSet:
     def check(self) -> int:
         return int(self.dev_err.item())
 
+    def subset(self, lo: int, hi: int) -> "UnitRange":
+        """Units [lo, hi) as a unit set of their own, for a DecodePath that
+        runs them apart from the others (for example two groups of sessions
+        decoding on two streams). Same device buffers and error word."""
+        return UnitRange(self, lo, hi)
+
+
     def close(self) -> None:
         if self._host_ptr is not None:
             torch.cuda.synchronize(self.device)
@@ -139,3 +146,22 @@ class UnitSet:
             self.close()
         except Exception:
             pass
+
+
+class UnitRange:
+    """Units [lo, hi) of a UnitSet: a device copy of their ``dsa_unit``
+    descriptors (pointing at the parent's buffers), the parent's error word.
+    Calls on different ranges touch disjoint units and may run concurrently;
+    calls on one range follow the C ABI's ordering rules."""
+
+    def __init__(self, parent: UnitSet, lo: int, hi: int):
+        if not (0 <= lo < hi <= parent.U):
+            raise ValueError(f"unit range [{lo}, {hi}) outside [0, {parent.U})")
+        self.parent, self.lo, self.hi = parent, lo, hi
+        self.U, self.S, self.lmax, self.device = hi - lo, parent.S, parent.lmax, parent.device
+        self.dev_err = parent.dev_err
+        raw = parent.units.view(-1, ctypes.sizeof(abi.DsaUnit))
+        self.units = raw[lo:hi].contiguous().view(-1)
+
+    def check(self) -> int:
+        return self.parent.check()

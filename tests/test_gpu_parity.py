@@ -107,6 +107,56 @@ FUSED = [
 ]
 
 
+def test_two_session_groups_on_two_streams():
+    """Two groups of sessions, each with its own DecodePath over its units
+    (UnitSet.subset) and its own stream, the groups' scorings alternating
+    through events as in the bench's group schedule: within a step one group's
+    gather copy, attention and append run beside the other group's scoring.
+    After every step every unit matches the oracle (selection, classes,
+    counters, gathered rows, cache state, attention)."""
+    import torch
+    from decode_attention_dsa_gb300.step import DecodePath
+    from oracle.decode import decode_step
+    wl = W.WORKLOADS[0].with_(name="groups", sessions=2, layers=2, L0=3000, S=256, K=256, H=16, steps=6,
+                              warm="last_s")
+    pair = Pair(wl)
+    pair.check_slots = True
+    abi = pair.abi
+    ranges = [(0, 2), (2, 4)]
+    paths = [DecodePath(pair.g.subset(lo, hi), wl.R, wl.K, wl.H, wl.A, wl.scale()) for lo, hi in ranges]
+    streams = [torch.cuda.Stream() for _ in ranges]
+    assigned = [torch.cuda.Event() for _ in ranges]
+    for st in streams:
+        st.wait_stream(torch.cuda.current_stream())
+    for step in range(wl.steps):
+        per, t = pair.inputs(step)
+        for g, ((lo, hi), p, st) in enumerate(zip(ranges, paths, streams)):
+            u = p.u
+            with torch.cuda.stream(st):
+                if step > 0 or g > 0:
+                    st.wait_event(assigned[1 - g])
+                p.score_topk(t["q_idx"][lo:hi], t["w"][lo:hi], st)
+                abi.hot_gather_assign(u.units, u.U, p.R, p.K, step, p.topk, p.cls, p.counters, p.ws_gather,
+                                      p.ws_gather_bytes, u.dev_err, st)
+                assigned[g].record(st)
+                abi.hot_gather_copy(u.units, u.U, p.R, p.K, p.topk, p.cls, p.rows, p.ws_gather,
+                                    p.ws_gather_bytes, u.dev_err, st)
+                p.attend(t["q_lat"][lo:hi], t["q_rope"][lo:hi], st)
+                p.append(t["new_rows"][lo:hi], t["new_keys"][lo:hi], st)
+        torch.cuda.synchronize()
+        cat = lambda name: np.concatenate([getattr(p, name).cpu().numpy() for p in paths])
+        g = dict(topk=cat("topk"), cls=cat("cls"), counters=cat("counters"), out=cat("out"), lse=cat("lse"),
+                 rows=cat("rows"))
+        pair.last_inputs = per
+        ores = {}
+        for i, u in enumerate(pair.uidx):
+            x = per[i]
+            ores[u] = decode_step(pair.o[u], step, wl.K, wl.scale(), x.q_idx, x.w, x.q_lat, x.q_rope,
+                                  x.new_rows, x.new_keys, attention=True)
+        check_step(pair, g, ores)
+        assert pair.g.check() == 0
+
+
 @pytest.mark.parametrize("wl", FUSED, ids=[w.name[:12] for w in FUSED])
 def test_fused_gather_attention(wl):
     """hot_gather_attn: same classification, state, slot bytes and attention
