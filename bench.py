@@ -79,13 +79,18 @@ def parse():
                          "overlapping the attention (default: split)")
     ap.add_argument("--no-pipeline", action="store_true",
                     help="run every step serially, all units in lockstep (same as --schedule serial)")
-    ap.add_argument("--schedule", choices=["groups", "lockstep", "serial"], default=None,
-                    help="groups: the sessions in two halves, each decoding step after step on its own "
-                         "stream, so one half's gather copy and attention overlap the other half's "
-                         "scoring (the default where the workload streams more than L2 and has two or "
-                         "more sessions); lockstep: all units, each step's copy and attention overlapping "
-                         "the next step's scoring (a step's next query would have to be known before "
-                         "its attention ends); serial: one step after the other")
+    ap.add_argument("--score-sms", type=int, default=SCORE_SMS,
+                    help="partition schedule: SMs of the partition the scoring runs on")
+    ap.add_argument("--schedule", choices=["partition", "groups", "lockstep", "serial"], default=None,
+                    help="partition: the sessions in two halves, each decoding step after step; the GPU "
+                         "split into two SM partitions, every scoring on the first, the rest of each step "
+                         "on the second, so one half's selection, gather and attention run beside the "
+                         "other half's scoring (the default where the workload streams more than L2 and "
+                         "has two or more sessions); groups: the same halves on ordinary streams, one "
+                         "half's gather copy and attention overlapping the other half's scoring; "
+                         "lockstep: all units, each step's copy and attention overlapping the next step's "
+                         "scoring (a step's next query would have to be known before its attention "
+                         "ends); serial: one step after the other")
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--cpu-sample-steps", type=int, default=None)
     ap.add_argument("--oracle-child", type=str, default=None, help=argparse.SUPPRESS)
@@ -328,7 +333,7 @@ class WorkloadRun:
     The timed segments are consecutive parts of one continuous decode, so
     every timed step selects rows no earlier step has read."""
 
-    def __init__(self, wl, K, Wm, nseg, mirror, fused, use_graph, pipeline="serial"):
+    def __init__(self, wl, K, Wm, nseg, mirror, fused, use_graph, pipeline="serial", score_sms=None):
         import torch
         from decode_attention_dsa_gb300 import abi
         from decode_attention_dsa_gb300.step import DecodePath
@@ -356,7 +361,8 @@ class WorkloadRun:
         self.next_seg = 0
         self.pipeline = pipeline == "lockstep"
         self.groups = None
-        if pipeline == "groups":
+        self.part = None
+        if pipeline in ("groups", "partition"):
             # sessions [0, S/2) and [S/2, S): units are session-major
             half = (wl.sessions // 2) * wl.layers
             self.granges = [(0, half), (half, U)]
@@ -365,6 +371,19 @@ class WorkloadRun:
             self.gstreams = [torch.cuda.Stream() for _ in self.granges]
             self.g_assigned = [torch.cuda.Event() for _ in self.granges]
             self.groups = True
+        if pipeline == "partition":
+            # the scorings run on one SM partition, the rest of the steps on the other
+            assert not use_graph, "a partition's streams are not captured into a CUDA graph"
+            self.part, self.rest = abi.dsa_partition_split(score_sms or SCORE_SMS)
+            self.part_sms, self.rest_sms = abi.dsa_partition_sms(self.part), abi.dsa_partition_sms(self.rest)
+            self.pstream = abi.dsa_partition_stream(self.part)
+            self.tstreams = [abi.dsa_partition_stream(self.rest) for _ in self.granges]
+            self.text = [torch.cuda.ExternalStream(st) for st in self.tstreams]
+            # the gathers read the host mirrors from the second partition
+            abi.dsa_touch_mirror(self.units.units, U, wlr.lmax, self.tstreams[0])
+            abi.dsa_stream_wait_stream(torch.cuda.current_stream(), self.tstreams[0])
+            # (e2e) a group's host copies run on an ordinary stream of their own
+            self.cstreams = [torch.cuda.Stream() for _ in self.granges]
         if self.pipeline:
             self.path.enable_pipeline()
             # (e2e) input copies of the next step, issued on a copy stream
@@ -467,8 +486,69 @@ class WorkloadRun:
         ev[1].record()
         return [ev]
 
+    def _record_partition(self, s0, e2e=None):
+        """K steps of each session group, step after step on the group's own
+        stream of the second SM partition, with every scoring on the first
+        partition's stream (the groups' scorings alternate there): a group's
+        selection, gather assignment and copy, attention and append run on
+        their own SMs beside the other group's scoring. A group's scoring
+        follows its previous step; its selection follows its scoring. With
+        e2e, a group's input and output copies run on an ordinary copy stream
+        between its steps. One event pair brackets them."""
+        torch, abi, rnd = self.torch, self.abi, self.abi.ROUND_AUTO
+        main = torch.cuda.current_stream()
+        names = ("q_idx", "w", "q_lat", "q_rope", "new_rows", "new_keys")
+        ev = [torch.cuda.Event(enable_timing=True) for _ in range(2)]
+        ev[0].record()
+        for ts in self.tstreams + [self.pstream]:
+            abi.dsa_stream_wait_stream(ts, main)
+        for cs in self.cstreams:
+            cs.wait_stream(main)
+        for i in range(self.K):
+            s = s0 + i
+            for g, ((lo, hi), p, ts) in enumerate(zip(self.granges, self.gpaths, self.tstreams)):
+                u = p.u
+                if e2e is None:
+                    qi, w, ql, qr, nr, nk = tuple(x[lo:hi] for x in self.step_args(s))
+                    abi.dsa_stream_wait_stream(self.pstream, ts)
+                else:
+                    # this step's inputs over the previous step's (whose last
+                    # readers are on the group's stream)
+                    hpack, dpack, dev_in, out_host, _ = e2e[g]
+                    cs = self.cstreams[g]
+                    abi.dsa_stream_wait_stream(cs, ts)
+                    with torch.cuda.stream(cs):
+                        dpack[0].copy_(hpack[s], non_blocking=True)
+                    qi, w, ql, qr, nr, nk = (dev_in[0][n] for n in names)
+                    abi.dsa_stream_wait_stream(self.pstream, cs)
+                p.score(qi, w, self.pstream)
+                abi.dsa_stream_wait_stream(ts, self.pstream)
+                p.select(ts)
+                abi.hot_gather_assign(u.units, u.U, p.R, p.K, rnd, p.topk, p.cls, p.counters, p.ws_gather,
+                                      p.ws_gather_bytes, u.dev_err, ts)
+                abi.hot_gather_copy(u.units, u.U, p.R, p.K, p.topk, p.cls, p.rows, p.ws_gather,
+                                    p.ws_gather_bytes, u.dev_err, ts)
+                p.attend(ql, qr, ts)
+                p.append(nr, nk, ts)
+                with torch.cuda.stream(self.text[g]):
+                    self.ctr[lo:hi].add_(p.counters)
+                if e2e is not None:
+                    # the step's output to the host; the next step's attention
+                    # (after its scoring, after its input copy) waits for it
+                    abi.dsa_stream_wait_stream(cs, ts)
+                    with torch.cuda.stream(cs):
+                        out_host[i].copy_(p.out, non_blocking=True)
+        for ts in self.tstreams:
+            abi.dsa_stream_wait_stream(main, ts)
+        for cs in self.cstreams:
+            main.wait_stream(cs)
+        ev[1].record()
+        return [ev]
+
     def _record(self, s0, per_call, e2e=None):
         torch, path, rnd = self.torch, self.path, self.abi.ROUND_AUTO
+        if self.part is not None and not per_call:
+            return self._record_partition(s0, e2e)
         if self.groups and not per_call:
             return self._record_groups(s0, e2e)
         if self.pipeline and not per_call:
@@ -578,6 +658,10 @@ class WorkloadRun:
         return self._pack(0, self.wl.U, self.path.out.shape)
 
     def close(self):
+        if self.part is not None:
+            self.abi.dsa_partition_destroy(self.part)
+            self.abi.dsa_partition_destroy(self.rest)
+            self.part = self.rest = None
         self.units.close()
         del self.inp, self.flush
         self.torch.cuda.synchronize()
@@ -632,13 +716,16 @@ def measure_restore(run, n_units):
 
 
 BREAKDOWN_SEGS = 3
+SCORE_SMS = 104           # partition schedule: SMs the scorings run on
 E2E_SEGS = 3
 L2_BYTES = 126 << 20
 
 
 def use_pipeline(args, wl):
-    """The step schedule: "groups" (two halves of the sessions, each decoding
-    step after step on its own stream, overlapping each other) or "lockstep"
+    """The step schedule: "partition" (two halves of the sessions, each
+    decoding step after step, every scoring on one SM partition and the rest
+    of the steps on the other), "groups" (the same halves on ordinary streams,
+    overlapping each other) or "lockstep"
     (every unit; a step's gather copy and attention overlap the next step's
     scoring) where the path allows it (one appended row, no selection reuse,
     split path) and every step streams more than L2 holds, so that no L2 flush
@@ -650,7 +737,7 @@ def use_pipeline(args, wl):
         return "serial"
     if args.schedule == "lockstep" or wl.sessions < 2:
         return "lockstep"
-    return "groups"
+    return "groups" if args.schedule == "groups" else "partition"
 
 
 def measure(args, wl, K, Wm, mirror, reps, world, clocks=None, e2e=False, breakdown=True):
@@ -659,11 +746,16 @@ def measure(args, wl, K, Wm, mirror, reps, world, clocks=None, e2e=False, breakd
     with events around each call, calls serial), the cache counters and
     (optionally) e2e over 3 more segments. Returns a dict."""
     import torch
-    use_graph = not args.no_graph
+    sched = use_pipeline(args, wl)
+    use_graph = not args.no_graph and sched != "partition"
     fused = args.path == "fused"
-    nseg = reps + (BREAKDOWN_SEGS if breakdown else 0) + (E2E_SEGS if e2e else 0)
-    run = WorkloadRun(wl, K, Wm, nseg, mirror, fused, use_graph, pipeline=use_pipeline(args, wl))
+    # the partition schedule's kernels load into their green contexts at
+    # their first launches there: one untimed segment first
+    warm_seg = 1 if sched == "partition" else 0
+    nseg = warm_seg + reps + (BREAKDOWN_SEGS if breakdown else 0) + (E2E_SEGS if e2e else 0)
+    run = WorkloadRun(wl, K, Wm, nseg, mirror, fused, use_graph, pipeline=sched, score_sms=args.score_sms)
     path, U = run.path, wl.U
+    warm = [run.segment() for _ in range(warm_seg)]
     heads = [run.segment() for _ in range(reps)]
     bds = [run.segment(per_call=True) for _ in range(BREAKDOWN_SEGS)] if breakdown else []
     e2e_bufs = None
@@ -671,6 +763,8 @@ def measure(args, wl, K, Wm, mirror, reps, world, clocks=None, e2e=False, breakd
         e2e_bufs, h2d, d2h = run.e2e_buffers()
         e2es = [run.segment(e2e=e2e_bufs) for _ in range(E2E_SEGS)]
     run.start()
+    for seg in warm:
+        run.run_segment(seg)
     totals, ctrs = [], []
     for seg in heads:
         ev = run.run_segment(seg, clocks=clocks)
@@ -790,14 +884,21 @@ def run_gpu(args, rank: int, world: int):
                    "flushed before every timed step (512 MiB write outside the bracket)"),
             "selection_reuse_every": wl.reuse_every,
             "path": "hot_gather_attn (fused)" if args.path == "fused" else {
+                "partition": ("two session groups (sessions [0, S/2) and [S/2, S)), each decoding step after "
+                              "step; the GPU split into two SM partitions (green contexts): every scoring runs "
+                              f"on the first ({getattr(run, 'part_sms', 0)} SMs), the groups' scorings "
+                              "alternating there; a group's selection, gather, attention and append run on the "
+                              f"second ({getattr(run, 'rest_sms', 0)} SMs), beside the other group's scoring"),
                 "groups": ("two session groups (sessions [0, S/2) and [S/2, S)), each decoding step after "
                            "step on its own stream (score, select, gather, attention, append); one group's "
                            "gather copy and attention overlap the other group's scoring"),
                 "lockstep": ("lockstep pipeline: each step's gather copy and attention (side stream) overlap "
                              "the next step's score and select"),
                 "serial": "hot_gather + mla_decode_attn, append concurrent"}[pipe],
-            "timing": f"median of {reps} consecutive {K}-step segments of one decode (one CUDA graph each) "
-                      f"after {Wm} warm-up steps",
+            "timing": f"median of {reps} consecutive {K}-step segments of one decode "
+                      f"({'one CUDA graph each' if run.use_graph else 'launched directly'}) "
+                      f"after {Wm} warm-up steps"
+                      + (f" and one untimed {K}-step segment of the schedule" if pipe == "partition" else ""),
             "parallelism": "replicas" if world > 1 else "single GPU"}),
         "tok_per_s": value * wl.A / wl.layers,
         "segments_ms_per_step": [t / K for t in res["totals_ms"]],
@@ -808,7 +909,7 @@ def run_gpu(args, rank: int, world: int):
                              f"call, calls serial ({res['breakdown_step_ms']:.4f} ms/step there)")
     line["clocks"] = clk
     line["gpu_launches"] = res["launches_per_step"] * K
-    line["cuda_graph"] = not args.no_graph
+    line["cuda_graph"] = run.use_graph
     if "e2e" in res:
         line["e2e"] = res["e2e"]
     run.close()

@@ -58,8 +58,16 @@ SIGNATURES = {
     "dsa_host_alloc": (ctypes.c_int, [ctypes.POINTER(_VP), ctypes.POINTER(_VP), _SZ]),
     "dsa_host_free": (ctypes.c_int, [_VP]),
     "hc_init": (ctypes.c_int, [_VP, _I32, _I32, _VP, _I32, _I64, _VP, _VP]),
+    "dsa_touch_mirror": (ctypes.c_int, [_VP, _I32, _I64, _VP]),
     "dsa_score_topk_workspace": (_SZ, [_I32, _I32, _I64]),
     "dsa_score_topk": (ctypes.c_int, [_VP, _I32, _I32, _I32, _VP, _VP, _VP, _I64, _VP, _SZ, _VP, _VP]),
+    "dsa_score": (ctypes.c_int, [_VP, _I32, _I32, _I32, _VP, _VP, _I64, _VP, _SZ, _VP, _VP]),
+    "dsa_topk_select": (ctypes.c_int, [_VP, _I32, _I32, _I32, _VP, _I64, _VP, _SZ, _VP, _VP]),
+    "dsa_partition_split": (ctypes.c_int, [_I32, ctypes.POINTER(_VP), ctypes.POINTER(_VP)]),
+    "dsa_partition_sms": (ctypes.c_int, [_VP]),
+    "dsa_partition_stream": (ctypes.c_int, [_VP, ctypes.POINTER(_VP)]),
+    "dsa_stream_wait_stream": (ctypes.c_int, [_VP, _VP]),
+    "dsa_partition_destroy": (ctypes.c_int, [_VP]),
     "dsa_score_topk_noalloc": (ctypes.c_int, [_VP, _I32, _I32, _I32, _VP, _VP, _VP, _I64, _VP, _VP]),
     "dsa_reuse_selection": (ctypes.c_int, [_VP, _VP, _I32, _I32, _I32, _I32, _VP, _VP, _VP]),
     "hot_gather_workspace": (_SZ, [_I32, _I32, _I32]),
@@ -160,6 +168,10 @@ def hc_init(units, U, warm, l0, max_slots, max_lmax, dev_err, stream=None):
                                          _p(dev_err), _s(stream)))
 
 
+def dsa_touch_mirror(units, U, max_lmax, stream=None):
+    return _ok("dsa_touch_mirror", load().dsa_touch_mirror(_p(units), U, max_lmax, _s(stream)))
+
+
 def dsa_score_topk_workspace(U, R, max_len) -> int:
     return load().dsa_score_topk_workspace(U, R, max_len)
 
@@ -168,6 +180,44 @@ def dsa_score_topk(units, U, R, K, q, w, topk_idx, max_len, ws, ws_bytes, dev_er
     return _ok("dsa_score_topk", load().dsa_score_topk(
         _p(units), U, R, K, _p(q), _p(w), _p(topk_idx), max_len, _p(ws), ws_bytes, _p(dev_err),
         _s(stream)))
+
+
+def dsa_score(units, U, R, K, q, w, max_len, ws, ws_bytes, dev_err, stream=None):
+    return _ok("dsa_score", load().dsa_score(
+        _p(units), U, R, K, _p(q), _p(w), max_len, _p(ws), ws_bytes, _p(dev_err), _s(stream)))
+
+
+def dsa_topk_select(units, U, R, K, topk_idx, max_len, ws, ws_bytes, dev_err, stream=None):
+    return _ok("dsa_topk_select", load().dsa_topk_select(
+        _p(units), U, R, K, _p(topk_idx), max_len, _p(ws), ws_bytes, _p(dev_err), _s(stream)))
+
+
+def dsa_partition_split(min_sms: int, first: bool = True, second: bool = True):
+    """Split the current device's SMs: returns (first, second) partition
+    handles (None where not asked for)."""
+    p1, p2 = _VP(), _VP()
+    _ok("dsa_partition_split", load().dsa_partition_split(
+        int(min_sms), ctypes.byref(p1) if first else None, ctypes.byref(p2) if second else None))
+    return (p1.value if first else None), (p2.value if second else None)
+
+
+def dsa_partition_sms(part) -> int:
+    return load().dsa_partition_sms(part)
+
+
+def dsa_partition_stream(part) -> int:
+    """A new stream of the partition (a raw cudaStream_t handle)."""
+    s = _VP()
+    _ok("dsa_partition_stream", load().dsa_partition_stream(part, ctypes.byref(s)))
+    return s.value
+
+
+def dsa_stream_wait_stream(waiter, signaller):
+    return _ok("dsa_stream_wait_stream", load().dsa_stream_wait_stream(_s(waiter), _s(signaller)))
+
+
+def dsa_partition_destroy(part):
+    return _ok("dsa_partition_destroy", load().dsa_partition_destroy(part))
 
 
 def dsa_score_topk_noalloc(units, U, R, K, q, w, topk_idx, max_len, dev_err, stream=None):

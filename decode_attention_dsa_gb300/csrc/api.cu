@@ -451,14 +451,18 @@ extern "C" int hc_init(const dsa_unit* units, int32_t U, int32_t warm, const int
     k_init_slots<<<dim3((unsigned)gs, U), INIT_THREADS, 0, st>>>(units, warm, l0);
     if (dsa_launch_status() != DSA_OK) return DSA_ERR_CUDA;
   }
-  // touch every host page of the mirrors (page size of this host)
+  return dsa_touch_mirror(units, U, max_lmax, stream);
+}
+
+extern "C" int dsa_touch_mirror(const dsa_unit* units, int32_t U, int64_t max_lmax, void* stream) {
+  if (!units || U < 1 || U > 65535 || max_lmax < 0) return DSA_ERR_ARG;
+  // one read per host page of the mirrors (page size of this host)
   const long pg = sysconf(_SC_PAGESIZE);
   const int64_t stride = pg >= 16 ? (int64_t)pg / 16 * 16 : 4096;
   const int64_t pages = (max_lmax * DSA_ROW_BYTES + stride - 1) / stride;
   const int64_t gt = std::min<int64_t>(std::max<int64_t>((pages + INIT_THREADS - 1) / INIT_THREADS, 1), 1024);
-  k_touch_mirror<<<dim3((unsigned)gt, U), INIT_THREADS, 0, st>>>(units, stride);
-  if (dsa_launch_status() != DSA_OK) return DSA_ERR_CUDA;
-  return DSA_OK;
+  k_touch_mirror<<<dim3((unsigned)gt, U), INIT_THREADS, 0, static_cast<cudaStream_t>(stream)>>>(units, stride);
+  return dsa_launch_status();
 }
 
 namespace {

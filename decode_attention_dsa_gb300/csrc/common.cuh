@@ -34,6 +34,10 @@ struct DsaPerDevice {
   int num_sms[DSA_MAX_DEVICES] = {};
 };
 
+// SMs that kernels launched on `st` may use: those of the SM partition
+// (green context) the stream belongs to, else `device_sms` (partition.cu).
+int dsa_stream_sms(cudaStream_t st, int device_sms);
+
 // Every kernel of the library prefers the largest shared-memory carveout. An
 // SM whose L1/shared split was set for a kernel with little shared memory
 // takes a CTA that needs more only after it has drained, so a small kernel of

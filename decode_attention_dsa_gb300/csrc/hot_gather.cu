@@ -52,6 +52,9 @@ constexpr int COPY_WARPS = COPY_THREADS / 32;
 // 0.90 vs 1.02 ms per step on 32 units x Top-2048 with 1 vs 4 blocks per SM.
 constexpr int COPY_BLOCKS_PER_SM = 4;
 constexpr int64_t COPY_BW_ENTRIES = 65536;
+// On an SM partition of its own (no kernel beside it to slow), the copy keeps
+// as many reads in flight as its blocks allow: 8 blocks of 256 threads per SM.
+constexpr int COPY_MAX_BLOCKS_PER_SM = 8;
 // Between COPY_MID_ENTRIES and COPY_BW_ENTRIES the kernel decides itself: if
 // the call's fills (rows read over the host link) reach COPY_BW_FILLS, only
 // one block per SM copies (the rest leave at once); a call with that many
@@ -493,11 +496,17 @@ extern "C" int hot_gather_copy(const dsa_unit* units, int32_t U, int32_t R, int3
   });
   if (ok != DSA_OK) return ok;
   const int64_t entries = (int64_t)U * R * K;
-  const int64_t per_sm = entries >= COPY_BW_ENTRIES ? 1 : COPY_BLOCKS_PER_SM;
-  const int64_t blocks = std::max<int64_t>(
-      1, std::min<int64_t>((2 * entries + COPY_WARPS - 1) / COPY_WARPS, per_sm * pd.num_sms[dev]));
-  // mid-size calls: one block per SM if the fills turn out to bind on the host link
-  const int bw_blocks = (entries >= COPY_MID_ENTRIES && entries < COPY_BW_ENTRIES) ? pd.num_sms[dev] : 0;
+  const int sms = dsa_stream_sms(static_cast<cudaStream_t>(stream), pd.num_sms[dev]);
+  const bool own_sms = sms < pd.num_sms[dev];   // the stream has an SM partition of its own
+  // Beside other kernels (a scoring that holds the SMs) host-link reads in
+  // flight beyond what the link serves only slow those kernels: the copy
+  // takes one block per SM from COPY_BW_ENTRIES selected entries on, and
+  // mid-size calls do so once their fills turn out to bind on the host link.
+  // On an SM partition of its own, it fills the partition instead.
+  const int64_t per_sm = own_sms ? COPY_MAX_BLOCKS_PER_SM : entries >= COPY_BW_ENTRIES ? 1 : COPY_BLOCKS_PER_SM;
+  const int64_t blocks =
+      std::max<int64_t>(1, std::min<int64_t>((2 * entries + COPY_WARPS - 1) / COPY_WARPS, per_sm * sms));
+  const int bw_blocks = (!own_sms && entries >= COPY_MID_ENTRIES && entries < COPY_BW_ENTRIES) ? sms : 0;
   return launch_pdl(k_copy, dim3((unsigned)blocks), dim3(COPY_THREADS), 0, static_cast<cudaStream_t>(stream),
                     units, (int)U, (int)R, (int)K, topk_idx, cls, rows, gather_ws(ws, U, R, K), dev_err,
                     bw_blocks);

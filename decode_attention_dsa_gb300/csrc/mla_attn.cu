@@ -605,8 +605,8 @@ int launch_attn(int32_t U, int32_t R, int32_t H, int32_t K, const uint16_t* q_la
   // allows for all of them, at most MAX_CTAS, at least one chunk per run
   const int nchunks = (K + NC - 1) / NC;
   const int64_t UR = (int64_t)U * R;
-  const int64_t want = std::min<int64_t>(std::min<int64_t>(std::max<int64_t>(1, pd.num_sms[dev] / UR), nchunks),
-                                         MAX_CTAS);
+  const int sms = dsa_stream_sms(st, pd.num_sms[dev]);   // the stream's SM partition, if any
+  const int64_t want = std::min<int64_t>(std::min<int64_t>(std::max<int64_t>(1, sms / UR), nchunks), MAX_CTAS);
   const int cpp = (int)((nchunks + want - 1) / want);
   const int parts = (nchunks + cpp - 1) / cpp;
   float* ws_o = ws;

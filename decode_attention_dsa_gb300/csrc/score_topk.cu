@@ -107,45 +107,66 @@ __device__ __forceinline__ uint32_t ordered_key(float s) {
 // CUDA-core fp32 (and the fp64) dot products bit for bit. ReLU, head weights
 // and the sum over heads follow on the CUDA cores, one thread per position.
 
-constexpr int SCORE_THREADS = 128;       // one position (TMEM lane) per thread
+constexpr int SCORE_EPI_THREADS = 128;   // epilogue warps 0-3: one position (TMEM lane) per thread
+constexpr int SCORE_PRODUCER_WARP = 4;   // issues the key copies
+constexpr int SCORE_MMA_WARP = 5;        // issues the MMAs, owns the tensor memory
+constexpr int SCORE_THREADS = 192;
 constexpr int SCORE_TILE = 128;          // positions per tile = MMA M
 constexpr int SCORE_STAGE = SCORE_TILE * 128;   // 16 KB of bf16 keys
 constexpr int SCORE_MAX_STAGES = 6;
-constexpr int SCORE_TMEM_COLS = 128;     // two accumulators of N <= 64 columns
+// CTAs per SM: on an SM partition (fewer SMs than the device's) the stream
+// of keys per SM is what bounds the kernel, and every CTA's stages add to
+// the bytes in flight (5 CTAs: 375 vs 392 us for 2.15 GB on 104 SMs). On the
+// whole device HBM bounds it at 4 already (333 us either way), and a fifth
+// CTA only crowds out the gather copy that shares its SMs (0.90 vs 0.83 ms
+// per step for the capacity batch in two session groups).
+constexpr int SCORE_MAX_CTAS_PER_SM = 6;
+constexpr int SCORE_FULL_DEVICE_CTAS_PER_SM = 4;
+constexpr int SCORE_TMEM_PER_SM = 512;   // tensor-memory columns of an SM
+// The shared histogram holds two 16-bit bin counts per 32-bit word. A CTA
+// flushes it to the call's histogram at least every SCORE_FLUSH_TILES tiles
+// of a unit (511 x 128 = 65,408 positions), so no count passes 65,535.
+constexpr int SCORE_HIST_WORDS = HIST1_BINS / 2;
+constexpr int SCORE_FLUSH_TILES = 511;
 
 // N of the MMA: 8 heads per query row, padded to a multiple of 16.
 __host__ __device__ inline int score_npad(int R) { return (8 * R + 15) / 16 * 16; }
+// Tensor-memory columns of one accumulator (two per CTA).
+__host__ __device__ inline int score_acc_cols(int R) { return score_npad(R) <= 32 ? 32 : 64; }
 
 struct ScoreLayout {
   int nst;            // key stages (operand A of one tile each)
-  size_t b_off;       // query operand B, two buffers of npad rows x 128 B
+  size_t b_off;       // query operand B: nb buffers of npad rows x 128 B (one
+                      // when every CTA stays within one unit, else two)
   size_t b_bytes;
-  size_t hist_off;    // R x 4096 bins
-  size_t w_off;       // head weights, two buffers of R x 8
-  size_t bar_off;     // nst copy barriers, 2 MMA barriers, TMEM address, fail flag
+  size_t hist_off;    // R x 2048 words (4096 16-bit bins)
+  size_t bar_off;     // barriers (full and empty per stage, full and empty per
+                      // accumulator), TMEM address, failure flag
   size_t bytes;
 };
 
-__host__ __device__ inline ScoreLayout score_layout(int R, int nst) {
+__host__ __device__ inline ScoreLayout score_layout(int R, int nst, int nb) {
   ScoreLayout l;
   l.nst = nst;
   l.b_off = (size_t)nst * SCORE_STAGE;
   l.b_bytes = dsa_align((size_t)score_npad(R) * 128, 1024);
-  l.hist_off = l.b_off + 2 * l.b_bytes;
-  l.w_off = l.hist_off + (size_t)R * HIST1_BINS * 4;
-  l.bar_off = dsa_align(l.w_off + 2 * (size_t)R * 8 * 4, 16);
-  l.bytes = l.bar_off + (SCORE_MAX_STAGES + 2) * 8 + 16;
+  l.hist_off = l.b_off + (size_t)nb * l.b_bytes;
+  l.bar_off = dsa_align(l.hist_off + (size_t)R * SCORE_HIST_WORDS * 4, 16);
+  l.bytes = l.bar_off + (2 * SCORE_MAX_STAGES + 4) * 8 + 16;
   return l;
 }
 
-// The stage count and CTAs per SM for R query rows: as many CTAs per SM as
-// fit (up to four; each CTA's tile loop is a latency chain, so more CTAs hide
-// more of it than more stages per CTA do), then as many stages as still fit.
-inline void score_config(int R, int* nst, int* per_sm) {
+// The stage count and CTAs per SM for R query rows and nb operand-B
+// buffers: as many CTAs per SM as shared and tensor memory allow, up to
+// max_ctas (the bytes in flight per SM are the stages of all its CTAs, and a
+// CTA's roles overlap only within one tile's chain), then as many stages as
+// still fit.
+inline void score_config(int R, int nb, int max_ctas, int* nst, int* per_sm) {
   constexpr size_t SM_BYTES = 228 * 1024;
   // dynamic bytes + alignment slack, static shared memory, the per-CTA reserve
-  auto cta_bytes = [R](int s) { return score_layout(R, s).bytes + 1024 + 256 + 1024; };
-  int c = (int)std::max<size_t>(1, std::min<size_t>(4, SM_BYTES / cta_bytes(2)));
+  auto cta_bytes = [R, nb](int s) { return score_layout(R, s, nb).bytes + 1024 + 1024 + 1024; };
+  const int tmem_cap = SCORE_TMEM_PER_SM / (2 * score_acc_cols(R));
+  int c = (int)std::max<size_t>(1, std::min<size_t>(std::min(max_ctas, tmem_cap), SM_BYTES / cta_bytes(2)));
   int s = 2;
   while (s < SCORE_MAX_STAGES && (size_t)c * cta_bytes(s + 1) <= SM_BYTES) ++s;
   *nst = s;
@@ -208,32 +229,40 @@ struct ScoreArgs {
   int32_t* dev_err;
 };
 
-// Per CTA: a contiguous range of the flattened (unit, tile) space, software
-// pipelined over its valid tiles j = 0, 1, ...:
-//   copies   lane 0 of warp 1 issues one tiled TMA copy for tile j + NST - 1
-//            (the keys land swizzled, ready for the MMA) as soon as the MMA
-//            that read that stage completes;
-//   MMA      thread 0 waits for tile j's stage, issues its four MMAs into
-//            accumulator j & 1 and commits them to MMA barrier j & 1;
-//   epilogue meanwhile every thread finishes tile j - 1 from the other
-//            accumulator (its stage is then free for the next copy).
-// The query rows sit in operand B buffer (unit change count & 1), so a unit
-// change never overwrites a B that an MMA in flight may read.
+// Per CTA: a contiguous range of the flattened (unit, tile) space. Its valid
+// tiles j = 0, 1, ... pass through three roles that meet only at mbarriers:
+//   producer (warp 4)   one tiled TMA copy per tile into stage j % NST (the
+//                       keys land swizzled, ready for the MMA), once the MMAs
+//                       that read the stage's previous tile are done;
+//   MMA (warp 5)        once tile j's keys have landed and accumulator j & 1
+//                       is free, four tcgen05.mma into it; their completion
+//                       frees the key stage and hands the accumulator on;
+//   epilogue (warps 0-3, one position per thread) reads the accumulator,
+//                       frees it, then ReLU, head weights, order-preserving
+//                       key, warp-aggregated shared histogram and the largest
+//                       key of each warp's 32 positions (for the select).
+// No role waits for another except at these barriers, so the stream of a CTA
+// is bounded by its copies in flight and the slowest role, not by the sum of
+// a tile's steps. The query rows of the tile's unit sit in operand-B buffer
+// (unit change count & 1); the MMA warp writes a new unit's rows once every
+// MMA it issued before is done.
 __global__ void __launch_bounds__(SCORE_THREADS) k_dsa_score(const __grid_constant__ CUtensorMap tmpl, ScoreArgs a) {
   extern __shared__ __align__(1024) uint8_t sm_raw[];
   // the swizzled operand layouts need a 1024-byte aligned base
   uint8_t* sm = sm_raw + ((1024u - (tc::smem_u32(sm_raw) & 1023u)) & 1023u);
   const int R = a.R, NST = a.nst;
   if (NST < 2 || NST > SCORE_MAX_STAGES) return;   // the launch never passes these (barrier slots)
-  const ScoreLayout lay = score_layout(R, NST);
+  const ScoreLayout lay = score_layout(R, NST, a.cpu > 0 ? 1 : 2);
   const int npad = score_npad(R);
+  const uint32_t acols = (uint32_t)score_acc_cols(R);
   uint32_t* hs = reinterpret_cast<uint32_t*>(sm + lay.hist_off);
-  float* sw0 = reinterpret_cast<float*>(sm + lay.w_off);              // [2][R * 8]
-  uint64_t* full = reinterpret_cast<uint64_t*>(sm + lay.bar_off);     // [NST]
-  uint64_t* mma_bar = full + SCORE_MAX_STAGES;                        // [2]
-  uint32_t* s_tmem = reinterpret_cast<uint32_t*>(mma_bar + 2);
+  uint64_t* full = reinterpret_cast<uint64_t*>(sm + lay.bar_off);   // [NST] keys landed
+  uint64_t* empty = full + SCORE_MAX_STAGES;                        // [NST] stage read by its MMAs
+  uint64_t* acc_full = empty + SCORE_MAX_STAGES;                    // [2] accumulator written
+  uint64_t* acc_empty = acc_full + 2;                               // [2] accumulator read
+  uint32_t* s_tmem = reinterpret_cast<uint32_t*>(acc_empty + 2);
   int* s_fail = reinterpret_cast<int*>(s_tmem + 1);
-  const int tid = threadIdx.x, warp = tid >> 5;
+  const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
 
   // this CTA's tiles: [f0, f1) of the flattened (unit, tile) space. With
   // a.cpu CTAs per unit every range lies inside one unit (one query operand,
@@ -259,16 +288,21 @@ __global__ void __launch_bounds__(SCORE_THREADS) k_dsa_score(const __grid_consta
   __shared__ int s_ntv[UCACHE];               // valid tiles of the unit (0 if L <= K)
   __shared__ int s_len[UCACHE];
   __shared__ const uint16_t* s_keys[UCACHE];
-  for (int i = tid; i < R * HIST1_BINS; i += SCORE_THREADS) hs[i] = 0;
+  for (int i = tid; i < R * SCORE_HIST_WORDS; i += SCORE_THREADS) hs[i] = 0;
   uint8_t* my_tmaps = a.tmaps + (size_t)blockIdx.x * SCORE_TMAP_SLOTS * 128;
   if (tid == 0) {
-    for (int s = 0; s < NST; ++s) tc::mbar_init(&full[s], 1);
-    tc::mbar_init(&mma_bar[0], 1);
-    tc::mbar_init(&mma_bar[1], 1);
+    for (int s = 0; s < NST; ++s) {
+      tc::mbar_init(&full[s], 1);
+      tc::mbar_init(&empty[s], 1);
+    }
+    for (int c = 0; c < 2; ++c) {
+      tc::mbar_init(&acc_full[c], 1);
+      tc::mbar_init(&acc_empty[c], SCORE_EPI_THREADS / 32);   // one arrival per epilogue warp
+    }
     *s_fail = 0;
     tc::fence_mbar_init();
   }
-  if (warp == 0) tc::tmem_alloc(s_tmem, SCORE_TMEM_COLS);
+  if (warp == SCORE_MMA_WARP) tc::tmem_alloc(s_tmem, 2 * acols);
   tc::fence_before_sync();
   __syncthreads();
   tc::fence_after_sync();
@@ -289,7 +323,7 @@ __global__ void __launch_bounds__(SCORE_THREADS) k_dsa_score(const __grid_consta
       if (!ok) dsa_flag(a.dev_err, DSA_DEVERR_BOUNDS);
     }
   }
-  __syncthreads();
+  __syncthreads();     // the map slots hold the template; the unit cache is filled
 
   auto tile_of = [&](int k, int& u, int& t) {
     int tt = t0 + k;
@@ -325,193 +359,205 @@ __global__ void __launch_bounds__(SCORE_THREADS) k_dsa_score(const __grid_consta
     }
     return ntiles;
   };
-  // thread 0: tile k into `stage` by one TMA copy. A unit's map is made when
-  // its first tile is issued, in the next slot in turn: every unit issued has
-  // at least one tile, so a slot is rewritten only SCORE_TMAP_SLOTS units (and
-  // as many tiles, more than the NST copies in flight) after its last use.
-  int tmap_u = -1, tmap_n = -1;
-  auto issue = [&](int k, int stage) {
-    int u, t;
-    tile_of(k, u, t);
-    if (u != tmap_u) {
-      tmap_u = u;
-      ++tmap_n;
-      tmap_set_unit(my_tmaps + (size_t)(tmap_n & (SCORE_TMAP_SLOTS - 1)) * 128, unit_keys(u), unit_len(u));
+  // Bounded wait of one lane. A lane whose wait runs out flags the call and
+  // the CTA; every other wait then gives up too, so all roles leave their
+  // loops (this does not happen in normal runs).
+  volatile int* vfail = s_fail;
+  auto wait = [&](uint64_t* bar, uint32_t parity) -> bool {
+    const long long c0 = clock64();
+    while (!tc::mbar_try_wait(bar, parity)) {
+      if (*vfail) return false;
+      if (clock64() - c0 > (1LL << 32)) {
+        atomicOr(s_fail, 1);
+        dsa_flag(a.dev_err, DSA_DEVERR_TIMEOUT);
+        return false;
+      }
     }
-    tc::mbar_arrive_expect_tx(&full[stage], (uint32_t)SCORE_STAGE);
-    tma_tile(sm + stage * SCORE_STAGE, my_tmaps + (size_t)(tmap_n & (SCORE_TMAP_SLOTS - 1)) * 128, t * SCORE_TILE,
-             &full[stage]);
+    return true;
   };
+  // lane 0 waits, the warp follows its verdict
+  auto warp_wait = [&](uint64_t* bar, uint32_t parity) -> bool {
+    bool ok = true;
+    if (lane == 0) ok = wait(bar, parity);
+    return __shfl_sync(0xffffffffu, ok ? 1 : 0, 0) != 0;
+  };
+
+  long long issued = 0;     // producer: copies issued
+  long long last_mma = -1;  // MMA warp: the last tile whose MMAs were issued
+  int hist_u = -1;          // epilogue: unit whose counts the shared histogram holds
   auto flush_hist = [&](int u) {
     uint32_t* gh = a.hist + (size_t)u * R * HIST1_BINS;
-    for (int i = tid; i < R * HIST1_BINS; i += SCORE_THREADS) {
+    for (int i = tid; i < R * SCORE_HIST_WORDS; i += SCORE_EPI_THREADS) {
       const uint32_t c = hs[i];
       if (c) {
-        atomicAdd(&gh[i], c);
+        const int r = i / SCORE_HIST_WORDS;
+        uint32_t* g = gh + (size_t)r * HIST1_BINS + 2 * (i - r * SCORE_HIST_WORDS);
+        if (c & 0xFFFFu) atomicAdd(g, c & 0xFFFFu);
+        if (c >> 16) atomicAdd(g + 1, c >> 16);
         hs[i] = 0;
       }
     }
   };
 
-  // prologue: the first NST valid tiles. The copies are issued (and
-  // tracked) by lane 0 of warp 1, so that warp 0, whose lane 0 issues the
-  // MMAs, carries no more than its share of the per-tile chain.
-  constexpr int COPY_TID = 32;
-  int k_iss = -1;      // last tile whose copy was issued
-  long long issued = 0;
-  __syncthreads();     // the map slots hold the template
-  if (tid == COPY_TID) {
-    for (int s = 0; s < NST; ++s) {
-      const int kn = next_valid(k_iss + 1);
-      k_iss = kn;
-      if (kn >= ntiles) break;
-      issue(kn, s);
-      ++issued;
+  if (warp == SCORE_PRODUCER_WARP) {
+    // ---- producer. A unit's tensor map is made when its first tile is
+    // issued, in the next slot in turn: every unit issued has at least one
+    // tile, so a slot is rewritten only SCORE_TMAP_SLOTS units (and as many
+    // tiles, more than the NST copies in flight) after its last use.
+    int tmap_u = -1, tmap_n = -1;
+    long long j = 0;
+    for (int k = next_valid(0); k < ntiles; k = next_valid(k + 1), ++j) {
+      const int s = (int)(j % NST);
+      if (j >= NST && !warp_wait(&empty[s], (uint32_t)((j / NST - 1) & 1))) break;
+      if (lane == 0) {
+        int u, t;
+        tile_of(k, u, t);
+        if (u != tmap_u) {
+          tmap_u = u;
+          ++tmap_n;
+          tmap_set_unit(my_tmaps + (size_t)(tmap_n & (SCORE_TMAP_SLOTS - 1)) * 128, unit_keys(u), unit_len(u));
+        }
+        tc::mbar_arrive_expect_tx(&full[s], (uint32_t)SCORE_STAGE);
+        tma_tile(sm + s * SCORE_STAGE, my_tmaps + (size_t)(tmap_n & (SCORE_TMAP_SLOTS - 1)) * 128,
+                 t * SCORE_TILE, &full[s]);
+      }
+      __syncwarp();
+      issued = j + 1;
     }
-  }
-
-  int k = next_valid(0);          // tile of this iteration (its MMA)
-  long long j = 0;                // its index in the valid sequence
-  int stage = 0;                  // its stage
-  int bsel = 1, mma_u = -1;       // operand-B buffer of the unit being multiplied
-  // the tile whose epilogue runs in this iteration (the previous one)
-  int pu = -1, pt = 0, pn = 0, pstage = 0, pbsel = 0;
-  int hist_u = -1;                // unit whose counts the shared histogram holds
-  bool failed = false;
-  long long last_mma = -1;        // (thread 0) the last tile whose MMAs were issued
-  while (true) {
-    const bool have = k < ntiles;
-    int u = 0, t = 0, n = 0;
-    if (have) {
+  } else if (warp == SCORE_MMA_WARP) {
+    // ---- MMA issue
+    int mma_u = -1, bsel = 1;
+    long long j = 0;
+    for (int k = next_valid(0); k < ntiles; k = next_valid(k + 1), ++j) {
+      int u, t;
       tile_of(k, u, t);
-      n = min(SCORE_TILE, unit_len(u) - t * SCORE_TILE);
       if (u != mma_u) {
-        // new unit: its query rows into the other B buffer (the MMAs in
-        // flight read this one at most), its head weights likewise
+        // new unit: its query rows into the other B buffer, once every MMA
+        // issued so far (the last reader of that buffer among them) is done
+        if (j > 0 && !warp_wait(&acc_full[(j - 1) & 1], (uint32_t)(((j - 1) >> 1) & 1))) break;
         mma_u = u;
         bsel ^= 1;
         uint8_t* sB = sm + lay.b_off + bsel * lay.b_bytes;
         const uint16_t* qu = a.q + (size_t)u * R * 512;
-        for (int i = tid; i < npad * 8; i += SCORE_THREADS) {
+        for (int i = lane; i < npad * 8; i += 32) {
           const int row = i >> 3, c = i & 7;
           uint4 v = make_uint4(0, 0, 0, 0);
           if (row < 8 * R) v = *reinterpret_cast<const uint4*>(qu + (size_t)row * 64 + 8 * c);
           *reinterpret_cast<uint4*>(sB + (row >> 3) * 1024 + (row & 7) * 128 + ((c ^ (row & 7)) << 4)) = v;
         }
-        for (int i = tid; i < R * 8; i += SCORE_THREADS) sw0[bsel * R * 8 + i] = a.w[(size_t)u * R * 8 + i];
         tc::fence_async_shared();
-        __syncthreads();
+        __syncwarp();
       }
-      if (tid == 0) {
-        // tile j's keys have landed: issue its MMAs into accumulator j & 1
-        if (tc::mbar_wait(&full[stage], (uint32_t)((j / NST) & 1))) {
-          last_mma = j;
+      const int s = (int)(j % NST), acc = (int)(j & 1);
+      bool ok = true;
+      if (lane == 0) {
+        ok = wait(&full[s], (uint32_t)((j / NST) & 1));
+        if (ok && j >= 2) ok = wait(&acc_empty[acc], (uint32_t)(((j >> 1) - 1) & 1));
+        if (ok) {
           tc::fence_after_sync();
-          const uint32_t aa = tc::smem_u32(sm + stage * SCORE_STAGE);
+          const uint32_t aa = tc::smem_u32(sm + s * SCORE_STAGE);
           const uint32_t bb = tc::smem_u32(sm + lay.b_off + bsel * lay.b_bytes);
-          const uint32_t d = tmem + (uint32_t)(j & 1) * 64;
+          const uint32_t d = tmem + (uint32_t)acc * acols;
 #pragma unroll
           for (int kk = 0; kk < 4; ++kk)
             tc::mma_f16(d, tc::sdesc_sw128(aa + kk * 32, 16, 1024), tc::sdesc_sw128(bb + kk * 32, 16, 1024),
                         a.idesc, kk > 0);
-          tc::mma_commit(&mma_bar[j & 1]);
-        } else {
-          atomicOr(s_fail, 1);
+          tc::mma_commit(&empty[s]);
+          tc::mma_commit(&acc_full[acc]);
+          last_mma = j;
         }
       }
+      if (!__shfl_sync(0xffffffffu, ok ? 1 : 0, 0)) break;
     }
-    if (pu >= 0) {
-      // ---- previous tile: its MMAs are done, its stage takes the next copy,
-      //      then its epilogue
-      if (pu != hist_u) {
-        // the shared histogram moves to the new unit (every thread flushes and
-        // clears its own bins; the barrier keeps the epilogue's counts out)
-        if (hist_u >= 0) flush_hist(hist_u);
-        hist_u = pu;
-        __syncthreads();
+  } else {
+    // ---- epilogue. A warp whose wait gave up keeps walking the tiles
+    // without touching them, so that every epilogue thread meets the same
+    // histogram barriers.
+    bool dead = false;
+    int since = 0;            // tiles counted into the shared histogram since its last flush
+    long long j = 0;
+    for (int k = next_valid(0); k < ntiles; k = next_valid(k + 1), ++j) {
+      int u, t;
+      tile_of(k, u, t);
+      if (u != hist_u || since == SCORE_FLUSH_TILES) {
+        // the histogram moves to a new unit, or its 16-bit counts could
+        // overflow with one more tile: all counts so far are in (barrier),
+        // each thread flushes and clears its own words, and the second
+        // barrier keeps new counts out until then
+        if (hist_u >= 0) {
+          asm volatile("bar.sync 1, %0;" ::"r"(SCORE_EPI_THREADS) : "memory");
+          flush_hist(hist_u);
+          asm volatile("bar.sync 1, %0;" ::"r"(SCORE_EPI_THREADS) : "memory");
+        }
+        hist_u = u;
+        since = 0;
       }
-      const long long jp = j - 1;
-      bool ok = tc::mbar_wait(&mma_bar[jp & 1], (uint32_t)((jp >> 1) & 1));
-      ok = __all_sync(0xffffffffu, ok);
+      ++since;
+      const int acc = (int)(j & 1);
+      if (!dead) dead = !warp_wait(&acc_full[acc], (uint32_t)((j >> 1) & 1));
+      if (dead) continue;
       tc::fence_after_sync();
-      if (ok) {
-        if (tid == COPY_TID) {
-          const int kn = k_iss < ntiles ? next_valid(k_iss + 1) : ntiles;
-          k_iss = kn;
-          if (kn < ntiles) {
-            issue(kn, pstage);
-            ++issued;
-          }
+      const int n = min(SCORE_TILE, unit_len(u) - t * SCORE_TILE);
+      const float* wu = a.w + (size_t)u * R * 8;
+      const int p = tid;
+      for (int r = 0; r < R; ++r) {
+        uint32_t d[8];
+        tmem_ld8_nowait(tmem + ((uint32_t)(32 * warp) << 16) + (uint32_t)acc * acols + 8 * r, d);
+        tmem_ld_wait();
+        if (r == R - 1) {
+          // the accumulator is read: the MMA two tiles on may overwrite it
+          tc::fence_before_sync();
+          __syncwarp();
+          if (lane == 0) tc::mbar_arrive(&acc_empty[acc]);
         }
-        __syncwarp();   // warp 1 converges before the warp-wide TMEM loads
-        const float* sw = sw0 + pbsel * R * 8;
-        const int p = tid;
-        for (int r = 0; r < R; ++r) {
-          uint32_t d[8];
-          tmem_ld8_nowait(tmem + ((uint32_t)(32 * warp) << 16) + (uint32_t)(jp & 1) * 64 + 8 * r, d);
-          tmem_ld_wait();
-          uint32_t key = 0u;   // positions past the history count as the smallest key
-          if (p < pn) {
-            float sc = 0.f;
+        uint32_t key = 0u;   // positions past the history count as the smallest key
+        if (p < n) {
+          float sc = 0.f;
 #pragma unroll
-            for (int h = 0; h < 8; ++h) sc = fmaf(sw[r * 8 + h], fmaxf(__uint_as_float(d[h]), 0.f), sc);
-            key = ordered_key(sc);
-            a.okeys[((size_t)pu * R + r) * a.stride + (size_t)pt * SCORE_TILE + p] = key;
-            const uint32_t bin = key >> 20;
-            const unsigned amask = __activemask();
-            const unsigned peers = __match_any_sync(amask, bin);
-            if ((int)(threadIdx.x & 31) == __ffs(peers) - 1)
-              atomicAdd(&hs[r * HIST1_BINS + bin], (uint32_t)__popc(peers));
-          }
-          // the warp's 32 positions form one group: its largest key lets the
-          // selection skip groups that hold no key of the threshold bin. A
-          // row holds stride / 32 groups; the last tile's groups past it
-          // (positions >= max_len only) have no slot and are not written.
-          const uint32_t gk = __reduce_max_sync(0xffffffffu, key);
-          const int64_t gi = (int64_t)pt * (SCORE_TILE / SEL_GROUP) + warp;
-          if ((tid & 31) == 0 && gi < a.stride / SEL_GROUP)
-            a.gmax[((size_t)pu * R + r) * (a.stride / SEL_GROUP) + gi] = gk;
+          for (int h = 0; h < 8; ++h) sc = fmaf(__ldg(wu + r * 8 + h), fmaxf(__uint_as_float(d[h]), 0.f), sc);
+          key = ordered_key(sc);
+          a.okeys[((size_t)u * R + r) * a.stride + (size_t)t * SCORE_TILE + p] = key;
+          const uint32_t bin = key >> 20;
+          const unsigned amask = __activemask();
+          const unsigned peers = __match_any_sync(amask, bin);
+          if (lane == __ffs(peers) - 1)
+            atomicAdd(&hs[r * SCORE_HIST_WORDS + (bin >> 1)], (uint32_t)__popc(peers) << (16 * (bin & 1)));
         }
-      } else {
-        atomicOr(s_fail, 1);
+        // the warp's 32 positions form one group: its largest key lets the
+        // selection skip groups that hold no key of the threshold bin. A
+        // row holds stride / 32 groups; the last tile's groups past it
+        // (positions >= max_len only) have no slot and are not written.
+        const uint32_t gk = __reduce_max_sync(0xffffffffu, key);
+        const int64_t gi = (int64_t)t * (SCORE_TILE / SEL_GROUP) + warp;
+        if (lane == 0 && gi < a.stride / SEL_GROUP) a.gmax[((size_t)u * R + r) * (a.stride / SEL_GROUP) + gi] = gk;
       }
     }
-    tc::fence_before_sync();
-    __syncthreads();   // accumulator (j - 1) & 1 is read before the next MMA writes it
-    if (*s_fail) {
-      failed = true;
-      break;
+    if (hist_u >= 0) {
+      asm volatile("bar.sync 1, %0;" ::"r"(SCORE_EPI_THREADS) : "memory");
+      flush_hist(hist_u);
     }
-    if (!have) break;
-    pu = u;
-    pt = t;
-    pn = n;
-    pstage = stage;
-    pbsel = bsel;
-    ++j;
-    stage = stage + 1 == NST ? 0 : stage + 1;
-    k = next_valid(k + 1);
   }
-  if (failed) {
-    // A wait gave up (this does not happen in normal runs): the call's
-    // selection is void. Every thread left the loop together; the MMAs and
-    // copies that may still be in flight get one more bounded wait each so
-    // that nothing lands after the CTA is gone.
-    if (tid == 0) {
-      dsa_flag(a.dev_err, DSA_DEVERR_TIMEOUT);
-      for (long long i = last_mma - 1; i <= last_mma; ++i)
-        if (i >= 0) tc::mbar_wait(&mma_bar[i & 1], (uint32_t)((i >> 1) & 1));
-    }
-    if (tid == COPY_TID)
-      for (long long i = j; i < issued; ++i) tc::mbar_wait(&full[i % NST], (uint32_t)((i / NST) & 1));
-  } else if (hist_u >= 0) {
-    __syncthreads();
-    flush_hist(hist_u);
-  }
+
   tc::fence_before_sync();
-  __syncthreads();
+  __syncthreads();     // every role has left its loop
   tc::fence_after_sync();
-  if (warp == 0) tc::tmem_dealloc(tmem, SCORE_TMEM_COLS);
+  if (*vfail) {
+    // A wait gave up: the call's selection is void. Nothing may land after
+    // the CTA is gone: the MMAs and copies still in flight get one more
+    // bounded wait each.
+    if (warp == SCORE_MMA_WARP && lane == 0 && last_mma >= 0)
+      tc::mbar_wait(&acc_full[last_mma & 1], (uint32_t)((last_mma >> 1) & 1));
+    if (warp == SCORE_PRODUCER_WARP && lane == 0) {
+      for (int s = 0; s < NST && s < issued; ++s) {
+        const long long last = s + (issued - 1 - s) / NST * NST;   // the stage's last copy
+        tc::mbar_wait(&full[s], (uint32_t)((last / NST) & 1));
+      }
+    }
+  }
+  if (warp == SCORE_MMA_WARP) {
+    __syncwarp();
+    tc::tmem_dealloc(tmem, 2 * acols);
+  }
 }
 
 // Among `nb` histogram bins (held by threads 0..nb-1, thread t <-> bin
@@ -1047,27 +1093,32 @@ extern "C" size_t dsa_score_topk_workspace(int32_t U, int32_t R, int64_t max_len
          SCORE_TMAP_BYTES;
 }
 
-extern "C" int dsa_score_topk(const dsa_unit* units, int32_t U, int32_t R, int32_t K,
-                              const uint16_t* q, const float* w, int32_t* topk_idx,
-                              int64_t max_len, void* ws, size_t ws_bytes, int32_t* dev_err,
-                              void* stream) {
-  if (!units || !q || !w || !topk_idx) return DSA_ERR_ARG;
+namespace {
+
+// Argument checks shared by the scoring and selection entry points.
+int check_score_args(const dsa_unit* units, int32_t U, int32_t R, int32_t K, int64_t max_len, const void* ws,
+                     size_t ws_bytes) {
+  if (!units) return DSA_ERR_ARG;
   if (U < 1 || U > 65535 || R < 1 || R > DSA_MAX_ROWS || max_len < 0) return DSA_ERR_ARG;
   if ((int64_t)U * R > 65535) return DSA_ERR_ARG;
   if (K < 1 || K > DSA_MAX_K) return DSA_ERR_SHAPE;
   if (!ws || ws_bytes < dsa_score_topk_workspace(U, R, max_len)) return DSA_ERR_WS;
   if (reinterpret_cast<uintptr_t>(ws) & 15u) return DSA_ERR_ARG;   // its keys are read by bulk copies
-  cudaStream_t st = static_cast<cudaStream_t>(stream);
-  TopkWs tw = topk_ws(ws, U, R, max_len);
-  if (reinterpret_cast<uintptr_t>(q) & 15u) return DSA_ERR_ARG;   // query rows are read as 16-byte vectors
-  int dev = 0;
-  const int ok = dsa_device_setup(g_setup, &dev, [](int d) {
+  return DSA_OK;
+}
+
+int score_setup(int* dev) {
+  return dsa_device_setup(g_setup, dev, [](int d) {
     if (encode_template(d) != DSA_OK) return DSA_ERR_CUDA;
     size_t mx = 0;
     for (int r = 1; r <= DSA_MAX_ROWS; ++r) {
-      int nst = 2, per_sm = 1;
-      score_config(r, &nst, &per_sm);
-      mx = std::max(mx, score_layout(r, nst).bytes + 1024);
+      for (int nb = 1; nb <= 2; ++nb) {
+        for (int cap : {SCORE_FULL_DEVICE_CTAS_PER_SM, SCORE_MAX_CTAS_PER_SM}) {
+          int nst = 2, per_sm = 1;
+          score_config(r, nb, cap, &nst, &per_sm);
+          mx = std::max(mx, score_layout(r, nst, nb).bytes + 1024);
+        }
+      }
     }
     DSA_CUDA_TRY(dsa_prefer_shared(k_dsa_score));
     DSA_CUDA_TRY(dsa_prefer_shared(k_topk_select));
@@ -1076,46 +1127,91 @@ extern "C" int dsa_score_topk(const dsa_unit* units, int32_t U, int32_t R, int32
                                       (int)select_smem()));
     return DSA_OK;
   });
+}
+
+}  // namespace
+
+extern "C" int dsa_score(const dsa_unit* units, int32_t U, int32_t R, int32_t K, const uint16_t* q,
+                         const float* w, int64_t max_len, void* ws, size_t ws_bytes, int32_t* dev_err,
+                         void* stream) {
+  if (!q || !w) return DSA_ERR_ARG;
+  const int chk = check_score_args(units, U, R, K, max_len, ws, ws_bytes);
+  if (chk != DSA_OK) return chk;
+  if (reinterpret_cast<uintptr_t>(q) & 15u) return DSA_ERR_ARG;   // query rows are read as 16-byte vectors
+  cudaStream_t st = static_cast<cudaStream_t>(stream);
+  TopkWs tw = topk_ws(ws, U, R, max_len);
+  int dev = 0;
+  const int ok = score_setup(&dev);
   if (ok != DSA_OK) return ok;
-  const int num_sms = g_setup.num_sms[dev];
   const int64_t tpu = (max_len + SCORE_TILE - 1) / SCORE_TILE;
-  if (tpu > 0) {
-    if (tpu * U > 0x7fffffffLL) return DSA_ERR_ARG;
-    int nst = 2, per_sm = 1;
-    score_config(R, &nst, &per_sm);
-    ScoreArgs a;
-    a.units = units;
-    a.q = q;
-    a.w = w;
-    a.hist = tw.hist;
-    a.okeys = tw.keys;
-    a.gmax = tw.gmax;
-    a.stride = tw.stride;
-    a.max_len = max_len;
-    a.tpu = (int)tpu;
-    a.U = U;
-    a.R = R;
-    a.K = K;
-    a.nst = nst;
-    a.idesc = tc::idesc_bf16_f32(SCORE_TILE, score_npad(R));
-    a.tmaps = tw.tmaps;
-    a.dev_err = dev_err;
-    const int64_t slots = std::min<int64_t>((int64_t)per_sm * num_sms, SCORE_MAX_GRID);
-    int64_t grid;
-    if (U <= slots) {
-      // whole CTAs per unit
-      a.cpu = (int)std::min<int64_t>(slots / U, tpu);
-      grid = (int64_t)a.cpu * U;
-    } else {
-      a.cpu = 0;
-      grid = std::min<int64_t>(tpu * U, slots);
-    }
-    if (launch_pdl(k_dsa_score, dim3((unsigned)grid), dim3(SCORE_THREADS), score_layout(R, nst).bytes + 1024, st,
-                   g_tmpl[dev], a) != DSA_OK)
-      return DSA_ERR_CUDA;
+  if (tpu == 0) return DSA_OK;
+  if (tpu * U > 0x7fffffffLL) return DSA_ERR_ARG;
+  // The persistent grid fills the SMs the stream may use: all of the
+  // device's, or those of the SM partition the stream belongs to.
+  const int num_sms = dsa_stream_sms(st, g_setup.num_sms[dev]);
+  // one operand-B buffer when every CTA stays within one unit (the grid
+  // holds at least one CTA per unit), else two
+  const int cap = num_sms < g_setup.num_sms[dev] ? SCORE_MAX_CTAS_PER_SM : SCORE_FULL_DEVICE_CTAS_PER_SM;
+  int nst = 2, per_sm = 1;
+  score_config(R, 1, cap, &nst, &per_sm);
+  int nb = 1;
+  if (U > std::min<int64_t>((int64_t)per_sm * num_sms, SCORE_MAX_GRID)) {
+    nb = 2;
+    score_config(R, nb, cap, &nst, &per_sm);
   }
-  return launch_pdl(k_topk_select, dim3(SEL_CLUSTER, U * R), dim3(SEL_THREADS), select_smem(), st, units, R,
-                    K, tw.hist, tw.keys, tw.gmax, tw.stride, topk_idx, max_len, dev_err);
+  ScoreArgs a;
+  a.units = units;
+  a.q = q;
+  a.w = w;
+  a.hist = tw.hist;
+  a.okeys = tw.keys;
+  a.gmax = tw.gmax;
+  a.stride = tw.stride;
+  a.max_len = max_len;
+  a.tpu = (int)tpu;
+  a.U = U;
+  a.R = R;
+  a.K = K;
+  a.nst = nst;
+  a.idesc = tc::idesc_bf16_f32(SCORE_TILE, score_npad(R));
+  a.tmaps = tw.tmaps;
+  a.dev_err = dev_err;
+  const int64_t slots = std::min<int64_t>((int64_t)per_sm * num_sms, SCORE_MAX_GRID);
+  int64_t grid;
+  if (nb == 1) {
+    // whole CTAs per unit
+    a.cpu = (int)std::min<int64_t>(slots / U, tpu);
+    grid = (int64_t)a.cpu * U;
+  } else {
+    a.cpu = 0;
+    grid = std::min<int64_t>(tpu * U, slots);
+  }
+  return launch_pdl(k_dsa_score, dim3((unsigned)grid), dim3(SCORE_THREADS), score_layout(R, nst, nb).bytes + 1024,
+                    st, g_tmpl[dev], a);
+}
+
+extern "C" int dsa_topk_select(const dsa_unit* units, int32_t U, int32_t R, int32_t K, int32_t* topk_idx,
+                               int64_t max_len, void* ws, size_t ws_bytes, int32_t* dev_err, void* stream) {
+  if (!topk_idx) return DSA_ERR_ARG;
+  const int chk = check_score_args(units, U, R, K, max_len, ws, ws_bytes);
+  if (chk != DSA_OK) return chk;
+  TopkWs tw = topk_ws(ws, U, R, max_len);
+  int dev = 0;
+  const int ok = score_setup(&dev);
+  if (ok != DSA_OK) return ok;
+  return launch_pdl(k_topk_select, dim3(SEL_CLUSTER, U * R), dim3(SEL_THREADS), select_smem(),
+                    static_cast<cudaStream_t>(stream), units, R, K, tw.hist, tw.keys, tw.gmax, tw.stride, topk_idx,
+                    max_len, dev_err);
+}
+
+extern "C" int dsa_score_topk(const dsa_unit* units, int32_t U, int32_t R, int32_t K,
+                              const uint16_t* q, const float* w, int32_t* topk_idx,
+                              int64_t max_len, void* ws, size_t ws_bytes, int32_t* dev_err,
+                              void* stream) {
+  if (!topk_idx) return DSA_ERR_ARG;
+  const int st = dsa_score(units, U, R, K, q, w, max_len, ws, ws_bytes, dev_err, stream);
+  if (st != DSA_OK) return st;
+  return dsa_topk_select(units, U, R, K, topk_idx, max_len, ws, ws_bytes, dev_err, stream);
 }
 
 // ---------------------------------------------------------------------------

@@ -60,6 +60,26 @@ class DecodePath:
         abi.dsa_score_topk(u.units, u.U, self.R, self.K, q_idx, w, self.topk, self.max_len,
                            self.ws_topk, self.ws_topk_bytes, u.dev_err, stream)
 
+    def score(self, q_idx, w, stream=None):
+        """The scoring half of score_topk (dsa_score); select() completes it."""
+        u = self.u
+        units, U = (self.src_units, self.Us) if self.sources else (u.units, u.U)
+        abi.dsa_score(units, U, self.R, self.K, q_idx, w, self.max_len, self.ws_topk, self.ws_topk_bytes,
+                      u.dev_err, stream)
+
+    def select(self, stream=None):
+        """The selection half of score_topk (dsa_topk_select), ordered after
+        score() by the caller."""
+        u = self.u
+        if self.sources:
+            abi.dsa_topk_select(self.src_units, self.Us, self.R, self.K, self.src_topk, self.max_len,
+                                self.ws_topk, self.ws_topk_bytes, u.dev_err, stream)
+            abi.dsa_reuse_selection(self.topk, self.src_topk, u.U, self.Us, self.R, self.K, self.src_of,
+                                    u.dev_err, stream)
+            return
+        abi.dsa_topk_select(u.units, u.U, self.R, self.K, self.topk, self.max_len, self.ws_topk,
+                            self.ws_topk_bytes, u.dev_err, stream)
+
     def gather(self, rnd: int, stream=None):
         u = self.u
         abi.hot_gather(u.units, u.U, self.R, self.K, rnd, self.topk, self.cls, self.rows,

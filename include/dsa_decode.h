@@ -190,6 +190,18 @@ int dsa_host_free(void* host_ptr);
 int hc_init(const dsa_unit* units, int32_t U, int32_t warm, const int64_t* l0,
             int32_t max_slots, int64_t max_lmax, int32_t* dev_err, void* stream);
 
+/*
+ * The last part of hc_init alone: one read of every host page of each unit's
+ * mirror ([0, lmax) rows), enqueued on `stream`. The address translations it
+ * sets up serve kernels of the same context: measured on a GB300, gathers on
+ * an SM partition's streams (dsa_partition_split, a green context) paid for
+ * them again over their first 25 to 80 decode steps (up to 5 ms per step)
+ * although hc_init had run on an ordinary stream. Call it once on a stream of
+ * each partition whose kernels read the mirrors. Units whose arrays are not
+ * 16-byte aligned are skipped. max_lmax: host bound, max over units of lmax.
+ */
+int dsa_touch_mirror(const dsa_unit* units, int32_t U, int64_t max_lmax, void* stream);
+
 /* --------------------------------------------- A1 + A2: DSA score and Top-K */
 
 /*
@@ -221,6 +233,74 @@ int dsa_score_topk(const dsa_unit* units, int32_t U, int32_t R, int32_t K,
                    const uint16_t* q, const float* w, int32_t* topk_idx,
                    int64_t max_len, void* ws, size_t ws_bytes,
                    int32_t* dev_err, void* stream);
+
+/*
+ * The two halves of dsa_score_topk, for callers that run them on different
+ * streams (dsa_score_topk is dsa_score then dsa_topk_select on one stream).
+ * Same arguments and workspace; the workspace of one call pair must not be
+ * used by another call until dsa_topk_select has run.
+ *   dsa_score        scores the units into the workspace (ordered score keys,
+ *                    histograms, group maxima): one launch of the persistent
+ *                    score kernel, whose grid fills the SMs that `stream` may
+ *                    use (the SMs of the partition it belongs to, see
+ *                    dsa_partition_split, else the whole device).
+ *   dsa_topk_select  selects the Top-K from what dsa_score left in the
+ *                    workspace and clears it for the next call; it must be
+ *                    ordered after dsa_score (same stream, or an event).
+ */
+int dsa_score(const dsa_unit* units, int32_t U, int32_t R, int32_t K,
+              const uint16_t* q, const float* w, int64_t max_len,
+              void* ws, size_t ws_bytes, int32_t* dev_err, void* stream);
+int dsa_topk_select(const dsa_unit* units, int32_t U, int32_t R, int32_t K,
+                    int32_t* topk_idx, int64_t max_len, void* ws,
+                    size_t ws_bytes, int32_t* dev_err, void* stream);
+
+/* ------------------------------------------------- SM partitions (schedule) */
+
+/*
+ * Partitions of the current device's SMs (CUDA green contexts): kernels
+ * launched on a partition's streams run only on its SMs. Their use: the
+ * indexer's score kernel streams every key from HBM on a persistent grid that
+ * holds all the SMs it may use until it ends, so the rest of another batch's
+ * step (selection, slot assignment, gather, attention) can run beside it only
+ * on SMs it was not given. Kernels of this library size their grids to the
+ * partition of the stream they are launched on.
+ *
+ * dsa_partition_split splits the device in two. The device's SMs come as
+ * co-scheduling groups (SMs of one GPU processing cluster, 8 on a GB300)
+ * plus some SMs that form no whole group. `first` takes those leftovers,
+ * then whole groups until it holds at least min_sms; `second` takes the
+ * groups left, whole, so that thread-block clusters (the Top-K select
+ * launches 8-CTA clusters) fit there.
+ *   min_sms  1 <= min_sms < the device's SM count.
+ *   first    out (may be NULL: not created): the first partition.
+ *   second   out (may be NULL: not created): the second partition.
+ * Returns DSA_ERR_ARG for a count that leaves nothing for a requested second
+ * partition, DSA_ERR_CUDA where the driver has no green contexts or refuses.
+ * The caller owns the partitions (dsa_partition_destroy).
+ *
+ * dsa_partition_sms     the SMs of a partition.
+ * dsa_partition_stream  a new non-blocking stream of the partition (a
+ *                       cudaStream_t, owned by the partition, valid until
+ *                       dsa_partition_destroy).
+ * dsa_stream_wait_stream  work queued later on `waiter` waits for the work
+ *                       queued so far on `signaller`. Either may be a
+ *                       partition's stream or an ordinary stream of the
+ *                       device: an event recorded on a partition's stream
+ *                       must come from its own context, so ordinary events
+ *                       (cudaEventRecord) cannot order partition streams;
+ *                       this call can.
+ * dsa_partition_destroy waits for the work queued on the partition's streams,
+ *                       then releases them and the green context.
+ * A partition is used from one host thread at a time; its streams are not
+ * captured into CUDA graphs.
+ */
+typedef struct dsa_partition dsa_partition;
+int dsa_partition_split(int32_t min_sms, dsa_partition** first, dsa_partition** second);
+int dsa_partition_sms(const dsa_partition* part);
+int dsa_partition_stream(dsa_partition* part, void** stream);
+int dsa_stream_wait_stream(void* waiter, void* signaller);
+int dsa_partition_destroy(dsa_partition* part);
 
 /*
  * dsa_score_topk without a caller workspace, for callers that cannot

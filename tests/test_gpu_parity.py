@@ -130,6 +130,8 @@ def test_two_session_groups_on_two_streams():
         st.wait_stream(torch.cuda.current_stream())
     for step in range(wl.steps):
         per, t = pair.inputs(step)
+        for st in streams:
+            st.wait_stream(torch.cuda.current_stream())     # the step's inputs
         for g, ((lo, hi), p, st) in enumerate(zip(ranges, paths, streams)):
             u = p.u
             with torch.cuda.stream(st):
@@ -155,6 +157,64 @@ def test_two_session_groups_on_two_streams():
                                   x.new_rows, x.new_keys, attention=True)
         check_step(pair, g, ores)
         assert pair.g.check() == 0
+
+
+def test_scoring_on_sm_partition_beside_the_other_group():
+    """The partition schedule: two session groups; the GPU split into two SM
+    partitions; every scoring (dsa_score) on the first partition's stream, the
+    groups' scorings alternating there; each group's selection, gather,
+    attention and append on its own stream of the second partition; the
+    order kept by dsa_stream_wait_stream. After every step every unit matches
+    the oracle."""
+    import torch
+    from decode_attention_dsa_gb300.step import DecodePath
+    from oracle.decode import decode_step
+    wl = W.WORKLOADS[0].with_(name="partition", sessions=2, layers=2, L0=3000, S=256, K=256, H=16, steps=6,
+                              warm="last_s")
+    pair = Pair(wl)
+    pair.check_slots = True
+    abi = pair.abi
+    first, second = abi.dsa_partition_split(64)
+    ranges = [(0, 2), (2, 4)]
+    paths = [DecodePath(pair.g.subset(lo, hi), wl.R, wl.K, wl.H, wl.A, wl.scale()) for lo, hi in ranges]
+    try:
+        assert abi.dsa_partition_sms(first) >= 64 and abi.dsa_partition_sms(second) >= 8
+        pstream = abi.dsa_partition_stream(first)
+        streams = [abi.dsa_partition_stream(second) for _ in ranges]
+        for step in range(wl.steps):
+            per, t = pair.inputs(step)
+            cur = torch.cuda.current_stream()
+            for st in streams:
+                abi.dsa_stream_wait_stream(st, cur)     # the step's inputs
+            for g, ((lo, hi), p, st) in enumerate(zip(ranges, paths, streams)):
+                u = p.u
+                abi.dsa_stream_wait_stream(pstream, st)
+                p.score(t["q_idx"][lo:hi], t["w"][lo:hi], pstream)
+                abi.dsa_stream_wait_stream(st, pstream)
+                p.select(st)
+                abi.hot_gather_assign(u.units, u.U, p.R, p.K, step, p.topk, p.cls, p.counters, p.ws_gather,
+                                      p.ws_gather_bytes, u.dev_err, st)
+                abi.hot_gather_copy(u.units, u.U, p.R, p.K, p.topk, p.cls, p.rows, p.ws_gather,
+                                    p.ws_gather_bytes, u.dev_err, st)
+                p.attend(t["q_lat"][lo:hi], t["q_rope"][lo:hi], st)
+                p.append(t["new_rows"][lo:hi], t["new_keys"][lo:hi], st)
+            for st in streams:
+                abi.dsa_stream_wait_stream(cur, st)
+            torch.cuda.synchronize()
+            cat = lambda name: np.concatenate([getattr(p, name).cpu().numpy() for p in paths])
+            g = dict(topk=cat("topk"), cls=cat("cls"), counters=cat("counters"), out=cat("out"),
+                     lse=cat("lse"), rows=cat("rows"))
+            pair.last_inputs = per
+            ores = {}
+            for i, u in enumerate(pair.uidx):
+                x = per[i]
+                ores[u] = decode_step(pair.o[u], step, wl.K, wl.scale(), x.q_idx, x.w, x.q_lat, x.q_rope,
+                                      x.new_rows, x.new_keys, attention=True)
+            check_step(pair, g, ores)
+            assert pair.g.check() == 0
+    finally:
+        abi.dsa_partition_destroy(first)
+        abi.dsa_partition_destroy(second)
 
 
 @pytest.mark.parametrize("wl", FUSED, ids=[w.name[:12] for w in FUSED])

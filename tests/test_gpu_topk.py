@@ -17,8 +17,10 @@ def _need_gpu():
         pytest.skip("no CUDA device")
 
 
-def _run(keys_list, q, w, K):
-    """keys_list: per unit bf16 bits [L_u, 64]; q: bf16 bits [U, R, 8, 64]; w: [U, R, 8]."""
+def _run(keys_list, q, w, K, streams=None):
+    """keys_list: per unit bf16 bits [L_u, 64]; q: bf16 bits [U, R, 8, 64]; w: [U, R, 8].
+    With `streams` = (score stream, select stream), dsa_score and
+    dsa_topk_select run there, ordered by dsa_stream_wait_stream."""
     import torch
     from decode_attention_dsa_gb300 import abi
     from decode_attention_dsa_gb300.units import UnitSet
@@ -36,7 +38,15 @@ def _run(keys_list, q, w, K):
     wt = torch.from_numpy(np.ascontiguousarray(w, dtype=np.float32)).cuda()
     for _ in range(2):          # twice: the workspace must come back clean
         out.fill_(-5)
-        abi.dsa_score_topk(g.units, U, R, K, qt, wt, out, lmax, ws, ws_b, g.dev_err)
+        if streams is None:
+            abi.dsa_score_topk(g.units, U, R, K, qt, wt, out, lmax, ws, ws_b, g.dev_err)
+        else:
+            cur = torch.cuda.current_stream()
+            abi.dsa_stream_wait_stream(streams[0], cur)
+            abi.dsa_score(g.units, U, R, K, qt, wt, lmax, ws, ws_b, g.dev_err, streams[0])
+            abi.dsa_stream_wait_stream(streams[1], streams[0])
+            abi.dsa_topk_select(g.units, U, R, K, out, lmax, ws, ws_b, g.dev_err, streams[1])
+            abi.dsa_stream_wait_stream(cur, streams[1])
         torch.cuda.synchronize()
         got = out.cpu().numpy()
         for u, k in enumerate(keys_list):
@@ -107,3 +117,26 @@ def test_short_history_in_few_tiles_and_empty_cluster_ranges():
     q = _bits(rng.integers(-4, 5, size=(4, 1, 8, 64)))
     w = rng.integers(1, 5, size=(4, 1, 8))
     _run(keys, q, w, 2048)
+
+
+@pytest.mark.parametrize("min_sms", [8, 96])
+def test_score_and_select_on_two_sm_partitions(min_sms):
+    """dsa_score on the first of two SM partitions (its persistent grid sized
+    to the partition's SMs, whole CTAs per unit where the grid holds one per
+    unit) and dsa_topk_select (8-CTA clusters) on the second: the same Top-K
+    as the oracle, for units of unequal, ragged lengths."""
+    import torch
+    from decode_attention_dsa_gb300 import abi
+    rng = np.random.default_rng(11)
+    keys = [_bits(rng.integers(-4, 5, size=(n, 64))) for n in (70001, 257, 33333, 128, 90000)]
+    q = _bits(rng.integers(-4, 5, size=(5, 2, 8, 64)))
+    w = rng.integers(1, 5, size=(5, 2, 8))
+    first, second = abi.dsa_partition_split(min_sms)
+    try:
+        n1, n2 = abi.dsa_partition_sms(first), abi.dsa_partition_sms(second)
+        assert n1 >= min_sms and n2 >= 8
+        assert n1 + n2 == torch.cuda.get_device_properties(0).multi_processor_count
+        _run(keys, q, w, 2048, streams=(abi.dsa_partition_stream(first), abi.dsa_partition_stream(second)))
+    finally:
+        abi.dsa_partition_destroy(first)
+        abi.dsa_partition_destroy(second)
