@@ -93,6 +93,23 @@ def test_host_side_validation(lib):
                                  None, None) == lib.DSA_ERR_SHAPE
         assert L.hot_gather_attn(fake, 1, 1, K, 64, 0, fake, fake, fake, 0.04, fake, fake, fake, None,
                                  fake, 1 << 30, None, None) == lib.DSA_ERR_SHAPE
+    # the two halves of dsa_score_topk check the same arguments
+    assert L.dsa_score(fake, 1, 1, 8, None, fake, 10, fake, 1 << 20, None, None) == lib.DSA_ERR_ARG
+    assert L.dsa_score(fake, 1, 1, 5000, fake, fake, 10, fake, 1 << 20, None, None) == lib.DSA_ERR_SHAPE
+    assert L.dsa_score(fake, 1, 1, 8, fake, fake, 10, fake, 16, None, None) == lib.DSA_ERR_WS
+    assert L.dsa_score(fake, 1, 1, 8, fake + 8, fake, 10, fake, 1 << 24, None, None) == lib.DSA_ERR_ARG
+    assert L.dsa_topk_select(fake, 1, 1, 8, None, 10, fake, 1 << 20, None, None) == lib.DSA_ERR_ARG
+    assert L.dsa_topk_select(fake, 1, 9, 8, fake, 10, fake, 1 << 20, None, None) == lib.DSA_ERR_ARG
+    assert L.dsa_topk_select(fake, 1, 1, 8, fake, 10, fake + 4, 1 << 24, None, None) == lib.DSA_ERR_ARG
+    assert L.dsa_touch_mirror(None, 1, 10, None) == lib.DSA_ERR_ARG
+    assert L.dsa_touch_mirror(fake, 0, 10, None) == lib.DSA_ERR_ARG
+    # SM partitions: argument checks come before any driver call
+    p1, p2 = ctypes.c_void_p(), ctypes.c_void_p()
+    assert L.dsa_partition_split(0, ctypes.byref(p1), ctypes.byref(p2)) == lib.DSA_ERR_ARG
+    assert L.dsa_partition_split(8, None, None) == lib.DSA_ERR_ARG
+    assert L.dsa_partition_stream(None, ctypes.byref(p1)) == lib.DSA_ERR_ARG
+    assert L.dsa_partition_destroy(None) == lib.DSA_ERR_ARG
+    assert L.dsa_partition_sms(None) == 0
     h, d = ctypes.c_void_p(), ctypes.c_void_p()
     assert L.dsa_host_alloc(None, ctypes.byref(d), 16) == lib.DSA_ERR_ARG
     assert L.dsa_host_alloc(ctypes.byref(h), ctypes.byref(d), 0) == lib.DSA_ERR_ARG
