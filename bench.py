@@ -76,7 +76,7 @@ def parse():
                     help="layer l reuses the selection of layer l - l %% N (1: every layer scores)")
     ap.add_argument("--path", choices=["fused", "split"], default=None,
                     help="fused: hot_gather_attn; split: hot_gather + mla_decode_attn with the append "
-                         "overlapping the attention (default: split)")
+                         "overlapping the attention (default: fused in the partition schedule, else split)")
     ap.add_argument("--no-pipeline", action="store_true",
                     help="run every step serially, all units in lockstep (same as --schedule serial)")
     ap.add_argument("--score-sms", type=int, default=SCORE_SMS,
@@ -382,8 +382,14 @@ class WorkloadRun:
             # the gathers read the host mirrors from the second partition
             abi.dsa_touch_mirror(self.units.units, U, wlr.lmax, self.tstreams[0])
             abi.dsa_stream_wait_stream(torch.cuda.current_stream(), self.tstreams[0])
-            # (e2e) a group's host copies run on an ordinary stream of their own
-            self.cstreams = [torch.cuda.Stream() for _ in self.granges]
+            # (e2e) a group's input and output copies run on ordinary streams
+            self.cin = [torch.cuda.Stream() for _ in self.granges]
+            self.cout = [torch.cuda.Stream() for _ in self.granges]
+            self.ev_in = [[torch.cuda.Event(), torch.cuda.Event()] for _ in self.granges]
+            self.pext = torch.cuda.ExternalStream(self.pstream)
+            if fused:
+                for p in self.gpaths:
+                    p.prepare_fused()
         if self.pipeline:
             self.path.enable_pipeline()
             # (e2e) input copies of the next step, issued on a copy stream
@@ -490,11 +496,12 @@ class WorkloadRun:
         """K steps of each session group, step after step on the group's own
         stream of the second SM partition, with every scoring on the first
         partition's stream (the groups' scorings alternate there): a group's
-        selection, gather assignment and copy, attention and append run on
-        their own SMs beside the other group's scoring. A group's scoring
-        follows its previous step; its selection follows its scoring. With
-        e2e, a group's input and output copies run on an ordinary copy stream
-        between its steps. One event pair brackets them."""
+        selection, gather and attention, and append run on their own SMs
+        beside the other group's scoring. A group's scoring follows its
+        previous step; its selection follows its scoring. With e2e, a group's
+        inputs reach the device two steps ahead (two buffers, an ordinary
+        copy stream) and its outputs leave on another ordinary stream, which
+        the group's next attention waits for. One event pair brackets them."""
         torch, abi, rnd = self.torch, self.abi, self.abi.ROUND_AUTO
         main = torch.cuda.current_stream()
         names = ("q_idx", "w", "q_lat", "q_rope", "new_rows", "new_keys")
@@ -502,46 +509,57 @@ class WorkloadRun:
         ev[0].record()
         for ts in self.tstreams + [self.pstream]:
             abi.dsa_stream_wait_stream(ts, main)
-        for cs in self.cstreams:
-            cs.wait_stream(main)
+        if e2e is not None:
+            for g in range(len(self.granges)):
+                hpack, dpack, _, _, _ = e2e[g]
+                self.cin[g].wait_stream(main)
+                self.cout[g].wait_stream(main)
+                for s in (s0, s0 + 1):
+                    with torch.cuda.stream(self.cin[g]):
+                        dpack[s & 1].copy_(hpack[s], non_blocking=True)
+                    self.ev_in[g][s & 1].record(self.cin[g])
         for i in range(self.K):
             s = s0 + i
             for g, ((lo, hi), p, ts) in enumerate(zip(self.granges, self.gpaths, self.tstreams)):
                 u = p.u
                 if e2e is None:
                     qi, w, ql, qr, nr, nk = tuple(x[lo:hi] for x in self.step_args(s))
-                    abi.dsa_stream_wait_stream(self.pstream, ts)
                 else:
-                    # this step's inputs over the previous step's (whose last
-                    # readers are on the group's stream)
                     hpack, dpack, dev_in, out_host, _ = e2e[g]
-                    cs = self.cstreams[g]
-                    abi.dsa_stream_wait_stream(cs, ts)
-                    with torch.cuda.stream(cs):
-                        dpack[0].copy_(hpack[s], non_blocking=True)
-                    qi, w, ql, qr, nr, nk = (dev_in[0][n] for n in names)
-                    abi.dsa_stream_wait_stream(self.pstream, cs)
+                    qi, w, ql, qr, nr, nk = (dev_in[s & 1][n] for n in names)
+                    self.pext.wait_event(self.ev_in[g][s & 1])        # this step's inputs are in
+                abi.dsa_stream_wait_stream(self.pstream, ts)
                 p.score(qi, w, self.pstream)
                 abi.dsa_stream_wait_stream(ts, self.pstream)
                 p.select(ts)
-                abi.hot_gather_assign(u.units, u.U, p.R, p.K, rnd, p.topk, p.cls, p.counters, p.ws_gather,
-                                      p.ws_gather_bytes, u.dev_err, ts)
-                abi.hot_gather_copy(u.units, u.U, p.R, p.K, p.topk, p.cls, p.rows, p.ws_gather,
-                                    p.ws_gather_bytes, u.dev_err, ts)
-                p.attend(ql, qr, ts)
+                if e2e is not None:
+                    abi.dsa_stream_wait_stream(ts, self.cout[g])     # the previous output is read out
+                if self.fused:
+                    p.gather_attend(rnd, ql, qr, ts)
+                else:
+                    abi.hot_gather_assign(u.units, u.U, p.R, p.K, rnd, p.topk, p.cls, p.counters, p.ws_gather,
+                                          p.ws_gather_bytes, u.dev_err, ts)
+                    abi.hot_gather_copy(u.units, u.U, p.R, p.K, p.topk, p.cls, p.rows, p.ws_gather,
+                                        p.ws_gather_bytes, u.dev_err, ts)
+                    p.attend(ql, qr, ts)
                 p.append(nr, nk, ts)
                 with torch.cuda.stream(self.text[g]):
                     self.ctr[lo:hi].add_(p.counters)
                 if e2e is not None:
-                    # the step's output to the host; the next step's attention
-                    # (after its scoring, after its input copy) waits for it
-                    abi.dsa_stream_wait_stream(cs, ts)
-                    with torch.cuda.stream(cs):
+                    abi.dsa_stream_wait_stream(self.cout[g], ts)
+                    with torch.cuda.stream(self.cout[g]):
                         out_host[i].copy_(p.out, non_blocking=True)
+                    if i + 2 < self.K:
+                        # step s + 2's inputs into the buffer this step has finished with
+                        abi.dsa_stream_wait_stream(self.cin[g], ts)
+                        with torch.cuda.stream(self.cin[g]):
+                            dpack[s & 1].copy_(hpack[s + 2], non_blocking=True)
+                        self.ev_in[g][s & 1].record(self.cin[g])
         for ts in self.tstreams:
             abi.dsa_stream_wait_stream(main, ts)
-        for cs in self.cstreams:
-            main.wait_stream(cs)
+        if e2e is not None:
+            for st in self.cin + self.cout:
+                main.wait_stream(st)
         ev[1].record()
         return [ev]
 
@@ -716,7 +734,7 @@ def measure_restore(run, n_units):
 
 
 BREAKDOWN_SEGS = 3
-SCORE_SMS = 104           # partition schedule: SMs the scorings run on
+SCORE_SMS = 112           # partition schedule: SMs the scorings run on
 E2E_SEGS = 3
 L2_BYTES = 126 << 20
 
@@ -732,7 +750,8 @@ def use_pipeline(args, wl):
     is needed between the steps; else "serial" (no overlap)."""
     if args.no_pipeline or args.schedule == "serial":
         return "serial"
-    ok = (wl.A == 1 and wl.reuse_every == 1 and args.path != "fused" and wl.U * wl.L0 * 128 > 4 * L2_BYTES)
+    ok = (wl.A == 1 and wl.reuse_every == 1 and (args.path != "fused" or args.schedule == "partition")
+          and wl.U * wl.L0 * 128 > 4 * L2_BYTES)
     if not ok:
         return "serial"
     if args.schedule == "lockstep" or wl.sessions < 2:
@@ -748,7 +767,8 @@ def measure(args, wl, K, Wm, mirror, reps, world, clocks=None, e2e=False, breakd
     import torch
     sched = use_pipeline(args, wl)
     use_graph = not args.no_graph and sched != "partition"
-    fused = args.path == "fused"
+    # the partition schedule gathers inside the attention unless told otherwise
+    fused = args.path == "fused" or (args.path is None and sched == "partition")
     # the partition schedule's kernels load into their green contexts at
     # their first launches there: one untimed segment first
     warm_seg = 1 if sched == "partition" else 0
@@ -776,7 +796,8 @@ def measure(args, wl, K, Wm, mirror, reps, world, clocks=None, e2e=False, breakd
         torch.distributed.all_reduce(t, op=torch.distributed.ReduceOp.MAX)
         total_ms = float(t.item())
     import numpy as np
-    lps = sum(p.launches_per_step() for p in run.gpaths) if run.groups else path.launches_per_step()
+    lps = (sum(p.launches_per_step(fused) for p in run.gpaths) if run.groups else
+           path.launches_per_step(fused and not run.pipeline))
     res = {"run": run, "totals_ms": totals, "total_ms": total_ms, "ctr": np.mean(ctrs, axis=0),
            "launches_per_step": lps}
     if breakdown:
@@ -883,12 +904,15 @@ def run_gpu(args, rank: int, world: int):
             "l2": ("not flushed: every step streams more than L2 holds (keys of all units)" if pipe != "serial" else
                    "flushed before every timed step (512 MiB write outside the bracket)"),
             "selection_reuse_every": wl.reuse_every,
-            "path": "hot_gather_attn (fused)" if args.path == "fused" else {
+            "path": "hot_gather_attn (fused)" if args.path == "fused" and pipe != "partition" else {
                 "partition": ("two session groups (sessions [0, S/2) and [S/2, S)), each decoding step after "
                               "step; the GPU split into two SM partitions (green contexts): every scoring runs "
                               f"on the first ({getattr(run, 'part_sms', 0)} SMs), the groups' scorings "
-                              "alternating there; a group's selection, gather, attention and append run on the "
-                              f"second ({getattr(run, 'rest_sms', 0)} SMs), beside the other group's scoring"),
+                              "alternating there; a group's selection, "
+                              + ("gather fused into the attention (hot_gather_attn)" if run.fused else
+                                 "gather (hot_gather_assign + hot_gather_copy), attention")
+                              + f" and append run on the second ({getattr(run, 'rest_sms', 0)} SMs), beside "
+                              "the other group's scoring"),
                 "groups": ("two session groups (sessions [0, S/2) and [S/2, S)), each decoding step after "
                            "step on its own stream (score, select, gather, attention, append); one group's "
                            "gather copy and attention overlap the other group's scoring"),

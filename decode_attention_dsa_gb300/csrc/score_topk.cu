@@ -404,11 +404,14 @@ __global__ void __launch_bounds__(SCORE_THREADS) k_dsa_score(const __grid_consta
     // issued, in the next slot in turn: every unit issued has at least one
     // tile, so a slot is rewritten only SCORE_TMAP_SLOTS units (and as many
     // tiles, more than the NST copies in flight) after its last use.
+    // Stage s = j % NST and the parity of its use j / NST advance with j
+    // (no integer division in the loop).
     int tmap_u = -1, tmap_n = -1;
+    int s = 0;
+    uint32_t use_par = 0;
     long long j = 0;
     for (int k = next_valid(0); k < ntiles; k = next_valid(k + 1), ++j) {
-      const int s = (int)(j % NST);
-      if (j >= NST && !warp_wait(&empty[s], (uint32_t)((j / NST - 1) & 1))) break;
+      if (j >= NST && !warp_wait(&empty[s], use_par ^ 1u)) break;   // the stage's previous use is read
       if (lane == 0) {
         int u, t;
         tile_of(k, u, t);
@@ -423,10 +426,16 @@ __global__ void __launch_bounds__(SCORE_THREADS) k_dsa_score(const __grid_consta
       }
       __syncwarp();
       issued = j + 1;
+      if (++s == NST) {
+        s = 0;
+        use_par ^= 1u;
+      }
     }
   } else if (warp == SCORE_MMA_WARP) {
     // ---- MMA issue
     int mma_u = -1, bsel = 1;
+    int s = 0;
+    uint32_t use_par = 0;     // parity of stage s's use j / NST
     long long j = 0;
     for (int k = next_valid(0); k < ntiles; k = next_valid(k + 1), ++j) {
       int u, t;
@@ -448,10 +457,10 @@ __global__ void __launch_bounds__(SCORE_THREADS) k_dsa_score(const __grid_consta
         tc::fence_async_shared();
         __syncwarp();
       }
-      const int s = (int)(j % NST), acc = (int)(j & 1);
+      const int acc = (int)(j & 1);
       bool ok = true;
       if (lane == 0) {
-        ok = wait(&full[s], (uint32_t)((j / NST) & 1));
+        ok = wait(&full[s], use_par);
         if (ok && j >= 2) ok = wait(&acc_empty[acc], (uint32_t)(((j >> 1) - 1) & 1));
         if (ok) {
           tc::fence_after_sync();
@@ -468,6 +477,10 @@ __global__ void __launch_bounds__(SCORE_THREADS) k_dsa_score(const __grid_consta
         }
       }
       if (!__shfl_sync(0xffffffffu, ok ? 1 : 0, 0)) break;
+      if (++s == NST) {
+        s = 0;
+        use_par ^= 1u;
+      }
     }
   } else {
     // ---- epilogue. A warp whose wait gave up keeps walking the tiles

@@ -91,12 +91,19 @@ class DecodePath:
                             self.scale, self.out, self.lse, self.ws_attn, self.ws_attn_bytes,
                             u.dev_err, stream)
 
+    def prepare_fused(self):
+        """The workspace of gather_attend (zero-filled on the current stream;
+        allocate it before the first call when that call runs on another
+        stream)."""
+        if not hasattr(self, "ws_fused"):
+            u = self.u
+            self.ws_fused_bytes = abi.hot_gather_attn_workspace(u.U, self.R, self.H, self.K)
+            self.ws_fused = torch.zeros(self.ws_fused_bytes, dtype=torch.uint8, device=u.device)
+
     def gather_attend(self, rnd: int, q_lat, q_rope, stream=None):
         """hot_gather + attention in one call (rows read from their sources)."""
         u = self.u
-        if not hasattr(self, "ws_fused"):
-            self.ws_fused_bytes = abi.hot_gather_attn_workspace(u.U, self.R, self.H, self.K)
-            self.ws_fused = torch.zeros(self.ws_fused_bytes, dtype=torch.uint8, device=u.device)
+        self.prepare_fused()
         abi.hot_gather_attn(u.units, u.U, self.R, self.K, self.H, rnd, self.topk, q_lat, q_rope, self.scale,
                             self.cls, self.counters, self.out, self.lse, self.ws_fused, self.ws_fused_bytes,
                             u.dev_err, stream)
@@ -202,7 +209,8 @@ class DecodePath:
         """Make `stream` (default: the current stream) wait for the side stream."""
         (stream if stream is not None else torch.cuda.current_stream()).wait_event(self.ev_done)
 
-    def launches_per_step(self) -> int:
+    def launches_per_step(self, fused: bool = False) -> int:
         """Kernel launches one step enqueues (score, select, [reuse copy],
-        classify+assign, copy, attention parts, attention merge, append)."""
-        return 8 if self.sources else 7
+        classify+assign, copy (not with the fused gather), attention parts,
+        attention merge, append)."""
+        return (8 if self.sources else 7) - (1 if fused else 0)

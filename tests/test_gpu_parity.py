@@ -159,13 +159,14 @@ def test_two_session_groups_on_two_streams():
         assert pair.g.check() == 0
 
 
-def test_scoring_on_sm_partition_beside_the_other_group():
+@pytest.mark.parametrize("fused", [False, True], ids=["split", "fused"])
+def test_scoring_on_sm_partition_beside_the_other_group(fused):
     """The partition schedule: two session groups; the GPU split into two SM
     partitions; every scoring (dsa_score) on the first partition's stream, the
-    groups' scorings alternating there; each group's selection, gather,
-    attention and append on its own stream of the second partition; the
-    order kept by dsa_stream_wait_stream. After every step every unit matches
-    the oracle."""
+    groups' scorings alternating there; each group's selection, gather
+    (split, or fused into the attention), attention and append on its own
+    stream of the second partition; the order kept by dsa_stream_wait_stream.
+    After every step every unit matches the oracle."""
     import torch
     from decode_attention_dsa_gb300.step import DecodePath
     from oracle.decode import decode_step
@@ -181,6 +182,10 @@ def test_scoring_on_sm_partition_beside_the_other_group():
         assert abi.dsa_partition_sms(first) >= 64 and abi.dsa_partition_sms(second) >= 8
         pstream = abi.dsa_partition_stream(first)
         streams = [abi.dsa_partition_stream(second) for _ in ranges]
+        if fused:
+            for p in paths:
+                p.prepare_fused()
+            torch.cuda.synchronize()
         for step in range(wl.steps):
             per, t = pair.inputs(step)
             cur = torch.cuda.current_stream()
@@ -192,11 +197,14 @@ def test_scoring_on_sm_partition_beside_the_other_group():
                 p.score(t["q_idx"][lo:hi], t["w"][lo:hi], pstream)
                 abi.dsa_stream_wait_stream(st, pstream)
                 p.select(st)
-                abi.hot_gather_assign(u.units, u.U, p.R, p.K, step, p.topk, p.cls, p.counters, p.ws_gather,
-                                      p.ws_gather_bytes, u.dev_err, st)
-                abi.hot_gather_copy(u.units, u.U, p.R, p.K, p.topk, p.cls, p.rows, p.ws_gather,
-                                    p.ws_gather_bytes, u.dev_err, st)
-                p.attend(t["q_lat"][lo:hi], t["q_rope"][lo:hi], st)
+                if fused:
+                    p.gather_attend(step, t["q_lat"][lo:hi], t["q_rope"][lo:hi], st)
+                else:
+                    abi.hot_gather_assign(u.units, u.U, p.R, p.K, step, p.topk, p.cls, p.counters,
+                                          p.ws_gather, p.ws_gather_bytes, u.dev_err, st)
+                    abi.hot_gather_copy(u.units, u.U, p.R, p.K, p.topk, p.cls, p.rows, p.ws_gather,
+                                        p.ws_gather_bytes, u.dev_err, st)
+                    p.attend(t["q_lat"][lo:hi], t["q_rope"][lo:hi], st)
                 p.append(t["new_rows"][lo:hi], t["new_keys"][lo:hi], st)
             for st in streams:
                 abi.dsa_stream_wait_stream(cur, st)
@@ -210,7 +218,7 @@ def test_scoring_on_sm_partition_beside_the_other_group():
                 x = per[i]
                 ores[u] = decode_step(pair.o[u], step, wl.K, wl.scale(), x.q_idx, x.w, x.q_lat, x.q_rope,
                                       x.new_rows, x.new_keys, attention=True)
-            check_step(pair, g, ores)
+            check_step(pair, g, ores, rows=not fused)
             assert pair.g.check() == 0
     finally:
         abi.dsa_partition_destroy(first)
