@@ -81,6 +81,8 @@ def parse():
                     help="run every step serially, all units in lockstep (same as --schedule serial)")
     ap.add_argument("--score-sms", type=int, default=SCORE_SMS,
                     help="partition schedule: SMs of the partition the scoring runs on")
+    ap.add_argument("--groups", type=int, default=GROUPS,
+                    help="partition schedule: session groups whose scorings take turns on the scoring partition")
     ap.add_argument("--schedule", choices=["partition", "groups", "lockstep", "serial"], default=None,
                     help="partition: the sessions in two halves, each decoding step after step; the GPU "
                          "split into two SM partitions, every scoring on the first, the rest of each step "
@@ -312,6 +314,14 @@ class ClockSampler:
 
 # ---------------------------------------------------------------- GPU arm
 
+def session_groups(sessions: int, layers: int, n: int):
+    """`n` contiguous groups of the sessions, as unit ranges [lo, hi) (units
+    are session-major), sizes differing by at most one session."""
+    n = max(1, min(n, sessions))
+    b = [round(i * sessions / n) for i in range(n + 1)]
+    return [(b0 * layers, b1 * layers) for b0, b1 in zip(b, b[1:])]
+
+
 def traffic_for(kernel: str):
     """DRAM bytes per launch from the committed ncu summary, if the kernel's
     source has not changed since it was captured."""
@@ -333,7 +343,7 @@ class WorkloadRun:
     The timed segments are consecutive parts of one continuous decode, so
     every timed step selects rows no earlier step has read."""
 
-    def __init__(self, wl, K, Wm, nseg, mirror, fused, use_graph, pipeline="serial", score_sms=None):
+    def __init__(self, wl, K, Wm, nseg, mirror, fused, use_graph, pipeline="serial", score_sms=None, ngroups=2):
         import torch
         from decode_attention_dsa_gb300 import abi
         from decode_attention_dsa_gb300.step import DecodePath
@@ -363,9 +373,9 @@ class WorkloadRun:
         self.groups = None
         self.part = None
         if pipeline in ("groups", "partition"):
-            # sessions [0, S/2) and [S/2, S): units are session-major
-            half = (wl.sessions // 2) * wl.layers
-            self.granges = [(0, half), (half, U)]
+            # contiguous groups of sessions (units are session-major); the
+            # group schedule alternates two of them
+            self.granges = session_groups(wl.sessions, wl.layers, ngroups if pipeline == "partition" else 2)
             self.gpaths = [DecodePath(self.units.subset(lo, hi), wl.R, wl.K, wl.H, wl.A, wl.scale())
                            for lo, hi in self.granges]
             self.gstreams = [torch.cuda.Stream() for _ in self.granges]
@@ -734,7 +744,8 @@ def measure_restore(run, n_units):
 
 
 BREAKDOWN_SEGS = 3
-SCORE_SMS = 112           # partition schedule: SMs the scorings run on
+SCORE_SMS = 120           # partition schedule: SMs the scorings run on
+GROUPS = 2                # partition schedule: session groups taking turns on them
 E2E_SEGS = 3
 L2_BYTES = 126 << 20
 
@@ -773,7 +784,8 @@ def measure(args, wl, K, Wm, mirror, reps, world, clocks=None, e2e=False, breakd
     # their first launches there: one untimed segment first
     warm_seg = 1 if sched == "partition" else 0
     nseg = warm_seg + reps + (BREAKDOWN_SEGS if breakdown else 0) + (E2E_SEGS if e2e else 0)
-    run = WorkloadRun(wl, K, Wm, nseg, mirror, fused, use_graph, pipeline=sched, score_sms=args.score_sms)
+    run = WorkloadRun(wl, K, Wm, nseg, mirror, fused, use_graph, pipeline=sched, score_sms=args.score_sms,
+                      ngroups=args.groups)
     path, U = run.path, wl.U
     warm = [run.segment() for _ in range(warm_seg)]
     heads = [run.segment() for _ in range(reps)]
@@ -905,14 +917,16 @@ def run_gpu(args, rank: int, world: int):
                    "flushed before every timed step (512 MiB write outside the bracket)"),
             "selection_reuse_every": wl.reuse_every,
             "path": "hot_gather_attn (fused)" if args.path == "fused" and pipe != "partition" else {
-                "partition": ("two session groups (sessions [0, S/2) and [S/2, S)), each decoding step after "
-                              "step; the GPU split into two SM partitions (green contexts): every scoring runs "
+                "partition": (f"{len(getattr(run, 'granges', ()))} session groups (contiguous, sizes "
+                              f"{[(hi - lo) // wl.layers for lo, hi in getattr(run, 'granges', ())]} sessions), "
+                              "each decoding step after step; the GPU split into two SM partitions (green "
+                              "contexts): every scoring runs "
                               f"on the first ({getattr(run, 'part_sms', 0)} SMs), the groups' scorings "
-                              "alternating there; a group's selection, "
+                              "taking turns there; a group's selection, "
                               + ("gather fused into the attention (hot_gather_attn)" if run.fused else
                                  "gather (hot_gather_assign + hot_gather_copy), attention")
                               + f" and append run on the second ({getattr(run, 'rest_sms', 0)} SMs), beside "
-                              "the other group's scoring"),
+                              "the other groups' scorings"),
                 "groups": ("two session groups (sessions [0, S/2) and [S/2, S)), each decoding step after "
                            "step on its own stream (score, select, gather, attention, append); one group's "
                            "gather copy and attention overlap the other group's scoring"),

@@ -186,10 +186,6 @@ __device__ __forceinline__ float dequant_tile(const uint8_t* raw, uint8_t* tile,
   return fmaxf(__low2float(vmax), __high2float(vmax));
 }
 
-__device__ __forceinline__ void cp_async16(void* dst_smem, const void* src) {
-  asm volatile("cp.async.cg.shared.global [%0], [%1], 16;" ::"r"(tc::smem_u32(dst_smem)), "l"(src) : "memory");
-}
-
 // A: one run of chunks [cpp * part, cpp * part + cpp) of (unit, query row)
 // ur = blockIdx.y, part = blockIdx.x.
 template <bool GATHER>
@@ -230,9 +226,12 @@ k_attn_parts(int R, int H, int K, int cpp, const uint16_t* __restrict__ q_lat, c
   bool failed = ms->fail != 0;
   pdl_wait();   // everything above touched only this CTA's shared and tensor memory
 
-  // Stage chunk c's rows. Compact rows: one bulk copy (thread 0) on bar_t.
-  // Gathered rows: 16-byte async copies from each row's source (all threads;
-  // the caller waits with cp.async.wait_group and a barrier).
+  // Stage chunk c's rows, completion counted on bar_t (one phase per chunk).
+  // Compact rows: one bulk copy (thread 0). Gathered rows: one bulk copy per
+  // row from its source (an HBM slot, the ring or the host mirror; 656 bytes,
+  // 16-byte aligned), so a host row crosses the link as whole sectors; rows
+  // without a source are zero-filled by their thread (the caller's barrier
+  // after the wait publishes them).
   auto stage = [&](int c) {
     const int j0 = c * NC, n = min(NC, K - j0);
     if (!GATHER) {
@@ -269,14 +268,21 @@ k_attn_parts(int R, int H, int K, int cpp, const uint16_t* __restrict__ q_lat, c
         ms->dst[tid] = dst;
       }
       __syncthreads();
-      for (int t = tid; t < n * 41; t += THREADS) {
-        const int jj = t / 41, q = t % 41;
-        const uint8_t* src = ms->src[jj];
-        uint8_t* d = sR + jj * DSA_ROW_BYTES + 16 * q;
-        if (src) cp_async16(d, src + 16 * q);
-        else *reinterpret_cast<uint4*>(d) = make_uint4(0u, 0u, 0u, 0u);
+      if (tid == 0) {
+        uint32_t bytes = 0;
+        for (int jj = 0; jj < n; ++jj) bytes += ms->src[jj] ? (uint32_t)DSA_ROW_BYTES : 0u;
+        tc::mbar_arrive_expect_tx(&ms->bar_t, bytes);
       }
-      asm volatile("cp.async.commit_group;" ::: "memory");
+      if (tid < n) {
+        const uint8_t* src = ms->src[tid];
+        uint8_t* d = sR + tid * DSA_ROW_BYTES;
+        if (src) {
+          tc::bulk_g2s(d, src, DSA_ROW_BYTES, &ms->bar_t);
+        } else {
+          for (int q = 0; q < DSA_ROW_BYTES / 16; ++q)
+            reinterpret_cast<uint4*>(d)[q] = make_uint4(0u, 0u, 0u, 0u);
+        }
+      }
     }
   };
   if (!failed && c0 < c1) stage(c0);
@@ -326,11 +332,7 @@ k_attn_parts(int R, int H, int K, int cpp, const uint16_t* __restrict__ q_lat, c
     // ---- rows staged; the tile and P are free once the previous chunk's
     //      O^T product is done
     if (!failed) {
-      if (!GATHER) {
-        if (!tc::mbar_wait(&ms->bar_t, (uint32_t)(i & 1))) atomicOr(&ms->fail, 1);
-      } else {
-        asm volatile("cp.async.wait_group 0;" ::: "memory");
-      }
+      if (!tc::mbar_wait(&ms->bar_t, (uint32_t)(i & 1))) atomicOr(&ms->fail, 1);
       if (i > 0 && !tc::mbar_wait(&ms->bar_o, (uint32_t)((i - 1) & 1))) atomicOr(&ms->fail, 1);
     }
     if (tid < NC) {
@@ -501,12 +503,11 @@ k_attn_parts(int R, int H, int K, int cpp, const uint16_t* __restrict__ q_lat, c
   }
   // (a value whose fp16 rounding reaches 65504, including an overflow)
   if (vmax >= 65504.f) dsa_flag(dev_err, DSA_DEVERR_QRANGE);
-  if (GATHER) asm volatile("cp.async.wait_group 0;" ::: "memory");
   if (failed && tid == 0) {
     dsa_flag(dev_err, DSA_DEVERR_TIMEOUT);
     // nothing may still land in shared memory or run on tensor memory once
     // the CTA is gone
-    if (!GATHER && nt > 0) tc::mbar_wait(&ms->bar_t, (uint32_t)((nt - 1) & 1));
+    if (nt > 0) tc::mbar_wait(&ms->bar_t, (uint32_t)((nt - 1) & 1));
     if (ns > 0) tc::mbar_wait(&ms->bar_s, (uint32_t)((ns - 1) & 1));
     if (no > 0) tc::mbar_wait(&ms->bar_o, (uint32_t)((no - 1) & 1));
   }
