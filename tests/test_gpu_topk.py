@@ -119,6 +119,39 @@ def test_short_history_in_few_tiles_and_empty_cluster_ranges():
     _run(keys, q, w, 2048)
 
 
+@pytest.mark.parametrize("R", [1, 2])
+def test_more_units_than_score_ctas(R):
+    """More units than the persistent score grid holds CTAs (4 per SM on the
+    whole device): the grid cuts the flattened (unit, tile) space evenly, so
+    CTAs cross unit boundaries (the query operand alternates between its two
+    buffers, the shared histogram is flushed at each unit change). Ragged
+    histories of 1 to 4 tiles, some shorter than K (every position kept)."""
+    rng = np.random.default_rng(21 + R)
+    lens = rng.integers(40, 520, size=700)
+    keys = [_bits(rng.integers(-4, 5, size=(int(n), 64))) for n in lens]
+    q = _bits(rng.integers(-4, 5, size=(700, R, 8, 64)))
+    w = rng.integers(1, 5, size=(700, R, 8))
+    _run(keys, q, w, 64)
+
+
+@pytest.mark.parametrize("R", [1, 3])
+def test_more_units_than_score_ctas_on_a_partition(R):
+    """The same on an SM partition (five CTAs per SM): 200 units on the first
+    partition of a split at 8 SMs (its 32 SMs hold 160 CTAs)."""
+    from decode_attention_dsa_gb300 import abi
+    rng = np.random.default_rng(31 + R)
+    lens = rng.integers(200, 3000, size=200)
+    keys = [_bits(rng.integers(-4, 5, size=(int(n), 64))) for n in lens]
+    q = _bits(rng.integers(-4, 5, size=(200, R, 8, 64)))
+    w = rng.integers(1, 5, size=(200, R, 8))
+    first, second = abi.dsa_partition_split(8)
+    try:
+        _run(keys, q, w, 256, streams=(abi.dsa_partition_stream(first), abi.dsa_partition_stream(second)))
+    finally:
+        abi.dsa_partition_destroy(first)
+        abi.dsa_partition_destroy(second)
+
+
 @pytest.mark.parametrize("min_sms", [8, 96])
 def test_score_and_select_on_two_sm_partitions(min_sms):
     """dsa_score on the first of two SM partitions (its persistent grid sized
