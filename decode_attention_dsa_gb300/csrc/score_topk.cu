@@ -10,32 +10,34 @@
 // kernel time they saved, so here the whole select is one clustered launch.
 //
 // Design (GB300):
-//  * k_dsa_score: a persistent grid (two to four CTAs per SM) walks the
-//    flattened (unit, tile) space. Each 128-position tile of bf16 keys (16 KB,
-//    contiguous) arrives by a 1-D bulk TMA copy into one of several stages;
-//    each thread rewrites its position's 128-byte row in place into the
-//    128-byte-swizzled K-major operand layout (bank-conflict-free order), and
-//    one thread issues four tcgen05.mma kind::f16 (bf16 x bf16 -> fp32, M = 128
-//    positions, N = 8 heads per query row padded to 16, K = 64) against the
-//    unit's query rows held as operand B. The epilogue reads the thread's TMEM
-//    lane (its position), applies ReLU and the head weights, and turns each
-//    score into an order-preserving uint32 key (written coalesced) that feeds a
-//    4096-bin shared histogram of its top 12 bits (one shared atomic per
-//    distinct bin per warp), merged into a global per-(unit, row) histogram
-//    when the CTA leaves a unit. The next copy into a stage is issued as soon
-//    as the MMA that read it completes.
-//  * k_topk_select: one 8-CTA thread-block cluster per (unit, row). The global
-//    histogram gives the bin b1 of the K-th largest key. One pass streams each
-//    CTA's key range through shared memory (1-D bulk TMA copies of 4096-key
-//    tiles, two in flight) in position order: it counts the keys above b1,
-//    pushes the candidates inside b1 to every CTA of the cluster through
-//    distributed shared memory, and keeps every key of bin >= b1 with its
-//    position in an ordered list (block scans per tile). Every CTA finds the
-//    exact threshold key T (and how many keys equal to T are taken) by a
-//    local radix select over the candidates; if they do not fit, three
-//    refinement passes with cluster-summed histograms find T instead. The
-//    output is compacted from the ordered list (or, if it overflowed, from
-//    the whole range): keys above T, and keys equal to T lowest position first.
+//  * k_dsa_score: a persistent grid, as many CTAs per SM as shared and tensor
+//    memory allow (4 on the whole device, 5 on an SM partition of fewer SMs,
+//    for one query row), walks the flattened (unit, tile) space, whole CTAs
+//    per unit where the grid holds one per unit. Three roles per CTA meet
+//    only at mbarriers: a producer warp copies each 128-position tile of bf16
+//    keys (16 KB) by tiled TMA through a per-unit tensor map made on the
+//    device, landing 128-byte swizzled as MMA operand A; an MMA warp issues
+//    four tcgen05.mma kind::f16 (bf16 x bf16 -> fp32, M = 128 positions,
+//    N = 8 heads per query row padded to 16, K = 64) against the unit's query
+//    rows held as operand B, into one of two TMEM accumulators; four epilogue
+//    warps read the accumulator (one position per thread), apply ReLU and the
+//    head weights, and turn each score into an order-preserving uint32 key
+//    (written coalesced) counted in a shared histogram of its top 12 bits
+//    (two 16-bit bins per word, one shared atomic per distinct bin per warp),
+//    merged into the call's per-(unit, row) histogram when the CTA leaves a
+//    unit; each warp also writes the largest key of its 32 positions.
+//  * k_topk_select: one 8-CTA thread-block cluster per (unit, row). The
+//    histogram gives the bin b1 of the K-th largest key. Each warp of a CTA
+//    owns a run of 32-key groups and reads only the groups whose largest key
+//    reaches b1; it counts the keys above b1, pushes the candidates inside b1
+//    to every CTA of the cluster through distributed shared memory, and keeps
+//    every key of bin >= b1 with its position in an ordered per-warp list.
+//    Every CTA finds the exact threshold key T (and how many keys equal to T
+//    are taken) by a local radix select over the candidates; if they do not
+//    fit, refinement passes with cluster-summed histograms find T instead.
+//    Each warp compacts its own list at the offset the counts before it give
+//    (or, if a list overflowed, the CTA compacts from its whole range): keys
+//    above T, and keys equal to T lowest position first.
 #include <algorithm>
 #include <cooperative_groups.h>
 #include <cuda.h>
