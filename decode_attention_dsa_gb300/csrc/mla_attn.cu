@@ -10,11 +10,15 @@
 // Two launches per call:
 //  A. k_attn_parts: the K selected rows of a (unit, query row) are cut into
 //     chunks of 64 and the chunks into `parts` contiguous runs, one CTA per
-//     run (runs sized so that all CTAs fill the GPU once). A CTA keeps the
-//     query block (64 heads x 576, fp16) in shared memory and, per chunk:
-//  1. one 1-D bulk TMA copy brings the chunk's rows (up to 64 x 656 B) into a
-//     staging buffer; the copy of the next chunk is issued as soon as this
-//     chunk is dequantised, so it lands while this chunk's products run;
+//     run (runs sized so that all CTAs fill the stream's SMs once). A CTA
+//     keeps the query block (64 heads x 576, fp16) in shared memory and, per
+//     chunk:
+//  1. bulk TMA copies bring the chunk's rows (up to 64 x 656 B) into a
+//     staging buffer: one copy of the compact rows (mla_decode_attn), or with
+//     the gather fused in (hot_gather_attn) one copy per row from its source
+//     (HBM slot, ring or host mirror), the fills then written to their slots
+//     from shared memory; the copies of the next chunk are issued as soon as
+//     this chunk is dequantised, so they land while this chunk's products run;
 //  2. dequantisation writes an fp16 tile [64 rows][576] (latent int8 * fp16
 //     scale rounded once to fp16; RoPE bf16 -> fp16), 128-byte swizzled;
 //  3. S = Q K^T on the tensor cores (tcgen05.mma kind::f16, M = 128: the 64

@@ -478,6 +478,9 @@ int mla_decode_attn(int32_t U, int32_t R, int32_t H, int32_t K,
  * replacement, counters, cache state and out/lse are exactly those of
  * hot_gather + mla_decode_attn; only the compact `rows` buffer is not
  * produced. Duplicate misses of different query rows each read the mirror.
+ * Each row is staged by one 656-byte bulk copy from its source, the next
+ * chunk's rows while the current chunk is multiplied; the attention's runs
+ * fill the SMs of the stream's partition (or the device).
  *   Arguments as in hot_gather and mla_decode_attn; ws holds
  *   hot_gather_attn_workspace(U, R, H, K) bytes, 256-byte aligned.
  *   Shapes: those of mla_decode_attn.
