@@ -761,7 +761,8 @@ def use_pipeline(args, wl):
     is needed between the steps; else "serial" (no overlap)."""
     if args.no_pipeline or args.schedule == "serial":
         return "serial"
-    ok = (wl.A == 1 and wl.reuse_every == 1 and (args.path != "fused" or args.schedule == "partition")
+    # the fused gather runs in the partition schedule (the default) or serially
+    ok = (wl.A == 1 and wl.reuse_every == 1 and (args.path != "fused" or args.schedule in (None, "partition"))
           and wl.U * wl.L0 * 128 > 4 * L2_BYTES)
     if not ok:
         return "serial"
