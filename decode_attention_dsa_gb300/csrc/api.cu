@@ -14,12 +14,8 @@
 // Here the write-back is a plain kernel store of 64 ring rows (41,984 B) into
 // the mapped mirror: no DMA operation, no host involvement.
 #include <algorithm>
-#include <cstdio>
 #include <cstring>
-#include <map>
-#include <mutex>
 
-#include <sys/mman.h>
 #include <unistd.h>
 
 #include <cuda_fp16.h>
@@ -418,62 +414,16 @@ extern "C" int dsa_check(int32_t dev_err_value) {
   return dev_err_value == 0 ? DSA_OK : DSA_ERR_DEVICE_CHECK;
 }
 
-namespace {
-
-// Mirrors of at least this size are mapped from anonymous memory advised for
-// transparent huge pages and then registered (page-locked, mapped): a miss
-// reads a random row of gigabytes of host memory, and huge pages let far
-// fewer address translations cover the mirror than base pages do.
-constexpr size_t HUGE_MIRROR_MIN = (size_t)64 << 20;
-
-struct HostMapping {
-  void* base;     // mmap base
-  size_t len;     // mmap length
-};
-std::mutex g_host_mu;
-std::map<void*, HostMapping> g_host_maps;   // registered mirror -> its mapping
-
-size_t huge_page_bytes() {
-  size_t hp = (size_t)2 << 20;
-  if (FILE* f = std::fopen("/sys/kernel/mm/transparent_hugepage/hpage_pmd_size", "r")) {
-    unsigned long long v = 0;
-    if (std::fscanf(f, "%llu", &v) == 1 && v >= 4096 && (v & (v - 1)) == 0 && v <= ((size_t)1 << 30)) hp = v;
-    std::fclose(f);
-  }
-  return hp;
-}
-
-// Anonymous memory aligned to (and advised for) huge pages, registered as
-// mapped host memory; nullptr where any step fails (nothing is left behind).
-void* huge_host_alloc(size_t bytes) {
-  const size_t hp = huge_page_bytes();
-  const size_t len = (bytes + hp - 1) / hp * hp;
-  void* raw = mmap(nullptr, len + hp, PROT_READ | PROT_WRITE, MAP_PRIVATE | MAP_ANONYMOUS, -1, 0);
-  if (raw == MAP_FAILED) return nullptr;
-  uint8_t* p = reinterpret_cast<uint8_t*>(((uintptr_t)raw + hp - 1) / hp * hp);
-  madvise(p, len, MADV_HUGEPAGE);   // advice only: without huge pages the mirror still works
-  if (cudaHostRegister(p, len, cudaHostRegisterMapped | cudaHostRegisterPortable) != cudaSuccess) {
-    cudaGetLastError();
-    munmap(raw, len + hp);
-    return nullptr;
-  }
-  std::lock_guard<std::mutex> lock(g_host_mu);
-  g_host_maps[p] = HostMapping{raw, len + hp};
-  return p;
-}
-
-}  // namespace
-
 extern "C" int dsa_host_alloc(void** host_ptr, void** dev_ptr, size_t bytes) {
   if (!host_ptr || !dev_ptr || bytes == 0) return DSA_ERR_ARG;
   *host_ptr = nullptr;
   *dev_ptr = nullptr;
-  void* h = bytes >= HUGE_MIRROR_MIN ? huge_host_alloc(bytes) : nullptr;
-  if (!h && cudaHostAlloc(&h, bytes, cudaHostAllocMapped | cudaHostAllocPortable) != cudaSuccess)
+  void* h = nullptr;
+  if (cudaHostAlloc(&h, bytes, cudaHostAllocMapped | cudaHostAllocPortable) != cudaSuccess)
     return DSA_ERR_CUDA;
   void* d = nullptr;
   if (cudaHostGetDevicePointer(&d, h, 0) != cudaSuccess) {
-    dsa_host_free(h);
+    cudaFreeHost(h);
     return DSA_ERR_CUDA;
   }
   *host_ptr = h;
@@ -483,19 +433,7 @@ extern "C" int dsa_host_alloc(void** host_ptr, void** dev_ptr, size_t bytes) {
 
 extern "C" int dsa_host_free(void* host_ptr) {
   if (!host_ptr) return DSA_ERR_ARG;
-  HostMapping m{nullptr, 0};
-  {
-    std::lock_guard<std::mutex> lock(g_host_mu);
-    auto it = g_host_maps.find(host_ptr);
-    if (it != g_host_maps.end()) {
-      m = it->second;
-      g_host_maps.erase(it);
-    }
-  }
-  if (!m.base) return cudaFreeHost(host_ptr) == cudaSuccess ? DSA_OK : DSA_ERR_CUDA;
-  const bool ok = cudaHostUnregister(host_ptr) == cudaSuccess;
-  munmap(m.base, m.len);
-  return ok ? DSA_OK : DSA_ERR_CUDA;
+  return cudaFreeHost(host_ptr) == cudaSuccess ? DSA_OK : DSA_ERR_CUDA;
 }
 
 extern "C" int hc_init(const dsa_unit* units, int32_t U, int32_t warm, const int64_t* l0,

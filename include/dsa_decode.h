@@ -161,14 +161,9 @@ int dsa_wait_selftest(int64_t limit_cycles, int32_t complete, int32_t* dev_err, 
  * registration stall lands on the decode path).
  *   host_ptr  out: host address (page-locked, mapped, portable).
  *   dev_ptr   out: the device-accessible alias to put in dsa_unit.mirror.
- * From 64 MiB on the memory is anonymous memory aligned to the host's
- * transparent huge page size and advised for huge pages, then registered
- * (cudaHostRegister, mapped and portable): misses read random rows of
- * gigabytes of host memory, and huge pages let a few translations cover the
- * whole mirror (on a GB300 host, 512 MiB pages held the 22 GB mirror of the
- * capacity batch). Where that fails, or below 64 MiB, cudaHostAlloc.
- * Returns DSA_ERR_CUDA if the allocation fails. Free with dsa_host_free()
- * (either kind). This is setup, not part of a decode step.
+ * (cudaHostAlloc, mapped and portable.)
+ * Returns DSA_ERR_CUDA if the allocation fails. Free with dsa_host_free().
+ * This is setup, not part of a decode step.
  */
 int dsa_host_alloc(void** host_ptr, void** dev_ptr, size_t bytes);
 int dsa_host_free(void* host_ptr);
