@@ -3,7 +3,8 @@
 The first kernel cuts the K selected rows of a (unit, query row) into chunks
 of 64 and the chunks into at most 16 contiguous runs, one CTA per run; a CTA
 keeps the query block and a 64-row fp16 tile in shared memory, stages the raw
-rows of a chunk with one bulk copy, and stores its unnormalised 64 x 512 fp32
+rows of a chunk with one bulk copy (or, with the gather fused in, one bulk
+copy per row from its source), and stores its unnormalised 64 x 512 fp32
 output slice-major (16 slices of 32 columns, each a contiguous [64 heads][32]
 block) plus its 64 row maxima and sums. The second kernel has one block per
 (unit, query row) and slice. This restates the kernels' index arithmetic and
@@ -121,3 +122,30 @@ def test_merge_reads_every_run_and_writes_every_output_once():
                     assert src % 4 == 0 and src + 4 <= MAX_CTAS * PART_O
                 out[h, s * SLICE + 4 * q4:s * SLICE + 4 * q4 + 4] += 1
         assert (out == 1).all()
+
+
+def test_runs_follow_the_streams_sms():
+    """On an SM partition the runs fill the partition's SMs (the launch
+    passes the stream's SM count): fewer, longer runs, still every chunk once."""
+    for sms in (32, 40, 48, 120, 152):
+        for UR in (1, 16, 32):
+            for K in (64, 2048, 1500, 300):
+                cpp, parts = runs(K, UR, sms)
+                nchunks = (K + NC - 1) // NC
+                assert parts * UR <= max(UR, sms) or parts == 1
+                assert (parts - 1) * cpp < nchunks <= parts * cpp
+
+
+def test_gathered_row_copies_stay_in_the_staging_region():
+    """The fused gather stages a chunk with one bulk copy per row: row j of
+    the chunk lands at R_OFF + 656 j, 16-byte aligned, 656 bytes (a multiple
+    of 16), and the 64 rows end where the next region begins."""
+    assert 656 % 16 == 0 and R_OFF % 16 == 0
+    for j in range(NC):
+        dst = R_OFF + 656 * j
+        assert dst % 16 == 0
+        assert R_OFF <= dst and dst + 656 <= MISC_OFF
+    # a source row p of a mirror, slot or ring array is 16-byte aligned when
+    # the array is (the kernels skip units whose arrays are not)
+    for p in (0, 1, 2, 3, 1048575):
+        assert (656 * p) % 16 == 0
